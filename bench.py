@@ -1,0 +1,470 @@
+#!/usr/bin/env python
+"""Blended-prefill benchmark (CacheBlend selective KV recompute) on GB300.
+
+Default workload: one Llama-2-7B-shaped layer (d 4096, 32 heads x 128, SwiGLU 11008, RoPE
+1e4, bf16, random-init N(0, 0.02)) run as a three-layer shared-weight stack (pre-check,
+check, steady), 6 chunks x 640 cached tokens + 256 query tokens = 4096 tokens, r = 15 %.
+One step = one whole blended prefill: re-position every layer's chunk KV, run the three
+layers (HKVD selection at the check layer), lm_head argmax of the last row.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun), every rank runs an independent
+replica of the request on its own GPU: the method has no exchange step ("replicas only").
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from non_prefix_kv_gb300 import synth  # noqa: E402
+
+METRIC = "blended-prefill tokens/s & TTFT ms, 7B-shape 4K ctx, 15% recompute, 1 GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="llama7b_layer_4k", choices=sorted(synth.WORKLOADS))
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--profile-steps", type=int, default=3)
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------------------ distributed
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def shard_requests(n_requests: int, rank: int, world: int):
+    """Requests are independent: rank r serves every world-th request (replicas when there
+    are fewer requests than ranks, so per-GPU work stays fixed: weak scaling)."""
+    mine = list(range(rank, n_requests, world))
+    return mine if mine else [rank % n_requests]
+
+
+# ------------------------------------------------------------------------------ peaks / clocks
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.path)
+        except Exception:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        # samples under load: the upper half of the power draw
+        if pw and len(pw) == len(sm):
+            thr = statistics.median(pw)
+            loaded = [s for s, p in zip(sm, pw) if p >= thr] or sm
+        else:
+            loaded = sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ------------------------------------------------------------------------------ FLOP model
+def step_flops(wl, sel_sums):
+    """Algorithmic FLOPs of one blended step: GEMMs 2*M*N*K, attention 4*H*hd*sum(p+1).
+    sel_sums: per layer (rows, sum of (position + 1) over the rows that attend)."""
+    s = wl.shape
+    d, F, qc, W = s.d_model, s.d_ff, s.q_width, s.kv_width
+    N, n_c = wl.n_tokens, wl.n_cached
+    total = 0.0
+    for l, (M, psum, mode) in enumerate(sel_sums):
+        if mode == "precheck":
+            total += 2.0 * N * d * qc + 2.0 * (N - n_c) * d * 2 * W
+        elif mode in ("check", "gradual"):
+            m_in = N if mode == "check" else sel_sums[l - 1][0]
+            total += 2.0 * m_in * d * 2 * W + 2.0 * M * d * qc
+        else:
+            total += 2.0 * M * d * (qc + 2 * W)
+        total += 4.0 * s.n_heads * s.head_dim * psum
+        total += 2.0 * M * qc * d + 2.0 * M * d * 2 * F + 2.0 * M * F * d
+    total += 2.0 * s.vocab * d
+    return total
+
+
+# ------------------------------------------------------------------------------ CPU oracle sample
+def oracle_sample(wl, frac_rows=4):
+    """Times the CPU oracle on a bounded sample of the step: the steady layer (selective
+    Q/K/V, attention over the full KV, O-proj, FFN) for every frac_rows-th selected row at
+    the full model shape.  Returns (seconds, sample FLOPs, description)."""
+    import oracle.cacheblend_oracle as O
+    s = wl.shape
+    N, n_c = wl.n_tokens, wl.n_cached
+    k = O.budget(n_c, wl.ratio, n_c)
+    g = synth.rng(wl.seed, synth.P_NOISE)
+    S = np.sort(np.concatenate([g.choice(n_c, k, replace=False), np.arange(n_c, N)]))
+    rows = S[::frac_rows]
+    layer = synth.make_layer_weights(s, synth.rng(wl.seed, synth.P_WEIGHTS))
+    x = synth.test_tensor((len(rows), s.d_model), 7, dtype=s.dtype)
+    K = synth.test_tensor((N, s.n_kv_heads, s.head_dim), 8, dtype=s.dtype)
+    V = synth.test_tensor((N, s.n_kv_heads, s.head_dim), 9, dtype=s.dtype)
+    t0 = time.perf_counter()
+    a = O.rmsnorm(x, layer["attn_norm"], s.rms_eps)
+    p = O.project_qkv(layer, a, rows, s)
+    o = O.attend(p["q"], rows, K, V)
+    O.out_ffn(layer, x, o, s)
+    dt = time.perf_counter() - t0
+    M = len(rows)
+    fl = (2.0 * M * s.d_model * s.qkv_width + 4.0 * s.n_heads * s.head_dim * float(np.sum(rows + 1))
+          + 2.0 * M * s.q_width * s.d_model + 6.0 * M * s.d_model * s.d_ff)
+    desc = (f"oracle steady layer on {M} of {len(S)} selected rows (every {frac_rows}th) at the full "
+            f"{s.d_model}/{s.n_heads}x{s.head_dim}/{s.d_ff} shape over {N} keys, fp64 numpy; "
+            f"scaled to one step by the algorithmic FLOP ratio")
+    return dt, fl, desc
+
+
+def cpu_threads():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def nominal_step_flops(wl):
+    """FLOPs of a step with the expected selection sizes and uniformly spread cached rows."""
+    s = wl.shape
+    N, n_c = wl.n_tokens, wl.n_cached
+    import oracle.cacheblend_oracle as O
+    k = O.budget(n_c, wl.ratio, n_c)
+    q_sum = float(np.sum(np.arange(n_c, N) + 1))
+    sel_psum = q_sum + k * (n_c / 2.0)
+    plan = []
+    for l in range(s.n_layers):
+        if l < wl.check_layer:
+            plan.append((N, N * (N + 1) / 2.0, "precheck"))
+        elif l == wl.check_layer:
+            plan.append((k + N - n_c, sel_psum, "check"))
+        else:
+            plan.append((k + N - n_c, sel_psum, "steady"))
+    return step_flops(wl, plan)
+
+
+# ------------------------------------------------------------------------------ reference arm
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = synth.WORKLOADS[args.workload]
+    full = nominal_step_flops(wl)
+    times = []
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        dt, fl, desc = oracle_sample(wl)
+        if i >= args.warmup:
+            times.append(dt * full / fl)
+    t_step = statistics.median(times)
+    value = wl.n_tokens * wl.n_requests / t_step
+    cores = cpu_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "n_tokens": wl.n_tokens, "chunks": f"{len(wl.order)}x{wl.chunk_len}",
+                       "n_query": wl.n_query, "ratio": wl.ratio, "layers": wl.shape.n_layers},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "ttft_ms": t_step * 1e3}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------ our arm
+def our_arm(args):
+    import torch
+
+    from non_prefix_kv_gb300 import binding as B
+    from non_prefix_kv_gb300 import build as nb
+    from non_prefix_kv_gb300 import engine as E
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    nb.build()          # no-op when the in-tree library is current; fails loudly without nvcc
+    B.lib()
+    wl = synth.WORKLOADS[args.workload]
+    shape = wl.shape
+    dev = torch.device("cuda", local)
+
+    t_setup = time.perf_counter()
+    dm = E.DeviceModel.random_on_device(shape, seed=wl.seed)
+    reqs_h = synth.make_requests(wl)
+    mine = shard_requests(len(reqs_h), rank, world)
+    eng = E.BlendEngine(dm, wl.n_tokens)
+    pool = eng.precompute_pool(reqs_h[0].chunk_tokens)
+    reqs = [E.Request(eng, pool, reqs_h[i].order, reqs_h[i].tokens) for i in mine]
+    ratios = []
+    for l in range(shape.n_layers):
+        if l < wl.check_layer:
+            ratios.append(None)
+        elif wl.gradual:
+            ratios.append(B.cb_gradual_ratio(wl.ratio, l, wl.check_layer, 1.5))
+        else:
+            ratios.append(wl.ratio)
+    plan = E.layer_plan(shape, wl.n_tokens, wl.n_cached, ratios, wl.check_layer, wl.gradual)
+    torch.cuda.synchronize()
+    setup_s = time.perf_counter() - t_setup
+
+    def step():
+        for r in reqs:
+            E.run_blend(r, plan)
+
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    stream.synchronize()
+    B.cb_sync(stream, 120.0)
+
+    # capture one step in a CUDA graph (host launch overhead out of the timed loop)
+    n0 = B.cb_kernel_launch_count()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    launches_per_step = B.cb_kernel_launch_count() - n0
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            graph.replay()
+    stream.synchronize()
+
+    # ---------------- timed region: K graph replays
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                graph.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms_local = ev0.elapsed_time(ev1) / args.steps
+    ms = max_over_ranks(ms_local, world, dev)
+    clocks = clk.summary()
+    B.cb_sync(stream, 120.0)
+    tokens_per_step = wl.n_tokens * len(reqs)
+    value = tokens_per_step * world / (ms / 1e3)
+
+    # ---------------- per-kernel timing pass (events around every launch, eager)
+    torch.cuda.synchronize()
+    B.cb_profile_begin(100000)
+    with torch.cuda.stream(stream):
+        for _ in range(args.profile_steps):
+            step()
+    recs = B.cb_profile_end(100000)
+    # selected rows of each layer (for the attention FLOPs)
+    with torch.cuda.stream(stream):
+        for r in reqs:
+            E.run_blend(r, plan, keep_history=True)
+    stream.synchronize()
+    sel_sums = []
+    for l, (mode, _) in enumerate(plan):
+        S = reqs[0].sel_hist[l].cpu().numpy().astype(np.float64)
+        name = {B.CB_LAYER_PRECHECK: "precheck", B.CB_LAYER_CHECK: "check", B.CB_LAYER_STEADY: "steady",
+                B.CB_LAYER_GRADUAL: "gradual"}[mode]
+        sel_sums.append((len(S), float(np.sum(S + 1)), name))
+    flops = step_flops(wl, sel_sums) * len(reqs)
+    attn_flops_step = sum(4.0 * shape.n_heads * shape.head_dim * ps for _, ps, _ in sel_sums) * len(reqs)
+
+    peaks, peak_src = load_peaks()
+    kinds = {}
+    for r in recs:
+        kd = kinds.setdefault(r["kind"], {"launches": 0, "ms": 0.0, "flops": 0.0, "bytes": 0.0})
+        kd["launches"] += 1
+        kd["ms"] += r["ms"]
+        kd["flops"] += r["flops"]
+        kd["bytes"] += r["bytes"]
+    if "attention" in kinds:
+        kinds["attention"]["flops"] = attn_flops_step * args.profile_steps
+    tot_ms = sum(k["ms"] for k in kinds.values()) or 1.0
+    kernels = {}
+    for name, kd in sorted(kinds.items(), key=lambda kv: -kv[1]["ms"]):
+        ent = {"launches_per_step": kd["launches"] / args.profile_steps, "ms_per_step": kd["ms"] / args.profile_steps,
+               "share": kd["ms"] / tot_ms}
+        if kd["flops"]:
+            ent["tflops"] = kd["flops"] / (kd["ms"] / 1e3) / 1e12
+        if kd["bytes"]:
+            ent["gbs"] = kd["bytes"] / (kd["ms"] / 1e3) / 1e9
+        kernels[name] = ent
+    g = kinds.get("gemm", {"launches": 0, "ms": 1.0, "flops": 0.0})
+    gemm_flops_launch = g["flops"] / max(g["launches"], 1)
+    gemm_ms_launch = g["ms"] / max(g["launches"], 1)
+    achieved = gemm_flops_launch / (gemm_ms_launch / 1e3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]) if shape.dtype == "bf16" \
+        else peaks.get("bf16_tflops_sustained", 1700.0) / 16.0
+    roofline = {"bound": "tensor", "kernel": "k_gemm_tc (tcgen05 bf16 GEMM, all launches of a step)",
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{peak_src} bf16_tflops_sustained", "traffic": None,
+                "flops_per_launch": gemm_flops_launch, "ms_per_launch": gemm_ms_launch}
+    hbm_kernels = {}
+    for name in ("rope_shift", "deviation", "copy_rows", "lmhead_gemv"):
+        if name in kinds and kinds[name]["bytes"]:
+            gbs = kinds[name]["bytes"] / (kinds[name]["ms"] / 1e3) / 1e9
+            hbm_kernels[name] = {"gbs": gbs, "frac": gbs / peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])}
+
+    # ---------------- end to end through the public API: pinned host in, token out
+    e2e = None
+    if not args.no_e2e:
+        r0 = reqs[0]
+        host_k = [t.cpu().pin_memory() for t in pool.k]
+        host_v = [t.cpu().pin_memory() for t in pool.v]
+        host_tok = torch.from_numpy(r0.tokens_host).pin_memory()
+        out_tok = torch.empty(1, dtype=torch.int32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host_k + host_v) + host_tok.numel() * 4
+        times = []
+        for i in range(args.warmup + args.steps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            with torch.cuda.stream(stream):
+                for l in range(shape.n_layers):
+                    pool.k[l].copy_(host_k[l], non_blocking=True)
+                    pool.v[l].copy_(host_v[l], non_blocking=True)
+                r0.tokens.copy_(host_tok, non_blocking=True)
+                E.run_blend(r0, plan)
+                out_tok.copy_(r0.token, non_blocking=True)
+            stream.synchronize()
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        t_e2e = statistics.median(times)
+        e2e = {"value": wl.n_tokens / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": 4, "ttft_ms": t_e2e * 1e3, "first_token": int(out_tok.item())}
+    B.cb_sync(stream, 120.0)
+
+    # ---------------- CPU oracle baseline (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, fl, desc = oracle_sample(wl)
+        t_step = dt * nominal_step_flops(wl) / fl
+        cpu = {"value": wl.n_tokens / t_step, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+               "sample": desc, "sample_s": dt}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "ttft_ms": ms / len(reqs), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": shape.dtype, "data": "synthetic (seeded random weights/tokens)",
+        "config": {"workload": wl.name, "n_tokens": wl.n_tokens, "chunks": f"{len(wl.order)}x{wl.chunk_len}",
+                   "n_query": wl.n_query, "ratio": wl.ratio, "layers": shape.n_layers,
+                   "shape": f"d{shape.d_model}/H{shape.n_heads}/Hkv{shape.n_kv_heads}/hd{shape.head_dim}/F{shape.d_ff}",
+                   "requests_per_rank": len(reqs), "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (weights + chunk KV + blended KV > 129 MB); CUDA-graph replay"},
+        "gpu_launches": int(launches_per_step * args.steps),
+        "launches_per_step": int(launches_per_step),
+        "step_tflops": flops / (ms / 1e3) / 1e12,
+        "roofline": roofline, "hbm_kernels": hbm_kernels, "kernels": kernels,
+        "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "setup_s": setup_s,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return reference_arm(args)
+    return our_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,303 @@
+/*
+ * cacheblend.h — C ABI of the GB300 (sm_103a) selective-KV-recompute library.
+ *
+ * The library fuses key/value caches that were precomputed for each document chunk in
+ * isolation into one long-context prefill, recomputing only the tokens whose KV deviates
+ * most (CacheBlend).  Sources cited below by short tag:
+ *   [CB-A] "論文解説: CacheBlend — RAGシステム向けKV Cache融合による高速LLMサービング"
+ *          (0h-n0.github.io/posts/paper-2312-03052)
+ *   [CB-B] CacheBlend explainer, abeam.tech (2026-09-20-cacheblend-rag-cached-knowledge-fusion)
+ *   [PC]   "論文解説: Prompt Cache — モジュラーAttention再利用による低レイテンシ推論"
+ *          (0h-n0.github.io/posts/paper-2402-01008)
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - Memory: the caller allocates every device buffer; the library allocates nothing on
+ *    the call path.  Scratch comes from a caller-provided device workspace whose size
+ *    cb_workspace_bytes() returns.  Pointers named *_host are host memory; all others
+ *    are device memory.  The library never frees caller memory.
+ *  - Streams: every call takes a cudaStream_t (passed as void*, NULL = legacy default
+ *    stream), enqueues its kernels on it and returns without synchronising, unless the
+ *    description says otherwise.
+ *  - Errors: an int status.  All argument checks run on the host before any launch, so a
+ *    call that returns an error has enqueued nothing.  Kernels that detect bad data at run
+ *    time (a non-finite deviation score, an index out of range) set a sticky device error
+ *    word that cb_sync() returns; they never trap.
+ *  - Layout: row-major, token-major.  A K or V cache is [n_rows, n_kv_heads * head_dim]
+ *    (heads contiguous inside a row).  Hidden rows are [n, d_model].  Weights are stored
+ *    output-major, [out_features, in_features], so a projection is y = x W^T.
+ *  - Positions: in a blended sequence the row index is the token's position.  RoPE pairs
+ *    are interleaved (x[2i], x[2i+1]) and rotate by pos * theta_i, theta_i =
+ *    base^(-2i/head_dim) ([CB-A] §RoPE).  A cos/sin table built by cb_rope_table() is
+ *    passed to every call that rotates.
+ *  - Element type: dims->dtype (CB_F32 or CB_BF16) applies to every floating tensor of a
+ *    call except where a parameter says float (fp32); arithmetic is fp32 in both.
+ */
+#ifndef CACHEBLEND_H
+#define CACHEBLEND_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------------------- */
+#define CB_OK               0
+#define CB_ERR_INVALID_ARG  1   /* null pointer, negative size, bad enum               */
+#define CB_ERR_SHAPE        2   /* sizes inconsistent with each other or the dims      */
+#define CB_ERR_DTYPE        3   /* unsupported element type                            */
+#define CB_ERR_WORKSPACE    4   /* workspace smaller than cb_workspace_bytes() asks    */
+#define CB_ERR_NONFINITE    5   /* NaN/Inf deviation score (reported by cb_sync)       */
+#define CB_ERR_CUDA         6   /* a CUDA runtime/driver call failed                   */
+#define CB_ERR_TIMEOUT      7   /* cb_sync waited longer than its limit                */
+#define CB_ERR_UNSUPPORTED  8   /* a shape the kernels do not handle (see message)     */
+#define CB_ERR_DEVICE       9   /* a kernel recorded an out-of-range index             */
+
+#define CB_F32   0
+#define CB_BF16  1
+
+#define CB_DEV_KV  0   /* deviation over K and V                                     */
+#define CB_DEV_K   1   /* deviation over K only (the page's select_hkvd_tokens code)  */
+
+#define CB_LAYER_PRECHECK 0   /* layer before the check layer: every row            */
+#define CB_LAYER_CHECK    1   /* HKVD selection over all cached rows                 */
+#define CB_LAYER_STEADY   2   /* reuse the incoming row set (fixed mode)             */
+#define CB_LAYER_GRADUAL  3   /* re-select inside the incoming row set               */
+
+typedef struct {
+    int32_t d_model;      /* d                                                       */
+    int32_t n_heads;      /* H  query heads                                          */
+    int32_t n_kv_heads;   /* Hkv  (GQA: H % Hkv == 0; query head h reads h / (H/Hkv)) */
+    int32_t head_dim;     /* hd (even)                                               */
+    int32_t d_ff;         /* F  SwiGLU width                                         */
+    int32_t vocab;        /* lm_head rows                                            */
+    double  rope_base;    /* RoPE base (1e4 Llama, 5e6 Yi)                           */
+    float   rms_eps;      /* RMSNorm epsilon                                         */
+    int32_t dtype;        /* CB_F32 or CB_BF16                                       */
+} cb_dims;
+
+/* One decoder layer's weights (device, dims->dtype).  Pre-norm Llama layer, no biases. */
+typedef struct {
+    const void* attn_norm;   /* [d]                                                 */
+    const void* wqkv;        /* [(H + 2 Hkv) hd, d]: rows of Wq, then Wk, then Wv    */
+    const void* wo;          /* [d, H hd]                                           */
+    const void* ffn_norm;    /* [d]                                                 */
+    const void* w_gate_up;   /* [2F, d]: rows 0..F-1 gate, rows F..2F-1 up           */
+    const void* w_down;      /* [d, F]                                              */
+} cb_layer_w;
+
+/* ---- housekeeping ----------------------------------------------------------------- */
+
+/* Human-readable text for a status code (static storage). */
+const char* cb_status_string(int status);
+
+/* Detail of the last error raised on the calling thread (static, thread-local). */
+const char* cb_last_error_message(void);
+
+/* Waits for `stream` (polling, up to timeout_s seconds; <= 0 means no limit), then reads
+ * and clears the sticky device error word.  Returns CB_OK, CB_ERR_TIMEOUT (nothing was
+ * cancelled; the work is still queued), CB_ERR_NONFINITE, CB_ERR_DEVICE or CB_ERR_CUDA.
+ * The pages' synchronize() ([CB-A] §vLLM integration). */
+int cb_sync(void* stream, double timeout_s);
+
+/* Device workspace (bytes) large enough for every call below on rows up to n_tok and a
+ * selected set of up to m_max rows, for these dims.  Host-only. */
+int cb_workspace_bytes(const cb_dims* dims, int64_t n_tok, int64_t m_max, size_t* out_host);
+
+/* HKVD budget: k = floor(n_cached * ratio) in double, at least 1 when ratio > 0, 0 when
+ * ratio == 0, at most n_cand ([CB-A] §HKVD selection code: max(int(N*r), 1)).
+ * Host-only.  Returns k, or -1 for a ratio outside [0, 1] or a negative size. */
+int64_t cb_hkvd_budget(int64_t n_cached, double ratio, int64_t n_cand);
+
+/* Gradual-filtering ratio of `layer`: r_l = r + (r1 - r) 2^-(layer - check_layer),
+ * r1 = min(1, r1_factor * r) ([CB-A] §Gradual filtering: r1 slightly above r, r_i
+ * approaching r).  Host-only.  Returns -1 for layer < check_layer. */
+double cb_gradual_ratio(double r, int32_t layer, int32_t check_layer, double r1_factor);
+
+/* Load-controller ratio r* = max(r_min, T_load / T_prefill) ([CB-A] §Pipelining and load
+ * controller).  Host-only. */
+double cb_load_controller_ratio(double r_min, double t_load_s, double t_prefill_s);
+
+/* ---- RoPE --------------------------------------------------------------------------- */
+
+/* Fills cos_sin [max_pos][head_dim/2][2] (fp32: cos, sin) with cos/sin(p theta_i) for
+ * p in [0, max_pos), the angle formed in fp64 on the device and rounded once
+ * ([CB-A] §RoPE rotation matrix R(m)).  Negative rotations use the same table with the
+ * sine negated. */
+int cb_rope_table(float* cos_sin, int32_t max_pos, int32_t head_dim, double base,
+                  void* stream);
+
+/* Re-positions cached keys: k_dst[i] = R(delta[i]) k_src[src_row[i]], and copies values
+ * v_dst[i] = v_src[src_row[i]] ([PC] §RoPE position adjustment, k(p) = R(p-p') k(p');
+ * [CB-B] position correction when loading chunk KV).
+ *   k_src, v_src : [*, Hkv hd] source rows (e.g. a pool of precomputed chunk caches)
+ *   src_row      : [n_rows] int32 source row per destination row, or NULL (row i)
+ *   delta        : [n_rows] int32 position offset p - p', |delta| < max_pos
+ *   k_dst, v_dst : [n_rows, Hkv hd]; v_src/v_dst may both be NULL (keys only).
+ * In-place (k_dst == k_src) is allowed only with src_row == NULL. */
+int cb_rope_shift(void* k_dst, void* v_dst, const void* k_src, const void* v_src,
+                  const int32_t* src_row, const int32_t* delta, int64_t n_rows,
+                  const cb_dims* dims, const float* cos_sin, int32_t max_pos, void* stream);
+
+/* ---- HKVD selection ----------------------------------------------------------------- */
+
+/* Per-candidate deviation and top-k ([CB-A] §KV deviation; §HKVD selection code):
+ *   scores[c] = sum_e (k_new[new_row[c]][e] - k_ref[ref_row[c]][e])^2
+ *             (+ the same over V when dev_mode == CB_DEV_KV), fp32 accumulation;
+ *   sel       = the k candidates with the largest scores, ties to the lower candidate
+ *               index, written ascending as ref_row values (length k).
+ *   k_new/v_new : [*, Hkv hd] freshly computed rows; k_ref/v_ref : [*, Hkv hd] the cache
+ *   new_row/ref_row : [n_cand] int32 ascending row maps, or NULL (identity)
+ *   scores : [n_cand] fp32 (output, may be NULL)
+ * 0 <= k <= n_cand.  A non-finite score sets CB_ERR_NONFINITE (cb_sync). */
+int cb_kv_deviation_topk(const void* k_new, const void* v_new, const void* k_ref,
+                         const void* v_ref, const int32_t* new_row, const int32_t* ref_row,
+                         int32_t n_cand, int32_t k, int32_t dev_mode, const cb_dims* dims,
+                         float* scores, int32_t* sel, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/* Top-k of given fp32 scores (>= 0, finite), ties to the lower index, output ascending
+ * as cand[c] (cand NULL = c).  The selection step alone, for bit-exact checks. */
+int cb_topk_from_scores(const float* scores, const int32_t* cand, int32_t n_cand,
+                        int32_t k, int32_t* sel, void* ws, size_t ws_bytes, void* stream);
+
+/* ---- row movement ------------------------------------------------------------------- */
+
+/* dst[i] = src[idx[i]] for i < n; rows of row_bytes bytes (a multiple of 4); idx NULL
+ * means i ([CB-A] §Selective recomputation, Step 1: restrict the input to S). */
+int cb_gather_rows(void* dst, const void* src, const int32_t* idx, int64_t n,
+                   int64_t row_bytes, void* stream);
+
+/* KV expansion ([CB-A] §Selective recomputation, Step 3: K_new = Concat(K_pre[not S],
+ * K_recomp[S])):  k_cache[dst_idx[i]] = k_rows[src_idx[i]] and the same for V, i < n.
+ * src_idx NULL means i.  Rows are [Hkv hd]. */
+int cb_scatter_kv(void* k_cache, void* v_cache, const void* k_rows, const void* v_rows,
+                  const int32_t* dst_idx, const int32_t* src_idx, int64_t n,
+                  const cb_dims* dims, void* stream);
+
+/* ---- selective layer pieces --------------------------------------------------------- */
+
+/* Q/K/V of selected rows ([CB-A] §Selective recomputation, Step 2; [CB-B] §技術の仕組み):
+ *   a = RMSNorm(x[rows[i]]) * attn_norm;  q = a Wq^T, k = a Wk^T, v = a Wv^T;
+ *   RoPE on q and k at position pos[i].
+ *   x : [*, d];  rows : [M] int32 or NULL (i);  pos : [M] int32 (< max_pos)
+ *   q : [M, H hd] or NULL;  k, v : [M, Hkv hd] or both NULL. */
+int cb_selective_qkv(const void* x, const int32_t* rows, const int32_t* pos, int32_t M,
+                     const cb_dims* dims, const cb_layer_w* w, const float* cos_sin,
+                     int32_t max_pos, void* q, void* k, void* v, void* ws, size_t ws_bytes,
+                     void* stream);
+
+/* Selected queries over the whole causal KV ([CB-A] §Selective recomputation, Step 4;
+ * [CB-B]: the selected tokens attend over the entire input):
+ *   out[j, h] = softmax_t<=q_pos[j]( q[j,h] . k_cache[t, g(h)] / sqrt(hd) ) v_cache[t, g(h)]
+ *   q : [M, H hd];  q_pos : [M] int32 causal bound (row index = position), each < n_kv
+ *   k_cache, v_cache : [n_kv, Hkv hd];  out : [M, H hd]. */
+int cb_partial_attention(const void* q, const int32_t* q_pos, int32_t M,
+                         const void* k_cache, const void* v_cache, int64_t n_kv,
+                         const cb_dims* dims, void* out, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/* O-projection with residual and SwiGLU FFN with residual, on M rows
+ * ([CB-A] §Selective recomputation, Step 4, the next layer's input):
+ *   h = x_res + attn Wo^T;  y = h + (SiLU(b Wg^T) * (b Wu^T)) Wd^T,  b = RMSNorm(h) g.
+ *   attn : [M, H hd];  x_res : [M, d];  x_out : [M, d] (may alias x_res). */
+int cb_o_proj_ffn(const void* attn, const void* x_res, int32_t M, const cb_dims* dims,
+                  const cb_layer_w* w, void* x_out, void* ws, size_t ws_bytes, void* stream);
+
+/* One layer of the blend ([CB-A] §Selective recomputation Steps 1-4, §HKVD selection,
+ * §Gradual filtering).  Rows of the sequence are 0..n_tok-1; rows < n_cached come from
+ * chunk caches already re-positioned into k_cache/v_cache ([n_tok, Hkv hd], updated in
+ * place); rows >= n_cached are the uncached suffix.  Forced rows F = [n_cached, n_tok)
+ * plus row n_tok-1 are always recomputed.
+ *   x_in [m_in, d] : hidden rows of the incoming set s_in (ascending; NULL = 0..m_in-1)
+ *   mode PRECHECK  : all rows (m_in == n_tok); Q for every row, K/V only for rows
+ *                    >= n_cached; output all rows.
+ *   mode CHECK     : all rows in; K/V for every row; deviation over the cached,
+ *                    unforced rows; S = top-k_budget U F.
+ *   mode STEADY    : S = s_in.
+ *   mode GRADUAL   : K/V for s_in; deviation over its cached, unforced rows;
+ *                    S = top-k_budget U F (a subset of s_in).
+ *   For CHECK/STEADY/GRADUAL: K/V of S are written into the cache (Step 3), then Q of S,
+ *   attention of S over the cache, O-proj and FFN give x_out [m_out, d] for the rows
+ *   s_out [m_out] (ascending).
+ *   sel_override : [k_budget] ascending cache rows that replace the top-k choice (the
+ *                  forced rows are still added), or NULL.
+ *   scores_out   : [n_cand] fp32 deviation scores, or NULL (CHECK/GRADUAL only).
+ *   m_out_host   : receives m_out (known on the host before any launch: no sync).
+ * x_out must not alias x_in. */
+int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode,
+                   const void* x_in, const int32_t* s_in, int32_t m_in,
+                   int64_t n_tok, int64_t n_cached, void* k_cache, void* v_cache,
+                   const float* cos_sin, int32_t max_pos, int32_t k_budget, int32_t dev_mode,
+                   const int32_t* sel_override, void* x_out, int32_t* s_out,
+                   int32_t* m_out_host, float* scores_out, void* ws, size_t ws_bytes,
+                   void* stream);
+
+/* Standard causal prefill of n tokens at positions pos0..pos0+n-1 through n_layers
+ * layers: the quality reference (KV^full, [CB-A] §KV cache definitions; [CB-B] "full KV
+ * recompute") and the per-chunk precompute (KV^pre, pos0 = 0).
+ *   layers_host : host array of n_layers cb_layer_w;  embed : [vocab, d]
+ *   tokens : [n] int32 device;  k_out_host/v_out_host : host arrays of n_layers device
+ *   pointers, each [n, Hkv hd];  h_last : [d] hidden row n-1 after the last layer;
+ *   x_all : [n, d] final hidden rows, or NULL. */
+int cb_full_prefill(const cb_dims* dims, int32_t n_layers, const cb_layer_w* layers_host,
+                    const void* embed, const int32_t* tokens, int32_t n, int32_t pos0,
+                    void* const* k_out_host, void* const* v_out_host, void* h_last,
+                    void* x_all, const float* cos_sin, int32_t max_pos, void* ws,
+                    size_t ws_bytes, void* stream);
+
+/* First answer token: token[0] = argmax_v (RMSNorm(h) final_norm) . w_lm[v], lowest v on
+ * ties.  h : [d];  w_lm : [vocab, d];  logits : [vocab] fp32 or NULL;  token : [1] int32
+ * device. */
+int cb_lmhead_argmax(const void* h, const void* final_norm, const void* w_lm,
+                     const cb_dims* dims, float* logits, int32_t* token, void* ws,
+                     size_t ws_bytes, void* stream);
+
+/* ---- launch accounting and per-launch timing ---------------------------------------- */
+
+/* Kernel families reported by the profiler. */
+#define CB_PROF_ROPE_SHIFT 0
+#define CB_PROF_COPY_ROWS  1
+#define CB_PROF_RMSNORM    2
+#define CB_PROF_GEMM       3
+#define CB_PROF_ATTENTION  4
+#define CB_PROF_DEVIATION  5
+#define CB_PROF_TOPK       6
+#define CB_PROF_INDEX      7
+#define CB_PROF_LMHEAD     8
+#define CB_PROF_ARGMAX     9
+#define CB_PROF_ROPE_TABLE 10
+
+typedef struct {
+    int32_t kind;      /* CB_PROF_*                                                     */
+    int32_t aux;       /* GEMM: epilogue kind; otherwise 0                              */
+    int64_t m, n, k;   /* launch sizes (GEMM: M, N, K; attention: queries, keys, heads) */
+    double  flops;     /* algorithmic floating-point operations (0 if not known on host) */
+    double  bytes;     /* algorithmic HBM bytes (compulsory reads + writes)             */
+    float   ms;        /* device time between events recorded around the launch        */
+} cb_prof_record;
+
+/* Number of kernels this library has launched in the process (host-side count). */
+int64_t cb_kernel_launch_count(void);
+
+/* Starts recording a CUDA-event pair around every kernel launch made by the calling
+ * thread, up to max_records launches.  Not for use while a stream is being captured. */
+int cb_profile_begin(int32_t max_records);
+
+/* Stops recording, waits for the recorded events, writes up to max_records records
+ * (host memory) and their count. */
+int cb_profile_end(cb_prof_record* out_host, int32_t max_records, int32_t* n_out_host);
+
+/* Plain projection y = x W^T on the same GEMM kernels the layer calls use (tcgen05/TMEM
+ * for bf16, exact-fp32 SIMT for fp32); the "Q/K/V transform" primitive of [CB-A]
+ * §Selective recomputation Step 2 without an epilogue.  x : [M, K], w : [N, K], y : [M, N],
+ * all of element type `dtype`.  bf16 needs N % 16 == 0 and K % 8 == 0; fp32 N % 4 == 0. */
+int cb_linear(const void* x, const void* w, void* y, int32_t M, int32_t N, int32_t K, int32_t dtype,
+              void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CACHEBLEND_H */

@@ -1,0 +1,249 @@
+"""Thin ctypes binding of libcacheblend.so: the C entry points under the same names,
+taking torch tensors (device memory) and marshalling them to raw pointers.  No arithmetic
+of the method happens here; every step runs in the library's CUDA kernels.  Raises
+CBError on any non-zero status.  Fails loudly when the library has not been built."""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional, Sequence
+
+from . import build as _build
+
+CB_OK = 0
+CB_F32, CB_BF16 = 0, 1
+CB_DEV_KV, CB_DEV_K = 0, 1
+CB_LAYER_PRECHECK, CB_LAYER_CHECK, CB_LAYER_STEADY, CB_LAYER_GRADUAL = 0, 1, 2, 3
+STATUS_NAMES = {0: "CB_OK", 1: "CB_ERR_INVALID_ARG", 2: "CB_ERR_SHAPE", 3: "CB_ERR_DTYPE",
+                4: "CB_ERR_WORKSPACE", 5: "CB_ERR_NONFINITE", 6: "CB_ERR_CUDA", 7: "CB_ERR_TIMEOUT",
+                8: "CB_ERR_UNSUPPORTED", 9: "CB_ERR_DEVICE"}
+
+
+class CBError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class cb_dims(C.Structure):
+    _fields_ = [("d_model", C.c_int32), ("n_heads", C.c_int32), ("n_kv_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("d_ff", C.c_int32), ("vocab", C.c_int32),
+                ("rope_base", C.c_double), ("rms_eps", C.c_float), ("dtype", C.c_int32)]
+
+
+class cb_layer_w(C.Structure):
+    _fields_ = [("attn_norm", C.c_void_p), ("wqkv", C.c_void_p), ("wo", C.c_void_p),
+                ("ffn_norm", C.c_void_p), ("w_gate_up", C.c_void_p), ("w_down", C.c_void_p)]
+
+
+class cb_prof_record(C.Structure):
+    _fields_ = [("kind", C.c_int32), ("aux", C.c_int32), ("m", C.c_int64), ("n", C.c_int64), ("k", C.c_int64),
+                ("flops", C.c_double), ("bytes", C.c_double), ("ms", C.c_float)]
+
+
+PROF_KINDS = {0: "rope_shift", 1: "copy_rows", 2: "rmsnorm", 3: "gemm", 4: "attention", 5: "deviation",
+              6: "topk", 7: "index", 8: "lmhead_gemv", 9: "argmax", 10: "rope_table"}
+
+_P = C.c_void_p
+_I32 = C.c_int32
+_I64 = C.c_int64
+_SZ = C.c_size_t
+_PROTOS = {
+    "cb_status_string": (C.c_char_p, [C.c_int]),
+    "cb_last_error_message": (C.c_char_p, []),
+    "cb_sync": (C.c_int, [_P, C.c_double]),
+    "cb_workspace_bytes": (C.c_int, [C.POINTER(cb_dims), _I64, _I64, C.POINTER(_SZ)]),
+    "cb_hkvd_budget": (_I64, [_I64, C.c_double, _I64]),
+    "cb_gradual_ratio": (C.c_double, [C.c_double, _I32, _I32, C.c_double]),
+    "cb_load_controller_ratio": (C.c_double, [C.c_double, C.c_double, C.c_double]),
+    "cb_rope_table": (C.c_int, [_P, _I32, _I32, C.c_double, _P]),
+    "cb_rope_shift": (C.c_int, [_P, _P, _P, _P, _P, _P, _I64, C.POINTER(cb_dims), _P, _I32, _P]),
+    "cb_kv_deviation_topk": (C.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, C.POINTER(cb_dims),
+                                       _P, _P, _P, _SZ, _P]),
+    "cb_topk_from_scores": (C.c_int, [_P, _P, _I32, _I32, _P, _P, _SZ, _P]),
+    "cb_gather_rows": (C.c_int, [_P, _P, _P, _I64, _I64, _P]),
+    "cb_scatter_kv": (C.c_int, [_P, _P, _P, _P, _P, _P, _I64, C.POINTER(cb_dims), _P]),
+    "cb_selective_qkv": (C.c_int, [_P, _P, _P, _I32, C.POINTER(cb_dims), C.POINTER(cb_layer_w), _P, _I32,
+                                   _P, _P, _P, _P, _SZ, _P]),
+    "cb_partial_attention": (C.c_int, [_P, _P, _I32, _P, _P, _I64, C.POINTER(cb_dims), _P, _P, _SZ, _P]),
+    "cb_o_proj_ffn": (C.c_int, [_P, _P, _I32, C.POINTER(cb_dims), C.POINTER(cb_layer_w), _P, _P, _SZ, _P]),
+    "cb_blend_layer": (C.c_int, [C.POINTER(cb_dims), C.POINTER(cb_layer_w), _I32, _P, _P, _I32, _I64, _I64,
+                                 _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, C.POINTER(_I32), _P, _P, _SZ, _P]),
+    "cb_full_prefill": (C.c_int, [C.POINTER(cb_dims), _I32, C.POINTER(cb_layer_w), _P, _P, _I32, _I32,
+                                  C.POINTER(_P), C.POINTER(_P), _P, _P, _P, _I32, _P, _SZ, _P]),
+    "cb_lmhead_argmax": (C.c_int, [_P, _P, _P, C.POINTER(cb_dims), _P, _P, _P, _SZ, _P]),
+    "cb_linear": (C.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _P]),
+    "cb_kernel_launch_count": (_I64, []),
+    "cb_profile_begin": (C.c_int, [_I32]),
+    "cb_profile_end": (C.c_int, [C.POINTER(cb_prof_record), _I32, C.POINTER(_I32)]),
+}
+
+_LIB = None
+
+
+def lib():
+    """Load the in-tree library (never builds implicitly on the call path)."""
+    global _LIB
+    if _LIB is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with non_prefix_kv_gb300.build.build()")
+        L = C.CDLL(path)
+        for name, (res, args) in _PROTOS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, st: int):
+    if st != CB_OK:
+        raise CBError(fn, st, lib().cb_last_error_message().decode(errors="replace"))
+
+
+def _nbytes(t) -> int:
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+# ---- host helpers -------------------------------------------------------------------------
+def cb_hkvd_budget(n_cached: int, ratio: float, n_cand: int) -> int:
+    return int(lib().cb_hkvd_budget(n_cached, ratio, n_cand))
+
+
+def cb_gradual_ratio(r: float, layer: int, check_layer: int, r1_factor: float = 1.5) -> float:
+    return float(lib().cb_gradual_ratio(r, layer, check_layer, r1_factor))
+
+
+def cb_load_controller_ratio(r_min: float, t_load_s: float, t_prefill_s: float) -> float:
+    return float(lib().cb_load_controller_ratio(r_min, t_load_s, t_prefill_s))
+
+
+def cb_workspace_bytes(dims: cb_dims, n_tok: int, m_max: int) -> int:
+    out = _SZ(0)
+    _check("cb_workspace_bytes", lib().cb_workspace_bytes(C.byref(dims), n_tok, m_max, C.byref(out)))
+    return int(out.value)
+
+
+def cb_sync(stream=None, timeout_s: float = 60.0) -> None:
+    _check("cb_sync", lib().cb_sync(_stream(stream), timeout_s))
+
+
+# ---- device entry points --------------------------------------------------------------------
+def cb_rope_table(cos_sin, max_pos: int, head_dim: int, base: float, stream=None):
+    _check("cb_rope_table", lib().cb_rope_table(_ptr(cos_sin), max_pos, head_dim, base, _stream(stream)))
+
+
+def cb_rope_shift(k_dst, v_dst, k_src, v_src, src_row, delta, n_rows: int, dims: cb_dims, cos_sin,
+                  max_pos: int, stream=None):
+    _check("cb_rope_shift", lib().cb_rope_shift(_ptr(k_dst), _ptr(v_dst), _ptr(k_src), _ptr(v_src),
+                                                _ptr(src_row), _ptr(delta), n_rows, C.byref(dims),
+                                                _ptr(cos_sin), max_pos, _stream(stream)))
+
+
+def cb_kv_deviation_topk(k_new, v_new, k_ref, v_ref, new_row, ref_row, n_cand: int, k: int, dev_mode: int,
+                         dims: cb_dims, scores, sel, ws, stream=None):
+    _check("cb_kv_deviation_topk", lib().cb_kv_deviation_topk(
+        _ptr(k_new), _ptr(v_new), _ptr(k_ref), _ptr(v_ref), _ptr(new_row), _ptr(ref_row), n_cand, k,
+        dev_mode, C.byref(dims), _ptr(scores), _ptr(sel), _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def cb_topk_from_scores(scores, cand, n_cand: int, k: int, sel, ws, stream=None):
+    _check("cb_topk_from_scores", lib().cb_topk_from_scores(_ptr(scores), _ptr(cand), n_cand, k, _ptr(sel),
+                                                            _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def cb_gather_rows(dst, src, idx, n: int, row_bytes: int, stream=None):
+    _check("cb_gather_rows", lib().cb_gather_rows(_ptr(dst), _ptr(src), _ptr(idx), n, row_bytes,
+                                                  _stream(stream)))
+
+
+def cb_scatter_kv(k_cache, v_cache, k_rows, v_rows, dst_idx, src_idx, n: int, dims: cb_dims, stream=None):
+    _check("cb_scatter_kv", lib().cb_scatter_kv(_ptr(k_cache), _ptr(v_cache), _ptr(k_rows), _ptr(v_rows),
+                                                _ptr(dst_idx), _ptr(src_idx), n, C.byref(dims),
+                                                _stream(stream)))
+
+
+def cb_selective_qkv(x, rows, pos, M: int, dims: cb_dims, w: cb_layer_w, cos_sin, max_pos: int, q, k, v,
+                     ws, stream=None):
+    _check("cb_selective_qkv", lib().cb_selective_qkv(
+        _ptr(x), _ptr(rows), _ptr(pos), M, C.byref(dims), C.byref(w), _ptr(cos_sin), max_pos, _ptr(q),
+        _ptr(k), _ptr(v), _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def cb_partial_attention(q, q_pos, M: int, k_cache, v_cache, n_kv: int, dims: cb_dims, out, ws=None,
+                         stream=None):
+    _check("cb_partial_attention", lib().cb_partial_attention(
+        _ptr(q), _ptr(q_pos), M, _ptr(k_cache), _ptr(v_cache), n_kv, C.byref(dims), _ptr(out), _ptr(ws),
+        _nbytes(ws), _stream(stream)))
+
+
+def cb_o_proj_ffn(attn, x_res, M: int, dims: cb_dims, w: cb_layer_w, x_out, ws, stream=None):
+    _check("cb_o_proj_ffn", lib().cb_o_proj_ffn(_ptr(attn), _ptr(x_res), M, C.byref(dims), C.byref(w),
+                                                _ptr(x_out), _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def cb_blend_layer(dims: cb_dims, w: cb_layer_w, mode: int, x_in, s_in, m_in: int, n_tok: int, n_cached: int,
+                   k_cache, v_cache, cos_sin, max_pos: int, k_budget: int, dev_mode: int, sel_override,
+                   x_out, s_out, scores_out, ws, stream=None) -> int:
+    m_out = _I32(0)
+    _check("cb_blend_layer", lib().cb_blend_layer(
+        C.byref(dims), C.byref(w), mode, _ptr(x_in), _ptr(s_in), m_in, n_tok, n_cached, _ptr(k_cache),
+        _ptr(v_cache), _ptr(cos_sin), max_pos, k_budget, dev_mode, _ptr(sel_override), _ptr(x_out),
+        _ptr(s_out), C.byref(m_out), _ptr(scores_out), _ptr(ws), _nbytes(ws), _stream(stream)))
+    return int(m_out.value)
+
+
+def cb_full_prefill(dims: cb_dims, layers: Sequence[cb_layer_w], embed, tokens, n: int, pos0: int,
+                    k_out: Sequence, v_out: Sequence, h_last, x_all, cos_sin, max_pos: int, ws, stream=None):
+    L = len(layers)
+    arr_w = (cb_layer_w * L)(*layers)
+    arr_k = (C.c_void_p * L)(*[_ptr(t) for t in k_out])
+    arr_v = (C.c_void_p * L)(*[_ptr(t) for t in v_out])
+    _check("cb_full_prefill", lib().cb_full_prefill(
+        C.byref(dims), L, arr_w, _ptr(embed), _ptr(tokens), n, pos0, arr_k, arr_v, _ptr(h_last), _ptr(x_all),
+        _ptr(cos_sin), max_pos, _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def cb_lmhead_argmax(h, final_norm, w_lm, dims: cb_dims, logits, token, ws, stream=None):
+    _check("cb_lmhead_argmax", lib().cb_lmhead_argmax(_ptr(h), _ptr(final_norm), _ptr(w_lm), C.byref(dims),
+                                                      _ptr(logits), _ptr(token), _ptr(ws), _nbytes(ws),
+                                                      _stream(stream)))
+
+
+def cb_linear(x, w, y, M: int, N: int, K: int, dtype: int, stream=None):
+    _check("cb_linear", lib().cb_linear(_ptr(x), _ptr(w), _ptr(y), M, N, K, dtype, _stream(stream)))
+
+
+def cb_kernel_launch_count() -> int:
+    return int(lib().cb_kernel_launch_count())
+
+
+def cb_profile_begin(max_records: int = 4096):
+    _check("cb_profile_begin", lib().cb_profile_begin(max_records))
+
+
+def cb_profile_end(max_records: int = 4096):
+    """Returns a list of dicts {kind, aux, m, n, k, flops, bytes, ms}, one per launch."""
+    arr = (cb_prof_record * max_records)()
+    n = _I32(0)
+    _check("cb_profile_end", lib().cb_profile_end(arr, max_records, C.byref(n)))
+    return [{"kind": PROF_KINDS.get(r.kind, str(r.kind)), "aux": r.aux, "m": r.m, "n": r.n, "k": r.k,
+             "flops": r.flops, "bytes": r.bytes, "ms": r.ms} for r in arr[:n.value]]

@@ -1,0 +1,698 @@
+// C ABI of the selective-KV-recompute library: host-side validation, workspace carving and
+// the per-layer orchestration of the kernels.  Every argument check happens before the first
+// launch, so a call that returns an error has enqueued nothing.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+#include <time.h>
+
+#include <algorithm>
+#include <atomic>
+#include <vector>
+
+#include "../../include/cacheblend.h"
+#include "cb_internal.h"
+
+namespace cb {
+uint32_t take_error_gemm_tc();
+cudaError_t launch_gemm_simt_bf16(const GemmDesc& g, cudaStream_t s);
+}  // namespace cb
+
+using namespace cb;
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+#define CB_CUDA(expr)                                                                    \
+  do {                                                                                   \
+    cudaError_t e__ = (expr);                                                            \
+    if (e__ != cudaSuccess)                                                              \
+      return fail(CB_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e__));         \
+  } while (0)
+
+inline cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
+
+// ---- launch accounting and optional per-launch CUDA-event timing (calling thread only)
+std::atomic<long long> g_launches{0};
+
+struct ProfState {
+  bool on = false;
+  int cap = 0;
+  std::vector<cudaEvent_t> ev;        // 2 per record, created once and reused
+  std::vector<cb_prof_record> rec;
+};
+thread_local ProfState g_prof;
+
+struct ProfScope {
+  int idx = -1;
+  cudaStream_t s;
+  ProfScope(int kind, int aux, int64_t m, int64_t n, int64_t k, double flops, double bytes, cudaStream_t st)
+      : s(st) {
+    if (m <= 0) return;          // the launcher returns without launching
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    ProfState& P = g_prof;
+    if (!P.on || (int)P.rec.size() >= P.cap) return;
+    idx = (int)P.rec.size();
+    cb_prof_record r{};
+    r.kind = kind;
+    r.aux = aux;
+    r.m = m;
+    r.n = n;
+    r.k = k;
+    r.flops = flops;
+    r.bytes = bytes;
+    P.rec.push_back(r);
+    cudaEventRecord(P.ev[2 * idx], s);
+  }
+  ~ProfScope() {
+    if (idx >= 0) cudaEventRecord(g_prof.ev[2 * idx + 1], s);
+  }
+};
+
+// wraps one kernel launch: counts it and, when profiling, brackets it with events
+#define CB_LAUNCH(kind, aux, m, n, k, flops, bytes, stream, expr)         \
+  do {                                                                    \
+    ProfScope ps__(kind, aux, m, n, k, flops, bytes, stream);             \
+    CB_CUDA(expr);                                                        \
+  } while (0)
+
+inline size_t esize(int dt) { return dt == CB_BF16 ? 2 : 4; }
+
+double gemm_flops(const GemmDesc& g) {
+  return 2.0 * g.M * g.N * g.K * (g.epi.kind == EPI_SWIGLU ? 2 : 1);
+}
+// compulsory HBM traffic of one GEMM launch: A, B (both halves for SwiGLU), C (+ residual)
+double gemm_bytes(int dt, const GemmDesc& g) {
+  const double B = (double)esize(dt);
+  const double nb = (g.epi.kind == EPI_SWIGLU ? 2.0 : 1.0) * g.N;
+  double b = B * ((double)g.M * g.K + nb * g.K + (double)g.M * g.N);
+  if (g.epi.kind == EPI_RESID) b += B * (double)g.M * g.N;
+  return b;
+}
+
+#define L_GEMM(dt, gexpr, s)                                                                  \
+  do {                                                                                        \
+    const GemmDesc g__ = (gexpr);                                                             \
+    CB_LAUNCH(CB_PROF_GEMM, g__.epi.kind, g__.M, g__.N, g__.K, gemm_flops(g__), gemm_bytes(dt, g__), s, \
+              launch_gemm(dt, g__, s));                                                       \
+  } while (0)
+#define L_IOTA(out, n, start, s) \
+  CB_LAUNCH(CB_PROF_INDEX, 0, (n), 0, 0, 0.0, 4.0 * (n), s, launch_iota(out, n, start, s))
+#define L_RMSNORM(dti, dto, out, x, rows, g, n, d, eps, s)                                       \
+  CB_LAUNCH(CB_PROF_RMSNORM, 0, (n), (d), 0, 3.0 * (n) * (d),                                    \
+            (double)(n) * (d) * (esize(dti) + esize(dto)), s, launch_rmsnorm(dti, dto, out, x, rows, g, n, d, eps, s))
+#define L_ATTN(dt, q, qpos, M, kc, vc, nkv, H, Hkv, hd, out, ws, wsb, s)                         \
+  CB_LAUNCH(CB_PROF_ATTENTION, 0, (M), (nkv), (H), 0.0, 0.0, s,                                  \
+            launch_attention(dt, q, qpos, M, kc, vc, nkv, H, Hkv, hd, out, ws, wsb, s))
+#define L_COPY(dst, di, src, si, n, rb, db, sb, s)                                               \
+  CB_LAUNCH(CB_PROF_COPY_ROWS, 0, (n), (rb), 0, 0.0, 2.0 * (n) * (rb), s,                        \
+            launch_copy_rows(dst, di, src, si, n, rb, db, sb, s))
+#define L_DEV(dt, kn, vn, kr, vr, nr, rr, nc, W, usev, sc, s)                                    \
+  CB_LAUNCH(CB_PROF_DEVIATION, 0, (nc), (W), (usev), 3.0 * (nc) * (W) * ((usev) ? 2 : 1),        \
+            (double)(nc) * (W) * esize(dt) * ((usev) ? 4 : 2) + 4.0 * (nc), s,                   \
+            launch_deviation(dt, kn, vn, kr, vr, nr, rr, nc, W, usev, sc, s))
+#define L_TOPK(sc, n, k, ord, s) \
+  CB_LAUNCH(CB_PROF_TOPK, 0, (n), (k), 0, 0.0, 4.0 * (n) + 4.0 * (k), s, launch_topk(sc, n, k, ord, s))
+#define L_MAP(ord, k, map, out, s) \
+  CB_LAUNCH(CB_PROF_INDEX, 0, (k), 0, 0, 0.0, 12.0 * (k), s, launch_map_rows(ord, k, map, out, s))
+#define L_BUILD_SEL(ord, k, cr, f0, fp0, nf, so, ko, s)                                          \
+  CB_LAUNCH(CB_PROF_INDEX, 0, (k) + (nf), 0, 0, 0.0, 16.0 * ((k) + (nf)), s,                     \
+            launch_build_sel(ord, k, cr, f0, fp0, nf, so, ko, s))
+#define L_R2P(rows, k, sin, m, out, s) \
+  CB_LAUNCH(CB_PROF_INDEX, 0, (k), 0, 0, 0.0, 8.0 * (k), s, launch_rows_to_positions(rows, k, sin, m, out, s))
+#define L_ROPE_SHIFT(dt, kd, vd, ks, vs, sr, dl, n, W, hd, tab, mp, s)                           \
+  CB_LAUNCH(CB_PROF_ROPE_SHIFT, 0, (n), (W), 0, 3.0 * (n) * (W),                                 \
+            (double)(n) * (W) * esize(dt) * ((vd) ? 4 : 2) + 4.0 * (n), s,                       \
+            launch_rope_shift(dt, kd, vd, ks, vs, sr, dl, n, W, hd, tab, mp, s))
+#define L_LMGEMV(dt, lg, hn, w, V, d, s)                                                         \
+  CB_LAUNCH(CB_PROF_LMHEAD, 0, (V), (d), 0, 2.0 * (V) * (d), (double)(V) * (d) * esize(dt) + 4.0 * (V), s, \
+            launch_lm_gemv(dt, lg, hn, w, V, d, s))
+#define L_ARGMAX(lg, V, tok, s) \
+  CB_LAUNCH(CB_PROF_ARGMAX, 0, (V), 0, 0, 0.0, 4.0 * (V), s, launch_argmax(lg, V, tok, s))
+#define L_ROPE_TABLE(tab, mp, hd, base, s)                                                       \
+  CB_LAUNCH(CB_PROF_ROPE_TABLE, 0, (int64_t)(mp) * (hd) / 2, (hd), 0, 0.0, 4.0 * (mp) * (hd), s, \
+            launch_rope_table(tab, mp, hd, base, s))
+
+int check_dims(const cb_dims* d) {
+  if (!d) return fail(CB_ERR_INVALID_ARG, "dims is NULL");
+  if (d->dtype != CB_F32 && d->dtype != CB_BF16) return fail(CB_ERR_DTYPE, "dtype %d", d->dtype);
+  if (d->d_model <= 0 || d->n_heads <= 0 || d->n_kv_heads <= 0 || d->head_dim <= 0 || d->d_ff <= 0 ||
+      d->vocab <= 0)
+    return fail(CB_ERR_SHAPE, "non-positive dimension");
+  if (d->n_heads % d->n_kv_heads) return fail(CB_ERR_SHAPE, "n_heads %% n_kv_heads != 0");
+  if (d->head_dim % 32 || d->head_dim > 256)
+    return fail(CB_ERR_UNSUPPORTED, "head_dim must be a multiple of 32, at most 256");
+  if (d->d_model % 16 || d->d_ff % 16)
+    return fail(CB_ERR_UNSUPPORTED, "d_model and d_ff must be multiples of 16");
+  if (!(d->rope_base > 1.0) || !(d->rms_eps >= 0.0f)) return fail(CB_ERR_INVALID_ARG, "rope_base/rms_eps");
+  return CB_OK;
+}
+
+int check_w(const cb_layer_w* w) {
+  if (!w || !w->attn_norm || !w->wqkv || !w->wo || !w->ffn_norm || !w->w_gate_up || !w->w_down)
+    return fail(CB_ERR_INVALID_ARG, "layer weight pointer is NULL");
+  return CB_OK;
+}
+
+// bump allocator over the caller's workspace; base == nullptr measures only
+struct Carver {
+  char* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<char*>(b)) {}
+  void* take(size_t bytes) {
+    off = (off + 255) & ~size_t(255);
+    void* p = base ? base + off : nullptr;
+    off += bytes;
+    return p;
+  }
+};
+
+struct LayerWs {
+  void *a, *q, *knew, *vnew, *attn, *h, *b, *act, *xg, *ag, *xa, *xb, *attn_ws;
+  float *scores, *hn, *logits;
+  int32_t *ord, *keep, *pos, *rows;
+};
+
+// R = rows entering the layer, M = rows selected (M <= R)
+LayerWs carve_layer(Carver& c, const cb_dims* d, int64_t R, int64_t M) {
+  const size_t B = esize(d->dtype);
+  const int64_t qc = (int64_t)d->n_heads * d->head_dim, W = (int64_t)d->n_kv_heads * d->head_dim;
+  LayerWs w{};
+  w.a = c.take(R * d->d_model * B);
+  w.q = c.take(std::max(R, M) * qc * B);
+  w.knew = c.take(R * W * B);
+  w.vnew = c.take(R * W * B);
+  w.attn = c.take(std::max(R, M) * qc * B);
+  w.h = c.take(std::max(R, M) * d->d_model * B);
+  w.b = c.take(std::max(R, M) * d->d_model * B);
+  w.act = c.take(std::max(R, M) * d->d_ff * B);
+  w.xg = c.take(M * d->d_model * B);
+  w.ag = c.take(M * d->d_model * B);
+  w.xa = c.take(R * d->d_model * B);
+  w.xb = c.take(R * d->d_model * B);
+  w.scores = static_cast<float*>(c.take(R * 4));
+  w.ord = static_cast<int32_t*>(c.take(R * 4));
+  w.keep = static_cast<int32_t*>(c.take(R * 4));
+  w.pos = static_cast<int32_t*>(c.take(R * 4));
+  w.rows = static_cast<int32_t*>(c.take(R * 4));
+  w.hn = static_cast<float*>(c.take(d->d_model * 4));
+  w.logits = static_cast<float*>(c.take((size_t)d->vocab * 4));
+  const size_t aw = attention_ws_bytes(d->dtype, std::max(R, M), d->n_heads, d->head_dim);
+  w.attn_ws = c.take(aw);
+  return w;
+}
+
+size_t layer_ws_bytes(const cb_dims* d, int64_t R, int64_t M) {
+  Carver c(nullptr);
+  carve_layer(c, d, R, M);
+  return c.off + 256;
+}
+
+int need_ws(const cb_dims* d, int64_t R, int64_t M, void* ws, size_t ws_bytes, LayerWs* out) {
+  const size_t need = layer_ws_bytes(d, R, M);
+  if (!ws) return fail(CB_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
+  if (ws_bytes < need) return fail(CB_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, need);
+  Carver c(ws);
+  *out = carve_layer(c, d, R, M);
+  return CB_OK;
+}
+
+GemmDesc make_gemm(int M, int N, int K, const void* A, int64_t lda, const void* B, int64_t ldb) {
+  GemmDesc g;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.A = A;
+  g.lda = lda;
+  g.B = B;
+  g.ldb = ldb;
+  return g;
+}
+
+// Q/K/V GEMM over columns [col0, col0 + ncols) of Wqkv for M rows of normalised input a.
+GemmDesc qkv_desc(const cb_dims* d, const cb_layer_w* w, const void* a, int M, int col0, int ncols, void* q,
+                  void* k, void* v, const int32_t* pos, const int32_t* kv_row, const float* tab, int max_pos) {
+  const size_t B = esize(d->dtype);
+  const int qc = d->n_heads * d->head_dim, W = d->n_kv_heads * d->head_dim;
+  GemmDesc g = make_gemm(M, ncols, d->d_model, a, d->d_model,
+                         static_cast<const char*>(w->wqkv) + (size_t)col0 * d->d_model * B, d->d_model);
+  g.epi.kind = EPI_QKV;
+  g.epi.col0 = col0;
+  g.epi.q_cols = qc;
+  g.epi.kv_cols = W;
+  g.epi.hd = d->head_dim;
+  g.epi.q = q;
+  g.epi.ldq = qc;
+  g.epi.k = k;
+  g.epi.v = v;
+  g.epi.ldkv = W;
+  g.epi.pos = pos;
+  g.epi.kv_row = kv_row;
+  g.epi.rope = tab;
+  g.epi.max_pos = max_pos;
+  return g;
+}
+
+// h = x_res + attn Wo^T ; x_out = h + (silu(b Wg^T) * b Wu^T) Wd^T, b = RMSNorm(h) g
+int o_ffn(const cb_dims* d, const cb_layer_w* w, const void* attn, const void* x_res, int M, void* x_out,
+          const LayerWs& ws, cudaStream_t s) {
+  if (M == 0) return CB_OK;
+  const int qc = d->n_heads * d->head_dim;
+  GemmDesc go = make_gemm(M, d->d_model, qc, attn, qc, w->wo, qc);
+  go.epi.kind = EPI_RESID;
+  go.epi.out = ws.h;
+  go.epi.ldo = d->d_model;
+  go.epi.resid = x_res;
+  go.epi.ldr = d->d_model;
+  L_GEMM(d->dtype, go, s);
+  L_RMSNORM(d->dtype, d->dtype, ws.b, ws.h, nullptr, w->ffn_norm, M, d->d_model, d->rms_eps, s);
+  GemmDesc gu = make_gemm(M, d->d_ff, d->d_model, ws.b, d->d_model, w->w_gate_up, d->d_model);
+  gu.b_up_row = d->d_ff;
+  gu.epi.kind = EPI_SWIGLU;
+  gu.epi.out = ws.act;
+  gu.epi.ldo = d->d_ff;
+  L_GEMM(d->dtype, gu, s);
+  GemmDesc gd = make_gemm(M, d->d_model, d->d_ff, ws.act, d->d_ff, w->w_down, d->d_ff);
+  gd.epi.kind = EPI_RESID;
+  gd.epi.out = x_out;
+  gd.epi.ldo = d->d_model;
+  gd.epi.resid = ws.h;
+  gd.epi.ldr = d->d_model;
+  L_GEMM(d->dtype, gd, s);
+  return CB_OK;
+}
+
+double now_s() {
+  timespec ts;
+  clock_gettime(CLOCK_MONOTONIC, &ts);
+  return ts.tv_sec + 1e-9 * ts.tv_nsec;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* cb_status_string(int status) {
+  switch (status) {
+    case CB_OK: return "ok";
+    case CB_ERR_INVALID_ARG: return "invalid argument";
+    case CB_ERR_SHAPE: return "inconsistent shape";
+    case CB_ERR_DTYPE: return "unsupported dtype";
+    case CB_ERR_WORKSPACE: return "workspace too small";
+    case CB_ERR_NONFINITE: return "non-finite deviation score";
+    case CB_ERR_CUDA: return "CUDA error";
+    case CB_ERR_TIMEOUT: return "timed out";
+    case CB_ERR_UNSUPPORTED: return "unsupported shape";
+    case CB_ERR_DEVICE: return "device-side index or wait error";
+    default: return "unknown status";
+  }
+}
+
+const char* cb_last_error_message(void) { return g_msg; }
+
+int cb_sync(void* stream, double timeout_s) {
+  const double t0 = now_s();
+  for (;;) {
+    cudaError_t e = cudaStreamQuery(S(stream));
+    if (e == cudaSuccess) break;
+    if (e != cudaErrorNotReady) return fail(CB_ERR_CUDA, "stream error: %s", cudaGetErrorString(e));
+    if (timeout_s > 0 && now_s() - t0 > timeout_s)
+      return fail(CB_ERR_TIMEOUT, "stream not idle after %.3f s", timeout_s);
+    timespec ts{0, 50000};
+    nanosleep(&ts, nullptr);
+  }
+  const uint32_t bits = take_error_mem() | take_error_gemm() | take_error_gemm_tc() | take_error_attn();
+  if (bits & ERRBIT_NONFINITE) return fail(CB_ERR_NONFINITE, "a deviation score was NaN/Inf");
+  if (bits & ERRBIT_INDEX) return fail(CB_ERR_DEVICE, "a kernel met an out-of-range index");
+  if (bits & ERRBIT_TIMEOUT) return fail(CB_ERR_DEVICE, "a kernel's bounded wait expired");
+  return CB_OK;
+}
+
+int cb_workspace_bytes(const cb_dims* dims, int64_t n_tok, int64_t m_max, size_t* out_host) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!out_host || n_tok < 1 || m_max < 0) return fail(CB_ERR_INVALID_ARG, "workspace query arguments");
+  *out_host = layer_ws_bytes(dims, n_tok, std::max<int64_t>(m_max, n_tok));
+  return CB_OK;
+}
+
+int64_t cb_hkvd_budget(int64_t n_cached, double ratio, int64_t n_cand) {
+  if (n_cached < 0 || n_cand < 0 || !(ratio >= 0.0) || ratio > 1.0) return -1;
+  if (ratio == 0.0) return 0;
+  int64_t k = (int64_t)floor((double)n_cached * ratio);
+  if (k < 1) k = 1;
+  if (k > n_cand) k = n_cand;
+  return k;
+}
+
+double cb_gradual_ratio(double r, int32_t layer, int32_t check_layer, double r1_factor) {
+  if (layer < check_layer) return -1.0;
+  const double r1 = std::min(1.0, r1_factor * r);
+  return r + (r1 - r) * ldexp(1.0, -(layer - check_layer));
+}
+
+double cb_load_controller_ratio(double r_min, double t_load_s, double t_prefill_s) {
+  if (!(t_prefill_s > 0.0)) return r_min;
+  return std::max(r_min, t_load_s / t_prefill_s);
+}
+
+int cb_rope_table(float* cos_sin, int32_t max_pos, int32_t head_dim, double base, void* stream) {
+  if (!cos_sin || max_pos < 1 || head_dim < 2 || head_dim % 2 || !(base > 1.0))
+    return fail(CB_ERR_INVALID_ARG, "rope table arguments");
+  L_ROPE_TABLE(cos_sin, max_pos, head_dim, base, S(stream));
+  return CB_OK;
+}
+
+int cb_rope_shift(void* k_dst, void* v_dst, const void* k_src, const void* v_src, const int32_t* src_row,
+                  const int32_t* delta, int64_t n_rows, const cb_dims* dims, const float* cos_sin,
+                  int32_t max_pos, void* stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (n_rows < 0) return fail(CB_ERR_SHAPE, "n_rows < 0");
+  if (n_rows == 0) return CB_OK;
+  if (!k_dst || !k_src || !delta || !cos_sin || max_pos < 1)
+    return fail(CB_ERR_INVALID_ARG, "rope_shift pointer is NULL");
+  if ((v_dst == nullptr) != (v_src == nullptr)) return fail(CB_ERR_INVALID_ARG, "v_dst/v_src must both be set or NULL");
+  if (k_dst == k_src && src_row) return fail(CB_ERR_INVALID_ARG, "in-place shift needs src_row == NULL");
+  const int W = dims->n_kv_heads * dims->head_dim;
+  L_ROPE_SHIFT(dims->dtype, k_dst, v_dst, k_src, v_src, src_row, delta, n_rows, W, dims->head_dim, cos_sin, max_pos, S(stream));
+  return CB_OK;
+}
+
+int cb_kv_deviation_topk(const void* k_new, const void* v_new, const void* k_ref, const void* v_ref,
+                         const int32_t* new_row, const int32_t* ref_row, int32_t n_cand, int32_t k,
+                         int32_t dev_mode, const cb_dims* dims, float* scores, int32_t* sel, void* ws,
+                         size_t ws_bytes, void* stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (n_cand < 0 || k < 0 || k > n_cand) return fail(CB_ERR_SHAPE, "need 0 <= k <= n_cand");
+  if (dev_mode != CB_DEV_KV && dev_mode != CB_DEV_K) return fail(CB_ERR_INVALID_ARG, "dev_mode");
+  if (n_cand == 0) return CB_OK;
+  if (!k_new || !k_ref || (dev_mode == CB_DEV_KV && (!v_new || !v_ref)) || (k > 0 && !sel))
+    return fail(CB_ERR_INVALID_ARG, "deviation pointer is NULL");
+  const size_t need = 256 + (size_t)n_cand * 8 + 512;
+  if (!ws || ws_bytes < need) return fail(CB_ERR_WORKSPACE, "workspace %zu < %zu", ws_bytes, need);
+  Carver c(ws);
+  float* sc = scores ? scores : static_cast<float*>(c.take((size_t)n_cand * 4));
+  int32_t* ord = static_cast<int32_t*>(c.take((size_t)n_cand * 4));
+  const int W = dims->n_kv_heads * dims->head_dim;
+  L_DEV(dims->dtype, k_new, v_new, k_ref, v_ref, new_row, ref_row, n_cand, W, dev_mode == CB_DEV_KV, sc, S(stream));
+  if (k > 0) {
+    L_TOPK(sc, n_cand, k, ord, S(stream));
+    L_MAP(ord, k, ref_row, sel, S(stream));
+  }
+  return CB_OK;
+}
+
+int cb_topk_from_scores(const float* scores, const int32_t* cand, int32_t n_cand, int32_t k, int32_t* sel,
+                        void* ws, size_t ws_bytes, void* stream) {
+  if (n_cand < 0 || k < 0 || k > n_cand) return fail(CB_ERR_SHAPE, "need 0 <= k <= n_cand");
+  if (n_cand == 0) return CB_OK;
+  if (!scores || (k > 0 && !sel)) return fail(CB_ERR_INVALID_ARG, "topk pointer is NULL");
+  const size_t need = 256 + (size_t)n_cand * 4;
+  if (!ws || ws_bytes < need) return fail(CB_ERR_WORKSPACE, "workspace %zu < %zu", ws_bytes, need);
+  Carver c(ws);
+  int32_t* ord = static_cast<int32_t*>(c.take((size_t)n_cand * 4));
+  L_TOPK(scores, n_cand, k, ord, S(stream));
+  if (k > 0) L_MAP(ord, k, cand, sel, S(stream));
+  return CB_OK;
+}
+
+int cb_gather_rows(void* dst, const void* src, const int32_t* idx, int64_t n, int64_t row_bytes, void* stream) {
+  if (n < 0 || row_bytes < 0 || row_bytes % 4) return fail(CB_ERR_SHAPE, "n/row_bytes");
+  if (n == 0) return CB_OK;
+  if (!dst || !src) return fail(CB_ERR_INVALID_ARG, "gather pointer is NULL");
+  L_COPY(dst, nullptr, src, idx, n, row_bytes, -1, -1, S(stream));
+  return CB_OK;
+}
+
+int cb_scatter_kv(void* k_cache, void* v_cache, const void* k_rows, const void* v_rows, const int32_t* dst_idx,
+                  const int32_t* src_idx, int64_t n, const cb_dims* dims, void* stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (n < 0) return fail(CB_ERR_SHAPE, "n < 0");
+  if (n == 0) return CB_OK;
+  if (!k_cache || !k_rows || !dst_idx || ((v_cache == nullptr) != (v_rows == nullptr)))
+    return fail(CB_ERR_INVALID_ARG, "scatter pointer is NULL");
+  const int64_t rb = (int64_t)dims->n_kv_heads * dims->head_dim * esize(dims->dtype);
+  L_COPY(k_cache, dst_idx, k_rows, src_idx, n, rb, -1, -1, S(stream));
+  if (v_cache) L_COPY(v_cache, dst_idx, v_rows, src_idx, n, rb, -1, -1, S(stream));
+  return CB_OK;
+}
+
+int cb_selective_qkv(const void* x, const int32_t* rows, const int32_t* pos, int32_t M, const cb_dims* dims,
+                     const cb_layer_w* w, const float* cos_sin, int32_t max_pos, void* q, void* k, void* v,
+                     void* ws, size_t ws_bytes, void* stream) {
+  int st = check_dims(dims);
+  if (st || (st = check_w(w))) return st;
+  if (M < 0) return fail(CB_ERR_SHAPE, "M < 0");
+  if (M == 0) return CB_OK;
+  if (!x || !pos || !cos_sin || (!q && !k) || ((k == nullptr) != (v == nullptr)))
+    return fail(CB_ERR_INVALID_ARG, "selective_qkv pointer is NULL");
+  LayerWs L;
+  if ((st = need_ws(dims, M, M, ws, ws_bytes, &L))) return st;
+  const int qc = dims->n_heads * dims->head_dim, W = dims->n_kv_heads * dims->head_dim;
+  L_RMSNORM(dims->dtype, dims->dtype, L.a, x, rows, w->attn_norm, M, dims->d_model, dims->rms_eps, S(stream));
+  const int col0 = q ? 0 : qc;
+  const int ncols = (q ? qc : 0) + (k ? 2 * W : 0);
+  L_GEMM(dims->dtype, qkv_desc(dims, w, L.a, M, col0, ncols, q, k, v, pos, nullptr, cos_sin, max_pos), S(stream));
+  return CB_OK;
+}
+
+int cb_partial_attention(const void* q, const int32_t* q_pos, int32_t M, const void* k_cache, const void* v_cache,
+                         int64_t n_kv, const cb_dims* dims, void* out, void* ws, size_t ws_bytes, void* stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (M < 0 || n_kv < 1) return fail(CB_ERR_SHAPE, "M/n_kv");
+  if (M == 0) return CB_OK;
+  if (!q || !q_pos || !k_cache || !v_cache || !out) return fail(CB_ERR_INVALID_ARG, "attention pointer is NULL");
+  const size_t need = attention_ws_bytes(dims->dtype, M, dims->n_heads, dims->head_dim);
+  if (need && (!ws || ws_bytes < need)) return fail(CB_ERR_WORKSPACE, "workspace %zu < %zu", ws_bytes, need);
+  L_ATTN(dims->dtype, q, q_pos, M, k_cache, v_cache, n_kv, dims->n_heads, dims->n_kv_heads, dims->head_dim, out, ws, ws_bytes, S(stream));
+  return CB_OK;
+}
+
+int cb_o_proj_ffn(const void* attn, const void* x_res, int32_t M, const cb_dims* dims, const cb_layer_w* w,
+                  void* x_out, void* ws, size_t ws_bytes, void* stream) {
+  int st = check_dims(dims);
+  if (st || (st = check_w(w))) return st;
+  if (M < 0) return fail(CB_ERR_SHAPE, "M < 0");
+  if (M == 0) return CB_OK;
+  if (!attn || !x_res || !x_out) return fail(CB_ERR_INVALID_ARG, "o_proj_ffn pointer is NULL");
+  LayerWs L;
+  if ((st = need_ws(dims, M, M, ws, ws_bytes, &L))) return st;
+  return o_ffn(dims, w, attn, x_res, M, x_out, L, S(stream));
+}
+
+int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const void* x_in, const int32_t* s_in,
+                   int32_t m_in, int64_t n_tok, int64_t n_cached, void* k_cache, void* v_cache,
+                   const float* cos_sin, int32_t max_pos, int32_t k_budget, int32_t dev_mode,
+                   const int32_t* sel_override, void* x_out, int32_t* s_out, int32_t* m_out_host,
+                   float* scores_out, void* ws, size_t ws_bytes, void* stream) {
+  int st = check_dims(dims);
+  if (st || (st = check_w(w))) return st;
+  if (!x_in || !k_cache || !v_cache || !cos_sin || !x_out || !s_out || !m_out_host)
+    return fail(CB_ERR_INVALID_ARG, "blend_layer pointer is NULL");
+  if (x_out == x_in) return fail(CB_ERR_INVALID_ARG, "x_out must not alias x_in");
+  if (n_tok < 1 || n_tok > INT32_MAX || n_cached < 0 || n_cached > n_tok)
+    return fail(CB_ERR_SHAPE, "need 0 <= n_cached <= n_tok, n_tok >= 1");
+  if (n_tok > max_pos) return fail(CB_ERR_SHAPE, "rope table (%d) shorter than n_tok (%lld)", max_pos, (long long)n_tok);
+  if (dev_mode != CB_DEV_KV && dev_mode != CB_DEV_K) return fail(CB_ERR_INVALID_ARG, "dev_mode");
+  const int N = (int)n_tok;
+  const int f0 = (int)std::min<int64_t>(n_cached, n_tok - 1);   // first forced row
+  const int n_forced = N - f0;
+  const int qc = dims->n_heads * dims->head_dim, W = dims->n_kv_heads * dims->head_dim;
+  const size_t B = esize(dims->dtype);
+  const bool use_v = dev_mode == CB_DEV_KV;
+  cudaStream_t s = S(stream);
+  LayerWs L;
+
+  switch (mode) {
+    case CB_LAYER_PRECHECK: {
+      if (m_in != N) return fail(CB_ERR_SHAPE, "PRECHECK needs m_in == n_tok");
+      if ((st = need_ws(dims, N, N, ws, ws_bytes, &L))) return st;
+      *m_out_host = N;
+      L_IOTA(s_out, N, 0, s);
+      L_RMSNORM(dims->dtype, dims->dtype, L.a, x_in, nullptr, w->attn_norm, N, dims->d_model, dims->rms_eps, s);
+      L_GEMM(dims->dtype, qkv_desc(dims, w, L.a, N, 0, qc, L.q, nullptr, nullptr, s_out, nullptr, cos_sin, max_pos), s);
+      if (N > n_cached) {
+        const int nu = N - (int)n_cached;
+        const void* a_u = static_cast<const char*>(L.a) + (size_t)n_cached * dims->d_model * B;
+        L_GEMM(dims->dtype, qkv_desc(dims, w, a_u, nu, qc, 2 * W, nullptr, k_cache, v_cache, s_out + n_cached, s_out + n_cached, cos_sin, max_pos), s);
+      }
+      L_ATTN(dims->dtype, L.q, s_out, N, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
+      return o_ffn(dims, w, L.attn, x_in, N, x_out, L, s);
+    }
+    case CB_LAYER_CHECK:
+    case CB_LAYER_GRADUAL: {
+      const bool check = mode == CB_LAYER_CHECK;
+      if (check && m_in != N) return fail(CB_ERR_SHAPE, "CHECK needs m_in == n_tok");
+      if (!check && (m_in < n_forced || m_in > N)) return fail(CB_ERR_SHAPE, "GRADUAL needs n_forced <= m_in <= n_tok");
+      if (!check && !s_in && m_in != N) return fail(CB_ERR_INVALID_ARG, "GRADUAL needs s_in");
+      const int n_cand = check ? f0 : m_in - n_forced;
+      if (k_budget < 0 || k_budget > n_cand)
+        return fail(CB_ERR_SHAPE, "k_budget %d outside [0, %d]", k_budget, n_cand);
+      const int M = k_budget + n_forced;
+      if ((st = need_ws(dims, m_in, M, ws, ws_bytes, &L))) return st;
+      *m_out_host = M;
+      const int32_t* rows_in = s_in;
+      if (check || !s_in) {
+        L_IOTA(L.rows, m_in, 0, s);
+        rows_in = L.rows;
+      }
+      float* sc = scores_out ? scores_out : L.scores;
+      L_RMSNORM(dims->dtype, dims->dtype, L.a, x_in, nullptr, w->attn_norm, m_in, dims->d_model, dims->rms_eps, s);
+      L_GEMM(dims->dtype, qkv_desc(dims, w, L.a, m_in, qc, 2 * W, nullptr, L.knew, L.vnew, rows_in, nullptr, cos_sin, max_pos), s);
+      L_DEV(dims->dtype, L.knew, L.vnew, k_cache, v_cache, nullptr, rows_in, n_cand, W, use_v, sc, s);
+      if (k_budget > 0) {
+        if (sel_override)
+          L_R2P(sel_override, k_budget, check ? nullptr : rows_in, n_cand, L.ord, s);
+        else
+          L_TOPK(sc, n_cand, k_budget, L.ord, s);
+      }
+      L_BUILD_SEL(L.ord, k_budget, rows_in, f0, m_in - n_forced, n_forced, s_out, L.keep, s);
+      // Step 3, KV expansion: the recomputed K/V of S replace the cached rows
+      L_COPY(k_cache, s_out, L.knew, L.keep, M, (int64_t)W * B, N, m_in, s);
+      L_COPY(v_cache, s_out, L.vnew, L.keep, M, (int64_t)W * B, N, m_in, s);
+      L_COPY(L.ag, nullptr, L.a, L.keep, M, (int64_t)dims->d_model * B, M, m_in, s);
+      L_GEMM(dims->dtype, qkv_desc(dims, w, L.ag, M, 0, qc, L.q, nullptr, nullptr, s_out, nullptr, cos_sin, max_pos), s);
+      L_ATTN(dims->dtype, L.q, s_out, M, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
+      L_COPY(L.xg, nullptr, x_in, L.keep, M, (int64_t)dims->d_model * B, M, m_in, s);
+      return o_ffn(dims, w, L.attn, L.xg, M, x_out, L, s);
+    }
+    case CB_LAYER_STEADY: {
+      if (m_in < 1 || m_in > N) return fail(CB_ERR_SHAPE, "STEADY needs 1 <= m_in <= n_tok");
+      if (!s_in && m_in != N) return fail(CB_ERR_INVALID_ARG, "STEADY needs s_in");
+      if ((st = need_ws(dims, m_in, m_in, ws, ws_bytes, &L))) return st;
+      *m_out_host = m_in;
+      if (s_in)
+        CB_CUDA(cudaMemcpyAsync(s_out, s_in, (size_t)m_in * 4, cudaMemcpyDeviceToDevice, s));
+      else
+        L_IOTA(s_out, m_in, 0, s);
+      L_RMSNORM(dims->dtype, dims->dtype, L.a, x_in, nullptr, w->attn_norm, m_in, dims->d_model, dims->rms_eps, s);
+      L_GEMM(dims->dtype, qkv_desc(dims, w, L.a, m_in, 0, qc + 2 * W, L.q, k_cache, v_cache, s_out, s_out, cos_sin, max_pos), s);
+      L_ATTN(dims->dtype, L.q, s_out, m_in, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
+      return o_ffn(dims, w, L.attn, x_in, m_in, x_out, L, s);
+    }
+    default:
+      return fail(CB_ERR_INVALID_ARG, "mode %d", mode);
+  }
+}
+
+int cb_full_prefill(const cb_dims* dims, int32_t n_layers, const cb_layer_w* layers_host, const void* embed,
+                    const int32_t* tokens, int32_t n, int32_t pos0, void* const* k_out_host,
+                    void* const* v_out_host, void* h_last, void* x_all, const float* cos_sin, int32_t max_pos,
+                    void* ws, size_t ws_bytes, void* stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (n_layers < 1 || !layers_host || !embed || !tokens || !k_out_host || !v_out_host || !cos_sin)
+    return fail(CB_ERR_INVALID_ARG, "full_prefill argument is NULL");
+  for (int l = 0; l < n_layers; ++l) {
+    if ((st = check_w(&layers_host[l]))) return st;
+    if (!k_out_host[l] || !v_out_host[l]) return fail(CB_ERR_INVALID_ARG, "k_out/v_out[%d] is NULL", l);
+  }
+  if (n < 1 || pos0 < 0) return fail(CB_ERR_SHAPE, "n >= 1, pos0 >= 0");
+  if ((int64_t)pos0 + n > max_pos) return fail(CB_ERR_SHAPE, "rope table shorter than pos0 + n");
+  LayerWs L;
+  if ((st = need_ws(dims, n, n, ws, ws_bytes, &L))) return st;
+  cudaStream_t s = S(stream);
+  const size_t B = esize(dims->dtype);
+  const int qc = dims->n_heads * dims->head_dim, W = dims->n_kv_heads * dims->head_dim;
+  const int64_t row_b = (int64_t)dims->d_model * B;
+  L_COPY(L.xa, nullptr, embed, tokens, n, row_b, n, dims->vocab, s);
+  L_IOTA(L.pos, n, pos0, s);
+  L_IOTA(L.rows, n, 0, s);
+  void* x = L.xa;
+  void* y = L.xb;
+  for (int l = 0; l < n_layers; ++l) {
+    const cb_layer_w* w = &layers_host[l];
+    L_RMSNORM(dims->dtype, dims->dtype, L.a, x, nullptr, w->attn_norm, n, dims->d_model, dims->rms_eps, s);
+    L_GEMM(dims->dtype, qkv_desc(dims, w, L.a, n, 0, qc + 2 * W, L.q, k_out_host[l], v_out_host[l], L.pos, nullptr, cos_sin, max_pos), s);
+    L_ATTN(dims->dtype, L.q, L.rows, n, k_out_host[l], v_out_host[l], n, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
+    if ((st = o_ffn(dims, w, L.attn, x, n, y, L, s))) return st;
+    std::swap(x, y);
+  }
+  if (h_last)
+    CB_CUDA(cudaMemcpyAsync(h_last, static_cast<char*>(x) + (size_t)(n - 1) * row_b, row_b, cudaMemcpyDeviceToDevice, s));
+  if (x_all) CB_CUDA(cudaMemcpyAsync(x_all, x, (size_t)n * row_b, cudaMemcpyDeviceToDevice, s));
+  return CB_OK;
+}
+
+int cb_lmhead_argmax(const void* h, const void* final_norm, const void* w_lm, const cb_dims* dims, float* logits,
+                     int32_t* token, void* ws, size_t ws_bytes, void* stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!h || !final_norm || !w_lm || !token) return fail(CB_ERR_INVALID_ARG, "lmhead pointer is NULL");
+  const size_t need = 256 + (size_t)dims->d_model * 4 + 256 + (size_t)dims->vocab * 4 + 256;
+  if (!ws || ws_bytes < need) return fail(CB_ERR_WORKSPACE, "workspace %zu < %zu", ws_bytes, need);
+  Carver c(ws);
+  float* hn = static_cast<float*>(c.take((size_t)dims->d_model * 4));
+  float* lg = logits ? logits : static_cast<float*>(c.take((size_t)dims->vocab * 4));
+  cudaStream_t s = S(stream);
+  L_RMSNORM(dims->dtype, CB_F32, hn, h, nullptr, final_norm, 1, dims->d_model, dims->rms_eps, s);
+  L_LMGEMV(dims->dtype, lg, hn, w_lm, dims->vocab, dims->d_model, s);
+  L_ARGMAX(lg, dims->vocab, token, s);
+  return CB_OK;
+}
+
+// y = x W^T (plain linear layer) on the same GEMM kernels as the layer path.
+int cb_linear(const void* x, const void* w, void* y, int32_t M, int32_t N, int32_t K, int32_t dtype, void* stream) {
+  if (dtype != CB_F32 && dtype != CB_BF16) return fail(CB_ERR_DTYPE, "dtype %d", dtype);
+  if (M < 0 || N < 1 || K < 1) return fail(CB_ERR_SHAPE, "M/N/K");
+  if (M == 0) return CB_OK;
+  if (!x || !w || !y) return fail(CB_ERR_INVALID_ARG, "linear pointer is NULL");
+  if (dtype == CB_BF16 && (N % 16 || K % 8)) return fail(CB_ERR_UNSUPPORTED, "bf16 needs N %% 16 == 0, K %% 8 == 0");
+  if (dtype == CB_F32 && N % 4) return fail(CB_ERR_UNSUPPORTED, "fp32 needs N %% 4 == 0");
+  GemmDesc g = make_gemm(M, N, K, x, K, w, K);
+  g.epi.kind = EPI_STORE;
+  g.epi.out = y;
+  g.epi.ldo = N;
+  L_GEMM(dtype, g, S(stream));
+  return CB_OK;
+}
+
+int64_t cb_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int cb_profile_begin(int32_t max_records) {
+  if (max_records < 1) return fail(CB_ERR_INVALID_ARG, "max_records < 1");
+  ProfState& P = g_prof;
+  while ((int)P.ev.size() < 2 * max_records) {
+    cudaEvent_t e;
+    CB_CUDA(cudaEventCreate(&e));
+    P.ev.push_back(e);
+  }
+  P.rec.clear();
+  P.rec.reserve(max_records);
+  P.cap = max_records;
+  P.on = true;
+  return CB_OK;
+}
+
+int cb_profile_end(cb_prof_record* out_host, int32_t max_records, int32_t* n_out_host) {
+  ProfState& P = g_prof;
+  P.on = false;
+  if (!n_out_host) return fail(CB_ERR_INVALID_ARG, "n_out_host is NULL");
+  const int n = std::min<int>((int)P.rec.size(), std::max(0, max_records));
+  for (int i = 0; i < (int)P.rec.size(); ++i) {
+    CB_CUDA(cudaEventSynchronize(P.ev[2 * i + 1]));
+    float ms = 0.f;
+    CB_CUDA(cudaEventElapsedTime(&ms, P.ev[2 * i], P.ev[2 * i + 1]));
+    P.rec[i].ms = ms;
+  }
+  if (out_host && n > 0) memcpy(out_host, P.rec.data(), sizeof(cb_prof_record) * n);
+  *n_out_host = n;
+  P.rec.clear();
+  return CB_OK;
+}
+
+}  // extern "C"

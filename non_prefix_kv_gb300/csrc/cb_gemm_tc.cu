@@ -1,0 +1,226 @@
+// bf16 GEMM on the 5th-generation tensor cores: TMA-fed shared-memory pipeline, tcgen05.mma
+// into a TMEM accumulator, fused epilogues (RoPE + KV scatter, residual add, SwiGLU).
+//
+//   acc[m][n] = sum_k A[m][k] * B[n][k]      A: activations [M, K], B: weight rows [N, K]
+//
+// One 128 x 256 output tile per CTA (SwiGLU: 128 gate + 128 up columns -> 128 outputs),
+// K consumed in 64-element (128-byte) slabs through a 4-stage ring.  Warp roles:
+//   warp 0 lane 0 : TMA producer     warp 1 : TMEM allocator, lane 0 issues the MMAs
+//   warps 2..5    : epilogue, each reading the 32 TMEM lanes (rows) its warp may access.
+#include <cuda.h>
+
+#include "cb_common.cuh"
+#include "cb_epilogue.cuh"
+#include "cb_internal.h"
+#include "cb_tc.cuh"
+
+namespace cb {
+
+static __device__ uint32_t g_err_tc;
+
+uint32_t take_error_gemm_tc() {
+  uint32_t v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_tc, sizeof(v)) != cudaSuccess) return ERRBIT_INDEX;
+  cudaMemcpyToSymbol(g_err_tc, &z, sizeof(z));
+  return v;
+}
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;   // 16 KB
+constexpr int B_BYTES = BN * BK * 2;   // 32 KB
+constexpr int SMEM_BYTES = STAGES * (A_BYTES + B_BYTES) + 1024 /*align slack*/ + 256 /*barriers*/;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 256;
+
+__global__ void __launch_bounds__(THREADS, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const GemmDesc g, int swiglu) {
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte aligned base for the 128-byte-swizzled tiles
+  const uint32_t raw_addr = tc::smem_u32(smem_raw);
+  uint8_t* base = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
+  uint8_t* smA = base;
+  uint8_t* smB = base + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + STAGES * (A_BYTES + B_BYTES));
+  uint64_t* full = bars;                 // [STAGES] TMA -> MMA
+  uint64_t* empty = bars + STAGES;       // [STAGES] MMA -> TMA
+  uint64_t* acc_full = bars + 2 * STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * BM;
+  const int n0 = blockIdx.x * (swiglu ? BN / 2 : BN);   // output column origin
+  const int KB = (g.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    tc::mbar_init(acc_full, 1);
+    tc::fence_mbar_init();
+    tc::tma_prefetch_desc(&tmA);
+    tc::tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- producer
+    for (int kb = 0; kb < KB; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t ph = (kb / STAGES) & 1;
+      if (!tc::mbar_wait(&empty[s], ph ^ 1)) {
+        atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
+        break;
+      }
+      tc::mbar_expect_tx(&full[s], A_BYTES + B_BYTES);
+      tc::tma_load_2d(smA + s * A_BYTES, &tmA, &full[s], kb * BK, m0);
+      if (swiglu) {
+        tc::tma_load_2d(smB + s * B_BYTES, &tmB, &full[s], kb * BK, n0);
+        tc::tma_load_2d(smB + s * B_BYTES + B_BYTES / 2, &tmB, &full[s], kb * BK,
+                        (int)g.b_up_row + n0);
+      } else {
+        tc::tma_load_2d(smB + s * B_BYTES, &tmB, &full[s], kb * BK, n0);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer
+    constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
+    bool ok = true;
+    for (int kb = 0; kb < KB; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t ph = (kb / STAGES) & 1;
+      if (!tc::mbar_wait(&full[s], ph)) {
+        atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
+        ok = false;
+        break;
+      }
+      tc::tc_fence_after();
+      const uint64_t a_desc = tc::desc_sw128(tc::smem_u32(smA + s * A_BYTES));
+      const uint64_t b_desc = tc::desc_sw128(tc::smem_u32(smB + s * B_BYTES));
+#pragma unroll
+      for (int k = 0; k < BK / 16; ++k) {
+        // advance 16 bf16 = 32 bytes along K inside the swizzled 128-byte row
+        tc::mma_bf16(tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, (kb | k) != 0);
+      }
+      tc::mma_commit(&empty[s]);
+    }
+    if (ok) tc::mma_commit(acc_full);
+  } else if (warp >= 2) {
+    // ---------------- epilogue
+    const int lane_base = (warp & 3) * 32;
+    const int m = m0 + lane_base + lane;
+    // every lane waits, then the warp re-converges before the .sync.aligned TMEM loads
+    const bool ready = __all_sync(0xffffffffu, tc::mbar_wait(acc_full, 0));
+    if (!ready) {
+      if (lane == 0) atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
+    } else {
+      tc::tc_fence_after();
+      const uint32_t trow = tmem + (static_cast<uint32_t>(lane_base) << 16);
+      if (!swiglu) {
+        for (int c = 0; c < BN / 16; ++c) {
+          float v[16];
+          tc::tmem_ld16(trow + c * 16, v);
+          const int n = n0 + c * 16;
+          if (m < g.M && n < g.N) {
+            if (!epi_apply<bf16, 16>(g.epi, m, n, v)) atomicOr(&g_err_tc, ERRBIT_INDEX);
+          }
+        }
+      } else {
+        for (int c = 0; c < BN / 32; ++c) {
+          float gt[16], up[16];
+          tc::tmem_ld16(trow + c * 16, gt);
+          tc::tmem_ld16(trow + BN / 2 + c * 16, up);
+          const int j = n0 + c * 16;
+          if (m < g.M && j < g.N) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) gt[i] = silu_f(gt[i]) * up[i];
+            st_vec<bf16, 16>(static_cast<bf16*>(g.epi.out) + (int64_t)m * g.epi.ldo + j, gt);
+          }
+        }
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ---- host: tensor maps through the driver entry point (no libcuda link dependency)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// rows x cols (cols innermost, contiguous), row stride ld elements; box = box_rows x 64
+bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
+              int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// Host preconditions (checked by the caller's validation, re-checked here): K % 8 == 0,
+// lda/ldb % 8 == 0, A and B 16-byte aligned, N % 16 == 0.
+cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t s) {
+  if (g.M == 0 || g.N == 0) return cudaSuccess;
+  if (g.K % 8 || g.lda % 8 || g.ldb % 8 || g.N % 16 || ((uintptr_t)g.A & 15) || ((uintptr_t)g.B & 15))
+    return cudaErrorInvalidValue;
+  const bool swiglu = g.epi.kind == EPI_SWIGLU;
+  CUtensorMap tmA, tmB;
+  if (!make_map(&tmA, g.A, g.M, g.K, g.lda, BM)) return cudaErrorInvalidValue;
+  const int64_t b_rows = swiglu ? g.b_up_row + g.N : g.N;
+  if (!make_map(&tmB, g.B, b_rows, g.K, g.ldb, swiglu ? BN / 2 : BN)) return cudaErrorInvalidValue;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  const int out_cols = swiglu ? BN / 2 : BN;
+  dim3 grid((g.N + out_cols - 1) / out_cols, (g.M + BM - 1) / BM);
+  k_gemm_tc<<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, g, swiglu ? 1 : 0);
+  return cudaGetLastError();
+}
+
+}  // namespace cb

@@ -1,0 +1,99 @@
+// Internal launcher interface between the C ABI layer and the kernel translation units.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace cb {
+
+enum DType { DT_F32 = 0, DT_BF16 = 1 };
+
+// bits of the sticky device error words
+enum : uint32_t {
+  ERRBIT_NONFINITE = 1u,   // a deviation score was NaN/Inf (or negative)
+  ERRBIT_INDEX = 2u,       // an index or position fell outside its buffer
+  ERRBIT_TIMEOUT = 4u,     // a bounded device wait gave up
+};
+
+// GEMM epilogues.  The GEMM computes acc[m][n] = sum_k A[m][k] * B[n][k] (B = weight rows,
+// output-major), then hands groups of consecutive columns of one row to the epilogue.
+enum EpiKind {
+  EPI_STORE = 0,   // out[m][n] = acc
+  EPI_RESID = 1,   // out[m][n] = acc + resid[m][n]
+  EPI_QKV = 2,     // column n + col0 of the fused Wqkv: q | k | v segments, RoPE on q, k
+  EPI_SWIGLU = 3,  // out[m][j] = silu(gate_j) * up_j  (tensor-core path only)
+};
+
+struct EpiParams {
+  int kind = EPI_STORE;
+  void* out = nullptr;
+  int64_t ldo = 0;
+  const void* resid = nullptr;
+  int64_t ldr = 0;
+  // EPI_QKV
+  int col0 = 0;        // first Wqkv row covered by this launch
+  int q_cols = 0;      // H * hd
+  int kv_cols = 0;     // Hkv * hd
+  int hd = 0;
+  void* q = nullptr;   // [M, q_cols]
+  int64_t ldq = 0;
+  void* k = nullptr;   // rows kv_row[m] (or m) of [*, kv_cols]
+  void* v = nullptr;
+  int64_t ldkv = 0;
+  const int32_t* pos = nullptr;     // [M] RoPE position per row
+  const int32_t* kv_row = nullptr;  // [M] destination row of k/v, or null
+  const float* rope = nullptr;      // cos/sin table [max_pos][hd/2][2]
+  int max_pos = 0;
+};
+
+struct GemmDesc {
+  int M = 0, N = 0, K = 0;
+  const void* A = nullptr;  // [M, K], row stride lda elements
+  int64_t lda = 0;
+  const void* B = nullptr;  // [N, K] rows, stride ldb elements
+  int64_t ldb = 0;
+  int64_t b_up_row = 0;     // EPI_SWIGLU: row of B holding the 'up' partner of row 0
+  EpiParams epi;
+};
+
+// ---- cb_mem.cu ------------------------------------------------------------------------
+cudaError_t launch_rope_table(float* tab, int max_pos, int hd, double base, cudaStream_t s);
+cudaError_t launch_rope_shift(int dt, void* kd, void* vd, const void* ks, const void* vs,
+                              const int32_t* src_row, const int32_t* delta, int64_t n_rows,
+                              int W, int hd, const float* tab, int max_pos, cudaStream_t s);
+cudaError_t launch_copy_rows(void* dst, const int32_t* dst_idx, const void* src,
+                             const int32_t* src_idx, int64_t n, int64_t row_bytes,
+                             int64_t dst_bound, int64_t src_bound, cudaStream_t s);
+cudaError_t launch_rmsnorm(int dt_in, int dt_out, void* out, const void* x,
+                           const int32_t* rows, const void* g, int64_t n, int d, float eps,
+                           cudaStream_t s);
+cudaError_t launch_deviation(int dt, const void* kn, const void* vn, const void* kr,
+                             const void* vr, const int32_t* new_row, const int32_t* ref_row,
+                             int n_cand, int W, int use_v, float* scores, cudaStream_t s);
+cudaError_t launch_topk(const float* scores, int n, int k, int32_t* out_ord, cudaStream_t s);
+cudaError_t launch_map_rows(const int32_t* ord, int k, const int32_t* map, int32_t* out,
+                            cudaStream_t s);
+cudaError_t launch_build_sel(const int32_t* ord, int k, const int32_t* cand_row,
+                             int32_t forced_row0, int32_t forced_pos0, int n_forced,
+                             int32_t* s_out, int32_t* keep_out, cudaStream_t s);
+cudaError_t launch_rows_to_positions(const int32_t* rows, int k, const int32_t* s_in, int m_in,
+                                     int32_t* pos_out, cudaStream_t s);
+cudaError_t launch_iota(int32_t* out, int n, int32_t start, cudaStream_t s);
+cudaError_t launch_swiglu(int dt, void* out, const void* gu, int64_t M, int F, cudaStream_t s);
+cudaError_t launch_lm_gemv(int dt, float* logits, const float* hn, const void* w, int V, int d,
+                           cudaStream_t s);
+cudaError_t launch_argmax(const float* logits, int V, int32_t* token, cudaStream_t s);
+uint32_t take_error_mem();
+
+// ---- cb_gemm.cu -----------------------------------------------------------------------
+cudaError_t launch_gemm(int dt, const GemmDesc& g, cudaStream_t s);
+uint32_t take_error_gemm();
+
+// ---- cb_attn.cu -----------------------------------------------------------------------
+size_t attention_ws_bytes(int dt, int64_t M, int H, int hd);
+cudaError_t launch_attention(int dt, const void* q, const int32_t* q_pos, int M,
+                             const void* kc, const void* vc, int64_t n_kv, int H, int Hkv,
+                             int hd, void* out, void* ws, size_t ws_bytes, cudaStream_t s);
+uint32_t take_error_attn();
+
+}  // namespace cb

@@ -1,0 +1,573 @@
+// Bandwidth- and latency-bound kernels of the blend path: RoPE table and re-rotation,
+// row gather/scatter, RMSNorm, KV deviation, exact top-k, selection bookkeeping,
+// lm_head GEMV + argmax.
+//
+// Sources: CacheBlend explainer (0h-n0.github.io/posts/paper-2312-03052) — §KV deviation,
+// §HKVD selection, §Selective recomputation Steps 1 and 3, §RoPE; Prompt Cache explainer
+// (0h-n0.github.io/posts/paper-2402-01008) — §RoPE position adjustment.
+#include "cb_common.cuh"
+#include "cb_internal.h"
+
+namespace cb {
+
+static __device__ uint32_t g_err_mem;
+
+static int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (n <= 0) n = 148;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+// grid for a grid-stride loop: enough blocks for the work, at most 8 resident per SM
+static unsigned grid_for(int64_t work_items, int threads) {
+  int64_t b = (work_items + threads - 1) / threads;
+  int64_t cap = (int64_t)sm_count() * 8;
+  if (b > cap) b = cap;
+  if (b < 1) b = 1;
+  return (unsigned)b;
+}
+
+uint32_t take_error_mem() {
+  uint32_t v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_mem, sizeof(v)) != cudaSuccess) return ERRBIT_INDEX;
+  cudaMemcpyToSymbol(g_err_mem, &z, sizeof(z));
+  return v;
+}
+
+// ------------------------------------------------------------------------ RoPE table
+// tab[p][i] = (cos(p theta_i), sin(p theta_i)), theta_i = base^(-2i/hd); angle in fp64.
+__global__ void k_rope_table(float2* tab, int max_pos, int half, int hd, double base) {
+  int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= (int64_t)max_pos * half) return;
+  int p = (int)(t / half), i = (int)(t % half);
+  double theta = pow(base, -2.0 * (double)i / (double)hd);
+  double s, c;
+  sincos((double)p * theta, &s, &c);
+  tab[t] = make_float2((float)c, (float)s);
+}
+
+cudaError_t launch_rope_table(float* tab, int max_pos, int hd, double base, cudaStream_t s) {
+  int half = hd / 2;
+  int64_t n = (int64_t)max_pos * half;
+  if (n == 0) return cudaSuccess;
+  k_rope_table<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(reinterpret_cast<float2*>(tab),
+                                                           max_pos, half, hd, base);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------ RoPE shift
+// k_dst[r] = R(delta[r]) k_src[src_row[r]]; v_dst[r] = v_src[src_row[r]].
+// One thread per 8 consecutive elements (4 rotation pairs, never crossing a head since
+// hd % 8 == 0).  The negative-offset rotation negates the sine.
+template <typename T>
+__global__ void __launch_bounds__(256) k_rope_shift(T* __restrict__ kd, T* __restrict__ vd,
+                                                    const T* ks, const T* __restrict__ vs,
+                                                    const int32_t* __restrict__ src_row,
+                                                    const int32_t* __restrict__ delta,
+                                                    int64_t n_rows, int W, int hd,
+                                                    const float2* __restrict__ tab, int max_pos) {
+  const int per_row = W >> 3;
+  const int half = hd >> 1;
+  const int64_t total = n_rows * per_row;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = t / per_row;
+    const int c0 = (int)(t - r * per_row) << 3;
+    const int64_t sr = src_row ? (int64_t)src_row[r] : r;
+    const int dl = delta[r];
+    const int ad = dl < 0 ? -dl : dl;
+    if (ad >= max_pos || sr < 0) {
+      atomicOr(&g_err_mem, ERRBIT_INDEX);
+      continue;
+    }
+    const float sg = dl < 0 ? -1.0f : 1.0f;
+    float x[8], y[8];
+    ld8(ks + sr * W + c0, x);
+    const float2* tb = tab + (int64_t)ad * half + ((c0 % hd) >> 1);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 cs = tb[q];
+      const float c = cs.x, sn = cs.y * sg;
+      y[2 * q] = x[2 * q] * c - x[2 * q + 1] * sn;
+      y[2 * q + 1] = x[2 * q] * sn + x[2 * q + 1] * c;
+    }
+    st8(kd + r * W + c0, y);
+    if (vd) {
+      float v[8];
+      ld8(vs + sr * W + c0, v);
+      st8(vd + r * W + c0, v);
+    }
+  }
+}
+
+cudaError_t launch_rope_shift(int dt, void* kd, void* vd, const void* ks, const void* vs,
+                              const int32_t* src_row, const int32_t* delta, int64_t n_rows,
+                              int W, int hd, const float* tab, int max_pos, cudaStream_t s) {
+  if (n_rows == 0) return cudaSuccess;
+  const int64_t work = n_rows * (W / 8);
+  const unsigned grid = grid_for(work, 256);
+  const float2* t2 = reinterpret_cast<const float2*>(tab);
+  if (dt == DT_BF16)
+    k_rope_shift<bf16><<<grid, 256, 0, s>>>((bf16*)kd, (bf16*)vd, (const bf16*)ks,
+                                            (const bf16*)vs, src_row, delta, n_rows, W, hd, t2,
+                                            max_pos);
+  else
+    k_rope_shift<float><<<grid, 256, 0, s>>>((float*)kd, (float*)vd, (const float*)ks,
+                                             (const float*)vs, src_row, delta, n_rows, W, hd, t2,
+                                             max_pos);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------ row copies
+// dst[dst_idx[r]] = src[src_idx[r]] for rows of rv vector words.  Index checks against the
+// known buffer heights (bound < 0: unknown) record ERRBIT_INDEX and skip the row.
+template <typename V>
+__global__ void __launch_bounds__(256) k_copy_rows(V* __restrict__ dst, const int32_t* __restrict__ di,
+                                                   const V* __restrict__ src,
+                                                   const int32_t* __restrict__ si, int64_t n,
+                                                   int64_t rv, int64_t dbound, int64_t sbound) {
+  const int64_t total = n * rv;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = t / rv, c = t - r * rv;
+    const int64_t d = di ? (int64_t)di[r] : r;
+    const int64_t sr = si ? (int64_t)si[r] : r;
+    if (d < 0 || sr < 0 || (dbound >= 0 && d >= dbound) || (sbound >= 0 && sr >= sbound)) {
+      atomicOr(&g_err_mem, ERRBIT_INDEX);
+      continue;
+    }
+    dst[d * rv + c] = src[sr * rv + c];
+  }
+}
+
+cudaError_t launch_copy_rows(void* dst, const int32_t* dst_idx, const void* src,
+                             const int32_t* src_idx, int64_t n, int64_t row_bytes,
+                             int64_t dst_bound, int64_t src_bound, cudaStream_t s) {
+  if (n == 0 || row_bytes == 0) return cudaSuccess;
+  const bool v16 = (row_bytes % 16 == 0) && ((uintptr_t)dst % 16 == 0) && ((uintptr_t)src % 16 == 0);
+  if (v16) {
+    const int64_t rv = row_bytes / 16;
+    k_copy_rows<uint4><<<grid_for(n * rv, 256), 256, 0, s>>>((uint4*)dst, dst_idx, (const uint4*)src,
+                                                           src_idx, n, rv, dst_bound, src_bound);
+  } else {
+    const int64_t rv = row_bytes / 4;
+    k_copy_rows<uint32_t><<<grid_for(n * rv, 256), 256, 0, s>>>((uint32_t*)dst, dst_idx,
+                                                              (const uint32_t*)src, src_idx, n, rv,
+                                                              dst_bound, src_bound);
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------ RMSNorm
+// out[r] = x[rows[r]] / sqrt(mean(x^2) + eps) * g.  One block per row.
+template <typename Ti, typename To>
+__global__ void __launch_bounds__(256) k_rmsnorm(To* __restrict__ out, const Ti* __restrict__ x,
+                                                 const int32_t* __restrict__ rows,
+                                                 const Ti* __restrict__ g, int d, float eps) {
+  __shared__ float red[32];
+  const int64_t r = blockIdx.x;
+  const int64_t src = rows ? (int64_t)rows[r] : r;
+  const Ti* xr = x + src * d;
+  float ss = 0.f;
+  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+    float v[8];
+    ld8(xr + c, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(v[i], v[i], ss);
+  }
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  ss = warp_sum(ss);
+  if (lane == 0) red[w] = ss;
+  __syncthreads();
+  if (w == 0) {
+    float t = lane < nw ? red[lane] : 0.f;
+    t = warp_sum(t);
+    if (lane == 0) red[0] = t;
+  }
+  __syncthreads();
+  const float inv = rsqrtf(red[0] / (float)d + eps);
+  To* orow = out + r * d;
+  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+    float v[8], gg[8], y[8];
+    ld8(xr + c, v);
+    ld8(g + c, gg);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = v[i] * inv * gg[i];
+    st8(orow + c, y);
+  }
+}
+
+cudaError_t launch_rmsnorm(int dt_in, int dt_out, void* out, const void* x, const int32_t* rows,
+                           const void* g, int64_t n, int d, float eps, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const int threads = d >= 2048 ? 256 : (d >= 512 ? 64 : 32);
+  if (dt_in == DT_BF16 && dt_out == DT_BF16)
+    k_rmsnorm<bf16, bf16><<<(unsigned)n, threads, 0, s>>>((bf16*)out, (const bf16*)x, rows,
+                                                          (const bf16*)g, d, eps);
+  else if (dt_in == DT_BF16)
+    k_rmsnorm<bf16, float><<<(unsigned)n, threads, 0, s>>>((float*)out, (const bf16*)x, rows,
+                                                           (const bf16*)g, d, eps);
+  else
+    k_rmsnorm<float, float><<<(unsigned)n, threads, 0, s>>>((float*)out, (const float*)x, rows,
+                                                            (const float*)g, d, eps);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------ KV deviation
+// scores[c] = sum (kn[new_row[c]] - kr[ref_row[c]])^2 (+ V).  One warp per candidate;
+// each lane reads 16-byte vectors, partial sums reduced by shuffles (fixed order).
+template <typename T>
+__global__ void __launch_bounds__(256) k_deviation(const T* __restrict__ kn, const T* __restrict__ vn,
+                                                   const T* __restrict__ kr, const T* __restrict__ vr,
+                                                   const int32_t* __restrict__ new_row,
+                                                   const int32_t* __restrict__ ref_row, int n_cand,
+                                                   int W, int use_v, float* __restrict__ scores) {
+  const int lane = threadIdx.x & 31;
+  const int warps_total = (gridDim.x * blockDim.x) >> 5;
+  for (int c = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; c < n_cand; c += warps_total) {
+    const int64_t rn = new_row ? (int64_t)new_row[c] : c;
+    const int64_t rr = ref_row ? (int64_t)ref_row[c] : c;
+    float acc = 0.f;
+    const T* a = kn + rn * W;
+    const T* b = kr + rr * W;
+    for (int e = lane * 8; e < W; e += 256) {
+      float x[8], y[8];
+      ld8(a + e, x);
+      ld8(b + e, y);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float d = x[i] - y[i];
+        acc = fmaf(d, d, acc);
+      }
+    }
+    if (use_v) {
+      const T* av = vn + rn * W;
+      const T* bv = vr + rr * W;
+      for (int e = lane * 8; e < W; e += 256) {
+        float x[8], y[8];
+        ld8(av + e, x);
+        ld8(bv + e, y);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float d = x[i] - y[i];
+          acc = fmaf(d, d, acc);
+        }
+      }
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) {
+      scores[c] = acc;
+      if (!isfinite(acc)) atomicOr(&g_err_mem, ERRBIT_NONFINITE);
+    }
+  }
+}
+
+cudaError_t launch_deviation(int dt, const void* kn, const void* vn, const void* kr,
+                             const void* vr, const int32_t* new_row, const int32_t* ref_row,
+                             int n_cand, int W, int use_v, float* scores, cudaStream_t s) {
+  if (n_cand == 0) return cudaSuccess;
+  const unsigned grid = grid_for((int64_t)n_cand * 32, 256);
+  if (dt == DT_BF16)
+    k_deviation<bf16><<<grid, 256, 0, s>>>((const bf16*)kn, (const bf16*)vn, (const bf16*)kr,
+                                           (const bf16*)vr, new_row, ref_row, n_cand, W, use_v,
+                                           scores);
+  else
+    k_deviation<float><<<grid, 256, 0, s>>>((const float*)kn, (const float*)vn, (const float*)kr,
+                                            (const float*)vr, new_row, ref_row, n_cand, W, use_v,
+                                            scores);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------ exact top-k
+// Scores are finite and >= 0, so their IEEE bit patterns (with -0 folded to +0) order
+// them as unsigned integers.  A 4-pass radix select (8 bits per pass) finds the k-th
+// largest key T and how many keys equal to T must be taken; a block-wide scan in index
+// order then takes every key > T and the lowest-index keys == T, writing the selected
+// ordinals in ascending order.  One block of 1024 threads per problem.
+__device__ __forceinline__ uint32_t score_key(float s) {
+  return s == 0.0f ? 0u : __float_as_uint(s);
+}
+
+// exclusive block scan of v (blockDim.x <= 1024); *total receives the block sum
+__device__ __forceinline__ int block_excl_scan(int v, int* total, int* sh) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int t = lane < nw ? sh[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    sh[lane] = t;
+  }
+  __syncthreads();
+  const int base = w ? sh[w - 1] : 0;
+  *total = sh[nw - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
+__global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores, int n, int k,
+                                               int32_t* __restrict__ out) {
+  __shared__ int hist[256];
+  __shared__ int sh[32];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_remaining;
+  const int tid = threadIdx.x, bd = blockDim.x;
+  // validity check of every score (finite, non-negative)
+  for (int i = tid; i < n; i += bd) {
+    const float v = scores[i];
+    if (!(v >= 0.0f) || isinf(v)) atomicOr(&g_err_mem, ERRBIT_NONFINITE);
+  }
+  if (k <= 0) return;
+  if (k >= n) {
+    for (int i = tid; i < n; i += bd) out[i] = i;
+    return;
+  }
+  uint32_t prefix = 0, mask = 0;
+  int remaining = k;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += bd) hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += bd) {
+      const uint32_t key = score_key(scores[i]);
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int cum = 0, dsel = 0;
+      for (int dg = 255; dg >= 0; --dg) {
+        if (cum + hist[dg] >= remaining) {
+          dsel = dg;
+          break;
+        }
+        cum += hist[dg];
+      }
+      s_prefix = prefix | ((uint32_t)dsel << shift);
+      s_remaining = remaining - cum;
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    remaining = s_remaining;
+    mask |= 255u << shift;
+    __syncthreads();
+  }
+  int eq_base = 0, out_base = 0;
+  for (int i0 = 0; i0 < n; i0 += bd) {
+    const int i = i0 + tid;
+    const uint32_t key = i < n ? score_key(scores[i]) : 0u;
+    const int gt = (i < n) && key > prefix;
+    const int eq = (i < n) && key == prefix;
+    int eq_tot;
+    const int eq_rank = block_excl_scan(eq, &eq_tot, sh);
+    const int take = gt || (eq && (eq_base + eq_rank) < remaining);
+    int take_tot;
+    const int pos = block_excl_scan(take, &take_tot, sh);
+    if (take) out[out_base + pos] = i;
+    eq_base += eq_tot;
+    out_base += take_tot;
+  }
+}
+
+cudaError_t launch_topk(const float* scores, int n, int k, int32_t* out_ord, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  k_topk<<<1, 1024, 0, s>>>(scores, n, k, out_ord);
+  return cudaGetLastError();
+}
+
+// out[i] = map[ord[i]] (map null: ord[i])
+__global__ void k_map_rows(const int32_t* ord, int k, const int32_t* map, int32_t* out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < k) out[i] = map ? map[ord[i]] : ord[i];
+}
+
+cudaError_t launch_map_rows(const int32_t* ord, int k, const int32_t* map, int32_t* out,
+                            cudaStream_t s) {
+  if (k == 0) return cudaSuccess;
+  k_map_rows<<<(k + 255) / 256, 256, 0, s>>>(ord, k, map, out);
+  return cudaGetLastError();
+}
+
+// Selected set S = (candidate rows of the top-k ordinals) ++ (forced rows), ascending by
+// construction since every forced row lies above every candidate row.  keep_out gives each
+// row's position inside the layer's input row set.
+__global__ void k_build_sel(const int32_t* ord, int k, const int32_t* cand_row, int32_t forced_row0,
+                            int32_t forced_pos0, int n_forced, int32_t* s_out, int32_t* keep_out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < k) {
+    const int o = ord[i];
+    s_out[i] = cand_row ? cand_row[o] : o;
+    if (keep_out) keep_out[i] = o;
+  } else if (i < k + n_forced) {
+    const int f = i - k;
+    s_out[i] = forced_row0 + f;
+    if (keep_out) keep_out[i] = forced_pos0 + f;
+  }
+}
+
+cudaError_t launch_build_sel(const int32_t* ord, int k, const int32_t* cand_row,
+                             int32_t forced_row0, int32_t forced_pos0, int n_forced,
+                             int32_t* s_out, int32_t* keep_out, cudaStream_t s) {
+  const int n = k + n_forced;
+  if (n == 0) return cudaSuccess;
+  k_build_sel<<<(n + 255) / 256, 256, 0, s>>>(ord, k, cand_row, forced_row0, forced_pos0, n_forced,
+                                             s_out, keep_out);
+  return cudaGetLastError();
+}
+
+// pos_out[i] = position of rows[i] inside the ascending s_in[0..m_in) (s_in null: rows[i]
+// itself, checked < m_in).  A row that is absent records ERRBIT_INDEX and maps to 0.
+__global__ void k_rows_to_positions(const int32_t* rows, int k, const int32_t* s_in, int m_in,
+                                    int32_t* pos_out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= k) return;
+  const int r = rows[i];
+  if (!s_in) {
+    if (r < 0 || r >= m_in) {
+      atomicOr(&g_err_mem, ERRBIT_INDEX);
+      pos_out[i] = 0;
+    } else {
+      pos_out[i] = r;
+    }
+    return;
+  }
+  int lo = 0, hi = m_in;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (s_in[mid] < r) lo = mid + 1; else hi = mid;
+  }
+  if (lo < m_in && s_in[lo] == r) {
+    pos_out[i] = lo;
+  } else {
+    atomicOr(&g_err_mem, ERRBIT_INDEX);
+    pos_out[i] = 0;
+  }
+}
+
+cudaError_t launch_rows_to_positions(const int32_t* rows, int k, const int32_t* s_in, int m_in,
+                                     int32_t* pos_out, cudaStream_t s) {
+  if (k == 0) return cudaSuccess;
+  k_rows_to_positions<<<(k + 255) / 256, 256, 0, s>>>(rows, k, s_in, m_in, pos_out);
+  return cudaGetLastError();
+}
+
+__global__ void k_iota(int32_t* out, int n, int32_t start) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = start + i;
+}
+
+cudaError_t launch_iota(int32_t* out, int n, int32_t start, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  k_iota<<<(n + 255) / 256, 256, 0, s>>>(out, n, start);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------ SwiGLU (SIMT path)
+// out[m][j] = silu(gu[m][j]) * gu[m][F + j]
+template <typename T>
+__global__ void k_swiglu(T* __restrict__ out, const T* __restrict__ gu, int64_t M, int F) {
+  const int64_t total = M * F;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = t / F, j = t - m * F;
+    const float g = to_f(gu[m * 2 * F + j]);
+    const float u = to_f(gu[m * 2 * F + F + j]);
+    out[t] = from_f<T>(silu_f(g) * u);
+  }
+}
+
+cudaError_t launch_swiglu(int dt, void* out, const void* gu, int64_t M, int F, cudaStream_t s) {
+  if (M == 0) return cudaSuccess;
+  const unsigned grid = grid_for(M * F, 256);
+  if (dt == DT_BF16)
+    k_swiglu<bf16><<<grid, 256, 0, s>>>((bf16*)out, (const bf16*)gu, M, F);
+  else
+    k_swiglu<float><<<grid, 256, 0, s>>>((float*)out, (const float*)gu, M, F);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------ lm_head
+// logits[v] = hn . w[v]; one warp per vocabulary row, 16-byte weight loads.
+template <typename T>
+__global__ void __launch_bounds__(256) k_lm_gemv(float* __restrict__ logits, const float* __restrict__ hn,
+                                                 const T* __restrict__ w, int V, int d) {
+  const int lane = threadIdx.x & 31;
+  const int warps_total = (gridDim.x * blockDim.x) >> 5;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < V; r += warps_total) {
+    const T* wr = w + (int64_t)r * d;
+    float acc = 0.f;
+    for (int c = lane * 8; c < d; c += 256) {
+      float a[8], b[8];
+      ld8(wr + c, a);
+      ld8(hn + c, b);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc = fmaf(a[i], b[i], acc);
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) logits[r] = acc;
+  }
+}
+
+cudaError_t launch_lm_gemv(int dt, float* logits, const float* hn, const void* w, int V, int d,
+                           cudaStream_t s) {
+  const unsigned grid = grid_for((int64_t)V * 32, 256);
+  if (dt == DT_BF16)
+    k_lm_gemv<bf16><<<grid, 256, 0, s>>>(logits, hn, (const bf16*)w, V, d);
+  else
+    k_lm_gemv<float><<<grid, 256, 0, s>>>(logits, hn, (const float*)w, V, d);
+  return cudaGetLastError();
+}
+
+// argmax with ties to the lowest index: maximise (ordered float bits, ~index) as a u64
+__device__ __forceinline__ uint32_t ordered_bits(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(1024) k_argmax(const float* __restrict__ logits, int V, int32_t* token) {
+  __shared__ unsigned long long red[32];
+  unsigned long long best = 0ull;
+  for (int i = threadIdx.x; i < V; i += blockDim.x) {
+    const unsigned long long key =
+        ((unsigned long long)ordered_bits(logits[i]) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)i);
+    best = key > best ? key : best;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
+    best = y > best ? y : best;
+  }
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (lane == 0) red[w] = best;
+  __syncthreads();
+  if (w == 0) {
+    best = lane < (int)(blockDim.x >> 5) ? red[lane] : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
+      best = y > best ? y : best;
+    }
+    if (lane == 0) token[0] = (int32_t)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+  }
+}
+
+cudaError_t launch_argmax(const float* logits, int V, int32_t* token, cudaStream_t s) {
+  k_argmax<<<1, 1024, 0, s>>>(logits, V, token);
+  return cudaGetLastError();
+}
+
+}  // namespace cb

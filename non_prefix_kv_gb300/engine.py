@@ -1,0 +1,223 @@
+"""Request driver for blended prefill: device-resident weights, the chunk-KV pool, and the
+per-layer loop of the CacheBlend pipeline (CacheBlend explainer,
+0h-n0.github.io/posts/paper-2312-03052, §Pipelining: fetch a layer's chunk KV, run the
+layer's partial prefill, synchronize).  Marshalling and host bookkeeping only: every
+arithmetic step runs in libcacheblend's kernels."""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import List, Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import binding as B
+from .synth import ModelShape
+
+
+def torch_dtype(shape: ModelShape):
+    return torch.bfloat16 if shape.dtype == "bf16" else torch.float32
+
+
+def make_dims(shape: ModelShape) -> B.cb_dims:
+    return B.cb_dims(shape.d_model, shape.n_heads, shape.n_kv_heads, shape.head_dim, shape.d_ff, shape.vocab,
+                     float(shape.rope_base), float(shape.rms_eps), B.CB_BF16 if shape.dtype == "bf16" else B.CB_F32)
+
+
+class DeviceModel:
+    """Weights on the device in the shape's storage dtype."""
+
+    def __init__(self, shape: ModelShape, layers: List[dict], embed, final_norm, w_lm):
+        self.shape = shape
+        self.dims = make_dims(shape)
+        self.layers = layers
+        self.embed, self.final_norm, self.w_lm = embed, final_norm, w_lm
+        self.layers_c = [B.cb_layer_w(*(l[k].data_ptr() for k in
+                                        ("attn_norm", "wqkv", "wo", "ffn_norm", "w_gate_up", "w_down")))
+                         for l in layers]
+
+    @classmethod
+    def from_host(cls, model: dict, device="cuda") -> "DeviceModel":
+        """Upload a synth.make_model() dict (values already representable in the dtype)."""
+        shape = model["shape"]
+        dt = torch_dtype(shape)
+
+        def up(a):
+            return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device).to(dt)
+
+        cache = {}
+        layers = []
+        for l in model["layers"]:
+            if id(l) not in cache:
+                cache[id(l)] = {k: up(v) for k, v in l.items()}
+            layers.append(cache[id(l)])
+        return cls(shape, layers, up(model["embed"]), up(model["final_norm"]), up(model["w_lm"]))
+
+    @classmethod
+    def random_on_device(cls, shape: ModelShape, seed: int = 0, device="cuda") -> "DeviceModel":
+        """Random-init weights drawn on the device (seeded torch CUDA generator) for shapes
+        too large to draw on the host: matrices N(0, w_std), embeddings N(0, emb_std),
+        gains 1."""
+        dt = torch_dtype(shape)
+        g = torch.Generator(device=device)
+        g.manual_seed(seed * 1000003 + 1)
+        d, F = shape.d_model, shape.d_ff
+
+        def normal(*sz, std):
+            return (torch.randn(*sz, generator=g, device=device, dtype=torch.float32) * std).to(dt)
+
+        n_distinct = 1 if shape.shared_layers else shape.n_layers
+        distinct = []
+        for _ in range(n_distinct):
+            distinct.append({
+                "attn_norm": torch.ones(d, device=device, dtype=dt),
+                "wqkv": normal(shape.qkv_width, d, std=shape.w_std),
+                "wo": normal(d, shape.q_width, std=shape.w_std),
+                "ffn_norm": torch.ones(d, device=device, dtype=dt),
+                "w_gate_up": normal(2 * F, d, std=shape.w_std),
+                "w_down": normal(d, F, std=shape.w_std),
+            })
+        layers = [distinct[0 if shape.shared_layers else i] for i in range(shape.n_layers)]
+        embed = normal(shape.vocab, d, std=shape.emb_std)
+        w_lm = normal(shape.vocab, d, std=shape.w_std)
+        return cls(shape, layers, embed, torch.ones(d, device=device, dtype=dt), w_lm)
+
+
+@dataclass
+class ChunkPool:
+    """Per-layer K/V of every distinct chunk, precomputed alone at local positions 0..n-1."""
+    k: List[torch.Tensor]          # per layer [rows, Hkv*hd]
+    v: List[torch.Tensor]
+    offsets: List[int]             # first pool row of each chunk
+    lens: List[int]
+
+
+class BlendEngine:
+    def __init__(self, dm: DeviceModel, n_tok_max: int, max_pos: Optional[int] = None, device="cuda"):
+        self.dm = dm
+        self.device = device
+        s = dm.shape
+        self.max_pos = int(max_pos or n_tok_max)
+        self.cos_sin = torch.empty(self.max_pos * s.head_dim, dtype=torch.float32, device=device)
+        B.cb_rope_table(self.cos_sin, self.max_pos, s.head_dim, float(s.rope_base))
+        self.ws = torch.empty(B.cb_workspace_bytes(dm.dims, n_tok_max, n_tok_max), dtype=torch.uint8,
+                              device=device)
+        self.n_tok_max = n_tok_max
+
+    # ---- precompute (offline: KV^pre) ------------------------------------------------------
+    def precompute_pool(self, chunk_tokens: Sequence[np.ndarray]) -> ChunkPool:
+        s = self.dm.shape
+        lens = [len(t) for t in chunk_tokens]
+        offs = list(np.cumsum([0] + lens[:-1]))
+        rows = int(sum(lens))
+        dt = torch_dtype(s)
+        k = [torch.empty(rows, s.kv_width, dtype=dt, device=self.device) for _ in range(s.n_layers)]
+        v = [torch.empty(rows, s.kv_width, dtype=dt, device=self.device) for _ in range(s.n_layers)]
+        for t, off, n in zip(chunk_tokens, offs, lens):
+            tok = torch.from_numpy(np.asarray(t, np.int32)).to(self.device)
+            B.cb_full_prefill(self.dm.dims, self.dm.layers_c, self.dm.embed, tok, n, 0,
+                              [kk[off:off + n] for kk in k], [vv[off:off + n] for vv in v], None, None,
+                              self.cos_sin, self.max_pos, self.ws)
+        return ChunkPool(k, v, [int(o) for o in offs], lens)
+
+    def full_prefill(self, tokens: torch.Tensor, k_out, v_out, h_last, x_all=None, pos0: int = 0):
+        B.cb_full_prefill(self.dm.dims, self.dm.layers_c, self.dm.embed, tokens, tokens.numel(), pos0, k_out,
+                          v_out, h_last, x_all, self.cos_sin, self.max_pos, self.ws)
+
+
+class Request:
+    """Device state of one blended-prefill request: chunk order, token ids, the blended
+    K/V cache of every layer, hidden-row buffers."""
+
+    def __init__(self, eng: BlendEngine, pool: ChunkPool, order: Sequence[int], tokens: np.ndarray):
+        s = eng.dm.shape
+        dev = eng.device
+        dt = torch_dtype(s)
+        self.eng, self.pool = eng, pool
+        self.order = list(order)
+        self.n_cached = int(sum(pool.lens[c] for c in order))
+        self.N = int(len(tokens))
+        src, delta = [], []
+        start = 0
+        for c in order:
+            n = pool.lens[c]
+            src.extend(range(pool.offsets[c], pool.offsets[c] + n))
+            delta.extend([start] * n)                 # p - p' = slot start (p' = local position)
+            start += n
+        self.src_row = torch.tensor(src, dtype=torch.int32, device=dev)
+        self.delta = torch.tensor(delta, dtype=torch.int32, device=dev)
+        self.tokens_host = np.asarray(tokens, np.int32)
+        self.tokens = torch.from_numpy(self.tokens_host).to(dev)
+        self.K = [torch.zeros(self.N, s.kv_width, dtype=dt, device=dev) for _ in range(s.n_layers)]
+        self.V = [torch.zeros(self.N, s.kv_width, dtype=dt, device=dev) for _ in range(s.n_layers)]
+        self.x = [torch.empty(self.N, s.d_model, dtype=dt, device=dev) for _ in range(2)]
+        self.s = [torch.empty(self.N, dtype=torch.int32, device=dev) for _ in range(2)]
+        self.scores = torch.empty(self.N, dtype=torch.float32, device=dev)
+        self.token = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.sel_hist: List[torch.Tensor] = []
+        self.m_hist: List[int] = []
+
+
+def layer_plan(shape: ModelShape, n_tok: int, n_cached: int, ratios: Sequence[Optional[float]],
+               check_layer: int = 1, gradual: bool = False):
+    """Host bookkeeping of the per-layer mode and HKVD budget (k and |S| are known before
+    any launch, so the loop never waits on the device)."""
+    f0 = min(n_cached, n_tok - 1)
+    n_forced = n_tok - f0
+    plan = []
+    m_in = n_tok
+    for l in range(shape.n_layers):
+        if l < check_layer:
+            plan.append((B.CB_LAYER_PRECHECK, 0))
+            m_in = n_tok
+        elif l == check_layer:
+            k = B.cb_hkvd_budget(n_cached, ratios[l], f0)
+            plan.append((B.CB_LAYER_CHECK, k))
+            m_in = k + n_forced
+        elif gradual:
+            n_cand = m_in - n_forced
+            k = B.cb_hkvd_budget(n_cached, ratios[l], n_cand)
+            plan.append((B.CB_LAYER_GRADUAL, k))
+            m_in = k + n_forced
+        else:
+            plan.append((B.CB_LAYER_STEADY, 0))
+    return plan
+
+
+def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None, keep_history=False,
+              assemble: bool = True, stream=None):
+    """One blended prefill: re-position the chunk KV of every layer, run the layer plan,
+    then the lm_head argmax.  Returns the number of rows carried out of the last layer."""
+    eng = req.eng
+    dm = eng.dm
+    s = dm.shape
+    dims = dm.dims
+    esz = 2 if s.dtype == "bf16" else 4
+    if assemble:
+        for l in range(s.n_layers):
+            B.cb_rope_shift(req.K[l], req.V[l], req.pool.k[l], req.pool.v[l], req.src_row, req.delta,
+                            req.n_cached, dims, eng.cos_sin, eng.max_pos, stream)
+    B.cb_gather_rows(req.x[0], dm.embed, req.tokens, req.N, s.d_model * esz, stream)
+    cur = 0
+    m_in = req.N
+    s_in = None
+    if keep_history:
+        req.sel_hist, req.m_hist = [], []
+    for l, (mode, k) in enumerate(plan):
+        ov = None if sel_override is None else sel_override.get(l)
+        m_out = B.cb_blend_layer(dims, dm.layers_c[l], mode, req.x[cur], s_in, m_in, req.N, req.n_cached,
+                                 req.K[l], req.V[l], eng.cos_sin, eng.max_pos, k, dev_mode, ov,
+                                 req.x[1 - cur], req.s[1 - cur],
+                                 req.scores if mode in (B.CB_LAYER_CHECK, B.CB_LAYER_GRADUAL) else None,
+                                 eng.ws, stream)
+        cur = 1 - cur
+        s_in = req.s[cur]
+        m_in = m_out
+        if keep_history:
+            req.sel_hist.append(req.s[cur][:m_out].clone())
+            req.m_hist.append(m_out)
+    req.m_last = m_in
+    req.x_last = req.x[cur]
+    h_last = req.x[cur][m_in - 1]
+    B.cb_lmhead_argmax(h_last, dm.final_norm, dm.w_lm, dims, None, req.token, eng.ws, stream)
+    return m_in

@@ -133,12 +133,14 @@ def round_bf16(a: np.ndarray) -> np.ndarray:
     Storage conversion only: every value the device sees in a bf16 run is exactly the
     float32 returned here, so both sides start from identical numbers.
     """
-    a = np.ascontiguousarray(a, dtype=np.float32)
-    u = a.view(np.uint32).astype(np.uint64)
-    lsb = (u >> 16) & 1
-    r = ((u + 0x7FFF + lsb) >> 16) << 16
-    out = (r & 0xFFFFFFFF).astype(np.uint32).view(np.float32)
-    return out.reshape(a.shape)
+    out = np.array(a, dtype=np.float32, copy=True, order="C")
+    u = out.view(np.uint32)
+    # finite inputs never overflow 32 bits here: |u| <= 0xFF7FFFFF, + 0x8000
+    lsb = (u >> 16) & np.uint32(1)
+    u += np.uint32(0x7FFF)
+    u += lsb
+    u &= np.uint32(0xFFFF0000)
+    return out
 
 
 def bf16_bits(a: np.ndarray) -> np.ndarray:

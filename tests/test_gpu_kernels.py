@@ -1,0 +1,352 @@
+"""Per-entry-point parity of the CUDA path against the CPU oracle on seeded inputs.
+Index and copy results are compared bit-exactly; floats by relative Frobenius error."""
+import numpy as np
+import pytest
+
+import oracle.cacheblend_oracle as O
+from non_prefix_kv_gb300 import synth
+from tests.gpu_util import TOL, dev, dev_i32, ensure_lib, host, rel, tdt, torch_mod
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    torch_mod()
+    ensure_lib()
+    from non_prefix_kv_gb300 import binding
+    return binding
+
+
+def dims_for(B, shape):
+    from non_prefix_kv_gb300 import engine as E
+    return E.make_dims(shape)
+
+
+SHAPE_F32 = synth.ModelShape(n_layers=2, d_model=256, n_heads=4, n_kv_heads=4, head_dim=64, d_ff=688,
+                             vocab=1024, dtype="f32", w_std=0.05)
+SHAPE_BF16 = synth.ModelShape(n_layers=2, d_model=512, n_heads=8, n_kv_heads=2, head_dim=64, d_ff=1024,
+                              vocab=2048, dtype="bf16", w_std=0.04)
+
+
+def rope_tab(B, max_pos, hd, base):
+    torch = torch_mod()
+    t = torch.empty(max_pos * hd, dtype=torch.float32, device="cuda")
+    B.cb_rope_table(t, max_pos, hd, base)
+    return t
+
+
+# ------------------------------------------------------------------------------ RoPE
+@pytest.mark.parametrize("base", [1e4, 5e6])
+def test_rope_table(B, base):
+    hd, P = 128, 16384
+    t = host(rope_tab(B, P, hd, base)).reshape(P, hd // 2, 2)
+    pos = np.arange(P)[:, None]
+    ang = pos * O.rope_theta(hd, base)
+    assert np.max(np.abs(t[..., 0] - np.cos(ang))) < 2e-7
+    assert np.max(np.abs(t[..., 1] - np.sin(ang))) < 2e-7
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_rope_shift_gather_and_negative_offsets(B, dtype):
+    torch = torch_mod()
+    shape = synth.ModelShape(1, 256, 6, 3, 64, 256, 64, dtype=dtype)
+    dims = dims_for(B, shape)
+    W = shape.kv_width
+    n_src, n = 500, 333
+    g = synth.rng(11, synth.P_NOISE)
+    ks = synth.test_tensor((n_src, W), 12, dtype=dtype)
+    vs = synth.test_tensor((n_src, W), 13, dtype=dtype)
+    src_row = g.integers(0, n_src, n).astype(np.int32)
+    delta = g.integers(-5000, 16383, n).astype(np.int32)
+    delta[:3] = [0, 16383, -16383]
+    tab = rope_tab(B, 16384, shape.head_dim, shape.rope_base)
+    kd = torch.empty(n, W, dtype=tdt(dtype), device="cuda")
+    vd = torch.empty_like(kd)
+    B.cb_rope_shift(kd, vd, dev(ks, dtype), dev(vs, dtype), dev_i32(src_row), dev_i32(delta), n, dims, tab, 16384)
+    B.cb_sync(None)
+    want = O.rope_shift(ks[src_row].reshape(n, 3, 64), delta, shape.rope_base).reshape(n, W)
+    assert rel(host(kd), want) < (2e-6 if dtype == "f32" else 4e-3)
+    np.testing.assert_array_equal(host(vd), vs[src_row])
+
+
+def test_rope_shift_in_place_keys_only(B):
+    torch = torch_mod()
+    shape = synth.ModelShape(1, 256, 2, 2, 128, 256, 64, dtype="bf16")
+    dims = dims_for(B, shape)
+    k0 = synth.test_tensor((640, 256), 14, dtype="bf16")
+    k = dev(k0, "bf16")
+    delta = np.full(640, 1280, np.int32)
+    tab = rope_tab(B, 4096, 128, 1e4)
+    B.cb_rope_shift(k, None, k, None, None, dev_i32(delta), 640, dims, tab, 4096)
+    B.cb_sync(None)
+    want = O.rope_shift(k0.reshape(640, 2, 128), 1280, 1e4).reshape(640, 256)
+    assert rel(host(k), want) < 4e-3
+
+
+# ------------------------------------------------------------------------------ selection
+def _topk_case(g, n, kind):
+    if kind == "random":
+        s = g.random(n).astype(np.float32) * 100
+    elif kind == "ties":
+        s = g.integers(0, 4, n).astype(np.float32)
+    elif kind == "equal":
+        s = np.full(n, 2.5, np.float32)
+    else:  # zeros of both signs and subnormals among ordinary values
+        s = g.random(n).astype(np.float32)
+        s[::3] = 0.0
+        s[1::7] = -0.0
+        s[2::11] = np.float32(1e-40)
+    return s
+
+
+@pytest.mark.parametrize("n", [1, 5, 1000, 3840, 15360, 16391])
+@pytest.mark.parametrize("kind", ["random", "ties", "equal", "zeros"])
+def test_topk_from_scores_bit_exact(B, n, kind):
+    torch = torch_mod()
+    g = synth.rng(n + len(kind), synth.P_NOISE)
+    s = _topk_case(g, n, kind)
+    cand = np.sort(g.choice(4 * n, size=n, replace=False)).astype(np.int32)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    sel = torch.empty(n, dtype=torch.int32, device="cuda")
+    for k in sorted({0, 1, n // 7, n // 2, max(n - 1, 0), n}):
+        for use_cand in (False, True):
+            B.cb_topk_from_scores(dev(s), dev_i32(cand) if use_cand else None, n, k, sel, ws)
+            B.cb_sync(None)
+            got = sel[:k].cpu().numpy()
+            want = O.topk_rows(s, cand if use_cand else np.arange(n), k)
+            np.testing.assert_array_equal(got, want)
+
+
+def test_topk_flags_nonfinite(B):
+    torch = torch_mod()
+    s = np.ones(100, np.float32)
+    s[17] = np.nan
+    ws = torch.empty(1 << 16, dtype=torch.uint8, device="cuda")
+    sel = torch.empty(100, dtype=torch.int32, device="cuda")
+    B.cb_topk_from_scores(dev(s), None, 100, 10, sel, ws)
+    with pytest.raises(B.CBError) as e:
+        B.cb_sync(None)
+    assert e.value.status == 5
+    B.cb_sync(None)      # the error word was cleared
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dev_mode", [0, 1])
+def test_kv_deviation_topk(B, dtype, dev_mode):
+    torch = torch_mod()
+    shape = synth.ModelShape(1, 256, 8, 2, 128, 256, 64, dtype=dtype)
+    dims = dims_for(B, shape)
+    W = shape.kv_width
+    n_ref, n_new, n_cand, k = 3000, 2000, 1500, 225
+    g = synth.rng(21, synth.P_NOISE)
+    kr = synth.test_tensor((n_ref, W), 22, dtype=dtype)
+    vr = synth.test_tensor((n_ref, W), 23, dtype=dtype)
+    kn = synth.test_tensor((n_new, W), 24, dtype=dtype)
+    vn = synth.test_tensor((n_new, W), 25, dtype=dtype)
+    new_row = np.sort(g.choice(n_new, n_cand, replace=False)).astype(np.int32)
+    ref_row = np.sort(g.choice(n_ref, n_cand, replace=False)).astype(np.int32)
+    scores = torch.empty(n_cand, dtype=torch.float32, device="cuda")
+    sel = torch.empty(k, dtype=torch.int32, device="cuda")
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    B.cb_kv_deviation_topk(dev(kn, dtype), dev(vn, dtype), dev(kr, dtype), dev(vr, dtype), dev_i32(new_row),
+                           dev_i32(ref_row), n_cand, k, dev_mode, dims, scores, sel, ws)
+    B.cb_sync(None)
+    if dev_mode == 0:
+        want = O.kv_deviation(kn[new_row], kr[ref_row], vn[new_row], vr[ref_row])
+    else:
+        want = O.kv_deviation(kn[new_row], kr[ref_row])
+    got = host(scores)
+    assert np.max(np.abs(got - want) / want) < 1e-5
+    # the selection is a valid top-k of the exact scores up to fp32 rounding of the sums
+    chosen = sel.cpu().numpy()
+    assert np.all(np.diff(chosen) > 0) and np.all(np.isin(chosen, ref_row))
+    mask = np.isin(ref_row, chosen)
+    assert mask.sum() == k
+    assert want[mask].min() >= want[~mask].max() * (1 - 2e-5)
+    ref_sel = O.topk_rows(want, ref_row, k)
+    srt = np.sort(want)[::-1]
+    if (srt[k - 1] - srt[k]) / srt[k - 1] > 2e-5:
+        np.testing.assert_array_equal(chosen, ref_sel)
+
+
+# ------------------------------------------------------------------------------ row copies
+@pytest.mark.parametrize("row_bytes", [4 * 37, 16 * 64])
+def test_gather_scatter_bitwise(B, row_bytes):
+    torch = torch_mod()
+    g = synth.rng(31, synth.P_NOISE)
+    n_src, n = 700, 450
+    src = g.integers(0, 2**31, (n_src, row_bytes // 4)).astype(np.int32)
+    idx = g.integers(0, n_src, n).astype(np.int32)
+    dst = torch.empty(n, row_bytes // 4, dtype=torch.int32, device="cuda")
+    B.cb_gather_rows(dst, dev_i32(src), dev_i32(idx), n, row_bytes)
+    B.cb_sync(None)
+    np.testing.assert_array_equal(dst.cpu().numpy(), src[idx])
+    # scatter of K/V rows (dims fix the row width): bf16 rows of W = 2 * 256
+    shape = synth.ModelShape(1, 256, 2, 2, 128, 256, 64, dtype="bf16")
+    dims = dims_for(B, shape)
+    cache = synth.test_tensor((800, 256), 32, dtype="bf16")
+    rows = synth.test_tensor((300, 256), 33, dtype="bf16")
+    dst_idx = np.sort(g.choice(800, 300, replace=False)).astype(np.int32)
+    src_idx = g.permutation(300).astype(np.int32)
+    kc, vc = dev(cache, "bf16"), dev(cache, "bf16")
+    B.cb_scatter_kv(kc, vc, dev(rows, "bf16"), dev(rows, "bf16"), dev_i32(dst_idx), dev_i32(src_idx), 300, dims)
+    B.cb_sync(None)
+    want = cache.copy()
+    want[dst_idx] = rows[src_idx]
+    np.testing.assert_array_equal(host(kc), want)
+    np.testing.assert_array_equal(host(vc), want)
+
+
+# ------------------------------------------------------------------------------ GEMM
+@pytest.mark.parametrize("M,N,K", [(1, 16, 64), (7, 256, 72), (127, 272, 4096), (129, 512, 136),
+                                   (300, 4096, 1024), (832, 1024, 4096), (1000, 768, 11008)])
+def test_linear_bf16_tensor_cores(B, M, N, K):
+    torch = torch_mod()
+    x = synth.test_tensor((M, K), 40 + M, dtype="bf16")
+    w = synth.test_tensor((N, K), 41 + N, std=0.02, dtype="bf16")
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    B.cb_linear(dev(x, "bf16"), dev(w, "bf16"), y, M, N, K, B.CB_BF16)
+    B.cb_sync(None)
+    want = x.astype(np.float64) @ w.astype(np.float64).T
+    assert rel(host(y), want) < 5e-3
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4, 3), (65, 100, 129), (300, 688, 256)])
+def test_linear_f32(B, M, N, K):
+    torch = torch_mod()
+    x = synth.test_tensor((M, K), 50, dtype="f32")
+    w = synth.test_tensor((N, K), 51, dtype="f32")
+    y = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    B.cb_linear(dev(x), dev(w), y, M, N, K, B.CB_F32)
+    B.cb_sync(None)
+    assert rel(host(y), x.astype(np.float64) @ w.astype(np.float64).T) < 1e-6
+
+
+# ------------------------------------------------------------------------------ layer pieces
+def _layer(shape, seed=0):
+    return synth.make_layer_weights(shape, synth.rng(seed, synth.P_WEIGHTS), gains="random")
+
+
+def _layer_dev(B, shape, layer):
+    t = {k: dev(v, shape.dtype) for k, v in layer.items()}
+    w = B.cb_layer_w(*(t[k].data_ptr() for k in ("attn_norm", "wqkv", "wo", "ffn_norm", "w_gate_up", "w_down")))
+    return t, w
+
+
+@pytest.mark.parametrize("shape", [SHAPE_F32, SHAPE_BF16], ids=["f32", "bf16_gqa"])
+@pytest.mark.parametrize("M", [1, 7, 129])
+def test_selective_qkv(B, shape, M):
+    torch = torch_mod()
+    dims = dims_for(B, shape)
+    layer = _layer(shape)
+    t, w = _layer_dev(B, shape, layer)
+    n_x = 300
+    x = synth.test_tensor((n_x, shape.d_model), 60, dtype=shape.dtype)
+    g = synth.rng(61, synth.P_NOISE)
+    rows = np.sort(g.choice(n_x, M, replace=False)).astype(np.int32)
+    pos = g.integers(0, 9000, M).astype(np.int32)
+    tab = rope_tab(B, 9000, shape.head_dim, shape.rope_base)
+    q = torch.empty(M, shape.q_width, dtype=tdt(shape.dtype), device="cuda")
+    k = torch.empty(M, shape.kv_width, dtype=tdt(shape.dtype), device="cuda")
+    v = torch.empty_like(k)
+    ws = torch.empty(B.cb_workspace_bytes(dims, n_x, n_x), dtype=torch.uint8, device="cuda")
+    B.cb_selective_qkv(dev(x, shape.dtype), dev_i32(rows), dev_i32(pos), M, dims, w, tab, 9000, q, k, v, ws)
+    B.cb_sync(None)
+    a = O.rmsnorm(x[rows], layer["attn_norm"], shape.rms_eps)
+    p = O.project_qkv(layer, a, pos, shape)
+    tol = TOL[shape.dtype]
+    assert rel(host(q), p["q"].reshape(M, -1)) < tol
+    assert rel(host(k), p["k"].reshape(M, -1)) < tol
+    assert rel(host(v), p["v"].reshape(M, -1)) < tol
+
+
+@pytest.mark.parametrize("shape", [SHAPE_F32, SHAPE_BF16], ids=["f32", "bf16_gqa"])
+@pytest.mark.parametrize("M", [1, 7, 129])
+def test_partial_attention(B, shape, M):
+    torch = torch_mod()
+    dims = dims_for(B, shape)
+    N = 700
+    H, Hkv, hd = shape.n_heads, shape.n_kv_heads, shape.head_dim
+    g = synth.rng(70 + M, synth.P_NOISE)
+    K = synth.test_tensor((N, Hkv * hd), 71, dtype=shape.dtype)
+    V = synth.test_tensor((N, Hkv * hd), 72, dtype=shape.dtype)
+    q = synth.test_tensor((M, H * hd), 73, std=0.3, dtype=shape.dtype)
+    q_pos = np.sort(g.choice(N, M, replace=False)).astype(np.int32)
+    q_pos[0] = 0 if M > 1 else q_pos[0]
+    q_pos[-1] = N - 1
+    out = torch.empty(M, H * hd, dtype=tdt(shape.dtype), device="cuda")
+    B.cb_partial_attention(dev(q, shape.dtype), dev_i32(q_pos), M, dev(K, shape.dtype), dev(V, shape.dtype), N,
+                           dims, out)
+    B.cb_sync(None)
+    want = O.attend(q.reshape(M, H, hd), q_pos, K.reshape(N, Hkv, hd), V.reshape(N, Hkv, hd))
+    assert rel(host(out), want) < TOL[shape.dtype] / (10 if shape.dtype == "f32" else 2)
+
+
+@pytest.mark.parametrize("shape", [SHAPE_F32, SHAPE_BF16], ids=["f32", "bf16_gqa"])
+@pytest.mark.parametrize("M", [1, 130])
+def test_o_proj_ffn(B, shape, M):
+    torch = torch_mod()
+    dims = dims_for(B, shape)
+    layer = _layer(shape, seed=3)
+    t, w = _layer_dev(B, shape, layer)
+    attn = synth.test_tensor((M, shape.q_width), 80, dtype=shape.dtype)
+    xr = synth.test_tensor((M, shape.d_model), 81, dtype=shape.dtype)
+    out = torch.empty(M, shape.d_model, dtype=tdt(shape.dtype), device="cuda")
+    ws = torch.empty(B.cb_workspace_bytes(dims, M, M), dtype=torch.uint8, device="cuda")
+    B.cb_o_proj_ffn(dev(attn, shape.dtype), dev(xr, shape.dtype), M, dims, w, out, ws)
+    B.cb_sync(None)
+    want = O.out_ffn(layer, xr, attn, shape)
+    assert rel(host(out), want) < TOL[shape.dtype]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_lmhead_argmax(B, dtype):
+    torch = torch_mod()
+    shape = synth.ModelShape(1, 512, 4, 4, 128, 512, 5000, dtype=dtype)
+    dims = dims_for(B, shape)
+    model = {"shape": shape, "final_norm": synth.test_tensor((512,), 90, std=0.2, dtype=dtype) + 1,
+             "w_lm": synth.test_tensor((5000, 512), 91, std=0.02, dtype=dtype)}
+    model["final_norm"] = synth.round_bf16(model["final_norm"]) if dtype == "bf16" else model["final_norm"]
+    h = synth.test_tensor((512,), 92, dtype=dtype)
+    logits = torch.empty(5000, dtype=torch.float32, device="cuda")
+    tok = torch.empty(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    B.cb_lmhead_argmax(dev(h, dtype), dev(model["final_norm"], dtype), dev(model["w_lm"], dtype), dims, logits,
+                       tok, ws)
+    B.cb_sync(None)
+    want_tok, want_logits = O.lm_head_argmax(model, h)
+    got = host(logits)
+    assert rel(got, want_logits) < 1e-5
+    top2 = np.sort(want_logits)[-2:]
+    if top2[1] - top2[0] > 1e-4 * abs(top2[1]):
+        assert int(tok.item()) == want_tok
+    # ties go to the lowest index
+    w2 = np.zeros((5000, 512), np.float32)
+    w2[[7, 3, 4000]] = 1.0
+    B.cb_lmhead_argmax(dev(h, dtype), dev(np.ones(512, np.float32), dtype), dev(w2, dtype), dims, None, tok, ws)
+    B.cb_sync(None)
+    assert int(tok.item()) == (3 if np.sum(h, dtype=np.float64) > 0 else 0)
+
+
+def test_full_prefill_f32_matches_oracle(B):
+    torch = torch_mod()
+    shape = synth.WORKLOADS["tiny_f32"].shape
+    dims = dims_for(B, shape)
+    model = synth.make_model(shape, seed=0)
+    from non_prefix_kv_gb300 import engine as E
+    dm = E.DeviceModel.from_host(model)
+    eng = E.BlendEngine(dm, 416)
+    toks = synth.rng(0, synth.P_TOKENS).integers(0, shape.vocab, 200).astype(np.int32)
+    k_out = [torch.empty(200, shape.kv_width, device="cuda") for _ in range(2)]
+    v_out = [torch.empty(200, shape.kv_width, device="cuda") for _ in range(2)]
+    h = torch.empty(shape.d_model, device="cuda")
+    x_all = torch.empty(200, shape.d_model, device="cuda")
+    eng.full_prefill(dev_i32(toks), k_out, v_out, h, x_all, pos0=17)
+    B.cb_sync(None)
+    ref = O.full_prefill(model, toks, pos0=17)
+    for l in range(2):
+        assert rel(host(k_out[l]), ref["K"][l].reshape(200, -1)) < 1e-5
+        assert rel(host(v_out[l]), ref["V"][l].reshape(200, -1)) < 1e-5
+    assert rel(host(x_all), ref["x"][-1]) < 1e-5
+    assert rel(host(h), ref["h_last"]) < 1e-5

@@ -1,0 +1,153 @@
+"""CPU-only checks of the C ABI: the library loads, exports every entry point the header
+declares, its host-side helpers agree with the oracle, and argument validation rejects bad
+calls before any launch (no GPU is touched by these calls)."""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle.cacheblend_oracle as O
+from non_prefix_kv_gb300 import binding as B
+from non_prefix_kv_gb300 import build as nb
+from tests.conftest import ROOT, read_golden
+
+HEADER = os.path.join(ROOT, "include", "cacheblend.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    nb.build()
+    return B.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cb_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_north_star_calls():
+    names = declared_symbols()
+    for n in ["cb_rope_shift", "cb_kv_deviation_topk", "cb_gather_rows", "cb_selective_qkv",
+              "cb_partial_attention", "cb_scatter_kv", "cb_blend_layer", "cb_full_prefill"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(nb.LIB)
+    missing = [n for n in declared_symbols() if not hasattr(raw, n)]
+    assert not missing, missing
+    # and the binding wraps every one of them under the same name
+    for n in declared_symbols():
+        assert n in B._PROTOS
+
+
+def test_budget_matches_oracle(lib):
+    for n, r, k in read_golden("budget_table.txt"):
+        assert B.cb_hkvd_budget(int(n), float(r), 1 << 40) == int(k)
+    g = np.random.default_rng(0)
+    for _ in range(2000):
+        n = int(g.integers(0, 20000))
+        r = float(g.choice([0.0, 1.0, g.random(), 0.05, 0.1, 0.15, 0.18]))
+        cand = int(g.integers(0, n + 1))
+        assert B.cb_hkvd_budget(n, r, cand) == O.budget(n, r, cand)
+    assert B.cb_hkvd_budget(10, 1.5, 10) == -1
+    assert B.cb_hkvd_budget(10, -0.1, 10) == -1
+
+
+def test_gradual_schedule_matches_oracle(lib):
+    for r in [0.05, 0.15, 0.18, 0.7, 1.0]:
+        sched = O.ratio_schedule(r, 32, 1, True)
+        for l in range(32):
+            got = B.cb_gradual_ratio(r, l, 1, 1.5)
+            if sched[l] is None:
+                assert got == -1.0
+            else:
+                assert got == sched[l]
+
+
+def test_load_controller(lib):
+    assert B.cb_load_controller_ratio(0.15, 0.016, 0.020) == O.optimal_ratio(0.15, 0.016, 0.020)
+    assert B.cb_load_controller_ratio(0.15, 0.001, 0.020) == 0.15
+
+
+def test_status_strings(lib):
+    for code in range(10):
+        assert lib.cb_status_string(code)
+    assert lib.cb_status_string(99) == b"unknown status"
+
+
+def _dims(**kw):
+    base = dict(d_model=256, n_heads=4, n_kv_heads=4, head_dim=64, d_ff=688, vocab=1024, rope_base=1e4,
+                rms_eps=1e-5, dtype=B.CB_F32)
+    base.update(kw)
+    return B.cb_dims(**base)
+
+
+def test_workspace_query_and_dims_validation(lib):
+    n = B.cb_workspace_bytes(_dims(), 416, 416)
+    assert n > 416 * 256 * 4
+    with pytest.raises(B.CBError) as e:
+        B.cb_workspace_bytes(_dims(dtype=7), 416, 416)
+    assert e.value.status == 3
+    with pytest.raises(B.CBError) as e:
+        B.cb_workspace_bytes(_dims(n_kv_heads=3), 416, 416)
+    assert e.value.status == 2
+    with pytest.raises(B.CBError) as e:
+        B.cb_workspace_bytes(_dims(head_dim=48), 416, 416)
+    assert e.value.status == 8
+
+
+FAKE = 0x10000   # never dereferenced: every call below fails validation before launching
+
+
+def test_entry_points_reject_bad_arguments_before_launch(lib):
+    d = _dims()
+    w = B.cb_layer_w(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)
+    st = lib.cb_rope_shift(FAKE, None, FAKE, FAKE, None, None, 10, ctypes.byref(d), FAKE, 100, None)
+    assert st == 1        # delta NULL
+    st = lib.cb_rope_shift(FAKE, FAKE, FAKE, None, None, FAKE, 10, ctypes.byref(d), FAKE, 100, None)
+    assert st == 1        # v_dst without v_src
+    st = lib.cb_kv_deviation_topk(FAKE, FAKE, FAKE, FAKE, None, None, 10, 11, 0, ctypes.byref(d), None, FAKE,
+                                  FAKE, 1 << 20, None)
+    assert st == 2        # k > n_cand
+    st = lib.cb_topk_from_scores(FAKE, None, 100, 5, FAKE, FAKE, 16, None)
+    assert st == 4        # workspace too small
+    st = lib.cb_gather_rows(FAKE, FAKE, None, 3, 6, None)
+    assert st == 2        # row_bytes not a multiple of 4
+    m_out = ctypes.c_int32(-1)
+    args = lambda mode, m_in, k, ws_bytes=1 << 40: (ctypes.byref(d), ctypes.byref(w), mode, FAKE, None, m_in, 416,
+                                                   384, FAKE, FAKE, FAKE, 416, k, 0, None, FAKE + 64, FAKE,
+                                                   ctypes.byref(m_out), None, FAKE, ws_bytes, None)
+    assert lib.cb_blend_layer(*args(B.CB_LAYER_CHECK, 416, 385)) == 2     # k > candidates (384)
+    assert lib.cb_blend_layer(*args(B.CB_LAYER_CHECK, 400, 5)) == 2       # CHECK needs all rows
+    assert lib.cb_blend_layer(*args(B.CB_LAYER_PRECHECK, 416, 0, 100)) == 4
+    assert lib.cb_blend_layer(*args(9, 416, 0)) == 1
+    assert m_out.value == -1          # nothing reported for a rejected call
+    st = lib.cb_blend_layer(ctypes.byref(d), ctypes.byref(w), 0, FAKE, None, 416, 416, 384, FAKE, FAKE, FAKE,
+                            100, 0, 0, None, FAKE + 64, FAKE, ctypes.byref(m_out), None, FAKE, 1 << 40, None)
+    assert st == 2                    # rope table shorter than the sequence
+    assert b"rope table" in lib.cb_last_error_message()
+    st = lib.cb_linear(FAKE, FAKE, FAKE, 4, 24, 64, B.CB_BF16, None)
+    assert st == 8                    # bf16 N % 16
+
+
+def test_layer_plan_sizes_match_oracle_selection(lib):
+    from non_prefix_kv_gb300 import engine as E
+    from non_prefix_kv_gb300 import synth
+    wl = synth.WORKLOADS["llama7b_32_4k"]
+    ratios = O.ratio_schedule(wl.ratio, wl.shape.n_layers, 1, True)
+    plan = E.layer_plan(wl.shape, wl.n_tokens, wl.n_cached, ratios, gradual=True)
+    n_forced = wl.n_tokens - wl.n_cached
+    m = wl.n_tokens
+    for l, (mode, k) in enumerate(plan):
+        if l == 0:
+            assert mode == B.CB_LAYER_PRECHECK
+            continue
+        n_cand = wl.n_cached if l == 1 else m - n_forced
+        assert k == O.budget(wl.n_cached, ratios[l], n_cand)
+        m = k + n_forced
+    assert plan[1][1] == O.budget(3840, min(1.0, 1.5 * 0.15))

@@ -158,6 +158,26 @@ int cb_kv_deviation_topk(const void* k_new, const void* v_new, const void* k_ref
                          float* scores, int32_t* sel, void* ws, size_t ws_bytes,
                          void* stream);
 
+/* Allocation-free variant of cb_kv_deviation_topk, for callers that cannot hand the
+ * library device memory: for example a plugin running inside a host program that owns and
+ * pre-partitions all device memory, or a latency-critical caller that must not call
+ * cudaMalloc (which can synchronise the device).  The pages have no counterpart: this is
+ * a deployment convenience, not a step of the method.
+ * Same arguments and results as cb_kv_deviation_topk, without the workspace.  Its scratch
+ * (a score and an ordinal per candidate) is a fixed 512 KiB array in the library's device
+ * memory, held by every GPU that loads the library until the process exits.
+ *   - n_cand is limited to 65536; larger returns CB_ERR_UNSUPPORTED before any launch.
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - Every call shares the one array and it keeps the last call's contents: calls that
+ *     may overlap on the GPU (different streams, or different host threads, on the same
+ *     device) race with each other.  Serialise them. */
+int cb_kv_deviation_topk_noalloc(const void* k_new, const void* v_new, const void* k_ref,
+                                 const void* v_ref, const int32_t* new_row,
+                                 const int32_t* ref_row, int32_t n_cand, int32_t k,
+                                 int32_t dev_mode, const cb_dims* dims, float* scores,
+                                 int32_t* sel, void* stream);
+
 /* Top-k of given fp32 scores (>= 0, finite), ties to the lower index, output ascending
  * as cand[c] (cand NULL = c).  The selection step alone, for bit-exact checks. */
 int cb_topk_from_scores(const float* scores, const int32_t* cand, int32_t n_cand,

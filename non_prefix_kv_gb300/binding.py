@@ -60,6 +60,8 @@ _PROTOS = {
     "cb_rope_shift": (C.c_int, [_P, _P, _P, _P, _P, _P, _I64, C.POINTER(cb_dims), _P, _I32, _P]),
     "cb_kv_deviation_topk": (C.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, C.POINTER(cb_dims),
                                        _P, _P, _P, _SZ, _P]),
+    "cb_kv_deviation_topk_noalloc": (C.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, C.POINTER(cb_dims),
+                                               _P, _P, _P]),
     "cb_topk_from_scores": (C.c_int, [_P, _P, _I32, _I32, _P, _P, _SZ, _P]),
     "cb_gather_rows": (C.c_int, [_P, _P, _P, _I64, _I64, _P]),
     "cb_scatter_kv": (C.c_int, [_P, _P, _P, _P, _P, _P, _I64, C.POINTER(cb_dims), _P]),
@@ -163,6 +165,15 @@ def cb_kv_deviation_topk(k_new, v_new, k_ref, v_ref, new_row, ref_row, n_cand: i
     _check("cb_kv_deviation_topk", lib().cb_kv_deviation_topk(
         _ptr(k_new), _ptr(v_new), _ptr(k_ref), _ptr(v_ref), _ptr(new_row), _ptr(ref_row), n_cand, k,
         dev_mode, C.byref(dims), _ptr(scores), _ptr(sel), _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def cb_kv_deviation_topk_noalloc(k_new, v_new, k_ref, v_ref, new_row, ref_row, n_cand: int, k: int,
+                                 dev_mode: int, dims: cb_dims, scores, sel, stream=None):
+    """Same as cb_kv_deviation_topk, with the scratch in the library's fixed device array
+    (for callers that cannot allocate; at most 65536 candidates; overlapping calls race)."""
+    _check("cb_kv_deviation_topk_noalloc", lib().cb_kv_deviation_topk_noalloc(
+        _ptr(k_new), _ptr(v_new), _ptr(k_ref), _ptr(v_ref), _ptr(new_row), _ptr(ref_row), n_cand, k,
+        dev_mode, C.byref(dims), _ptr(scores), _ptr(sel), _stream(stream)))
 
 
 def cb_topk_from_scores(scores, cand, n_cand: int, k: int, sel, ws, stream=None):

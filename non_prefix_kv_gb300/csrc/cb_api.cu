@@ -414,6 +414,26 @@ int cb_kv_deviation_topk(const void* k_new, const void* v_new, const void* k_ref
   return CB_OK;
 }
 
+int cb_kv_deviation_topk_noalloc(const void* k_new, const void* v_new, const void* k_ref, const void* v_ref,
+                                 const int32_t* new_row, const int32_t* ref_row, int32_t n_cand, int32_t k,
+                                 int32_t dev_mode, const cb_dims* dims, float* scores, int32_t* sel, void* stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (n_cand < 0 || k < 0 || k > n_cand) return fail(CB_ERR_SHAPE, "need 0 <= k <= n_cand");
+  if (n_cand > noalloc_max_candidates())
+    return fail(CB_ERR_UNSUPPORTED, "n_cand %d exceeds the fixed scratch of %d candidates", n_cand,
+                noalloc_max_candidates());
+  if (dev_mode != CB_DEV_KV && dev_mode != CB_DEV_K) return fail(CB_ERR_INVALID_ARG, "dev_mode");
+  if (n_cand == 0) return CB_OK;
+  if (!k_new || !k_ref || (dev_mode == CB_DEV_KV && (!v_new || !v_ref)) || (k > 0 && !sel))
+    return fail(CB_ERR_INVALID_ARG, "deviation pointer is NULL");
+  const int W = dims->n_kv_heads * dims->head_dim;
+  CB_CUDA(launch_deviation_topk_noalloc(dims->dtype, k_new, v_new, k_ref, v_ref, new_row, ref_row, n_cand, k, W,
+                                        dev_mode == CB_DEV_KV, scores, sel, S(stream)));
+  g_launches.fetch_add(k > 0 ? 3 : 1, std::memory_order_relaxed);
+  return CB_OK;
+}
+
 int cb_topk_from_scores(const float* scores, const int32_t* cand, int32_t n_cand, int32_t k, int32_t* sel,
                         void* ws, size_t ws_bytes, void* stream) {
   if (n_cand < 0 || k < 0 || k > n_cand) return fail(CB_ERR_SHAPE, "need 0 <= k <= n_cand");

@@ -84,6 +84,11 @@ cudaError_t launch_lm_gemv(int dt, float* logits, const float* hn, const void* w
                            cudaStream_t s);
 cudaError_t launch_argmax(const float* logits, int V, int32_t* token, cudaStream_t s);
 uint32_t take_error_mem();
+int noalloc_max_candidates();
+cudaError_t launch_deviation_topk_noalloc(int dt, const void* kn, const void* vn, const void* kr,
+                                          const void* vr, const int32_t* new_row,
+                                          const int32_t* ref_row, int n_cand, int k, int W,
+                                          int use_v, float* scores, int32_t* sel, cudaStream_t s);
 
 // ---- cb_gemm.cu -----------------------------------------------------------------------
 cudaError_t launch_gemm(int dt, const GemmDesc& g, cudaStream_t s);

@@ -5,6 +5,8 @@
 // Sources: CacheBlend explainer (0h-n0.github.io/posts/paper-2312-03052) — §KV deviation,
 // §HKVD selection, §Selective recomputation Steps 1 and 3, §RoPE; Prompt Cache explainer
 // (0h-n0.github.io/posts/paper-2402-01008) — §RoPE position adjustment.
+#include <mutex>
+
 #include "cb_common.cuh"
 #include "cb_internal.h"
 
@@ -568,6 +570,54 @@ __global__ void __launch_bounds__(1024) k_argmax(const float* __restrict__ logit
 cudaError_t launch_argmax(const float* logits, int V, int32_t* token, cudaStream_t s) {
   k_argmax<<<1, 1024, 0, s>>>(logits, V, token);
   return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------ allocation-free variant
+// Scratch of the deviation/top-k entry point for callers that cannot allocate device memory:
+// one fixed array per device, 8 bytes per candidate (fp32 score + int32 ordinal), held for
+// the life of the process by every device that loads the library.  Every call shares it.
+constexpr int kNoAllocMaxCand = 65536;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[(size_t)kNoAllocMaxCand * 8];
+
+int noalloc_max_candidates() { return kNoAllocMaxCand; }
+
+// The array's name is only a host-side stand-in in host code; its device address is looked
+// up once per device (with that device current) and reused.
+static cudaError_t noalloc_scratch_address(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
+// Same kernels as the workspace path; scores (when the caller passes none) and the top-k
+// ordinals live in the fixed array.  Both are fully written before they are read, so
+// nothing in it has to start at zero.  n_cand <= kNoAllocMaxCand is checked by the caller.
+cudaError_t launch_deviation_topk_noalloc(int dt, const void* kn, const void* vn, const void* kr,
+                                          const void* vr, const int32_t* new_row,
+                                          const int32_t* ref_row, int n_cand, int k, int W,
+                                          int use_v, float* scores, int32_t* sel, cudaStream_t s) {
+  void* base = nullptr;
+  cudaError_t e = noalloc_scratch_address(&base);
+  if (e != cudaSuccess) return e;
+  float* sc = scores ? scores : static_cast<float*>(base);
+  int32_t* ord = reinterpret_cast<int32_t*>(static_cast<char*>(base) + (size_t)kNoAllocMaxCand * 4);
+  e = launch_deviation(dt, kn, vn, kr, vr, new_row, ref_row, n_cand, W, use_v, sc, s);
+  if (e != cudaSuccess || k <= 0) return e;
+  e = launch_topk(sc, n_cand, k, ord, s);
+  if (e != cudaSuccess) return e;
+  return launch_map_rows(ord, k, ref_row, sel, s);
 }
 
 }  // namespace cb

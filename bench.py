@@ -394,6 +394,18 @@ def our_arm(args):
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "peak_source": f"{peak_src} bf16_tflops_sustained", "traffic": None,
                 "flops_per_launch": gemm_flops_launch, "ms_per_launch": gemm_ms_launch}
+    gemms = {}
+    for r in recs:
+        if r["kind"] != "gemm":
+            continue
+        key = (r["m"], r["n"], r["k"], r["aux"])
+        e = gemms.setdefault(key, [0, 0.0, r["flops"]])
+        e[0] += 1
+        e[1] += r["ms"]
+    epi_names = {0: "store", 1: "resid", 2: "qkv", 3: "swiglu"}
+    gemm_detail = [{"m": k[0], "n": k[1], "k": k[2], "epi": epi_names.get(k[3], k[3]),
+                    "us": 1e3 * v[1] / v[0], "tflops": v[2] / (v[1] / v[0] / 1e3) / 1e12}
+                   for k, v in sorted(gemms.items(), key=lambda kv: -kv[1][1])]
     hbm_kernels = {}
     for name in ("rope_shift", "deviation", "copy_rows", "lmhead_gemv"):
         if name in kinds and kinds[name]["bytes"]:
@@ -448,7 +460,7 @@ def our_arm(args):
         "gpu_launches": int(launches_per_step * args.steps),
         "launches_per_step": int(launches_per_step),
         "step_tflops": flops / (ms / 1e3) / 1e12,
-        "roofline": roofline, "hbm_kernels": hbm_kernels, "kernels": kernels,
+        "roofline": roofline, "hbm_kernels": hbm_kernels, "kernels": kernels, "gemm_launches": gemm_detail,
         "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "setup_s": setup_s,
     }
     if rank == 0:

@@ -16,6 +16,7 @@
 
 namespace cb {
 uint32_t take_error_gemm_tc();
+uint32_t take_error_attn_tc();
 cudaError_t launch_gemm_simt_bf16(const GemmDesc& g, cudaStream_t s);
 }  // namespace cb
 
@@ -331,7 +332,8 @@ int cb_sync(void* stream, double timeout_s) {
     timespec ts{0, 50000};
     nanosleep(&ts, nullptr);
   }
-  const uint32_t bits = take_error_mem() | take_error_gemm() | take_error_gemm_tc() | take_error_attn();
+  const uint32_t bits = take_error_mem() | take_error_gemm() | take_error_gemm_tc() | take_error_attn() |
+                        take_error_attn_tc();
   if (bits & ERRBIT_NONFINITE) return fail(CB_ERR_NONFINITE, "a deviation score was NaN/Inf");
   if (bits & ERRBIT_INDEX) return fail(CB_ERR_DEVICE, "a kernel met an out-of-range index");
   if (bits & ERRBIT_TIMEOUT) return fail(CB_ERR_DEVICE, "a kernel's bounded wait expired");

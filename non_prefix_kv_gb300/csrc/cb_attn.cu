@@ -5,7 +5,7 @@
 //   out[j, h] = sum_{t <= q_pos[j]} softmax_t(q[j,h] . K[t,g] / sqrt(hd)) V[t,g],
 //   g = h / (H / Hkv)
 //
-// SIMT kernel: one 128-thread block per (query row, head); each warp streams a contiguous
+// SIMT kernel (fp32 parity mode): one 128-thread block per (query row, head); each warp streams a contiguous
 // quarter of the visible keys with an online softmax, lanes splitting the head dimension;
 // the four partial states are merged at the end.  fp32 arithmetic throughout.
 #include <math.h>
@@ -122,12 +122,20 @@ static cudaError_t launch_simt(const void* q, const int32_t* q_pos, int M, const
   return cudaGetLastError();
 }
 
+bool attention_tc_supported(int hd);
+cudaError_t launch_attention_tc(const void* q, const int32_t* q_pos, int M, const void* kc, const void* vc,
+                                int64_t n_kv, int H, int Hkv, int hd, void* out, cudaStream_t s);
+
+// bf16 with head_dim 64/128 runs on the tcgen05 kernel (cb_attn_tc.cu); fp32 (the exact
+// parity mode) and other head sizes on the SIMT kernel above.
 cudaError_t launch_attention(int dt, const void* q, const int32_t* q_pos, int M, const void* kc,
                              const void* vc, int64_t n_kv, int H, int Hkv, int hd, void* out,
                              void* ws, size_t ws_bytes, cudaStream_t s) {
   (void)ws;
   (void)ws_bytes;
   if (M == 0) return cudaSuccess;
+  if (dt == DT_BF16 && attention_tc_supported(hd))
+    return launch_attention_tc(q, q_pos, M, kc, vc, n_kv, H, Hkv, hd, out, s);
   if (dt == DT_BF16) return launch_simt<bf16>(q, q_pos, M, kc, vc, n_kv, H, Hkv, hd, out, s);
   return launch_simt<float>(q, q_pos, M, kc, vc, n_kv, H, Hkv, hd, out, s);
 }

@@ -283,6 +283,30 @@ def test_partial_attention(B, shape, M):
     assert rel(host(out), want) < TOL[shape.dtype] / (10 if shape.dtype == "f32" else 2)
 
 
+@pytest.mark.parametrize("H,Hkv,hd", [(4, 4, 128), (8, 2, 64), (7, 1, 128)])
+@pytest.mark.parametrize("M,N,qstd,order", [(1, 1, 0.3, "asc"), (128, 300, 0.3, "asc"), (257, 2100, 3.0, "asc"),
+                                            (300, 4096, 1.0, "shuffled"), (129, 129, 8.0, "asc")])
+def test_partial_attention_bf16_tensor_cores(B, H, Hkv, hd, M, N, qstd, order):
+    """Tile edges (M, N around 128), GQA groups of 1/4/7, softmax ranges wide enough to
+    force the lazy rescale of O, and query positions in any order."""
+    torch = torch_mod()
+    shape = synth.ModelShape(1, 256, H, Hkv, hd, 256, 64, dtype="bf16")
+    dims = dims_for(B, shape)
+    g = synth.rng(M * 7 + N, synth.P_NOISE)
+    K = synth.test_tensor((N, Hkv * hd), 74, dtype="bf16")
+    V = synth.test_tensor((N, Hkv * hd), 75, dtype="bf16")
+    q = synth.test_tensor((M, H * hd), 76, std=qstd, dtype="bf16")
+    q_pos = np.sort(g.choice(N, M, replace=False)).astype(np.int32)
+    q_pos[-1] = N - 1
+    if order == "shuffled":
+        q_pos = g.permutation(q_pos).astype(np.int32)
+    out = torch.empty(M, H * hd, dtype=torch.bfloat16, device="cuda")
+    B.cb_partial_attention(dev(q, "bf16"), dev_i32(q_pos), M, dev(K, "bf16"), dev(V, "bf16"), N, dims, out)
+    B.cb_sync(None)
+    want = O.attend(q.reshape(M, H, hd), q_pos, K.reshape(N, Hkv, hd), V.reshape(N, Hkv, hd))
+    assert rel(host(out), want) < 5e-3
+
+
 @pytest.mark.parametrize("shape", [SHAPE_F32, SHAPE_BF16], ids=["f32", "bf16_gqa"])
 @pytest.mark.parametrize("M", [1, 130])
 def test_o_proj_ffn(B, shape, M):

@@ -1,0 +1,133 @@
+"""Per-entry-point microbenchmark: times one library call at a given shape with CUDA events
+and prints achieved TFLOP/s or GB/s against the algorithmic work.  Also the small, single-
+kernel command that ncu captures are taken on.
+
+  python -m non_prefix_kv_gb300.microbench gemm --m 4096 --n 8192 --k 4096 [--epi swiglu]
+  python -m non_prefix_kv_gb300.microbench attention --m 832 --n 4096 --heads 32 --kv-heads 32 --hd 128
+  python -m non_prefix_kv_gb300.microbench rope_shift --rows 3840 --width 4096
+  python -m non_prefix_kv_gb300.microbench deviation --cand 3840 --width 4096 --k 576
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import sys
+
+import numpy as np
+import torch
+
+from . import binding as B
+from . import build as nb
+from . import engine as E
+from .synth import ModelShape
+
+
+def _time(fn, iters: int, warmup: int):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(iters):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+def run(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("what", choices=["gemm", "attention", "rope_shift", "deviation"])
+    p.add_argument("--m", type=int, default=4096)
+    p.add_argument("--n", type=int, default=8192)
+    p.add_argument("--k", type=int, default=4096)
+    p.add_argument("--epi", choices=["store", "swiglu"], default="store")
+    p.add_argument("--heads", type=int, default=32)
+    p.add_argument("--kv-heads", type=int, default=32)
+    p.add_argument("--hd", type=int, default=128)
+    p.add_argument("--rows", type=int, default=3840)
+    p.add_argument("--width", type=int, default=4096)
+    p.add_argument("--cand", type=int, default=3840)
+    p.add_argument("--iters", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    a = p.parse_args(argv)
+    nb.build()
+    B.lib()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    bf = torch.bfloat16
+    out = {"what": a.what}
+    if a.what == "gemm":
+        if a.epi == "store":
+            x = torch.randn(a.m, a.k, device="cuda", generator=g).to(bf)
+            w = (torch.randn(a.n, a.k, device="cuda", generator=g) * 0.02).to(bf)
+            y = torch.empty(a.m, a.n, device="cuda", dtype=bf)
+            ms = _time(lambda: B.cb_linear(x, w, y, a.m, a.n, a.k, B.CB_BF16), a.iters, a.warmup)
+            fl = 2.0 * a.m * a.n * a.k
+        else:
+            # gate/up GEMM with the fused SwiGLU epilogue, inside the O-proj + FFN call
+            shape = ModelShape(1, a.k, 1, 1, 128, a.n, 64, dtype="bf16")
+            dims = E.make_dims(shape)
+            lw = {"attn_norm": torch.ones(a.k, device="cuda", dtype=bf),
+                  "wqkv": torch.zeros(384, a.k, device="cuda", dtype=bf),
+                  "wo": (torch.randn(a.k, 128, device="cuda", generator=g) * 0.02).to(bf),
+                  "ffn_norm": torch.ones(a.k, device="cuda", dtype=bf),
+                  "w_gate_up": (torch.randn(2 * a.n, a.k, device="cuda", generator=g) * 0.02).to(bf),
+                  "w_down": (torch.randn(a.k, a.n, device="cuda", generator=g) * 0.02).to(bf)}
+            cw = B.cb_layer_w(*(lw[k].data_ptr() for k in ("attn_norm", "wqkv", "wo", "ffn_norm", "w_gate_up",
+                                                            "w_down")))
+            attn = torch.randn(a.m, 128, device="cuda", generator=g).to(bf)
+            x = torch.randn(a.m, a.k, device="cuda", generator=g).to(bf)
+            y = torch.empty_like(x)
+            ws = torch.empty(B.cb_workspace_bytes(dims, a.m, a.m), dtype=torch.uint8, device="cuda")
+            ms = _time(lambda: B.cb_o_proj_ffn(attn, x, a.m, dims, cw, y, ws), a.iters, a.warmup)
+            fl = 2.0 * a.m * a.k * (128 + 3 * a.n)
+        out.update(ms=ms, tflops=fl / (ms / 1e3) / 1e12, m=a.m, n=a.n, k=a.k, epi=a.epi)
+    elif a.what == "attention":
+        shape = ModelShape(1, 256, a.heads, a.kv_heads, a.hd, 256, 64, dtype="bf16")
+        dims = E.make_dims(shape)
+        n = a.n
+        K = torch.randn(n, a.kv_heads * a.hd, device="cuda", generator=g).to(bf)
+        V = torch.randn(n, a.kv_heads * a.hd, device="cuda", generator=g).to(bf)
+        q = torch.randn(a.m, a.heads * a.hd, device="cuda", generator=g).to(bf)
+        rng = np.random.default_rng(0)
+        pos = np.sort(rng.choice(n, a.m, replace=False)) if a.m < n else np.arange(n)[:a.m]
+        pos[-1] = n - 1
+        q_pos = torch.from_numpy(pos.astype(np.int32)).cuda()
+        o = torch.empty_like(q)
+        ms = _time(lambda: B.cb_partial_attention(q, q_pos, a.m, K, V, n, dims, o), a.iters, a.warmup)
+        fl = 4.0 * a.heads * a.hd * float(np.sum(pos + 1))
+        out.update(ms=ms, tflops=fl / (ms / 1e3) / 1e12, m=a.m, n=n)
+    elif a.what == "rope_shift":
+        hd = a.hd
+        shape = ModelShape(1, 256, a.width // hd, a.width // hd, hd, 256, 64, dtype="bf16")
+        dims = E.make_dims(shape)
+        tab = torch.empty(16384 * hd, device="cuda")
+        B.cb_rope_table(tab, 16384, hd, 1e4)
+        ks = torch.randn(a.rows, a.width, device="cuda", generator=g).to(bf)
+        vs = torch.randn(a.rows, a.width, device="cuda", generator=g).to(bf)
+        kd, vd = torch.empty_like(ks), torch.empty_like(vs)
+        delta = torch.full((a.rows,), 1280, dtype=torch.int32, device="cuda")
+        ms = _time(lambda: B.cb_rope_shift(kd, vd, ks, vs, None, delta, a.rows, dims, tab, 16384), a.iters,
+                   a.warmup)
+        by = 4.0 * a.rows * a.width * 2
+        out.update(ms=ms, gbs=by / (ms / 1e3) / 1e9, rows=a.rows, width=a.width)
+    else:
+        hd = a.hd
+        shape = ModelShape(1, 256, a.width // hd, a.width // hd, hd, 256, 64, dtype="bf16")
+        dims = E.make_dims(shape)
+        tens = [torch.randn(a.cand, a.width, device="cuda", generator=g).to(bf) for _ in range(4)]
+        sc = torch.empty(a.cand, device="cuda")
+        sel = torch.empty(max(a.k, 1), dtype=torch.int32, device="cuda")
+        ws = torch.empty(1 << 22, dtype=torch.uint8, device="cuda")
+        ms = _time(lambda: B.cb_kv_deviation_topk(tens[0], tens[1], tens[2], tens[3], None, None, a.cand, a.k, 0,
+                                                  dims, sc, sel, ws), a.iters, a.warmup)
+        by = 4.0 * a.cand * a.width * 2
+        out.update(ms=ms, gbs=by / (ms / 1e3) / 1e9, cand=a.cand, width=a.width, k=a.k)
+    B.cb_sync(None)
+    print(json.dumps(out))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(run())

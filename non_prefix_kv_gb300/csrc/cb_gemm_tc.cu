@@ -3,8 +3,10 @@
 //
 //   acc[m][n] = sum_k A[m][k] * B[n][k]      A: activations [M, K], B: weight rows [N, K]
 //
-// One 128 x 256 output tile per CTA (SwiGLU: 128 gate + 128 up columns -> 128 outputs),
-// K consumed in 64-element (128-byte) slabs through a 4-stage ring.  Warp roles:
+// Persistent: one CTA per SM walks 128 x 256 output tiles (SwiGLU: 128 gate + 128 up
+// columns -> 128 outputs), K consumed in 64-element (128-byte) slabs through a 4-stage
+// ring; two TMEM accumulators let the epilogue of one tile overlap the next tile's MMAs.
+// Warp roles:
 //   warp 0 lane 0 : TMA producer     warp 1 : TMEM allocator, lane 0 issues the MMAs
 //   warps 2..5    : epilogue, each reading the 32 TMEM lanes (rows) its warp may access.
 #include <cuda.h>
@@ -35,7 +37,7 @@ constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int SMEM_BYTES = STAGES * (A_BYTES + B_BYTES) + 1024 /*align slack*/ + 256 /*barriers*/;
 constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t TMEM_COLS = 512;   // two 256-column accumulators
 
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -47,14 +49,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smA = base;
   uint8_t* smB = base + STAGES * A_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + STAGES * (A_BYTES + B_BYTES));
-  uint64_t* full = bars;                 // [STAGES] TMA -> MMA
-  uint64_t* empty = bars + STAGES;       // [STAGES] MMA -> TMA
-  uint64_t* acc_full = bars + 2 * STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  uint64_t* full = bars;                     // [STAGES] TMA -> MMA
+  uint64_t* empty = bars + STAGES;           // [STAGES] MMA -> TMA
+  uint64_t* acc_full = bars + 2 * STAGES;    // [2] MMA -> epilogue
+  uint64_t* acc_empty = bars + 2 * STAGES + 2;  // [2] epilogue -> MMA
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * BM;
-  const int n0 = blockIdx.x * (swiglu ? BN / 2 : BN);   // output column origin
+  const int out_cols = swiglu ? BN / 2 : BN;
+  const int num_m = (g.M + BM - 1) / BM;
+  const int num_n = (g.N + out_cols - 1) / out_cols;
+  const int total = num_m * num_n;
   const int KB = (g.K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
@@ -62,7 +67,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    tc::mbar_init(acc_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&acc_full[b], 1);
+      tc::mbar_init(&acc_empty[b], 4);
+    }
     tc::fence_mbar_init();
     tc::tma_prefetch_desc(&tmA);
     tc::tma_prefetch_desc(&tmB);
@@ -76,59 +84,82 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Tiles are visited M-fastest: the CTAs in flight share a few weight tiles and the whole
+  // (small) activation matrix, so both stay in L2 and each is read from HBM about once.
   if (warp == 0 && lane == 0) {
     // ---------------- producer
-    for (int kb = 0; kb < KB; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t ph = (kb / STAGES) & 1;
-      if (!tc::mbar_wait(&empty[s], ph ^ 1)) {
-        atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
-        break;
-      }
-      tc::mbar_expect_tx(&full[s], A_BYTES + B_BYTES);
-      tc::tma_load_2d(smA + s * A_BYTES, &tmA, &full[s], kb * BK, m0);
-      if (swiglu) {
-        tc::tma_load_2d(smB + s * B_BYTES, &tmB, &full[s], kb * BK, n0);
-        tc::tma_load_2d(smB + s * B_BYTES + B_BYTES / 2, &tmB, &full[s], kb * BK,
-                        (int)g.b_up_row + n0);
-      } else {
-        tc::tma_load_2d(smB + s * B_BYTES, &tmB, &full[s], kb * BK, n0);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+      const int m0 = (t % num_m) * BM;
+      const int n0 = (t / num_m) * out_cols;
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!tc::mbar_wait(&empty[s], ph ^ 1)) {
+          atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
+          ok = false;
+          break;
+        }
+        tc::mbar_expect_tx(&full[s], A_BYTES + B_BYTES);
+        tc::tma_load_2d(smA + s * A_BYTES, &tmA, &full[s], kb * BK, m0);
+        if (swiglu) {
+          tc::tma_load_2d(smB + s * B_BYTES, &tmB, &full[s], kb * BK, n0);
+          tc::tma_load_2d(smB + s * B_BYTES + B_BYTES / 2, &tmB, &full[s], kb * BK, (int)g.b_up_row + n0);
+        } else {
+          tc::tma_load_2d(smB + s * B_BYTES, &tmB, &full[s], kb * BK, n0);
+        }
       }
     }
   } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
+    // ---------------- MMA issuer: accumulator b = local tile index & 1
     constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
+    uint32_t it = 0, i = 0;
     bool ok = true;
-    for (int kb = 0; kb < KB; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t ph = (kb / STAGES) & 1;
-      if (!tc::mbar_wait(&full[s], ph)) {
-        atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
+    for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++i) {
+      const uint32_t b = i & 1;
+      if (!tc::mbar_wait(&acc_empty[b], ((i >> 1) & 1) ^ 1)) {
         ok = false;
         break;
       }
       tc::tc_fence_after();
-      const uint64_t a_desc = tc::desc_sw128(tc::smem_u32(smA + s * A_BYTES));
-      const uint64_t b_desc = tc::desc_sw128(tc::smem_u32(smB + s * B_BYTES));
+      const uint32_t d_tmem = tmem + b * BN;
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!tc::mbar_wait(&full[s], ph)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint64_t a_desc = tc::desc_sw128(tc::smem_u32(smA + s * A_BYTES));
+        const uint64_t b_desc = tc::desc_sw128(tc::smem_u32(smB + s * B_BYTES));
 #pragma unroll
-      for (int k = 0; k < BK / 16; ++k) {
-        // advance 16 bf16 = 32 bytes along K inside the swizzled 128-byte row
-        tc::mma_bf16(tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, (kb | k) != 0);
+        for (int k = 0; k < BK / 16; ++k) {
+          // advance 16 bf16 = 32 bytes along K inside the swizzled 128-byte row
+          tc::mma_bf16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, (kb | k) != 0);
+        }
+        tc::mma_commit(&empty[s]);
       }
-      tc::mma_commit(&empty[s]);
+      if (ok) tc::mma_commit(&acc_full[b]);
     }
-    if (ok) tc::mma_commit(acc_full);
+    if (!ok) atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
   } else if (warp >= 2) {
-    // ---------------- epilogue
+    // ---------------- epilogue: drains accumulator b while the MMAs fill the other one
     const int lane_base = (warp & 3) * 32;
-    const int m = m0 + lane_base + lane;
-    // every lane waits, then the warp re-converges before the .sync.aligned TMEM loads
-    const bool ready = __all_sync(0xffffffffu, tc::mbar_wait(acc_full, 0));
-    if (!ready) {
-      if (lane == 0) atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
-    } else {
+    uint32_t i = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
+      const uint32_t b = i & 1;
+      const int m0 = (t % num_m) * BM;
+      const int n0 = (t / num_m) * out_cols;
+      const int m = m0 + lane_base + lane;
+      // every lane waits, then the warp re-converges before the .sync.aligned TMEM loads
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&acc_full[b], (i >> 1) & 1))) {
+        if (lane == 0) atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
+        break;
+      }
       tc::tc_fence_after();
-      const uint32_t trow = tmem + (static_cast<uint32_t>(lane_base) << 16);
+      const uint32_t trow = tmem + b * BN + (static_cast<uint32_t>(lane_base) << 16);
       if (!swiglu) {
         for (int c = 0; c < BN / 16; ++c) {
           float v[16];
@@ -146,11 +177,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int j = n0 + c * 16;
           if (m < g.M && j < g.N) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) gt[i] = silu_f(gt[i]) * up[i];
+            for (int q = 0; q < 16; ++q) gt[q] = silu_f(gt[q]) * up[q];
             st_vec<bf16, 16>(static_cast<bf16*>(g.epi.out) + (int64_t)m * g.epi.ldo + j, gt);
           }
         }
       }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&acc_empty[b]);
     }
   }
   tc::tc_fence_before();
@@ -218,7 +252,11 @@ cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t s) {
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int out_cols = swiglu ? BN / 2 : BN;
-  dim3 grid((g.N + out_cols - 1) / out_cols, (g.M + BM - 1) / BM);
+  const int tiles = ((g.N + out_cols - 1) / out_cols) * ((g.M + BM - 1) / BM);
+  static int sms[64] = {0};
+  if (dev >= 0 && dev < 64 && !sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+  const int n_sm = (dev >= 0 && dev < 64 && sms[dev] > 0) ? sms[dev] : 148;
+  const int grid = tiles < n_sm ? tiles : n_sm;
   k_gemm_tc<<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, g, swiglu ? 1 : 0);
   return cudaGetLastError();
 }

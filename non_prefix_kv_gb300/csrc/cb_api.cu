@@ -135,11 +135,11 @@ double gemm_bytes(int dt, const GemmDesc& g) {
   CB_LAUNCH(CB_PROF_ROPE_SHIFT, 0, (n), (W), 0, 3.0 * (n) * (W),                                 \
             (double)(n) * (W) * esize(dt) * ((vd) ? 4 : 2) + 4.0 * (n), s,                       \
             launch_rope_shift(dt, kd, vd, ks, vs, sr, dl, n, W, hd, tab, mp, s))
-#define L_LMGEMV(dt, lg, hn, w, V, d, s)                                                         \
+#define L_LMGEMV(dt, lg, hn, w, V, d, bb, s)                                                     \
   CB_LAUNCH(CB_PROF_LMHEAD, 0, (V), (d), 0, 2.0 * (V) * (d), (double)(V) * (d) * esize(dt) + 4.0 * (V), s, \
-            launch_lm_gemv(dt, lg, hn, w, V, d, s))
-#define L_ARGMAX(lg, V, tok, s) \
-  CB_LAUNCH(CB_PROF_ARGMAX, 0, (V), 0, 0, 0.0, 4.0 * (V), s, launch_argmax(lg, V, tok, s))
+            launch_lm_gemv(dt, lg, hn, w, V, d, bb, s))
+#define L_ARGMAX(bb, n, tok, s) \
+  CB_LAUNCH(CB_PROF_ARGMAX, 0, (n), 0, 0, 0.0, 8.0 * (n), s, launch_argmax_keys(bb, n, tok, s))
 #define L_ROPE_TABLE(tab, mp, hd, base, s)                                                       \
   CB_LAUNCH(CB_PROF_ROPE_TABLE, 0, (int64_t)(mp) * (hd) / 2, (hd), 0, 0.0, 4.0 * (mp) * (hd), s, \
             launch_rope_table(tab, mp, hd, base, s))
@@ -655,15 +655,17 @@ int cb_lmhead_argmax(const void* h, const void* final_norm, const void* w_lm, co
   int st = check_dims(dims);
   if (st) return st;
   if (!h || !final_norm || !w_lm || !token) return fail(CB_ERR_INVALID_ARG, "lmhead pointer is NULL");
-  const size_t need = 256 + (size_t)dims->d_model * 4 + 256 + (size_t)dims->vocab * 4 + 256;
+  const int nb = (int)lm_block_best_count(dims->vocab);
+  const size_t need = 256 + (size_t)dims->d_model * 4 + 256 + (size_t)dims->vocab * 4 + 256 + (size_t)nb * 8 + 256;
   if (!ws || ws_bytes < need) return fail(CB_ERR_WORKSPACE, "workspace %zu < %zu", ws_bytes, need);
   Carver c(ws);
   float* hn = static_cast<float*>(c.take((size_t)dims->d_model * 4));
   float* lg = logits ? logits : static_cast<float*>(c.take((size_t)dims->vocab * 4));
+  unsigned long long* bb = static_cast<unsigned long long*>(c.take((size_t)nb * 8));
   cudaStream_t s = S(stream);
   L_RMSNORM(dims->dtype, CB_F32, hn, h, nullptr, final_norm, 1, dims->d_model, dims->rms_eps, s);
-  L_LMGEMV(dims->dtype, lg, hn, w_lm, dims->vocab, dims->d_model, s);
-  L_ARGMAX(lg, dims->vocab, token, s);
+  L_LMGEMV(dims->dtype, lg, hn, w_lm, dims->vocab, dims->d_model, bb, s);
+  L_ARGMAX(bb, nb, token, s);
   return CB_OK;
 }
 

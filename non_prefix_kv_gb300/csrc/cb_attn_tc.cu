@@ -10,9 +10,13 @@
 //   O  += P_j V_j          tcgen05.mma, A = P (K-major), B = V_j (MN-major), TMEM accum
 // The running max m is raised lazily: O (in TMEM) is rescaled only when a row's max grows by
 // more than 2^8, so most tiles never touch O.  S is double-buffered in TMEM so the MMA warp
-// computes S_{j+1} while the softmax warps work on S_j; K/V tiles stream through a 2-stage
-// TMA ring.  Warp roles: 0 = TMA producer, 1 = TMEM allocator + MMA issuer, 2..5 = softmax
-// and epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
+// computes S_{j+1} while the softmax warps work on S_j; P is double-buffered in shared
+// memory so writing P_j never waits for P_{j-1}.V_{j-1}; each softmax thread pulls its
+// share of a score row out of TMEM in one round trip; K tiles stream through a 2-stage
+// TMA ring (V single-buffered).  Warp roles: 0 = TMA producer, 1 = TMEM allocator + MMA
+// issuer, 2..9 = softmax and epilogue: warp w reads TMEM lanes 32*(w%4)..+31, and the two
+// warps sharing a lane quarter split each score row's 128 columns, exchanging row max and
+// row sum through shared memory.
 #include <cuda.h>
 #include <math.h>
 
@@ -36,7 +40,8 @@ namespace {
 constexpr int BM = 128;              // queries per CTA
 constexpr int BN = 128;              // keys per tile
 constexpr int SLAB = 128 * 128;      // bytes of one [128 rows x 64 bf16] swizzled slab
-constexpr int THREADS = 192;
+constexpr int NSOFT = 8;             // softmax warps: two per TMEM lane quarter
+constexpr int THREADS = 32 * (2 + NSOFT);
 constexpr uint32_t TMEM_COLS = 512;  // S0 | S1 | O
 constexpr uint32_t TM_S0 = 0, TM_O = 256;
 constexpr float kRescaleLog2 = 8.0f;
@@ -46,16 +51,21 @@ struct Layout {
   static constexpr int NSLAB = HD / 64;
   static constexpr int Q_BYTES = NSLAB * SLAB;
   static constexpr int KV_BYTES = NSLAB * SLAB;
-  static constexpr int P_BYTES = 2 * SLAB;
+  static constexpr int P_BYTES = 2 * SLAB;                // one [128 x 128] P tile
+  static constexpr int NP = 2;                            // P double buffer
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;           // 2 stages
-  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;      // 2 stages
-  static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;      // 1 stage
+  static constexpr int OFF_P = OFF_V + KV_BYTES;
+  static constexpr int OFF_X = OFF_P + NP * P_BYTES;      // row max / sum exchange
+  static constexpr int X_BYTES = (2 * 2 + 2) * BM * 4;
+  static constexpr int OFF_BAR = OFF_X + X_BYTES;
   static constexpr int BYTES = OFF_BAR + 256;
   // one CTA per SM: it owns all 512 TMEM columns
   static constexpr int SMEM = (BYTES + 1024) > 120 * 1024 ? (BYTES + 1024) : 120 * 1024;
 };
+
+__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, %0;" ::"n"(NSOFT * 32) : "memory"); }
 
 template <int HD>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -70,17 +80,22 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sK = base + L::OFF_K;
   uint8_t* sV = base + L::OFF_V;
   uint8_t* sP = base + L::OFF_P;
+  float* xmax = reinterpret_cast<float*>(base + L::OFF_X);   // [2 parity][2 half][BM]
+  float* xsum = xmax + 4 * BM;                                 // [2 half][BM]
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::OFF_BAR);
   uint64_t* q_full = bars + 0;
   uint64_t* k_full = bars + 1;     // [2]
-  uint64_t* v_full = bars + 3;     // [2]
-  uint64_t* kv_empty = bars + 5;   // [2]
+  uint64_t* k_empty = bars + 3;    // [2]
+  uint64_t* v_full = bars + 5;
+  uint64_t* v_empty = bars + 6;
   uint64_t* s_full = bars + 7;     // [2]
   uint64_t* s_free = bars + 9;     // [2]
-  uint64_t* p_full = bars + 11;
-  uint64_t* pv_done = bars + 12;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
-  int* s_qmax = reinterpret_cast<int*>(bars + 14);
+  // per P buffer b (tiles with j % 2 == b): P written / P.V done.  One barrier per buffer
+  // keeps every waiter at most one phase behind its producer.
+  uint64_t* p_full = bars + 11;    // [2]
+  uint64_t* pv_done = bars + 13;   // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  int* s_qmax = reinterpret_cast<int*>(bars + 16);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qt = gridDim.x - 1 - blockIdx.x;      // the longest (latest) query tiles first
@@ -92,13 +107,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc::mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&k_full[i], 1);
-      tc::mbar_init(&v_full[i], 1);
-      tc::mbar_init(&kv_empty[i], 1);
+      tc::mbar_init(&k_empty[i], 1);
       tc::mbar_init(&s_full[i], 1);
-      tc::mbar_init(&s_free[i], 4);
+      tc::mbar_init(&s_free[i], NSOFT);
+      tc::mbar_init(&pv_done[i], 1);
+      tc::mbar_init(&p_full[i], NSOFT);
     }
-    tc::mbar_init(p_full, 4);
-    tc::mbar_init(pv_done, 1);
+    tc::mbar_init(v_full, 1);
+    tc::mbar_init(v_empty, 1);
     tc::fence_mbar_init();
     tc::tma_prefetch_desc(&tmQ);
     tc::tma_prefetch_desc(&tmK);
@@ -141,17 +157,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int s = 0; s < L::NSLAB; ++s) tc::tma_load_2d(sQ + s * SLAB, &tmQ, q_full, h * HD + 64 * s, m0);
     for (int j = 0; j < T; ++j) {
       const int st = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      if (!tc::mbar_wait(&kv_empty[st], ph ^ 1)) {
+      if (!tc::mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1)) {
         atomicOr(&g_err_attn_tc, ERRBIT_TIMEOUT);
         break;
       }
       tc::mbar_expect_tx(&k_full[st], L::KV_BYTES);
       for (int s = 0; s < L::NSLAB; ++s)
         tc::tma_load_2d(sK + st * L::KV_BYTES + s * SLAB, &tmK, &k_full[st], g * HD + 64 * s, j * BN);
-      tc::mbar_expect_tx(&v_full[st], L::KV_BYTES);
-      for (int s = 0; s < L::NSLAB; ++s)
-        tc::tma_load_2d(sV + st * L::KV_BYTES + s * SLAB, &tmV, &v_full[st], g * HD + 64 * s, j * BN);
+      if (!tc::mbar_wait(v_empty, (j & 1) ^ 1)) {
+        atomicOr(&g_err_attn_tc, ERRBIT_TIMEOUT);
+        break;
+      }
+      tc::mbar_expect_tx(v_full, L::KV_BYTES);
+      for (int s = 0; s < L::NSLAB; ++s) tc::tma_load_2d(sV + s * SLAB, &tmV, v_full, g * HD + 64 * s, j * BN);
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------------ MMA issuer
@@ -175,29 +193,33 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc::mma_bf16(tmem + TM_S0 + st * BN, a, b, idesc_s, k > 0);
         }
         tc::mma_commit(&s_full[st]);
+        tc::mma_commit(&k_empty[st]);
       }
       if (j >= 1) {
         const int jj = j - 1;
-        const int st = jj & 1;
-        if (!tc::mbar_wait(p_full, jj & 1) || !tc::mbar_wait(&v_full[st], (jj >> 1) & 1)) {
+        if (!tc::mbar_wait(&p_full[jj & 1], (jj >> 1) & 1) || !tc::mbar_wait(v_full, jj & 1)) {
           ok = false;
           break;
         }
         tc::tc_fence_after();
+        const uint8_t* pb = sP + (jj & 1) * L::P_BYTES;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t a = tc::desc_sw128(tc::smem_u32(sP + (k >> 2) * SLAB) + (k & 3) * 32);
-          const uint64_t b = tc::desc_sw128_mn(tc::smem_u32(sV + st * L::KV_BYTES) + k * 16 * 128, SLAB);
+          const uint64_t a = tc::desc_sw128(tc::smem_u32(pb + (k >> 2) * SLAB) + (k & 3) * 32);
+          const uint64_t b = tc::desc_sw128_mn(tc::smem_u32(sV) + k * 16 * 128, SLAB);
           tc::mma_bf16(tmem + TM_O, a, b, idesc_o, (jj > 0 || k > 0) ? 1u : 0u);
         }
-        tc::mma_commit(pv_done);
-        tc::mma_commit(&kv_empty[st]);
+        tc::mma_commit(&pv_done[jj & 1]);
+        tc::mma_commit(v_empty);
       }
     }
     if (!ok) atomicOr(&g_err_attn_tc, ERRBIT_TIMEOUT);
   } else if (warp >= 2) {
     // ------------------------------------------------------------------ softmax + epilogue
+    // Two warps per TMEM lane quarter: `half` 0 owns score columns 0..63 (keys, and P slab
+    // 0) and O columns 0..HD/2-1; half 1 owns the other 64 keys and the other O half.
     const int lane_base = (warp & 3) * 32;
+    const int half = (warp - 2) >> 2;
     const int r = lane_base + lane;
     const int m = m0 + r;
     int qp = 0;
@@ -206,98 +228,121 @@ __global__ void __launch_bounds__(THREADS, 1)
       qp = qp < 0 ? 0 : (qp >= n_kv ? (int)(n_kv - 1) : qp);
     }
     const uint32_t trow = tmem + (static_cast<uint32_t>(lane_base) << 16);
+    const uint32_t tO = trow + TM_O + half * (HD / 2);
     float m_used = -INFINITY, l = 0.f;
+    // ok is warp-uniform.  A failed (timed-out) wait stops the work of this warp but never
+    // the loop: every softmax warp reaches every named barrier, so none can be left waiting.
     bool ok = true;
-    uint8_t* prow = sP + r * 128;
     for (int j = 0; j < T; ++j) {
       const int sb = j & 1;
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&s_full[sb], (j >> 1) & 1))) {
-        ok = false;
-        break;
-      }
-      tc::tc_fence_after();
-      const uint32_t ts = trow + TM_S0 + sb * BN;
-      const int key0 = j * BN;
-      // pass 1: row max of the visible scores (log2 units)
-      float mt = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < BN / 16; ++c) {
-        float v[16];
-        tc::tmem_ld16(ts + c * 16, v);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float x = (key0 + c * 16 + i <= qp) ? v[i] * scale_log2 : -INFINITY;
-          mt = fmaxf(mt, x);
-        }
-      }
-      // P buffer free and O stable once the previous P.V has completed
-      if (j >= 1) {
-        if (!__all_sync(0xffffffffu, tc::mbar_wait(pv_done, (j - 1) & 1))) {
-          ok = false;
-          break;
-        }
+      ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(&s_full[sb], (j >> 1) & 1));
+      uint32_t sr[64];
+      if (ok) {
         tc::tc_fence_after();
+        tc::tmem_ld64_nowait(trow + TM_S0 + sb * BN + half * 64, sr);
+        tc::tmem_wait_ld();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&s_free[sb]);   // the MMA may refill this S buffer
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) sr[i] = 0u;
       }
+      const int key0 = j * BN + half * 64;
+      const bool full_row = key0 + 63 <= qp;            // no causal mask in these 64 keys
+      // eight independent partial maxima keep the reduction off one dependency chain
+      float pmx[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) pmx[a] = -INFINITY;
+      if (full_row) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) pmx[i & 7] = fmaxf(pmx[i & 7], __uint_as_float(sr[i]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (key0 + i <= qp) pmx[i & 7] = fmaxf(pmx[i & 7], __uint_as_float(sr[i]));
+      }
+      const float pm = fmaxf(fmaxf(fmaxf(pmx[0], pmx[1]), fmaxf(pmx[2], pmx[3])),
+                             fmaxf(fmaxf(pmx[4], pmx[5]), fmaxf(pmx[6], pmx[7])));
+      float* xm = xmax + (j & 1) * 2 * BM;
+      xm[half * BM + r] = pm;
+      softmax_bar();
+      if (!ok) continue;
+      const float mt = fmaxf(xm[r], xm[BM + r]) * scale_log2;
       const float m_new = fmaxf(m_used, mt);
       if (j == 0) {
         m_used = m_new;
       } else {
         const bool need = m_new > m_used + kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
+          // O must be stable: the previous tile's P.V has completed
+          ok = __all_sync(0xffffffffu, tc::mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1));
+          if (!ok) continue;
+          tc::tc_fence_after();
           const float alpha = need ? tc::ex2_approx(m_used - m_new) : 1.0f;
 #pragma unroll 1
-          for (int c = 0; c < HD / 16; ++c) {
+          for (int c = 0; c < HD / 32; ++c) {
             float o[16];
-            tc::tmem_ld16(trow + TM_O + c * 16, o);
+            tc::tmem_ld16(tO + c * 16, o);
 #pragma unroll
             for (int i = 0; i < 16; ++i) o[i] *= alpha;
-            tc::tmem_st16(trow + TM_O + c * 16, o);
+            tc::tmem_st16(tO + c * 16, o);
           }
           l *= alpha;
           if (need) m_used = m_new;
         }
       }
-      // pass 2: P = exp2(x - m_used) in bf16, row sum of the rounded values, swizzled store
-#pragma unroll 1
-      for (int c = 0; c < BN / 16; ++c) {
-        float v[16];
-        tc::tmem_ld16(ts + c * 16, v);
-        uint32_t pk[8];
+      // P buffer (j & 1) was last read by the P.V of tile j - 2
+      if (j >= 2) {
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(&pv_done[j & 1], ((j - 2) >> 1) & 1));
+        if (!ok) continue;
+      }
+      uint8_t* prow = sP + (j & 1) * L::P_BYTES + half * SLAB + r * 128;
+      const float mo = m_used;
+      float ls[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int k0 = key0 + c * 16 + 2 * i;
-          const float p0 = (k0 <= qp) ? tc::ex2_approx(v[2 * i] * scale_log2 - m_used) : 0.f;
-          const float p1 = (k0 + 1 <= qp) ? tc::ex2_approx(v[2 * i + 1] * scale_log2 - m_used) : 0.f;
+      for (int a = 0; a < 8; ++a) ls[a] = 0.f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int k0 = c * 8 + 2 * i;
+          float p0 = tc::ex2_approx(fmaf(__uint_as_float(sr[k0]), scale_log2, -mo));
+          float p1 = tc::ex2_approx(fmaf(__uint_as_float(sr[k0 + 1]), scale_log2, -mo));
+          if (!full_row) {
+            p0 = (key0 + k0 <= qp) ? p0 : 0.f;
+            p1 = (key0 + k0 + 1 <= qp) ? p1 : 0.f;
+          }
           const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
           const float2 back = __bfloat1622float2(b2);
-          l += back.x + back.y;
+          ls[(2 * i) & 7] += back.x;
+          ls[(2 * i + 1) & 7] += back.y;
           pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
         }
-        // keys c*16 .. c*16+15 are 16-byte chunks 2c and 2c+1 of the row (slab = chunk / 8)
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int chunk = 2 * c + h2;
-          const int slab = chunk >> 3, cc = chunk & 7;
-          uint4* dst = reinterpret_cast<uint4*>(prow + slab * SLAB + ((cc ^ (r & 7)) << 4));
-          *dst = make_uint4(pk[4 * h2], pk[4 * h2 + 1], pk[4 * h2 + 2], pk[4 * h2 + 3]);
-        }
+        // keys 8c .. 8c+7 of this half form 16-byte chunk c of the row in slab `half`
+        uint4* dst = reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4));
+        *dst = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       tc::tc_fence_before();
       tc::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        tc::mbar_arrive(&s_free[sb]);
-        tc::mbar_arrive(p_full);
-      }
+      if (lane == 0) tc::mbar_arrive(&p_full[j & 1]);
     }
-    if (ok && __all_sync(0xffffffffu, tc::mbar_wait(pv_done, (T - 1) & 1))) {
+    const bool done = ok && __all_sync(0xffffffffu, tc::mbar_wait(&pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1));
+    // row sum = both halves' partial sums (every softmax warp reaches this barrier)
+    xsum[half * BM + r] = l;
+    softmax_bar();
+    if (done) {
       tc::tc_fence_after();
-      const float inv = l > 0.f ? 1.0f / l : 0.f;
-      bf16* orow = out + (int64_t)m * H * HD + (int64_t)h * HD;
+      const float lt = xsum[r] + xsum[BM + r];
+      const float inv = lt > 0.f ? 1.0f / lt : 0.f;
+      bf16* orow = out + (int64_t)m * H * HD + (int64_t)h * HD + half * (HD / 2);
 #pragma unroll 1
-      for (int c = 0; c < HD / 16; ++c) {
+      for (int c = 0; c < HD / 32; ++c) {
         float o[16];
-        tc::tmem_ld16(trow + TM_O + c * 16, o);
+        tc::tmem_ld16(tO + c * 16, o);
 #pragma unroll
         for (int i = 0; i < 16; ++i) o[i] *= inv;
         if (m < M) {

@@ -503,12 +503,33 @@ cudaError_t launch_swiglu(int dt, void* out, const void* gu, int64_t M, int F, c
 }
 
 // ------------------------------------------------------------------------ lm_head
-// logits[v] = hn . w[v]; one warp per vocabulary row, 16-byte weight loads.
+// argmax with ties to the lowest index: maximise (ordered float bits, ~index) as a u64
+__device__ __forceinline__ uint32_t ordered_bits(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ unsigned long long argmax_key(float v, int i) {
+  return ((unsigned long long)ordered_bits(v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)i);
+}
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long y = __shfl_xor_sync(0xffffffffu, v, o);
+    v = y > v ? y : v;
+  }
+  return v;
+}
+
+// logits[v] = hn . w[v]; one warp per vocabulary row, 16-byte weight loads.  Each block
+// also leaves the best (logit, lowest index) key of its rows in block_best[blockIdx.x].
 template <typename T>
 __global__ void __launch_bounds__(256) k_lm_gemv(float* __restrict__ logits, const float* __restrict__ hn,
-                                                 const T* __restrict__ w, int V, int d) {
-  const int lane = threadIdx.x & 31;
+                                                 const T* __restrict__ w, int V, int d,
+                                                 unsigned long long* __restrict__ block_best) {
+  __shared__ unsigned long long red[8];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int warps_total = (gridDim.x * blockDim.x) >> 5;
+  unsigned long long best = 0ull;
   for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < V; r += warps_total) {
     const T* wr = w + (int64_t)r * d;
     float acc = 0.f;
@@ -521,54 +542,51 @@ __global__ void __launch_bounds__(256) k_lm_gemv(float* __restrict__ logits, con
     }
     acc = warp_sum(acc);
     if (lane == 0) logits[r] = acc;
+    const unsigned long long key = argmax_key(acc, r);
+    best = key > best ? key : best;
+  }
+  if (lane == 0) red[wid] = best;
+  __syncthreads();
+  if (wid == 0) {
+    unsigned long long b = lane < (int)(blockDim.x >> 5) ? red[lane] : 0ull;
+    b = warp_max_u64(b);
+    if (lane == 0) block_best[blockIdx.x] = b;
   }
 }
 
+static unsigned lm_grid(int V) { return grid_for((int64_t)V * 32, 256); }
+
+size_t lm_block_best_count(int V) { return lm_grid(V); }
+
 cudaError_t launch_lm_gemv(int dt, float* logits, const float* hn, const void* w, int V, int d,
-                           cudaStream_t s) {
-  const unsigned grid = grid_for((int64_t)V * 32, 256);
+                           unsigned long long* block_best, cudaStream_t s) {
+  const unsigned grid = lm_grid(V);
   if (dt == DT_BF16)
-    k_lm_gemv<bf16><<<grid, 256, 0, s>>>(logits, hn, (const bf16*)w, V, d);
+    k_lm_gemv<bf16><<<grid, 256, 0, s>>>(logits, hn, (const bf16*)w, V, d, block_best);
   else
-    k_lm_gemv<float><<<grid, 256, 0, s>>>(logits, hn, (const float*)w, V, d);
+    k_lm_gemv<float><<<grid, 256, 0, s>>>(logits, hn, (const float*)w, V, d, block_best);
   return cudaGetLastError();
 }
 
-// argmax with ties to the lowest index: maximise (ordered float bits, ~index) as a u64
-__device__ __forceinline__ uint32_t ordered_bits(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__global__ void __launch_bounds__(1024) k_argmax(const float* __restrict__ logits, int V, int32_t* token) {
+// token = index of the largest block key
+__global__ void __launch_bounds__(1024) k_argmax_keys(const unsigned long long* __restrict__ keys, int n,
+                                                      int32_t* token) {
   __shared__ unsigned long long red[32];
   unsigned long long best = 0ull;
-  for (int i = threadIdx.x; i < V; i += blockDim.x) {
-    const unsigned long long key =
-        ((unsigned long long)ordered_bits(logits[i]) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)i);
-    best = key > best ? key : best;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
-    best = y > best ? y : best;
-  }
+  for (int i = threadIdx.x; i < n; i += blockDim.x) best = keys[i] > best ? keys[i] : best;
+  best = warp_max_u64(best);
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   if (lane == 0) red[w] = best;
   __syncthreads();
   if (w == 0) {
     best = lane < (int)(blockDim.x >> 5) ? red[lane] : 0ull;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
-      best = y > best ? y : best;
-    }
+    best = warp_max_u64(best);
     if (lane == 0) token[0] = (int32_t)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
   }
 }
 
-cudaError_t launch_argmax(const float* logits, int V, int32_t* token, cudaStream_t s) {
-  k_argmax<<<1, 1024, 0, s>>>(logits, V, token);
+cudaError_t launch_argmax_keys(const unsigned long long* keys, int n, int32_t* token, cudaStream_t s) {
+  k_argmax_keys<<<1, 1024, 0, s>>>(keys, n, token);
   return cudaGetLastError();
 }
 

@@ -275,6 +275,20 @@ int cb_lmhead_argmax(const void* h, const void* final_norm, const void* w_lm,
                      const cb_dims* dims, float* logits, int32_t* token, void* ws,
                      size_t ws_bytes, void* stream);
 
+/* ---- layer-ahead loading ------------------------------------------------------------ */
+
+/* Starts the copy of one layer's cached chunk KV from pinned host memory to the device on
+ * `side_stream` and records `done_event` (a cudaEvent_t) behind it, so the next layer's KV
+ * loads while the current layer recomputes ([CB-A] §Pipelining and load controller: layer
+ * i+1's KV is fetched during layer i's selective recompute; [CB-B] §ロードと再計算を重ねる).
+ * dev_dst and pinned_src must not overlap; bytes may be 0. */
+int cb_prefetch_layer(void* dev_dst, const void* pinned_src, size_t bytes, void* side_stream,
+                      void* done_event);
+
+/* Makes `stream` wait (on the device, without blocking the host) for `event`, typically the
+ * done_event of cb_prefetch_layer, before its next launch. */
+int cb_stream_wait(void* stream, void* event);
+
 /* ---- launch accounting and per-launch timing ---------------------------------------- */
 
 /* Kernel families reported by the profiler. */

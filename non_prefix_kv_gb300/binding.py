@@ -75,6 +75,8 @@ _PROTOS = {
                                   C.POINTER(_P), C.POINTER(_P), _P, _P, _P, _I32, _P, _SZ, _P]),
     "cb_lmhead_argmax": (C.c_int, [_P, _P, _P, C.POINTER(cb_dims), _P, _P, _P, _SZ, _P]),
     "cb_linear": (C.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _P]),
+    "cb_prefetch_layer": (C.c_int, [_P, _P, _SZ, _P, _P]),
+    "cb_stream_wait": (C.c_int, [_P, _P]),
     "cb_kernel_launch_count": (_I64, []),
     "cb_profile_begin": (C.c_int, [_I32]),
     "cb_profile_end": (C.c_int, [C.POINTER(cb_prof_record), _I32, C.POINTER(_I32)]),
@@ -258,3 +260,16 @@ def cb_profile_end(max_records: int = 4096):
     _check("cb_profile_end", lib().cb_profile_end(arr, max_records, C.byref(n)))
     return [{"kind": PROF_KINDS.get(r.kind, str(r.kind)), "aux": r.aux, "m": r.m, "n": r.n, "k": r.k,
              "flops": r.flops, "bytes": r.bytes, "ms": r.ms} for r in arr[:n.value]]
+
+
+def _event(ev) -> int:
+    return ev if isinstance(ev, int) else ev.cuda_event
+
+
+def cb_prefetch_layer(dev_dst, pinned_src, nbytes: int, side_stream, done_event):
+    _check("cb_prefetch_layer", lib().cb_prefetch_layer(_ptr(dev_dst), _ptr(pinned_src), nbytes,
+                                                        _stream(side_stream), _event(done_event)))
+
+
+def cb_stream_wait(stream, event):
+    _check("cb_stream_wait", lib().cb_stream_wait(_stream(stream), _event(event)))

@@ -685,6 +685,23 @@ int cb_linear(const void* x, const void* w, void* y, int32_t M, int32_t N, int32
   return CB_OK;
 }
 
+int cb_prefetch_layer(void* dev_dst, const void* pinned_src, size_t bytes, void* side_stream, void* done_event) {
+  if (bytes > 0 && (!dev_dst || !pinned_src)) return fail(CB_ERR_INVALID_ARG, "prefetch pointer is NULL");
+  if (!done_event) return fail(CB_ERR_INVALID_ARG, "done_event is NULL");
+  const char* d = static_cast<const char*>(dev_dst);
+  const char* h = static_cast<const char*>(pinned_src);
+  if (bytes > 0 && d < h + bytes && h < d + bytes) return fail(CB_ERR_INVALID_ARG, "source and destination overlap");
+  if (bytes > 0) CB_CUDA(cudaMemcpyAsync(dev_dst, pinned_src, bytes, cudaMemcpyHostToDevice, S(side_stream)));
+  CB_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(done_event), S(side_stream)));
+  return CB_OK;
+}
+
+int cb_stream_wait(void* stream, void* event) {
+  if (!event) return fail(CB_ERR_INVALID_ARG, "event is NULL");
+  CB_CUDA(cudaStreamWaitEvent(S(stream), static_cast<cudaEvent_t>(event), 0));
+  return CB_OK;
+}
+
 int64_t cb_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int cb_profile_begin(int32_t max_records) {

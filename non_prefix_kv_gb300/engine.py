@@ -184,26 +184,53 @@ def layer_plan(shape: ModelShape, n_tok: int, n_cached: int, ratios: Sequence[Op
     return plan
 
 
+class HostPool:
+    """The chunk-KV pool kept in pinned host memory (the storage tier of the pages' design),
+    with a side stream and one event per layer for layer-ahead loading."""
+
+    def __init__(self, pool: ChunkPool):
+        self.k = [t.cpu().pin_memory() for t in pool.k]
+        self.v = [t.cpu().pin_memory() for t in pool.v]
+        self.side = torch.cuda.Stream()
+        self.done = [torch.cuda.Event() for _ in pool.k]
+        self.nbytes = sum(t.numel() * t.element_size() for t in self.k + self.v)
+
+
 def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None, keep_history=False,
-              assemble: bool = True, stream=None):
+              assemble: bool = True, stream=None, host_pool: Optional[HostPool] = None):
     """One blended prefill: re-position the chunk KV of every layer, run the layer plan,
-    then the lm_head argmax.  Returns the number of rows carried out of the last layer."""
+    then the lm_head argmax.  Returns the number of rows carried out of the last layer.
+
+    With host_pool, every layer's chunk KV is first copied from pinned host memory on a
+    side stream, all layers queued up front; layer l waits only for its own copy, so the
+    load of layer l+1 overlaps the recompute of layer l."""
     eng = req.eng
     dm = eng.dm
     s = dm.shape
     dims = dm.dims
     esz = 2 if s.dtype == "bf16" else 4
-    if assemble:
+    if host_pool is not None:
+        main = torch.cuda.current_stream() if stream is None else stream
+        host_pool.side.wait_stream(main)          # the device pool is free once prior work is done
+        for l in range(s.n_layers):
+            nk = host_pool.k[l].numel() * host_pool.k[l].element_size()
+            B.cb_prefetch_layer(req.pool.k[l], host_pool.k[l], nk, host_pool.side, host_pool.done[l])
+            B.cb_prefetch_layer(req.pool.v[l], host_pool.v[l], nk, host_pool.side, host_pool.done[l])
+    B.cb_gather_rows(req.x[0], dm.embed, req.tokens, req.N, s.d_model * esz, stream)
+    if assemble and host_pool is None:
         for l in range(s.n_layers):
             B.cb_rope_shift(req.K[l], req.V[l], req.pool.k[l], req.pool.v[l], req.src_row, req.delta,
                             req.n_cached, dims, eng.cos_sin, eng.max_pos, stream)
-    B.cb_gather_rows(req.x[0], dm.embed, req.tokens, req.N, s.d_model * esz, stream)
     cur = 0
     m_in = req.N
     s_in = None
     if keep_history:
         req.sel_hist, req.m_hist = [], []
     for l, (mode, k) in enumerate(plan):
+        if assemble and host_pool is not None:
+            B.cb_stream_wait(stream, host_pool.done[l])
+            B.cb_rope_shift(req.K[l], req.V[l], req.pool.k[l], req.pool.v[l], req.src_row, req.delta,
+                            req.n_cached, dims, eng.cos_sin, eng.max_pos, stream)
         ov = None if sel_override is None else sel_override.get(l)
         m_out = B.cb_blend_layer(dims, dm.layers_c[l], mode, req.x[cur], s_in, m_in, req.N, req.n_cached,
                                  req.K[l], req.V[l], eng.cos_sin, eng.max_pos, k, dev_mode, ov,

@@ -134,3 +134,33 @@ def test_blend_bf16_gqa(E):
     wl = synth.Workload("bf16_gqa", shape, chunk_len=160, n_distinct=3, order=(0, 1, 2, 1), n_query=48,
                         ratio=0.2)
     run_case(E, wl, 0.2, True, TOL["bf16"], check_sets=False)
+
+
+def test_layer_ahead_loading_matches_resident_pool(E):
+    """Loading every layer's chunk KV from pinned host memory on a side stream, one event per
+    layer, gives bit-identical results to the device-resident pool."""
+    torch = torch_mod()
+    from non_prefix_kv_gb300 import binding as B
+    wl = synth.Workload("bf16_small", BF16_SMALL, chunk_len=96, n_distinct=4, order=(0, 1, 2, 3), n_query=32,
+                        ratio=0.15)
+    model = synth.make_model(wl.shape, seed=1)
+    req_h = synth.make_requests(wl)[0]
+    dm = E.DeviceModel.from_host(model)
+    eng = E.BlendEngine(dm, wl.n_tokens)
+    pool = eng.precompute_pool(req_h.chunk_tokens)
+    hp = E.HostPool(pool)
+    plan = E.layer_plan(wl.shape, wl.n_tokens, wl.n_cached, [None, 0.15, 0.15])
+    a = E.Request(eng, pool, req_h.order, req_h.tokens)
+    E.run_blend(a, plan)
+    B.cb_sync(None)
+    ka = [t.clone() for t in a.K]
+    xa = a.x_last[:a.m_last].clone()
+    ta = int(a.token.item())
+    for t in pool.k + pool.v:        # the streamed run must reload the whole pool
+        t.zero_()
+    b = E.Request(eng, pool, req_h.order, req_h.tokens)
+    E.run_blend(b, plan, host_pool=hp)
+    B.cb_sync(None)
+    for l in range(wl.shape.n_layers):
+        assert torch.equal(ka[l], b.K[l])
+    assert torch.equal(xa, b.x_last[:b.m_last]) and ta == int(b.token.item())

@@ -1,0 +1,122 @@
+"""Parity at the benchmark's full size: the 7B-shaped three-layer shared-weight stack over
+4096 tokens (6 chunks x 640 + 256 query, r = 15 %), run by the same engine calls the
+benchmark replays.  The oracle cannot run the whole blend at this size in seconds, so the
+checks are (a) outputs it can compute one piece at a time and (b) properties that hold at
+any size."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle.cacheblend_oracle as O
+from non_prefix_kv_gb300 import synth
+from tests.gpu_util import ensure_lib, host, rel, torch_mod
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def setup():
+    torch = torch_mod()
+    ensure_lib()
+    from non_prefix_kv_gb300 import binding as B
+    from non_prefix_kv_gb300 import engine as E
+    wl = synth.WORKLOADS["llama7b_layer_4k"]
+    model = synth.make_model(wl.shape, seed=wl.seed)
+    req_h = synth.make_requests(wl)[0]
+    dm = E.DeviceModel.from_host(model)
+    eng = E.BlendEngine(dm, wl.n_tokens)
+    pool = eng.precompute_pool(req_h.chunk_tokens)
+    ratios = O.ratio_schedule(wl.ratio, wl.shape.n_layers, wl.check_layer, wl.gradual)
+    plan = E.layer_plan(wl.shape, wl.n_tokens, wl.n_cached, ratios)
+    req = E.Request(eng, pool, req_h.order, req_h.tokens)
+    E.run_blend(req, plan, keep_history=True)
+    B.cb_sync(None)
+    one_layer = dict(model, shape=dataclasses.replace(wl.shape, n_layers=1), layers=model["layers"][:1])
+    return dict(torch=torch, B=B, E=E, wl=wl, model=model, one_layer=one_layer, req_h=req_h, dm=dm, eng=eng,
+                pool=pool, plan=plan, req=req)
+
+
+def test_chunk_precompute_matches_oracle(setup):
+    """KV^pre of the first chunk through all three layers (the layers share weights)."""
+    s = setup
+    ref = O.full_prefill(s["model"], s["req_h"].chunk_tokens[0], 0)
+    n = s["pool"].lens[0]
+    for l in range(s["wl"].shape.n_layers):
+        assert rel(host(s["pool"].k[l][:n]), ref["K"][l].reshape(n, -1)) < 1e-2
+        assert rel(host(s["pool"].v[l][:n]), ref["V"][l].reshape(n, -1)) < 1e-2
+
+
+def test_repositioned_chunk_keys_match_oracle(setup):
+    """The second slot's cached keys are its chunk's local-position keys re-rotated by 640."""
+    s = setup
+    c = s["req_h"].order[1]
+    ref = O.full_prefill(s["one_layer"], s["req_h"].chunk_tokens[c], 0)
+    n = s["pool"].lens[c]
+    want = O.rope_shift(ref["K"][0], 640, s["wl"].shape.rope_base).reshape(n, -1)
+    got = host(s["req"].K[0][640:640 + n])
+    assert rel(got, want) < 1e-2
+    # values are copied untouched (layer 0 is never recomputed for cached rows)
+    off = s["pool"].offsets[c]
+    np.testing.assert_array_equal(host(s["req"].V[0][640:640 + n]), host(s["pool"].v[0][off:off + n]))
+
+
+def test_precheck_layer_prefix_rows_match_oracle(setup):
+    """Layer 0 runs every row; rows of the first chunk only see the first chunk, so their
+    output equals a one-layer prefill of that chunk alone."""
+    s = setup
+    torch, B, E = s["torch"], s["B"], s["E"]
+    req = s["req"]
+    x0 = torch.empty_like(req.x[0])
+    B.cb_gather_rows(x0, s["dm"].embed, req.tokens, req.N, s["wl"].shape.d_model * 2)
+    x1 = torch.empty_like(req.x[0])
+    s_out = torch.empty(req.N, dtype=torch.int32, device="cuda")
+    Kc = [t.clone() for t in req.K]
+    Vc = [t.clone() for t in req.V]
+    m = B.cb_blend_layer(s["dm"].dims, s["dm"].layers_c[0], B.CB_LAYER_PRECHECK, x0, None, req.N, req.N,
+                         req.n_cached, Kc[0], Vc[0], s["eng"].cos_sin, s["eng"].max_pos, 0, 0, None, x1, s_out,
+                         None, s["eng"].ws)
+    B.cb_sync(None)
+    assert m == req.N
+    ref = O.full_prefill(s["one_layer"], s["req_h"].chunk_tokens[s["req_h"].order[0]], 0)
+    rows = [0, 1, 17, 128, 333, 639]
+    assert rel(host(x1[rows]), ref["x"][1][rows]) < 1e-2
+
+
+def test_selection_structure_and_true_prefix(setup):
+    s = setup
+    req, wl = s["req"], s["wl"]
+    N, n_c = wl.n_tokens, wl.n_cached
+    k = O.budget(n_c, wl.ratio, n_c)
+    assert s["plan"][1][1] == k == 576
+    for l in (1, 2):
+        S = req.sel_hist[l].cpu().numpy()
+        assert len(S) == k + (N - n_c) == 832
+        assert np.all(np.diff(S) > 0)
+        np.testing.assert_array_equal(S[-(N - n_c):], np.arange(n_c, N))
+        # the first chunk is a true prefix: identical KV, score exactly 0, never selected
+        assert not np.any(S < 640)
+    np.testing.assert_array_equal(req.sel_hist[1].cpu().numpy(), req.sel_hist[2].cpu().numpy())
+    sc = req.scores[:n_c].cpu().numpy()
+    assert np.all(sc[:640] == 0.0) and np.all(sc[640:] > 0.0)
+    # the top-k rows are exactly the k largest of the kernel's own scores, ties to the lower row
+    want = np.sort(np.lexsort((np.arange(n_c), -sc.astype(np.float64)))[:k])
+    np.testing.assert_array_equal(req.sel_hist[1].cpu().numpy()[:k], want)
+
+
+def test_zero_ratio_keeps_the_rerotated_cache_bit_exact(setup):
+    s = setup
+    torch, B, E = s["torch"], s["B"], s["E"]
+    req = E.Request(s["eng"], s["pool"], s["req_h"].order, s["req_h"].tokens)
+    ratios0 = O.ratio_schedule(0.0, s["wl"].shape.n_layers, 1, False)
+    plan0 = E.layer_plan(s["wl"].shape, req.N, req.n_cached, ratios0)
+    E.run_blend(req, plan0)
+    B.cb_sync(None)
+    for l in range(s["wl"].shape.n_layers):
+        kd = torch.empty(req.n_cached, s["wl"].shape.kv_width, dtype=torch.bfloat16, device="cuda")
+        vd = torch.empty_like(kd)
+        B.cb_rope_shift(kd, vd, s["pool"].k[l], s["pool"].v[l], req.src_row, req.delta, req.n_cached,
+                        s["dm"].dims, s["eng"].cos_sin, s["eng"].max_pos)
+        B.cb_sync(None)
+        assert torch.equal(req.K[l][:req.n_cached], kd)
+        assert torch.equal(req.V[l][:req.n_cached], vd)

@@ -461,7 +461,7 @@ def our_arm(args):
         e2e = {"value": wl.n_tokens / res[True], "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": 4, "ttft_ms": res[True] * 1e3, "first_token": int(out_tok.item()),
                "layer_ahead_loading": True, "ttft_ms_without_overlap": res[False] * 1e3,
-               "h2d_gbs_without_overlap": h2d / res[False] / 1e9}
+               "h2d_gbs_serial": h2d / max(res[False] - ms / 1e3 / len(reqs), 1e-6) / 1e9}
     B.cb_sync(stream, 120.0)
 
     # ---------------- CPU oracle baseline (rank 0, N = 1 only)

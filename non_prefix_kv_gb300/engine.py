@@ -193,6 +193,8 @@ class HostPool:
         self.v = [t.cpu().pin_memory() for t in pool.v]
         self.side = torch.cuda.Stream()
         self.done = [torch.cuda.Event() for _ in pool.k]
+        for ev in self.done:          # torch creates the CUDA event on its first record
+            ev.record(self.side)
         self.nbytes = sum(t.numel() * t.element_size() for t in self.k + self.v)
 
 

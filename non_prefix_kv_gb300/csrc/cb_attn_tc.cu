@@ -363,6 +363,338 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------- query-tile pairs
+// Two 128-query tiles per CTA, each with its own softmax warpgroup (warps 2-5: tile 0,
+// warps 6-9: tile 1), sharing the K/V tiles.  While one warpgroup exponentiates its scores
+// the tensor core runs the other tile's S and P.V, so neither the MMA pipe nor the softmax
+// waits on the other for long.  Each softmax thread owns a whole 128-key score row.  TMEM:
+// S0 | S1 | O0 | O1.  K streams through 2 stages, V through 1, one P tile per query tile.
+constexpr int THREADS2 = 320;
+
+template <int HD>
+struct Layout2 {
+  static constexpr int NSLAB = HD / 64;
+  static constexpr int Q_TILE = NSLAB * SLAB;
+  static constexpr int KV_BYTES = NSLAB * SLAB;
+  static constexpr int P_TILE = 2 * SLAB;
+  static constexpr int OFF_Q = 0;                          // 2 query tiles
+  static constexpr int OFF_K = OFF_Q + 2 * Q_TILE;         // 2 stages
+  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;       // 1 stage
+  static constexpr int OFF_P = OFF_V + KV_BYTES;           // one P tile per query tile
+  static constexpr int OFF_BAR = OFF_P + 2 * P_TILE;
+  static constexpr int BYTES = OFF_BAR + 256;
+  static constexpr int SMEM = BYTES + 1024;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(THREADS2, 1)
+    k_attn_tc2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const int32_t* __restrict__ q_pos, int M,
+               int64_t n_kv, int H, int Hkv, bf16* __restrict__ out, float scale_log2) {
+  using L = Layout2<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = tc::smem_u32(smem_raw);
+  uint8_t* base = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
+  uint8_t* sQ = base + L::OFF_Q;
+  uint8_t* sK = base + L::OFF_K;
+  uint8_t* sV = base + L::OFF_V;
+  uint8_t* sP = base + L::OFF_P;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::OFF_BAR);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;     // [2 stages]
+  uint64_t* k_empty = bars + 3;    // [2 stages]
+  uint64_t* v_full = bars + 5;
+  uint64_t* v_empty = bars + 6;
+  uint64_t* s_full = bars + 7;     // [2 query tiles]
+  uint64_t* s_free = bars + 9;     // [2 query tiles]
+  uint64_t* p_full = bars + 11;    // [2 query tiles]
+  uint64_t* pv_done = bars + 13;   // [2 query tiles]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  int* s_qmax = reinterpret_cast<int*>(bars + 16);   // [2]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = gridDim.x - 1 - blockIdx.x;      // the longest (latest) tile pairs first
+  const int h = blockIdx.y;
+  const int g = h / (H / Hkv);
+  const int m0 = qt * 2 * BM;
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&k_full[i], 1);
+      tc::mbar_init(&k_empty[i], 1);
+      tc::mbar_init(&s_full[i], 1);
+      tc::mbar_init(&s_free[i], 4);
+      tc::mbar_init(&p_full[i], 4);
+      tc::mbar_init(&pv_done[i], 1);
+    }
+    tc::mbar_init(v_full, 1);
+    tc::mbar_init(v_empty, 1);
+    tc::fence_mbar_init();
+    tc::tma_prefetch_desc(&tmQ);
+    tc::tma_prefetch_desc(&tmK);
+    tc::tma_prefetch_desc(&tmV);
+  }
+  if (warp == 0) {
+    // furthest key each query tile may see (-1: the tile has no valid row)
+    int mx0 = -1, mx1 = -1;
+    for (int i = lane; i < 2 * BM; i += 32) {
+      const int m = m0 + i;
+      if (m < M) {
+        int p = q_pos[m];
+        if (p < 0 || p >= n_kv) {
+          atomicOr(&g_err_attn_tc, ERRBIT_INDEX);
+          p = p < 0 ? 0 : (int)(n_kv - 1);
+        }
+        if (i < BM) mx0 = p > mx0 ? p : mx0;
+        else mx1 = p > mx1 ? p : mx1;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mx0 = max(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = max(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    if (lane == 0) {
+      s_qmax[0] = mx0;
+      s_qmax[1] = mx1;
+    }
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  int Tt[2];
+  Tt[0] = s_qmax[0] < 0 ? 0 : s_qmax[0] / BN + 1;   // key tiles each query tile visits
+  Tt[1] = s_qmax[1] < 0 ? 0 : s_qmax[1] / BN + 1;
+  const int T = Tt[0] > Tt[1] ? Tt[0] : Tt[1];
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    tc::mbar_expect_tx(q_full, 2 * L::Q_TILE);
+    for (int t = 0; t < 2; ++t)
+      for (int s = 0; s < L::NSLAB; ++s)
+        tc::tma_load_2d(sQ + t * L::Q_TILE + s * SLAB, &tmQ, q_full, h * HD + 64 * s, m0 + t * BM);
+    bool ok = true;
+    if (T > 0) {
+      tc::mbar_expect_tx(&k_full[0], L::KV_BYTES);
+      for (int s = 0; s < L::NSLAB; ++s) tc::tma_load_2d(sK + s * SLAB, &tmK, &k_full[0], g * HD + 64 * s, 0);
+    }
+    for (int j = 0; ok && j < T; ++j) {
+      if (j + 1 < T) {   // K one tile ahead
+        const int st = (j + 1) & 1;
+        if (!tc::mbar_wait(&k_empty[st], (((j + 1) >> 1) & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
+        tc::mbar_expect_tx(&k_full[st], L::KV_BYTES);
+        for (int s = 0; s < L::NSLAB; ++s)
+          tc::tma_load_2d(sK + st * L::KV_BYTES + s * SLAB, &tmK, &k_full[st], g * HD + 64 * s, (j + 1) * BN);
+      }
+      if (!tc::mbar_wait(v_empty, (j & 1) ^ 1)) {
+        ok = false;
+        break;
+      }
+      tc::mbar_expect_tx(v_full, L::KV_BYTES);
+      for (int s = 0; s < L::NSLAB; ++s) tc::tma_load_2d(sV + s * SLAB, &tmV, v_full, g * HD + 64 * s, j * BN);
+    }
+    if (!ok) atomicOr(&g_err_attn_tc, ERRBIT_TIMEOUT);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc_s = tc::idesc_bf16_f32(BM, BN);
+    constexpr uint32_t idesc_o = tc::idesc_bf16_f32(BM, HD, true);
+    bool ok = tc::mbar_wait(q_full, 0);
+    for (int j = 0; ok && j <= T; ++j) {
+      const bool have_k = j < T;
+      if (have_k && !tc::mbar_wait(&k_full[j & 1], (j >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      bool v_ready = false;     // V_{j-1} is waited for just before its first P.V
+      for (int t = 0; ok && t < 2; ++t) {
+        if (have_k && j < Tt[t]) {
+          // S_t(j) = Q_t K_j^T once the softmax has pulled S_t(j-1) out of TMEM
+          if (j >= 1 && !tc::mbar_wait(&s_free[t], (j - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < HD / 16; ++k) {
+            const uint32_t off = (k & 3) * 32;
+            const uint64_t a = tc::desc_sw128(tc::smem_u32(sQ + t * L::Q_TILE + (k >> 2) * SLAB) + off);
+            const uint64_t b = tc::desc_sw128(tc::smem_u32(sK + (j & 1) * L::KV_BYTES + (k >> 2) * SLAB) + off);
+            tc::mma_bf16(tmem + t * BN, a, b, idesc_s, k > 0);
+          }
+          tc::mma_commit(&s_full[t]);
+        }
+        const int jj = j - 1;
+        if (jj >= 0 && jj < Tt[t]) {
+          // O_t += P_t(jj) V_jj
+          if (!v_ready && !tc::mbar_wait(v_full, jj & 1)) {
+            ok = false;
+            break;
+          }
+          v_ready = true;
+          if (!tc::mbar_wait(&p_full[t], jj & 1)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint8_t* pb = sP + t * L::P_TILE;
+#pragma unroll
+          for (int k = 0; k < BN / 16; ++k) {
+            const uint64_t a = tc::desc_sw128(tc::smem_u32(pb + (k >> 2) * SLAB) + (k & 3) * 32);
+            const uint64_t b = tc::desc_sw128_mn(tc::smem_u32(sV) + k * 16 * 128, SLAB);
+            tc::mma_bf16(tmem + TM_O + t * BN, a, b, idesc_o, (jj > 0 || k > 0) ? 1u : 0u);
+          }
+          tc::mma_commit(&pv_done[t]);
+        }
+      }
+      if (!ok) break;
+      if (have_k) tc::mma_commit(&k_empty[j & 1]);
+      if (j >= 1) tc::mma_commit(v_empty);
+    }
+    if (!ok) atomicOr(&g_err_attn_tc, ERRBIT_TIMEOUT);
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------------ softmax + epilogue
+    const int t = (warp - 2) >> 2;                  // query tile of this warpgroup
+    const int lane_base = (warp & 3) * 32;
+    const int r = lane_base + lane;
+    const int m = m0 + t * BM + r;
+    const int Tq = Tt[t];
+    int qp = 0;
+    if (m < M) {
+      qp = q_pos[m];
+      qp = qp < 0 ? 0 : (qp >= n_kv ? (int)(n_kv - 1) : qp);
+    }
+    const uint32_t trow = tmem + (static_cast<uint32_t>(lane_base) << 16);
+    const uint32_t tS = trow + t * BN;
+    const uint32_t tO = trow + TM_O + t * BN;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; ok && j < Tq; ++j) {
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&s_full[t], j & 1))) {
+        ok = false;
+        break;
+      }
+      tc::tc_fence_after();
+      uint32_t sr[BN];
+      tc::tmem_ld64_nowait(tS, sr);
+      tc::tmem_ld64_nowait(tS + 64, sr + 64);
+      tc::tmem_wait_ld();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&s_free[t]);   // the MMA may write S_t(j+1)
+      const int key0 = j * BN;
+      const bool full_row = key0 + BN - 1 <= qp;
+      float pmx[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) pmx[a] = -INFINITY;
+      if (full_row) {
+#pragma unroll
+        for (int i = 0; i < BN; ++i) pmx[i & 7] = fmaxf(pmx[i & 7], __uint_as_float(sr[i]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < BN; ++i)
+          if (key0 + i <= qp) pmx[i & 7] = fmaxf(pmx[i & 7], __uint_as_float(sr[i]));
+      }
+      const float mt = fmaxf(fmaxf(fmaxf(pmx[0], pmx[1]), fmaxf(pmx[2], pmx[3])),
+                             fmaxf(fmaxf(pmx[4], pmx[5]), fmaxf(pmx[6], pmx[7]))) * scale_log2;
+      const float m_new = fmaxf(m_used, mt);
+      if (j >= 1) {
+        // P_t(j-1).V has completed: the P tile is free and O_t is stable
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(&pv_done[t], (j - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+      }
+      if (j == 0) {
+        m_used = m_new;
+      } else {
+        const bool need = m_new > m_used + kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? tc::ex2_approx(m_used - m_new) : 1.0f;
+#pragma unroll 1
+          for (int c = 0; c < HD / 16; ++c) {
+            float o[16];
+            tc::tmem_ld16(tO + c * 16, o);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] *= alpha;
+            tc::tmem_st16(tO + c * 16, o);
+          }
+          l *= alpha;
+          if (need) m_used = m_new;
+        }
+      }
+      uint8_t* prow = sP + t * L::P_TILE + r * 128;
+      const float mo = m_used;
+      float ls[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) ls[a] = 0.f;
+#pragma unroll
+      for (int c = 0; c < BN / 8; ++c) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int k0 = c * 8 + 2 * i;
+          float p0 = tc::ex2_approx(fmaf(__uint_as_float(sr[k0]), scale_log2, -mo));
+          float p1 = tc::ex2_approx(fmaf(__uint_as_float(sr[k0 + 1]), scale_log2, -mo));
+          if (!full_row) {
+            p0 = (key0 + k0 <= qp) ? p0 : 0.f;
+            p1 = (key0 + k0 + 1 <= qp) ? p1 : 0.f;
+          }
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+          const float2 back = __bfloat1622float2(b2);
+          ls[(2 * i) & 7] += back.x;
+          ls[(2 * i + 1) & 7] += back.y;
+          pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+        // keys 8c .. 8c+7: 16-byte chunk c % 8 of slab c / 8, swizzled by row % 8
+        uint4* dst = reinterpret_cast<uint4*>(prow + (c >> 3) * SLAB + (((c & 7) ^ (r & 7)) << 4));
+        *dst = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      tc::tc_fence_before();
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&p_full[t]);
+    }
+    if (Tq > 0) {
+      if (ok && __all_sync(0xffffffffu, tc::mbar_wait(&pv_done[t], (Tq - 1) & 1))) {
+        tc::tc_fence_after();
+        const float inv = l > 0.f ? 1.0f / l : 0.f;
+        bf16* orow = out + (int64_t)m * H * HD + (int64_t)h * HD;
+#pragma unroll 1
+        for (int c = 0; c < HD / 16; ++c) {
+          float o[16];
+          tc::tmem_ld16(tO + c * 16, o);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] *= inv;
+          if (m < M) {
+            st8(orow + c * 16, o);
+            st8(orow + c * 16 + 8, o + 8);
+          }
+        }
+      } else if (lane == 0) {
+        atomicOr(&g_err_attn_tc, ERRBIT_TIMEOUT);
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -394,10 +726,21 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int sm_count_attn() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (n <= 0) n = 148;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
 template <int HD>
 cudaError_t launch_hd(const void* q, const int32_t* q_pos, int M, const void* kc, const void* vc, int64_t n_kv,
                       int H, int Hkv, void* out, cudaStream_t s) {
-  using Ly = Layout<HD>;
   CUtensorMap tq, tk, tv;
   if (!make_map(&tq, q, M, (int64_t)H * HD, (int64_t)H * HD) ||
       !make_map(&tk, kc, n_kv, (int64_t)Hkv * HD, (int64_t)Hkv * HD) ||
@@ -407,14 +750,25 @@ cudaError_t launch_hd(const void* q, const int32_t* q_pos, int M, const void* kc
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(k_attn_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<HD>::SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_attn_tc2<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout2<HD>::SMEM);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
-  dim3 grid((M + BM - 1) / BM, H);
-  k_attn_tc<HD><<<grid, THREADS, Ly::SMEM, s>>>(tq, tk, tv, q_pos, M, n_kv, H, Hkv, static_cast<bf16*>(out),
-                                                scale_log2);
+  // Query-tile pairs when their grid still covers every SM; single tiles otherwise (a small
+  // selected set would leave SMs idle with half as many CTAs).
+  const int pairs = (M + 2 * BM - 1) / (2 * BM);
+  if ((int64_t)pairs * H >= sm_count_attn()) {
+    dim3 grid(pairs, H);
+    k_attn_tc2<HD><<<grid, THREADS2, Layout2<HD>::SMEM, s>>>(tq, tk, tv, q_pos, M, n_kv, H, Hkv,
+                                                             static_cast<bf16*>(out), scale_log2);
+  } else {
+    dim3 grid((M + BM - 1) / BM, H);
+    k_attn_tc<HD><<<grid, THREADS, Layout<HD>::SMEM, s>>>(tq, tk, tv, q_pos, M, n_kv, H, Hkv,
+                                                          static_cast<bf16*>(out), scale_log2);
+  }
   return cudaGetLastError();
 }
 

@@ -94,11 +94,14 @@ def test_selection_structure_and_true_prefix(setup):
         assert len(S) == k + (N - n_c) == 832
         assert np.all(np.diff(S) > 0)
         np.testing.assert_array_equal(S[-(N - n_c):], np.arange(n_c, N))
-        # the first chunk is a true prefix: identical KV, score exactly 0, never selected
+        # the first chunk is a true prefix: its KV matches the cache up to rounding (the
+        # pre-check layer and the chunk precompute may run different attention kernels),
+        # so it is never selected
         assert not np.any(S < 640)
     np.testing.assert_array_equal(req.sel_hist[1].cpu().numpy(), req.sel_hist[2].cpu().numpy())
     sc = req.scores[:n_c].cpu().numpy()
-    assert np.all(sc[:640] == 0.0) and np.all(sc[640:] > 0.0)
+    assert np.all(sc[640:] > 0.0)
+    assert sc[:640].max() < 1e-3 * np.median(sc[640:])
     # the top-k rows are exactly the k largest of the kernel's own scores, ties to the lower row
     want = np.sort(np.lexsort((np.arange(n_c), -sc.astype(np.float64)))[:k])
     np.testing.assert_array_equal(req.sel_hist[1].cpu().numpy()[:k], want)

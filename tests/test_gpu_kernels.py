@@ -307,6 +307,29 @@ def test_partial_attention_bf16_tensor_cores(B, H, Hkv, hd, M, N, qstd, order):
     assert rel(host(out), want) < 5e-3
 
 
+@pytest.mark.parametrize("H,Hkv,hd,M,N", [(32, 8, 128, 1100, 3000), (40, 40, 64, 1000, 1000),
+                                          (32, 32, 128, 4096, 4096)])
+def test_partial_attention_query_tile_pairs(B, H, Hkv, hd, M, N):
+    """Shapes whose (256-query pair x head) grid covers every SM take the two-tile kernel:
+    a last pair whose second tile is empty, GQA, shuffled positions, full causal."""
+    torch = torch_mod()
+    shape = synth.ModelShape(1, 256, H, Hkv, hd, 256, 64, dtype="bf16")
+    dims = dims_for(B, shape)
+    g = synth.rng(H + M, synth.P_NOISE)
+    K = synth.test_tensor((N, Hkv * hd), 77, dtype="bf16")
+    V = synth.test_tensor((N, Hkv * hd), 78, dtype="bf16")
+    q = synth.test_tensor((M, H * hd), 79, std=1.0, dtype="bf16")
+    q_pos = np.sort(g.choice(N, M, replace=False)).astype(np.int32) if M < N else np.arange(N, dtype=np.int32)
+    if M == 1100:
+        q_pos = g.permutation(q_pos).astype(np.int32)
+    out = torch.empty(M, H * hd, dtype=torch.bfloat16, device="cuda")
+    B.cb_partial_attention(dev(q, "bf16"), dev_i32(q_pos), M, dev(K, "bf16"), dev(V, "bf16"), N, dims, out)
+    B.cb_sync(None)
+    rows = np.unique(np.concatenate([np.arange(0, M, 97), [M - 1]]))   # sampled rows of the oracle
+    want = O.attend(q.reshape(M, H, hd)[rows], q_pos[rows], K.reshape(N, Hkv, hd), V.reshape(N, Hkv, hd))
+    assert rel(host(out)[rows], want) < 5e-3
+
+
 @pytest.mark.parametrize("shape", [SHAPE_F32, SHAPE_BF16], ids=["f32", "bf16_gqa"])
 @pytest.mark.parametrize("M", [1, 130])
 def test_o_proj_ffn(B, shape, M):

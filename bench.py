@@ -422,6 +422,36 @@ def our_arm(args):
             gbs = kinds[name]["bytes"] / (kinds[name]["ms"] / 1e3) / 1e9
             hbm_kernels[name] = {"gbs": gbs, "frac": gbs / peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])}
 
+    # ---------------- the quality reference: full prefill of the same request on the GPU
+    # (every token through every layer, then the same lm_head), replayed from a CUDA graph
+    r0 = reqs[0]
+    h_last = torch.empty(shape.d_model, dtype=r0.x[0].dtype, device=dev)
+    full_tok = torch.empty(1, dtype=torch.int32, device=dev)
+
+    def full_step():
+        eng.full_prefill(r0.tokens, r0.K, r0.V, h_last)
+        B.cb_lmhead_argmax(h_last, dm.final_norm, dm.w_lm, dm.dims, None, full_tok, eng.ws)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            full_step()
+    stream.synchronize()
+    gfull = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gfull, stream=stream):
+        full_step()
+    n_full = max(3, min(args.steps, 10))
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(n_full):
+            gfull.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    full_ms = ev0.elapsed_time(ev1) / n_full
+    B.cb_sync(stream, 120.0)
+    full = {"ttft_ms": full_ms, "tokens_per_s": wl.n_tokens / (full_ms / 1e3),
+            "blended_speedup": full_ms / (ms / len(reqs)), "steps": n_full}
+
     # ---------------- end to end through the public API: pinned host in, token out
     # The step's inputs are the token ids and every layer's chunk KV, held in pinned host
     # memory (the storage tier); each layer's KV is loaded on a side stream one layer ahead
@@ -485,7 +515,7 @@ def our_arm(args):
         "launches_per_step": int(launches_per_step),
         "step_tflops": flops / (ms / 1e3) / 1e12,
         "roofline": roofline, "hbm_kernels": hbm_kernels, "kernels": kernels, "gemm_launches": gemm_detail,
-        "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "setup_s": setup_s,
+        "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "full_prefill": full, "setup_s": setup_s,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

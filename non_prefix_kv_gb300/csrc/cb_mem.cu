@@ -235,34 +235,33 @@ __global__ void __launch_bounds__(256) k_deviation(const T* __restrict__ kn, con
   for (int c = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; c < n_cand; c += warps_total) {
     const int64_t rn = new_row ? (int64_t)new_row[c] : c;
     const int64_t rr = ref_row ? (int64_t)ref_row[c] : c;
-    float acc = 0.f;
+    float acc = 0.f, accv = 0.f;
     const T* a = kn + rn * W;
     const T* b = kr + rr * W;
+    const T* av = vn + rn * W;
+    const T* bv = vr + rr * W;
     for (int e = lane * 8; e < W; e += 256) {
-      float x[8], y[8];
+      float x[8], y[8], xv[8], yv[8];
       ld8(a + e, x);
       ld8(b + e, y);
+      if (use_v) {
+        ld8(av + e, xv);
+        ld8(bv + e, yv);
+      }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float d = x[i] - y[i];
         acc = fmaf(d, d, acc);
       }
-    }
-    if (use_v) {
-      const T* av = vn + rn * W;
-      const T* bv = vr + rr * W;
-      for (int e = lane * 8; e < W; e += 256) {
-        float x[8], y[8];
-        ld8(av + e, x);
-        ld8(bv + e, y);
+      if (use_v) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float d = x[i] - y[i];
-          acc = fmaf(d, d, acc);
+          const float d = xv[i] - yv[i];
+          accv = fmaf(d, d, accv);
         }
       }
     }
-    acc = warp_sum(acc);
+    acc = warp_sum(acc) + warp_sum(accv);
     if (lane == 0) {
       scores[c] = acc;
       if (!isfinite(acc)) atomicOr(&g_err_mem, ERRBIT_NONFINITE);
@@ -350,17 +349,37 @@ __global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores,
       if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
     }
     __syncthreads();
-    if (tid == 0) {
-      int cum = 0, dsel = 0;
-      for (int dg = 255; dg >= 0; --dg) {
-        if (cum + hist[dg] >= remaining) {
-          dsel = dg;
-          break;
-        }
-        cum += hist[dg];
+    if (tid < 32) {
+      // warp-parallel search, from the top digit down, for the digit holding the
+      // remaining-th largest key: lane l owns digits 255-8l .. 248-8l
+      const int lane = tid;
+      int cnt[8], own = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        cnt[i] = hist[255 - 8 * lane - i];
+        own += cnt[i];
       }
-      s_prefix = prefix | ((uint32_t)dsel << shift);
-      s_remaining = remaining - cum;
+      int incl = own;   // inclusive prefix over lanes = keys in digits >= this lane's lowest
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int excl = incl - own;
+      const unsigned hit = __ballot_sync(0xffffffffu, excl < remaining && incl >= remaining);
+      if (lane == __ffs(hit) - 1) {
+        int cum = excl, dsel = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (cum + cnt[i] >= remaining) {
+            dsel = 255 - 8 * lane - i;
+            break;
+          }
+          cum += cnt[i];
+        }
+        s_prefix = prefix | ((uint32_t)dsel << shift);
+        s_remaining = remaining - cum;
+      }
     }
     __syncthreads();
     prefix = s_prefix;
@@ -532,15 +551,31 @@ __global__ void __launch_bounds__(256) k_lm_gemv(float* __restrict__ logits, con
   unsigned long long best = 0ull;
   for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < V; r += warps_total) {
     const T* wr = w + (int64_t)r * d;
-    float acc = 0.f;
-    for (int c = lane * 8; c < d; c += 256) {
+    float acc0 = 0.f, acc1 = 0.f;
+    int c = lane * 8;
+    for (; c + 768 < d; c += 1024) {     // four 16-byte weight loads in flight per lane
+      float a[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) ld8(wr + c + 256 * u, a[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float b[8];
+        ld8(hn + c + 256 * u, b);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (u & 1) acc1 = fmaf(a[u][i], b[i], acc1);
+          else acc0 = fmaf(a[u][i], b[i], acc0);
+        }
+      }
+    }
+    for (; c < d; c += 256) {
       float a[8], b[8];
       ld8(wr + c, a);
       ld8(hn + c, b);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc = fmaf(a[i], b[i], acc);
+      for (int i = 0; i < 8; ++i) acc0 = fmaf(a[i], b[i], acc0);
     }
-    acc = warp_sum(acc);
+    float acc = warp_sum(acc0 + acc1);
     if (lane == 0) logits[r] = acc;
     const unsigned long long key = argmax_key(acc, r);
     best = key > best ? key : best;

@@ -505,23 +505,21 @@ __global__ void __launch_bounds__(THREADS2, 1)
     if (!ok) atomicOr(&g_err_attn_tc, ERRBIT_TIMEOUT);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------------ MMA issuer
+    // Event-driven: probe every pending operation and issue whichever is ready, so a late
+    // softmax warpgroup never holds back the other query tile's S or P.V.  K stage j % 2 is
+    // released once S_0(j) and S_1(j) are both issued, V once both P.V(j) are.
     constexpr uint32_t idesc_s = tc::idesc_bf16_f32(BM, BN);
     constexpr uint32_t idesc_o = tc::idesc_bf16_f32(BM, HD, true);
     bool ok = tc::mbar_wait(q_full, 0);
-    for (int j = 0; ok && j <= T; ++j) {
-      const bool have_k = j < T;
-      if (have_k && !tc::mbar_wait(&k_full[j & 1], (j >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      bool v_ready = false;     // V_{j-1} is waited for just before its first P.V
-      for (int t = 0; ok && t < 2; ++t) {
-        if (have_k && j < Tt[t]) {
-          // S_t(j) = Q_t K_j^T once the softmax has pulled S_t(j-1) out of TMEM
-          if (j >= 1 && !tc::mbar_wait(&s_free[t], (j - 1) & 1)) {
-            ok = false;
-            break;
-          }
+    int ns[2] = {0, 0}, np[2] = {0, 0};     // next S / P.V tile per query tile
+    uint32_t idle = 0;
+    while (ok && (ns[0] < Tt[0] || ns[1] < Tt[1] || np[0] < Tt[0] || np[1] < Tt[1])) {
+      bool progressed = false;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int j = ns[t];
+        if (j < Tt[t] && tc::mbar_test(&k_full[j & 1], (j >> 1) & 1) &&
+            (j == 0 || tc::mbar_test(&s_free[t], (j - 1) & 1))) {
           tc::tc_fence_after();
 #pragma unroll
           for (int k = 0; k < HD / 16; ++k) {
@@ -531,33 +529,32 @@ __global__ void __launch_bounds__(THREADS2, 1)
             tc::mma_bf16(tmem + t * BN, a, b, idesc_s, k > 0);
           }
           tc::mma_commit(&s_full[t]);
+          ns[t] = j + 1;
+          // the other tile is done with K_j too (issued it, or never needs it)
+          if (ns[1 - t] > j || Tt[1 - t] <= j) tc::mma_commit(&k_empty[j & 1]);
+          progressed = true;
         }
-        const int jj = j - 1;
-        if (jj >= 0 && jj < Tt[t]) {
-          // O_t += P_t(jj) V_jj
-          if (!v_ready && !tc::mbar_wait(v_full, jj & 1)) {
-            ok = false;
-            break;
-          }
-          v_ready = true;
-          if (!tc::mbar_wait(&p_full[t], jj & 1)) {
-            ok = false;
-            break;
-          }
+        const int q = np[t];
+        if (q < Tt[t] && q < ns[t] && tc::mbar_test(v_full, q & 1) && tc::mbar_test(&p_full[t], q & 1)) {
           tc::tc_fence_after();
           const uint8_t* pb = sP + t * L::P_TILE;
 #pragma unroll
           for (int k = 0; k < BN / 16; ++k) {
             const uint64_t a = tc::desc_sw128(tc::smem_u32(pb + (k >> 2) * SLAB) + (k & 3) * 32);
             const uint64_t b = tc::desc_sw128_mn(tc::smem_u32(sV) + k * 16 * 128, SLAB);
-            tc::mma_bf16(tmem + TM_O + t * BN, a, b, idesc_o, (jj > 0 || k > 0) ? 1u : 0u);
+            tc::mma_bf16(tmem + TM_O + t * BN, a, b, idesc_o, (q > 0 || k > 0) ? 1u : 0u);
           }
           tc::mma_commit(&pv_done[t]);
+          np[t] = q + 1;
+          if (np[1 - t] > q || Tt[1 - t] <= q) tc::mma_commit(v_empty);
+          progressed = true;
         }
       }
-      if (!ok) break;
-      if (have_k) tc::mma_commit(&k_empty[j & 1]);
-      if (j >= 1) tc::mma_commit(v_empty);
+      if (progressed) {
+        idle = 0;
+      } else if (++idle > (1u << 26)) {
+        ok = false;
+      }
     }
     if (!ok) atomicOr(&g_err_attn_tc, ERRBIT_TIMEOUT);
   } else if (warp >= 2) {

@@ -200,7 +200,8 @@ def test_gather_scatter_bitwise(B, row_bytes):
 
 # ------------------------------------------------------------------------------ GEMM
 @pytest.mark.parametrize("M,N,K", [(1, 16, 64), (7, 256, 72), (127, 272, 4096), (129, 512, 136),
-                                   (300, 4096, 1024), (832, 1024, 4096), (1000, 768, 11008)])
+                                   (300, 4096, 1024), (832, 1024, 4096), (1000, 768, 11008),
+                                   (832, 4096, 4096), (4096, 4096, 1000), (256, 8192, 4096)])
 def test_linear_bf16_tensor_cores(B, M, N, K):
     torch = torch_mod()
     x = synth.test_tensor((M, K), 40 + M, dtype="bf16")

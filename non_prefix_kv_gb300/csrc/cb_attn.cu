@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(128) k_attn_simt(const T* __restrict__ q, cons
                                                    const T* __restrict__ kc, const T* __restrict__ vc,
                                                    int64_t n_kv, int H, int Hkv, T* __restrict__ out,
                                                    float scale) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int HD = DPL * 32;
   __shared__ float s_m[4], s_l[4];
   __shared__ float s_o[4][HD];
@@ -105,11 +107,12 @@ static cudaError_t launch_simt(const void* q, const int32_t* q_pos, int M, const
                                cudaStream_t s) {
   dim3 grid(M, H);
   const float scale = 1.0f / sqrtf((float)hd);
-#define CB_ATTN_CASE(DPL)                                                                          \
-  case DPL * 32:                                                                                   \
-    k_attn_simt<T, DPL><<<grid, 128, 0, s>>>((const T*)q, q_pos, (const T*)kc, (const T*)vc, n_kv, \
-                                             H, Hkv, (T*)out, scale);                              \
-    break;
+#define CB_ATTN_CASE(DPL)                                                                               \
+  case DPL * 32: {                                                                                      \
+    const cudaError_t e_ = launch_k(k_attn_simt<T, DPL>, dim3(grid), dim3(128), 0, s, (const T*)q, q_pos, \
+                                    (const T*)kc, (const T*)vc, n_kv, H, Hkv, (T*)out, scale);            \
+    if (e_ != cudaSuccess) return e_;                                                                   \
+  } break;
   switch (hd) {
     CB_ATTN_CASE(1)
     CB_ATTN_CASE(2)

@@ -72,6 +72,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const int32_t* __restrict__ q_pos, int M,
               int64_t n_kv, int H, int Hkv, bf16* __restrict__ out, float scale_log2) {
+  pdl_wait();
+  pdl_trigger();
   using L = Layout<HD>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = tc::smem_u32(smem_raw);
@@ -391,6 +393,8 @@ __global__ void __launch_bounds__(THREADS2, 1)
     k_attn_tc2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const int32_t* __restrict__ q_pos, int M,
                int64_t n_kv, int H, int Hkv, bf16* __restrict__ out, float scale_log2) {
+  pdl_wait();
+  pdl_trigger();
   using L = Layout2<HD>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = tc::smem_u32(smem_raw);
@@ -759,12 +763,12 @@ cudaError_t launch_hd(const void* q, const int32_t* q_pos, int M, const void* kc
   const int pairs = (M + 2 * BM - 1) / (2 * BM);
   if ((int64_t)pairs * H >= sm_count_attn()) {
     dim3 grid(pairs, H);
-    k_attn_tc2<HD><<<grid, THREADS2, Layout2<HD>::SMEM, s>>>(tq, tk, tv, q_pos, M, n_kv, H, Hkv,
-                                                             static_cast<bf16*>(out), scale_log2);
+    { const cudaError_t e_ = launch_k(k_attn_tc2<HD>, dim3(grid), dim3(THREADS2), Layout2<HD>::SMEM, s, tq, tk, tv, q_pos, M, n_kv, H, Hkv,
+                                                             static_cast<bf16*>(out), scale_log2); if (e_ != cudaSuccess) return e_; }
   } else {
     dim3 grid((M + BM - 1) / BM, H);
-    k_attn_tc<HD><<<grid, THREADS, Layout<HD>::SMEM, s>>>(tq, tk, tv, q_pos, M, n_kv, H, Hkv,
-                                                          static_cast<bf16*>(out), scale_log2);
+    { const cudaError_t e_ = launch_k(k_attn_tc<HD>, dim3(grid), dim3(THREADS), Layout<HD>::SMEM, s, tq, tk, tv, q_pos, M, n_kv, H, Hkv,
+                                                          static_cast<bf16*>(out), scale_log2); if (e_ != cudaSuccess) return e_; }
   }
   return cudaGetLastError();
 }

@@ -21,6 +21,8 @@ uint32_t take_error_gemm() {
 // (b_up_row + j) of B; the block then writes out[m][j] = silu(gate) * up for 32 j.
 template <typename T>
 __global__ void __launch_bounds__(256) k_gemm_simt(const GemmDesc g) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float As[16][64 + 1];
   __shared__ float Bs[16][64 + 1];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -102,7 +104,7 @@ static cudaError_t launch_simt(const GemmDesc& g, cudaStream_t s) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;
   const int cols = g.epi.kind == EPI_SWIGLU ? 32 : 64;
   dim3 grid((g.N + cols - 1) / cols, (g.M + 63) / 64);
-  k_gemm_simt<T><<<grid, 256, 0, s>>>(g);
+  { const cudaError_t e_ = launch_k(k_gemm_simt<T>, dim3(grid), dim3(256), 0, s, g); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 

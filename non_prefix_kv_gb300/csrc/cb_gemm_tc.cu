@@ -83,6 +83,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the prologue above overlaps the previous kernel's tail; inputs are read only from here
+  pdl_wait();
+  pdl_trigger();
 
   // Tiles are visited M-fastest: the CTAs in flight share a few weight tiles and the whole
   // (small) activation matrix, so both stay in L2 and each is read from HBM about once.
@@ -257,7 +260,7 @@ cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t s) {
   if (dev >= 0 && dev < 64 && !sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
   const int n_sm = (dev >= 0 && dev < 64 && sms[dev] > 0) ? sms[dev] : 148;
   const int grid = tiles < n_sm ? tiles : n_sm;
-  k_gemm_tc<<<grid, THREADS, SMEM_BYTES, s>>>(tmA, tmB, g, swiglu ? 1 : 0);
+  { const cudaError_t e_ = launch_k(k_gemm_tc, dim3(grid), dim3(THREADS), SMEM_BYTES, s, tmA, tmB, g, swiglu ? 1 : 0); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 

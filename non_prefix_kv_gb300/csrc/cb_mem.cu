@@ -45,6 +45,8 @@ uint32_t take_error_mem() {
 // ------------------------------------------------------------------------ RoPE table
 // tab[p][i] = (cos(p theta_i), sin(p theta_i)), theta_i = base^(-2i/hd); angle in fp64.
 __global__ void k_rope_table(float2* tab, int max_pos, int half, int hd, double base) {
+  pdl_wait();
+  pdl_trigger();
   int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= (int64_t)max_pos * half) return;
   int p = (int)(t / half), i = (int)(t % half);
@@ -58,8 +60,8 @@ cudaError_t launch_rope_table(float* tab, int max_pos, int hd, double base, cuda
   int half = hd / 2;
   int64_t n = (int64_t)max_pos * half;
   if (n == 0) return cudaSuccess;
-  k_rope_table<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(reinterpret_cast<float2*>(tab),
-                                                           max_pos, half, hd, base);
+  { const cudaError_t e_ = launch_k(k_rope_table, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, reinterpret_cast<float2*>(tab),
+                                                           max_pos, half, hd, base); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
@@ -74,6 +76,8 @@ __global__ void __launch_bounds__(256) k_rope_shift(T* __restrict__ kd, T* __res
                                                     const int32_t* __restrict__ delta,
                                                     int64_t n_rows, int W, int hd,
                                                     const float2* __restrict__ tab, int max_pos) {
+  pdl_wait();
+  pdl_trigger();
   const int per_row = W >> 3;
   const int half = hd >> 1;
   const int64_t total = n_rows * per_row;
@@ -116,13 +120,13 @@ cudaError_t launch_rope_shift(int dt, void* kd, void* vd, const void* ks, const 
   const unsigned grid = grid_for(work, 256);
   const float2* t2 = reinterpret_cast<const float2*>(tab);
   if (dt == DT_BF16)
-    k_rope_shift<bf16><<<grid, 256, 0, s>>>((bf16*)kd, (bf16*)vd, (const bf16*)ks,
+    { const cudaError_t e_ = launch_k(k_rope_shift<bf16>, dim3(grid), dim3(256), 0, s, (bf16*)kd, (bf16*)vd, (const bf16*)ks,
                                             (const bf16*)vs, src_row, delta, n_rows, W, hd, t2,
-                                            max_pos);
+                                            max_pos); if (e_ != cudaSuccess) return e_; }
   else
-    k_rope_shift<float><<<grid, 256, 0, s>>>((float*)kd, (float*)vd, (const float*)ks,
+    { const cudaError_t e_ = launch_k(k_rope_shift<float>, dim3(grid), dim3(256), 0, s, (float*)kd, (float*)vd, (const float*)ks,
                                              (const float*)vs, src_row, delta, n_rows, W, hd, t2,
-                                             max_pos);
+                                             max_pos); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
@@ -134,6 +138,8 @@ __global__ void __launch_bounds__(256) k_copy_rows(V* __restrict__ dst, const in
                                                    const V* __restrict__ src,
                                                    const int32_t* __restrict__ si, int64_t n,
                                                    int64_t rv, int64_t dbound, int64_t sbound) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t total = n * rv;
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
        t += (int64_t)gridDim.x * blockDim.x) {
@@ -155,13 +161,13 @@ cudaError_t launch_copy_rows(void* dst, const int32_t* dst_idx, const void* src,
   const bool v16 = (row_bytes % 16 == 0) && ((uintptr_t)dst % 16 == 0) && ((uintptr_t)src % 16 == 0);
   if (v16) {
     const int64_t rv = row_bytes / 16;
-    k_copy_rows<uint4><<<grid_for(n * rv, 256), 256, 0, s>>>((uint4*)dst, dst_idx, (const uint4*)src,
-                                                           src_idx, n, rv, dst_bound, src_bound);
+    { const cudaError_t e_ = launch_k(k_copy_rows<uint4>, dim3(grid_for(n * rv, 256)), dim3(256), 0, s, (uint4*)dst, dst_idx, (const uint4*)src,
+                                                           src_idx, n, rv, dst_bound, src_bound); if (e_ != cudaSuccess) return e_; }
   } else {
     const int64_t rv = row_bytes / 4;
-    k_copy_rows<uint32_t><<<grid_for(n * rv, 256), 256, 0, s>>>((uint32_t*)dst, dst_idx,
+    { const cudaError_t e_ = launch_k(k_copy_rows<uint32_t>, dim3(grid_for(n * rv, 256)), dim3(256), 0, s, (uint32_t*)dst, dst_idx,
                                                               (const uint32_t*)src, src_idx, n, rv,
-                                                              dst_bound, src_bound);
+                                                              dst_bound, src_bound); if (e_ != cudaSuccess) return e_; }
   }
   return cudaGetLastError();
 }
@@ -172,6 +178,8 @@ template <typename Ti, typename To>
 __global__ void __launch_bounds__(256) k_rmsnorm(To* __restrict__ out, const Ti* __restrict__ x,
                                                  const int32_t* __restrict__ rows,
                                                  const Ti* __restrict__ g, int d, float eps) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[32];
   const int64_t r = blockIdx.x;
   const int64_t src = rows ? (int64_t)rows[r] : r;
@@ -210,14 +218,14 @@ cudaError_t launch_rmsnorm(int dt_in, int dt_out, void* out, const void* x, cons
   if (n == 0) return cudaSuccess;
   const int threads = d >= 2048 ? 256 : (d >= 512 ? 64 : 32);
   if (dt_in == DT_BF16 && dt_out == DT_BF16)
-    k_rmsnorm<bf16, bf16><<<(unsigned)n, threads, 0, s>>>((bf16*)out, (const bf16*)x, rows,
-                                                          (const bf16*)g, d, eps);
+    { const cudaError_t e_ = launch_k(k_rmsnorm<bf16, bf16>, dim3((unsigned)n), dim3(threads), 0, s, (bf16*)out, (const bf16*)x, rows,
+                                                          (const bf16*)g, d, eps); if (e_ != cudaSuccess) return e_; }
   else if (dt_in == DT_BF16)
-    k_rmsnorm<bf16, float><<<(unsigned)n, threads, 0, s>>>((float*)out, (const bf16*)x, rows,
-                                                           (const bf16*)g, d, eps);
+    { const cudaError_t e_ = launch_k(k_rmsnorm<bf16, float>, dim3((unsigned)n), dim3(threads), 0, s, (float*)out, (const bf16*)x, rows,
+                                                           (const bf16*)g, d, eps); if (e_ != cudaSuccess) return e_; }
   else
-    k_rmsnorm<float, float><<<(unsigned)n, threads, 0, s>>>((float*)out, (const float*)x, rows,
-                                                            (const float*)g, d, eps);
+    { const cudaError_t e_ = launch_k(k_rmsnorm<float, float>, dim3((unsigned)n), dim3(threads), 0, s, (float*)out, (const float*)x, rows,
+                                                            (const float*)g, d, eps); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
@@ -230,6 +238,8 @@ __global__ void __launch_bounds__(256) k_deviation(const T* __restrict__ kn, con
                                                    const int32_t* __restrict__ new_row,
                                                    const int32_t* __restrict__ ref_row, int n_cand,
                                                    int W, int use_v, float* __restrict__ scores) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int warps_total = (gridDim.x * blockDim.x) >> 5;
   for (int c = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; c < n_cand; c += warps_total) {
@@ -275,13 +285,13 @@ cudaError_t launch_deviation(int dt, const void* kn, const void* vn, const void*
   if (n_cand == 0) return cudaSuccess;
   const unsigned grid = grid_for((int64_t)n_cand * 32, 256);
   if (dt == DT_BF16)
-    k_deviation<bf16><<<grid, 256, 0, s>>>((const bf16*)kn, (const bf16*)vn, (const bf16*)kr,
+    { const cudaError_t e_ = launch_k(k_deviation<bf16>, dim3(grid), dim3(256), 0, s, (const bf16*)kn, (const bf16*)vn, (const bf16*)kr,
                                            (const bf16*)vr, new_row, ref_row, n_cand, W, use_v,
-                                           scores);
+                                           scores); if (e_ != cudaSuccess) return e_; }
   else
-    k_deviation<float><<<grid, 256, 0, s>>>((const float*)kn, (const float*)vn, (const float*)kr,
+    { const cudaError_t e_ = launch_k(k_deviation<float>, dim3(grid), dim3(256), 0, s, (const float*)kn, (const float*)vn, (const float*)kr,
                                             (const float*)vr, new_row, ref_row, n_cand, W, use_v,
-                                            scores);
+                                            scores); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
@@ -324,6 +334,8 @@ __device__ __forceinline__ int block_excl_scan(int v, int* total, int* sh) {
 
 __global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores, int n, int k,
                                                int32_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int hist[256];
   __shared__ int sh[32];
   __shared__ uint32_t s_prefix;
@@ -406,12 +418,14 @@ __global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores,
 
 cudaError_t launch_topk(const float* scores, int n, int k, int32_t* out_ord, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  k_topk<<<1, 1024, 0, s>>>(scores, n, k, out_ord);
+  { const cudaError_t e_ = launch_k(k_topk, dim3(1), dim3(1024), 0, s, scores, n, k, out_ord); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
 // out[i] = map[ord[i]] (map null: ord[i])
 __global__ void k_map_rows(const int32_t* ord, int k, const int32_t* map, int32_t* out) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < k) out[i] = map ? map[ord[i]] : ord[i];
 }
@@ -419,7 +433,7 @@ __global__ void k_map_rows(const int32_t* ord, int k, const int32_t* map, int32_
 cudaError_t launch_map_rows(const int32_t* ord, int k, const int32_t* map, int32_t* out,
                             cudaStream_t s) {
   if (k == 0) return cudaSuccess;
-  k_map_rows<<<(k + 255) / 256, 256, 0, s>>>(ord, k, map, out);
+  { const cudaError_t e_ = launch_k(k_map_rows, dim3((k + 255) / 256), dim3(256), 0, s, ord, k, map, out); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
@@ -428,6 +442,8 @@ cudaError_t launch_map_rows(const int32_t* ord, int k, const int32_t* map, int32
 // row's position inside the layer's input row set.
 __global__ void k_build_sel(const int32_t* ord, int k, const int32_t* cand_row, int32_t forced_row0,
                             int32_t forced_pos0, int n_forced, int32_t* s_out, int32_t* keep_out) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < k) {
     const int o = ord[i];
@@ -445,8 +461,8 @@ cudaError_t launch_build_sel(const int32_t* ord, int k, const int32_t* cand_row,
                              int32_t* s_out, int32_t* keep_out, cudaStream_t s) {
   const int n = k + n_forced;
   if (n == 0) return cudaSuccess;
-  k_build_sel<<<(n + 255) / 256, 256, 0, s>>>(ord, k, cand_row, forced_row0, forced_pos0, n_forced,
-                                             s_out, keep_out);
+  { const cudaError_t e_ = launch_k(k_build_sel, dim3((n + 255) / 256), dim3(256), 0, s, ord, k, cand_row, forced_row0, forced_pos0, n_forced,
+                                             s_out, keep_out); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
@@ -454,6 +470,8 @@ cudaError_t launch_build_sel(const int32_t* ord, int k, const int32_t* cand_row,
 // itself, checked < m_in).  A row that is absent records ERRBIT_INDEX and maps to 0.
 __global__ void k_rows_to_positions(const int32_t* rows, int k, const int32_t* s_in, int m_in,
                                     int32_t* pos_out) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= k) return;
   const int r = rows[i];
@@ -482,18 +500,20 @@ __global__ void k_rows_to_positions(const int32_t* rows, int k, const int32_t* s
 cudaError_t launch_rows_to_positions(const int32_t* rows, int k, const int32_t* s_in, int m_in,
                                      int32_t* pos_out, cudaStream_t s) {
   if (k == 0) return cudaSuccess;
-  k_rows_to_positions<<<(k + 255) / 256, 256, 0, s>>>(rows, k, s_in, m_in, pos_out);
+  { const cudaError_t e_ = launch_k(k_rows_to_positions, dim3((k + 255) / 256), dim3(256), 0, s, rows, k, s_in, m_in, pos_out); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
 __global__ void k_iota(int32_t* out, int n, int32_t start) {
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) out[i] = start + i;
 }
 
 cudaError_t launch_iota(int32_t* out, int n, int32_t start, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  k_iota<<<(n + 255) / 256, 256, 0, s>>>(out, n, start);
+  { const cudaError_t e_ = launch_k(k_iota, dim3((n + 255) / 256), dim3(256), 0, s, out, n, start); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
@@ -501,6 +521,8 @@ cudaError_t launch_iota(int32_t* out, int n, int32_t start, cudaStream_t s) {
 // out[m][j] = silu(gu[m][j]) * gu[m][F + j]
 template <typename T>
 __global__ void k_swiglu(T* __restrict__ out, const T* __restrict__ gu, int64_t M, int F) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t total = M * F;
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
        t += (int64_t)gridDim.x * blockDim.x) {
@@ -515,9 +537,9 @@ cudaError_t launch_swiglu(int dt, void* out, const void* gu, int64_t M, int F, c
   if (M == 0) return cudaSuccess;
   const unsigned grid = grid_for(M * F, 256);
   if (dt == DT_BF16)
-    k_swiglu<bf16><<<grid, 256, 0, s>>>((bf16*)out, (const bf16*)gu, M, F);
+    { const cudaError_t e_ = launch_k(k_swiglu<bf16>, dim3(grid), dim3(256), 0, s, (bf16*)out, (const bf16*)gu, M, F); if (e_ != cudaSuccess) return e_; }
   else
-    k_swiglu<float><<<grid, 256, 0, s>>>((float*)out, (const float*)gu, M, F);
+    { const cudaError_t e_ = launch_k(k_swiglu<float>, dim3(grid), dim3(256), 0, s, (float*)out, (const float*)gu, M, F); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
@@ -545,6 +567,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) k_lm_gemv(float* __restrict__ logits, const float* __restrict__ hn,
                                                  const T* __restrict__ w, int V, int d,
                                                  unsigned long long* __restrict__ block_best) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ unsigned long long red[8];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int warps_total = (gridDim.x * blockDim.x) >> 5;
@@ -597,15 +621,17 @@ cudaError_t launch_lm_gemv(int dt, float* logits, const float* hn, const void* w
                            unsigned long long* block_best, cudaStream_t s) {
   const unsigned grid = lm_grid(V);
   if (dt == DT_BF16)
-    k_lm_gemv<bf16><<<grid, 256, 0, s>>>(logits, hn, (const bf16*)w, V, d, block_best);
+    { const cudaError_t e_ = launch_k(k_lm_gemv<bf16>, dim3(grid), dim3(256), 0, s, logits, hn, (const bf16*)w, V, d, block_best); if (e_ != cudaSuccess) return e_; }
   else
-    k_lm_gemv<float><<<grid, 256, 0, s>>>(logits, hn, (const float*)w, V, d, block_best);
+    { const cudaError_t e_ = launch_k(k_lm_gemv<float>, dim3(grid), dim3(256), 0, s, logits, hn, (const float*)w, V, d, block_best); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
 // token = index of the largest block key
 __global__ void __launch_bounds__(1024) k_argmax_keys(const unsigned long long* __restrict__ keys, int n,
                                                       int32_t* token) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ unsigned long long red[32];
   unsigned long long best = 0ull;
   for (int i = threadIdx.x; i < n; i += blockDim.x) best = keys[i] > best ? keys[i] : best;
@@ -621,7 +647,7 @@ __global__ void __launch_bounds__(1024) k_argmax_keys(const unsigned long long* 
 }
 
 cudaError_t launch_argmax_keys(const unsigned long long* keys, int n, int32_t* token, cudaStream_t s) {
-  k_argmax_keys<<<1, 1024, 0, s>>>(keys, n, token);
+  { const cudaError_t e_ = launch_k(k_argmax_keys, dim3(1), dim3(1024), 0, s, keys, n, token); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 

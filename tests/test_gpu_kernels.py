@@ -27,6 +27,9 @@ SHAPE_F32 = synth.ModelShape(n_layers=2, d_model=256, n_heads=4, n_kv_heads=4, h
                              vocab=1024, dtype="f32", w_std=0.05)
 SHAPE_BF16 = synth.ModelShape(n_layers=2, d_model=512, n_heads=8, n_kv_heads=2, head_dim=64, d_ff=1024,
                               vocab=2048, dtype="bf16", w_std=0.04)
+# a mid-size GQA layer: at 640 rows every GEMM spans several tiles in M, N and K
+SHAPE_BF16_MID = synth.ModelShape(n_layers=2, d_model=2048, n_heads=16, n_kv_heads=4, head_dim=128, d_ff=2048,
+                                  vocab=2048, dtype="bf16", w_std=0.02)
 
 
 def rope_tab(B, max_pos, hd, base):
@@ -199,9 +202,11 @@ def test_gather_scatter_bitwise(B, row_bytes):
 
 
 # ------------------------------------------------------------------------------ GEMM
+# ragged M, N and K tails, single-wave and multi-wave tile counts, the 7B layer's shapes
 @pytest.mark.parametrize("M,N,K", [(1, 16, 64), (7, 256, 72), (127, 272, 4096), (129, 512, 136),
                                    (300, 4096, 1024), (832, 1024, 4096), (1000, 768, 11008),
-                                   (832, 4096, 4096), (4096, 4096, 1000), (256, 8192, 4096)])
+                                   (832, 4096, 4096), (4096, 4096, 1000), (256, 8192, 4096),
+                                   (832, 12288, 4096), (4096, 4096, 11008)])
 def test_linear_bf16_tensor_cores(B, M, N, K):
     torch = torch_mod()
     x = synth.test_tensor((M, K), 40 + M, dtype="bf16")
@@ -235,14 +240,15 @@ def _layer_dev(B, shape, layer):
     return t, w
 
 
-@pytest.mark.parametrize("shape", [SHAPE_F32, SHAPE_BF16], ids=["f32", "bf16_gqa"])
-@pytest.mark.parametrize("M", [1, 7, 129])
+@pytest.mark.parametrize("shape,M", [(SHAPE_F32, 1), (SHAPE_F32, 7), (SHAPE_F32, 129), (SHAPE_BF16, 1),
+                                     (SHAPE_BF16, 7), (SHAPE_BF16, 129), (SHAPE_BF16_MID, 640)],
+                         ids=["f32-1", "f32-7", "f32-129", "bf16-1", "bf16-7", "bf16-129", "bf16_mid-640"])
 def test_selective_qkv(B, shape, M):
     torch = torch_mod()
     dims = dims_for(B, shape)
     layer = _layer(shape)
     t, w = _layer_dev(B, shape, layer)
-    n_x = 300
+    n_x = max(300, M + 100)
     x = synth.test_tensor((n_x, shape.d_model), 60, dtype=shape.dtype)
     g = synth.rng(61, synth.P_NOISE)
     rows = np.sort(g.choice(n_x, M, replace=False)).astype(np.int32)
@@ -331,8 +337,9 @@ def test_partial_attention_query_tile_pairs(B, H, Hkv, hd, M, N):
     assert rel(host(out)[rows], want) < 5e-3
 
 
-@pytest.mark.parametrize("shape", [SHAPE_F32, SHAPE_BF16], ids=["f32", "bf16_gqa"])
-@pytest.mark.parametrize("M", [1, 130])
+@pytest.mark.parametrize("shape,M", [(SHAPE_F32, 1), (SHAPE_F32, 130), (SHAPE_BF16, 1), (SHAPE_BF16, 130),
+                                     (SHAPE_BF16_MID, 640)], ids=["f32-1", "f32-130", "bf16-1", "bf16-130",
+                                                                  "bf16_mid-640"])
 def test_o_proj_ffn(B, shape, M):
     torch = torch_mod()
     dims = dims_for(B, shape)

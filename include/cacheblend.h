@@ -244,7 +244,10 @@ int cb_o_proj_ffn(const void* attn, const void* x_res, int32_t M, const cb_dims*
  *   s_out [m_out] (ascending).
  *   sel_override : [k_budget] ascending cache rows that replace the top-k choice (the
  *                  forced rows are still added), or NULL.
- *   scores_out   : [n_cand] fp32 deviation scores, or NULL (CHECK/GRADUAL only).
+ *   scores_out   : [n_cand] fp32 deviation scores, or NULL (CHECK/GRADUAL only).  For
+ *                  bf16 the squared differences are taken in the K/V GEMM's epilogue as
+ *                  the new rows are produced (one fp32 partial per 128 columns, summed in
+ *                  column order); fp32 runs the standalone deviation kernel.
  *   m_out_host   : receives m_out (known on the host before any launch: no sync).
  * x_out must not alias x_in. */
 int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode,

@@ -122,6 +122,9 @@ double gemm_bytes(int dt, const GemmDesc& g) {
   CB_LAUNCH(CB_PROF_DEVIATION, 0, (nc), (W), (usev), 3.0 * (nc) * (W) * ((usev) ? 2 : 1),        \
             (double)(nc) * (W) * esize(dt) * ((usev) ? 4 : 2) + 4.0 * (nc), s,                   \
             launch_deviation(dt, kn, vn, kr, vr, nr, rr, nc, W, usev, sc, s))
+#define L_DEVRED(part, np, ld, nc, W, usev, sc, s)                                               \
+  CB_LAUNCH(CB_PROF_DEVIATION, 1, (nc), (W), (usev), (double)(nc) * (np), 4.0 * (nc) * ((np) + 1), s, \
+            launch_dev_reduce(part, np, ld, nc, sc, s))
 #define L_TOPK(sc, n, k, ord, s) \
   CB_LAUNCH(CB_PROF_TOPK, 0, (n), (k), 0, 0.0, 4.0 * (n) + 4.0 * (k), s, launch_topk(sc, n, k, ord, s))
 #define L_MAP(ord, k, map, out, s) \
@@ -180,9 +183,15 @@ struct Carver {
 
 struct LayerWs {
   void *a, *q, *knew, *vnew, *attn, *h, *b, *act, *xg, *ag, *xa, *xb, *attn_ws;
-  float *scores, *hn, *logits;
+  float *scores, *hn, *logits, *dev_part;
   int32_t *ord, *keep, *pos, *rows;
 };
+
+// deviation partials per row of the K/V GEMM: one per half of each column tile
+int dev_parts(const cb_dims* d) {
+  const int W = d->n_kv_heads * d->head_dim;
+  return 2 * ((2 * W + kGemmTileN - 1) / kGemmTileN);
+}
 
 // R = rows entering the layer, M = rows selected (M <= R)
 LayerWs carve_layer(Carver& c, const cb_dims* d, int64_t R, int64_t M) {
@@ -202,6 +211,7 @@ LayerWs carve_layer(Carver& c, const cb_dims* d, int64_t R, int64_t M) {
   w.xa = c.take(R * d->d_model * B);
   w.xb = c.take(R * d->d_model * B);
   w.scores = static_cast<float*>(c.take(R * 4));
+  w.dev_part = static_cast<float*>(c.take((size_t)dev_parts(d) * R * 4));
   w.ord = static_cast<int32_t*>(c.take(R * 4));
   w.keep = static_cast<int32_t*>(c.take(R * 4));
   w.pos = static_cast<int32_t*>(c.take(R * 4));
@@ -574,8 +584,22 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
       }
       float* sc = scores_out ? scores_out : L.scores;
       L_RMSNORM(dims->dtype, dims->dtype, L.a, x_in, nullptr, w->attn_norm, m_in, dims->d_model, dims->rms_eps, s);
-      L_GEMM(dims->dtype, qkv_desc(dims, w, L.a, m_in, qc, 2 * W, nullptr, L.knew, L.vnew, rows_in, nullptr, cos_sin, max_pos), s);
-      L_DEV(dims->dtype, L.knew, L.vnew, k_cache, v_cache, nullptr, rows_in, n_cand, W, use_v, sc, s);
+      GemmDesc gkv = qkv_desc(dims, w, L.a, m_in, qc, 2 * W, nullptr, L.knew, L.vnew, rows_in, nullptr, cos_sin, max_pos);
+      if (dims->dtype == CB_BF16) {
+        // the deviation is taken in the K/V GEMM's epilogue; a small pass sums the tiles
+        gkv.epi.dev_part = L.dev_part;
+        gkv.epi.dev_ld = m_in;
+        gkv.epi.k_ref = k_cache;
+        gkv.epi.v_ref = v_cache;
+        gkv.epi.ref_row = rows_in;
+        gkv.epi.ref_rows = N;
+        gkv.epi.dev_use_v = use_v ? 1 : 0;
+        L_GEMM(dims->dtype, gkv, s);
+        L_DEVRED(L.dev_part, dev_parts(dims), m_in, n_cand, W, use_v, sc, s);
+      } else {
+        L_GEMM(dims->dtype, gkv, s);
+        L_DEV(dims->dtype, L.knew, L.vnew, k_cache, v_cache, nullptr, rows_in, n_cand, W, use_v, sc, s);
+      }
       if (k_budget > 0) {
         if (sel_override)
           L_R2P(sel_override, k_budget, check ? nullptr : rows_in, n_cand, L.ord, s);

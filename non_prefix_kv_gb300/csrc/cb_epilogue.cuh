@@ -86,4 +86,22 @@ __device__ __forceinline__ bool epi_apply(const EpiParams& p, int m, int n, floa
   }
 }
 
+// Squared deviation of 16 new K/V values (rotated, rounded to bf16 as they are stored)
+// from the 16 cached bf16 values in r: one chunk of the per-token KV deviation of HKVD
+// selection (CacheBlend explainer, §Selective recomputation Step 1), taken where the new
+// K/V are produced.
+__device__ __forceinline__ float sq_dev16(const float* v, const uint4* r) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(r);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 c = __bfloat1622float2(h[i]);
+    const float d0 = __bfloat162float(__float2bfloat16_rn(v[2 * i])) - c.x;
+    const float d1 = __bfloat162float(__float2bfloat16_rn(v[2 * i + 1])) - c.y;
+    s = fmaf(d0, d0, s);
+    s = fmaf(d1, d1, s);
+  }
+  return s;
+}
+
 }  // namespace cb

@@ -8,7 +8,8 @@
 // ring; two TMEM accumulators let the epilogue of one tile overlap the next tile's MMAs.
 // Warp roles:
 //   warp 0 lane 0 : TMA producer     warp 1 : TMEM allocator, lane 0 issues the MMAs
-//   warps 2..5    : epilogue, each reading the 32 TMEM lanes (rows) its warp may access.
+//   warps 2..9    : epilogue; warp w reads the 32 TMEM lanes (rows) of quadrant w % 4 and
+//                   one half of the accumulator columns, so two warps share each row band.
 #include <cuda.h>
 
 #include "cb_common.cuh"
@@ -30,13 +31,14 @@ uint32_t take_error_gemm_tc() {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BN = kGemmTileN;
 constexpr int BK = 64;
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int SMEM_BYTES = STAGES * (A_BYTES + B_BYTES) + 1024 /*align slack*/ + 256 /*barriers*/;
-constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;   // two 256-column accumulators
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -69,7 +71,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&acc_full[b], 1);
-      tc::mbar_init(&acc_empty[b], 4);
+      tc::mbar_init(&acc_empty[b], EPI_WARPS);
     }
     tc::fence_mbar_init();
     tc::tma_prefetch_desc(&tmA);
@@ -150,6 +152,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp >= 2) {
     // ---------------- epilogue: drains accumulator b while the MMAs fill the other one
     const int lane_base = (warp & 3) * 32;
+    const int half = (warp - 2) >> 2;        // which half of the accumulator columns
+    constexpr int CH = BN / 32;              // 16-column chunks per warp
     uint32_t i = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
       const uint32_t b = i & 1;
@@ -163,8 +167,59 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc::tc_fence_after();
       const uint32_t trow = tmem + b * BN + (static_cast<uint32_t>(lane_base) << 16);
-      if (!swiglu) {
-        for (int c = 0; c < BN / 16; ++c) {
+      if (!swiglu && g.epi.dev_part != nullptr) {
+        // K/V columns with the deviation against the cached row: the cached values of the
+        // chunk DEV_AHEAD further on are loaded while this chunk is processed
+        const EpiParams& p = g.epi;
+        int64_t rr = -1;
+        if (m < g.M) {
+          rr = p.ref_row ? (int64_t)p.ref_row[m] : (int64_t)m;
+          if (rr < 0 || rr >= p.ref_rows) {
+            atomicOr(&g_err_tc, ERRBIT_INDEX);
+            rr = -1;
+          }
+        }
+        auto ref_ptr = [&](int c) -> const uint4* {
+          const int n = n0 + (half * CH + c) * 16;
+          if (rr < 0 || n >= g.N) return nullptr;
+          const int gc = p.col0 + n;
+          if (gc < p.q_cols) return nullptr;
+          const bool is_v = gc >= p.q_cols + p.kv_cols;
+          if (is_v && !p.dev_use_v) return nullptr;
+          return reinterpret_cast<const uint4*>(static_cast<const bf16*>(is_v ? p.v_ref : p.k_ref) + rr * p.ldkv +
+                                                (gc - p.q_cols - (is_v ? p.kv_cols : 0)));
+        };
+        constexpr int DEV_AHEAD = 4;
+        uint4 ring[DEV_AHEAD][2];
+#pragma unroll
+        for (int c = 0; c < DEV_AHEAD; ++c) {
+          const uint4* q = ref_ptr(c);
+          if (q) {
+            ring[c][0] = __ldg(q);
+            ring[c][1] = __ldg(q + 1);
+          }
+        }
+        float dsum = 0.f;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          float v[16];
+          tc::tmem_ld16(trow + (half * CH + c) * 16, v);
+          const int n = n0 + (half * CH + c) * 16;
+          if (m < g.M && n < g.N) {
+            if (!epi_apply<bf16, 16>(p, m, n, v)) atomicOr(&g_err_tc, ERRBIT_INDEX);
+          }
+          if (ref_ptr(c)) dsum += sq_dev16(v, ring[c % DEV_AHEAD]);
+          if (c + DEV_AHEAD < CH) {
+            const uint4* q = ref_ptr(c + DEV_AHEAD);
+            if (q) {
+              ring[c % DEV_AHEAD][0] = __ldg(q);
+              ring[c % DEV_AHEAD][1] = __ldg(q + 1);
+            }
+          }
+        }
+        if (m < g.M) p.dev_part[((int64_t)(n0 / BN) * 2 + half) * p.dev_ld + m] = dsum;
+      } else if (!swiglu) {
+        for (int c = half * CH; c < (half + 1) * CH; ++c) {
           float v[16];
           tc::tmem_ld16(trow + c * 16, v);
           const int n = n0 + c * 16;
@@ -173,7 +228,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       } else {
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = half * (CH / 2); c < (half + 1) * (CH / 2); ++c) {
           float gt[16], up[16];
           tc::tmem_ld16(trow + c * 16, gt);
           tc::tmem_ld16(trow + BN / 2 + c * 16, up);

@@ -44,7 +44,18 @@ struct EpiParams {
   const int32_t* kv_row = nullptr;  // [M] destination row of k/v, or null
   const float* rope = nullptr;      // cos/sin table [max_pos][hd/2][2]
   int max_pos = 0;
+  // EPI_QKV on the tensor-core path: squared deviation of the (bf16-rounded) K/V columns
+  // from the cached rows, one partial per output row and half of a kGemmTileN-column tile
+  float* dev_part = nullptr;        // [2 * ceil(N / kGemmTileN)][dev_ld]
+  int64_t dev_ld = 0;
+  const void* k_ref = nullptr;      // rows ref_row[m] (or m) of [ref_rows, kv_cols]
+  const void* v_ref = nullptr;
+  const int32_t* ref_row = nullptr;
+  int64_t ref_rows = 0;
+  int dev_use_v = 1;
 };
+
+constexpr int kGemmTileN = 256;     // output columns per tensor-core GEMM tile
 
 struct GemmDesc {
   int M = 0, N = 0, K = 0;
@@ -67,6 +78,8 @@ cudaError_t launch_copy_rows(void* dst, const int32_t* dst_idx, const void* src,
 cudaError_t launch_rmsnorm(int dt_in, int dt_out, void* out, const void* x,
                            const int32_t* rows, const void* g, int64_t n, int d, float eps,
                            cudaStream_t s);
+cudaError_t launch_dev_reduce(const float* part, int n_parts, int64_t ld, int n_cand, float* scores,
+                              cudaStream_t s);
 cudaError_t launch_deviation(int dt, const void* kn, const void* vn, const void* kr,
                              const void* vr, const int32_t* new_row, const int32_t* ref_row,
                              int n_cand, int W, int use_v, float* scores, cudaStream_t s);

@@ -279,6 +279,27 @@ __global__ void __launch_bounds__(256) k_deviation(const T* __restrict__ kn, con
   }
 }
 
+// scores[c] = sum over column tiles t (in order) of part[t][c], the per-tile partials the
+// Q/K/V GEMM epilogue leaves when it computes the deviation in place.
+__global__ void k_dev_reduce(const float* __restrict__ part, int n_parts, int64_t ld, int n_cand,
+                             float* __restrict__ scores) {
+  pdl_wait();
+  pdl_trigger();
+  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < n_cand; c += gridDim.x * blockDim.x) {
+    float acc = 0.f;
+    for (int t = 0; t < n_parts; ++t) acc += part[t * ld + c];
+    scores[c] = acc;
+    if (!isfinite(acc)) atomicOr(&g_err_mem, ERRBIT_NONFINITE);
+  }
+}
+
+cudaError_t launch_dev_reduce(const float* part, int n_parts, int64_t ld, int n_cand, float* scores,
+                              cudaStream_t s) {
+  if (n_cand == 0) return cudaSuccess;
+  { const cudaError_t e_ = launch_k(k_dev_reduce, dim3(grid_for(n_cand, 256)), dim3(256), 0, s, part, n_parts, ld, n_cand, scores); if (e_ != cudaSuccess) return e_; }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_deviation(int dt, const void* kn, const void* vn, const void* kr,
                              const void* vr, const int32_t* new_row, const int32_t* ref_row,
                              int n_cand, int W, int use_v, float* scores, cudaStream_t s) {

@@ -355,6 +355,59 @@ def test_o_proj_ffn(B, shape, M):
     assert rel(host(out), want) < TOL[shape.dtype]
 
 
+@pytest.mark.parametrize("shape,dev_mode", [(SHAPE_BF16, 0), (SHAPE_BF16, 1), (SHAPE_BF16_MID, 0)],
+                         ids=["bf16-kv", "bf16-k", "bf16_mid-kv"])
+def test_check_layer_deviation_in_kv_gemm_epilogue(B, shape, dev_mode):
+    """bf16 check layers take the KV deviation inside the K/V GEMM's epilogue.  The scores
+    equal the standalone deviation of the same K/V rows (the selective Q/K/V call runs the
+    same GEMM, so its rows are bitwise the layer's) up to fp32 summation order, the set is
+    the top-k of those scores plus the forced rows, and the scores match the oracle's
+    deviation of the exact K/V within bf16 error."""
+    torch = torch_mod()
+    dims = dims_for(B, shape)
+    layer = _layer(shape, seed=5)
+    t, w = _layer_dev(B, shape, layer)
+    N, n_cand, k_budget = 700, 600, 90
+    x = synth.test_tensor((N, shape.d_model), 90, dtype="bf16")
+    kc = synth.test_tensor((N, shape.kv_width), 91, std=0.3, dtype="bf16")
+    vc = synth.test_tensor((N, shape.kv_width), 92, std=0.3, dtype="bf16")
+    tab = rope_tab(B, N, shape.head_dim, shape.rope_base)
+    ws = torch.empty(B.cb_workspace_bytes(dims, N, N), dtype=torch.uint8, device="cuda")
+    x_out = torch.empty(N, shape.d_model, dtype=torch.bfloat16, device="cuda")
+    s_out = torch.empty(N, dtype=torch.int32, device="cuda")
+    scores = torch.empty(N, dtype=torch.float32, device="cuda")
+    m = B.cb_blend_layer(dims, w, B.CB_LAYER_CHECK, dev(x, "bf16"), None, N, N, n_cand, dev(kc, "bf16"),
+                         dev(vc, "bf16"), tab, N, k_budget, dev_mode, None, x_out, s_out, scores, ws)
+    B.cb_sync(None)
+    assert m == k_budget + (N - n_cand)
+    got = host(scores)[:n_cand].astype(np.float64)
+
+    rows = dev_i32(np.arange(N, dtype=np.int32))
+    q = torch.empty(N, shape.q_width, dtype=torch.bfloat16, device="cuda")
+    kn = torch.empty(N, shape.kv_width, dtype=torch.bfloat16, device="cuda")
+    vn = torch.empty_like(kn)
+    B.cb_selective_qkv(dev(x, "bf16"), rows, rows, N, dims, w, tab, N, q, kn, vn, ws)
+    sc2 = torch.empty(n_cand, dtype=torch.float32, device="cuda")
+    sel2 = torch.empty(k_budget, dtype=torch.int32, device="cuda")
+    B.cb_kv_deviation_topk(kn, vn, dev(kc, "bf16"), dev(vc, "bf16"), None, None, n_cand, k_budget, dev_mode,
+                           dims, sc2, sel2, ws)
+    B.cb_sync(None)
+    want = host(sc2).astype(np.float64)
+    assert np.max(np.abs(got - want) / want) < 1e-5
+
+    S = s_out[:m].cpu().numpy()
+    np.testing.assert_array_equal(S[k_budget:], np.arange(n_cand, N))
+    top = np.sort(np.lexsort((np.arange(n_cand), -got))[:k_budget])
+    np.testing.assert_array_equal(S[:k_budget], top)
+
+    a = O.rmsnorm(x, layer["attn_norm"], shape.rms_eps)
+    p = O.project_qkv(layer, a, np.arange(N), shape)
+    k_ex, v_ex = p["k"].reshape(N, -1)[:n_cand], p["v"].reshape(N, -1)[:n_cand]
+    ref = (O.kv_deviation(k_ex, kc[:n_cand], v_ex, vc[:n_cand]) if dev_mode == 0
+           else O.kv_deviation(k_ex, kc[:n_cand]))
+    assert rel(got, ref) < 2e-2
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_lmhead_argmax(B, dtype):
     torch = torch_mod()

@@ -13,6 +13,8 @@ Sources (cited by short tag in each docstring):
           Fusion" explainer (abeam.tech, 2026-09-20-cacheblend-rag-cached-knowledge-fusion)
   [PC]    "論文解説: Prompt Cache — モジュラーAttention再利用による低レイテンシ推論"
           (0h-n0.github.io/posts/paper-2402-01008)
+  [CG]    "論文解説: CacheGen — KVキャッシュ圧縮とストリーミングで長文コンテキストのLLM推論を
+          高速化" (0h-n0.github.io/posts/paper-2401-12191)
 
 Readings taken where the pages are silent or disagree (each is listed with its reason in
 the design notes of the repository):
@@ -30,6 +32,10 @@ the design notes of the repository):
       rows of S_l have their K/V overwritten.
   R7  Ties in top-k go to the lower row index; the selected rows are returned ascending.
   R8  RMSNorm eps = 1e-5, no biases, untied lm_head, argmax ties to the lowest index.
+  R9  8-bit chunk KV: per channel of one chunk's K (or V) of one layer, zero = min over
+      the chunk's rows, scale = (max - min) / 255 floored at 1e-8, code = round half to
+      even of (x - zero) / scale; the code is decided in float32 (the pages fix no
+      precision), one IEEE operation per step, so both sides decide it bit for bit.
 
 Parity status of each function is stated in its docstring ("pinned by" / "parity
 unpinned").
@@ -375,6 +381,52 @@ def blend(model: dict, chunk_kv: Sequence[dict], order: Sequence[int], tokens: n
     return {"K": K, "V": V, "S": hist["S"], "scores": hist["scores"], "cand": hist["cand"],
             "x": hist["x"], "h_last": h_last, "token": tok, "logits": logits,
             "n_cached": n_cached, "forced": forced_sorted}
+
+
+# ----------------------------------------------------------------------------------------
+# 8-bit per-channel chunk KV ([CG] §Step 1 per-channel quantization; entropy coding out)
+# ----------------------------------------------------------------------------------------
+F32 = np.float32
+
+
+def kv_quantize(x, bits: int = 8):
+    """Per-channel asymmetric quantization of one chunk's K (or V) of one layer ([CG] §Step 1:
+    per channel c, z_c = min over tokens, s_c = (max - min) / (2^b - 1); code =
+    round((x - z_c) / s_c)).  R9: float32, one rounding per operation, half to even, codes
+    clipped to [0, 2^b - 1], the scale floored at 1e-8 (the page's listing clamps it so a
+    constant channel does not divide by zero).
+    Returns (codes uint8 [n, C], scale f32 [C], zero f32 [C]) for x [n, ...] (C = the
+    trailing size).
+    Pinned by: integer-valued channels with unit and even scales (codes = values, halves to
+    even), min -> 0 and max -> 2^b - 1, the round-trip bound |x^ - x| <= s/2 (+ float32
+    rounding), constant channels."""
+    x2 = np.asarray(x, F32).reshape(len(x), -1)
+    levels = F32(2 ** bits - 1)
+    zero = x2.min(axis=0)
+    scale = np.maximum((x2.max(axis=0) - zero) / levels, F32(1e-8)).astype(F32)
+    codes = np.clip(np.rint((x2 - zero) / scale), 0, levels).astype(np.uint8)
+    return codes, scale, zero
+
+
+def kv_dequantize(codes, scale, zero) -> np.ndarray:
+    """x^ = code * s + z in float32, the product rounded before the sum ([CG] decode step)."""
+    return (np.asarray(codes, F32) * np.asarray(scale, F32)).astype(F32) + np.asarray(zero, F32)
+
+
+def quantize_chunks(chunk_kv: Sequence[dict]) -> List[dict]:
+    """The chunk store kept as 8-bit codes: every chunk's K and V of every layer quantized
+    per channel, then decoded again (what the blend sees after loading)."""
+    out = []
+    for kv in chunk_kv:
+        d = dict(kv)
+        for key in ("K", "V"):
+            layers = []
+            for t in kv[key]:
+                q, sc, z = kv_quantize(t)
+                layers.append(kv_dequantize(q, sc, z).astype(F64).reshape(t.shape))
+            d[key] = layers
+        out.append(d)
+    return out
 
 
 # ----------------------------------------------------------------------------------------

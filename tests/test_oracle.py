@@ -387,3 +387,56 @@ def test_cost_pins():
             assert abs(O.t_load(per_tok, n, thr) * 1e3 - want) / want < tol
     assert O.optimal_ratio(0.15, 0.016, 0.020) == 0.8
     assert O.optimal_ratio(0.15, 0.001, 0.020) == 0.15
+
+
+# ------------------------------------------------------------------ 8-bit chunk KV
+def test_kv_quantize_integer_channels_and_half_to_even():
+    """Channel 0 spans 0..255 (scale 1: codes are the values); channel 1 spans 0..510
+    (scale 2: odd values land on .5 and round to the even code, as the page's round
+    does)."""
+    x = np.zeros((6, 2), np.float32)
+    x[:, 0] = [0, 1, 2, 7, 128, 255]
+    x[:, 1] = [0, 3, 5, 7, 101, 510]
+    q, s, z = O.kv_quantize(x)
+    assert s.tolist() == [1.0, 2.0] and z.tolist() == [0.0, 0.0]
+    assert q[:, 0].tolist() == [0, 1, 2, 7, 128, 255]
+    assert q[:, 1].tolist() == [0, 2, 2, 4, 50, 255]     # 1.5->2, 2.5->2, 3.5->4, 50.5->50
+    np.testing.assert_array_equal(O.kv_dequantize(q, s, z)[:, 0], x[:, 0])
+
+
+def test_kv_quantize_range_and_roundtrip_bound():
+    g = np.random.default_rng(5)
+    x = (g.standard_normal((300, 64)) * g.uniform(0.01, 5.0, 64) + g.uniform(-3, 3, 64)).astype(np.float32)
+    q, s, z = O.kv_quantize(x)
+    assert q.dtype == np.uint8
+    np.testing.assert_array_equal(q[np.argmin(x, axis=0), np.arange(64)], 0)
+    np.testing.assert_array_equal(q[np.argmax(x, axis=0), np.arange(64)], 255)
+    np.testing.assert_allclose(s, (x.max(0).astype(np.float64) - x.min(0)) / 255, rtol=1e-6)
+    err = np.abs(O.kv_dequantize(q, s, z).astype(np.float64) - x)
+    assert np.all(err <= s * 0.5 + 4 * np.abs(x) * 2.0 ** -24 + 1e-7)
+    # each code is a nearest level of (x - z) / s
+    t = (x.astype(np.float64) - z) / s
+    assert np.all(np.abs(q - t) <= 0.5 + 1e-4)
+
+
+def test_kv_quantize_constant_channel():
+    x = np.full((5, 3), 1.25, np.float32)
+    x[:, 2] = [-1, 0, 1, 2, 3]
+    q, s, z = O.kv_quantize(x)
+    assert np.all(q[:, :2] == 0) and s[0] == np.float32(1e-8)
+    np.testing.assert_array_equal(O.kv_dequantize(q, s, z)[:, :2], x[:, :2])
+
+
+def test_quantized_chunks_blend_stays_close():
+    """The decoded 8-bit chunk store changes each cached K/V entry by at most half a step,
+    and a blend over it keeps the selection structure."""
+    model, pool, order, tokens, chunk_kv = micro_setup()
+    q = O.quantize_chunks(chunk_kv)
+    for a, b in zip(chunk_kv, q):
+        for key in ("K", "V"):
+            for t, u in zip(a[key], b[key]):
+                span = t.reshape(len(t), -1).max(0) - t.reshape(len(t), -1).min(0)
+                assert np.all(np.abs(u - t).reshape(len(t), -1) <= span / 255 * 0.5 + 1e-6)
+    ratios = O.ratio_schedule(0.3, MICRO.n_layers, 1, False)
+    ref = O.blend(model, q, order, tokens, ratios)
+    assert len(ref["S"][1]) == O.budget(ref["n_cached"], 0.3, ref["n_cached"]) + len(ref["forced"])

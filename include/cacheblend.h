@@ -141,6 +141,30 @@ int cb_rope_shift(void* k_dst, void* v_dst, const void* k_src, const void* v_src
                   const int32_t* src_row, const int32_t* delta, int64_t n_rows,
                   const cb_dims* dims, const float* cos_sin, int32_t max_pos, void* stream);
 
+/* ---- 8-bit chunk KV ([CG] §Step 1 per-channel quantization; entropy coding is not done) */
+
+/* Quantizes one chunk's K (or V) of one layer per channel c (column): z_c = min over the
+ * rows, s_c = max((max - z_c) / 255, 1e-8), code = round-half-even((x - z_c) / s_c)
+ * clipped to [0, 255]; every step is one IEEE fp32 operation, so the codes are
+ * reproducible bit for bit.  A non-finite input sets the device error word.
+ *   x : [n_rows, W] of `dtype`;  codes : [n_rows, W] uint8;  scale, zero : [W] fp32. */
+int cb_kv_quantize(const void* x, int64_t n_rows, int32_t W, int32_t dtype, uint8_t* codes,
+                   float* scale, float* zero, void* stream);
+
+/* cb_rope_shift from an 8-bit chunk store, decoding as it re-positions:
+ *   x = code * s + z (fp32 product rounded before the sum), s and z from row qrow[i] of
+ *   the per-chunk tables; k_dst[i] = R(delta[i]) x_k[src_row[i]], v_dst[i] = x_v[src_row[i]].
+ *   k_codes, v_codes : [n_src_rows, Hkv hd] uint8 (8-byte aligned)
+ *   k_scale, k_zero, v_scale, v_zero : [n_qrows, Hkv hd] fp32 (16-byte aligned)
+ *   src_row : [n_rows] or NULL (row i);  qrow : [n_rows] in [0, n_qrows)
+ *   delta, cos_sin, max_pos as in cb_rope_shift;  v_* all NULL = keys only.
+ * Half the bytes of the bf16 store cross the host link and are read by this pass. */
+int cb_rope_shift_q8(void* k_dst, void* v_dst, const uint8_t* k_codes, const uint8_t* v_codes,
+                     const float* k_scale, const float* k_zero, const float* v_scale,
+                     const float* v_zero, const int32_t* src_row, int64_t n_src_rows,
+                     const int32_t* qrow, int32_t n_qrows, const int32_t* delta, int64_t n_rows,
+                     const cb_dims* dims, const float* cos_sin, int32_t max_pos, void* stream);
+
 /* ---- HKVD selection ----------------------------------------------------------------- */
 
 /* Per-candidate deviation and top-k ([CB-A] §KV deviation; §HKVD selection code):
@@ -306,6 +330,7 @@ int cb_stream_wait(void* stream, void* event);
 #define CB_PROF_LMHEAD     8
 #define CB_PROF_ARGMAX     9
 #define CB_PROF_ROPE_TABLE 10
+#define CB_PROF_QUANT      11
 
 typedef struct {
     int32_t kind;      /* CB_PROF_*                                                     */

@@ -42,7 +42,7 @@ class cb_prof_record(C.Structure):
 
 
 PROF_KINDS = {0: "rope_shift", 1: "copy_rows", 2: "rmsnorm", 3: "gemm", 4: "attention", 5: "deviation",
-              6: "topk", 7: "index", 8: "lmhead_gemv", 9: "argmax", 10: "rope_table"}
+              6: "topk", 7: "index", 8: "lmhead_gemv", 9: "argmax", 10: "rope_table", 11: "kv_quantize"}
 
 _P = C.c_void_p
 _I32 = C.c_int32
@@ -75,6 +75,9 @@ _PROTOS = {
                                   C.POINTER(_P), C.POINTER(_P), _P, _P, _P, _I32, _P, _SZ, _P]),
     "cb_lmhead_argmax": (C.c_int, [_P, _P, _P, C.POINTER(cb_dims), _P, _P, _P, _SZ, _P]),
     "cb_linear": (C.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _P]),
+    "cb_kv_quantize": (C.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _P]),
+    "cb_rope_shift_q8": (C.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _I32, _P, _I64,
+                                   C.POINTER(cb_dims), _P, _I32, _P]),
     "cb_prefetch_layer": (C.c_int, [_P, _P, _SZ, _P, _P]),
     "cb_stream_wait": (C.c_int, [_P, _P]),
     "cb_kernel_launch_count": (_I64, []),
@@ -243,6 +246,19 @@ def cb_lmhead_argmax(h, final_norm, w_lm, dims: cb_dims, logits, token, ws, stre
 
 def cb_linear(x, w, y, M: int, N: int, K: int, dtype: int, stream=None):
     _check("cb_linear", lib().cb_linear(_ptr(x), _ptr(w), _ptr(y), M, N, K, dtype, _stream(stream)))
+
+
+def cb_kv_quantize(x, n_rows: int, W: int, dtype: int, codes, scale, zero, stream=None):
+    _check("cb_kv_quantize", lib().cb_kv_quantize(_ptr(x), n_rows, W, dtype, _ptr(codes), _ptr(scale), _ptr(zero),
+                                                  _stream(stream)))
+
+
+def cb_rope_shift_q8(k_dst, v_dst, k_codes, v_codes, k_scale, k_zero, v_scale, v_zero, src_row, n_src_rows: int,
+                     qrow, n_qrows: int, delta, n_rows: int, dims: cb_dims, cos_sin, max_pos: int, stream=None):
+    _check("cb_rope_shift_q8", lib().cb_rope_shift_q8(
+        _ptr(k_dst), _ptr(v_dst), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale), _ptr(k_zero), _ptr(v_scale),
+        _ptr(v_zero), _ptr(src_row), n_src_rows, _ptr(qrow), n_qrows, _ptr(delta), n_rows, C.byref(dims),
+        _ptr(cos_sin), max_pos, _stream(stream)))
 
 
 def cb_kernel_launch_count() -> int:

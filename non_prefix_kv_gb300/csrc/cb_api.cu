@@ -401,6 +401,42 @@ int cb_rope_shift(void* k_dst, void* v_dst, const void* k_src, const void* v_src
   return CB_OK;
 }
 
+int cb_kv_quantize(const void* x, int64_t n_rows, int32_t W, int32_t dtype, uint8_t* codes, float* scale,
+                   float* zero, void* stream) {
+  if (dtype != CB_F32 && dtype != CB_BF16) return fail(CB_ERR_DTYPE, "dtype %d", dtype);
+  if (n_rows < 0 || W < 1) return fail(CB_ERR_SHAPE, "need n_rows >= 0, W >= 1");
+  if (n_rows == 0) return CB_OK;
+  if (!x || !codes || !scale || !zero) return fail(CB_ERR_INVALID_ARG, "kv_quantize pointer is NULL");
+  CB_LAUNCH(CB_PROF_QUANT, 0, n_rows, W, 0, 0.0, (double)n_rows * W * (2.0 * esize(dtype) + 1.0) + 8.0 * W,
+            S(stream), launch_kv_quantize(dtype, x, n_rows, W, codes, scale, zero, S(stream)));
+  return CB_OK;
+}
+
+int cb_rope_shift_q8(void* k_dst, void* v_dst, const uint8_t* k_codes, const uint8_t* v_codes, const float* k_scale,
+                     const float* k_zero, const float* v_scale, const float* v_zero, const int32_t* src_row,
+                     int64_t n_src_rows, const int32_t* qrow, int32_t n_qrows, const int32_t* delta, int64_t n_rows,
+                     const cb_dims* dims, const float* cos_sin, int32_t max_pos, void* stream) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (n_rows < 0 || n_src_rows < 0 || n_qrows < 0) return fail(CB_ERR_SHAPE, "negative size");
+  if (n_rows == 0) return CB_OK;
+  if (!k_dst || !k_codes || !k_scale || !k_zero || !qrow || !delta || !cos_sin || max_pos < 1)
+    return fail(CB_ERR_INVALID_ARG, "rope_shift_q8 pointer is NULL");
+  if ((v_dst == nullptr) != (v_codes == nullptr) || (v_dst && (!v_scale || !v_zero)))
+    return fail(CB_ERR_INVALID_ARG, "v_dst, v_codes, v_scale, v_zero must all be set or all NULL");
+  if (!src_row && n_src_rows < n_rows) return fail(CB_ERR_SHAPE, "n_src_rows < n_rows with src_row NULL");
+  const uintptr_t a = (uintptr_t)k_codes | (uintptr_t)v_codes;
+  const uintptr_t b = (uintptr_t)k_scale | (uintptr_t)k_zero | (uintptr_t)v_scale | (uintptr_t)v_zero;
+  if ((a & 7) || (b & 15)) return fail(CB_ERR_INVALID_ARG, "codes need 8-byte, scale/zero 16-byte alignment");
+  const int W = dims->n_kv_heads * dims->head_dim;
+  const double bytes = (double)n_rows * W * ((v_dst ? 2.0 : 1.0) * (1.0 + esize(dims->dtype))) + 4.0 * n_rows;
+  CB_LAUNCH(CB_PROF_ROPE_SHIFT, 1, n_rows, W, 0, 3.0 * n_rows * W, bytes, S(stream),
+            launch_rope_shift_q8(dims->dtype, k_dst, v_dst, k_codes, v_codes, k_scale, k_zero, v_scale, v_zero, src_row,
+                                 n_src_rows, qrow, n_qrows, delta, n_rows, W, dims->head_dim, cos_sin, max_pos,
+                                 S(stream)));
+  return CB_OK;
+}
+
 int cb_kv_deviation_topk(const void* k_new, const void* v_new, const void* k_ref, const void* v_ref,
                          const int32_t* new_row, const int32_t* ref_row, int32_t n_cand, int32_t k,
                          int32_t dev_mode, const cb_dims* dims, float* scores, int32_t* sel, void* ws,

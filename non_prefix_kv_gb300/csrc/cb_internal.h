@@ -72,6 +72,13 @@ cudaError_t launch_rope_table(float* tab, int max_pos, int hd, double base, cuda
 cudaError_t launch_rope_shift(int dt, void* kd, void* vd, const void* ks, const void* vs,
                               const int32_t* src_row, const int32_t* delta, int64_t n_rows,
                               int W, int hd, const float* tab, int max_pos, cudaStream_t s);
+cudaError_t launch_kv_quantize(int dt, const void* x, int64_t n, int W, uint8_t* q, float* scale,
+                               float* zero, cudaStream_t s);
+cudaError_t launch_rope_shift_q8(int dt, void* kd, void* vd, const uint8_t* kq, const uint8_t* vq,
+                                 const float* ks, const float* kz, const float* vs, const float* vz,
+                                 const int32_t* src_row, int64_t n_src, const int32_t* qrow, int n_q,
+                                 const int32_t* delta, int64_t n_rows, int W, int hd, const float* tab,
+                                 int max_pos, cudaStream_t s);
 cudaError_t launch_copy_rows(void* dst, const int32_t* dst_idx, const void* src,
                              const int32_t* src_idx, int64_t n, int64_t row_bytes,
                              int64_t dst_bound, int64_t src_bound, cudaStream_t s);

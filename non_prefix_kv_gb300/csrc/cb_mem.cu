@@ -130,6 +130,144 @@ cudaError_t launch_rope_shift(int dt, void* kd, void* vd, const void* ks, const 
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------------ 8-bit chunk KV
+// Per-channel asymmetric quantization of one [n, W] block (CacheGen explainer, §Step 1
+// per-channel quantization): zero = min over the rows, scale = max((max - min) / 255,
+// 1e-8), code = rint((x - zero) / scale) clipped to [0, 255]; every step is one IEEE fp32
+// operation so the code decision is reproducible.  A block owns 32 channels (a warp reads
+// 32 consecutive channels of a row); its 8 warps stride the rows, then combine.
+template <typename T>
+__global__ void __launch_bounds__(256) k_kv_quantize(const T* __restrict__ x, int64_t n, int W,
+                                                     uint8_t* __restrict__ q, float* __restrict__ scale,
+                                                     float* __restrict__ zero) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float s_lo[8][32], s_hi[8][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + lane;
+  float lo = INFINITY, hi = -INFINITY;
+  bool bad = false;
+  if (c < W) {
+    for (int64_t t = w; t < n; t += 8) {
+      const float v = to_f(x[t * W + c]);
+      bad |= !isfinite(v);
+      lo = fminf(lo, v);
+      hi = fmaxf(hi, v);
+    }
+  }
+  s_lo[w][lane] = lo;
+  s_hi[w][lane] = hi;
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    lo = fminf(lo, s_lo[i][lane]);
+    hi = fmaxf(hi, s_hi[i][lane]);
+  }
+  if (bad) atomicOr(&g_err_mem, ERRBIT_NONFINITE);
+  if (c >= W) return;
+  const float sc = fmaxf(__fdiv_rn(__fsub_rn(hi, lo), 255.0f), 1e-8f);
+  if (w == 0) {
+    scale[c] = sc;
+    zero[c] = lo;
+  }
+  for (int64_t t = w; t < n; t += 8) {
+    const float v = to_f(x[t * W + c]);
+    const float r = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v, lo), sc)), 0.0f), 255.0f);
+    q[t * W + c] = static_cast<uint8_t>(r);
+  }
+}
+
+cudaError_t launch_kv_quantize(int dt, const void* x, int64_t n, int W, uint8_t* q, float* scale,
+                               float* zero, cudaStream_t s) {
+  if (n == 0 || W == 0) return cudaSuccess;
+  const dim3 grid((unsigned)((W + 31) / 32));
+  if (dt == DT_BF16)
+    { const cudaError_t e_ = launch_k(k_kv_quantize<bf16>, grid, dim3(256), 0, s, (const bf16*)x, n, W, q, scale, zero); if (e_ != cudaSuccess) return e_; }
+  else
+    { const cudaError_t e_ = launch_k(k_kv_quantize<float>, grid, dim3(256), 0, s, (const float*)x, n, W, q, scale, zero); if (e_ != cudaSuccess) return e_; }
+  return cudaGetLastError();
+}
+
+// x = code * s + z (product rounded, then the sum: no fused multiply-add) for 8 channels
+__device__ __forceinline__ void dequant8(const uint8_t* q, const float* sc, const float* zp, float* x) {
+  const uint2 u = *reinterpret_cast<const uint2*>(q);
+  const float4 s0 = reinterpret_cast<const float4*>(sc)[0], s1 = reinterpret_cast<const float4*>(sc)[1];
+  const float4 z0 = reinterpret_cast<const float4*>(zp)[0], z1 = reinterpret_cast<const float4*>(zp)[1];
+  const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+  const float zv[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t word = i < 4 ? u.x : u.y;
+    const float code = static_cast<float>((word >> (8 * (i & 3))) & 0xffu);
+    x[i] = __fadd_rn(__fmul_rn(code, sv[i]), zv[i]);
+  }
+}
+
+// k_dst[r] = R(delta[r]) dequant(k_codes[src_row[r]]), v_dst[r] = dequant(v_codes[src_row[r]])
+// with the scale/zero row qrow[r] of the per-chunk tables: loading 8-bit chunk KV and
+// re-positioning it in one pass (one thread per 8 channels, as k_rope_shift).
+template <typename T>
+__global__ void __launch_bounds__(256) k_rope_shift_q8(T* __restrict__ kd, T* __restrict__ vd,
+                                                       const uint8_t* __restrict__ kq,
+                                                       const uint8_t* __restrict__ vq,
+                                                       const float* __restrict__ ks, const float* __restrict__ kz,
+                                                       const float* __restrict__ vs, const float* __restrict__ vz,
+                                                       const int32_t* __restrict__ src_row, int64_t n_src,
+                                                       const int32_t* __restrict__ qrow, int n_q,
+                                                       const int32_t* __restrict__ delta, int64_t n_rows, int W,
+                                                       int hd, const float2* __restrict__ tab, int max_pos) {
+  pdl_wait();
+  pdl_trigger();
+  const int per_row = W >> 3;
+  const int half = hd >> 1;
+  const int64_t total = n_rows * per_row;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = t / per_row;
+    const int c0 = (int)(t - r * per_row) << 3;
+    const int64_t sr = src_row ? (int64_t)src_row[r] : r;
+    const int qi = qrow[r];
+    const int dl = delta[r];
+    const int ad = dl < 0 ? -dl : dl;
+    if (ad >= max_pos || sr < 0 || sr >= n_src || qi < 0 || qi >= n_q) {
+      atomicOr(&g_err_mem, ERRBIT_INDEX);
+      continue;
+    }
+    const float sg = dl < 0 ? -1.0f : 1.0f;
+    float x[8], y[8];
+    dequant8(kq + sr * W + c0, ks + (int64_t)qi * W + c0, kz + (int64_t)qi * W + c0, x);
+    const float2* tb = tab + (int64_t)ad * half + ((c0 % hd) >> 1);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 cs = tb[q];
+      const float c = cs.x, sn = cs.y * sg;
+      y[2 * q] = x[2 * q] * c - x[2 * q + 1] * sn;
+      y[2 * q + 1] = x[2 * q] * sn + x[2 * q + 1] * c;
+    }
+    st8(kd + r * W + c0, y);
+    if (vd) {
+      float v[8];
+      dequant8(vq + sr * W + c0, vs + (int64_t)qi * W + c0, vz + (int64_t)qi * W + c0, v);
+      st8(vd + r * W + c0, v);
+    }
+  }
+}
+
+cudaError_t launch_rope_shift_q8(int dt, void* kd, void* vd, const uint8_t* kq, const uint8_t* vq,
+                                 const float* ks, const float* kz, const float* vs, const float* vz,
+                                 const int32_t* src_row, int64_t n_src, const int32_t* qrow, int n_q,
+                                 const int32_t* delta, int64_t n_rows, int W, int hd, const float* tab,
+                                 int max_pos, cudaStream_t s) {
+  if (n_rows == 0) return cudaSuccess;
+  const unsigned grid = grid_for(n_rows * (W / 8), 256);
+  const float2* t2 = reinterpret_cast<const float2*>(tab);
+  if (dt == DT_BF16)
+    { const cudaError_t e_ = launch_k(k_rope_shift_q8<bf16>, dim3(grid), dim3(256), 0, s, (bf16*)kd, (bf16*)vd, kq, vq, ks, kz, vs, vz, src_row, n_src, qrow, n_q, delta, n_rows, W, hd, t2, max_pos); if (e_ != cudaSuccess) return e_; }
+  else
+    { const cudaError_t e_ = launch_k(k_rope_shift_q8<float>, dim3(grid), dim3(256), 0, s, (float*)kd, (float*)vd, kq, vq, ks, kz, vs, vz, src_row, n_src, qrow, n_q, delta, n_rows, W, hd, t2, max_pos); if (e_ != cudaSuccess) return e_; }
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------------ row copies
 // dst[dst_idx[r]] = src[src_idx[r]] for rows of rv vector words.  Index checks against the
 // known buffer heights (bound < 0: unknown) record ERRBIT_INDEX and skip the row.

@@ -92,6 +92,44 @@ class ChunkPool:
     lens: List[int]
 
 
+    def layer_tensors(self, l: int) -> List[torch.Tensor]:
+        return [self.k[l], self.v[l]]
+
+
+@dataclass
+class ChunkPoolQ8:
+    """The chunk-KV pool as 8-bit per-channel codes (CacheGen explainer,
+    0h-n0.github.io/posts/paper-2401-12191, §Step 1): per layer the K and V codes
+    [rows, Hkv*hd] uint8 and, per chunk, the scale/zero of every channel [n_chunks, Hkv*hd]."""
+    kq: List[torch.Tensor]
+    vq: List[torch.Tensor]
+    ks: List[torch.Tensor]
+    kz: List[torch.Tensor]
+    vs: List[torch.Tensor]
+    vz: List[torch.Tensor]
+    offsets: List[int]
+    lens: List[int]
+
+    @classmethod
+    def from_pool(cls, pool: ChunkPool, dims: B.cb_dims) -> "ChunkPoolQ8":
+        W = pool.k[0].shape[1]
+        nc = len(pool.lens)
+        dev = pool.k[0].device
+        L = len(pool.k)
+        q = cls([torch.empty_like(pool.k[l], dtype=torch.uint8) for l in range(L)],
+                [torch.empty_like(pool.v[l], dtype=torch.uint8) for l in range(L)],
+                *[[torch.empty(nc, W, dtype=torch.float32, device=dev) for _ in range(L)] for _ in range(4)],
+                list(pool.offsets), list(pool.lens))
+        for l in range(L):
+            for c, (off, n) in enumerate(zip(pool.offsets, pool.lens)):
+                B.cb_kv_quantize(pool.k[l][off:off + n], n, W, dims.dtype, q.kq[l][off:off + n], q.ks[l][c], q.kz[l][c])
+                B.cb_kv_quantize(pool.v[l][off:off + n], n, W, dims.dtype, q.vq[l][off:off + n], q.vs[l][c], q.vz[l][c])
+        return q
+
+    def layer_tensors(self, l: int) -> List[torch.Tensor]:
+        return [self.kq[l], self.vq[l], self.ks[l], self.kz[l], self.vs[l], self.vz[l]]
+
+
 class BlendEngine:
     def __init__(self, dm: DeviceModel, n_tok_max: int, max_pos: Optional[int] = None, device="cuda"):
         self.dm = dm
@@ -137,15 +175,18 @@ class Request:
         self.order = list(order)
         self.n_cached = int(sum(pool.lens[c] for c in order))
         self.N = int(len(tokens))
-        src, delta = [], []
+        src, delta, qrow = [], [], []
         start = 0
         for c in order:
             n = pool.lens[c]
             src.extend(range(pool.offsets[c], pool.offsets[c] + n))
             delta.extend([start] * n)                 # p - p' = slot start (p' = local position)
+            qrow.extend([c] * n)                      # chunk of the row (8-bit pool tables)
             start += n
         self.src_row = torch.tensor(src, dtype=torch.int32, device=dev)
         self.delta = torch.tensor(delta, dtype=torch.int32, device=dev)
+        self.qrow = torch.tensor(qrow, dtype=torch.int32, device=dev)
+        self.n_pool_rows = int(sum(pool.lens))
         self.tokens_host = np.asarray(tokens, np.int32)
         self.tokens = torch.from_numpy(self.tokens_host).to(dev)
         self.K = [torch.zeros(self.N, s.kv_width, dtype=dt, device=dev) for _ in range(s.n_layers)]
@@ -185,17 +226,27 @@ def layer_plan(shape: ModelShape, n_tok: int, n_cached: int, ratios: Sequence[Op
 
 
 class HostPool:
-    """The chunk-KV pool kept in pinned host memory (the storage tier of the pages' design),
-    with a side stream and one event per layer for layer-ahead loading."""
+    """A chunk-KV pool (bf16 or 8-bit) mirrored in pinned host memory (the storage tier of
+    the pages' design), with a side stream and one event per layer for layer-ahead loading
+    into the device pool."""
 
-    def __init__(self, pool: ChunkPool):
-        self.k = [t.cpu().pin_memory() for t in pool.k]
-        self.v = [t.cpu().pin_memory() for t in pool.v]
+    def __init__(self, pool):
+        self.pool = pool
+        n_layers = len(pool.k) if isinstance(pool, ChunkPool) else len(pool.kq)
+        self.dev = [pool.layer_tensors(l) for l in range(n_layers)]
+        self.host = [[t.cpu().pin_memory() for t in ts] for ts in self.dev]
         self.side = torch.cuda.Stream()
-        self.done = [torch.cuda.Event() for _ in pool.k]
+        self.done = [torch.cuda.Event() for _ in range(n_layers)]
         for ev in self.done:          # torch creates the CUDA event on its first record
             ev.record(self.side)
-        self.nbytes = sum(t.numel() * t.element_size() for t in self.k + self.v)
+        self.nbytes = sum(t.numel() * t.element_size() for ts in self.host for t in ts)
+
+    def prefetch_all(self, stream):
+        """Queue every layer's copy on the side stream once `stream`'s prior work is done."""
+        self.side.wait_stream(stream)
+        for l, (hs, ds) in enumerate(zip(self.host, self.dev)):
+            for h, d in zip(hs, ds):
+                B.cb_prefetch_layer(d, h, h.numel() * h.element_size(), self.side, self.done[l])
 
 
 def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None, keep_history=False,
@@ -212,17 +263,24 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
     dims = dm.dims
     esz = 2 if s.dtype == "bf16" else 4
     if host_pool is not None:
-        main = torch.cuda.current_stream() if stream is None else stream
-        host_pool.side.wait_stream(main)          # the device pool is free once prior work is done
-        for l in range(s.n_layers):
-            nk = host_pool.k[l].numel() * host_pool.k[l].element_size()
-            B.cb_prefetch_layer(req.pool.k[l], host_pool.k[l], nk, host_pool.side, host_pool.done[l])
-            B.cb_prefetch_layer(req.pool.v[l], host_pool.v[l], nk, host_pool.side, host_pool.done[l])
+        if host_pool.pool is not req.pool:
+            raise ValueError("host_pool must mirror the request's pool")
+        host_pool.prefetch_all(torch.cuda.current_stream() if stream is None else stream)
+
+    def assemble_layer(l):
+        if isinstance(req.pool, ChunkPoolQ8):
+            p = req.pool
+            B.cb_rope_shift_q8(req.K[l], req.V[l], p.kq[l], p.vq[l], p.ks[l], p.kz[l], p.vs[l], p.vz[l],
+                               req.src_row, req.n_pool_rows, req.qrow, len(p.lens), req.delta, req.n_cached, dims,
+                               eng.cos_sin, eng.max_pos, stream)
+        else:
+            B.cb_rope_shift(req.K[l], req.V[l], req.pool.k[l], req.pool.v[l], req.src_row, req.delta,
+                            req.n_cached, dims, eng.cos_sin, eng.max_pos, stream)
+
     B.cb_gather_rows(req.x[0], dm.embed, req.tokens, req.N, s.d_model * esz, stream)
     if assemble and host_pool is None:
         for l in range(s.n_layers):
-            B.cb_rope_shift(req.K[l], req.V[l], req.pool.k[l], req.pool.v[l], req.src_row, req.delta,
-                            req.n_cached, dims, eng.cos_sin, eng.max_pos, stream)
+            assemble_layer(l)
     cur = 0
     m_in = req.N
     s_in = None
@@ -231,8 +289,7 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
     for l, (mode, k) in enumerate(plan):
         if assemble and host_pool is not None:
             B.cb_stream_wait(stream, host_pool.done[l])
-            B.cb_rope_shift(req.K[l], req.V[l], req.pool.k[l], req.pool.v[l], req.src_row, req.delta,
-                            req.n_cached, dims, eng.cos_sin, eng.max_pos, stream)
+            assemble_layer(l)
         ov = None if sel_override is None else sel_override.get(l)
         m_out = B.cb_blend_layer(dims, dm.layers_c[l], mode, req.x[cur], s_in, m_in, req.N, req.n_cached,
                                  req.K[l], req.V[l], eng.cos_sin, eng.max_pos, k, dev_mode, ov,

@@ -37,7 +37,23 @@ def _near_tie(ref, l, got_set, tol):
     return all(abs(sc[idx[r]] - kth) <= tol * kth for r in diff if r in idx)
 
 
-def run_case(E, wl, r, gradual, tol, check_sets=True):
+def q8_pool_from_codes(E, pool, chunk_kv, dims):
+    """An 8-bit device pool holding the oracle's codes of the oracle's chunk KV, so the GPU
+    decodes exactly the values the oracle blends with (the quantizer itself is checked bit
+    for bit in the kernel tests)."""
+    torch = torch_mod()
+    q = E.ChunkPoolQ8.from_pool(pool, dims)
+    for c, (off, n) in enumerate(zip(pool.offsets, pool.lens)):
+        for l in range(len(pool.k)):
+            for key, codes, sc, zp in (("K", q.kq, q.ks, q.kz), ("V", q.vq, q.vs, q.vz)):
+                cq, cs, cz = O.kv_quantize(chunk_kv[c][key][l])
+                codes[l][off:off + n] = torch.from_numpy(cq).cuda()
+                sc[l][c] = torch.from_numpy(cs).cuda()
+                zp[l][c] = torch.from_numpy(cz).cuda()
+    return q
+
+
+def run_case(E, wl, r, gradual, tol, check_sets=True, q8=False):
     torch = torch_mod()
     shape = wl.shape
     model = synth.make_model(shape, seed=wl.seed)
@@ -45,7 +61,8 @@ def run_case(E, wl, r, gradual, tol, check_sets=True):
     tokens = req_h.tokens
     ratios = O.ratio_schedule(r, shape.n_layers, 1, gradual)
     chunk_kv = O.precompute_chunks(model, req_h.chunk_tokens)
-    ref = O.blend(model, chunk_kv, req_h.order, tokens, ratios, gradual=gradual)
+    blend_kv = O.quantize_chunks(chunk_kv) if q8 else chunk_kv
+    ref = O.blend(model, blend_kv, req_h.order, tokens, ratios, gradual=gradual)
 
     dm = E.DeviceModel.from_host(model)
     eng = E.BlendEngine(dm, len(tokens))
@@ -56,6 +73,8 @@ def run_case(E, wl, r, gradual, tol, check_sets=True):
         for l in range(shape.n_layers):
             assert rel(host(pool.k[l][off:off + n]), chunk_kv[c]["K"][l].reshape(n, -1)) < tol
             assert rel(host(pool.v[l][off:off + n]), chunk_kv[c]["V"][l].reshape(n, -1)) < tol
+    if q8:
+        pool = q8_pool_from_codes(E, pool, chunk_kv, dm.dims)
     req = E.Request(eng, pool, req_h.order, tokens)
     plan = E.layer_plan(shape, req.N, req.n_cached, ratios, gradual=gradual)
     m = E.run_blend(req, plan, keep_history=True)
@@ -111,6 +130,13 @@ def test_blend_tiny_f32_gradual_3_layers(E, r):
     run_case(E, wl, r, True, TOL["f32"])
 
 
+@pytest.mark.parametrize("r", [0.0, 0.15])
+def test_blend_tiny_f32_from_8bit_chunk_store(E, r):
+    """The chunk store kept as 8-bit per-channel codes, decoded while re-positioning: the
+    blend matches the oracle's blend over the decoded store."""
+    run_case(E, synth.WORKLOADS["tiny_f32"], r, False, TOL["f32"], q8=True)
+
+
 def test_blend_ragged_chunks_no_query_f32(E):
     # chunks of odd lengths and no uncached suffix: the only forced row is the last one
     shape = replace(synth.WORKLOADS["tiny_f32"].shape, n_layers=3)
@@ -136,9 +162,11 @@ def test_blend_bf16_gqa(E):
     run_case(E, wl, 0.2, True, TOL["bf16"], check_sets=False)
 
 
-def test_layer_ahead_loading_matches_resident_pool(E):
-    """Loading every layer's chunk KV from pinned host memory on a side stream, one event per
-    layer, gives bit-identical results to the device-resident pool."""
+@pytest.mark.parametrize("q8", [False, True], ids=["bf16_pool", "8bit_pool"])
+def test_layer_ahead_loading_matches_resident_pool(E, q8):
+    """Loading every layer's chunk KV (bf16, or 8-bit codes with their tables) from pinned
+    host memory on a side stream, one event per layer, gives bit-identical results to the
+    device-resident pool."""
     torch = torch_mod()
     from non_prefix_kv_gb300 import binding as B
     wl = synth.Workload("bf16_small", BF16_SMALL, chunk_len=96, n_distinct=4, order=(0, 1, 2, 3), n_query=32,
@@ -148,6 +176,8 @@ def test_layer_ahead_loading_matches_resident_pool(E):
     dm = E.DeviceModel.from_host(model)
     eng = E.BlendEngine(dm, wl.n_tokens)
     pool = eng.precompute_pool(req_h.chunk_tokens)
+    if q8:
+        pool = E.ChunkPoolQ8.from_pool(pool, dm.dims)
     hp = E.HostPool(pool)
     plan = E.layer_plan(wl.shape, wl.n_tokens, wl.n_cached, [None, 0.15, 0.15])
     a = E.Request(eng, pool, req_h.order, req_h.tokens)
@@ -156,8 +186,9 @@ def test_layer_ahead_loading_matches_resident_pool(E):
     ka = [t.clone() for t in a.K]
     xa = a.x_last[:a.m_last].clone()
     ta = int(a.token.item())
-    for t in pool.k + pool.v:        # the streamed run must reload the whole pool
-        t.zero_()
+    for ts in hp.dev:                # the streamed run must reload the whole pool
+        for t in ts:
+            t.zero_()
     b = E.Request(eng, pool, req_h.order, req_h.tokens)
     E.run_blend(b, plan, host_pool=hp)
     B.cb_sync(None)

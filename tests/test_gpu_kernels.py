@@ -201,6 +201,66 @@ def test_gather_scatter_bitwise(B, row_bytes):
     np.testing.assert_array_equal(host(vc), want)
 
 
+# ------------------------------------------------------------------------------ 8-bit chunk KV
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("n,W", [(1, 8), (5, 100), (640, 4096), (333, 264)])
+def test_kv_quantize_codes_bit_exact(B, dtype, n, W):
+    """Codes, scales and zeros equal the oracle's bit for bit (both decide in IEEE fp32)."""
+    torch = torch_mod()
+    x = synth.test_tensor((n, W), 70 + n, std=0.7, dtype=dtype)
+    x[:, W // 2] = x[0, W // 2]                     # a constant channel
+    codes = torch.empty(n, W, dtype=torch.uint8, device="cuda")
+    sc = torch.empty(W, dtype=torch.float32, device="cuda")
+    zp = torch.empty(W, dtype=torch.float32, device="cuda")
+    B.cb_kv_quantize(dev(x, dtype), n, W, B.CB_BF16 if dtype == "bf16" else B.CB_F32, codes, sc, zp)
+    B.cb_sync(None)
+    q, s, z = O.kv_quantize(x)
+    np.testing.assert_array_equal(codes.cpu().numpy(), q)
+    np.testing.assert_array_equal(sc.cpu().numpy(), s)
+    np.testing.assert_array_equal(zp.cpu().numpy(), z)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_rope_shift_q8_decodes_and_rotates(B, dtype):
+    """Rows gathered from an 8-bit store of three chunks, decoded with their chunk's tables
+    and re-rotated by positive and negative offsets, against the oracle's decode + RoPE."""
+    torch = torch_mod()
+    shape = synth.ModelShape(1, 256, 4, 2, 64, 256, 64, dtype=dtype)
+    dims = dims_for(B, shape)
+    W = shape.kv_width
+    lens = [40, 7, 90]
+    store = [synth.test_tensor((m, W), 80 + i, std=0.5, dtype=dtype) for i, m in enumerate(lens)]
+    qs = [O.kv_quantize(x) for x in store]
+    vstore = [synth.test_tensor((m, W), 90 + i, std=0.5, dtype=dtype) for i, m in enumerate(lens)]
+    vqs = [O.kv_quantize(x) for x in vstore]
+    kq = dev(np.concatenate([q[0] for q in qs]).astype(np.float32), "f32").to(torch.uint8)
+    vq = dev(np.concatenate([q[0] for q in vqs]).astype(np.float32), "f32").to(torch.uint8)
+    ks, kz = dev(np.stack([q[1] for q in qs]), "f32"), dev(np.stack([q[2] for q in qs]), "f32")
+    vs, vz = dev(np.stack([q[1] for q in vqs]), "f32"), dev(np.stack([q[2] for q in vqs]), "f32")
+    offs = np.cumsum([0] + lens[:-1])
+    g = synth.rng(95, synth.P_NOISE)
+    n_rows = 150
+    chunk = g.integers(0, 3, n_rows)
+    local = np.array([g.integers(0, lens[c]) for c in chunk])
+    src = (offs[chunk] + local).astype(np.int32)
+    delta = g.integers(-2000, 2000, n_rows).astype(np.int32)
+    tab = rope_tab(B, 2048, shape.head_dim, shape.rope_base)
+    kd = torch.empty(n_rows, W, dtype=tdt(dtype), device="cuda")
+    vd = torch.empty_like(kd)
+    B.cb_rope_shift_q8(kd, vd, kq, vq, ks, kz, vs, vz, dev_i32(src), sum(lens), dev_i32(chunk.astype(np.int32)), 3,
+                       dev_i32(delta), n_rows, dims, tab, 2048)
+    B.cb_sync(None)
+    dk = np.concatenate([O.kv_dequantize(*q) for q in qs])[src]
+    dv = np.concatenate([O.kv_dequantize(*q) for q in vqs])[src]
+    want_k = O.rope_shift(dk.reshape(n_rows, shape.n_kv_heads, shape.head_dim), delta,
+                          shape.rope_base).reshape(n_rows, -1)
+    if dtype == "f32":
+        np.testing.assert_array_equal(host(vd), dv)        # the decode itself is bit-exact
+        assert rel(host(kd), want_k) < 1e-6
+    else:
+        assert rel(host(vd), dv) < 4e-3 and rel(host(kd), want_k) < 4e-3
+
+
 # ------------------------------------------------------------------------------ GEMM
 # ragged M, N and K tails, single-wave and multi-wave tile counts, the 7B layer's shapes
 @pytest.mark.parametrize("M,N,K", [(1, 16, 64), (7, 256, 72), (127, 272, 4096), (129, 512, 136),

@@ -273,14 +273,19 @@ int cb_o_proj_ffn(const void* attn, const void* x_res, int32_t M, const cb_dims*
  *                  the new rows are produced (one fp32 partial per 128 columns, summed in
  *                  column order); fp32 runs the standalone deviation kernel.
  *   m_out_host   : receives m_out (known on the host before any launch: no sync).
+ *   kv_ready     : a cudaEvent_t marking when the cached rows of k_cache/v_cache have been
+ *                  written (e.g. re-positioned on a loading stream), or NULL.  The layer
+ *                  waits for it just before its first access to the cached rows: in
+ *                  PRECHECK after the Q and uncached-row K/V GEMMs (they touch only rows
+ *                  >= n_cached), so those overlap the load ([CB-A] §Pipelining).
  * x_out must not alias x_in. */
 int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode,
                    const void* x_in, const int32_t* s_in, int32_t m_in,
                    int64_t n_tok, int64_t n_cached, void* k_cache, void* v_cache,
                    const float* cos_sin, int32_t max_pos, int32_t k_budget, int32_t dev_mode,
                    const int32_t* sel_override, void* x_out, int32_t* s_out,
-                   int32_t* m_out_host, float* scores_out, void* ws, size_t ws_bytes,
-                   void* stream);
+                   int32_t* m_out_host, float* scores_out, void* kv_ready, void* ws,
+                   size_t ws_bytes, void* stream);
 
 /* Standard causal prefill of n tokens at positions pos0..pos0+n-1 through n_layers
  * layers: the quality reference (KV^full, [CB-A] §KV cache definitions; [CB-B] "full KV

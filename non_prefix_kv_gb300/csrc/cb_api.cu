@@ -566,7 +566,7 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
                    int32_t m_in, int64_t n_tok, int64_t n_cached, void* k_cache, void* v_cache,
                    const float* cos_sin, int32_t max_pos, int32_t k_budget, int32_t dev_mode,
                    const int32_t* sel_override, void* x_out, int32_t* s_out, int32_t* m_out_host,
-                   float* scores_out, void* ws, size_t ws_bytes, void* stream) {
+                   float* scores_out, void* kv_ready, void* ws, size_t ws_bytes, void* stream) {
   int st = check_dims(dims);
   if (st || (st = check_w(w))) return st;
   if (!x_in || !k_cache || !v_cache || !cos_sin || !x_out || !s_out || !m_out_host)
@@ -584,6 +584,9 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
   const bool use_v = dev_mode == CB_DEV_KV;
   cudaStream_t s = S(stream);
   LayerWs L;
+  // the stream waits for the cached rows right before its first access to them
+#define WAIT_CACHED_ROWS() \
+  do { if (kv_ready) CB_CUDA(cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(kv_ready), 0)); } while (0)
 
   switch (mode) {
     case CB_LAYER_PRECHECK: {
@@ -598,6 +601,7 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         const void* a_u = static_cast<const char*>(L.a) + (size_t)n_cached * dims->d_model * B;
         L_GEMM(dims->dtype, qkv_desc(dims, w, a_u, nu, qc, 2 * W, nullptr, k_cache, v_cache, s_out + n_cached, s_out + n_cached, cos_sin, max_pos), s);
       }
+      WAIT_CACHED_ROWS();
       L_ATTN(dims->dtype, L.q, s_out, N, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
       return o_ffn(dims, w, L.attn, x_in, N, x_out, L, s);
     }
@@ -620,6 +624,7 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
       }
       float* sc = scores_out ? scores_out : L.scores;
       L_RMSNORM(dims->dtype, dims->dtype, L.a, x_in, nullptr, w->attn_norm, m_in, dims->d_model, dims->rms_eps, s);
+      WAIT_CACHED_ROWS();
       GemmDesc gkv = qkv_desc(dims, w, L.a, m_in, qc, 2 * W, nullptr, L.knew, L.vnew, rows_in, nullptr, cos_sin, max_pos);
       if (dims->dtype == CB_BF16) {
         // the deviation is taken in the K/V GEMM's epilogue; a small pass sums the tiles
@@ -662,6 +667,7 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
       else
         L_IOTA(s_out, m_in, 0, s);
       L_RMSNORM(dims->dtype, dims->dtype, L.a, x_in, nullptr, w->attn_norm, m_in, dims->d_model, dims->rms_eps, s);
+      WAIT_CACHED_ROWS();
       L_GEMM(dims->dtype, qkv_desc(dims, w, L.a, m_in, 0, qc + 2 * W, L.q, k_cache, v_cache, s_out, s_out, cos_sin, max_pos), s);
       L_ATTN(dims->dtype, L.q, s_out, m_in, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
       return o_ffn(dims, w, L.attn, x_in, m_in, x_out, L, s);
@@ -669,6 +675,7 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
     default:
       return fail(CB_ERR_INVALID_ARG, "mode %d", mode);
   }
+#undef WAIT_CACHED_ROWS
 }
 
 int cb_full_prefill(const cb_dims* dims, int32_t n_layers, const cb_layer_w* layers_host, const void* embed,

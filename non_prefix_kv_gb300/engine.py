@@ -241,12 +241,17 @@ class HostPool:
             ev.record(self.side)
         self.nbytes = sum(t.numel() * t.element_size() for ts in self.host for t in ts)
 
-    def prefetch_all(self, stream):
-        """Queue every layer's copy on the side stream once `stream`'s prior work is done."""
+    def prefetch_all(self, stream, after_copy=None):
+        """Queue every layer's copy on the side stream once `stream`'s prior work is done;
+        after_copy(l, side_stream) enqueues more work on the landed layer (the
+        re-positioning) before the layer's event is recorded."""
         self.side.wait_stream(stream)
         for l, (hs, ds) in enumerate(zip(self.host, self.dev)):
             for h, d in zip(hs, ds):
                 B.cb_prefetch_layer(d, h, h.numel() * h.element_size(), self.side, self.done[l])
+            if after_copy is not None:
+                after_copy(l, self.side)
+                self.done[l].record(self.side)
 
 
 def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None, keep_history=False,
@@ -254,48 +259,47 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
     """One blended prefill: re-position the chunk KV of every layer, run the layer plan,
     then the lm_head argmax.  Returns the number of rows carried out of the last layer.
 
-    With host_pool, every layer's chunk KV is first copied from pinned host memory on a
-    side stream, all layers queued up front; layer l waits only for its own copy, so the
-    load of layer l+1 overlaps the recompute of layer l."""
+    With host_pool, every layer's chunk KV is copied from pinned host memory and
+    re-positioned on a side stream, all layers queued up front; layer l waits for its own
+    layer's event only where it first touches the cached rows (in the pre-check layer after
+    its Q and uncached-row K/V GEMMs), so loading overlaps recompute."""
     eng = req.eng
     dm = eng.dm
     s = dm.shape
     dims = dm.dims
     esz = 2 if s.dtype == "bf16" else 4
-    if host_pool is not None:
-        if host_pool.pool is not req.pool:
-            raise ValueError("host_pool must mirror the request's pool")
-        host_pool.prefetch_all(torch.cuda.current_stream() if stream is None else stream)
-
-    def assemble_layer(l):
+    def assemble_layer(l, st):
         if isinstance(req.pool, ChunkPoolQ8):
             p = req.pool
             B.cb_rope_shift_q8(req.K[l], req.V[l], p.kq[l], p.vq[l], p.ks[l], p.kz[l], p.vs[l], p.vz[l],
                                req.src_row, req.n_pool_rows, req.qrow, len(p.lens), req.delta, req.n_cached, dims,
-                               eng.cos_sin, eng.max_pos, stream)
+                               eng.cos_sin, eng.max_pos, st)
         else:
             B.cb_rope_shift(req.K[l], req.V[l], req.pool.k[l], req.pool.v[l], req.src_row, req.delta,
-                            req.n_cached, dims, eng.cos_sin, eng.max_pos, stream)
+                            req.n_cached, dims, eng.cos_sin, eng.max_pos, st)
+
+    if host_pool is not None:
+        if host_pool.pool is not req.pool:
+            raise ValueError("host_pool must mirror the request's pool")
+        host_pool.prefetch_all(torch.cuda.current_stream() if stream is None else stream,
+                               assemble_layer if assemble else None)
 
     B.cb_gather_rows(req.x[0], dm.embed, req.tokens, req.N, s.d_model * esz, stream)
     if assemble and host_pool is None:
         for l in range(s.n_layers):
-            assemble_layer(l)
+            assemble_layer(l, stream)
     cur = 0
     m_in = req.N
     s_in = None
     if keep_history:
         req.sel_hist, req.m_hist = [], []
     for l, (mode, k) in enumerate(plan):
-        if assemble and host_pool is not None:
-            B.cb_stream_wait(stream, host_pool.done[l])
-            assemble_layer(l)
         ov = None if sel_override is None else sel_override.get(l)
         m_out = B.cb_blend_layer(dims, dm.layers_c[l], mode, req.x[cur], s_in, m_in, req.N, req.n_cached,
                                  req.K[l], req.V[l], eng.cos_sin, eng.max_pos, k, dev_mode, ov,
                                  req.x[1 - cur], req.s[1 - cur],
                                  req.scores if mode in (B.CB_LAYER_CHECK, B.CB_LAYER_GRADUAL) else None,
-                                 eng.ws, stream)
+                                 eng.ws, stream, kv_ready=None if host_pool is None else host_pool.done[l])
         cur = 1 - cur
         s_in = req.s[cur]
         m_in = m_out

@@ -121,14 +121,14 @@ def test_entry_points_reject_bad_arguments_before_launch(lib):
     m_out = ctypes.c_int32(-1)
     args = lambda mode, m_in, k, ws_bytes=1 << 40: (ctypes.byref(d), ctypes.byref(w), mode, FAKE, None, m_in, 416,
                                                    384, FAKE, FAKE, FAKE, 416, k, 0, None, FAKE + 64, FAKE,
-                                                   ctypes.byref(m_out), None, FAKE, ws_bytes, None)
+                                                   ctypes.byref(m_out), None, None, FAKE, ws_bytes, None)
     assert lib.cb_blend_layer(*args(B.CB_LAYER_CHECK, 416, 385)) == 2     # k > candidates (384)
     assert lib.cb_blend_layer(*args(B.CB_LAYER_CHECK, 400, 5)) == 2       # CHECK needs all rows
     assert lib.cb_blend_layer(*args(B.CB_LAYER_PRECHECK, 416, 0, 100)) == 4
     assert lib.cb_blend_layer(*args(9, 416, 0)) == 1
     assert m_out.value == -1          # nothing reported for a rejected call
     st = lib.cb_blend_layer(ctypes.byref(d), ctypes.byref(w), 0, FAKE, None, 416, 416, 384, FAKE, FAKE, FAKE,
-                            100, 0, 0, None, FAKE + 64, FAKE, ctypes.byref(m_out), None, FAKE, 1 << 40, None)
+                            100, 0, 0, None, FAKE + 64, FAKE, ctypes.byref(m_out), None, None, FAKE, 1 << 40, None)
     assert st == 2                    # rope table shorter than the sequence
     assert b"rope table" in lib.cb_last_error_message()
     st = lib.cb_linear(FAKE, FAKE, FAKE, 4, 24, 64, B.CB_BF16, None)

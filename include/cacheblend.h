@@ -136,7 +136,9 @@ int cb_rope_table(float* cos_sin, int32_t max_pos, int32_t head_dim, double base
  *   src_row      : [n_rows] int32 source row per destination row, or NULL (row i)
  *   delta        : [n_rows] int32 position offset p - p', |delta| < max_pos
  *   k_dst, v_dst : [n_rows, Hkv hd]; v_src/v_dst may both be NULL (keys only).
- * In-place (k_dst == k_src) is allowed only with src_row == NULL. */
+ * In-place (k_dst == k_src) is allowed only with src_row == NULL.  The sources may be
+ * pinned host memory mapped at the same device address (read over the host link, no
+ * landing copy); any other host pointer is rejected before launch. */
 int cb_rope_shift(void* k_dst, void* v_dst, const void* k_src, const void* v_src,
                   const int32_t* src_row, const int32_t* delta, int64_t n_rows,
                   const cb_dims* dims, const float* cos_sin, int32_t max_pos, void* stream);
@@ -158,7 +160,8 @@ int cb_kv_quantize(const void* x, int64_t n_rows, int32_t W, int32_t dtype, uint
  *   k_scale, k_zero, v_scale, v_zero : [n_qrows, Hkv hd] fp32 (16-byte aligned)
  *   src_row : [n_rows] or NULL (row i);  qrow : [n_rows] in [0, n_qrows)
  *   delta, cos_sin, max_pos as in cb_rope_shift;  v_* all NULL = keys only.
- * Half the bytes of the bf16 store cross the host link and are read by this pass. */
+ * Half the bytes of the bf16 store cross the host link and are read by this pass; the
+ * codes may be pinned host memory mapped at the same device address (as cb_rope_shift). */
 int cb_rope_shift_q8(void* k_dst, void* v_dst, const uint8_t* k_codes, const uint8_t* v_codes,
                      const float* k_scale, const float* k_zero, const float* v_scale,
                      const float* v_zero, const int32_t* src_row, int64_t n_src_rows,

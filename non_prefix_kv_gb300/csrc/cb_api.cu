@@ -162,6 +162,20 @@ int check_dims(const cb_dims* d) {
   return CB_OK;
 }
 
+// A source the kernels read may live in pinned host memory (zero-copy over the host link)
+// only if that memory is mapped into the device address space at the same address.
+int check_readable(const void* p, const char* what) {
+  if (!p) return CB_OK;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(CB_ERR_INVALID_ARG, "%s: not a CUDA-visible pointer", what);
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return CB_OK;
+  if (a.type == cudaMemoryTypeHost && a.devicePointer == p) return CB_OK;
+  return fail(CB_ERR_INVALID_ARG, "%s: host memory not mapped at the same device address", what);
+}
+
 int check_w(const cb_layer_w* w) {
   if (!w || !w->attn_norm || !w->wqkv || !w->wo || !w->ffn_norm || !w->w_gate_up || !w->w_down)
     return fail(CB_ERR_INVALID_ARG, "layer weight pointer is NULL");
@@ -396,6 +410,7 @@ int cb_rope_shift(void* k_dst, void* v_dst, const void* k_src, const void* v_src
     return fail(CB_ERR_INVALID_ARG, "rope_shift pointer is NULL");
   if ((v_dst == nullptr) != (v_src == nullptr)) return fail(CB_ERR_INVALID_ARG, "v_dst/v_src must both be set or NULL");
   if (k_dst == k_src && src_row) return fail(CB_ERR_INVALID_ARG, "in-place shift needs src_row == NULL");
+  if ((st = check_readable(k_src, "k_src")) || (st = check_readable(v_src, "v_src"))) return st;
   const int W = dims->n_kv_heads * dims->head_dim;
   L_ROPE_SHIFT(dims->dtype, k_dst, v_dst, k_src, v_src, src_row, delta, n_rows, W, dims->head_dim, cos_sin, max_pos, S(stream));
   return CB_OK;
@@ -428,6 +443,7 @@ int cb_rope_shift_q8(void* k_dst, void* v_dst, const uint8_t* k_codes, const uin
   const uintptr_t a = (uintptr_t)k_codes | (uintptr_t)v_codes;
   const uintptr_t b = (uintptr_t)k_scale | (uintptr_t)k_zero | (uintptr_t)v_scale | (uintptr_t)v_zero;
   if ((a & 7) || (b & 15)) return fail(CB_ERR_INVALID_ARG, "codes need 8-byte, scale/zero 16-byte alignment");
+  if ((st = check_readable(k_codes, "k_codes")) || (st = check_readable(v_codes, "v_codes"))) return st;
   const int W = dims->n_kv_heads * dims->head_dim;
   const double bytes = (double)n_rows * W * ((v_dst ? 2.0 : 1.0) * (1.0 + esize(dims->dtype))) + 4.0 * n_rows;
   CB_LAUNCH(CB_PROF_ROPE_SHIFT, 1, n_rows, W, 0, 3.0 * n_rows * W, bytes, S(stream),

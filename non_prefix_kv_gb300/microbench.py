@@ -42,6 +42,7 @@ def run(argv=None):
     p.add_argument("--n", type=int, default=8192)
     p.add_argument("--k", type=int, default=4096)
     p.add_argument("--epi", choices=["store", "swiglu"], default="store")
+    p.add_argument("--host-src", action="store_true", help="rope_shift: sources in pinned host memory")
     p.add_argument("--heads", type=int, default=32)
     p.add_argument("--kv-heads", type=int, default=32)
     p.add_argument("--hd", type=int, default=128)
@@ -106,12 +107,14 @@ def run(argv=None):
         B.cb_rope_table(tab, 16384, hd, 1e4)
         ks = torch.randn(a.rows, a.width, device="cuda", generator=g).to(bf)
         vs = torch.randn(a.rows, a.width, device="cuda", generator=g).to(bf)
+        if a.host_src:
+            ks, vs = ks.cpu().pin_memory(), vs.cpu().pin_memory()
         kd, vd = torch.empty_like(ks), torch.empty_like(vs)
         delta = torch.full((a.rows,), 1280, dtype=torch.int32, device="cuda")
         ms = _time(lambda: B.cb_rope_shift(kd, vd, ks, vs, None, delta, a.rows, dims, tab, 16384), a.iters,
                    a.warmup)
         by = 4.0 * a.rows * a.width * 2
-        out.update(ms=ms, gbs=by / (ms / 1e3) / 1e9, rows=a.rows, width=a.width)
+        out.update(ms=ms, gbs=by / (ms / 1e3) / 1e9, rows=a.rows, width=a.width, host_src=a.host_src)
     else:
         hd = a.hd
         shape = ModelShape(1, 256, a.width // hd, a.width // hd, hd, 256, 64, dtype="bf16")

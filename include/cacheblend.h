@@ -54,6 +54,7 @@ extern "C" {
 #define CB_ERR_TIMEOUT      7   /* cb_sync waited longer than its limit                */
 #define CB_ERR_UNSUPPORTED  8   /* a shape the kernels do not handle (see message)     */
 #define CB_ERR_DEVICE       9   /* a kernel recorded an out-of-range index             */
+#define CB_ERR_IO          10   /* a storage read failed (cb_io_error_message says why) */
 
 #define CB_F32   0
 #define CB_BF16  1
@@ -366,6 +367,17 @@ int cb_profile_end(cb_prof_record* out_host, int32_t max_records, int32_t* n_out
  * all of element type `dtype`.  bf16 needs N % 16 == 0 and K % 8 == 0; fp32 N % 4 == 0. */
 int cb_linear(const void* x, const void* w, void* y, int32_t M, int32_t N, int32_t K, int32_t dtype,
               void* stream);
+
+/* ---- storage tier ---------------------------------------------------------------------- */
+
+/* Reads bytes [offset, offset + bytes) of the file at path into dst_host (typically pinned
+ * memory, so a following cb_prefetch_layer streams it to the device), with up to n_threads
+ * parallel positional reads of at least 4 MB each: the storage-to-host leg of layer-wise
+ * KV loading ([CB-A] §Pipelining and load controller).  Synchronous, host only.  Returns
+ * CB_OK or CB_ERR_IO (short file, open/read failure; cb_io_error_message gives the reason,
+ * for the calling thread). */
+int cb_file_read(const char* path, uint64_t offset, void* dst_host, size_t bytes, int32_t n_threads);
+const char* cb_io_error_message(void);
 
 #ifdef __cplusplus
 }

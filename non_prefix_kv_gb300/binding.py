@@ -16,7 +16,7 @@ CB_DEV_KV, CB_DEV_K = 0, 1
 CB_LAYER_PRECHECK, CB_LAYER_CHECK, CB_LAYER_STEADY, CB_LAYER_GRADUAL = 0, 1, 2, 3
 STATUS_NAMES = {0: "CB_OK", 1: "CB_ERR_INVALID_ARG", 2: "CB_ERR_SHAPE", 3: "CB_ERR_DTYPE",
                 4: "CB_ERR_WORKSPACE", 5: "CB_ERR_NONFINITE", 6: "CB_ERR_CUDA", 7: "CB_ERR_TIMEOUT",
-                8: "CB_ERR_UNSUPPORTED", 9: "CB_ERR_DEVICE"}
+                8: "CB_ERR_UNSUPPORTED", 9: "CB_ERR_DEVICE", 10: "CB_ERR_IO"}
 
 
 class CBError(RuntimeError):
@@ -76,6 +76,8 @@ _PROTOS = {
     "cb_lmhead_argmax": (C.c_int, [_P, _P, _P, C.POINTER(cb_dims), _P, _P, _P, _SZ, _P]),
     "cb_linear": (C.c_int, [_P, _P, _P, _I32, _I32, _I32, _I32, _P]),
     "cb_kv_quantize": (C.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _P]),
+    "cb_file_read": (C.c_int, [C.c_char_p, C.c_uint64, _P, _SZ, _I32]),
+    "cb_io_error_message": (C.c_char_p, []),
     "cb_rope_shift_q8": (C.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _I32, _P, _I64,
                                    C.POINTER(cb_dims), _P, _I32, _P]),
     "cb_prefetch_layer": (C.c_int, [_P, _P, _SZ, _P, _P]),
@@ -249,6 +251,13 @@ def cb_lmhead_argmax(h, final_norm, w_lm, dims: cb_dims, logits, token, ws, stre
 
 def cb_linear(x, w, y, M: int, N: int, K: int, dtype: int, stream=None):
     _check("cb_linear", lib().cb_linear(_ptr(x), _ptr(w), _ptr(y), M, N, K, dtype, _stream(stream)))
+
+
+def cb_file_read(path: str, offset: int, dst, nbytes: int, n_threads: int = 8):
+    """Read nbytes of the file at offset into dst (a pinned host tensor or raw pointer)."""
+    st = lib().cb_file_read(path.encode(), offset, _ptr(dst), nbytes, n_threads)
+    if st != CB_OK:
+        raise CBError("cb_file_read", st, lib().cb_io_error_message().decode(errors="replace"))
 
 
 def cb_kv_quantize(x, n_rows: int, W: int, dtype: int, codes, scale, zero, stream=None):

@@ -12,7 +12,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcacheblend.so")
-SOURCES = ["cb_mem.cu", "cb_gemm.cu", "cb_gemm_tc.cu", "cb_attn.cu", "cb_attn_tc.cu", "cb_api.cu"]
+SOURCES = ["cb_mem.cu", "cb_gemm.cu", "cb_gemm_tc.cu", "cb_attn.cu", "cb_attn_tc.cu", "cb_api.cu", "cb_io.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -339,6 +339,7 @@ const char* cb_status_string(int status) {
     case CB_ERR_TIMEOUT: return "timed out";
     case CB_ERR_UNSUPPORTED: return "unsupported shape";
     case CB_ERR_DEVICE: return "device-side index or wait error";
+    case CB_ERR_IO: return "storage read failed";
     default: return "unknown status";
   }
 }

@@ -5,6 +5,7 @@ layer's partial prefill, synchronize).  Marshalling and host bookkeeping only: e
 arithmetic step runs in libcacheblend's kernels."""
 from __future__ import annotations
 
+import threading
 from dataclasses import dataclass
 from typing import List, Optional, Sequence
 
@@ -254,15 +255,46 @@ class HostPool:
                 self.done[l].record(self.side)
 
 
+class FileStore:
+    """A chunk-KV pool (bf16 or 8-bit) kept in one file, the storage tier below pinned host
+    memory: every layer's tensors back to back in HostPool order, written once (offline).
+    read_layer(l) brings one layer into the HostPool's pinned buffers with cb_file_read."""
+
+    def __init__(self, path: str, host_pool: HostPool, n_threads: int = 8):
+        self.path, self.hp, self.n_threads = path, host_pool, n_threads
+        self.layout = []
+        off = 0
+        with open(path, "wb") as f:
+            for hs in host_pool.host:
+                ent = []
+                for h in hs:
+                    b = h.numel() * h.element_size()
+                    f.write(h.reshape(-1).view(torch.uint8).numpy().tobytes())
+                    ent.append((off, b))
+                    off += b
+                self.layout.append(ent)
+        self.nbytes = off
+
+    def read_layer(self, l: int):
+        for (off, b), h in zip(self.layout[l], self.hp.host[l]):
+            B.cb_file_read(self.path, off, h, b, self.n_threads)
+
+
 def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None, keep_history=False,
-              assemble: bool = True, stream=None, host_pool: Optional[HostPool] = None):
+              assemble: bool = True, stream=None, host_pool: Optional[HostPool] = None,
+              file_store: Optional[FileStore] = None):
     """One blended prefill: re-position the chunk KV of every layer, run the layer plan,
     then the lm_head argmax.  Returns the number of rows carried out of the last layer.
 
     With host_pool, every layer's chunk KV is copied from pinned host memory and
     re-positioned on a side stream, all layers queued up front; layer l waits for its own
     layer's event only where it first touches the cached rows (in the pre-check layer after
-    its Q and uncached-row K/V GEMMs), so loading overlaps recompute."""
+    its Q and uncached-row K/V GEMMs), so loading overlaps recompute.
+
+    With file_store (whose host pool is used), a loader thread reads each layer from the
+    file into pinned memory and then queues that layer's copy and re-positioning; the layer
+    loop waits on the host for the layer's read before queueing the layer (the pages'
+    generator pipeline: fetch layer l+1 while layer l computes)."""
     eng = req.eng
     dm = eng.dm
     s = dm.shape
@@ -278,9 +310,35 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
             B.cb_rope_shift(req.K[l], req.V[l], req.pool.k[l], req.pool.v[l], req.src_row, req.delta,
                             req.n_cached, dims, eng.cos_sin, eng.max_pos, st)
 
-    if host_pool is not None:
-        if host_pool.pool is not req.pool:
-            raise ValueError("host_pool must mirror the request's pool")
+    ready, errors, loader = None, [], None
+    if file_store is not None:
+        host_pool = file_store.hp
+    if host_pool is not None and host_pool.pool is not req.pool:
+        raise ValueError("host_pool must mirror the request's pool")
+    if file_store is not None:
+        hp = host_pool
+        hp.side.synchronize()              # the pinned buffers are no longer being copied from
+        hp.side.wait_stream(torch.cuda.current_stream() if stream is None else stream)
+        ready = [threading.Event() for _ in range(s.n_layers)]
+
+        def load():
+            try:
+                for l in range(s.n_layers):
+                    file_store.read_layer(l)
+                    for h, d in zip(hp.host[l], hp.dev[l]):
+                        B.cb_prefetch_layer(d, h, h.numel() * h.element_size(), hp.side, hp.done[l])
+                    if assemble:
+                        assemble_layer(l, hp.side)
+                        hp.done[l].record(hp.side)
+                    ready[l].set()
+            except BaseException as e:      # surfaced by the layer loop
+                errors.append(e)
+                for ev in ready:
+                    ev.set()
+
+        loader = threading.Thread(target=load, daemon=True)
+        loader.start()
+    elif host_pool is not None:
         host_pool.prefetch_all(torch.cuda.current_stream() if stream is None else stream,
                                assemble_layer if assemble else None)
 
@@ -294,6 +352,11 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
     if keep_history:
         req.sel_hist, req.m_hist = [], []
     for l, (mode, k) in enumerate(plan):
+        if ready is not None:
+            ready[l].wait()
+            if errors:
+                loader.join()
+                raise errors[0]
         ov = None if sel_override is None else sel_override.get(l)
         m_out = B.cb_blend_layer(dims, dm.layers_c[l], mode, req.x[cur], s_in, m_in, req.N, req.n_cached,
                                  req.K[l], req.V[l], eng.cos_sin, eng.max_pos, k, dev_mode, ov,
@@ -306,6 +369,8 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
         if keep_history:
             req.sel_hist.append(req.s[cur][:m_out].clone())
             req.m_hist.append(m_out)
+    if loader is not None:
+        loader.join()
     req.m_last = m_in
     req.x_last = req.x[cur]
     h_last = req.x[cur][m_in - 1]

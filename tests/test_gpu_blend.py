@@ -162,11 +162,12 @@ def test_blend_bf16_gqa(E):
     run_case(E, wl, 0.2, True, TOL["bf16"], check_sets=False)
 
 
-@pytest.mark.parametrize("q8", [False, True], ids=["bf16_pool", "8bit_pool"])
-def test_layer_ahead_loading_matches_resident_pool(E, q8):
+@pytest.mark.parametrize("q8,from_file", [(False, False), (True, False), (False, True), (True, True)],
+                         ids=["bf16_pool", "8bit_pool", "bf16_file", "8bit_file"])
+def test_layer_ahead_loading_matches_resident_pool(E, q8, from_file, tmp_path):
     """Loading every layer's chunk KV (bf16, or 8-bit codes with their tables) from pinned
-    host memory on a side stream, one event per layer, gives bit-identical results to the
-    device-resident pool."""
+    host memory on a side stream, one event per layer, or from a file read layer by layer
+    by a loader thread, gives bit-identical results to the device-resident pool."""
     torch = torch_mod()
     from non_prefix_kv_gb300 import binding as B
     wl = synth.Workload("bf16_small", BF16_SMALL, chunk_len=96, n_distinct=4, order=(0, 1, 2, 3), n_query=32,
@@ -189,8 +190,16 @@ def test_layer_ahead_loading_matches_resident_pool(E, q8):
     for ts in hp.dev:                # the streamed run must reload the whole pool
         for t in ts:
             t.zero_()
+    if from_file:
+        fs = E.FileStore(str(tmp_path / "chunk_store.bin"), hp)
+        for ts in hp.host:           # the pinned tier must be refilled from the file
+            for t in ts:
+                t.zero_()
     b = E.Request(eng, pool, req_h.order, req_h.tokens)
-    E.run_blend(b, plan, host_pool=hp)
+    if from_file:
+        E.run_blend(b, plan, file_store=fs)
+    else:
+        E.run_blend(b, plan, host_pool=hp)
     B.cb_sync(None)
     for l in range(wl.shape.n_layers):
         assert torch.equal(ka[l], b.K[l])

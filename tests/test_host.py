@@ -75,7 +75,7 @@ def test_load_controller(lib):
 
 
 def test_status_strings(lib):
-    for code in range(10):
+    for code in range(11):
         assert lib.cb_status_string(code)
     assert lib.cb_status_string(99) == b"unknown status"
 
@@ -151,3 +151,26 @@ def test_layer_plan_sizes_match_oracle_selection(lib):
         assert k == O.budget(wl.n_cached, ratios[l], n_cand)
         m = k + n_forced
     assert plan[1][1] == O.budget(3840, min(1.0, 1.5 * 0.15))
+
+
+def test_file_read_ranges_threads_and_errors(lib, tmp_path):
+    """The storage-tier reader returns exactly the requested byte range for any split over
+    threads (pieces of at least 4 MB), and reports missing files and short files as
+    CB_ERR_IO without touching the destination beyond the range."""
+    g = np.random.default_rng(3)
+    data = g.integers(0, 256, (9 << 20) + 12345, dtype=np.uint8)
+    path = tmp_path / "store.bin"
+    data.tofile(path)
+    for off, n, nt in [(0, len(data), 1), (0, len(data), 8), (777, (6 << 20) + 3, 3), (len(data) - 5, 5, 4),
+                       (123, 0, 2)]:
+        buf = np.full(n + 16, 0xAB, np.uint8)
+        B.cb_file_read(str(path), off, buf.ctypes.data, n, nt)
+        np.testing.assert_array_equal(buf[:n], data[off:off + n])
+        assert np.all(buf[n:] == 0xAB)
+    buf = np.zeros(64, np.uint8)
+    with pytest.raises(B.CBError) as e:
+        B.cb_file_read(str(tmp_path / "missing.bin"), 0, buf.ctypes.data, 64)
+    assert e.value.status == 10 and "missing.bin" in str(e.value)
+    with pytest.raises(B.CBError) as e:
+        B.cb_file_read(str(path), len(data) - 10, buf.ctypes.data, 64)
+    assert e.value.status == 10 and "end of file" in str(e.value)

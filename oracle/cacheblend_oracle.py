@@ -300,14 +300,40 @@ def assemble(model: dict, chunk_kv: Sequence[dict], order: Sequence[int], n_quer
     return K, V, n_cached
 
 
+def assemble_segments(model: dict, chunk_kv: Sequence[dict], segments: Sequence):
+    """Lay out a request made of segments: an int is a cached chunk (its KV re-rotated by
+    its slot's start, as in assemble), an array of token ids is uncached text (a system
+    prompt, a separator, a query) whose rows are computed, never cached ([CB-A] §vLLM
+    integration: separators between chunks; NEXT-3 reading: any number of uncached spans).
+    Returns K, V per layer with the cached rows filled, and the per-row cached mask."""
+    shape = model["shape"]
+    lens = [chunk_kv[g]["K"][0].shape[0] if isinstance(g, (int, np.integer)) else len(g) for g in segments]
+    N = int(sum(lens))
+    K = [np.zeros((N, shape.n_kv_heads, shape.head_dim), F64) for _ in range(shape.n_layers)]
+    V = [np.zeros_like(K[0]) for _ in range(shape.n_layers)]
+    cached = np.zeros(N, bool)
+    start = 0
+    for g, n in zip(segments, lens):
+        if isinstance(g, (int, np.integer)):
+            for l in range(shape.n_layers):
+                K[l][start:start + n] = rope_shift(chunk_kv[g]["K"][l], start, shape.rope_base)
+                V[l][start:start + n] = chunk_kv[g]["V"][l]
+            cached[start:start + n] = True
+        start += n
+    return K, V, cached
+
+
 def blend(model: dict, chunk_kv: Sequence[dict], order: Sequence[int], tokens: np.ndarray,
           ratios: Sequence[Optional[float]], check_layer: int = 1, gradual: bool = False,
-          dev_mode: str = "kv", sel_override: Optional[Dict[int, np.ndarray]] = None):
+          dev_mode: str = "kv", sel_override: Optional[Dict[int, np.ndarray]] = None,
+          segments: Optional[Sequence] = None):
     """CacheBlend selective KV recompute, layer by layer
     ([CB-A] §Selective recomputation Steps 1-4, §HKVD selection, §Gradual filtering;
     [CB-B] §技術の仕組み).
 
     tokens: the whole input (chunks in order, then the query suffix).
+    segments: optional general layout (see assemble_segments) replacing order + suffix:
+              every uncached row is forced, the budget counts cached rows.
     ratios: per-layer ratio (None before the check layer), see ratio_schedule.
     sel_override: optional {layer: top-k row set} replacing the HKVD choice at that layer
                   (teacher forcing: the forced rows are still added).
@@ -322,10 +348,15 @@ def blend(model: dict, chunk_kv: Sequence[dict], order: Sequence[int], tokens: n
     shape = model["shape"]
     L = shape.n_layers
     N = len(tokens)
-    n_chunk_rows = sum(chunk_kv[c]["K"][0].shape[0] for c in order)
-    K, V, n_cached = assemble(model, chunk_kv, order, N - n_chunk_rows)
-    pos_all = np.arange(N)
-    forced = set(range(n_cached, N)) | {N - 1}
+    if segments is None:
+        n_chunk_rows = sum(chunk_kv[c]["K"][0].shape[0] for c in order)
+        K, V, n_cached = assemble(model, chunk_kv, order, N - n_chunk_rows)
+        cached = np.arange(N) < n_cached
+    else:
+        K, V, cached = assemble_segments(model, chunk_kv, segments)
+        assert len(cached) == N
+        n_cached = int(cached.sum())
+    forced = set(np.nonzero(~cached)[0].tolist()) | {N - 1}
     forced_sorted = np.array(sorted(forced), dtype=np.int64)
 
     x = np.asarray(model["embed"], F64)[np.asarray(tokens)]   # hidden rows of S
@@ -337,7 +368,7 @@ def blend(model: dict, chunk_kv: Sequence[dict], order: Sequence[int], tokens: n
         if l < check_layer:
             # pre-check layer: every row; cached rows keep the re-rotated cache (R5)
             p = project_qkv(layer, a, S, shape)
-            unc = np.nonzero(S >= n_cached)[0]
+            unc = np.nonzero(~cached[S])[0]
             K[l][S[unc]] = p["k"][unc]
             V[l][S[unc]] = p["v"][unc]
             o = attend(p["q"], S, K[l], V[l])
@@ -346,7 +377,7 @@ def blend(model: dict, chunk_kv: Sequence[dict], order: Sequence[int], tokens: n
         elif l == check_layer or gradual:
             # check (or gradual) layer: fresh K/V for the carried rows, deviation vs cache
             p = project_qkv(layer, a, S, shape, want=("k", "v"))
-            cand_pos = np.array([i for i, r in enumerate(S) if r < n_cached and r not in forced],
+            cand_pos = np.array([i for i, r in enumerate(S) if cached[r] and r not in forced],
                                 dtype=np.int64)
             cand = S[cand_pos]
             if dev_mode == "kv":

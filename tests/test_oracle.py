@@ -440,3 +440,52 @@ def test_quantized_chunks_blend_stays_close():
     ratios = O.ratio_schedule(0.3, MICRO.n_layers, 1, False)
     ref = O.blend(model, q, order, tokens, ratios)
     assert len(ref["S"][1]) == O.budget(ref["n_cached"], 0.3, ref["n_cached"]) + len(ref["forced"])
+
+
+# ------------------------------------------------------------------ uncached segments
+def test_segments_in_chunk_then_query_order_equal_the_plain_blend():
+    model, pool, order, tokens, chunk_kv = micro_setup()
+    q = tokens[sum(len(pool[i]) for i in order):]
+    ratios = O.ratio_schedule(0.4, MICRO.n_layers, 1, True)
+    a = O.blend(model, chunk_kv, order, tokens, ratios, gradual=True)
+    b = O.blend(model, chunk_kv, order, tokens, ratios, gradual=True, segments=list(order) + [q])
+    for l in range(MICRO.n_layers):
+        np.testing.assert_array_equal(a["S"][l], b["S"][l])
+        np.testing.assert_array_equal(a["K"][l], b["K"][l])
+    np.testing.assert_array_equal(a["h_last"], b["h_last"])
+
+
+def test_segments_r1_equal_full_prefill_and_text_rows_always_forced():
+    """A system prompt, separators between chunks and a query: at r = 1 the blend is the
+    full prefill (I1); at any r every uncached row is in every layer's set."""
+    model, pool, order, tokens, chunk_kv = micro_setup()
+    g = synth.rng(7, synth.P_TOKENS)
+    sys_p, sep, q = (g.integers(0, MICRO.vocab, n).astype(np.int32) for n in (3, 1, 4))
+    segs = [sys_p, 0, sep, 2, sep, 1, q]
+    toks = np.concatenate([s if not isinstance(s, int) else pool[s] for s in segs])
+    full = O.full_prefill(model, toks, 0)
+    ref = O.blend(model, chunk_kv, None, toks, O.ratio_schedule(1.0, MICRO.n_layers, 1, False), segments=segs)
+    for l in range(MICRO.n_layers):
+        np.testing.assert_allclose(ref["K"][l], full["K"][l], rtol=1e-9, atol=1e-10)
+    np.testing.assert_allclose(ref["h_last"], full["x"][-1][-1], rtol=1e-9, atol=1e-10)
+    ref = O.blend(model, chunk_kv, None, toks, O.ratio_schedule(0.25, MICRO.n_layers, 1, True), gradual=True,
+                  segments=segs)
+    _, _, cached = O.assemble_segments(model, chunk_kv, segs)
+    text_rows = set(np.nonzero(~cached)[0].tolist()) | {len(toks) - 1}
+    for S in ref["S"][1:]:
+        assert text_rows <= set(S.tolist())
+    assert len(ref["S"][1]) == O.budget(int(cached.sum()), O.ratio_schedule(0.25, MICRO.n_layers, 1, True)[1],
+                                        int(cached.sum())) + len(text_rows)
+
+
+def test_prefix_caching_baseline_is_exact():
+    """Reusing only a true prefix (the first chunk) and recomputing every later row at every
+    layer reproduces the full prefill: the prefix-caching comparison workload."""
+    model, pool, order, tokens, chunk_kv = micro_setup()
+    rest = tokens[len(pool[order[0]]):]
+    full = O.full_prefill(model, tokens, 0)
+    ref = O.blend(model, chunk_kv, None, tokens, O.ratio_schedule(0.0, MICRO.n_layers, 1, False),
+                  segments=[order[0], rest])
+    for l in range(MICRO.n_layers):
+        np.testing.assert_allclose(ref["K"][l], full["K"][l], rtol=1e-9, atol=1e-10)
+    np.testing.assert_allclose(ref["h_last"], full["x"][-1][-1], rtol=1e-9, atol=1e-10)

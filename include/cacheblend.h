@@ -277,18 +277,30 @@ int cb_o_proj_ffn(const void* attn, const void* x_res, int32_t M, const cb_dims*
  *                  the new rows are produced (one fp32 partial per 128 columns, summed in
  *                  column order); fp32 runs the standalone deviation kernel.
  *   m_out_host   : receives m_out (known on the host before any launch: no sync).
- *   kv_ready     : a cudaEvent_t marking when the cached rows of k_cache/v_cache have been
- *                  written (e.g. re-positioned on a loading stream), or NULL.  The layer
- *                  waits for it just before its first access to the cached rows: in
- *                  PRECHECK after the Q and uncached-row K/V GEMMs (they touch only rows
- *                  >= n_cached), so those overlap the load ([CB-A] §Pipelining).
+ *   opts         : optional extras (NULL = none), see cb_layer_opts.
  * x_out must not alias x_in. */
+typedef struct {
+  /* Uncached rows anywhere in the request (a system prompt, separators, several query
+   * spans): [n_tok] device bytes, nonzero = forced row (recomputed at every layer).  It
+   * must mark row n_tok-1; n_forced is its count.  NULL = the default layout (forced
+   * rows = [n_cached, n_tok) plus row n_tok-1).  With a mask, n_cached is not used (the
+   * caller's k_budget already counts the cached rows), candidates are the unmarked rows
+   * of the incoming set, and m_out = k_budget + n_forced. */
+  const uint8_t* forced_mask;
+  int32_t n_forced;
+  /* A cudaEvent_t marking when the cached rows of k_cache/v_cache have been written (e.g.
+   * re-positioned on a loading stream), or NULL.  The layer waits for it just before its
+   * first access to the cached rows: in PRECHECK after the Q and uncached-row K/V GEMMs,
+   * which touch only forced rows, so those overlap the load ([CB-A] §Pipelining). */
+  void* kv_ready;
+} cb_layer_opts;
+
 int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode,
                    const void* x_in, const int32_t* s_in, int32_t m_in,
                    int64_t n_tok, int64_t n_cached, void* k_cache, void* v_cache,
                    const float* cos_sin, int32_t max_pos, int32_t k_budget, int32_t dev_mode,
                    const int32_t* sel_override, void* x_out, int32_t* s_out,
-                   int32_t* m_out_host, float* scores_out, void* kv_ready, void* ws,
+                   int32_t* m_out_host, float* scores_out, const cb_layer_opts* opts, void* ws,
                    size_t ws_bytes, void* stream);
 
 /* Standard causal prefill of n tokens at positions pos0..pos0+n-1 through n_layers

@@ -25,6 +25,10 @@ class CBError(RuntimeError):
         self.status = status
 
 
+class cb_layer_opts(C.Structure):
+    _fields_ = [("forced_mask", C.c_void_p), ("n_forced", C.c_int32), ("kv_ready", C.c_void_p)]
+
+
 class cb_dims(C.Structure):
     _fields_ = [("d_model", C.c_int32), ("n_heads", C.c_int32), ("n_kv_heads", C.c_int32),
                 ("head_dim", C.c_int32), ("d_ff", C.c_int32), ("vocab", C.c_int32),
@@ -70,7 +74,8 @@ _PROTOS = {
     "cb_partial_attention": (C.c_int, [_P, _P, _I32, _P, _P, _I64, C.POINTER(cb_dims), _P, _P, _SZ, _P]),
     "cb_o_proj_ffn": (C.c_int, [_P, _P, _I32, C.POINTER(cb_dims), C.POINTER(cb_layer_w), _P, _P, _SZ, _P]),
     "cb_blend_layer": (C.c_int, [C.POINTER(cb_dims), C.POINTER(cb_layer_w), _I32, _P, _P, _I32, _I64, _I64,
-                                 _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, C.POINTER(_I32), _P, _P, _P, _SZ, _P]),
+                                 _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, C.POINTER(_I32), _P,
+                                 C.POINTER(cb_layer_opts), _P, _SZ, _P]),
     "cb_full_prefill": (C.c_int, [C.POINTER(cb_dims), _I32, C.POINTER(cb_layer_w), _P, _P, _I32, _I32,
                                   C.POINTER(_P), C.POINTER(_P), _P, _P, _P, _I32, _P, _SZ, _P]),
     "cb_lmhead_argmax": (C.c_int, [_P, _P, _P, C.POINTER(cb_dims), _P, _P, _P, _SZ, _P]),
@@ -220,15 +225,20 @@ def cb_o_proj_ffn(attn, x_res, M: int, dims: cb_dims, w: cb_layer_w, x_out, ws, 
 
 def cb_blend_layer(dims: cb_dims, w: cb_layer_w, mode: int, x_in, s_in, m_in: int, n_tok: int, n_cached: int,
                    k_cache, v_cache, cos_sin, max_pos: int, k_budget: int, dev_mode: int, sel_override,
-                   x_out, s_out, scores_out, ws, stream=None, kv_ready=None) -> int:
+                   x_out, s_out, scores_out, ws, stream=None, kv_ready=None, forced_mask=None,
+                   n_forced: int = 0) -> int:
     """kv_ready: a torch.cuda.Event (or raw cudaEvent_t) the layer waits for just before it
-    first touches the cached rows, or None."""
+    first touches the cached rows, or None.  forced_mask/n_forced: uncached rows anywhere
+    (a uint8 device tensor over the tokens, marking the last row too), or None."""
     m_out = _I32(0)
-    ev = kv_ready if (kv_ready is None or isinstance(kv_ready, int)) else kv_ready.cuda_event
+    opts = None
+    if kv_ready is not None or forced_mask is not None:
+        ev = kv_ready if (kv_ready is None or isinstance(kv_ready, int)) else kv_ready.cuda_event
+        opts = C.byref(cb_layer_opts(_ptr(forced_mask), n_forced if forced_mask is not None else 0, ev))
     _check("cb_blend_layer", lib().cb_blend_layer(
         C.byref(dims), C.byref(w), mode, _ptr(x_in), _ptr(s_in), m_in, n_tok, n_cached, _ptr(k_cache),
         _ptr(v_cache), _ptr(cos_sin), max_pos, k_budget, dev_mode, _ptr(sel_override), _ptr(x_out),
-        _ptr(s_out), C.byref(m_out), _ptr(scores_out), ev, _ptr(ws), _nbytes(ws), _stream(stream)))
+        _ptr(s_out), C.byref(m_out), _ptr(scores_out), opts, _ptr(ws), _nbytes(ws), _stream(stream)))
     return int(m_out.value)
 
 

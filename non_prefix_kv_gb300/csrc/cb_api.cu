@@ -122,9 +122,15 @@ double gemm_bytes(int dt, const GemmDesc& g) {
   CB_LAUNCH(CB_PROF_DEVIATION, 0, (nc), (W), (usev), 3.0 * (nc) * (W) * ((usev) ? 2 : 1),        \
             (double)(nc) * (W) * esize(dt) * ((usev) ? 4 : 2) + 4.0 * (nc), s,                   \
             launch_deviation(dt, kn, vn, kr, vr, nr, rr, nc, W, usev, sc, s))
-#define L_DEVRED(part, np, ld, nc, W, usev, sc, s)                                               \
+#define L_DEVRED(part, np, ld, nc, cpos, W, usev, sc, s)                                         \
   CB_LAUNCH(CB_PROF_DEVIATION, 1, (nc), (W), (usev), (double)(nc) * (np), 4.0 * (nc) * ((np) + 1), s, \
-            launch_dev_reduce(part, np, ld, nc, sc, s))
+            launch_dev_reduce(part, np, ld, nc, cpos, sc, s))
+#define L_SPLIT(rows, m, mask, mlen, nf, cp, cr, fp, fr, s)                                      \
+  CB_LAUNCH(CB_PROF_INDEX, 1, (m), 0, 0, 0.0, 21.0 * (m), s,                                      \
+            launch_split_rows(rows, m, mask, mlen, nf, cp, cr, fp, fr, s))
+#define L_MERGE(ord, k, cr, cp, fr, fp, nf, so, ko, s)                                           \
+  CB_LAUNCH(CB_PROF_INDEX, 2, (k) + (nf), 0, 0, 0.0, 16.0 * ((k) + (nf)), s,                     \
+            launch_merge_sel(ord, k, cr, cp, fr, fp, nf, so, ko, s))
 #define L_TOPK(sc, n, k, ord, s) \
   CB_LAUNCH(CB_PROF_TOPK, 0, (n), (k), 0, 0.0, 4.0 * (n) + 4.0 * (k), s, launch_topk(sc, n, k, ord, s))
 #define L_MAP(ord, k, map, out, s) \
@@ -198,7 +204,7 @@ struct Carver {
 struct LayerWs {
   void *a, *q, *knew, *vnew, *attn, *h, *b, *act, *xg, *ag, *xa, *xb, *attn_ws;
   float *scores, *hn, *logits, *dev_part;
-  int32_t *ord, *keep, *pos, *rows;
+  int32_t *ord, *keep, *pos, *rows, *cpos, *crows, *fpos, *frows;
 };
 
 // deviation partials per row of the K/V GEMM: one per half of each column tile
@@ -230,6 +236,10 @@ LayerWs carve_layer(Carver& c, const cb_dims* d, int64_t R, int64_t M) {
   w.keep = static_cast<int32_t*>(c.take(R * 4));
   w.pos = static_cast<int32_t*>(c.take(R * 4));
   w.rows = static_cast<int32_t*>(c.take(R * 4));
+  w.cpos = static_cast<int32_t*>(c.take(R * 4));
+  w.crows = static_cast<int32_t*>(c.take(R * 4));
+  w.fpos = static_cast<int32_t*>(c.take(R * 4));
+  w.frows = static_cast<int32_t*>(c.take(R * 4));
   w.hn = static_cast<float*>(c.take(d->d_model * 4));
   w.logits = static_cast<float*>(c.take((size_t)d->vocab * 4));
   const size_t aw = attention_ws_bytes(d->dtype, std::max(R, M), d->n_heads, d->head_dim);
@@ -583,7 +593,7 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
                    int32_t m_in, int64_t n_tok, int64_t n_cached, void* k_cache, void* v_cache,
                    const float* cos_sin, int32_t max_pos, int32_t k_budget, int32_t dev_mode,
                    const int32_t* sel_override, void* x_out, int32_t* s_out, int32_t* m_out_host,
-                   float* scores_out, void* kv_ready, void* ws, size_t ws_bytes, void* stream) {
+                   float* scores_out, const cb_layer_opts* opts, void* ws, size_t ws_bytes, void* stream) {
   int st = check_dims(dims);
   if (st || (st = check_w(w))) return st;
   if (!x_in || !k_cache || !v_cache || !cos_sin || !x_out || !s_out || !m_out_host)
@@ -594,8 +604,13 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
   if (n_tok > max_pos) return fail(CB_ERR_SHAPE, "rope table (%d) shorter than n_tok (%lld)", max_pos, (long long)n_tok);
   if (dev_mode != CB_DEV_KV && dev_mode != CB_DEV_K) return fail(CB_ERR_INVALID_ARG, "dev_mode");
   const int N = (int)n_tok;
-  const int f0 = (int)std::min<int64_t>(n_cached, n_tok - 1);   // first forced row
-  const int n_forced = N - f0;
+  const uint8_t* fmask = opts ? opts->forced_mask : nullptr;
+  void* kv_ready = opts ? opts->kv_ready : nullptr;
+  if (fmask && (opts->n_forced < 1 || opts->n_forced > N))
+    return fail(CB_ERR_SHAPE, "n_forced %d outside [1, n_tok]", opts ? opts->n_forced : 0);
+  // default layout: forced rows [f0, N) (the uncached suffix and the last row)
+  const int f0 = (int)std::min<int64_t>(n_cached, n_tok - 1);
+  const int n_forced = fmask ? opts->n_forced : N - f0;
   const int qc = dims->n_heads * dims->head_dim, W = dims->n_kv_heads * dims->head_dim;
   const size_t B = esize(dims->dtype);
   const bool use_v = dev_mode == CB_DEV_KV;
@@ -613,7 +628,12 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
       L_IOTA(s_out, N, 0, s);
       L_RMSNORM(dims->dtype, dims->dtype, L.a, x_in, nullptr, w->attn_norm, N, dims->d_model, dims->rms_eps, s);
       L_GEMM(dims->dtype, qkv_desc(dims, w, L.a, N, 0, qc, L.q, nullptr, nullptr, s_out, nullptr, cos_sin, max_pos), s);
-      if (N > n_cached) {
+      if (fmask) {
+        // K/V of the forced rows, wherever they are: gather their normalised rows first
+        L_SPLIT(nullptr, N, fmask, N, n_forced, L.cpos, L.crows, L.fpos, L.frows, s);
+        L_COPY(L.ag, nullptr, L.a, L.frows, n_forced, (int64_t)dims->d_model * B, n_forced, N, s);
+        L_GEMM(dims->dtype, qkv_desc(dims, w, L.ag, n_forced, qc, 2 * W, nullptr, k_cache, v_cache, L.frows, L.frows, cos_sin, max_pos), s);
+      } else if (N > n_cached) {
         const int nu = N - (int)n_cached;
         const void* a_u = static_cast<const char*>(L.a) + (size_t)n_cached * dims->d_model * B;
         L_GEMM(dims->dtype, qkv_desc(dims, w, a_u, nu, qc, 2 * W, nullptr, k_cache, v_cache, s_out + n_cached, s_out + n_cached, cos_sin, max_pos), s);
@@ -628,7 +648,7 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
       if (check && m_in != N) return fail(CB_ERR_SHAPE, "CHECK needs m_in == n_tok");
       if (!check && (m_in < n_forced || m_in > N)) return fail(CB_ERR_SHAPE, "GRADUAL needs n_forced <= m_in <= n_tok");
       if (!check && !s_in && m_in != N) return fail(CB_ERR_INVALID_ARG, "GRADUAL needs s_in");
-      const int n_cand = check ? f0 : m_in - n_forced;
+      const int n_cand = (check && !fmask) ? f0 : m_in - n_forced;
       if (k_budget < 0 || k_budget > n_cand)
         return fail(CB_ERR_SHAPE, "k_budget %d outside [0, %d]", k_budget, n_cand);
       const int M = k_budget + n_forced;
@@ -640,6 +660,15 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         rows_in = L.rows;
       }
       float* sc = scores_out ? scores_out : L.scores;
+      // candidates: positions (GEMM rows) and rows of the cached, unforced incoming rows;
+      // without a mask they are the leading n_cand rows of the incoming set
+      const int32_t* cpos = nullptr;
+      const int32_t* crows = rows_in;
+      if (fmask) {
+        L_SPLIT(rows_in, m_in, fmask, N, n_forced, L.cpos, L.crows, L.fpos, L.frows, s);
+        cpos = L.cpos;
+        crows = L.crows;
+      }
       L_RMSNORM(dims->dtype, dims->dtype, L.a, x_in, nullptr, w->attn_norm, m_in, dims->d_model, dims->rms_eps, s);
       WAIT_CACHED_ROWS();
       GemmDesc gkv = qkv_desc(dims, w, L.a, m_in, qc, 2 * W, nullptr, L.knew, L.vnew, rows_in, nullptr, cos_sin, max_pos);
@@ -653,18 +682,21 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         gkv.epi.ref_rows = N;
         gkv.epi.dev_use_v = use_v ? 1 : 0;
         L_GEMM(dims->dtype, gkv, s);
-        L_DEVRED(L.dev_part, dev_parts(dims), m_in, n_cand, W, use_v, sc, s);
+        L_DEVRED(L.dev_part, dev_parts(dims), m_in, n_cand, cpos, W, use_v, sc, s);
       } else {
         L_GEMM(dims->dtype, gkv, s);
-        L_DEV(dims->dtype, L.knew, L.vnew, k_cache, v_cache, nullptr, rows_in, n_cand, W, use_v, sc, s);
+        L_DEV(dims->dtype, L.knew, L.vnew, k_cache, v_cache, cpos, crows, n_cand, W, use_v, sc, s);
       }
       if (k_budget > 0) {
         if (sel_override)
-          L_R2P(sel_override, k_budget, check ? nullptr : rows_in, n_cand, L.ord, s);
+          L_R2P(sel_override, k_budget, (check && !fmask) ? nullptr : crows, n_cand, L.ord, s);
         else
           L_TOPK(sc, n_cand, k_budget, L.ord, s);
       }
-      L_BUILD_SEL(L.ord, k_budget, rows_in, f0, m_in - n_forced, n_forced, s_out, L.keep, s);
+      if (fmask)
+        L_MERGE(L.ord, k_budget, L.crows, L.cpos, L.frows, L.fpos, n_forced, s_out, L.keep, s);
+      else
+        L_BUILD_SEL(L.ord, k_budget, rows_in, f0, m_in - n_forced, n_forced, s_out, L.keep, s);
       // Step 3, KV expansion: the recomputed K/V of S replace the cached rows
       L_COPY(k_cache, s_out, L.knew, L.keep, M, (int64_t)W * B, N, m_in, s);
       L_COPY(v_cache, s_out, L.vnew, L.keep, M, (int64_t)W * B, N, m_in, s);

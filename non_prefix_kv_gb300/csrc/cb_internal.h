@@ -85,8 +85,14 @@ cudaError_t launch_copy_rows(void* dst, const int32_t* dst_idx, const void* src,
 cudaError_t launch_rmsnorm(int dt_in, int dt_out, void* out, const void* x,
                            const int32_t* rows, const void* g, int64_t n, int d, float eps,
                            cudaStream_t s);
-cudaError_t launch_dev_reduce(const float* part, int n_parts, int64_t ld, int n_cand, float* scores,
-                              cudaStream_t s);
+cudaError_t launch_dev_reduce(const float* part, int n_parts, int64_t ld, int n_cand, const int32_t* cand_pos,
+                              float* scores, cudaStream_t s);
+cudaError_t launch_split_rows(const int32_t* rows_in, int m, const uint8_t* mask, int64_t mask_len,
+                              int n_forced, int32_t* cand_pos, int32_t* cand_rows, int32_t* forced_pos,
+                              int32_t* forced_rows, cudaStream_t s);
+cudaError_t launch_merge_sel(const int32_t* ord, int k, const int32_t* cand_rows, const int32_t* cand_pos,
+                             const int32_t* forced_rows, const int32_t* forced_pos, int nf, int32_t* s_out,
+                             int32_t* keep_out, cudaStream_t s);
 cudaError_t launch_deviation(int dt, const void* kn, const void* vn, const void* kr,
                              const void* vr, const int32_t* new_row, const int32_t* ref_row,
                              int n_cand, int W, int use_v, float* scores, cudaStream_t s);

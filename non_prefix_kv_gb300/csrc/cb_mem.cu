@@ -420,21 +420,22 @@ __global__ void __launch_bounds__(256) k_deviation(const T* __restrict__ kn, con
 // scores[c] = sum over column tiles t (in order) of part[t][c], the per-tile partials the
 // Q/K/V GEMM epilogue leaves when it computes the deviation in place.
 __global__ void k_dev_reduce(const float* __restrict__ part, int n_parts, int64_t ld, int n_cand,
-                             float* __restrict__ scores) {
+                             const int32_t* __restrict__ cand_pos, float* __restrict__ scores) {
   pdl_wait();
   pdl_trigger();
   for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < n_cand; c += gridDim.x * blockDim.x) {
+    const int64_t row = cand_pos ? (int64_t)cand_pos[c] : c;
     float acc = 0.f;
-    for (int t = 0; t < n_parts; ++t) acc += part[t * ld + c];
+    for (int t = 0; t < n_parts; ++t) acc += part[t * ld + row];
     scores[c] = acc;
     if (!isfinite(acc)) atomicOr(&g_err_mem, ERRBIT_NONFINITE);
   }
 }
 
-cudaError_t launch_dev_reduce(const float* part, int n_parts, int64_t ld, int n_cand, float* scores,
-                              cudaStream_t s) {
+cudaError_t launch_dev_reduce(const float* part, int n_parts, int64_t ld, int n_cand, const int32_t* cand_pos,
+                              float* scores, cudaStream_t s) {
   if (n_cand == 0) return cudaSuccess;
-  { const cudaError_t e_ = launch_k(k_dev_reduce, dim3(grid_for(n_cand, 256)), dim3(256), 0, s, part, n_parts, ld, n_cand, scores); if (e_ != cudaSuccess) return e_; }
+  { const cudaError_t e_ = launch_k(k_dev_reduce, dim3(grid_for(n_cand, 256)), dim3(256), 0, s, part, n_parts, ld, n_cand, cand_pos, scores); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
@@ -622,6 +623,108 @@ cudaError_t launch_build_sel(const int32_t* ord, int k, const int32_t* cand_row,
   if (n == 0) return cudaSuccess;
   { const cudaError_t e_ = launch_k(k_build_sel, dim3((n + 255) / 256), dim3(256), 0, s, ord, k, cand_row, forced_row0, forced_pos0, n_forced,
                                              s_out, keep_out); if (e_ != cudaSuccess) return e_; }
+  return cudaGetLastError();
+}
+
+// General row sets (uncached spans anywhere in the request): splits the ascending input
+// set rows_in[0..m) (null: 0..m-1) by the forced-row mask into the candidates (cached,
+// unforced) and the forced rows, each list ascending with the rows' positions in the input
+// set.  One block walks the set in tiles with a block scan; a forced count other than
+// n_forced, or a row outside the mask, records ERRBIT_INDEX.
+__global__ void __launch_bounds__(1024) k_split_rows(const int32_t* __restrict__ rows_in, int m,
+                                                     const uint8_t* __restrict__ mask, int64_t mask_len,
+                                                     int n_forced, int32_t* __restrict__ cand_pos,
+                                                     int32_t* __restrict__ cand_rows,
+                                                     int32_t* __restrict__ forced_pos,
+                                                     int32_t* __restrict__ forced_rows) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int sh[32];
+  int base_f = 0, base_c = 0;
+  const int n_cand = m - n_forced;
+  for (int t0 = 0; t0 < m; t0 += blockDim.x) {
+    const int i = t0 + threadIdx.x;
+    int r = -1, f = 0;
+    if (i < m) {
+      r = rows_in ? rows_in[i] : i;
+      if (r < 0 || r >= mask_len) {
+        atomicOr(&g_err_mem, ERRBIT_INDEX);
+        f = 1;
+      } else {
+        f = mask[r] != 0;
+      }
+    }
+    int tot;
+    const int pf = block_excl_scan(f, &tot, sh);
+    if (i < m) {
+      if (f) {
+        const int o = base_f + pf;
+        if (o < n_forced) {
+          forced_pos[o] = i;
+          forced_rows[o] = r;
+        }
+      } else {
+        const int o = base_c + (i - t0) - pf;
+        if (o < n_cand) {
+          cand_pos[o] = i;
+          cand_rows[o] = r;
+        }
+      }
+    }
+    base_f += tot;
+    base_c += min((int)blockDim.x, m - t0) - tot;
+  }
+  if (threadIdx.x == 0 && base_f != n_forced) atomicOr(&g_err_mem, ERRBIT_INDEX);
+}
+
+cudaError_t launch_split_rows(const int32_t* rows_in, int m, const uint8_t* mask, int64_t mask_len,
+                              int n_forced, int32_t* cand_pos, int32_t* cand_rows, int32_t* forced_pos,
+                              int32_t* forced_rows, cudaStream_t s) {
+  if (m == 0) return cudaSuccess;
+  { const cudaError_t e_ = launch_k(k_split_rows, dim3(1), dim3(1024), 0, s, rows_in, m, mask, mask_len, n_forced, cand_pos, cand_rows, forced_pos, forced_rows); if (e_ != cudaSuccess) return e_; }
+  return cudaGetLastError();
+}
+
+// S = candidate rows of the top-k ordinals merged with the forced rows, ascending; keep_out
+// gives each row's position in the layer's input set.  Both lists are ascending and
+// disjoint, so an element's output index is its own index plus the number of elements of
+// the other list below it (a binary search).
+__global__ void k_merge_sel(const int32_t* __restrict__ ord, int k, const int32_t* __restrict__ cand_rows,
+                            const int32_t* __restrict__ cand_pos, const int32_t* __restrict__ forced_rows,
+                            const int32_t* __restrict__ forced_pos, int nf, int32_t* __restrict__ s_out,
+                            int32_t* __restrict__ keep_out) {
+  pdl_wait();
+  pdl_trigger();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < k) {
+    const int o = ord[i];
+    const int r = cand_rows[o];
+    int lo = 0, hi = nf;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (forced_rows[mid] < r) lo = mid + 1; else hi = mid;
+    }
+    s_out[i + lo] = r;
+    if (keep_out) keep_out[i + lo] = cand_pos[o];
+  } else if (i < k + nf) {
+    const int j = i - k;
+    const int r = forced_rows[j];
+    int lo = 0, hi = k;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (cand_rows[ord[mid]] < r) lo = mid + 1; else hi = mid;
+    }
+    s_out[j + lo] = r;
+    if (keep_out) keep_out[j + lo] = forced_pos[j];
+  }
+}
+
+cudaError_t launch_merge_sel(const int32_t* ord, int k, const int32_t* cand_rows, const int32_t* cand_pos,
+                             const int32_t* forced_rows, const int32_t* forced_pos, int nf, int32_t* s_out,
+                             int32_t* keep_out, cudaStream_t s) {
+  const int n = k + nf;
+  if (n == 0) return cudaSuccess;
+  { const cudaError_t e_ = launch_k(k_merge_sel, dim3((n + 255) / 256), dim3(256), 0, s, ord, k, cand_rows, cand_pos, forced_rows, forced_pos, nf, s_out, keep_out); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 

@@ -165,25 +165,54 @@ class BlendEngine:
 
 
 class Request:
-    """Device state of one blended-prefill request: chunk order, token ids, the blended
-    K/V cache of every layer, hidden-row buffers."""
+    """Device state of one blended-prefill request: the row layout (cached chunk slots and
+    uncached spans), token ids, the blended K/V cache of every layer, hidden-row buffers.
 
-    def __init__(self, eng: BlendEngine, pool: ChunkPool, order: Sequence[int], tokens: np.ndarray):
+    Default layout: the chunks of `order` back to back, then the uncached query suffix.
+    With `segments` (each an int chunk id or an array of uncached token ids: a system
+    prompt, separators, query spans, in any order) the uncached rows are given to the
+    library as a forced-row mask; `tokens` is then the whole input in segment order."""
+
+    def __init__(self, eng: BlendEngine, pool, order: Sequence[int], tokens: np.ndarray, segments=None):
         s = eng.dm.shape
         dev = eng.device
         dt = torch_dtype(s)
         self.eng, self.pool = eng, pool
-        self.order = list(order)
-        self.n_cached = int(sum(pool.lens[c] for c in order))
         self.N = int(len(tokens))
+        if segments is None:
+            segments = list(order) + ([np.zeros(self.N - int(sum(pool.lens[c] for c in order)), np.int32)]
+                                      if self.N > sum(pool.lens[c] for c in order) else [])
+            general = False
+        else:
+            general = True
+        self.segments = list(segments)
+        self.order = [g for g in self.segments if isinstance(g, (int, np.integer))]
         src, delta, qrow = [], [], []
+        self.runs = []                                # (first blended row, first cached index, rows)
+        cached = np.zeros(self.N, bool)
         start = 0
-        for c in order:
-            n = pool.lens[c]
-            src.extend(range(pool.offsets[c], pool.offsets[c] + n))
-            delta.extend([start] * n)                 # p - p' = slot start (p' = local position)
-            qrow.extend([c] * n)                      # chunk of the row (8-bit pool tables)
+        for g in self.segments:
+            if isinstance(g, (int, np.integer)):
+                n = pool.lens[g]
+                if self.runs and self.runs[-1][0] + self.runs[-1][2] == start:
+                    r0, c0, m = self.runs[-1]
+                    self.runs[-1] = (r0, c0, m + n)
+                else:
+                    self.runs.append((start, len(src), n))
+                src.extend(range(pool.offsets[g], pool.offsets[g] + n))
+                delta.extend([start] * n)             # p - p' = slot start (p' = local position)
+                qrow.extend([int(g)] * n)             # chunk of the row (8-bit pool tables)
+                cached[start:start + n] = True
+            else:
+                n = len(g)
             start += n
+        if start != self.N:
+            raise ValueError(f"segments cover {start} rows, tokens {self.N}")
+        self.n_cached = int(cached.sum())             # the HKVD budget counts these rows
+        forced = ~cached
+        forced[self.N - 1] = True
+        self.n_forced = int(forced.sum())
+        self.forced_mask = torch.from_numpy(forced.astype(np.uint8)).to(dev) if general else None
         self.src_row = torch.tensor(src, dtype=torch.int32, device=dev)
         self.delta = torch.tensor(delta, dtype=torch.int32, device=dev)
         self.qrow = torch.tensor(qrow, dtype=torch.int32, device=dev)
@@ -199,13 +228,34 @@ class Request:
         self.sel_hist: List[torch.Tensor] = []
         self.m_hist: List[int] = []
 
+    start_rows = None      # device int32 rows entering the first layer (None: every row)
+    start_tokens = None
+
+    def plan(self, ratios: Sequence[Optional[float]], check_layer: int = 1, gradual: bool = False):
+        return layer_plan(self.eng.dm.shape, self.N, self.n_cached, ratios, check_layer, gradual,
+                          n_forced=self.n_forced)
+
+    def prefix_cache_plan(self):
+        """The prefix-caching comparison workload: only the cached rows before the first
+        uncached row are reused (a true prefix, exact), every later row is recomputed at
+        every layer.  Sets the first layer's rows and returns the all-steady plan."""
+        first = int(np.argmax(self.forced_mask.cpu().numpy() != 0)) if self.forced_mask is not None else \
+            min(self.n_cached, self.N - 1)
+        rows = np.arange(first, self.N, dtype=np.int32)
+        self.start_rows = torch.from_numpy(rows).to(self.tokens.device)
+        self.start_tokens = torch.from_numpy(self.tokens_host[first:].copy()).to(self.tokens.device)
+        return [(B.CB_LAYER_STEADY, 0)] * self.eng.dm.shape.n_layers
+
 
 def layer_plan(shape: ModelShape, n_tok: int, n_cached: int, ratios: Sequence[Optional[float]],
-               check_layer: int = 1, gradual: bool = False):
+               check_layer: int = 1, gradual: bool = False, n_forced: Optional[int] = None):
     """Host bookkeeping of the per-layer mode and HKVD budget (k and |S| are known before
-    any launch, so the loop never waits on the device)."""
-    f0 = min(n_cached, n_tok - 1)
-    n_forced = n_tok - f0
+    any launch, so the loop never waits on the device).  n_cached is the budget's base (the
+    cached rows); n_forced the always-recomputed rows (default: the rows after the cached
+    prefix, and at least the last row)."""
+    if n_forced is None:
+        n_forced = n_tok - min(n_cached, n_tok - 1)
+    f0 = n_tok - n_forced                  # candidates at the check layer
     plan = []
     m_in = n_tok
     for l in range(shape.n_layers):
@@ -301,14 +351,18 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
     dims = dm.dims
     esz = 2 if s.dtype == "bf16" else 4
     def assemble_layer(l, st):
-        if isinstance(req.pool, ChunkPoolQ8):
-            p = req.pool
-            B.cb_rope_shift_q8(req.K[l], req.V[l], p.kq[l], p.vq[l], p.ks[l], p.kz[l], p.vs[l], p.vz[l],
-                               req.src_row, req.n_pool_rows, req.qrow, len(p.lens), req.delta, req.n_cached, dims,
-                               eng.cos_sin, eng.max_pos, st)
-        else:
-            B.cb_rope_shift(req.K[l], req.V[l], req.pool.k[l], req.pool.v[l], req.src_row, req.delta,
-                            req.n_cached, dims, eng.cos_sin, eng.max_pos, st)
+        # one re-positioning pass per run of adjacent chunk slots
+        for r0, c0, n in req.runs:
+            kd, vd = req.K[l][r0:r0 + n], req.V[l][r0:r0 + n]
+            src, dl = req.src_row[c0:c0 + n], req.delta[c0:c0 + n]
+            if isinstance(req.pool, ChunkPoolQ8):
+                p = req.pool
+                B.cb_rope_shift_q8(kd, vd, p.kq[l], p.vq[l], p.ks[l], p.kz[l], p.vs[l], p.vz[l], src,
+                                   req.n_pool_rows, req.qrow[c0:c0 + n], len(p.lens), dl, n, dims, eng.cos_sin,
+                                   eng.max_pos, st)
+            else:
+                B.cb_rope_shift(kd, vd, req.pool.k[l], req.pool.v[l], src, dl, n, dims, eng.cos_sin, eng.max_pos,
+                                st)
 
     ready, errors, loader = None, [], None
     if file_store is not None:
@@ -342,13 +396,18 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
         host_pool.prefetch_all(torch.cuda.current_stream() if stream is None else stream,
                                assemble_layer if assemble else None)
 
-    B.cb_gather_rows(req.x[0], dm.embed, req.tokens, req.N, s.d_model * esz, stream)
+    if req.start_rows is None:
+        B.cb_gather_rows(req.x[0], dm.embed, req.tokens, req.N, s.d_model * esz, stream)
+        m_in, s_in = req.N, None
+    else:
+        # the first layer starts from a subset of rows (e.g. everything after a reused prefix)
+        m_in = int(req.start_rows.numel())
+        B.cb_gather_rows(req.x[0], dm.embed, req.start_tokens, m_in, s.d_model * esz, stream)
+        s_in = req.start_rows
     if assemble and host_pool is None:
         for l in range(s.n_layers):
             assemble_layer(l, stream)
     cur = 0
-    m_in = req.N
-    s_in = None
     if keep_history:
         req.sel_hist, req.m_hist = [], []
     for l, (mode, k) in enumerate(plan):
@@ -362,7 +421,8 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
                                  req.K[l], req.V[l], eng.cos_sin, eng.max_pos, k, dev_mode, ov,
                                  req.x[1 - cur], req.s[1 - cur],
                                  req.scores if mode in (B.CB_LAYER_CHECK, B.CB_LAYER_GRADUAL) else None,
-                                 eng.ws, stream, kv_ready=None if host_pool is None else host_pool.done[l])
+                                 eng.ws, stream, kv_ready=None if host_pool is None else host_pool.done[l],
+                                 forced_mask=req.forced_mask, n_forced=req.n_forced)
         cur = 1 - cur
         s_in = req.s[cur]
         m_in = m_out

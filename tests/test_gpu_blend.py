@@ -53,16 +53,33 @@ def q8_pool_from_codes(E, pool, chunk_kv, dims):
     return q
 
 
-def run_case(E, wl, r, gradual, tol, check_sets=True, q8=False):
+def with_text_segments(req_h, vocab, seed=11):
+    """A system prompt, separators between the chunks and the query: uncached spans spread
+    through the request (chunk order as in req_h)."""
+    g = synth.rng(seed, synth.P_TOKENS)
+    sys_p, sep = g.integers(0, vocab, 7).astype(np.int32), g.integers(0, vocab, 2).astype(np.int32)
+    q = g.integers(0, vocab, 20).astype(np.int32)
+    segs = [sys_p]
+    for i, c in enumerate(req_h.order):
+        segs += ([sep] if i else []) + [int(c)]
+    segs.append(q)
+    toks = np.concatenate([req_h.chunk_tokens[x] if isinstance(x, int) else x for x in segs]).astype(np.int32)
+    return segs, toks
+
+
+def run_case(E, wl, r, gradual, tol, check_sets=True, q8=False, segments=False):
     torch = torch_mod()
     shape = wl.shape
     model = synth.make_model(shape, seed=wl.seed)
     req_h = synth.make_requests(wl)[0]
     tokens = req_h.tokens
+    segs = None
+    if segments:
+        segs, tokens = with_text_segments(req_h, shape.vocab)
     ratios = O.ratio_schedule(r, shape.n_layers, 1, gradual)
     chunk_kv = O.precompute_chunks(model, req_h.chunk_tokens)
     blend_kv = O.quantize_chunks(chunk_kv) if q8 else chunk_kv
-    ref = O.blend(model, blend_kv, req_h.order, tokens, ratios, gradual=gradual)
+    ref = O.blend(model, blend_kv, req_h.order, tokens, ratios, gradual=gradual, segments=segs)
 
     dm = E.DeviceModel.from_host(model)
     eng = E.BlendEngine(dm, len(tokens))
@@ -75,8 +92,8 @@ def run_case(E, wl, r, gradual, tol, check_sets=True, q8=False):
             assert rel(host(pool.v[l][off:off + n]), chunk_kv[c]["V"][l].reshape(n, -1)) < tol
     if q8:
         pool = q8_pool_from_codes(E, pool, chunk_kv, dm.dims)
-    req = E.Request(eng, pool, req_h.order, tokens)
-    plan = E.layer_plan(shape, req.N, req.n_cached, ratios, gradual=gradual)
+    req = E.Request(eng, pool, req_h.order, tokens, segments=segs)
+    plan = req.plan(ratios, gradual=gradual)
     m = E.run_blend(req, plan, keep_history=True)
     from non_prefix_kv_gb300 import binding as B
     B.cb_sync(None)
@@ -135,6 +152,53 @@ def test_blend_tiny_f32_from_8bit_chunk_store(E, r):
     """The chunk store kept as 8-bit per-channel codes, decoded while re-positioning: the
     blend matches the oracle's blend over the decoded store."""
     run_case(E, synth.WORKLOADS["tiny_f32"], r, False, TOL["f32"], q8=True)
+
+
+@pytest.mark.parametrize("r,gradual", [(0.15, False), (0.3, True), (1.0, False)])
+def test_blend_with_uncached_spans_f32(E, r, gradual):
+    """System prompt, separators and query as uncached spans between the chunks (a forced-row
+    mask): sets, blended K/V and outputs against the oracle's segment blend."""
+    wl = synth.WORKLOADS["tiny_f32"]
+    wl = replace(wl, shape=replace(wl.shape, n_layers=3))
+    run_case(E, wl, r, gradual, TOL["f32"], segments=True)
+
+
+def test_blend_with_uncached_spans_bf16(E):
+    wl = synth.Workload("bf16_small", BF16_SMALL, chunk_len=96, n_distinct=4, order=(0, 1, 2, 3), n_query=32,
+                        ratio=0.15)
+    run_case(E, wl, 0.15, True, TOL["bf16"], check_sets=False, segments=True)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_prefix_caching_baseline_equals_full_prefill(E, dtype):
+    """The comparison workload that reuses only a true prefix (the first chunk) and
+    recomputes everything after it at every layer reproduces the full prefill."""
+    torch = torch_mod()
+    from non_prefix_kv_gb300 import binding as B
+    if dtype == "f32":
+        wl, tol = replace(synth.WORKLOADS["tiny_f32"], shape=replace(synth.WORKLOADS["tiny_f32"].shape, n_layers=3)), \
+            TOL["f32"]
+    else:
+        wl, tol = synth.Workload("bf16_small", BF16_SMALL, chunk_len=96, n_distinct=4, order=(0, 1, 2, 3),
+                                 n_query=32, ratio=0.15), TOL["bf16"]
+    shape = wl.shape
+    model = synth.make_model(shape, seed=wl.seed)
+    req_h = synth.make_requests(wl)[0]
+    first = req_h.order[0]
+    n0 = len(req_h.chunk_tokens[first])
+    full = O.full_prefill(model, req_h.tokens, 0)
+    dm = E.DeviceModel.from_host(model)
+    eng = E.BlendEngine(dm, len(req_h.tokens))
+    pool = eng.precompute_pool(req_h.chunk_tokens)
+    req = E.Request(eng, pool, None, req_h.tokens, segments=[int(first), req_h.tokens[n0:]])
+    m = E.run_blend(req, req.prefix_cache_plan(), keep_history=True)
+    B.cb_sync(None)
+    assert m == len(req_h.tokens) - n0
+    for l in range(shape.n_layers):
+        np.testing.assert_array_equal(req.sel_hist[l].cpu().numpy(), np.arange(n0, len(req_h.tokens)))
+        assert rel(host(req.K[l]), full["K"][l].reshape(req.N, -1)) < tol
+        assert rel(host(req.V[l]), full["V"][l].reshape(req.N, -1)) < tol
+    assert rel(host(req.x_last[m - 1]), full["x"][-1][-1]) < tol
 
 
 def test_blend_ragged_chunks_no_query_f32(E):

@@ -38,7 +38,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one k_gemm_tc launch of this
 # shape, from an ncu capture of the persistent double-buffered kernel; to be cleared when
 # that kernel changes.
-GEMM_TRAFFIC = {(4096, 11008, 4096, "swiglu"): 216.195840e6 + 76.475392e6}
+GEMM_TRAFFIC = {(4096, 11008, 4096, "swiglu"): 218.135808e6 + 77.495808e6}
 
 
 def parse_args(argv=None):
@@ -518,7 +518,8 @@ def our_arm(args):
                 "flops_per_launch": top[2], "ms_per_launch": top_ms,
                 "all_gemm_launches_tflops": all_gemm_tflops}
     hbm_kernels = {}
-    for name in ("rope_shift", "deviation", "copy_rows", "lmhead_gemv"):
+    # (bf16 takes the deviation inside the K/V GEMM; only its small tile-sum pass remains)
+    for name in ("rope_shift", "copy_rows", "lmhead_gemv") + (() if shape.dtype == "bf16" else ("deviation",)):
         if name in kinds and kinds[name]["bytes"]:
             gbs = kinds[name]["bytes"] / (kinds[name]["ms"] / 1e3) / 1e9
             hbm_kernels[name] = {"gbs": gbs, "frac": gbs / peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])}

@@ -32,10 +32,15 @@ the design notes of the repository):
       rows of S_l have their K/V overwritten.
   R7  Ties in top-k go to the lower row index; the selected rows are returned ascending.
   R8  RMSNorm eps = 1e-5, no biases, untied lm_head, argmax ties to the lowest index.
-  R9  8-bit chunk KV: per channel of one chunk's K (or V) of one layer, zero = min over
+  (R9-R11 concern the benchmark's layer stack, the weight layout and the RoPE table of the
+  CUDA path; they do not change what the oracle computes.)
+  R12 8-bit chunk KV: per channel of one chunk's K (or V) of one layer, zero = min over
       the chunk's rows, scale = (max - min) / 255 floored at 1e-8, code = round half to
       even of (x - zero) / scale; the code is decided in float32 (the pages fix no
       precision), one IEEE operation per step, so both sides decide it bit for bit.
+  R13 Uncached spans anywhere (system prompt, separators, query): every uncached row and
+      the last row are forced; the budget counts the cached rows; the pre-check layer
+      recomputes K/V of the uncached rows only.
 
 Parity status of each function is stated in its docstring ("pinned by" / "parity
 unpinned").
@@ -304,7 +309,7 @@ def assemble_segments(model: dict, chunk_kv: Sequence[dict], segments: Sequence)
     """Lay out a request made of segments: an int is a cached chunk (its KV re-rotated by
     its slot's start, as in assemble), an array of token ids is uncached text (a system
     prompt, a separator, a query) whose rows are computed, never cached ([CB-A] §vLLM
-    integration: separators between chunks; NEXT-3 reading: any number of uncached spans).
+    integration: separators between chunks; R13: any number of uncached spans).
     Returns K, V per layer with the cached rows filled, and the per-row cached mask."""
     shape = model["shape"]
     lens = [chunk_kv[g]["K"][0].shape[0] if isinstance(g, (int, np.integer)) else len(g) for g in segments]
@@ -423,7 +428,7 @@ F32 = np.float32
 def kv_quantize(x, bits: int = 8):
     """Per-channel asymmetric quantization of one chunk's K (or V) of one layer ([CG] §Step 1:
     per channel c, z_c = min over tokens, s_c = (max - min) / (2^b - 1); code =
-    round((x - z_c) / s_c)).  R9: float32, one rounding per operation, half to even, codes
+    round((x - z_c) / s_c)).  R12: float32, one rounding per operation, half to even, codes
     clipped to [0, 2^b - 1], the scale floored at 1e-8 (the page's listing clamps it so a
     constant channel does not divide by zero).
     Returns (codes uint8 [n, C], scale f32 [C], zero f32 [C]) for x [n, ...] (C = the

@@ -100,8 +100,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   int* s_qmax = reinterpret_cast<int*>(bars + 16);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = gridDim.x - 1 - blockIdx.x;      // the longest (latest) query tiles first
-  const int h = blockIdx.y;
+  // heads vary fastest in launch order and the latest (longest) query tiles come first, so
+  // every head's heavy tiles start in the first wave and the short ones fill in behind
+  const int qt = gridDim.y - 1 - blockIdx.y;
+  const int h = blockIdx.x;
   const int g = h / (H / Hkv);
   const int m0 = qt * BM;
 
@@ -417,8 +419,8 @@ __global__ void __launch_bounds__(THREADS2, 1)
   int* s_qmax = reinterpret_cast<int*>(bars + 16);   // [2]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = gridDim.x - 1 - blockIdx.x;      // the longest (latest) tile pairs first
-  const int h = blockIdx.y;
+  const int qt = gridDim.y - 1 - blockIdx.y;      // as in k_attn_tc: heads fastest, longest pairs first
+  const int h = blockIdx.x;
   const int g = h / (H / Hkv);
   const int m0 = qt * 2 * BM;
 
@@ -762,11 +764,11 @@ cudaError_t launch_hd(const void* q, const int32_t* q_pos, int M, const void* kc
   // selected set would leave SMs idle with half as many CTAs).
   const int pairs = (M + 2 * BM - 1) / (2 * BM);
   if ((int64_t)pairs * H >= sm_count_attn()) {
-    dim3 grid(pairs, H);
+    dim3 grid(H, pairs);
     { const cudaError_t e_ = launch_k(k_attn_tc2<HD>, dim3(grid), dim3(THREADS2), Layout2<HD>::SMEM, s, tq, tk, tv, q_pos, M, n_kv, H, Hkv,
                                                              static_cast<bf16*>(out), scale_log2); if (e_ != cudaSuccess) return e_; }
   } else {
-    dim3 grid((M + BM - 1) / BM, H);
+    dim3 grid(H, (M + BM - 1) / BM);
     { const cudaError_t e_ = launch_k(k_attn_tc<HD>, dim3(grid), dim3(THREADS), Layout<HD>::SMEM, s, tq, tk, tv, q_pos, M, n_kv, H, Hkv,
                                                           static_cast<bf16*>(out), scale_log2); if (e_ != cudaSuccess) return e_; }
   }

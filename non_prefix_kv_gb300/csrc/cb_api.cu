@@ -202,16 +202,14 @@ struct Carver {
 };
 
 struct LayerWs {
-  void *a, *q, *knew, *vnew, *attn, *h, *b, *act, *xg, *ag, *xa, *xb, *attn_ws;
+  void *a, *q, *knew, *vnew, *attn, *h, *b, *act, *xg, *ag, *qg, *xa, *xb, *attn_ws;
   float *scores, *hn, *logits, *dev_part;
   int32_t *ord, *keep, *pos, *rows, *cpos, *crows, *fpos, *frows;
 };
 
-// deviation partials per row of the K/V GEMM: one per half of each column tile
-int dev_parts(const cb_dims* d) {
-  const int W = d->n_kv_heads * d->head_dim;
-  return 2 * ((2 * W + kGemmTileN - 1) / kGemmTileN);
-}
+// deviation partials per row of a GEMM over ncols Wqkv columns: one per half column tile
+int dev_parts(int ncols) { return 2 * ((ncols + kGemmTileN - 1) / kGemmTileN); }
+int qkv_cols(const cb_dims* d) { return (d->n_heads + 2 * d->n_kv_heads) * d->head_dim; }
 
 // R = rows entering the layer, M = rows selected (M <= R)
 LayerWs carve_layer(Carver& c, const cb_dims* d, int64_t R, int64_t M) {
@@ -231,7 +229,8 @@ LayerWs carve_layer(Carver& c, const cb_dims* d, int64_t R, int64_t M) {
   w.xa = c.take(R * d->d_model * B);
   w.xb = c.take(R * d->d_model * B);
   w.scores = static_cast<float*>(c.take(R * 4));
-  w.dev_part = static_cast<float*>(c.take((size_t)dev_parts(d) * R * 4));
+  w.dev_part = static_cast<float*>(c.take((size_t)dev_parts(qkv_cols(d)) * R * 4));
+  w.qg = c.take(M * qc * B);
   w.ord = static_cast<int32_t*>(c.take(R * 4));
   w.keep = static_cast<int32_t*>(c.take(R * 4));
   w.pos = static_cast<int32_t*>(c.take(R * 4));
@@ -671,7 +670,13 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
       }
       L_RMSNORM(dims->dtype, dims->dtype, L.a, x_in, nullptr, w->attn_norm, m_in, dims->d_model, dims->rms_eps, s);
       WAIT_CACHED_ROWS();
-      GemmDesc gkv = qkv_desc(dims, w, L.a, m_in, qc, 2 * W, nullptr, L.knew, L.vnew, rows_in, nullptr, cos_sin, max_pos);
+      // A gradual layer whose incoming set is at most 25% larger than its selection computes
+      // Q for every incoming row in the same GEMM (one wider launch) and gathers the
+      // selected queries afterwards; otherwise Q is computed for the selected rows only.
+      const bool q_all = !check && (int64_t)m_in * 4 <= (int64_t)M * 5;
+      const int col0 = q_all ? 0 : qc, ncols = q_all ? qc + 2 * W : 2 * W;
+      GemmDesc gkv = qkv_desc(dims, w, L.a, m_in, col0, ncols, q_all ? L.q : nullptr, L.knew, L.vnew, rows_in, nullptr,
+                              cos_sin, max_pos);
       if (dims->dtype == CB_BF16) {
         // the deviation is taken in the K/V GEMM's epilogue; a small pass sums the tiles
         gkv.epi.dev_part = L.dev_part;
@@ -682,7 +687,7 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         gkv.epi.ref_rows = N;
         gkv.epi.dev_use_v = use_v ? 1 : 0;
         L_GEMM(dims->dtype, gkv, s);
-        L_DEVRED(L.dev_part, dev_parts(dims), m_in, n_cand, cpos, W, use_v, sc, s);
+        L_DEVRED(L.dev_part, dev_parts(ncols), m_in, n_cand, cpos, W, use_v, sc, s);
       } else {
         L_GEMM(dims->dtype, gkv, s);
         L_DEV(dims->dtype, L.knew, L.vnew, k_cache, v_cache, cpos, crows, n_cand, W, use_v, sc, s);
@@ -700,9 +705,15 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
       // Step 3, KV expansion: the recomputed K/V of S replace the cached rows
       L_COPY(k_cache, s_out, L.knew, L.keep, M, (int64_t)W * B, N, m_in, s);
       L_COPY(v_cache, s_out, L.vnew, L.keep, M, (int64_t)W * B, N, m_in, s);
-      L_COPY(L.ag, nullptr, L.a, L.keep, M, (int64_t)dims->d_model * B, M, m_in, s);
-      L_GEMM(dims->dtype, qkv_desc(dims, w, L.ag, M, 0, qc, L.q, nullptr, nullptr, s_out, nullptr, cos_sin, max_pos), s);
-      L_ATTN(dims->dtype, L.q, s_out, M, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
+      const void* qsel = L.q;
+      if (q_all) {
+        L_COPY(L.qg, nullptr, L.q, L.keep, M, (int64_t)qc * B, M, m_in, s);
+        qsel = L.qg;
+      } else {
+        L_COPY(L.ag, nullptr, L.a, L.keep, M, (int64_t)dims->d_model * B, M, m_in, s);
+        L_GEMM(dims->dtype, qkv_desc(dims, w, L.ag, M, 0, qc, L.q, nullptr, nullptr, s_out, nullptr, cos_sin, max_pos), s);
+      }
+      L_ATTN(dims->dtype, qsel, s_out, M, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
       L_COPY(L.xg, nullptr, x_in, L.keep, M, (int64_t)dims->d_model * B, M, m_in, s);
       return o_ffn(dims, w, L.attn, L.xg, M, x_out, L, s);
     }

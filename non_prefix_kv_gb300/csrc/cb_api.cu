@@ -122,9 +122,9 @@ double gemm_bytes(int dt, const GemmDesc& g) {
   CB_LAUNCH(CB_PROF_DEVIATION, 0, (nc), (W), (usev), 3.0 * (nc) * (W) * ((usev) ? 2 : 1),        \
             (double)(nc) * (W) * esize(dt) * ((usev) ? 4 : 2) + 4.0 * (nc), s,                   \
             launch_deviation(dt, kn, vn, kr, vr, nr, rr, nc, W, usev, sc, s))
-#define L_DEVRED(part, np, ld, nc, cpos, W, usev, sc, s)                                         \
-  CB_LAUNCH(CB_PROF_DEVIATION, 1, (nc), (W), (usev), (double)(nc) * (np), 4.0 * (nc) * ((np) + 1), s, \
-            launch_dev_reduce(part, np, ld, nc, cpos, sc, s))
+#define L_DEVRED(part, plo, np, ld, nc, cpos, W, usev, sc, s)                                    \
+  CB_LAUNCH(CB_PROF_DEVIATION, 1, (nc), (W), (usev), (double)(nc) * ((np) - (plo)),                 \
+            4.0 * (nc) * ((np) - (plo) + 1), s, launch_dev_reduce(part, plo, np, ld, nc, cpos, sc, s))
 #define L_SPLIT(rows, m, mask, mlen, nf, cp, cr, fp, fr, s)                                      \
   CB_LAUNCH(CB_PROF_INDEX, 1, (m), 0, 0, 0.0, 21.0 * (m), s,                                      \
             launch_split_rows(rows, m, mask, mlen, nf, cp, cr, fp, fr, s))
@@ -260,6 +260,52 @@ int need_ws(const cb_dims* d, int64_t R, int64_t M, void* ws, size_t ws_bytes, L
   *out = carve_layer(c, d, R, M);
   return CB_OK;
 }
+
+// Row copies batched into one launch when every row is a whole number of 16-byte words
+// at 16-byte aligned bases; otherwise one launch per copy.
+struct RowCopies {
+  CopyJobs J{};
+  struct One { void* d; const int32_t* di; const void* src; const int32_t* si; int64_t n, rb, db, sb; };
+  One list[kMaxCopyJobs];
+  int n = 0;
+  void add(void* d, const int32_t* di, const void* src, const int32_t* si, int64_t rows, int64_t rb, int64_t db,
+           int64_t sb) {
+    list[n++] = One{d, di, src, si, rows, rb, db, sb};
+  }
+  int launch(cudaStream_t s) {
+    bool vec = true;
+    int64_t acc = 0, bytes = 0, rows = 0;
+    int m = 0;
+    for (int i = 0; i < n; ++i) {
+      const One& o = list[i];
+      if (o.n == 0) continue;
+      vec = vec && o.rb % 16 == 0 && ((uintptr_t)o.d & 15) == 0 && ((uintptr_t)o.src & 15) == 0;
+      J.dst[m] = o.d;
+      J.src[m] = o.src;
+      J.di[m] = o.di;
+      J.si[m] = o.si;
+      J.rv[m] = o.rb / 16;
+      J.dbound[m] = o.db;
+      J.sbound[m] = o.sb;
+      acc += o.n * (o.rb / 16);
+      J.end[m] = acc;
+      bytes += 2 * o.n * o.rb;
+      rows += o.n;
+      ++m;
+    }
+    J.n = m;
+    if (m == 0) return CB_OK;
+    if (!vec) {
+      for (int i = 0; i < n; ++i) {
+        const One& o = list[i];
+        L_COPY(o.d, o.di, o.src, o.si, o.n, o.rb, o.db, o.sb, s);
+      }
+      return CB_OK;
+    }
+    CB_LAUNCH(CB_PROF_COPY_ROWS, m, rows, 0, 0, 0.0, (double)bytes, s, launch_copy_rows_multi(J, s));
+    return CB_OK;
+  }
+};
 
 GemmDesc make_gemm(int M, int N, int K, const void* A, int64_t lda, const void* B, int64_t ldb) {
   GemmDesc g;
@@ -687,7 +733,8 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         gkv.epi.ref_rows = N;
         gkv.epi.dev_use_v = use_v ? 1 : 0;
         L_GEMM(dims->dtype, gkv, s);
-        L_DEVRED(L.dev_part, dev_parts(ncols), m_in, n_cand, cpos, W, use_v, sc, s);
+        // partials of tiles that hold only Q columns are zero: start at the first K tile
+        L_DEVRED(L.dev_part, q_all ? 2 * (qc / kGemmTileN) : 0, dev_parts(ncols), m_in, n_cand, cpos, W, use_v, sc, s);
       } else {
         L_GEMM(dims->dtype, gkv, s);
         L_DEV(dims->dtype, L.knew, L.vnew, k_cache, v_cache, cpos, crows, n_cand, W, use_v, sc, s);
@@ -702,19 +749,23 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         L_MERGE(L.ord, k_budget, L.crows, L.cpos, L.frows, L.fpos, n_forced, s_out, L.keep, s);
       else
         L_BUILD_SEL(L.ord, k_budget, rows_in, f0, m_in - n_forced, n_forced, s_out, L.keep, s);
-      // Step 3, KV expansion: the recomputed K/V of S replace the cached rows
-      L_COPY(k_cache, s_out, L.knew, L.keep, M, (int64_t)W * B, N, m_in, s);
-      L_COPY(v_cache, s_out, L.vnew, L.keep, M, (int64_t)W * B, N, m_in, s);
-      const void* qsel = L.q;
-      if (q_all) {
-        L_COPY(L.qg, nullptr, L.q, L.keep, M, (int64_t)qc * B, M, m_in, s);
-        qsel = L.qg;
-      } else {
-        L_COPY(L.ag, nullptr, L.a, L.keep, M, (int64_t)dims->d_model * B, M, m_in, s);
-        L_GEMM(dims->dtype, qkv_desc(dims, w, L.ag, M, 0, qc, L.q, nullptr, nullptr, s_out, nullptr, cos_sin, max_pos), s);
+      // Step 3, KV expansion (the recomputed K/V of S replace the cached rows), and the
+      // gathers of S's queries (or normalised rows) and residual rows: one launch
+      {
+        RowCopies rc;
+        rc.add(k_cache, s_out, L.knew, L.keep, M, (int64_t)W * B, N, m_in);
+        rc.add(v_cache, s_out, L.vnew, L.keep, M, (int64_t)W * B, N, m_in);
+        if (q_all)
+          rc.add(L.qg, nullptr, L.q, L.keep, M, (int64_t)qc * B, M, m_in);
+        else
+          rc.add(L.ag, nullptr, L.a, L.keep, M, (int64_t)dims->d_model * B, M, m_in);
+        rc.add(L.xg, nullptr, x_in, L.keep, M, (int64_t)dims->d_model * B, M, m_in);
+        if ((st = rc.launch(s))) return st;
       }
+      const void* qsel = q_all ? L.qg : L.q;
+      if (!q_all)
+        L_GEMM(dims->dtype, qkv_desc(dims, w, L.ag, M, 0, qc, L.q, nullptr, nullptr, s_out, nullptr, cos_sin, max_pos), s);
       L_ATTN(dims->dtype, qsel, s_out, M, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
-      L_COPY(L.xg, nullptr, x_in, L.keep, M, (int64_t)dims->d_model * B, M, m_in, s);
       return o_ffn(dims, w, L.attn, L.xg, M, x_out, L, s);
     }
     case CB_LAYER_STEADY: {

@@ -85,8 +85,21 @@ cudaError_t launch_copy_rows(void* dst, const int32_t* dst_idx, const void* src,
 cudaError_t launch_rmsnorm(int dt_in, int dt_out, void* out, const void* x,
                            const int32_t* rows, const void* g, int64_t n, int d, float eps,
                            cudaStream_t s);
-cudaError_t launch_dev_reduce(const float* part, int n_parts, int64_t ld, int n_cand, const int32_t* cand_pos,
-                              float* scores, cudaStream_t s);
+cudaError_t launch_dev_reduce(const float* part, int part_lo, int n_parts, int64_t ld, int n_cand,
+                              const int32_t* cand_pos, float* scores, cudaStream_t s);
+constexpr int kMaxCopyJobs = 4;
+struct CopyJobs {          // row copies of 16-byte words: dst[di[r]] = src[si[r]] (null index: r)
+  void* dst[kMaxCopyJobs];
+  const void* src[kMaxCopyJobs];
+  const int32_t* di[kMaxCopyJobs];
+  const int32_t* si[kMaxCopyJobs];
+  int64_t rv[kMaxCopyJobs];       // 16-byte words per row
+  int64_t dbound[kMaxCopyJobs];   // row bounds for the index checks (< 0: unchecked)
+  int64_t sbound[kMaxCopyJobs];
+  int64_t end[kMaxCopyJobs];      // inclusive prefix sums of rows * rv
+  int n;
+};
+cudaError_t launch_copy_rows_multi(const CopyJobs& J, cudaStream_t s);
 cudaError_t launch_split_rows(const int32_t* rows_in, int m, const uint8_t* mask, int64_t mask_len,
                               int n_forced, int32_t* cand_pos, int32_t* cand_rows, int32_t* forced_pos,
                               int32_t* forced_rows, cudaStream_t s);

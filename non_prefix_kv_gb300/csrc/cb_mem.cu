@@ -310,6 +310,38 @@ cudaError_t launch_copy_rows(void* dst, const int32_t* dst_idx, const void* src,
   return cudaGetLastError();
 }
 
+// Up to kMaxCopyJobs independent row copies in one launch (the KV expansion and the row
+// gathers that follow a selection share their indices and their moment): job j owns the
+// linear work range [end[j-1], end[j]) of 16-byte words.
+__global__ void __launch_bounds__(256) k_copy_rows_multi(const CopyJobs J) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t total = J.end[J.n - 1];
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    int j = 0;
+    while (t >= J.end[j]) ++j;
+    const int64_t u = t - (j ? J.end[j - 1] : 0);
+    const int64_t rv = J.rv[j];
+    const int64_t r = u / rv, c = u - r * rv;
+    const int64_t d = J.di[j] ? (int64_t)J.di[j][r] : r;
+    const int64_t sr = J.si[j] ? (int64_t)J.si[j][r] : r;
+    if (d < 0 || sr < 0 || (J.dbound[j] >= 0 && d >= J.dbound[j]) || (J.sbound[j] >= 0 && sr >= J.sbound[j])) {
+      atomicOr(&g_err_mem, ERRBIT_INDEX);
+      continue;
+    }
+    static_cast<uint4*>(J.dst[j])[d * rv + c] = static_cast<const uint4*>(J.src[j])[sr * rv + c];
+  }
+}
+
+cudaError_t launch_copy_rows_multi(const CopyJobs& J, cudaStream_t s) {
+  if (J.n < 1 || J.n > kMaxCopyJobs) return cudaErrorInvalidValue;
+  const int64_t total = J.end[J.n - 1];
+  if (total == 0) return cudaSuccess;
+  { const cudaError_t e_ = launch_k(k_copy_rows_multi, dim3(grid_for(total, 256)), dim3(256), 0, s, J); if (e_ != cudaSuccess) return e_; }
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------------ RMSNorm
 // out[r] = x[rows[r]] / sqrt(mean(x^2) + eps) * g.  One block per row.
 template <typename Ti, typename To>
@@ -419,23 +451,24 @@ __global__ void __launch_bounds__(256) k_deviation(const T* __restrict__ kn, con
 
 // scores[c] = sum over column tiles t (in order) of part[t][c], the per-tile partials the
 // Q/K/V GEMM epilogue leaves when it computes the deviation in place.
-__global__ void k_dev_reduce(const float* __restrict__ part, int n_parts, int64_t ld, int n_cand,
+__global__ void k_dev_reduce(const float* __restrict__ part, int part_lo, int n_parts, int64_t ld, int n_cand,
                              const int32_t* __restrict__ cand_pos, float* __restrict__ scores) {
   pdl_wait();
   pdl_trigger();
   for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < n_cand; c += gridDim.x * blockDim.x) {
     const int64_t row = cand_pos ? (int64_t)cand_pos[c] : c;
     float acc = 0.f;
-    for (int t = 0; t < n_parts; ++t) acc += part[t * ld + row];
+#pragma unroll 8
+    for (int t = part_lo; t < n_parts; ++t) acc += part[t * ld + row];
     scores[c] = acc;
     if (!isfinite(acc)) atomicOr(&g_err_mem, ERRBIT_NONFINITE);
   }
 }
 
-cudaError_t launch_dev_reduce(const float* part, int n_parts, int64_t ld, int n_cand, const int32_t* cand_pos,
-                              float* scores, cudaStream_t s) {
+cudaError_t launch_dev_reduce(const float* part, int part_lo, int n_parts, int64_t ld, int n_cand,
+                              const int32_t* cand_pos, float* scores, cudaStream_t s) {
   if (n_cand == 0) return cudaSuccess;
-  { const cudaError_t e_ = launch_k(k_dev_reduce, dim3(grid_for(n_cand, 256)), dim3(256), 0, s, part, n_parts, ld, n_cand, cand_pos, scores); if (e_ != cudaSuccess) return e_; }
+  { const cudaError_t e_ = launch_k(k_dev_reduce, dim3(grid_for(n_cand, 256)), dim3(256), 0, s, part, part_lo, n_parts, ld, n_cand, cand_pos, scores); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 

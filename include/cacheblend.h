@@ -103,6 +103,14 @@ const char* cb_last_error_message(void);
  * The pages' synchronize() ([CB-A] §vLLM integration). */
 int cb_sync(void* stream, double timeout_s);
 
+/* Failure-path self test of the device-side bounded waits (every mbarrier wait of the
+ * tensor-core kernels is bounded): one tiny kernel waits on an mbarrier that is completed
+ * (arrive != 0) or that nothing completes.  In the second case the wait gives up after
+ * max_polls (1..2^20) tries, records the timeout in the device error word and returns;
+ * the next cb_sync reports CB_ERR_DEVICE ("bounded wait expired") and the context stays
+ * usable.  No trap, no hang. */
+int cb_selftest_wait(int32_t max_polls, int32_t arrive, void* stream);
+
 /* Device workspace (bytes) large enough for every call below on rows up to n_tok and a
  * selected set of up to m_max rows, for these dims.  Host-only. */
 int cb_workspace_bytes(const cb_dims* dims, int64_t n_tok, int64_t m_max, size_t* out_host);

@@ -420,6 +420,13 @@ int cb_sync(void* stream, double timeout_s) {
   return CB_OK;
 }
 
+int cb_selftest_wait(int32_t max_polls, int32_t arrive, void* stream) {
+  if (max_polls < 1 || max_polls > (1 << 20)) return fail(CB_ERR_INVALID_ARG, "max_polls outside [1, 2^20]");
+  CB_CUDA(launch_wait_selftest((uint32_t)max_polls, arrive ? 1 : 0, S(stream)));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return CB_OK;
+}
+
 int cb_workspace_bytes(const cb_dims* dims, int64_t n_tok, int64_t m_max, size_t* out_host) {
   int st = check_dims(dims);
   if (st) return st;

@@ -254,6 +254,22 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// Failure-path self test of the bounded waits every tcgen05 kernel uses: an mbarrier that
+// completes (arrive != 0) or that nothing completes; the wait gives up after max_polls
+// tries, records ERRBIT_TIMEOUT and the kernel returns, leaving the context usable.
+__global__ void k_wait_selftest(uint32_t max_polls, int arrive) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (arrive) tc::mbar_arrive(&bar);
+    if (!tc::mbar_wait_n(&bar, 0, max_polls)) atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
+  }
+}
+
 // ---- host: tensor maps through the driver entry point (no libcuda link dependency)
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -289,6 +305,11 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int
 }
 
 }  // namespace
+
+cudaError_t launch_wait_selftest(uint32_t max_polls, int arrive, cudaStream_t s) {
+  k_wait_selftest<<<1, 32, 0, s>>>(max_polls, arrive);
+  return cudaGetLastError();
+}
 
 // Host preconditions (checked by the caller's validation, re-checked here): K % 8 == 0,
 // lda/ldb % 8 == 0, A and B 16-byte aligned, N % 16 == 0.

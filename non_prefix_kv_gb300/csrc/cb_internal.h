@@ -100,6 +100,7 @@ struct CopyJobs {          // row copies of 16-byte words: dst[di[r]] = src[si[r
   int n;
 };
 cudaError_t launch_copy_rows_multi(const CopyJobs& J, cudaStream_t s);
+cudaError_t launch_wait_selftest(uint32_t max_polls, int arrive, cudaStream_t s);
 cudaError_t launch_split_rows(const int32_t* rows_in, int m, const uint8_t* mask, int64_t mask_len,
                               int n_forced, int32_t* cand_pos, int32_t* cand_rows, int32_t* forced_pos,
                               int32_t* forced_rows, cudaStream_t s);

@@ -142,6 +142,10 @@ class BlendEngine:
         self.ws = torch.empty(B.cb_workspace_bytes(dm.dims, n_tok_max, n_tok_max), dtype=torch.uint8,
                               device=device)
         self.n_tok_max = n_tok_max
+        # inputs shorter than this are prefilled in full: the blend's fixed overhead (pre-check
+        # and check layers) outweighs its savings there ([CB-A] §configuration parameters,
+        # minimum token count for blending, 256)
+        self.min_tokens = 256
 
     # ---- precompute (offline: KV^pre) ------------------------------------------------------
     def precompute_pool(self, chunk_tokens: Sequence[np.ndarray]) -> ChunkPool:
@@ -350,6 +354,18 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
     s = dm.shape
     dims = dm.dims
     esz = 2 if s.dtype == "bf16" else 4
+    if req.N < eng.min_tokens:
+        # too short to blend: a full prefill of the request (every row, every layer)
+        if host_pool is not None or file_store is not None:
+            raise ValueError("requests shorter than min_tokens are prefilled in full and load no chunk KV")
+        B.cb_full_prefill(dims, dm.layers_c, dm.embed, req.tokens, req.N, 0, req.K, req.V, None, req.x[0],
+                          eng.cos_sin, eng.max_pos, eng.ws, stream)
+        if keep_history:
+            rows = torch.arange(req.N, dtype=torch.int32, device=req.tokens.device)
+            req.sel_hist, req.m_hist = [rows] * s.n_layers, [req.N] * s.n_layers
+        req.m_last, req.x_last = req.N, req.x[0]
+        B.cb_lmhead_argmax(req.x[0][req.N - 1], dm.final_norm, dm.w_lm, dims, None, req.token, eng.ws, stream)
+        return req.N
     def assemble_layer(l, st):
         # one re-positioning pass per run of adjacent chunk slots
         for r0, c0, n in req.runs:

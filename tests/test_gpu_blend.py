@@ -268,3 +268,31 @@ def test_layer_ahead_loading_matches_resident_pool(E, q8, from_file, tmp_path):
     for l in range(wl.shape.n_layers):
         assert torch.equal(ka[l], b.K[l])
     assert torch.equal(xa, b.x_last[:b.m_last]) and ta == int(b.token.item())
+
+
+def test_short_request_is_prefilled_in_full(E):
+    """Below the blending threshold (256 tokens) the engine runs a full prefill of the
+    request: every layer's K/V and the output equal the oracle's full prefill."""
+    torch = torch_mod()
+    from non_prefix_kv_gb300 import binding as B
+    wl = replace(synth.WORKLOADS["tiny_f32"], chunk_len=64, n_query=24)
+    shape = wl.shape
+    model = synth.make_model(shape, seed=wl.seed)
+    req_h = synth.make_requests(wl)[0]
+    assert len(req_h.tokens) < 256
+    full = O.full_prefill(model, req_h.tokens, 0)
+    dm = E.DeviceModel.from_host(model)
+    eng = E.BlendEngine(dm, len(req_h.tokens))
+    pool = eng.precompute_pool(req_h.chunk_tokens)
+    req = E.Request(eng, pool, req_h.order, req_h.tokens)
+    ratios = O.ratio_schedule(0.15, shape.n_layers, 1, False)
+    m = E.run_blend(req, req.plan(ratios))
+    B.cb_sync(None)
+    assert m == req.N
+    for l in range(shape.n_layers):
+        assert rel(host(req.K[l]), full["K"][l].reshape(req.N, -1)) < TOL["f32"]
+    assert rel(host(req.x_last[m - 1]), full["x"][-1][-1]) < TOL["f32"]
+    tok, logits = O.lm_head_argmax(model, full["x"][-1][-1])
+    top2 = np.sort(logits)[-2:]
+    if top2[1] - top2[0] > 1e-2 * abs(top2[1]):
+        assert int(req.token.item()) == tok

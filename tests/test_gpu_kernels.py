@@ -518,3 +518,40 @@ def test_full_prefill_f32_matches_oracle(B):
         assert rel(host(v_out[l]), ref["V"][l].reshape(200, -1)) < 1e-5
     assert rel(host(x_all), ref["x"][-1]) < 1e-5
     assert rel(host(h), ref["h_last"]) < 1e-5
+
+
+# ------------------------------------------------------------------------------ failure paths
+def test_bounded_device_wait_expires_and_context_survives(B):
+    """A wait that nothing completes gives up after its bound, the error word reports it once,
+    and the same context keeps working (no trap, no hang)."""
+    torch = torch_mod()
+    B.cb_sync(None)
+    B.cb_selftest_wait(1000, arrive=False)
+    with pytest.raises(B.CBError) as e:
+        B.cb_sync(None)
+    assert e.value.status == 9 and "bounded wait" in str(e.value)
+    B.cb_selftest_wait(1000, arrive=True)
+    B.cb_sync(None)                       # completed wait: no error, the word was cleared
+    x = torch.ones(64, 64, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(64, 64, dtype=torch.bfloat16, device="cuda")
+    B.cb_linear(x, x, y, 64, 64, 64, B.CB_BF16)
+    B.cb_sync(None)
+    assert torch.all(y.float() == 64.0)
+
+
+def test_host_sync_limit_returns_timeout_then_completes(B):
+    """cb_sync with a limit shorter than the queued work returns CB_ERR_TIMEOUT without
+    cancelling anything; waiting again completes normally."""
+    torch = torch_mod()
+    n = 8192
+    x = torch.full((n, n), 0.01, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty_like(x)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(8):
+            B.cb_linear(x, x, y, n, n, n, B.CB_BF16, stream=s)
+    with pytest.raises(B.CBError) as e:
+        B.cb_sync(s, timeout_s=1e-5)
+    assert e.value.status == 7
+    B.cb_sync(s, timeout_s=0.0)
+    assert abs(float(y[0, 0]) - n * 1e-4) < 0.05 * n * 1e-4

@@ -605,6 +605,16 @@ def our_arm(args):
                 out_tok.copy_(r0.token, non_blocking=True)
             stream.synchronize()
 
+        # the recommended call for repeated request shapes: the whole request (uploads, loads,
+        # layers, read-back) captured once and replayed
+        rg = E.RequestGraph(r0, plan, host_pool=hp, stream=stream)
+        gtimes = []
+        for i in range(args.warmup + args.steps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            tok_g = rg.run(r0.tokens_host)
+            if i >= args.warmup:
+                gtimes.append(time.perf_counter() - t0)
         res = {}
         for overlap in (True, False):
             times = []
@@ -615,9 +625,13 @@ def our_arm(args):
                 if i >= args.warmup:
                     times.append(time.perf_counter() - t0)
             res[overlap] = statistics.median(times)
-        e2e = {"value": wl.n_tokens / res[True], "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": 4, "ttft_ms": res[True] * 1e3, "first_token": int(out_tok.item()),
-               "layer_ahead_loading": True, "ttft_ms_without_overlap": res[False] * 1e3,
+        t_graph = statistics.median(gtimes)
+        e2e = {"value": wl.n_tokens / t_graph, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": 4, "ttft_ms": t_graph * 1e3, "first_token": tok_g,
+               "api": "engine.RequestGraph (captured request: token upload, layer-ahead chunk-KV loading, "
+                      "layers, read-back)",
+               "layer_ahead_loading": True, "ttft_ms_eager": res[True] * 1e3,
+               "first_token_eager": int(out_tok.item()), "ttft_ms_without_overlap": res[False] * 1e3,
                "h2d_gbs_serial": h2d / max(res[False] - ms / 1e3 / len(reqs), 1e-6) / 1e9}
         if shape.dtype == "bf16":
             e2e["int8_store"] = int8_store_e2e(E, B, eng, dm, pool, r0, plan, stream, host_tok, args)

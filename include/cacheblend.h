@@ -341,6 +341,11 @@ int cb_lmhead_argmax(const void* h, const void* final_norm, const void* w_lm,
 int cb_prefetch_layer(void* dev_dst, const void* pinned_src, size_t bytes, void* side_stream,
                       void* done_event);
 
+/* Stream-ordered copy between any two CUDA-visible buffers (direction from the pointers,
+ * e.g. token ids from pinned host memory, the first-token id back to it); capturable in a
+ * CUDA graph like every call of this library. */
+int cb_copy_async(void* dst, const void* src, size_t bytes, void* stream);
+
 /* Makes `stream` wait (on the device, without blocking the host) for `event`, typically the
  * done_event of cb_prefetch_layer, before its next launch. */
 int cb_stream_wait(void* stream, void* event);

@@ -881,6 +881,13 @@ int cb_prefetch_layer(void* dev_dst, const void* pinned_src, size_t bytes, void*
   return CB_OK;
 }
 
+int cb_copy_async(void* dst, const void* src, size_t bytes, void* stream) {
+  if (bytes == 0) return CB_OK;
+  if (!dst || !src) return fail(CB_ERR_INVALID_ARG, "copy pointer is NULL");
+  CB_CUDA(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, S(stream)));
+  return CB_OK;
+}
+
 int cb_stream_wait(void* stream, void* event) {
   if (!event) return fail(CB_ERR_INVALID_ARG, "event is NULL");
   CB_CUDA(cudaStreamWaitEvent(S(stream), static_cast<cudaEvent_t>(event), 0));

@@ -296,3 +296,35 @@ def test_short_request_is_prefilled_in_full(E):
     top2 = np.sort(logits)[-2:]
     if top2[1] - top2[0] > 1e-2 * abs(top2[1]):
         assert int(req.token.item()) == tok
+
+
+def test_request_graph_replays_match_eager_runs(E):
+    """A request captured once (token upload, layer-ahead loading from pinned host memory,
+    layers, read-back) and replayed gives bit-identical results to eager runs, also after
+    the host swaps in another query."""
+    torch = torch_mod()
+    from non_prefix_kv_gb300 import binding as B
+    wl = synth.Workload("bf16_small", BF16_SMALL, chunk_len=96, n_distinct=4, order=(0, 1, 2, 3), n_query=32,
+                        ratio=0.15)
+    model = synth.make_model(wl.shape, seed=1)
+    req_h = synth.make_requests(wl)[0]
+    dm = E.DeviceModel.from_host(model)
+    eng = E.BlendEngine(dm, wl.n_tokens)
+    pool = eng.precompute_pool(req_h.chunk_tokens)
+    plan = E.layer_plan(wl.shape, wl.n_tokens, wl.n_cached, [None, 0.15, 0.15])
+    toks2 = req_h.tokens.copy()
+    toks2[-wl.n_query:] = synth.rng(99, synth.P_TOKENS).integers(0, wl.shape.vocab, wl.n_query)
+    eager = []
+    for t in (req_h.tokens, toks2):
+        a = E.Request(eng, pool, req_h.order, t)
+        E.run_blend(a, plan)
+        B.cb_sync(None)
+        eager.append(([k.clone() for k in a.K], a.x_last[:a.m_last].clone(), int(a.token.item())))
+    hp = E.HostPool(pool)
+    b = E.Request(eng, pool, req_h.order, req_h.tokens)
+    rg = E.RequestGraph(b, plan, host_pool=hp)
+    for t, (ks, xs, tok) in zip((req_h.tokens, toks2), eager):
+        assert rg.run(t) == tok
+        for l in range(wl.shape.n_layers):
+            assert torch.equal(ks[l], b.K[l])
+        assert torch.equal(xs, b.x_last[:b.m_last])

@@ -607,7 +607,11 @@ def our_arm(args):
 
         # the recommended call for repeated request shapes: the whole request (uploads, loads,
         # layers, read-back) captured once and replayed
-        rg = E.RequestGraph(r0, plan, host_pool=hp, stream=stream)
+        # the pre-check layer's chunk KV is not loaded: its K/V are recomputed from the
+        # embeddings (equal there up to rounding), which costs less than their transfer
+        rg = E.RequestGraph(r0, plan, host_pool=hp, stream=stream, recompute_precheck_kv=True)
+        pre_layers = [l for l, (mode, _) in enumerate(plan) if mode == B.CB_LAYER_PRECHECK]
+        h2d_graph = h2d - sum(t.numel() * t.element_size() for l in pre_layers for t in hp.host[l])
         gtimes = []
         for i in range(args.warmup + args.steps):
             torch.cuda.synchronize()
@@ -626,10 +630,11 @@ def our_arm(args):
                     times.append(time.perf_counter() - t0)
             res[overlap] = statistics.median(times)
         t_graph = statistics.median(gtimes)
-        e2e = {"value": wl.n_tokens / t_graph, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+        e2e = {"value": wl.n_tokens / t_graph, "unit": "tokens/s", "h2d_bytes_per_step": int(h2d_graph),
                "d2h_bytes_per_step": 4, "ttft_ms": t_graph * 1e3, "first_token": tok_g,
                "api": "engine.RequestGraph (captured request: token upload, layer-ahead chunk-KV loading, "
-                      "layers, read-back)",
+                      "layers, read-back; pre-check layer K/V recomputed instead of loaded)",
+               "h2d_bytes_per_step_eager": int(h2d),
                "layer_ahead_loading": True, "ttft_ms_eager": res[True] * 1e3,
                "first_token_eager": int(out_tok.item()), "ttft_ms_without_overlap": res[False] * 1e3,
                "h2d_gbs_serial": h2d / max(res[False] - ms / 1e3 / len(reqs), 1e-6) / 1e9}

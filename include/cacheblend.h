@@ -301,6 +301,11 @@ typedef struct {
    * first access to the cached rows: in PRECHECK after the Q and uncached-row K/V GEMMs,
    * which touch only forced rows, so those overlap the load ([CB-A] §Pipelining). */
   void* kv_ready;
+  /* PRECHECK only: nonzero = compute K/V for every row (one Q/K/V GEMM over all rows)
+   * instead of reusing the re-positioned cache for the cached rows.  At the pre-check
+   * layer the two agree up to rounding (its input is the context-free embedding, R5), so a
+   * caller that loads chunk KV over a slow link can skip that layer's load entirely. */
+  int32_t recompute_kv;
 } cb_layer_opts;
 
 int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode,

@@ -679,6 +679,13 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
       *m_out_host = N;
       L_IOTA(s_out, N, 0, s);
       L_RMSNORM(dims->dtype, dims->dtype, L.a, x_in, nullptr, w->attn_norm, N, dims->d_model, dims->rms_eps, s);
+      if (opts && opts->recompute_kv) {
+        // every row's Q, K and V in one GEMM; the cached rows are overwritten, not read
+        WAIT_CACHED_ROWS();
+        L_GEMM(dims->dtype, qkv_desc(dims, w, L.a, N, 0, qc + 2 * W, L.q, k_cache, v_cache, s_out, s_out, cos_sin, max_pos), s);
+        L_ATTN(dims->dtype, L.q, s_out, N, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
+        return o_ffn(dims, w, L.attn, x_in, N, x_out, L, s);
+      }
       L_GEMM(dims->dtype, qkv_desc(dims, w, L.a, N, 0, qc, L.q, nullptr, nullptr, s_out, nullptr, cos_sin, max_pos), s);
       if (fmask) {
         // K/V of the forced rows, wherever they are: gather their normalised rows first

@@ -296,12 +296,14 @@ class HostPool:
             ev.record(self.side)
         self.nbytes = sum(t.numel() * t.element_size() for ts in self.host for t in ts)
 
-    def prefetch_all(self, stream, after_copy=None):
-        """Queue every layer's copy on the side stream once `stream`'s prior work is done;
-        after_copy(l, side_stream) enqueues more work on the landed layer (the
-        re-positioning) before the layer's event is recorded."""
+    def prefetch_all(self, stream, after_copy=None, skip=()):
+        """Queue every layer's copy (but those in skip) on the side stream once `stream`'s
+        prior work is done; after_copy(l, side_stream) enqueues more work on the landed
+        layer (the re-positioning) before the layer's event is recorded."""
         self.side.wait_stream(stream)
         for l, (hs, ds) in enumerate(zip(self.host, self.dev)):
+            if l in skip:
+                continue
             for h, d in zip(hs, ds):
                 B.cb_prefetch_layer(d, h, h.numel() * h.element_size(), self.side, self.done[l])
             if after_copy is not None:
@@ -342,8 +344,10 @@ class RequestGraph:
     refreshes the token ids (run(tokens)); another chunk layout of the same sizes refreshes
     the request's row maps (src_row, delta) in place first."""
 
-    def __init__(self, req: Request, plan, host_pool: Optional[HostPool] = None, stream=None):
+    def __init__(self, req: Request, plan, host_pool: Optional[HostPool] = None, stream=None,
+                 recompute_precheck_kv: bool = False):
         self.req, self.plan, self.host_pool = req, plan, host_pool
+        self.recompute = recompute_precheck_kv
         self.stream = stream if stream is not None else torch.cuda.Stream()
         self.host_tokens = torch.from_numpy(req.tokens_host.copy()).pin_memory()
         self.out = torch.empty(1, dtype=torch.int32).pin_memory()
@@ -358,7 +362,8 @@ class RequestGraph:
     def _enqueue(self):
         with torch.cuda.stream(self.stream):
             B.cb_copy_async(self.req.tokens, self.host_tokens, self.req.N * 4, self.stream)
-            run_blend(self.req, self.plan, host_pool=self.host_pool, stream=self.stream)
+            run_blend(self.req, self.plan, host_pool=self.host_pool, stream=self.stream,
+                      recompute_precheck_kv=self.recompute)
             B.cb_copy_async(self.out, self.req.token, 4, self.stream)
 
     def run(self, tokens=None) -> int:
@@ -372,7 +377,7 @@ class RequestGraph:
 
 def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None, keep_history=False,
               assemble: bool = True, stream=None, host_pool: Optional[HostPool] = None,
-              file_store: Optional[FileStore] = None):
+              file_store: Optional[FileStore] = None, recompute_precheck_kv: bool = False):
     """One blended prefill: re-position the chunk KV of every layer, run the layer plan,
     then the lm_head argmax.  Returns the number of rows carried out of the last layer.
 
@@ -384,7 +389,11 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
     With file_store (whose host pool is used), a loader thread reads each layer from the
     file into pinned memory and then queues that layer's copy and re-positioning; the layer
     loop waits on the host for the layer's read before queueing the layer (the pages'
-    generator pipeline: fetch layer l+1 while layer l computes)."""
+    generator pipeline: fetch layer l+1 while layer l computes).
+
+    recompute_precheck_kv: the pre-check layers compute K/V for every row instead of using
+    the chunk caches, which agree with it up to rounding there (R5); their chunk KV is then
+    neither loaded nor re-positioned (a third of the host bytes of a three-layer stack)."""
     eng = req.eng
     dm = eng.dm
     s = dm.shape
@@ -416,6 +425,7 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
                 B.cb_rope_shift(kd, vd, req.pool.k[l], req.pool.v[l], src, dl, n, dims, eng.cos_sin, eng.max_pos,
                                 st)
 
+    skip = {l for l, (mode, _) in enumerate(plan) if mode == B.CB_LAYER_PRECHECK} if recompute_precheck_kv else set()
     ready, errors, loader = None, [], None
     if file_store is not None:
         host_pool = file_store.hp
@@ -430,6 +440,9 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
         def load():
             try:
                 for l in range(s.n_layers):
+                    if l in skip:
+                        ready[l].set()
+                        continue
                     file_store.read_layer(l)
                     for h, d in zip(hp.host[l], hp.dev[l]):
                         B.cb_prefetch_layer(d, h, h.numel() * h.element_size(), hp.side, hp.done[l])
@@ -446,7 +459,7 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
         loader.start()
     elif host_pool is not None:
         host_pool.prefetch_all(torch.cuda.current_stream() if stream is None else stream,
-                               assemble_layer if assemble else None)
+                               assemble_layer if assemble else None, skip)
 
     if req.start_rows is None:
         B.cb_gather_rows(req.x[0], dm.embed, req.tokens, req.N, s.d_model * esz, stream)
@@ -458,7 +471,8 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
         s_in = req.start_rows
     if assemble and host_pool is None:
         for l in range(s.n_layers):
-            assemble_layer(l, stream)
+            if l not in skip:
+                assemble_layer(l, stream)
     cur = 0
     if keep_history:
         req.sel_hist, req.m_hist = [], []
@@ -473,8 +487,9 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
                                  req.K[l], req.V[l], eng.cos_sin, eng.max_pos, k, dev_mode, ov,
                                  req.x[1 - cur], req.s[1 - cur],
                                  req.scores if mode in (B.CB_LAYER_CHECK, B.CB_LAYER_GRADUAL) else None,
-                                 eng.ws, stream, kv_ready=None if host_pool is None else host_pool.done[l],
-                                 forced_mask=req.forced_mask, n_forced=req.n_forced)
+                                 eng.ws, stream,
+                                 kv_ready=None if (host_pool is None or l in skip) else host_pool.done[l],
+                                 forced_mask=req.forced_mask, n_forced=req.n_forced, recompute_kv=l in skip)
         cur = 1 - cur
         s_in = req.s[cur]
         m_in = m_out

@@ -497,7 +497,7 @@ def our_arm(args):
         e = gemms.setdefault(key, [0, 0.0, r["flops"]])
         e[0] += 1
         e[1] += r["ms"]
-    epi_names = {0: "store", 1: "resid", 2: "qkv", 3: "swiglu"}
+    epi_names = {0: "store", 1: "resid", 2: "qkv", 3: "swiglu", 102: "qkv+qkv (two problems, one launch)"}
     gemm_detail = [{"m": k[0], "n": k[1], "k": k[2], "epi": epi_names.get(k[3], k[3]),
                     "us": 1e3 * v[1] / v[0], "tflops": v[2] / (v[1] / v[0] / 1e3) / 1e12}
                    for k, v in sorted(gemms.items(), key=lambda kv: -kv[1][1])]

@@ -107,6 +107,13 @@ double gemm_bytes(int dt, const GemmDesc& g) {
     CB_LAUNCH(CB_PROF_GEMM, g__.epi.kind, g__.M, g__.N, g__.K, gemm_flops(g__), gemm_bytes(dt, g__), s, \
               launch_gemm(dt, g__, s));                                                       \
   } while (0)
+#define L_GEMM2(dt, ga, gb, s)                                                                   \
+  do {                                                                                        \
+    const GemmDesc a__ = (ga), b__ = (gb);                                                    \
+    CB_LAUNCH(CB_PROF_GEMM, 100 + a__.epi.kind, a__.M + b__.M, a__.N, a__.K,                  \
+              gemm_flops(a__) + gemm_flops(b__), gemm_bytes(dt, a__) + gemm_bytes(dt, b__), s,  \
+              launch_gemm_pair(dt, a__, b__, s));                                             \
+  } while (0)
 #define L_IOTA(out, n, start, s) \
   CB_LAUNCH(CB_PROF_INDEX, 0, (n), 0, 0, 0.0, 4.0 * (n), s, launch_iota(out, n, start, s))
 #define L_RMSNORM(dti, dto, out, x, rows, g, n, d, eps, s)                                       \
@@ -686,16 +693,19 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         L_ATTN(dims->dtype, L.q, s_out, N, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
         return o_ffn(dims, w, L.attn, x_in, N, x_out, L, s);
       }
-      L_GEMM(dims->dtype, qkv_desc(dims, w, L.a, N, 0, qc, L.q, nullptr, nullptr, s_out, nullptr, cos_sin, max_pos), s);
+      // Q of every row and K/V of the uncached rows: independent, so one shared launch
+      const GemmDesc gq = qkv_desc(dims, w, L.a, N, 0, qc, L.q, nullptr, nullptr, s_out, nullptr, cos_sin, max_pos);
       if (fmask) {
         // K/V of the forced rows, wherever they are: gather their normalised rows first
         L_SPLIT(nullptr, N, fmask, N, n_forced, L.cpos, L.crows, L.fpos, L.frows, s);
         L_COPY(L.ag, nullptr, L.a, L.frows, n_forced, (int64_t)dims->d_model * B, n_forced, N, s);
-        L_GEMM(dims->dtype, qkv_desc(dims, w, L.ag, n_forced, qc, 2 * W, nullptr, k_cache, v_cache, L.frows, L.frows, cos_sin, max_pos), s);
+        L_GEMM2(dims->dtype, gq, qkv_desc(dims, w, L.ag, n_forced, qc, 2 * W, nullptr, k_cache, v_cache, L.frows, L.frows, cos_sin, max_pos), s);
       } else if (N > n_cached) {
         const int nu = N - (int)n_cached;
         const void* a_u = static_cast<const char*>(L.a) + (size_t)n_cached * dims->d_model * B;
-        L_GEMM(dims->dtype, qkv_desc(dims, w, a_u, nu, qc, 2 * W, nullptr, k_cache, v_cache, s_out + n_cached, s_out + n_cached, cos_sin, max_pos), s);
+        L_GEMM2(dims->dtype, gq, qkv_desc(dims, w, a_u, nu, qc, 2 * W, nullptr, k_cache, v_cache, s_out + n_cached, s_out + n_cached, cos_sin, max_pos), s);
+      } else {
+        L_GEMM(dims->dtype, gq, s);
       }
       WAIT_CACHED_ROWS();
       L_ATTN(dims->dtype, L.q, s_out, N, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);

@@ -110,10 +110,25 @@ static cudaError_t launch_simt(const GemmDesc& g, cudaStream_t s) {
 
 cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t s);  // cb_gemm_tc.cu
 
+cudaError_t launch_gemm_tc_group(const GemmDesc* gs, int n, cudaStream_t s);
+
 cudaError_t launch_gemm(int dt, const GemmDesc& g, cudaStream_t s) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;
   if (dt == DT_BF16) return launch_gemm_tc(g, s);
   return launch_simt<float>(g, s);
+}
+
+// Two independent GEMMs: one tensor-core launch sharing its tile walk when both are
+// non-empty bf16 problems, otherwise one after the other.
+cudaError_t launch_gemm_pair(int dt, const GemmDesc& a, const GemmDesc& b, cudaStream_t s) {
+  const bool ea = a.M == 0 || a.N == 0, eb = b.M == 0 || b.N == 0;
+  if (dt == DT_BF16 && !ea && !eb) {
+    const GemmDesc gs[2] = {a, b};
+    return launch_gemm_tc_group(gs, 2, s);
+  }
+  cudaError_t e = launch_gemm(dt, a, s);
+  if (e != cudaSuccess) return e;
+  return launch_gemm(dt, b, s);
 }
 
 // bf16 SIMT instance: an independent cross-check of the tensor-core GEMM.

@@ -42,8 +42,9 @@ constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;   // two 256-column accumulators
 
 __global__ void __launch_bounds__(THREADS, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              const GemmDesc g, int swiglu) {
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
+              const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+              const GemmDesc g0, const GemmDesc g1, int n_prob, int swiglu) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base for the 128-byte-swizzled tiles
   const uint32_t raw_addr = tc::smem_u32(smem_raw);
@@ -58,11 +59,22 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // one or two independent problems share the launch: problem 0's tiles come first, then
+  // problem 1's, so a short second GEMM fills the first one's partial last wave
   const int out_cols = swiglu ? BN / 2 : BN;
-  const int num_m = (g.M + BM - 1) / BM;
-  const int num_n = (g.N + out_cols - 1) / out_cols;
-  const int total = num_m * num_n;
-  const int KB = (g.K + BK - 1) / BK;
+  const int num_m0 = (g0.M + BM - 1) / BM;
+  const int t0 = num_m0 * ((g0.N + out_cols - 1) / out_cols);
+  const int num_m1 = n_prob > 1 ? (g1.M + BM - 1) / BM : 1;
+  const int total = t0 + (n_prob > 1 ? num_m1 * ((g1.N + out_cols - 1) / out_cols) : 0);
+  const int kb0 = (g0.K + BK - 1) / BK, kb1 = n_prob > 1 ? (g1.K + BK - 1) / BK : kb0;
+  // tile t -> problem, first row and first output column (M-fastest inside a problem)
+  auto locate = [&](int t, int& pr, int& m0, int& n0) {
+    pr = t >= t0;
+    const int u = pr ? t - t0 : t;
+    const int nm = pr ? num_m1 : num_m0;
+    m0 = (u % nm) * BM;
+    n0 = (u / nm) * out_cols;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -74,8 +86,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::mbar_init(&acc_empty[b], EPI_WARPS);
     }
     tc::fence_mbar_init();
-    tc::tma_prefetch_desc(&tmA);
-    tc::tma_prefetch_desc(&tmB);
+    tc::tma_prefetch_desc(&tmA0);
+    tc::tma_prefetch_desc(&tmB0);
+    if (n_prob > 1) {
+      tc::tma_prefetch_desc(&tmA1);
+      tc::tma_prefetch_desc(&tmB1);
+    }
   }
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, TMEM_COLS);
@@ -96,8 +112,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t it = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-      const int m0 = (t % num_m) * BM;
-      const int n0 = (t / num_m) * out_cols;
+      int pr, m0, n0;
+      locate(t, pr, m0, n0);
+      const CUtensorMap* tmA = pr ? &tmA1 : &tmA0;
+      const CUtensorMap* tmB = pr ? &tmB1 : &tmB0;
+      const int KB = pr ? kb1 : kb0;
       for (int kb = 0; kb < KB; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
@@ -107,12 +126,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         tc::mbar_expect_tx(&full[s], A_BYTES + B_BYTES);
-        tc::tma_load_2d(smA + s * A_BYTES, &tmA, &full[s], kb * BK, m0);
+        tc::tma_load_2d(smA + s * A_BYTES, tmA, &full[s], kb * BK, m0);
         if (swiglu) {
-          tc::tma_load_2d(smB + s * B_BYTES, &tmB, &full[s], kb * BK, n0);
-          tc::tma_load_2d(smB + s * B_BYTES + B_BYTES / 2, &tmB, &full[s], kb * BK, (int)g.b_up_row + n0);
+          tc::tma_load_2d(smB + s * B_BYTES, tmB, &full[s], kb * BK, n0);
+          tc::tma_load_2d(smB + s * B_BYTES + B_BYTES / 2, tmB, &full[s], kb * BK, (int)g0.b_up_row + n0);
         } else {
-          tc::tma_load_2d(smB + s * B_BYTES, &tmB, &full[s], kb * BK, n0);
+          tc::tma_load_2d(smB + s * B_BYTES, tmB, &full[s], kb * BK, n0);
         }
       }
     }
@@ -123,6 +142,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++i) {
       const uint32_t b = i & 1;
+      const int KB = t >= t0 ? kb1 : kb0;
       if (!tc::mbar_wait(&acc_empty[b], ((i >> 1) & 1) ^ 1)) {
         ok = false;
         break;
@@ -157,8 +177,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t i = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
       const uint32_t b = i & 1;
-      const int m0 = (t % num_m) * BM;
-      const int n0 = (t / num_m) * out_cols;
+      int pr, m0, n0;
+      locate(t, pr, m0, n0);
+      const GemmDesc& g = pr ? g1 : g0;
       const int m = m0 + lane_base + lane;
       // every lane waits, then the warp re-converges before the .sync.aligned TMEM loads
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&acc_full[b], (i >> 1) & 1))) {
@@ -313,15 +334,26 @@ cudaError_t launch_wait_selftest(uint32_t max_polls, int arrive, cudaStream_t s)
 
 // Host preconditions (checked by the caller's validation, re-checked here): K % 8 == 0,
 // lda/ldb % 8 == 0, A and B 16-byte aligned, N % 16 == 0.
-cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t s) {
-  if (g.M == 0 || g.N == 0) return cudaSuccess;
-  if (g.K % 8 || g.lda % 8 || g.ldb % 8 || g.N % 16 || ((uintptr_t)g.A & 15) || ((uintptr_t)g.B & 15))
-    return cudaErrorInvalidValue;
-  const bool swiglu = g.epi.kind == EPI_SWIGLU;
-  CUtensorMap tmA, tmB;
-  if (!make_map(&tmA, g.A, g.M, g.K, g.lda, BM)) return cudaErrorInvalidValue;
-  const int64_t b_rows = swiglu ? g.b_up_row + g.N : g.N;
-  if (!make_map(&tmB, g.B, b_rows, g.K, g.ldb, swiglu ? BN / 2 : BN)) return cudaErrorInvalidValue;
+cudaError_t launch_gemm_tc_group(const GemmDesc* gs, int n, cudaStream_t s) {
+  if (n < 1 || n > 2) return cudaErrorInvalidValue;
+  const bool swiglu = gs[0].epi.kind == EPI_SWIGLU;
+  if (n > 1 && (swiglu || gs[1].epi.kind == EPI_SWIGLU)) return cudaErrorInvalidValue;
+  CUtensorMap tmA[2], tmB[2];
+  int tiles = 0;
+  const int out_cols = swiglu ? BN / 2 : BN;
+  for (int p = 0; p < n; ++p) {
+    const GemmDesc& g = gs[p];
+    if (g.K % 8 || g.lda % 8 || g.ldb % 8 || g.N % 16 || ((uintptr_t)g.A & 15) || ((uintptr_t)g.B & 15))
+      return cudaErrorInvalidValue;
+    if (!make_map(&tmA[p], g.A, g.M, g.K, g.lda, BM)) return cudaErrorInvalidValue;
+    const int64_t b_rows = swiglu ? g.b_up_row + g.N : g.N;
+    if (!make_map(&tmB[p], g.B, b_rows, g.K, g.ldb, swiglu ? BN / 2 : BN)) return cudaErrorInvalidValue;
+    tiles += ((g.N + out_cols - 1) / out_cols) * ((g.M + BM - 1) / BM);
+  }
+  if (n == 1) {
+    tmA[1] = tmA[0];
+    tmB[1] = tmB[0];
+  }
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -330,14 +362,17 @@ cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  const int out_cols = swiglu ? BN / 2 : BN;
-  const int tiles = ((g.N + out_cols - 1) / out_cols) * ((g.M + BM - 1) / BM);
   static int sms[64] = {0};
   if (dev >= 0 && dev < 64 && !sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
   const int n_sm = (dev >= 0 && dev < 64 && sms[dev] > 0) ? sms[dev] : 148;
   const int grid = tiles < n_sm ? tiles : n_sm;
-  { const cudaError_t e_ = launch_k(k_gemm_tc, dim3(grid), dim3(THREADS), SMEM_BYTES, s, tmA, tmB, g, swiglu ? 1 : 0); if (e_ != cudaSuccess) return e_; }
+  { const cudaError_t e_ = launch_k(k_gemm_tc, dim3(grid), dim3(THREADS), SMEM_BYTES, s, tmA[0], tmB[0], tmA[1], tmB[1], gs[0], n > 1 ? gs[1] : gs[0], n, swiglu ? 1 : 0); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t s) {
+  if (g.M == 0 || g.N == 0) return cudaSuccess;
+  return launch_gemm_tc_group(&g, 1, s);
 }
 
 }  // namespace cb

@@ -133,6 +133,7 @@ cudaError_t launch_deviation_topk_noalloc(int dt, const void* kn, const void* vn
 
 // ---- cb_gemm.cu -----------------------------------------------------------------------
 cudaError_t launch_gemm(int dt, const GemmDesc& g, cudaStream_t s);
+cudaError_t launch_gemm_pair(int dt, const GemmDesc& a, const GemmDesc& b, cudaStream_t s);
 uint32_t take_error_gemm();
 
 // ---- cb_attn.cu -----------------------------------------------------------------------

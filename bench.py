@@ -50,6 +50,7 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="llama7b_layer_4k", choices=sorted(synth.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-quality", action="store_true", help="skip the blend-vs-full-prefill diagnostics")
     p.add_argument("--profile-steps", type=int, default=3)
     return p.parse_args(argv)
 
@@ -270,6 +271,56 @@ def reference_arm(args):
 
 
 # ------------------------------------------------------------------------------ our arm
+def quality_diagnostics(E, B, eng, pool, wl, r0, k_full, v_full, h_full, full_tok):
+    """Reported, not asserted (random-init weights; only the mechanics are meaningful): how
+    far the blended cache of the last layer and the last hidden row are from the full
+    prefill as r grows, and HKVD selection against a random pick of the same size."""
+    import numpy as np
+    import torch
+    L = wl.shape.n_layers
+
+    def ratios_for(r):
+        out = []
+        for l in range(L):
+            if l < wl.check_layer:
+                out.append(None)
+            elif wl.gradual:
+                out.append(B.cb_gradual_ratio(r, l, wl.check_layer, 1.5) if r > 0 else 0.0)
+            else:
+                out.append(r)
+        return out
+
+    def errors(req):
+        k = req.K[L - 1].float()
+        v = req.V[L - 1].float()
+        h = req.x_last[req.m_last - 1].float()
+        return {"k_rel_err_last_layer": float((k - k_full).norm() / k_full.norm()),
+                "v_rel_err_last_layer": float((v - v_full).norm() / v_full.norm()),
+                "h_last_rel_err": float((h - h_full).norm() / h_full.norm()),
+                "same_first_token": int(req.token.item()) == full_tok}
+
+    req = E.Request(eng, pool, r0.order, r0.tokens_host)
+    curve = {}
+    for r in (0.0, 0.05, 0.15, 0.3, 1.0):
+        plan = E.layer_plan(wl.shape, wl.n_tokens, wl.n_cached, ratios_for(r), wl.check_layer, wl.gradual)
+        E.run_blend(req, plan)
+        B.cb_sync(None)
+        curve[str(r)] = errors(req)
+    out = {"vs_full_prefill_by_ratio": curve}
+    if not wl.gradual:
+        plan = E.layer_plan(wl.shape, wl.n_tokens, wl.n_cached, ratios_for(wl.ratio), wl.check_layer, False)
+        c = wl.check_layer
+        k = plan[c][1]
+        n_cand = min(wl.n_cached, wl.n_tokens - 1)
+        g = np.random.default_rng([wl.seed, 7])
+        rows = np.sort(g.choice(n_cand, k, replace=False)).astype(np.int32)
+        E.run_blend(req, plan, sel_override={c: torch.from_numpy(rows).cuda()})
+        B.cb_sync(None)
+        out["random_pick_at_ratio"] = {"ratio": wl.ratio, **errors(req)}
+        out["hkvd_at_ratio"] = curve.get(str(wl.ratio))
+    return out
+
+
 def file_store_e2e(E, B, wl, r0, plan, stream, host_tok, hp, args, t_prefill_layer_ms, h2d_gbs):
     """The chunk store one tier lower: a file (written once, so the OS page cache is warm),
     read layer by layer into pinned memory by the library's parallel reader while earlier
@@ -554,6 +605,10 @@ def our_arm(args):
     B.cb_sync(stream, 120.0)
     full = {"ttft_ms": full_ms, "tokens_per_s": wl.n_tokens / (full_ms / 1e3),
             "blended_speedup": full_ms / (ms / len(reqs)), "steps": n_full}
+    quality = None
+    if not args.no_quality:
+        quality = quality_diagnostics(E, B, eng, pool, wl, r0, r0.K[-1].float().clone(), r0.V[-1].float().clone(),
+                                      h_last.float().clone(), int(full_tok.item()))
 
     # ---------------- the second comparison: prefix caching (only the first chunk, a true
     # prefix, is reused; every later row is recomputed at every layer), same request
@@ -673,7 +728,8 @@ def our_arm(args):
         "launches_per_step": int(launches_per_step),
         "step_tflops": flops / (ms / 1e3) / 1e12,
         "roofline": roofline, "hbm_kernels": hbm_kernels, "kernels": kernels, "gemm_launches": gemm_detail,
-        "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "full_prefill": full, "setup_s": setup_s,
+        "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "full_prefill": full, "quality_diagnostics": quality,
+        "setup_s": setup_s,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

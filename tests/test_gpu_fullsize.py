@@ -123,3 +123,33 @@ def test_zero_ratio_keeps_the_rerotated_cache_bit_exact(setup):
         B.cb_sync(None)
         assert torch.equal(req.K[l][:req.n_cached], kd)
         assert torch.equal(req.V[l][:req.n_cached], vd)
+
+
+@pytest.mark.parametrize("name", ["llama13b_40_8k", "yi34b_60_16k_b4"])
+def test_full_width_layer_of_the_larger_workloads(name):
+    """One layer at the 13B and Yi-34B widths (d 5120 / 7168, GQA 56/8 heads, FFN 13824 /
+    20480, RoPE base 1e4 / 5e6) over a 640-token chunk, as the chunk precompute runs it:
+    K, V and the layer's output rows against the oracle.  The vocabulary is cut to 4096 rows
+    (only the embedding lookup sees it)."""
+    torch = torch_mod()
+    ensure_lib()
+    from non_prefix_kv_gb300 import binding as B
+    from non_prefix_kv_gb300 import engine as E
+    wl = synth.WORKLOADS[name]
+    shape = dataclasses.replace(wl.shape, n_layers=1, vocab=4096)
+    model = synth.make_model(shape, seed=wl.seed)
+    tokens = synth.rng(wl.seed, synth.P_TOKENS).integers(0, shape.vocab, 640).astype(np.int32)
+    ref = O.full_prefill(model, tokens, 0)
+    dm = E.DeviceModel.from_host(model)
+    eng = E.BlendEngine(dm, len(tokens))
+    dt = E.torch_dtype(shape)
+    k = [torch.empty(len(tokens), shape.kv_width, dtype=dt, device="cuda")]
+    v = [torch.empty_like(k[0])]
+    x_all = torch.empty(len(tokens), shape.d_model, dtype=dt, device="cuda")
+    tok = torch.from_numpy(tokens).cuda()
+    eng.full_prefill(tok, k, v, None, x_all)
+    B.cb_sync(None)
+    n = len(tokens)
+    assert rel(host(k[0]), ref["K"][0].reshape(n, -1)) < 1e-2
+    assert rel(host(v[0]), ref["V"][0].reshape(n, -1)) < 1e-2
+    assert rel(host(x_all), ref["x"][1]) < 1e-2

@@ -189,12 +189,7 @@ cudaError_t launch_kv_quantize(int dt, const void* x, int64_t n, int W, uint8_t*
 }
 
 // x = code * s + z (product rounded, then the sum: no fused multiply-add) for 8 channels
-__device__ __forceinline__ void dequant8(const uint8_t* q, const float* sc, const float* zp, float* x) {
-  const uint2 u = *reinterpret_cast<const uint2*>(q);
-  const float4 s0 = reinterpret_cast<const float4*>(sc)[0], s1 = reinterpret_cast<const float4*>(sc)[1];
-  const float4 z0 = reinterpret_cast<const float4*>(zp)[0], z1 = reinterpret_cast<const float4*>(zp)[1];
-  const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-  const float zv[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+__device__ __forceinline__ void dequant8(uint2 u, const float* sv, const float* zv, float* x) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const uint32_t word = i < 4 ? u.x : u.y;
@@ -202,10 +197,18 @@ __device__ __forceinline__ void dequant8(const uint8_t* q, const float* sc, cons
     x[i] = __fadd_rn(__fmul_rn(code, sv[i]), zv[i]);
   }
 }
+__device__ __forceinline__ void load_tab8(const float* p, float* v) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+constexpr int kQ8Rows = 8;   // rows per thread: a chunk's scale/zero stay in registers across them
 
 // k_dst[r] = R(delta[r]) dequant(k_codes[src_row[r]]), v_dst[r] = dequant(v_codes[src_row[r]])
 // with the scale/zero row qrow[r] of the per-chunk tables: loading 8-bit chunk KV and
-// re-positioning it in one pass (one thread per 8 channels, as k_rope_shift).
+// re-positioning it in one pass.  A thread owns 8 channels of kQ8Rows consecutive rows
+// (consecutive threads: consecutive channel groups of the same rows) and reloads the
+// channels' scale/zero only when the row's chunk changes.
 template <typename T>
 __global__ void __launch_bounds__(256) k_rope_shift_q8(T* __restrict__ kd, T* __restrict__ vd,
                                                        const uint8_t* __restrict__ kq,
@@ -220,35 +223,71 @@ __global__ void __launch_bounds__(256) k_rope_shift_q8(T* __restrict__ kd, T* __
   pdl_trigger();
   const int per_row = W >> 3;
   const int half = hd >> 1;
-  const int64_t total = n_rows * per_row;
+  const int64_t n_blocks = (n_rows + kQ8Rows - 1) / kQ8Rows;
+  const int64_t total = n_blocks * per_row;
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
        t += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = t / per_row;
-    const int c0 = (int)(t - r * per_row) << 3;
-    const int64_t sr = src_row ? (int64_t)src_row[r] : r;
-    const int qi = qrow[r];
-    const int dl = delta[r];
-    const int ad = dl < 0 ? -dl : dl;
-    if (ad >= max_pos || sr < 0 || sr >= n_src || qi < 0 || qi >= n_q) {
-      atomicOr(&g_err_mem, ERRBIT_INDEX);
-      continue;
-    }
-    const float sg = dl < 0 ? -1.0f : 1.0f;
-    float x[8], y[8];
-    dequant8(kq + sr * W + c0, ks + (int64_t)qi * W + c0, kz + (int64_t)qi * W + c0, x);
-    const float2* tb = tab + (int64_t)ad * half + ((c0 % hd) >> 1);
+    const int64_t rb = t / per_row;
+    const int c0 = (int)(t - rb * per_row) << 3;
+    const int pair0 = (c0 % hd) >> 1;
+    // every row's indices and codes are loaded before any arithmetic (loads in flight)
+    int64_t rr[kQ8Rows];
+    int qv[kQ8Rows], dv[kQ8Rows];
+    uint2 uk[kQ8Rows], uv[kQ8Rows];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 cs = tb[q];
-      const float c = cs.x, sn = cs.y * sg;
-      y[2 * q] = x[2 * q] * c - x[2 * q + 1] * sn;
-      y[2 * q + 1] = x[2 * q] * sn + x[2 * q + 1] * c;
+    for (int j = 0; j < kQ8Rows; ++j) {
+      const int64_t r = rb * kQ8Rows + j;
+      rr[j] = -1;
+      uk[j] = uv[j] = make_uint2(0, 0);
+      if (r >= n_rows) continue;
+      const int64_t sr = src_row ? (int64_t)src_row[r] : r;
+      const int qi = qrow[r];
+      const int dl = delta[r];
+      const int ad = dl < 0 ? -dl : dl;
+      if (ad >= max_pos || sr < 0 || sr >= n_src || qi < 0 || qi >= n_q) {
+        atomicOr(&g_err_mem, ERRBIT_INDEX);
+        continue;
+      }
+      rr[j] = r;
+      qv[j] = qi;
+      dv[j] = dl;
+      uk[j] = *reinterpret_cast<const uint2*>(kq + sr * W + c0);
+      if (vd) uv[j] = *reinterpret_cast<const uint2*>(vq + sr * W + c0);
     }
-    st8(kd + r * W + c0, y);
-    if (vd) {
-      float v[8];
-      dequant8(vq + sr * W + c0, vs + (int64_t)qi * W + c0, vz + (int64_t)qi * W + c0, v);
-      st8(vd + r * W + c0, v);
+    int cur = -1;
+    float ksv[8], kzv[8], vsv[8], vzv[8];
+#pragma unroll
+    for (int j = 0; j < kQ8Rows; ++j) {
+      if (rr[j] < 0) continue;
+      const int64_t r = rr[j];
+      if (qv[j] != cur) {
+        cur = qv[j];
+        load_tab8(ks + (int64_t)cur * W + c0, ksv);
+        load_tab8(kz + (int64_t)cur * W + c0, kzv);
+        if (vd) {
+          load_tab8(vs + (int64_t)cur * W + c0, vsv);
+          load_tab8(vz + (int64_t)cur * W + c0, vzv);
+        }
+      }
+      const int dl = dv[j];
+      const int ad = dl < 0 ? -dl : dl;
+      const float sg = dl < 0 ? -1.0f : 1.0f;
+      float x[8], y[8];
+      dequant8(uk[j], ksv, kzv, x);
+      const float2* tb = tab + (int64_t)ad * half + pair0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 cs = tb[q];
+        const float c = cs.x, sn = cs.y * sg;
+        y[2 * q] = x[2 * q] * c - x[2 * q + 1] * sn;
+        y[2 * q + 1] = x[2 * q] * sn + x[2 * q + 1] * c;
+      }
+      st8(kd + r * W + c0, y);
+      if (vd) {
+        float v[8];
+        dequant8(uv[j], vsv, vzv, v);
+        st8(vd + r * W + c0, v);
+      }
     }
   }
 }
@@ -259,7 +298,7 @@ cudaError_t launch_rope_shift_q8(int dt, void* kd, void* vd, const uint8_t* kq, 
                                  const int32_t* delta, int64_t n_rows, int W, int hd, const float* tab,
                                  int max_pos, cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
-  const unsigned grid = grid_for(n_rows * (W / 8), 256);
+  const unsigned grid = grid_for((n_rows + kQ8Rows - 1) / kQ8Rows * (W / 8), 256);
   const float2* t2 = reinterpret_cast<const float2*>(tab);
   if (dt == DT_BF16)
     { const cudaError_t e_ = launch_k(k_rope_shift_q8<bf16>, dim3(grid), dim3(256), 0, s, (bf16*)kd, (bf16*)vd, kq, vq, ks, kz, vs, vz, src_row, n_src, qrow, n_q, delta, n_rows, W, hd, t2, max_pos); if (e_ != cudaSuccess) return e_; }

@@ -6,6 +6,8 @@ kernel command that ncu captures are taken on.
   python -m non_prefix_kv_gb300.microbench attention --m 832 --n 4096 --heads 32 --kv-heads 32 --hd 128
   python -m non_prefix_kv_gb300.microbench rope_shift --rows 3840 --width 4096
   python -m non_prefix_kv_gb300.microbench deviation --cand 3840 --width 4096 --k 576
+  python -m non_prefix_kv_gb300.microbench rope_shift_q8 --rows 3840 --width 4096
+  python -m non_prefix_kv_gb300.microbench check_layer --rows 4096 --k 576
 """
 from __future__ import annotations
 
@@ -37,7 +39,7 @@ def _time(fn, iters: int, warmup: int):
 
 def run(argv=None):
     p = argparse.ArgumentParser()
-    p.add_argument("what", choices=["gemm", "attention", "rope_shift", "deviation"])
+    p.add_argument("what", choices=["gemm", "attention", "rope_shift", "rope_shift_q8", "deviation", "check_layer"])
     p.add_argument("--m", type=int, default=4096)
     p.add_argument("--n", type=int, default=8192)
     p.add_argument("--k", type=int, default=4096)
@@ -115,6 +117,48 @@ def run(argv=None):
                    a.warmup)
         by = 4.0 * a.rows * a.width * 2
         out.update(ms=ms, gbs=by / (ms / 1e3) / 1e9, rows=a.rows, width=a.width, host_src=a.host_src)
+    elif a.what == "rope_shift_q8":
+        # decode + re-rotation of an 8-bit store of 6 chunks into rows of the blended cache
+        hd = a.hd
+        shape = ModelShape(1, 256, a.width // hd, a.width // hd, hd, 256, 64, dtype="bf16")
+        dims = E.make_dims(shape)
+        tab = torch.empty(16384 * hd, device="cuda")
+        B.cb_rope_table(tab, 16384, hd, 1e4)
+        kq = torch.randint(0, 256, (a.rows, a.width), device="cuda", generator=g, dtype=torch.uint8)
+        vq = torch.randint(0, 256, (a.rows, a.width), device="cuda", generator=g, dtype=torch.uint8)
+        tabs = [torch.rand(6, a.width, device="cuda", generator=g) * 0.01 for _ in range(4)]
+        qrow = (torch.arange(a.rows, device="cuda", dtype=torch.int32) * 6) // a.rows
+        delta = qrow * 640
+        kd = torch.empty(a.rows, a.width, device="cuda", dtype=bf)
+        vd = torch.empty_like(kd)
+        ms = _time(lambda: B.cb_rope_shift_q8(kd, vd, kq, vq, tabs[0], tabs[1], tabs[2], tabs[3], None, a.rows,
+                                              qrow, 6, delta, a.rows, dims, tab, 16384), a.iters, a.warmup)
+        by = 2.0 * a.rows * a.width * (1 + 2)
+        out.update(ms=ms, gbs=by / (ms / 1e3) / 1e9, rows=a.rows, width=a.width)
+    elif a.what == "check_layer":
+        # the check layer at the 7B shape: K/V GEMM over every row with the deviation in its
+        # epilogue, top-k, KV expansion, Q of the selection, attention, O-proj + FFN
+        shape = ModelShape(2, 4096, 32, 32, 128, 11008, 32000, dtype="bf16")
+        dims = E.make_dims(shape)
+        N, n_cached, k = a.rows, a.rows - 256, a.k
+
+        def rnd(*sz, std=0.02):
+            return (torch.randn(*sz, device="cuda", generator=g) * std).to(bf)
+        lw = {"attn_norm": torch.ones(4096, device="cuda", dtype=bf), "wqkv": rnd(12288, 4096),
+              "wo": rnd(4096, 4096), "ffn_norm": torch.ones(4096, device="cuda", dtype=bf),
+              "w_gate_up": rnd(22016, 4096), "w_down": rnd(4096, 11008)}
+        cw = B.cb_layer_w(*(lw[n].data_ptr() for n in ("attn_norm", "wqkv", "wo", "ffn_norm", "w_gate_up",
+                                                       "w_down")))
+        x = rnd(N, 4096, std=1.0)
+        kc, vc = rnd(N, 4096, std=0.5), rnd(N, 4096, std=0.5)
+        tab = torch.empty(N * 128, device="cuda")
+        B.cb_rope_table(tab, N, 128, 1e4)
+        xo = torch.empty_like(x)
+        so = torch.empty(N, dtype=torch.int32, device="cuda")
+        ws = torch.empty(B.cb_workspace_bytes(dims, N, N), dtype=torch.uint8, device="cuda")
+        ms = _time(lambda: B.cb_blend_layer(dims, cw, B.CB_LAYER_CHECK, x, None, N, N, n_cached, kc, vc, tab, N, k,
+                                            B.CB_DEV_KV, None, xo, so, None, ws), a.iters, a.warmup)
+        out.update(ms=ms, rows=N, k=k)
     else:
         hd = a.hd
         shape = ModelShape(1, 256, a.width // hd, a.width // hd, hd, 256, 64, dtype="bf16")

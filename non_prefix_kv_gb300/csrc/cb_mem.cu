@@ -355,21 +355,34 @@ cudaError_t launch_copy_rows(void* dst, const int32_t* dst_idx, const void* src,
 __global__ void __launch_bounds__(256) k_copy_rows_multi(const CopyJobs J) {
   pdl_wait();
   pdl_trigger();
+  constexpr int U = 4;                   // words per thread per pass, loaded before stored
   const int64_t total = J.end[J.n - 1];
-  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
-       t += (int64_t)gridDim.x * blockDim.x) {
-    int j = 0;
-    while (t >= J.end[j]) ++j;
-    const int64_t u = t - (j ? J.end[j - 1] : 0);
-    const int64_t rv = J.rv[j];
-    const int64_t r = u / rv, c = u - r * rv;
-    const int64_t d = J.di[j] ? (int64_t)J.di[j][r] : r;
-    const int64_t sr = J.si[j] ? (int64_t)J.si[j][r] : r;
-    if (d < 0 || sr < 0 || (J.dbound[j] >= 0 && d >= J.dbound[j]) || (J.sbound[j] >= 0 && sr >= J.sbound[j])) {
-      atomicOr(&g_err_mem, ERRBIT_INDEX);
-      continue;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t0 < total; t0 += U * stride) {
+    uint4 val[U];
+    uint4* dst[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      dst[k] = nullptr;
+      const int64_t t = t0 + k * stride;
+      if (t >= total) continue;
+      int j = 0;
+      while (t >= J.end[j]) ++j;
+      const int64_t u = t - (j ? J.end[j - 1] : 0);
+      const int64_t rv = J.rv[j];
+      const int64_t r = u / rv, c = u - r * rv;
+      const int64_t d = J.di[j] ? (int64_t)J.di[j][r] : r;
+      const int64_t sr = J.si[j] ? (int64_t)J.si[j][r] : r;
+      if (d < 0 || sr < 0 || (J.dbound[j] >= 0 && d >= J.dbound[j]) || (J.sbound[j] >= 0 && sr >= J.sbound[j])) {
+        atomicOr(&g_err_mem, ERRBIT_INDEX);
+        continue;
+      }
+      val[k] = static_cast<const uint4*>(J.src[j])[sr * rv + c];
+      dst[k] = static_cast<uint4*>(J.dst[j]) + d * rv + c;
     }
-    static_cast<uint4*>(J.dst[j])[d * rv + c] = static_cast<const uint4*>(J.src[j])[sr * rv + c];
+#pragma unroll
+    for (int k = 0; k < U; ++k)
+      if (dst[k]) *dst[k] = val[k];
   }
 }
 
@@ -511,10 +524,77 @@ cudaError_t launch_dev_reduce(const float* part, int part_lo, int n_parts, int64
   return cudaGetLastError();
 }
 
+// bf16 rows whose width is a multiple of 1024: each lane issues the 16-byte loads of four
+// column blocks of all four matrices (16 loads in flight) before the arithmetic.  The sum
+// order is fixed (per lane: K then V of each block; then the warp reduction).
+__global__ void __launch_bounds__(256) k_deviation_wide(const bf16* __restrict__ kn, const bf16* __restrict__ vn,
+                                                        const bf16* __restrict__ kr, const bf16* __restrict__ vr,
+                                                        const int32_t* __restrict__ new_row,
+                                                        const int32_t* __restrict__ ref_row, int n_cand, int W,
+                                                        int use_v, float* __restrict__ scores) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int warps_total = (gridDim.x * blockDim.x) >> 5;
+  for (int c = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; c < n_cand; c += warps_total) {
+    const int64_t rn = new_row ? (int64_t)new_row[c] : c;
+    const int64_t rr = ref_row ? (int64_t)ref_row[c] : c;
+    const uint4* a = reinterpret_cast<const uint4*>(kn + rn * W);
+    const uint4* b = reinterpret_cast<const uint4*>(kr + rr * W);
+    const uint4* av = reinterpret_cast<const uint4*>(vn + rn * W);
+    const uint4* bv = reinterpret_cast<const uint4*>(vr + rr * W);
+    float acc = 0.f, accv = 0.f;
+    for (int e = lane; e < (W >> 3); e += 128) {
+      uint4 x[4], y[4], xv[4], yv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        x[u] = __ldcs(a + e + 32 * u);
+        y[u] = __ldcs(b + e + 32 * u);
+        if (use_v) {
+          xv[u] = __ldcs(av + e + 32 * u);
+          yv[u] = __ldcs(bv + e + 32 * u);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const __nv_bfloat162* hx = reinterpret_cast<const __nv_bfloat162*>(&x[u]);
+        const __nv_bfloat162* hy = reinterpret_cast<const __nv_bfloat162*>(&y[u]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 fx = __bfloat1622float2(hx[q]), fy = __bfloat1622float2(hy[q]);
+          const float d0 = fx.x - fy.x, d1 = fx.y - fy.y;
+          acc = fmaf(d0, d0, acc);
+          acc = fmaf(d1, d1, acc);
+        }
+        if (use_v) {
+          const __nv_bfloat162* hxv = reinterpret_cast<const __nv_bfloat162*>(&xv[u]);
+          const __nv_bfloat162* hyv = reinterpret_cast<const __nv_bfloat162*>(&yv[u]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 fx = __bfloat1622float2(hxv[q]), fy = __bfloat1622float2(hyv[q]);
+            const float d0 = fx.x - fy.x, d1 = fx.y - fy.y;
+            accv = fmaf(d0, d0, accv);
+            accv = fmaf(d1, d1, accv);
+          }
+        }
+      }
+    }
+    acc = warp_sum(acc) + warp_sum(accv);
+    if (lane == 0) {
+      scores[c] = acc;
+      if (!isfinite(acc)) atomicOr(&g_err_mem, ERRBIT_NONFINITE);
+    }
+  }
+}
+
 cudaError_t launch_deviation(int dt, const void* kn, const void* vn, const void* kr,
                              const void* vr, const int32_t* new_row, const int32_t* ref_row,
                              int n_cand, int W, int use_v, float* scores, cudaStream_t s) {
   if (n_cand == 0) return cudaSuccess;
+  if (dt == DT_BF16 && W % 1024 == 0) {
+    { const cudaError_t e_ = launch_k(k_deviation_wide, dim3(grid_for((int64_t)n_cand * 32, 256)), dim3(256), 0, s, (const bf16*)kn, (const bf16*)vn, (const bf16*)kr, (const bf16*)vr, new_row, ref_row, n_cand, W, use_v, scores); if (e_ != cudaSuccess) return e_; }
+    return cudaGetLastError();
+  }
   const unsigned grid = grid_for((int64_t)n_cand * 32, 256);
   if (dt == DT_BF16)
     { const cudaError_t e_ = launch_k(k_deviation<bf16>, dim3(grid), dim3(256), 0, s, (const bf16*)kn, (const bf16*)vn, (const bf16*)kr,

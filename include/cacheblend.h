@@ -221,6 +221,13 @@ int cb_topk_from_scores(const float* scores, const int32_t* cand, int32_t n_cand
 
 /* ---- row movement ------------------------------------------------------------------- */
 
+/* RMSNorm of rows: out[i] = x[rows[i]] / sqrt(mean(x[rows[i]]^2) + eps) * gain (rows NULL:
+ * row i), the pre-norm of every layer ([CB-A] model: RMSNorm before attention and FFN).
+ *   x : [*, d] of dtype_in;  gain : [d] of dtype_in;  out : [n, d] of dtype_out
+ *   (bf16 -> bf16, bf16 -> fp32 or fp32 -> fp32);  d a multiple of 8.  Sums in fp32. */
+int cb_rmsnorm(void* out, const void* x, const int32_t* rows, int64_t n, int32_t d, const void* gain,
+               float eps, int32_t dtype_in, int32_t dtype_out, void* stream);
+
 /* dst[i] = src[idx[i]] for i < n; rows of row_bytes bytes (a multiple of 4); idx NULL
  * means i ([CB-A] §Selective recomputation, Step 1: restrict the input to S). */
 int cb_gather_rows(void* dst, const void* src, const int32_t* idx, int64_t n,

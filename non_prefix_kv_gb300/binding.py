@@ -85,6 +85,7 @@ _PROTOS = {
     "cb_file_read": (C.c_int, [C.c_char_p, C.c_uint64, _P, _SZ, _I32]),
     "cb_selftest_wait": (C.c_int, [_I32, _I32, _P]),
     "cb_copy_async": (C.c_int, [_P, _P, _SZ, _P]),
+    "cb_rmsnorm": (C.c_int, [_P, _P, _P, _I64, _I32, _P, C.c_float, _I32, _I32, _P]),
     "cb_io_error_message": (C.c_char_p, []),
     "cb_rope_shift_q8": (C.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _I32, _P, _I64,
                                    C.POINTER(cb_dims), _P, _I32, _P]),
@@ -272,6 +273,11 @@ def cb_file_read(path: str, offset: int, dst, nbytes: int, n_threads: int = 8):
     st = lib().cb_file_read(path.encode(), offset, _ptr(dst), nbytes, n_threads)
     if st != CB_OK:
         raise CBError("cb_file_read", st, lib().cb_io_error_message().decode(errors="replace"))
+
+
+def cb_rmsnorm(out, x, rows, n: int, d: int, gain, eps: float, dtype_in: int, dtype_out: int, stream=None):
+    _check("cb_rmsnorm", lib().cb_rmsnorm(_ptr(out), _ptr(x), _ptr(rows), n, d, _ptr(gain), eps, dtype_in,
+                                          dtype_out, _stream(stream)))
 
 
 def cb_copy_async(dst, src, nbytes: int, stream=None):

@@ -582,6 +582,18 @@ int cb_topk_from_scores(const float* scores, const int32_t* cand, int32_t n_cand
   return CB_OK;
 }
 
+int cb_rmsnorm(void* out, const void* x, const int32_t* rows, int64_t n, int32_t d, const void* gain, float eps,
+               int32_t dtype_in, int32_t dtype_out, void* stream) {
+  if ((dtype_in != CB_F32 && dtype_in != CB_BF16) || (dtype_out != CB_F32 && dtype_out != CB_BF16) ||
+      (dtype_in == CB_F32 && dtype_out == CB_BF16))
+    return fail(CB_ERR_DTYPE, "rmsnorm dtypes %d -> %d", dtype_in, dtype_out);
+  if (n < 0 || d < 8 || d % 8 || !(eps >= 0.0f)) return fail(CB_ERR_SHAPE, "rmsnorm n/d/eps");
+  if (n == 0) return CB_OK;
+  if (!out || !x || !gain) return fail(CB_ERR_INVALID_ARG, "rmsnorm pointer is NULL");
+  L_RMSNORM(dtype_in, dtype_out, out, x, rows, gain, n, d, eps, S(stream));
+  return CB_OK;
+}
+
 int cb_gather_rows(void* dst, const void* src, const int32_t* idx, int64_t n, int64_t row_bytes, void* stream) {
   if (n < 0 || row_bytes < 0 || row_bytes % 4) return fail(CB_ERR_SHAPE, "n/row_bytes");
   if (n == 0) return CB_OK;

@@ -39,7 +39,8 @@ def _time(fn, iters: int, warmup: int):
 
 def run(argv=None):
     p = argparse.ArgumentParser()
-    p.add_argument("what", choices=["gemm", "attention", "rope_shift", "rope_shift_q8", "deviation", "check_layer"])
+    p.add_argument("what", choices=["gemm", "attention", "rope_shift", "rope_shift_q8", "deviation", "check_layer",
+                                    "rmsnorm"])
     p.add_argument("--m", type=int, default=4096)
     p.add_argument("--n", type=int, default=8192)
     p.add_argument("--k", type=int, default=4096)
@@ -134,6 +135,14 @@ def run(argv=None):
         ms = _time(lambda: B.cb_rope_shift_q8(kd, vd, kq, vq, tabs[0], tabs[1], tabs[2], tabs[3], None, a.rows,
                                               qrow, 6, delta, a.rows, dims, tab, 16384), a.iters, a.warmup)
         by = 2.0 * a.rows * a.width * (1 + 2)
+        out.update(ms=ms, gbs=by / (ms / 1e3) / 1e9, rows=a.rows, width=a.width)
+    elif a.what == "rmsnorm":
+        x = torch.randn(a.rows, a.width, device="cuda", generator=g).to(bf)
+        gain = torch.ones(a.width, device="cuda", dtype=bf)
+        y = torch.empty_like(x)
+        ms = _time(lambda: B.cb_rmsnorm(y, x, None, a.rows, a.width, gain, 1e-5, B.CB_BF16, B.CB_BF16), a.iters,
+                   a.warmup)
+        by = 4.0 * a.rows * a.width
         out.update(ms=ms, gbs=by / (ms / 1e3) / 1e9, rows=a.rows, width=a.width)
     elif a.what == "check_layer":
         # the check layer at the 7B shape: K/V GEMM over every row with the deviation in its

@@ -435,9 +435,71 @@ __global__ void __launch_bounds__(256) k_rmsnorm(To* __restrict__ out, const Ti*
   }
 }
 
+// bf16 -> bf16 rows of up to 128*8*VPT elements: 128 threads per row, each holding its
+// VPT 16-byte vectors in registers between the sum and the scaling (the row is read once).
+template <int VPT>
+__global__ void __launch_bounds__(128) k_rmsnorm_reg(bf16* __restrict__ out, const bf16* __restrict__ x,
+                                                     const int32_t* __restrict__ rows,
+                                                     const bf16* __restrict__ g, int d, float eps) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float red[4];
+  const int64_t r = blockIdx.x;
+  const int64_t src = rows ? (int64_t)rows[r] : r;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + src * d);
+  const int nv = d >> 3;
+  uint4 v[VPT];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int c = threadIdx.x + 128 * i;
+    v[i] = c < nv ? xr[c] : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = __bfloat1622float2(h[q]);
+      ss = fmaf(f.x, f.x, ss);
+      ss = fmaf(f.y, f.y, ss);
+    }
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  const float inv = rsqrtf(((red[0] + red[1]) + (red[2] + red[3])) / (float)d + eps);
+  uint4* orow = reinterpret_cast<uint4*>(out + r * d);
+  const uint4* gv = reinterpret_cast<const uint4*>(g);
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int c = threadIdx.x + 128 * i;
+    if (c < nv) {
+      const uint4 gw = gv[c];
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+      const __nv_bfloat162* hg = reinterpret_cast<const __nv_bfloat162*>(&gw);
+      uint4 o;
+      __nv_bfloat162* ho = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(h[q]), fg = __bfloat1622float2(hg[q]);
+        ho[q] = __floats2bfloat162_rn(f.x * inv * fg.x, f.y * inv * fg.y);
+      }
+      orow[c] = o;
+    }
+  }
+}
+
 cudaError_t launch_rmsnorm(int dt_in, int dt_out, void* out, const void* x, const int32_t* rows,
                            const void* g, int64_t n, int d, float eps, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
+  if (dt_in == DT_BF16 && dt_out == DT_BF16 && d % 8 == 0 && d <= 128 * 8 * 8) {
+    if (d <= 128 * 8 * 4)
+      { const cudaError_t e_ = launch_k(k_rmsnorm_reg<4>, dim3((unsigned)n), dim3(128), 0, s, (bf16*)out, (const bf16*)x, rows, (const bf16*)g, d, eps); if (e_ != cudaSuccess) return e_; }
+    else
+      { const cudaError_t e_ = launch_k(k_rmsnorm_reg<8>, dim3((unsigned)n), dim3(128), 0, s, (bf16*)out, (const bf16*)x, rows, (const bf16*)g, d, eps); if (e_ != cudaSuccess) return e_; }
+    return cudaGetLastError();
+  }
   const int threads = d >= 2048 ? 256 : (d >= 512 ? 64 : 32);
   if (dt_in == DT_BF16 && dt_out == DT_BF16)
     { const cudaError_t e_ = launch_k(k_rmsnorm<bf16, bf16>, dim3((unsigned)n), dim3(threads), 0, s, (bf16*)out, (const bf16*)x, rows,

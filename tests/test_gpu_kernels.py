@@ -468,6 +468,29 @@ def test_check_layer_deviation_in_kv_gemm_epilogue(B, shape, dev_mode):
     assert rel(got, ref) < 2e-2
 
 
+# d up to 4096 and up to 8192 take the register-resident bf16 kernels, wider rows and fp32
+# input the generic one; a row list gathers, a ragged d covers a partial last vector pass.
+@pytest.mark.parametrize("din,dout", [("bf16", "bf16"), ("bf16", "f32"), ("f32", "f32")])
+@pytest.mark.parametrize("n,d,gather", [(1, 8, False), (5, 1000, True), (300, 4096, False), (77, 4104, True),
+                                        (64, 8192, True), (9, 8200, False)])
+def test_rmsnorm(B, din, dout, n, d, gather):
+    torch = torch_mod()
+    n_x = n + 13
+    x = synth.test_tensor((n_x, d), 70 + d, std=1.5, dtype=din)
+    g = synth.test_tensor((d,), 71 + d, std=0.3, dtype=din) + 1.0
+    g = synth.round_bf16(g) if din == "bf16" else g
+    rows = (synth.rng(72, synth.P_NOISE).permutation(n_x)[:n] if gather else np.arange(n)).astype(np.int32)
+    out = torch.empty((n, d), dtype=tdt(dout), device="cuda")
+    code = {"f32": B.CB_F32, "bf16": B.CB_BF16}
+    B.cb_rmsnorm(out, dev(x, din), dev_i32(rows) if gather else None, n, d, dev(g, din), 1e-5, code[din],
+                 code[dout])
+    B.cb_sync(None)
+    want = O.rmsnorm(x[rows], g, 1e-5)
+    assert rel(host(out), want) < TOL[dout if din == "f32" else "bf16"]
+    assert np.max(np.abs(host(out) - want)) < (1e-4 if dout == "f32" and din == "f32" else 3e-2) * np.max(
+        np.abs(want))
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_lmhead_argmax(B, dtype):
     torch = torch_mod()

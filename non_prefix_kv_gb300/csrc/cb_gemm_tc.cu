@@ -31,20 +31,30 @@ uint32_t take_error_gemm_tc() {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = kGemmTileN;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
-constexpr int B_BYTES = BN * BK * 2;   // 32 KB
-constexpr int SMEM_BYTES = STAGES * (A_BYTES + B_BYTES) + 1024 /*align slack*/ + 256 /*barriers*/;
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
-constexpr uint32_t TMEM_COLS = 512;   // two 256-column accumulators
+constexpr uint32_t TMEM_COLS = 512;   // two accumulators of up to 256 columns, 256 apart
 
+// Tile width BN (accumulator columns): 256, or 224 / 192 where the narrower tile needs fewer
+// waves over the SMs (a 512-tile GEMM is 3.37 waves of 152 SMs at 256 columns, exactly 4 at
+// 224).  A narrower tile leaves room for a fifth ring stage.
+template <int BN>
+struct TileCfg {
+  static_assert(BN % 32 == 0 && BN <= 256, "8 epilogue warps take BN/32 16-column chunks each");
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGES = BN == 256 ? 4 : 5;
+  static constexpr int SMEM_BYTES = STAGES * (A_BYTES + B_BYTES) + 1024 /*align slack*/ + 256 /*barriers*/;
+};
+
+template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
               const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
               const GemmDesc g0, const GemmDesc g1, int n_prob, int swiglu) {
+  constexpr int STAGES = TileCfg<BN>::STAGES;
+  constexpr int B_BYTES = TileCfg<BN>::B_BYTES;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base for the 128-byte-swizzled tiles
   const uint32_t raw_addr = tc::smem_u32(smem_raw);
@@ -148,7 +158,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       tc::tc_fence_after();
-      const uint32_t d_tmem = tmem + b * BN;
+      const uint32_t d_tmem = tmem + b * 256;
       for (int kb = 0; kb < KB; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
@@ -187,7 +197,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       tc::tc_fence_after();
-      const uint32_t trow = tmem + b * BN + (static_cast<uint32_t>(lane_base) << 16);
+      const uint32_t trow = tmem + b * 256 + (static_cast<uint32_t>(lane_base) << 16);
       if (!swiglu && g.epi.dev_part != nullptr) {
         // K/V columns with the deviation against the cached row: the cached values of the
         // chunk DEV_AHEAD further on are loaded while this chunk is processed
@@ -332,23 +342,56 @@ cudaError_t launch_wait_selftest(uint32_t max_polls, int arrive, cudaStream_t s)
   return cudaGetLastError();
 }
 
-// Host preconditions (checked by the caller's validation, re-checked here): K % 8 == 0,
-// lda/ldb % 8 == 0, A and B 16-byte aligned, N % 16 == 0.
-cudaError_t launch_gemm_tc_group(const GemmDesc* gs, int n, cudaStream_t s) {
-  if (n < 1 || n > 2) return cudaErrorInvalidValue;
-  const bool swiglu = gs[0].epi.kind == EPI_SWIGLU;
-  if (n > 1 && (swiglu || gs[1].epi.kind == EPI_SWIGLU)) return cudaErrorInvalidValue;
-  CUtensorMap tmA[2], tmB[2];
+namespace {
+
+int sm_count() {
+  static int sms[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+  return sms[dev] > 0 ? sms[dev] : 148;
+}
+
+int tiles_for(const GemmDesc* gs, int n, int out_cols) {
   int tiles = 0;
+  for (int p = 0; p < n; ++p) tiles += ((gs[p].N + out_cols - 1) / out_cols) * ((gs[p].M + BM - 1) / BM);
+  return tiles;
+}
+
+// Tile width for one launch: each SM's share of the work is ceil(tiles / SMs) tiles of BN
+// columns, so pick the BN with the smallest product; a narrower tile must save at least 5%
+// (it moves more operand bytes per FLOP).  SwiGLU (gate and up halves of 16-column chunks per
+// epilogue warp) and the fused deviation (partials laid out per 256 columns) keep 256.
+int pick_tile_n(const GemmDesc* gs, int n, int n_sm) {
+  if (gs[0].epi.kind == EPI_SWIGLU) return 256;
+  for (int p = 0; p < n; ++p)
+    if (gs[p].epi.dev_part != nullptr) return 256;
+  const int cand[3] = {256, 224, 192};
+  int best = 256;
+  int64_t best_cost = 0;
+  for (int c = 0; c < 3; ++c) {
+    const int64_t cost = (int64_t)((tiles_for(gs, n, cand[c]) + n_sm - 1) / n_sm) * cand[c];
+    if (c == 0 || cost * 20 <= best_cost * 19) {
+      if (c == 0 || cost < best_cost) {
+        best = cand[c];
+        best_cost = cost;
+      }
+    }
+  }
+  return best;
+}
+
+template <int BN>
+cudaError_t launch_tiles(const GemmDesc* gs, int n, bool swiglu, int n_sm, cudaStream_t s) {
+  constexpr int SMEM_BYTES = TileCfg<BN>::SMEM_BYTES;
+  CUtensorMap tmA[2], tmB[2];
   const int out_cols = swiglu ? BN / 2 : BN;
   for (int p = 0; p < n; ++p) {
     const GemmDesc& g = gs[p];
-    if (g.K % 8 || g.lda % 8 || g.ldb % 8 || g.N % 16 || ((uintptr_t)g.A & 15) || ((uintptr_t)g.B & 15))
-      return cudaErrorInvalidValue;
     if (!make_map(&tmA[p], g.A, g.M, g.K, g.lda, BM)) return cudaErrorInvalidValue;
     const int64_t b_rows = swiglu ? g.b_up_row + g.N : g.N;
     if (!make_map(&tmB[p], g.B, b_rows, g.K, g.ldb, swiglu ? BN / 2 : BN)) return cudaErrorInvalidValue;
-    tiles += ((g.N + out_cols - 1) / out_cols) * ((g.M + BM - 1) / BM);
   }
   if (n == 1) {
     tmA[1] = tmA[0];
@@ -358,16 +401,40 @@ cudaError_t launch_gemm_tc_group(const GemmDesc* gs, int n, cudaStream_t s) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  static int sms[64] = {0};
-  if (dev >= 0 && dev < 64 && !sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-  const int n_sm = (dev >= 0 && dev < 64 && sms[dev] > 0) ? sms[dev] : 148;
+  const int tiles = tiles_for(gs, n, out_cols);
   const int grid = tiles < n_sm ? tiles : n_sm;
-  { const cudaError_t e_ = launch_k(k_gemm_tc, dim3(grid), dim3(THREADS), SMEM_BYTES, s, tmA[0], tmB[0], tmA[1], tmB[1], gs[0], n > 1 ? gs[1] : gs[0], n, swiglu ? 1 : 0); if (e_ != cudaSuccess) return e_; }
+  const cudaError_t e = launch_k(k_gemm_tc<BN>, dim3(grid), dim3(THREADS), SMEM_BYTES, s, tmA[0], tmB[0], tmA[1],
+                                 tmB[1], gs[0], n > 1 ? gs[1] : gs[0], n, swiglu ? 1 : 0);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+// Host preconditions (checked by the caller's validation, re-checked here): K % 8 == 0,
+// lda/ldb % 8 == 0, A and B 16-byte aligned, N % 16 == 0.
+cudaError_t launch_gemm_tc_group(const GemmDesc* gs, int n, cudaStream_t s) {
+  if (n < 1 || n > 2) return cudaErrorInvalidValue;
+  const bool swiglu = gs[0].epi.kind == EPI_SWIGLU;
+  if (n > 1 && (swiglu || gs[1].epi.kind == EPI_SWIGLU)) return cudaErrorInvalidValue;
+  for (int p = 0; p < n; ++p) {
+    const GemmDesc& g = gs[p];
+    if (g.K % 8 || g.lda % 8 || g.ldb % 8 || g.N % 16 || ((uintptr_t)g.A & 15) || ((uintptr_t)g.B & 15))
+      return cudaErrorInvalidValue;
+  }
+  const int n_sm = sm_count();
+  switch (pick_tile_n(gs, n, n_sm)) {
+    case 224:
+      return launch_tiles<224>(gs, n, swiglu, n_sm, s);
+    case 192:
+      return launch_tiles<192>(gs, n, swiglu, n_sm, s);
+    default:
+      return launch_tiles<256>(gs, n, swiglu, n_sm, s);
+  }
 }
 
 cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t s) {

@@ -262,11 +262,13 @@ def test_rope_shift_q8_decodes_and_rotates(B, dtype):
 
 
 # ------------------------------------------------------------------------------ GEMM
-# ragged M, N and K tails, single-wave and multi-wave tile counts, the 7B layer's shapes
+# ragged M, N and K tails, single-wave and multi-wave tile counts, the 7B layer's shapes; the
+# launches cover the 256-, 224- and 192-column tile widths (4096 x 8192 keeps 256, 4096 x 4096
+# takes 224, 832 x 12288 takes 192)
 @pytest.mark.parametrize("M,N,K", [(1, 16, 64), (7, 256, 72), (127, 272, 4096), (129, 512, 136),
                                    (300, 4096, 1024), (832, 1024, 4096), (1000, 768, 11008),
                                    (832, 4096, 4096), (4096, 4096, 1000), (256, 8192, 4096),
-                                   (832, 12288, 4096), (4096, 4096, 11008)])
+                                   (832, 12288, 4096), (4096, 4096, 11008), (4096, 8192, 512)])
 def test_linear_bf16_tensor_cores(B, M, N, K):
     torch = torch_mod()
     x = synth.test_tensor((M, K), 40 + M, dtype="bf16")

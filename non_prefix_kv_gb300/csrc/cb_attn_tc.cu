@@ -371,8 +371,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) o[i] *= inv;
         if (m < M) {
-          st8(orow + c * 16, o);
-          st8(orow + c * 16 + 8, o + 8);
+          if ((reinterpret_cast<uintptr_t>(orow + c * 16) & 31) == 0) {
+            st16_v8(orow + c * 16, o);
+          } else {
+            st8(orow + c * 16, o);
+            st8(orow + c * 16 + 8, o + 8);
+          }
         }
       }
     } else if (lane == 0) {

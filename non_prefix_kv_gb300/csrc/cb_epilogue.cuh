@@ -13,6 +13,12 @@ namespace cb {
 
 template <typename T, int NV>
 __device__ __forceinline__ void st_vec(T* p, const float* v) {
+  if constexpr (NV == 16 && sizeof(T) == 2) {
+    if ((reinterpret_cast<uintptr_t>(p) & 31) == 0) {
+      st16_v8(p, v);
+      return;
+    }
+  }
   if constexpr (NV % 8 == 0) {
 #pragma unroll
     for (int i = 0; i < NV; i += 8) st8(p + i, v + i);
@@ -23,6 +29,12 @@ __device__ __forceinline__ void st_vec(T* p, const float* v) {
 }
 template <typename T, int NV>
 __device__ __forceinline__ void ld_vec(const T* p, float* v) {
+  if constexpr (NV == 16 && sizeof(T) == 2) {
+    if ((reinterpret_cast<uintptr_t>(p) & 31) == 0) {
+      ld16_v8(p, v);
+      return;
+    }
+  }
   if constexpr (NV % 8 == 0) {
 #pragma unroll
     for (int i = 0; i < NV; i += 8) ld8(p + i, v + i);

@@ -198,41 +198,55 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int s = 0; s < L::NSLAB; ++s)
         tc::tma_load_2d(sKV + st * L::KV_BYTES + s * SLAB, map, &kv_full[st], g * HD + 64 * s, (i >> 1) * BN);
     }
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer (warp 1)
     // S(0), S(1), then per key tile j: P.V(j) once its P is written, then S(j+2) into the
     // buffer of tile j-1, whose P.V was issued a softmax earlier and has normally completed.
+    // The whole warp runs the loop and waits; the elected lane issues.
     constexpr uint32_t idesc_s = tc::idesc_bf16_f32(BM, BN);
     constexpr uint32_t idesc_o = tc::idesc_bf16_f32(BM, HD, true);
-    bool ok = tc::mbar_wait(q_full, 0);
+    // descriptor of K/V slot 0 and of Q; the address field (bits 0-13, bytes >> 4) is advanced
+    // by plain addition below
+    const uint64_t kv_desc = tc::desc_sw128(tc::smem_u32(sKV));
+    const uint64_t v_desc = tc::desc_sw128_mn(tc::smem_u32(sKV), SLAB);
+    const uint64_t q_desc = tc::desc_sw128(tc::smem_u32(sQ));
+    // ok stays warp-uniform, so every lane reaches each elect.sync / __syncwarp
+    bool ok = __all_sync(0xffffffffu, tc::mbar_wait(q_full, 0));
     auto issue_s = [&](int jj) {
       const int b = jj % NSB, i = 2 * jj, st = i % NST;
-      ok = ok && tc::mbar_wait(&kv_full[st], (i / NST) & 1) &&
-           (jj < NSB || tc::mbar_wait(&pv_done[b], ((jj - NSB) / NSB) & 1));
+      ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(&kv_full[st], (i / NST) & 1) &&
+                                             (jj < NSB || tc::mbar_wait(&pv_done[b], ((jj - NSB) / NSB) & 1)));
       if (!ok) return;
       tc::tc_fence_after();
-      const uint32_t kb = tc::smem_u32(sKV + st * L::KV_BYTES);
-      const uint32_t qb = tc::smem_u32(sQ);
+      if (tc::elect_one()) {
+        const uint64_t kd = kv_desc + (uint64_t)((st * L::KV_BYTES) >> 4);
 #pragma unroll
-      for (int k = 0; k < HD / 16; ++k) {
-        const uint32_t off = (k >> 2) * SLAB + (k & 3) * 32;
-        tc::mma_bf16(tmem + TM_S0 + b * BN, tc::desc_sw128(qb + off), tc::desc_sw128(kb + off), idesc_s, k > 0);
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint32_t off = ((k >> 2) * SLAB + (k & 3) * 32) >> 4;
+          tc::mma_bf16(tmem + TM_S0 + b * BN, q_desc + off, kd + off, idesc_s, k > 0);
+        }
+        tc::mma_commit(&s_full[b]);
+        tc::mma_commit(&kv_empty[st]);
       }
-      tc::mma_commit(&s_full[b]);
-      tc::mma_commit(&kv_empty[st]);
+      __syncwarp();
     };
     auto issue_pv = [&](int jj) {
       const int b = jj % NSB, i = 2 * jj + 1, st = i % NST;
-      ok = ok && tc::mbar_wait(&p_full[b], (jj / NSB) & 1) && tc::mbar_wait(&kv_full[st], (i / NST) & 1);
+      ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(&p_full[b], (jj / NSB) & 1) &&
+                                             tc::mbar_wait(&kv_full[st], (i / NST) & 1));
       if (!ok) return;
       tc::tc_fence_after();
-      const uint32_t vb = tc::smem_u32(sKV + st * L::KV_BYTES);
+      if (tc::elect_one()) {
+        const uint64_t vd = v_desc + (uint64_t)((st * L::KV_BYTES) >> 4);
+        const uint32_t pa = tmem + TM_S0 + b * BN;
 #pragma unroll
-      for (int k = 0; k < BN / 16; ++k)
-        tc::mma_bf16_ts(tmem + TM_O1, tmem + TM_S0 + b * BN + k * 8, tc::desc_sw128_mn(vb + k * 16 * 128, SLAB),
-                        idesc_o, (jj > 0 || k > 0) ? 1u : 0u);
-      tc::mma_commit(&pv_done[b]);
-      tc::mma_commit(&kv_empty[st]);
+        for (int k = 0; k < BN / 16; ++k)
+          tc::mma_bf16_ts(tmem + TM_O1, pa + k * 8, vd + (uint64_t)((k * 16 * 128) >> 4), idesc_o,
+                          (jj > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit(&pv_done[b]);
+        tc::mma_commit(&kv_empty[st]);
+      }
+      __syncwarp();
     };
     issue_s(0);
     if (T > 1) issue_s(1);
@@ -240,7 +254,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       issue_pv(jj);
       if (jj + 2 < T) issue_s(jj + 2);
     }
-    if (!ok) atomicOr(&g_err_attn_tc, ERRBIT_TIMEOUT);
+    if (!ok && lane == 0) atomicOr(&g_err_attn_tc, ERRBIT_TIMEOUT);
   } else if (warp >= 2) {
     // ------------------------------------------------------------------ softmax + epilogue
     const int lane_base = (warp & 3) * 32;

@@ -75,6 +75,19 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// One lane of the (converged) warp returns true.  MMA issue loops run on a whole warp and
+// issue from the elected lane: the loop control and descriptor arithmetic stay warp-uniform,
+// which keeps the issuing warp from being starved of issue slots by busy neighbours (a
+// single-lane issuer measured 84-117 cycles per 128x128x16 MMA next to ALU-bound warps,
+// against 64 alone; the elected warp-wide loop, 64-66).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ---- TMEM -----------------------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),

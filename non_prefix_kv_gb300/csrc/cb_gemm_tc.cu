@@ -145,15 +145,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer: accumulator b = local tile index & 1
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (warp 1; the elected lane issues, all lanes wait, so the
+    // loop stays warp-uniform): accumulator b = local tile index & 1
     constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
+    // stage-0 descriptors; the address field (bytes >> 4) advances by plain addition
+    const uint64_t a_desc0 = tc::desc_sw128(tc::smem_u32(smA));
+    const uint64_t b_desc0 = tc::desc_sw128(tc::smem_u32(smB));
     uint32_t it = 0, i = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++i) {
       const uint32_t b = i & 1;
       const int KB = t >= t0 ? kb1 : kb0;
-      if (!tc::mbar_wait(&acc_empty[b], ((i >> 1) & 1) ^ 1)) {
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&acc_empty[b], ((i >> 1) & 1) ^ 1))) {
         ok = false;
         break;
       }
@@ -162,23 +166,29 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int kb = 0; kb < KB; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
-        if (!tc::mbar_wait(&full[s], ph)) {
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(&full[s], ph))) {
           ok = false;
           break;
         }
         tc::tc_fence_after();
-        const uint64_t a_desc = tc::desc_sw128(tc::smem_u32(smA + s * A_BYTES));
-        const uint64_t b_desc = tc::desc_sw128(tc::smem_u32(smB + s * B_BYTES));
+        if (tc::elect_one()) {
+          const uint64_t a_desc = a_desc0 + (uint64_t)((s * A_BYTES) >> 4);
+          const uint64_t b_desc = b_desc0 + (uint64_t)((s * B_BYTES) >> 4);
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          // advance 16 bf16 = 32 bytes along K inside the swizzled 128-byte row
-          tc::mma_bf16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, (kb | k) != 0);
+          for (int k = 0; k < BK / 16; ++k) {
+            // advance 16 bf16 = 32 bytes along K inside the swizzled 128-byte row
+            tc::mma_bf16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, (kb | k) != 0);
+          }
+          tc::mma_commit(&empty[s]);
         }
-        tc::mma_commit(&empty[s]);
+        __syncwarp();
       }
-      if (ok) tc::mma_commit(&acc_full[b]);
+      if (ok) {
+        if (tc::elect_one()) tc::mma_commit(&acc_full[b]);
+        __syncwarp();
+      }
     }
-    if (!ok) atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
+    if (!ok && lane == 0) atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
   } else if (warp >= 2) {
     // ---------------- epilogue: drains accumulator b while the MMAs fill the other one
     const int lane_base = (warp & 3) * 32;

@@ -8,16 +8,12 @@
 //                          row visible iff t <= q_pos[row]
 //   O  += P_j V_j          tcgen05.mma, B = V_j (MN-major), fp32 accumulator in TMEM
 // The running max m is raised lazily: O is rescaled only when a row's max grows by more
-// than 2^8, so most tiles never touch O.  Two kernels:
-//   k_attn_tc   one query tile per CTA (selected rows spread over the sequence).  S is
-//               triple-buffered in TMEM (S_0 | S_1 | S_2 | O), so S_{j+1} and S_{j+2} are
-//               computed while the softmax works on S_j; P_j is written back over S_j in TMEM
-//               (bf16 pairs) and the P.V MMA takes its A operand from there; K and V stream
-//               through a TMA ring.
-//   k_attn_tc2  two query tiles per CTA sharing each K/V tile (dense causal prefill); P
-//               goes through shared memory (128-byte-swizzled K-major) and an event-driven
-//               MMA issuer interleaves the two tiles' S and P.V.
-// Warp roles in both: 0 = TMA producer, 1 = TMEM allocator + MMA issuer, 2..9 = softmax and
+// than 2^8, so most tiles never touch O.  One CTA per (128-query tile, query head), launched
+// heads fastest and longest query tiles first.  S is triple-buffered in TMEM (S_0 | S_1 | S_2
+// | O), so S_{j+1} and S_{j+2} are computed while the softmax works on S_j; P_j is written
+// back over S_j in TMEM (bf16 pairs) and the P.V MMA takes its A operand from there; K and V
+// stream through a TMA ring.  Warp roles: 0 = TMA producer, 1 = TMEM allocator + MMA issuer
+// (the whole warp runs the issue loop, the elected lane issues), 2..9 = softmax and
 // epilogue; warp w reads TMEM lanes 32*(w%4)..+31.
 #include <cuda.h>
 #include <math.h>
@@ -45,8 +41,7 @@ constexpr int SLAB = 128 * 128;      // bytes of one [128 rows x 64 bf16] swizzl
 constexpr int NSOFT = 8;             // softmax warps: two per TMEM lane quarter
 constexpr int THREADS = 32 * (2 + NSOFT);
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S0 = 0, TM_O = 256;   // query-tile pairs: S_0 | S_1 | O_0 | O_1
-constexpr uint32_t TM_O1 = 384;             // single tile: S_0 | S_1 | S_2 | O
+constexpr uint32_t TM_S0 = 0, TM_O1 = 384;  // S_0 | S_1 | S_2 | O
 constexpr float kRescaleLog2 = 8.0f;
 
 template <int HD>
@@ -406,337 +401,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// ---------------------------------------------------------------------------- query-tile pairs
-// Two 128-query tiles per CTA, each with its own softmax warpgroup (warps 2-5: tile 0,
-// warps 6-9: tile 1), sharing the K/V tiles.  While one warpgroup exponentiates its scores
-// the tensor core runs the other tile's S and P.V, so neither the MMA pipe nor the softmax
-// waits on the other for long.  Each softmax thread owns a whole 128-key score row.  TMEM:
-// S0 | S1 | O0 | O1.  K streams through 2 stages, V through 1, one P tile per query tile.
-constexpr int THREADS2 = 320;
-
-template <int HD>
-struct Layout2 {
-  static constexpr int NSLAB = HD / 64;
-  static constexpr int Q_TILE = NSLAB * SLAB;
-  static constexpr int KV_BYTES = NSLAB * SLAB;
-  static constexpr int P_TILE = 2 * SLAB;
-  static constexpr int OFF_Q = 0;                          // 2 query tiles
-  static constexpr int OFF_K = OFF_Q + 2 * Q_TILE;         // 2 stages
-  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;       // 1 stage
-  static constexpr int OFF_P = OFF_V + KV_BYTES;           // one P tile per query tile
-  static constexpr int OFF_BAR = OFF_P + 2 * P_TILE;
-  static constexpr int BYTES = OFF_BAR + 256;
-  static constexpr int SMEM = BYTES + 1024;
-};
-
-template <int HD>
-__global__ void __launch_bounds__(THREADS2, 1)
-    k_attn_tc2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-               const __grid_constant__ CUtensorMap tmV, const int32_t* __restrict__ q_pos, int M,
-               int64_t n_kv, int H, int Hkv, bf16* __restrict__ out, float scale_log2) {
-  pdl_wait();
-  pdl_trigger();
-  using L = Layout2<HD>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = tc::smem_u32(smem_raw);
-  uint8_t* base = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
-  uint8_t* sQ = base + L::OFF_Q;
-  uint8_t* sK = base + L::OFF_K;
-  uint8_t* sV = base + L::OFF_V;
-  uint8_t* sP = base + L::OFF_P;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::OFF_BAR);
-  uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;     // [2 stages]
-  uint64_t* k_empty = bars + 3;    // [2 stages]
-  uint64_t* v_full = bars + 5;
-  uint64_t* v_empty = bars + 6;
-  uint64_t* s_full = bars + 7;     // [2 query tiles]
-  uint64_t* s_free = bars + 9;     // [2 query tiles]
-  uint64_t* p_full = bars + 11;    // [2 query tiles]
-  uint64_t* pv_done = bars + 13;   // [2 query tiles]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
-  int* s_qmax = reinterpret_cast<int*>(bars + 16);   // [2]
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = gridDim.y - 1 - blockIdx.y;      // as in k_attn_tc: heads fastest, longest pairs first
-  const int h = blockIdx.x;
-  const int g = h / (H / Hkv);
-  const int m0 = qt * 2 * BM;
-
-  if (threadIdx.x == 0) {
-    tc::mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&k_full[i], 1);
-      tc::mbar_init(&k_empty[i], 1);
-      tc::mbar_init(&s_full[i], 1);
-      tc::mbar_init(&s_free[i], 4);
-      tc::mbar_init(&p_full[i], 4);
-      tc::mbar_init(&pv_done[i], 1);
-    }
-    tc::mbar_init(v_full, 1);
-    tc::mbar_init(v_empty, 1);
-    tc::fence_mbar_init();
-    tc::tma_prefetch_desc(&tmQ);
-    tc::tma_prefetch_desc(&tmK);
-    tc::tma_prefetch_desc(&tmV);
-  }
-  if (warp == 0) {
-    // furthest key each query tile may see (-1: the tile has no valid row)
-    int mx0 = -1, mx1 = -1;
-    for (int i = lane; i < 2 * BM; i += 32) {
-      const int m = m0 + i;
-      if (m < M) {
-        int p = q_pos[m];
-        if (p < 0 || p >= n_kv) {
-          atomicOr(&g_err_attn_tc, ERRBIT_INDEX);
-          p = p < 0 ? 0 : (int)(n_kv - 1);
-        }
-        if (i < BM) mx0 = p > mx0 ? p : mx0;
-        else mx1 = p > mx1 ? p : mx1;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mx0 = max(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-      mx1 = max(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-    }
-    if (lane == 0) {
-      s_qmax[0] = mx0;
-      s_qmax[1] = mx1;
-    }
-  }
-  if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, TMEM_COLS);
-    tc::tmem_relinquish();
-  }
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  int Tt[2];
-  Tt[0] = s_qmax[0] < 0 ? 0 : s_qmax[0] / BN + 1;   // key tiles each query tile visits
-  Tt[1] = s_qmax[1] < 0 ? 0 : s_qmax[1] / BN + 1;
-  const int T = Tt[0] > Tt[1] ? Tt[0] : Tt[1];
-
-  if (warp == 0 && lane == 0) {
-    // ------------------------------------------------------------------ TMA producer
-    tc::mbar_expect_tx(q_full, 2 * L::Q_TILE);
-    for (int t = 0; t < 2; ++t)
-      for (int s = 0; s < L::NSLAB; ++s)
-        tc::tma_load_2d(sQ + t * L::Q_TILE + s * SLAB, &tmQ, q_full, h * HD + 64 * s, m0 + t * BM);
-    bool ok = true;
-    if (T > 0) {
-      tc::mbar_expect_tx(&k_full[0], L::KV_BYTES);
-      for (int s = 0; s < L::NSLAB; ++s) tc::tma_load_2d(sK + s * SLAB, &tmK, &k_full[0], g * HD + 64 * s, 0);
-    }
-    for (int j = 0; ok && j < T; ++j) {
-      if (j + 1 < T) {   // K one tile ahead
-        const int st = (j + 1) & 1;
-        if (!tc::mbar_wait(&k_empty[st], (((j + 1) >> 1) & 1) ^ 1)) {
-          ok = false;
-          break;
-        }
-        tc::mbar_expect_tx(&k_full[st], L::KV_BYTES);
-        for (int s = 0; s < L::NSLAB; ++s)
-          tc::tma_load_2d(sK + st * L::KV_BYTES + s * SLAB, &tmK, &k_full[st], g * HD + 64 * s, (j + 1) * BN);
-      }
-      if (!tc::mbar_wait(v_empty, (j & 1) ^ 1)) {
-        ok = false;
-        break;
-      }
-      tc::mbar_expect_tx(v_full, L::KV_BYTES);
-      for (int s = 0; s < L::NSLAB; ++s) tc::tma_load_2d(sV + s * SLAB, &tmV, v_full, g * HD + 64 * s, j * BN);
-    }
-    if (!ok) atomicOr(&g_err_attn_tc, ERRBIT_TIMEOUT);
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------------ MMA issuer
-    // Event-driven: probe every pending operation and issue whichever is ready, so a late
-    // softmax warpgroup never holds back the other query tile's S or P.V.  K stage j % 2 is
-    // released once S_0(j) and S_1(j) are both issued, V once both P.V(j) are.
-    constexpr uint32_t idesc_s = tc::idesc_bf16_f32(BM, BN);
-    constexpr uint32_t idesc_o = tc::idesc_bf16_f32(BM, HD, true);
-    bool ok = tc::mbar_wait(q_full, 0);
-    int ns[2] = {0, 0}, np[2] = {0, 0};     // next S / P.V tile per query tile
-    uint32_t idle = 0;
-    while (ok && (ns[0] < Tt[0] || ns[1] < Tt[1] || np[0] < Tt[0] || np[1] < Tt[1])) {
-      bool progressed = false;
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int j = ns[t];
-        if (j < Tt[t] && tc::mbar_test(&k_full[j & 1], (j >> 1) & 1) &&
-            (j == 0 || tc::mbar_test(&s_free[t], (j - 1) & 1))) {
-          tc::tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < HD / 16; ++k) {
-            const uint32_t off = (k & 3) * 32;
-            const uint64_t a = tc::desc_sw128(tc::smem_u32(sQ + t * L::Q_TILE + (k >> 2) * SLAB) + off);
-            const uint64_t b = tc::desc_sw128(tc::smem_u32(sK + (j & 1) * L::KV_BYTES + (k >> 2) * SLAB) + off);
-            tc::mma_bf16(tmem + t * BN, a, b, idesc_s, k > 0);
-          }
-          tc::mma_commit(&s_full[t]);
-          ns[t] = j + 1;
-          // the other tile is done with K_j too (issued it, or never needs it)
-          if (ns[1 - t] > j || Tt[1 - t] <= j) tc::mma_commit(&k_empty[j & 1]);
-          progressed = true;
-        }
-        const int q = np[t];
-        if (q < Tt[t] && q < ns[t] && tc::mbar_test(v_full, q & 1) && tc::mbar_test(&p_full[t], q & 1)) {
-          tc::tc_fence_after();
-          const uint8_t* pb = sP + t * L::P_TILE;
-#pragma unroll
-          for (int k = 0; k < BN / 16; ++k) {
-            const uint64_t a = tc::desc_sw128(tc::smem_u32(pb + (k >> 2) * SLAB) + (k & 3) * 32);
-            const uint64_t b = tc::desc_sw128_mn(tc::smem_u32(sV) + k * 16 * 128, SLAB);
-            tc::mma_bf16(tmem + TM_O + t * BN, a, b, idesc_o, (q > 0 || k > 0) ? 1u : 0u);
-          }
-          tc::mma_commit(&pv_done[t]);
-          np[t] = q + 1;
-          if (np[1 - t] > q || Tt[1 - t] <= q) tc::mma_commit(v_empty);
-          progressed = true;
-        }
-      }
-      if (progressed) {
-        idle = 0;
-      } else if (++idle > (1u << 26)) {
-        ok = false;
-      }
-    }
-    if (!ok) atomicOr(&g_err_attn_tc, ERRBIT_TIMEOUT);
-  } else if (warp >= 2) {
-    // ------------------------------------------------------------------ softmax + epilogue
-    const int t = (warp - 2) >> 2;                  // query tile of this warpgroup
-    const int lane_base = (warp & 3) * 32;
-    const int r = lane_base + lane;
-    const int m = m0 + t * BM + r;
-    const int Tq = Tt[t];
-    int qp = 0;
-    if (m < M) {
-      qp = q_pos[m];
-      qp = qp < 0 ? 0 : (qp >= n_kv ? (int)(n_kv - 1) : qp);
-    }
-    const uint32_t trow = tmem + (static_cast<uint32_t>(lane_base) << 16);
-    const uint32_t tS = trow + t * BN;
-    const uint32_t tO = trow + TM_O + t * BN;
-    float m_used = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; ok && j < Tq; ++j) {
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&s_full[t], j & 1))) {
-        ok = false;
-        break;
-      }
-      tc::tc_fence_after();
-      uint32_t sr[BN];
-      tc::tmem_ld64_nowait(tS, sr);
-      tc::tmem_ld64_nowait(tS + 64, sr + 64);
-      tc::tmem_wait_ld();
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&s_free[t]);   // the MMA may write S_t(j+1)
-      const int key0 = j * BN;
-      const bool full_row = key0 + BN - 1 <= qp;
-      float pmx[8];
-#pragma unroll
-      for (int a = 0; a < 8; ++a) pmx[a] = -INFINITY;
-      if (full_row) {
-#pragma unroll
-        for (int i = 0; i < BN; ++i) pmx[i & 7] = fmaxf(pmx[i & 7], __uint_as_float(sr[i]));
-      } else {
-#pragma unroll
-        for (int i = 0; i < BN; ++i)
-          if (key0 + i <= qp) pmx[i & 7] = fmaxf(pmx[i & 7], __uint_as_float(sr[i]));
-      }
-      const float mt = fmaxf(fmaxf(fmaxf(pmx[0], pmx[1]), fmaxf(pmx[2], pmx[3])),
-                             fmaxf(fmaxf(pmx[4], pmx[5]), fmaxf(pmx[6], pmx[7]))) * scale_log2;
-      const float m_new = fmaxf(m_used, mt);
-      if (j >= 1) {
-        // P_t(j-1).V has completed: the P tile is free and O_t is stable
-        if (!__all_sync(0xffffffffu, tc::mbar_wait(&pv_done[t], (j - 1) & 1))) {
-          ok = false;
-          break;
-        }
-        tc::tc_fence_after();
-      }
-      if (j == 0) {
-        m_used = m_new;
-      } else {
-        const bool need = m_new > m_used + kRescaleLog2;
-        if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? tc::ex2_approx(m_used - m_new) : 1.0f;
-#pragma unroll 1
-          for (int c = 0; c < HD / 16; ++c) {
-            float o[16];
-            tc::tmem_ld16(tO + c * 16, o);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] *= alpha;
-            tc::tmem_st16(tO + c * 16, o);
-          }
-          l *= alpha;
-          if (need) m_used = m_new;
-        }
-      }
-      uint8_t* prow = sP + t * L::P_TILE + r * 128;
-      const float mo = m_used;
-      float ls[8];
-#pragma unroll
-      for (int a = 0; a < 8; ++a) ls[a] = 0.f;
-#pragma unroll
-      for (int c = 0; c < BN / 8; ++c) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int k0 = c * 8 + 2 * i;
-          float p0 = tc::ex2_approx(fmaf(__uint_as_float(sr[k0]), scale_log2, -mo));
-          float p1 = tc::ex2_approx(fmaf(__uint_as_float(sr[k0 + 1]), scale_log2, -mo));
-          if (!full_row) {
-            p0 = (key0 + k0 <= qp) ? p0 : 0.f;
-            p1 = (key0 + k0 + 1 <= qp) ? p1 : 0.f;
-          }
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-          const float2 back = __bfloat1622float2(b2);
-          ls[(2 * i) & 7] += back.x;
-          ls[(2 * i + 1) & 7] += back.y;
-          pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
-        }
-        // keys 8c .. 8c+7: 16-byte chunk c % 8 of slab c / 8, swizzled by row % 8
-        uint4* dst = reinterpret_cast<uint4*>(prow + (c >> 3) * SLAB + (((c & 7) ^ (r & 7)) << 4));
-        *dst = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      }
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      tc::tc_fence_before();
-      tc::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&p_full[t]);
-    }
-    if (Tq > 0) {
-      if (ok && __all_sync(0xffffffffu, tc::mbar_wait(&pv_done[t], (Tq - 1) & 1))) {
-        tc::tc_fence_after();
-        const float inv = l > 0.f ? 1.0f / l : 0.f;
-        bf16* orow = out + (int64_t)m * H * HD + (int64_t)h * HD;
-#pragma unroll 1
-        for (int c = 0; c < HD / 16; ++c) {
-          float o[16];
-          tc::tmem_ld16(tO + c * 16, o);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] *= inv;
-          if (m < M) {
-            st8(orow + c * 16, o);
-            st8(orow + c * 16 + 8, o + 8);
-          }
-        }
-      } else if (lane == 0) {
-        atomicOr(&g_err_attn_tc, ERRBIT_TIMEOUT);
-      }
-    }
-  }
-  tc::tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, TMEM_COLS);
-  }
-}
-
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -768,18 +432,6 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int sm_count_attn() {
-  static int cached[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
-  int n = 0;
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  if (n <= 0) n = 148;
-  if (dev >= 0 && dev < 64) cached[dev] = n;
-  return n;
-}
-
 template <int HD>
 cudaError_t launch_hd(const void* q, const int32_t* q_pos, int M, const void* kc, const void* vc, int64_t n_kv,
                       int H, int Hkv, void* out, cudaStream_t s) {
@@ -794,25 +446,12 @@ cudaError_t launch_hd(const void* q, const int32_t* q_pos, int M, const void* kc
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(k_attn_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<HD>::SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_attn_tc2<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout2<HD>::SMEM);
-    if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
-  // Query-tile pairs for a dense causal prefill (every row attends) whose pair grid still
-  // covers every SM.  Selected rows spread over a longer sequence take single tiles: measured
-  // on GB300, 1280 rows x 8192 keys runs 22% faster that way, 3328 x 16384 2%, while a dense
-  // 8192 x 8192 runs 3% faster in pairs.
-  const int pairs = (M + 2 * BM - 1) / (2 * BM);
-  if ((int64_t)M >= n_kv && (int64_t)pairs * H >= sm_count_attn()) {
-    dim3 grid(H, pairs);
-    { const cudaError_t e_ = launch_k(k_attn_tc2<HD>, dim3(grid), dim3(THREADS2), Layout2<HD>::SMEM, s, tq, tk, tv, q_pos, M, n_kv, H, Hkv,
-                                                             static_cast<bf16*>(out), scale_log2); if (e_ != cudaSuccess) return e_; }
-  } else {
-    dim3 grid(H, (M + BM - 1) / BM);
-    { const cudaError_t e_ = launch_k(k_attn_tc<HD>, dim3(grid), dim3(THREADS), Layout<HD>::SMEM, s, tq, tk, tv, q_pos, M, n_kv, H, Hkv,
-                                                          static_cast<bf16*>(out), scale_log2); if (e_ != cudaSuccess) return e_; }
-  }
+  dim3 grid(H, (M + BM - 1) / BM);
+  { const cudaError_t e_ = launch_k(k_attn_tc<HD>, dim3(grid), dim3(THREADS), Layout<HD>::SMEM, s, tq, tk, tv, q_pos, M, n_kv, H, Hkv,
+                                    static_cast<bf16*>(out), scale_log2); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 

@@ -378,11 +378,9 @@ def test_partial_attention_bf16_tensor_cores(B, H, Hkv, hd, M, N, qstd, order):
 
 @pytest.mark.parametrize("H,Hkv,hd,M,N", [(32, 8, 128, 1100, 3000), (40, 40, 64, 1000, 1000),
                                           (32, 32, 128, 4096, 4096), (32, 8, 128, 2200, 2200)])
-def test_partial_attention_query_tile_pairs(B, H, Hkv, hd, M, N):
-    """Dense causal shapes (every row attends) whose (256-query pair x head) grid covers every
-    SM take the two-tile kernel: a last pair whose second tile is partly empty, GQA, full
-    causal.  Selected rows in shuffled order over a longer sequence (1100 of 3000) take the
-    single-tile kernel at the same scale."""
+def test_partial_attention_at_scale(B, H, Hkv, hd, M, N):
+    """Grids of several waves over the SMs: dense causal prefill (every row attends) with GQA
+    and a ragged last query tile, and selected rows in shuffled order over a longer sequence."""
     torch = torch_mod()
     shape = synth.ModelShape(1, 256, H, Hkv, hd, 256, 64, dtype="bf16")
     dims = dims_for(B, shape)

@@ -38,7 +38,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one k_gemm_tc launch of this
 # shape, from an ncu capture of the persistent double-buffered kernel; to be cleared when
 # that kernel changes.
-GEMM_TRAFFIC = {(4096, 11008, 4096, "swiglu"): 219.057152e6 + 78.519552e6}
+GEMM_TRAFFIC = {}
 
 
 def parse_args(argv=None):
@@ -569,6 +569,18 @@ def our_arm(args):
                 "traffic": GEMM_TRAFFIC.get(top_desc), "traffic_unit": "bytes per launch (ncu dram read+write)",
                 "flops_per_launch": top[2], "ms_per_launch": top_ms,
                 "all_gemm_launches_tflops": all_gemm_tflops}
+    # whole-step roofline: every launch at its own bound (its algorithmic bytes at the measured
+    # copy bandwidth, or its FLOPs at the sustained tensor rate, whichever is longer), summed
+    # over one step and set against the measured graph-replayed step
+    hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    floor_s = attn_flops_step / (peak * 1e12)
+    for r in recs:
+        if r["kind"] != "attention":
+            floor_s += max(r["bytes"] / (hbm_peak * 1e9), r["flops"] / (peak * 1e12)) / args.profile_steps
+    step_roofline = {"floor_ms": floor_s * 1e3, "measured_ms": ms, "frac": floor_s * 1e3 / ms,
+                     "model": "sum over the step's launches of max(algorithmic bytes / measured copy GB/s, "
+                              "FLOPs / measured sustained bf16 TFLOP/s); attention FLOPs from the selected rows' "
+                              "positions"}
     hbm_kernels = {}
     # (bf16 takes the deviation inside the K/V GEMM; only its small tile-sum pass remains)
     for name in ("rope_shift", "copy_rows", "lmhead_gemv") + (() if shape.dtype == "bf16" else ("deviation",)):
@@ -727,7 +739,7 @@ def our_arm(args):
         "gpu_launches": int(launches_per_step * args.steps),
         "launches_per_step": int(launches_per_step),
         "step_tflops": flops / (ms / 1e3) / 1e12,
-        "roofline": roofline, "hbm_kernels": hbm_kernels, "kernels": kernels, "gemm_launches": gemm_detail,
+        "roofline": roofline, "step_roofline": step_roofline, "hbm_kernels": hbm_kernels, "kernels": kernels, "gemm_launches": gemm_detail,
         "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "full_prefill": full, "quality_diagnostics": quality,
         "setup_s": setup_s,
     }

@@ -229,13 +229,15 @@ int cb_rmsnorm(void* out, const void* x, const int32_t* rows, int64_t n, int32_t
                float eps, int32_t dtype_in, int32_t dtype_out, void* stream);
 
 /* dst[i] = src[idx[i]] for i < n; rows of row_bytes bytes (a multiple of 4); idx NULL
- * means i ([CB-A] §Selective recomputation, Step 1: restrict the input to S). */
+ * means i ([CB-A] §Selective recomputation, Step 1: restrict the input to S).  dst and src
+ * must not overlap (rows are copied in parallel, in no fixed order). */
 int cb_gather_rows(void* dst, const void* src, const int32_t* idx, int64_t n,
                    int64_t row_bytes, void* stream);
 
 /* KV expansion ([CB-A] §Selective recomputation, Step 3: K_new = Concat(K_pre[not S],
  * K_recomp[S])):  k_cache[dst_idx[i]] = k_rows[src_idx[i]] and the same for V, i < n.
- * src_idx NULL means i.  Rows are [Hkv hd]. */
+ * src_idx NULL means i.  Rows are [Hkv hd].  The caches must not overlap the row
+ * buffers (rows are copied in parallel, in no fixed order). */
 int cb_scatter_kv(void* k_cache, void* v_cache, const void* k_rows, const void* v_rows,
                   const int32_t* dst_idx, const int32_t* src_idx, int64_t n,
                   const cb_dims* dims, void* stream);

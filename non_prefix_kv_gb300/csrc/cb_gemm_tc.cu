@@ -12,6 +12,8 @@
 //                   one half of the accumulator columns, so two warps share each row band.
 #include <cuda.h>
 
+#include <cstdlib>
+
 #include "cb_common.cuh"
 #include "cb_epilogue.cuh"
 #include "cb_internal.h"
@@ -47,6 +49,87 @@ struct TileCfg {
   static constexpr int STAGES = BN == 256 ? 4 : 5;
   static constexpr int SMEM_BYTES = STAGES * (A_BYTES + B_BYTES) + 1024 /*align slack*/ + 256 /*barriers*/;
 };
+
+// Epilogue of one output tile for one epilogue warp: this lane's accumulator row m (TMEM row
+// band at trow), the warp's half of the tile's columns [n0, n0 + BN).
+template <int BN>
+__device__ __forceinline__ void epilogue_tile(const GemmDesc& g, int m, int n0, int half, uint32_t trow,
+                                              int swiglu) {
+  constexpr int CH = BN / 32;              // 16-column chunks per warp
+  if (!swiglu && g.epi.dev_part != nullptr) {
+    // K/V columns with the deviation against the cached row: the cached values of the
+    // chunk DEV_AHEAD further on are loaded while this chunk is processed
+    const EpiParams& p = g.epi;
+    int64_t rr = -1;
+    if (m < g.M) {
+      rr = p.ref_row ? (int64_t)p.ref_row[m] : (int64_t)m;
+      if (rr < 0 || rr >= p.ref_rows) {
+        atomicOr(&g_err_tc, ERRBIT_INDEX);
+        rr = -1;
+      }
+    }
+    auto ref_ptr = [&](int c) -> const uint4* {
+      const int n = n0 + (half * CH + c) * 16;
+      if (rr < 0 || n >= g.N) return nullptr;
+      const int gc = p.col0 + n;
+      if (gc < p.q_cols) return nullptr;
+      const bool is_v = gc >= p.q_cols + p.kv_cols;
+      if (is_v && !p.dev_use_v) return nullptr;
+      return reinterpret_cast<const uint4*>(static_cast<const bf16*>(is_v ? p.v_ref : p.k_ref) + rr * p.ldkv +
+                                            (gc - p.q_cols - (is_v ? p.kv_cols : 0)));
+    };
+    constexpr int DEV_AHEAD = 4;
+    uint4 ring[DEV_AHEAD][2];
+#pragma unroll
+    for (int c = 0; c < DEV_AHEAD; ++c) {
+      const uint4* q = ref_ptr(c);
+      if (q) {
+        ring[c][0] = __ldg(q);
+        ring[c][1] = __ldg(q + 1);
+      }
+    }
+    float dsum = 0.f;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      float v[16];
+      tc::tmem_ld16(trow + (half * CH + c) * 16, v);
+      const int n = n0 + (half * CH + c) * 16;
+      if (m < g.M && n < g.N) {
+        if (!epi_apply<bf16, 16>(p, m, n, v)) atomicOr(&g_err_tc, ERRBIT_INDEX);
+      }
+      if (ref_ptr(c)) dsum += sq_dev16(v, ring[c % DEV_AHEAD]);
+      if (c + DEV_AHEAD < CH) {
+        const uint4* q = ref_ptr(c + DEV_AHEAD);
+        if (q) {
+          ring[c % DEV_AHEAD][0] = __ldg(q);
+          ring[c % DEV_AHEAD][1] = __ldg(q + 1);
+        }
+      }
+    }
+    if (m < g.M) p.dev_part[((int64_t)(n0 / BN) * 2 + half) * p.dev_ld + m] = dsum;
+  } else if (!swiglu) {
+    for (int c = half * CH; c < (half + 1) * CH; ++c) {
+      float v[16];
+      tc::tmem_ld16(trow + c * 16, v);
+      const int n = n0 + c * 16;
+      if (m < g.M && n < g.N) {
+        if (!epi_apply<bf16, 16>(g.epi, m, n, v)) atomicOr(&g_err_tc, ERRBIT_INDEX);
+      }
+    }
+  } else {
+    for (int c = half * (CH / 2); c < (half + 1) * (CH / 2); ++c) {
+      float gt[16], up[16];
+      tc::tmem_ld16(trow + c * 16, gt);
+      tc::tmem_ld16(trow + BN / 2 + c * 16, up);
+      const int j = n0 + c * 16;
+      if (m < g.M && j < g.N) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) gt[q] = silu_f(gt[q]) * up[q];
+        st_vec<bf16, 16>(static_cast<bf16*>(g.epi.out) + (int64_t)m * g.epi.ldo + j, gt);
+      }
+    }
+  }
+}
 
 template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -193,7 +276,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------- epilogue: drains accumulator b while the MMAs fill the other one
     const int lane_base = (warp & 3) * 32;
     const int half = (warp - 2) >> 2;        // which half of the accumulator columns
-    constexpr int CH = BN / 32;              // 16-column chunks per warp
     uint32_t i = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
       const uint32_t b = i & 1;
@@ -208,79 +290,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc::tc_fence_after();
       const uint32_t trow = tmem + b * 256 + (static_cast<uint32_t>(lane_base) << 16);
-      if (!swiglu && g.epi.dev_part != nullptr) {
-        // K/V columns with the deviation against the cached row: the cached values of the
-        // chunk DEV_AHEAD further on are loaded while this chunk is processed
-        const EpiParams& p = g.epi;
-        int64_t rr = -1;
-        if (m < g.M) {
-          rr = p.ref_row ? (int64_t)p.ref_row[m] : (int64_t)m;
-          if (rr < 0 || rr >= p.ref_rows) {
-            atomicOr(&g_err_tc, ERRBIT_INDEX);
-            rr = -1;
-          }
-        }
-        auto ref_ptr = [&](int c) -> const uint4* {
-          const int n = n0 + (half * CH + c) * 16;
-          if (rr < 0 || n >= g.N) return nullptr;
-          const int gc = p.col0 + n;
-          if (gc < p.q_cols) return nullptr;
-          const bool is_v = gc >= p.q_cols + p.kv_cols;
-          if (is_v && !p.dev_use_v) return nullptr;
-          return reinterpret_cast<const uint4*>(static_cast<const bf16*>(is_v ? p.v_ref : p.k_ref) + rr * p.ldkv +
-                                                (gc - p.q_cols - (is_v ? p.kv_cols : 0)));
-        };
-        constexpr int DEV_AHEAD = 4;
-        uint4 ring[DEV_AHEAD][2];
-#pragma unroll
-        for (int c = 0; c < DEV_AHEAD; ++c) {
-          const uint4* q = ref_ptr(c);
-          if (q) {
-            ring[c][0] = __ldg(q);
-            ring[c][1] = __ldg(q + 1);
-          }
-        }
-        float dsum = 0.f;
-#pragma unroll
-        for (int c = 0; c < CH; ++c) {
-          float v[16];
-          tc::tmem_ld16(trow + (half * CH + c) * 16, v);
-          const int n = n0 + (half * CH + c) * 16;
-          if (m < g.M && n < g.N) {
-            if (!epi_apply<bf16, 16>(p, m, n, v)) atomicOr(&g_err_tc, ERRBIT_INDEX);
-          }
-          if (ref_ptr(c)) dsum += sq_dev16(v, ring[c % DEV_AHEAD]);
-          if (c + DEV_AHEAD < CH) {
-            const uint4* q = ref_ptr(c + DEV_AHEAD);
-            if (q) {
-              ring[c % DEV_AHEAD][0] = __ldg(q);
-              ring[c % DEV_AHEAD][1] = __ldg(q + 1);
-            }
-          }
-        }
-        if (m < g.M) p.dev_part[((int64_t)(n0 / BN) * 2 + half) * p.dev_ld + m] = dsum;
-      } else if (!swiglu) {
-        for (int c = half * CH; c < (half + 1) * CH; ++c) {
-          float v[16];
-          tc::tmem_ld16(trow + c * 16, v);
-          const int n = n0 + c * 16;
-          if (m < g.M && n < g.N) {
-            if (!epi_apply<bf16, 16>(g.epi, m, n, v)) atomicOr(&g_err_tc, ERRBIT_INDEX);
-          }
-        }
-      } else {
-        for (int c = half * (CH / 2); c < (half + 1) * (CH / 2); ++c) {
-          float gt[16], up[16];
-          tc::tmem_ld16(trow + c * 16, gt);
-          tc::tmem_ld16(trow + BN / 2 + c * 16, up);
-          const int j = n0 + c * 16;
-          if (m < g.M && j < g.N) {
-#pragma unroll
-            for (int q = 0; q < 16; ++q) gt[q] = silu_f(gt[q]) * up[q];
-            st_vec<bf16, 16>(static_cast<bf16*>(g.epi.out) + (int64_t)m * g.epi.ldo + j, gt);
-          }
-        }
-      }
+      epilogue_tile<BN>(g, m, n0, half, trow, swiglu);
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&acc_empty[b]);
@@ -292,6 +302,194 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ---- two-SM variant: 256 x BN tiles computed by a CTA pair ------------------------------
+// A cluster of two CTAs on two SMs shares each tile: CTA r stages A rows [m0 + 128 r, +128)
+// and half of the B tile (rows n0 + r BN/2; for SwiGLU CTA 0 the gate rows, CTA 1 the up
+// rows) and receives accumulator rows [m0 + 128 r, +128) in its own TMEM; the even CTA issues
+// tcgen05.mma.cta_group::2 on both CTAs' stages.  Each SM thus stages and feeds its tensor
+// core half of B per tile instead of all of it.  Both CTAs' loads complete on the even CTA's
+// "full" barrier; the MMA completions arrive on both CTAs' "empty" and "accumulator full"
+// barriers; both CTAs' epilogue warps release an accumulator on the even CTA's barrier.
+template <int BN>
+struct PairCfg {
+  static_assert(BN == 256 || BN == 224 || BN == 192, "pair tiles are 256, 224 or 192 columns wide");
+  static constexpr int B_BYTES = (BN / 2) * BK * 2;   // this CTA's half of the B tile
+  static constexpr int STAGES = BN == 256 ? 6 : 7;
+  static constexpr int SMEM_BYTES = STAGES * (A_BYTES + B_BYTES) + 1024 /*align slack*/ + 256 /*barriers*/;
+};
+constexpr int PAIR_BM = 2 * BM;
+
+template <int BN>
+__global__ void __launch_bounds__(THREADS, 1)
+    k_gemm_tc_pair(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
+                   const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+                   const GemmDesc g0, const GemmDesc g1, int n_prob, int swiglu) {
+  constexpr int STAGES = PairCfg<BN>::STAGES;
+  constexpr int B_BYTES = PairCfg<BN>::B_BYTES;
+  extern __shared__ uint8_t smem_raw[];
+  // the same 1024-byte aligned layout in both CTAs (the pair MMA addresses both by offset)
+  const uint32_t raw_addr = tc::smem_u32(smem_raw);
+  uint8_t* base = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
+  uint8_t* smA = base;
+  uint8_t* smB = base + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + STAGES * (A_BYTES + B_BYTES));
+  uint64_t* full = bars;                        // [STAGES] both CTAs' TMA -> MMA (even CTA's copy used)
+  uint64_t* empty = bars + STAGES;              // [STAGES] MMA -> this CTA's TMA
+  uint64_t* acc_full = bars + 2 * STAGES;       // [2] MMA -> this CTA's epilogue
+  uint64_t* acc_empty = bars + 2 * STAGES + 2;  // [2] both CTAs' epilogues -> MMA (even CTA's copy used)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = tc::cluster_ctarank();
+  const int pair = (int)tc::cluster_id_x(), n_pairs = (int)tc::n_clusters_x();
+  const int out_cols = swiglu ? BN / 2 : BN;
+  const int num_m0 = (g0.M + PAIR_BM - 1) / PAIR_BM;
+  const int t0 = num_m0 * ((g0.N + out_cols - 1) / out_cols);
+  const int num_m1 = n_prob > 1 ? (g1.M + PAIR_BM - 1) / PAIR_BM : 1;
+  const int total = t0 + (n_prob > 1 ? num_m1 * ((g1.N + out_cols - 1) / out_cols) : 0);
+  const int kb0 = (g0.K + BK - 1) / BK, kb1 = n_prob > 1 ? (g1.K + BK - 1) / BK : kb0;
+  auto locate = [&](int t, int& pr, int& m0, int& n0) {
+    pr = t >= t0;
+    const int u = pr ? t - t0 : t;
+    const int nm = pr ? num_m1 : num_m0;
+    m0 = (u % nm) * PAIR_BM;
+    n0 = (u / nm) * out_cols;
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&acc_full[b], 1);
+      tc::mbar_init(&acc_empty[b], 2 * EPI_WARPS);
+    }
+    tc::fence_mbar_init();
+    tc::tma_prefetch_desc(&tmA0);
+    tc::tma_prefetch_desc(&tmB0);
+    if (n_prob > 1) {
+      tc::tma_prefetch_desc(&tmA1);
+      tc::tma_prefetch_desc(&tmB1);
+    }
+  }
+  if (warp == 1) {
+    tc::tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tc::tmem_relinquish_pair();
+  }
+  tc::tc_fence_before();
+  // both CTAs' barriers are initialised and both TMEM allocations made before either CTA
+  // signals the other
+  tc::cluster_sync();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();
+  pdl_trigger();
+
+  bool ok = true;
+  if (warp == 0 && lane == 0) {
+    // ---------------- producer (both CTAs)
+    uint32_t it = 0;
+    for (int t = pair; ok && t < total; t += n_pairs) {
+      int pr, m0, n0;
+      locate(t, pr, m0, n0);
+      const CUtensorMap* tmA = pr ? &tmA1 : &tmA0;
+      const CUtensorMap* tmB = pr ? &tmB1 : &tmB0;
+      const int KB = pr ? kb1 : kb0;
+      const int brow = swiglu ? (rank ? (int)g0.b_up_row + n0 : n0) : n0 + (int)rank * (BN / 2);
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!tc::mbar_wait(&empty[s], ph ^ 1)) {
+          ok = false;
+          break;
+        }
+        // the even CTA's barrier counts the bytes of both CTAs' loads
+        if (rank == 0) tc::mbar_expect_tx(&full[s], 2 * (A_BYTES + B_BYTES));
+        const uint32_t fb = tc::mapa_shared(tc::smem_u32(&full[s]), 0);
+        tc::tma_load_2d_pair(smA + s * A_BYTES, tmA, fb, kb * BK, m0 + (int)rank * BM);
+        tc::tma_load_2d_pair(smB + s * B_BYTES, tmB, fb, kb * BK, brow);
+      }
+    }
+    // wait until the MMAs have released every stage, so that no completion is still on its
+    // way to this CTA's barriers when it exits
+    for (uint32_t j = 0; ok && j < (uint32_t)STAGES; ++j, ++it)
+      ok = tc::mbar_wait(&empty[it % STAGES], ((it / STAGES) & 1) ^ 1);
+    if (!ok) atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
+  } else if (warp == 1 && rank == 0) {
+    // ---------------- pair MMA issuer (even CTA; the elected lane issues)
+    constexpr uint32_t idesc = tc::idesc_bf16_f32(PAIR_BM, BN);
+    const uint64_t a_desc0 = tc::desc_sw128(tc::smem_u32(smA));
+    const uint64_t b_desc0 = tc::desc_sw128(tc::smem_u32(smB));
+    uint32_t it = 0, i = 0;
+    for (int t = pair; ok && t < total; t += n_pairs, ++i) {
+      const uint32_t b = i & 1;
+      const int KB = t >= t0 ? kb1 : kb0;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&acc_empty[b], ((i >> 1) & 1) ^ 1))) {
+        ok = false;
+        break;
+      }
+      tc::tc_fence_after();
+      const uint32_t d_tmem = tmem + b * 256;
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(&full[s], ph))) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        if (tc::elect_one()) {
+          const uint64_t a_desc = a_desc0 + (uint64_t)((s * A_BYTES) >> 4);
+          const uint64_t b_desc = b_desc0 + (uint64_t)((s * B_BYTES) >> 4);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc::mma_bf16_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, (kb | k) != 0);
+          tc::mma_commit_pair(&empty[s], 0x3);
+        }
+        __syncwarp();
+      }
+      if (ok) {
+        if (tc::elect_one()) tc::mma_commit_pair(&acc_full[b], 0x3);
+        __syncwarp();
+      }
+    }
+    if (!ok && lane == 0) atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
+  } else if (warp >= 2) {
+    // ---------------- epilogue (both CTAs): this CTA's 128 rows of each tile
+    const int lane_base = (warp & 3) * 32;
+    const int half = (warp - 2) >> 2;
+    const uint32_t release0 = tc::mapa_shared(tc::smem_u32(&acc_empty[0]), 0);
+    const uint32_t release1 = tc::mapa_shared(tc::smem_u32(&acc_empty[1]), 0);
+    uint32_t i = 0;
+    for (int t = pair; t < total; t += n_pairs, ++i) {
+      const uint32_t b = i & 1;
+      int pr, m0, n0;
+      locate(t, pr, m0, n0);
+      const GemmDesc& g = pr ? g1 : g0;
+      const int m = m0 + (int)rank * BM + lane_base + lane;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&acc_full[b], (i >> 1) & 1))) {
+        if (lane == 0) atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
+        break;
+      }
+      tc::tc_fence_after();
+      const uint32_t trow = tmem + b * 256 + (static_cast<uint32_t>(lane_base) << 16);
+      epilogue_tile<BN>(g, m, n0, half, trow, swiglu);
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_cluster(b ? release1 : release0);
+    }
+  }
+  __syncwarp();
+  tc::tc_fence_before();
+  // neither CTA frees its TMEM (or exits) before the pair's last MMA and epilogue are done
+  tc::cluster_sync();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc_pair(tmem, TMEM_COLS);
   }
 }
 
@@ -423,6 +621,136 @@ cudaError_t launch_tiles(const GemmDesc* gs, int n, bool swiglu, int n_sm, cudaS
   return cudaGetLastError();
 }
 
+int pair_tiles_for(const GemmDesc* gs, int n, int out_cols) {
+  int tiles = 0;
+  for (int p = 0; p < n; ++p)
+    tiles += ((gs[p].N + out_cols - 1) / out_cols) * ((gs[p].M + PAIR_BM - 1) / PAIR_BM);
+  return tiles;
+}
+
+template <int BN>
+cudaError_t pair_attr() {
+  return cudaFuncSetAttribute(k_gemm_tc_pair<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              PairCfg<BN>::SMEM_BYTES);
+}
+
+cudaLaunchConfig_t pair_config(cudaLaunchAttribute* attr, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(THREADS);
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cfg;
+}
+
+// Co-resident CTA pairs on this device (one CTA per SM), once per device; 0 if pair launches
+// are unavailable.  Also sets the pair kernels' shared-memory limits.
+int pair_slots() {
+  static int slots[64];
+  static bool done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && done[dev]) return slots[dev];
+  int mp = 0;
+  if (pair_attr<256>() == cudaSuccess && pair_attr<224>() == cudaSuccess && pair_attr<192>() == cudaSuccess) {
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = pair_config(attr, 0);
+    cfg.dynamicSmemBytes = PairCfg<256>::SMEM_BYTES;
+    cfg.gridDim = dim3(2 * (sm_count() / 2));
+    if (cudaOccupancyMaxActiveClusters(&mp, k_gemm_tc_pair<256>, &cfg) != cudaSuccess) mp = 0;
+  }
+  cudaGetLastError();
+  if (dev >= 0 && dev < 64) {
+    slots[dev] = mp;
+    done[dev] = true;
+  }
+  return mp;
+}
+
+template <int BN>
+cudaError_t launch_pair(const GemmDesc* gs, int n, bool swiglu, int n_pairs, cudaStream_t s) {
+  CUtensorMap tmA[2], tmB[2];
+  for (int p = 0; p < n; ++p) {
+    const GemmDesc& g = gs[p];
+    if (!make_map(&tmA[p], g.A, g.M, g.K, g.lda, BM)) return cudaErrorInvalidValue;
+    const int64_t b_rows = swiglu ? g.b_up_row + g.N : g.N;
+    if (!make_map(&tmB[p], g.B, b_rows, g.K, g.ldb, BN / 2)) return cudaErrorInvalidValue;
+  }
+  if (n == 1) {
+    tmA[1] = tmA[0];
+    tmB[1] = tmB[0];
+  }
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = pair_config(attr, s);
+  cfg.dynamicSmemBytes = PairCfg<BN>::SMEM_BYTES;
+  const int tiles = pair_tiles_for(gs, n, swiglu ? BN / 2 : BN);
+  cfg.gridDim = dim3(2 * (tiles < n_pairs ? tiles : n_pairs));
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc_pair<BN>, tmA[0], tmB[0], tmA[1], tmB[1], gs[0],
+                                           n > 1 ? gs[1] : gs[0], n, swiglu ? 1 : 0);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// CB_GEMM_PAIR=0 forces single-SM tiles, =1 pair tiles wherever a pair launch is possible
+// (for measurement); unset, plan_tiles decides.
+int pair_mode() {
+  static int mode = -2;
+  if (mode == -2) {
+    const char* v = getenv("CB_GEMM_PAIR");
+    mode = (v && v[0] == '0') ? 0 : (v && v[0] == '1') ? 1 : -1;
+  }
+  return mode;
+}
+
+struct TilePlan {
+  bool pair;
+  int bn;
+};
+
+// Kernel and tile width of one launch.  A launch takes about (waves of tiles over the
+// co-resident CTAs, or pairs) x BN per SM.  A pair tile does the same per-SM work as a
+// single-SM tile of its width in about 1/1.12 of the time (measured at equal wave counts:
+// 4096 x 8192 x 4096 and 8192^3 ran 13-15% faster as pairs), but pads M to 256 rows: pairs
+// are taken only with at least two waves and at most 2% more padded rows than single tiles
+// (832 rows pad to 1024 as pairs), and there where their cost is lower.  SwiGLU and the
+// fused deviation keep 256 columns either way.
+TilePlan plan_tiles(const GemmDesc* gs, int n, int n_sm, int n_pairs) {
+  TilePlan tp{false, pick_tile_n(gs, n, n_sm)};
+  const int mode = pair_mode();
+  if (mode == 0 || n_pairs < 1) return tp;
+  bool fixed = gs[0].epi.kind == EPI_SWIGLU;
+  for (int p = 0; p < n; ++p) fixed = fixed || gs[p].epi.dev_part != nullptr;
+  const int cand[3] = {256, 224, 192};
+  int pbn = 256;
+  int64_t pcost = 0, pwaves = 0;
+  for (int c = 0; c < (fixed ? 1 : 3); ++c) {
+    const int out = gs[0].epi.kind == EPI_SWIGLU ? cand[c] / 2 : cand[c];
+    const int64_t waves = (pair_tiles_for(gs, n, out) + n_pairs - 1) / n_pairs;
+    const int64_t cost = waves * cand[c];
+    if (c == 0 || (cost * 20 <= pcost * 19 && cost < pcost)) {
+      pbn = cand[c];
+      pcost = cost;
+      pwaves = waves;
+    }
+  }
+  if (mode == 1) return TilePlan{true, pbn};
+  int64_t rows_single = 0, rows_pair = 0;
+  for (int p = 0; p < n; ++p) {
+    rows_single += (int64_t)((gs[p].M + BM - 1) / BM) * BM;
+    rows_pair += (int64_t)((gs[p].M + PAIR_BM - 1) / PAIR_BM) * PAIR_BM;
+  }
+  const int out_s = gs[0].epi.kind == EPI_SWIGLU ? tp.bn / 2 : tp.bn;
+  const int64_t scost = (int64_t)((tiles_for(gs, n, out_s) + n_sm - 1) / n_sm) * tp.bn;
+  if (pwaves >= 2 && rows_pair * 100 <= rows_single * 102 && pcost * 100 < scost * 112) return TilePlan{true, pbn};
+  return tp;
+}
+
 }  // namespace
 
 // Host preconditions (checked by the caller's validation, re-checked here): K % 8 == 0,
@@ -437,7 +765,19 @@ cudaError_t launch_gemm_tc_group(const GemmDesc* gs, int n, cudaStream_t s) {
       return cudaErrorInvalidValue;
   }
   const int n_sm = sm_count();
-  switch (pick_tile_n(gs, n, n_sm)) {
+  const int n_pairs = pair_slots();
+  const TilePlan tp = plan_tiles(gs, n, n_sm, n_pairs);
+  if (tp.pair) {
+    switch (tp.bn) {
+      case 224:
+        return launch_pair<224>(gs, n, swiglu, n_pairs, s);
+      case 192:
+        return launch_pair<192>(gs, n, swiglu, n_pairs, s);
+      default:
+        return launch_pair<256>(gs, n, swiglu, n_pairs, s);
+    }
+  }
+  switch (tp.bn) {
     case 224:
       return launch_tiles<224>(gs, n, swiglu, n_sm, s);
     case 192:

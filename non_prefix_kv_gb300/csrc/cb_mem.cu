@@ -309,7 +309,9 @@ cudaError_t launch_rope_shift_q8(int dt, void* kd, void* vd, const uint8_t* kq, 
 
 // ------------------------------------------------------------------------ row copies
 // dst[dst_idx[r]] = src[src_idx[r]] for rows of rv vector words.  Index checks against the
-// known buffer heights (bound < 0: unknown) record ERRBIT_INDEX and skip the row.
+// known buffer heights (bound < 0: unknown) record ERRBIT_INDEX and skip the row.  Each
+// thread loads U words (a grid stride apart) before it stores any, so every SM keeps
+// enough bytes in flight to stream from HBM.
 template <typename V>
 __global__ void __launch_bounds__(256) k_copy_rows(V* __restrict__ dst, const int32_t* __restrict__ di,
                                                    const V* __restrict__ src,
@@ -317,17 +319,30 @@ __global__ void __launch_bounds__(256) k_copy_rows(V* __restrict__ dst, const in
                                                    int64_t rv, int64_t dbound, int64_t sbound) {
   pdl_wait();
   pdl_trigger();
+  constexpr int U = 4;
   const int64_t total = n * rv;
-  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
-       t += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = t / rv, c = t - r * rv;
-    const int64_t d = di ? (int64_t)di[r] : r;
-    const int64_t sr = si ? (int64_t)si[r] : r;
-    if (d < 0 || sr < 0 || (dbound >= 0 && d >= dbound) || (sbound >= 0 && sr >= sbound)) {
-      atomicOr(&g_err_mem, ERRBIT_INDEX);
-      continue;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t0 < total; t0 += U * stride) {
+    V val[U];
+    int64_t at[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      at[k] = -1;
+      const int64_t t = t0 + k * stride;
+      if (t >= total) continue;
+      const int64_t r = t / rv, c = t - r * rv;
+      const int64_t d = di ? (int64_t)di[r] : r;
+      const int64_t sr = si ? (int64_t)si[r] : r;
+      if (d < 0 || sr < 0 || (dbound >= 0 && d >= dbound) || (sbound >= 0 && sr >= sbound)) {
+        atomicOr(&g_err_mem, ERRBIT_INDEX);
+        continue;
+      }
+      val[k] = src[sr * rv + c];
+      at[k] = d * rv + c;
     }
-    dst[d * rv + c] = src[sr * rv + c];
+#pragma unroll
+    for (int k = 0; k < U; ++k)
+      if (at[k] >= 0) dst[at[k]] = val[k];
   }
 }
 
@@ -1041,15 +1056,18 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
 // also leaves the best (logit, lowest index) key of its rows in block_best[blockIdx.x].
 template <typename T>
 __global__ void __launch_bounds__(256) k_lm_gemv(float* __restrict__ logits, const float* __restrict__ hn,
-                                                 const T* __restrict__ w, int V, int d,
+                                                 const T* __restrict__ w, int V, int d, int rows_per_warp,
                                                  unsigned long long* __restrict__ block_best) {
   pdl_wait();
   pdl_trigger();
   __shared__ unsigned long long red[8];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int warps_total = (gridDim.x * blockDim.x) >> 5;
+  // each warp owns rows_per_warp consecutive rows; the grid is sized so that every warp is
+  // resident at once and all of them finish together (no partial last round of rows)
+  const int r0 = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * rows_per_warp;
+  const int r1 = min(V, r0 + rows_per_warp);
   unsigned long long best = 0ull;
-  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < V; r += warps_total) {
+  for (int r = r0; r < r1; ++r) {
     const T* wr = w + (int64_t)r * d;
     float acc0 = 0.f, acc1 = 0.f;
     int c = lane * 8;
@@ -1089,17 +1107,27 @@ __global__ void __launch_bounds__(256) k_lm_gemv(float* __restrict__ logits, con
   }
 }
 
-static unsigned lm_grid(int V) { return grid_for((int64_t)V * 32, 256); }
+// rows per warp: the fewest that cover the vocabulary with the warps of 8 resident 256-thread
+// blocks per SM; the grid then holds just enough warps for that
+static int lm_rows_per_warp(int V) {
+  const int64_t warps = (int64_t)sm_count() * 8 * 8;
+  return (int)std::max<int64_t>(1, (V + warps - 1) / warps);
+}
+static unsigned lm_grid(int V) {
+  const int64_t warps = (V + lm_rows_per_warp(V) - 1) / lm_rows_per_warp(V);
+  return (unsigned)std::max<int64_t>(1, (warps + 7) / 8);
+}
 
 size_t lm_block_best_count(int V) { return lm_grid(V); }
 
 cudaError_t launch_lm_gemv(int dt, float* logits, const float* hn, const void* w, int V, int d,
                            unsigned long long* block_best, cudaStream_t s) {
   const unsigned grid = lm_grid(V);
+  const int rpw = lm_rows_per_warp(V);
   if (dt == DT_BF16)
-    { const cudaError_t e_ = launch_k(k_lm_gemv<bf16>, dim3(grid), dim3(256), 0, s, logits, hn, (const bf16*)w, V, d, block_best); if (e_ != cudaSuccess) return e_; }
+    { const cudaError_t e_ = launch_k(k_lm_gemv<bf16>, dim3(grid), dim3(256), 0, s, logits, hn, (const bf16*)w, V, d, rpw, block_best); if (e_ != cudaSuccess) return e_; }
   else
-    { const cudaError_t e_ = launch_k(k_lm_gemv<float>, dim3(grid), dim3(256), 0, s, logits, hn, (const float*)w, V, d, block_best); if (e_ != cudaSuccess) return e_; }
+    { const cudaError_t e_ = launch_k(k_lm_gemv<float>, dim3(grid), dim3(256), 0, s, logits, hn, (const float*)w, V, d, rpw, block_best); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 

@@ -8,6 +8,9 @@ kernel command that ncu captures are taken on.
   python -m non_prefix_kv_gb300.microbench deviation --cand 3840 --width 4096 --k 576
   python -m non_prefix_kv_gb300.microbench rope_shift_q8 --rows 3840 --width 4096
   python -m non_prefix_kv_gb300.microbench check_layer --rows 4096 --k 576
+  python -m non_prefix_kv_gb300.microbench rmsnorm --rows 4096 --width 4096
+  python -m non_prefix_kv_gb300.microbench gather --rows 4096 --width 4096 --n 32000
+  python -m non_prefix_kv_gb300.microbench lmhead --width 4096 --n 32000
 """
 from __future__ import annotations
 
@@ -40,7 +43,7 @@ def _time(fn, iters: int, warmup: int):
 def run(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("what", choices=["gemm", "attention", "rope_shift", "rope_shift_q8", "deviation", "check_layer",
-                                    "rmsnorm"])
+                                    "rmsnorm", "gather", "lmhead"])
     p.add_argument("--m", type=int, default=4096)
     p.add_argument("--n", type=int, default=8192)
     p.add_argument("--k", type=int, default=4096)
@@ -144,6 +147,26 @@ def run(argv=None):
                    a.warmup)
         by = 4.0 * a.rows * a.width
         out.update(ms=ms, gbs=by / (ms / 1e3) / 1e9, rows=a.rows, width=a.width)
+    elif a.what == "gather":
+        # embedding gather: rows of a [n, width] table at uniform random token ids
+        table = torch.randn(a.n, a.width, device="cuda", generator=g).to(bf)
+        ids = torch.randint(0, a.n, (a.rows,), device="cuda", generator=g, dtype=torch.int32)
+        y = torch.empty(a.rows, a.width, device="cuda", dtype=bf)
+        ms = _time(lambda: B.cb_gather_rows(y, table, ids, a.rows, a.width * 2), a.iters, a.warmup)
+        by = 4.0 * a.rows * a.width
+        out.update(ms=ms, gbs=by / (ms / 1e3) / 1e9, rows=a.rows, width=a.width, table_rows=a.n)
+    elif a.what == "lmhead":
+        # final RMSNorm of one row, [n, width] lm_head GEMV and argmax
+        shape = ModelShape(1, a.width, a.width // 128, a.width // 128, 128, 256, a.n, dtype="bf16")
+        dims = E.make_dims(shape)
+        h = torch.randn(a.width, device="cuda", generator=g).to(bf)
+        fn = torch.ones(a.width, device="cuda", dtype=bf)
+        w = (torch.randn(a.n, a.width, device="cuda", generator=g) * 0.02).to(bf)
+        tok = torch.empty(1, dtype=torch.int32, device="cuda")
+        ws = torch.empty(1 << 22, dtype=torch.uint8, device="cuda")
+        ms = _time(lambda: B.cb_lmhead_argmax(h, fn, w, dims, None, tok, ws), a.iters, a.warmup)
+        by = 2.0 * a.n * a.width
+        out.update(ms=ms, gbs=by / (ms / 1e3) / 1e9, vocab=a.n, width=a.width)
     elif a.what == "check_layer":
         # the check layer at the 7B shape: K/V GEMM over every row with the deviation in its
         # epilogue, top-k, KV expansion, Q of the selection, attention, O-proj + FFN

@@ -35,10 +35,10 @@ from non_prefix_kv_gb300 import synth  # noqa: E402
 
 METRIC = "blended-prefill tokens/s & TTFT ms, 7B-shape 4K ctx, 15% recompute, 1 GB300"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one k_gemm_tc launch of this
-# shape, from an ncu capture of the persistent double-buffered kernel; to be cleared when
-# that kernel changes.
-GEMM_TRAFFIC = {}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of this shape, from
+# an ncu capture of the CTA-pair tcgen05 GEMM (k_gemm_tc_pair); to be cleared when that
+# kernel changes.
+GEMM_TRAFFIC = {(4096, 11008, 4096, "swiglu"): 244.447232e6 + 79.988992e6}
 
 
 def parse_args(argv=None):
@@ -563,7 +563,7 @@ def our_arm(args):
         else peaks.get("bf16_tflops_sustained", 1700.0) / 16.0
     top_desc = (top_key[0], top_key[1], top_key[2], epi_names.get(top_key[3], top_key[3]))
     roofline = {"bound": "tensor",
-                "kernel": "k_gemm_tc M=%d N=%d K=%d epilogue=%s (largest launch of the step)" % top_desc,
+                "kernel": "tcgen05 GEMM M=%d N=%d K=%d epilogue=%s (largest launch of the step; CTA-pair kernel k_gemm_tc_pair at this shape)" % top_desc,
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
                 "traffic": GEMM_TRAFFIC.get(top_desc), "traffic_unit": "bytes per launch (ncu dram read+write)",

@@ -315,6 +315,13 @@ typedef struct {
    * layer the two agree up to rounding (its input is the context-free embedding, R5), so a
    * caller that loads chunk KV over a slow link can skip that layer's load entirely. */
   int32_t recompute_kv;
+  /* PRECHECK only, without forced_mask and recompute_kv: 0 = off; r in [1, n_cached] =
+   * compute K/V for rows [r, n_tok) (the cached rows from r on and the uncached suffix) and
+   * read the cache only for rows [0, r), so that a caller loading chunk KV over a slow link
+   * loads only the first r rows of this layer while the GEMMs run (the split that balances
+   * the two is the load controller's choice at this layer, [CB-A] §Pipelining and load
+   * controller).  kv_ready then marks rows [0, r) only. */
+  int32_t recompute_from;
 } cb_layer_opts;
 
 int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode,

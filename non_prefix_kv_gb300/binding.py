@@ -27,7 +27,7 @@ class CBError(RuntimeError):
 
 class cb_layer_opts(C.Structure):
     _fields_ = [("forced_mask", C.c_void_p), ("n_forced", C.c_int32), ("kv_ready", C.c_void_p),
-                ("recompute_kv", C.c_int32)]
+                ("recompute_kv", C.c_int32), ("recompute_from", C.c_int32)]
 
 
 class cb_dims(C.Structure):
@@ -230,16 +230,17 @@ def cb_o_proj_ffn(attn, x_res, M: int, dims: cb_dims, w: cb_layer_w, x_out, ws, 
 def cb_blend_layer(dims: cb_dims, w: cb_layer_w, mode: int, x_in, s_in, m_in: int, n_tok: int, n_cached: int,
                    k_cache, v_cache, cos_sin, max_pos: int, k_budget: int, dev_mode: int, sel_override,
                    x_out, s_out, scores_out, ws, stream=None, kv_ready=None, forced_mask=None,
-                   n_forced: int = 0, recompute_kv: bool = False) -> int:
+                   n_forced: int = 0, recompute_kv: bool = False, recompute_from: int = 0) -> int:
     """kv_ready: a torch.cuda.Event (or raw cudaEvent_t) the layer waits for just before it
     first touches the cached rows, or None.  forced_mask/n_forced: uncached rows anywhere
-    (a uint8 device tensor over the tokens, marking the last row too), or None."""
+    (a uint8 device tensor over the tokens, marking the last row too), or None.
+    recompute_from: PRECHECK only, recompute K/V from this row on (0: off)."""
     m_out = _I32(0)
     opts = None
-    if kv_ready is not None or forced_mask is not None or recompute_kv:
+    if kv_ready is not None or forced_mask is not None or recompute_kv or recompute_from:
         ev = kv_ready if (kv_ready is None or isinstance(kv_ready, int)) else kv_ready.cuda_event
         opts = C.byref(cb_layer_opts(_ptr(forced_mask), n_forced if forced_mask is not None else 0, ev,
-                                     1 if recompute_kv else 0))
+                                     1 if recompute_kv else 0, int(recompute_from)))
     _check("cb_blend_layer", lib().cb_blend_layer(
         C.byref(dims), C.byref(w), mode, _ptr(x_in), _ptr(s_in), m_in, n_tok, n_cached, _ptr(k_cache),
         _ptr(v_cache), _ptr(cos_sin), max_pos, k_budget, dev_mode, _ptr(sel_override), _ptr(x_out),

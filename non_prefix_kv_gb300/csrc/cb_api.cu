@@ -679,6 +679,12 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
   void* kv_ready = opts ? opts->kv_ready : nullptr;
   if (fmask && (opts->n_forced < 1 || opts->n_forced > N))
     return fail(CB_ERR_SHAPE, "n_forced %d outside [1, n_tok]", opts ? opts->n_forced : 0);
+  if (opts && opts->recompute_from != 0) {
+    if (mode != CB_LAYER_PRECHECK || fmask || opts->recompute_kv)
+      return fail(CB_ERR_INVALID_ARG, "recompute_from applies to PRECHECK without forced_mask or recompute_kv");
+    if (opts->recompute_from < 0 || opts->recompute_from > n_cached)
+      return fail(CB_ERR_SHAPE, "recompute_from %d outside [0, n_cached]", opts->recompute_from);
+  }
   // default layout: forced rows [f0, N) (the uncached suffix and the last row)
   const int f0 = (int)std::min<int64_t>(n_cached, n_tok - 1);
   const int n_forced = fmask ? opts->n_forced : N - f0;
@@ -705,17 +711,19 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         L_ATTN(dims->dtype, L.q, s_out, N, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
         return o_ffn(dims, w, L.attn, x_in, N, x_out, L, s);
       }
-      // Q of every row and K/V of the uncached rows: independent, so one shared launch
+      // Q of every row and K/V of the uncached rows (and of the cached rows from
+      // recompute_from on): independent, so one shared launch
       const GemmDesc gq = qkv_desc(dims, w, L.a, N, 0, qc, L.q, nullptr, nullptr, s_out, nullptr, cos_sin, max_pos);
+      const int kv0 = (opts && opts->recompute_from > 0) ? opts->recompute_from : (int)n_cached;
       if (fmask) {
         // K/V of the forced rows, wherever they are: gather their normalised rows first
         L_SPLIT(nullptr, N, fmask, N, n_forced, L.cpos, L.crows, L.fpos, L.frows, s);
         L_COPY(L.ag, nullptr, L.a, L.frows, n_forced, (int64_t)dims->d_model * B, n_forced, N, s);
         L_GEMM2(dims->dtype, gq, qkv_desc(dims, w, L.ag, n_forced, qc, 2 * W, nullptr, k_cache, v_cache, L.frows, L.frows, cos_sin, max_pos), s);
-      } else if (N > n_cached) {
-        const int nu = N - (int)n_cached;
-        const void* a_u = static_cast<const char*>(L.a) + (size_t)n_cached * dims->d_model * B;
-        L_GEMM2(dims->dtype, gq, qkv_desc(dims, w, a_u, nu, qc, 2 * W, nullptr, k_cache, v_cache, s_out + n_cached, s_out + n_cached, cos_sin, max_pos), s);
+      } else if (N > kv0) {
+        const int nu = N - kv0;
+        const void* a_u = static_cast<const char*>(L.a) + (size_t)kv0 * dims->d_model * B;
+        L_GEMM2(dims->dtype, gq, qkv_desc(dims, w, a_u, nu, qc, 2 * W, nullptr, k_cache, v_cache, s_out + kv0, s_out + kv0, cos_sin, max_pos), s);
       } else {
         L_GEMM(dims->dtype, gq, s);
       }

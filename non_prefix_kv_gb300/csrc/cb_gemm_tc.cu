@@ -645,7 +645,7 @@ cudaLaunchConfig_t pair_config(cudaLaunchAttribute* attr, cudaStream_t s) {
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
   return cfg;
 }
 

@@ -217,6 +217,7 @@ class Request:
         forced[self.N - 1] = True
         self.n_forced = int(forced.sum())
         self.forced_mask = torch.from_numpy(forced.astype(np.uint8)).to(dev) if general else None
+        self.src_host = np.asarray(src, np.int64)
         self.src_row = torch.tensor(src, dtype=torch.int32, device=dev)
         self.delta = torch.tensor(delta, dtype=torch.int32, device=dev)
         self.qrow = torch.tensor(qrow, dtype=torch.int32, device=dev)
@@ -235,6 +236,15 @@ class Request:
     start_rows = None      # device int32 rows entering the first layer (None: every row)
     start_tokens = None
 
+    def pool_ranges(self, n_rows: int):
+        """Pool rows feeding the request's first n_rows cached slots, as (first row, rows)
+        ranges of consecutive pool rows."""
+        src = self.src_host[:n_rows]
+        if len(src) == 0:
+            return []
+        cut = np.nonzero(np.diff(src) != 1)[0] + 1
+        return [(int(a[0]), int(len(a))) for a in np.split(src, cut)]
+
     def plan(self, ratios: Sequence[Optional[float]], check_layer: int = 1, gradual: bool = False):
         return layer_plan(self.eng.dm.shape, self.N, self.n_cached, ratios, check_layer, gradual,
                           n_forced=self.n_forced)
@@ -249,6 +259,25 @@ class Request:
         self.start_rows = torch.from_numpy(rows).to(self.tokens.device)
         self.start_tokens = torch.from_numpy(self.tokens_host[first:].copy()).to(self.tokens.device)
         return [(B.CB_LAYER_STEADY, 0)] * self.eng.dm.shape.n_layers
+
+
+def precheck_split_rows(shape: ModelShape, n_tok: int, n_cached: int, link_gbs: float, gemm_tflops: float,
+                        hbm_gbs: float) -> int:
+    """How many cached rows of the pre-check layer to load (the rest have their K/V
+    recomputed): the load controller's balance ([CB-A] §Pipelining and load controller)
+    applied at that layer, where recomputing is exact up to rounding (R5).  Loading X rows
+    over the host link and re-positioning them should take as long as the work queued ahead
+    of the layer's attention: RMSNorm and Q for every row, K/V for the other N - X rows.
+    Both sides are linear in X; the result is where they meet, rounded down to 64 rows."""
+    s = shape
+    esz = 2 if s.dtype == "bf16" else 4
+    N, d, qc, W = n_tok, s.d_model, s.q_width, s.kv_width
+    R, L, H = gemm_tflops * 1e12, link_gbs * 1e9, hbm_gbs * 1e9
+    t_q = 2.0 * N * d * qc / R + 2.0 * N * d * esz / H
+    c = 2.0 * d * 2 * W / R
+    l = 2.0 * W * esz / L + 4.0 * W * esz / H
+    x = int((t_q + N * c) / (c + l)) // 64 * 64
+    return max(1, min(n_cached, x))
 
 
 def layer_plan(shape: ModelShape, n_tok: int, n_cached: int, ratios: Sequence[Optional[float]],
@@ -296,19 +325,39 @@ class HostPool:
             ev.record(self.side)
         self.nbytes = sum(t.numel() * t.element_size() for ts in self.host for t in ts)
 
-    def prefetch_all(self, stream, after_copy=None, skip=()):
-        """Queue every layer's copy (but those in skip) on the side stream once `stream`'s
-        prior work is done; after_copy(l, side_stream) enqueues more work on the landed
-        layer (the re-positioning) before the layer's event is recorded."""
-        self.side.wait_stream(stream)
-        for l, (hs, ds) in enumerate(zip(self.host, self.dev)):
-            if l in skip:
-                continue
-            for h, d in zip(hs, ds):
+    def copy_layer(self, l: int, ranges=None):
+        """Queue layer l's copy on the side stream: the whole layer, or only the given
+        (first pool row, rows) ranges of its K and V (bf16/fp32 pools)."""
+        if ranges is not None and not isinstance(self.pool, ChunkPool):
+            raise ValueError("partial layer loads need a bf16/fp32 chunk pool")
+        for h, d in zip(self.host[l], self.dev[l]):
+            if ranges is None:
                 B.cb_prefetch_layer(d, h, h.numel() * h.element_size(), self.side, self.done[l])
-            if after_copy is not None:
-                after_copy(l, self.side)
-                self.done[l].record(self.side)
+            else:
+                rb = h.shape[1] * h.element_size()
+                for r0, n in ranges:
+                    B.cb_prefetch_layer(d[r0:r0 + n], h[r0:r0 + n], n * rb, self.side, self.done[l])
+
+    def begin(self, stream):
+        """Loads queued from here on start once `stream`'s prior work is done."""
+        self.side.wait_stream(stream)
+
+    def load_layer(self, l: int, after_copy=None, ranges=None):
+        """Queue layer l's copy (only the given row ranges, if any); after_copy(l,
+        side_stream) enqueues more work on the landed layer (the re-positioning) before the
+        layer's event is recorded."""
+        self.copy_layer(l, ranges)
+        if after_copy is not None:
+            after_copy(l, self.side)
+            self.done[l].record(self.side)
+
+    def prefetch_all(self, stream, after_copy=None, skip=(), partial=None):
+        """Queue every layer's copy (but those in skip; only some rows of the layers in
+        partial: {layer: ranges}) on the side stream once `stream`'s prior work is done."""
+        self.begin(stream)
+        for l in range(len(self.host)):
+            if l not in skip:
+                self.load_layer(l, after_copy, (partial or {}).get(l))
 
 
 class FileStore:
@@ -345,9 +394,10 @@ class RequestGraph:
     the request's row maps (src_row, delta) in place first."""
 
     def __init__(self, req: Request, plan, host_pool: Optional[HostPool] = None, stream=None,
-                 recompute_precheck_kv: bool = False):
+                 recompute_precheck_kv: bool = False, precheck_load_rows: Optional[int] = None):
         self.req, self.plan, self.host_pool = req, plan, host_pool
         self.recompute = recompute_precheck_kv
+        self.split = precheck_load_rows
         self.stream = stream if stream is not None else torch.cuda.Stream()
         self.host_tokens = torch.from_numpy(req.tokens_host.copy()).pin_memory()
         self.out = torch.empty(1, dtype=torch.int32).pin_memory()
@@ -363,7 +413,7 @@ class RequestGraph:
         with torch.cuda.stream(self.stream):
             B.cb_copy_async(self.req.tokens, self.host_tokens, self.req.N * 4, self.stream)
             run_blend(self.req, self.plan, host_pool=self.host_pool, stream=self.stream,
-                      recompute_precheck_kv=self.recompute)
+                      recompute_precheck_kv=self.recompute, precheck_load_rows=self.split)
             B.cb_copy_async(self.out, self.req.token, 4, self.stream)
 
     def run(self, tokens=None) -> int:
@@ -377,7 +427,8 @@ class RequestGraph:
 
 def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None, keep_history=False,
               assemble: bool = True, stream=None, host_pool: Optional[HostPool] = None,
-              file_store: Optional[FileStore] = None, recompute_precheck_kv: bool = False):
+              file_store: Optional[FileStore] = None, recompute_precheck_kv: bool = False,
+              precheck_load_rows: Optional[int] = None):
     """One blended prefill: re-position the chunk KV of every layer, run the layer plan,
     then the lm_head argmax.  Returns the number of rows carried out of the last layer.
 
@@ -393,7 +444,12 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
 
     recompute_precheck_kv: the pre-check layers compute K/V for every row instead of using
     the chunk caches, which agree with it up to rounding there (R5); their chunk KV is then
-    neither loaded nor re-positioned (a third of the host bytes of a three-layer stack)."""
+    neither loaded nor re-positioned (a third of the host bytes of a three-layer stack).
+
+    precheck_load_rows: the pre-check layers use the chunk caches for the first X cached
+    rows only and compute K/V for the rest (R5 again); only those X rows of their chunk KV
+    are loaded and re-positioned.  precheck_split_rows() picks the X at which the load
+    ends with the GEMMs that precede the layer's attention."""
     eng = req.eng
     dm = eng.dm
     s = dm.shape
@@ -411,9 +467,23 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
         req.m_last, req.x_last = req.N, req.x[0]
         B.cb_lmhead_argmax(req.x[0][req.N - 1], dm.final_norm, dm.w_lm, dims, None, req.token, eng.ws, stream)
         return req.N
+    pre = {l for l, (mode, _) in enumerate(plan) if mode == B.CB_LAYER_PRECHECK}
+    split = None
+    if precheck_load_rows is not None:
+        split = int(precheck_load_rows)
+        if req.forced_mask is not None or recompute_precheck_kv or not 0 < split <= req.n_cached:
+            raise ValueError("precheck_load_rows needs the default layout, 0 < X <= n_cached and no "
+                             "recompute_precheck_kv")
+
     def assemble_layer(l, st):
-        # one re-positioning pass per run of adjacent chunk slots
+        # one re-positioning pass per run of adjacent chunk slots (pre-check layers with a
+        # split: the rows below it only)
+        lim = split if (split is not None and l in pre) else None
         for r0, c0, n in req.runs:
+            if lim is not None:
+                if r0 >= lim:
+                    continue
+                n = min(n, lim - r0)
             kd, vd = req.K[l][r0:r0 + n], req.V[l][r0:r0 + n]
             src, dl = req.src_row[c0:c0 + n], req.delta[c0:c0 + n]
             if isinstance(req.pool, ChunkPoolQ8):
@@ -425,8 +495,9 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
                 B.cb_rope_shift(kd, vd, req.pool.k[l], req.pool.v[l], src, dl, n, dims, eng.cos_sin, eng.max_pos,
                                 st)
 
-    skip = {l for l, (mode, _) in enumerate(plan) if mode == B.CB_LAYER_PRECHECK} if recompute_precheck_kv else set()
-    ready, errors, loader = None, [], None
+    skip = set(pre) if recompute_precheck_kv else set()
+    partial = {l: req.pool_ranges(split) for l in pre} if split is not None else {}
+    ready, errors, loader, queue_loads = None, [], None, None
     if file_store is not None:
         host_pool = file_store.hp
     if host_pool is not None and host_pool.pool is not req.pool:
@@ -444,8 +515,7 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
                         ready[l].set()
                         continue
                     file_store.read_layer(l)
-                    for h, d in zip(hp.host[l], hp.dev[l]):
-                        B.cb_prefetch_layer(d, h, h.numel() * h.element_size(), hp.side, hp.done[l])
+                    hp.copy_layer(l, partial.get(l))
                     if assemble:
                         assemble_layer(l, hp.side)
                         hp.done[l].record(hp.side)
@@ -458,8 +528,20 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
         loader = threading.Thread(target=load, daemon=True)
         loader.start()
     elif host_pool is not None:
-        host_pool.prefetch_all(torch.cuda.current_stream() if stream is None else stream,
-                               assemble_layer if assemble else None, skip)
+        # the loads are queued in layer order, interleaved with the layers: layer 0's before
+        # anything else, layer l+1's right after layer l has been queued (the host runs far
+        # ahead of the device, so every load still starts as soon as the previous one ends,
+        # and the first layer's launches are not held back behind the later layers' calls)
+        host_pool.begin(torch.cuda.current_stream() if stream is None else stream)
+        queued = [0]
+
+        def queue_loads(upto):
+            while queued[0] < min(upto, s.n_layers):
+                l = queued[0]
+                if l not in skip:
+                    host_pool.load_layer(l, assemble_layer if assemble else None, partial.get(l))
+                queued[0] += 1
+        queue_loads(1)
 
     if req.start_rows is None:
         B.cb_gather_rows(req.x[0], dm.embed, req.tokens, req.N, s.d_model * esz, stream)
@@ -489,10 +571,13 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
                                  req.scores if mode in (B.CB_LAYER_CHECK, B.CB_LAYER_GRADUAL) else None,
                                  eng.ws, stream,
                                  kv_ready=None if (host_pool is None or l in skip) else host_pool.done[l],
-                                 forced_mask=req.forced_mask, n_forced=req.n_forced, recompute_kv=l in skip)
+                                 forced_mask=req.forced_mask, n_forced=req.n_forced, recompute_kv=l in skip,
+                                 recompute_from=split if (split is not None and l in pre) else 0)
         cur = 1 - cur
         s_in = req.s[cur]
         m_in = m_out
+        if queue_loads is not None:
+            queue_loads(l + 2)
         if keep_history:
             req.sel_hist.append(req.s[cur][:m_out].clone())
             req.m_hist.append(m_out)

@@ -67,7 +67,7 @@ def with_text_segments(req_h, vocab, seed=11):
     return segs, toks
 
 
-def run_case(E, wl, r, gradual, tol, check_sets=True, q8=False, segments=False, recompute=False):
+def run_case(E, wl, r, gradual, tol, check_sets=True, q8=False, segments=False, recompute=False, split=None):
     torch = torch_mod()
     shape = wl.shape
     model = synth.make_model(shape, seed=wl.seed)
@@ -94,7 +94,7 @@ def run_case(E, wl, r, gradual, tol, check_sets=True, q8=False, segments=False, 
         pool = q8_pool_from_codes(E, pool, chunk_kv, dm.dims)
     req = E.Request(eng, pool, req_h.order, tokens, segments=segs)
     plan = req.plan(ratios, gradual=gradual)
-    m = E.run_blend(req, plan, keep_history=True, recompute_precheck_kv=recompute)
+    m = E.run_blend(req, plan, keep_history=True, recompute_precheck_kv=recompute, precheck_load_rows=split)
     from non_prefix_kv_gb300 import binding as B
     B.cb_sync(None)
     forced_teacher = False
@@ -119,7 +119,8 @@ def run_case(E, wl, r, gradual, tol, check_sets=True, q8=False, segments=False, 
             if mode in (B.CB_LAYER_CHECK, B.CB_LAYER_GRADUAL) and k > 0:
                 T = np.setdiff1d(ref["S"][l], ref["forced"]).astype(np.int32)
                 override[l] = torch.from_numpy(T).cuda()
-        m = E.run_blend(req, plan, sel_override=override, keep_history=True, recompute_precheck_kv=recompute)
+        m = E.run_blend(req, plan, sel_override=override, keep_history=True, recompute_precheck_kv=recompute,
+                        precheck_load_rows=split)
         B.cb_sync(None)
         for l in range(shape.n_layers):
             np.testing.assert_array_equal(req.sel_hist[l].cpu().numpy(), ref["S"][l])
@@ -147,18 +148,21 @@ def test_blend_tiny_f32_gradual_3_layers(E, r):
     run_case(E, wl, r, True, TOL["f32"])
 
 
+@pytest.mark.parametrize("how", ["all", "split"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_blend_with_precheck_kv_recomputed(E, dtype):
-    """The pre-check layer computing K/V for every row instead of reusing the chunk caches
-    (they agree there up to rounding) matches the oracle's blend."""
+def test_blend_with_precheck_kv_recomputed(E, dtype, how):
+    """The pre-check layer computing K/V for every row (or for every row from a split on,
+    reading the chunk caches below it) instead of reusing the chunk caches (they agree
+    there up to rounding) matches the oracle's blend."""
+    kw = dict(recompute=True) if how == "all" else {}
     if dtype == "f32":
         wl = synth.WORKLOADS["tiny_f32"]
         wl = replace(wl, shape=replace(wl.shape, n_layers=3))
-        run_case(E, wl, 0.15, False, TOL["f32"], recompute=True)
+        run_case(E, wl, 0.15, False, TOL["f32"], split=None if how == "all" else 200, **kw)
     else:
         wl = synth.Workload("bf16_small", BF16_SMALL, chunk_len=96, n_distinct=4, order=(0, 1, 2, 3), n_query=32,
                             ratio=0.15)
-        run_case(E, wl, 0.15, True, TOL["bf16"], check_sets=False, recompute=True)
+        run_case(E, wl, 0.15, True, TOL["bf16"], check_sets=False, split=None if how == "all" else 160, **kw)
 
 
 @pytest.mark.parametrize("r", [0.0, 0.15])
@@ -241,13 +245,18 @@ def test_blend_bf16_gqa(E):
 
 
 @pytest.mark.parametrize("q8,from_file,recompute", [(False, False, False), (True, False, False), (False, True, False),
-                                                     (True, True, False), (False, False, True), (False, True, True)],
+                                                     (True, True, False), (False, False, True), (False, True, True),
+                                                     (False, False, 160), (False, True, 200)],
                          ids=["bf16_pool", "8bit_pool", "bf16_file", "8bit_file", "bf16_pool_recompute",
-                              "bf16_file_recompute"])
+                              "bf16_file_recompute", "bf16_pool_split", "bf16_file_split"])
 def test_layer_ahead_loading_matches_resident_pool(E, q8, from_file, recompute, tmp_path):
     """Loading every layer's chunk KV (bf16, or 8-bit codes with their tables) from pinned
     host memory on a side stream, one event per layer, or from a file read layer by layer
-    by a loader thread, gives bit-identical results to the device-resident pool."""
+    by a loader thread, gives bit-identical results to the device-resident pool; so does
+    loading only the first rows of the pre-check layer (an int: the split) and recomputing
+    the rest."""
+    split = None if isinstance(recompute, bool) else recompute
+    recompute = recompute is True
     torch = torch_mod()
     from non_prefix_kv_gb300 import binding as B
     wl = synth.Workload("bf16_small", BF16_SMALL, chunk_len=96, n_distinct=4, order=(0, 1, 2, 3), n_query=32,
@@ -262,7 +271,7 @@ def test_layer_ahead_loading_matches_resident_pool(E, q8, from_file, recompute, 
     hp = E.HostPool(pool)
     plan = E.layer_plan(wl.shape, wl.n_tokens, wl.n_cached, [None, 0.15, 0.15])
     a = E.Request(eng, pool, req_h.order, req_h.tokens)
-    E.run_blend(a, plan, recompute_precheck_kv=recompute)
+    E.run_blend(a, plan, recompute_precheck_kv=recompute, precheck_load_rows=split)
     B.cb_sync(None)
     ka = [t.clone() for t in a.K]
     xa = a.x_last[:a.m_last].clone()
@@ -277,9 +286,9 @@ def test_layer_ahead_loading_matches_resident_pool(E, q8, from_file, recompute, 
                 t.zero_()
     b = E.Request(eng, pool, req_h.order, req_h.tokens)
     if from_file:
-        E.run_blend(b, plan, file_store=fs, recompute_precheck_kv=recompute)
+        E.run_blend(b, plan, file_store=fs, recompute_precheck_kv=recompute, precheck_load_rows=split)
     else:
-        E.run_blend(b, plan, host_pool=hp, recompute_precheck_kv=recompute)
+        E.run_blend(b, plan, host_pool=hp, recompute_precheck_kv=recompute, precheck_load_rows=split)
     B.cb_sync(None)
     for l in range(wl.shape.n_layers):
         assert torch.equal(ka[l], b.K[l])

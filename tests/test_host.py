@@ -126,6 +126,16 @@ def test_entry_points_reject_bad_arguments_before_launch(lib):
     assert lib.cb_blend_layer(*args(B.CB_LAYER_CHECK, 400, 5)) == 2       # CHECK needs all rows
     assert lib.cb_blend_layer(*args(B.CB_LAYER_PRECHECK, 416, 0, 100)) == 4
     assert lib.cb_blend_layer(*args(9, 416, 0)) == 1
+    # recompute_from: PRECHECK only, within [0, n_cached] (384 cached rows)
+    def with_opts(mode, m_in, k, rfrom, rkv=0):
+        o = B.cb_layer_opts(None, 0, None, rkv, rfrom)
+        a = list(args(mode, m_in, k))
+        a[19] = ctypes.byref(o)
+        return lib.cb_blend_layer(*a)
+    assert with_opts(B.CB_LAYER_CHECK, 416, 5, 128) == 1
+    assert with_opts(B.CB_LAYER_PRECHECK, 416, 0, 385) == 2
+    assert with_opts(B.CB_LAYER_PRECHECK, 416, 0, -1) == 2
+    assert with_opts(B.CB_LAYER_PRECHECK, 416, 0, 128, rkv=1) == 1
     assert m_out.value == -1          # nothing reported for a rejected call
     st = lib.cb_blend_layer(ctypes.byref(d), ctypes.byref(w), 0, FAKE, None, 416, 416, 384, FAKE, FAKE, FAKE,
                             100, 0, 0, None, FAKE + 64, FAKE, ctypes.byref(m_out), None, None, FAKE, 1 << 40, None)
@@ -174,3 +184,29 @@ def test_file_read_ranges_threads_and_errors(lib, tmp_path):
     with pytest.raises(B.CBError) as e:
         B.cb_file_read(str(path), len(data) - 10, buf.ctypes.data, 64)
     assert e.value.status == 10 and "end of file" in str(e.value)
+
+
+def test_precheck_split_balances_load_and_recompute():
+    """The pre-check split: loading X rows (host link, then re-positioning) takes as long as
+    RMSNorm + Q for every row and K/V for the other rows, to within one 64-row step; a
+    faster link loads more rows, a faster GEMM recomputes more; clamped to the cached rows."""
+    from non_prefix_kv_gb300 import engine as E
+    from non_prefix_kv_gb300 import synth
+    shape = synth.WORKLOADS["llama7b_layer_4k"].shape
+    N, nc = 4096, 3840
+    d, qc, W = shape.d_model, shape.q_width, shape.kv_width
+
+    def sides(x, link, tf, hbm):
+        R, L, H = tf * 1e12, link * 1e9, hbm * 1e9
+        comp = 2.0 * N * d * qc / R + 2.0 * N * d * 2 / H + (N - x) * 2.0 * d * 2 * W / R
+        load = x * (2.0 * W * 2 / L + 4.0 * W * 2 / H)
+        return comp, load
+
+    x = E.precheck_split_rows(shape, N, nc, 200.0, 1800.0, 6800.0)
+    assert x % 64 == 0 and 0 < x < nc
+    c0, l0 = sides(x, 200.0, 1800.0, 6800.0)
+    c1, l1 = sides(x + 64, 200.0, 1800.0, 6800.0)
+    assert l0 <= c0 and l1 > c1                # the largest 64-row multiple that still hides
+    assert E.precheck_split_rows(shape, N, nc, 400.0, 1800.0, 6800.0) > x
+    assert E.precheck_split_rows(shape, N, nc, 200.0, 3600.0, 6800.0) < x
+    assert E.precheck_split_rows(shape, N, nc, 1e6, 1800.0, 6800.0) == nc

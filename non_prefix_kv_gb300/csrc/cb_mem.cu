@@ -578,26 +578,40 @@ __global__ void __launch_bounds__(256) k_deviation(const T* __restrict__ kn, con
   }
 }
 
-// scores[c] = sum over column tiles t (in order) of part[t][c], the per-tile partials the
-// Q/K/V GEMM epilogue leaves when it computes the deviation in place.
-__global__ void k_dev_reduce(const float* __restrict__ part, int part_lo, int n_parts, int64_t ld, int n_cand,
-                             const int32_t* __restrict__ cand_pos, float* __restrict__ scores) {
+// scores[c] = sum over column tiles t of part[t][c], the per-tile partials the Q/K/V GEMM
+// epilogue leaves when it computes the deviation in place.  A block owns 32 candidates: warp
+// w sums the partials t = part_lo + w, part_lo + w + 8, ... of its lane's candidate (every
+// load coalesced over the 32 candidates, eight warps' loads in flight together), then the
+// eight warp sums are added in warp order, so the result does not depend on the launch.
+__global__ void __launch_bounds__(256) k_dev_reduce(const float* __restrict__ part, int part_lo, int n_parts,
+                                                    int64_t ld, int n_cand, const int32_t* __restrict__ cand_pos,
+                                                    float* __restrict__ scores) {
   pdl_wait();
   pdl_trigger();
-  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < n_cand; c += gridDim.x * blockDim.x) {
+  __shared__ float red[8][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + lane;
+  float acc = 0.f;
+  if (c < n_cand) {
     const int64_t row = cand_pos ? (int64_t)cand_pos[c] : c;
-    float acc = 0.f;
-#pragma unroll 8
-    for (int t = part_lo; t < n_parts; ++t) acc += part[t * ld + row];
-    scores[c] = acc;
-    if (!isfinite(acc)) atomicOr(&g_err_mem, ERRBIT_NONFINITE);
+#pragma unroll 4
+    for (int t = part_lo + w; t < n_parts; t += 8) acc += part[t * ld + row];
+  }
+  red[w][lane] = acc;
+  __syncthreads();
+  if (w == 0 && c < n_cand) {
+    float sum = red[0][lane];
+#pragma unroll
+    for (int j = 1; j < 8; ++j) sum += red[j][lane];
+    scores[c] = sum;
+    if (!isfinite(sum)) atomicOr(&g_err_mem, ERRBIT_NONFINITE);
   }
 }
 
 cudaError_t launch_dev_reduce(const float* part, int part_lo, int n_parts, int64_t ld, int n_cand,
                               const int32_t* cand_pos, float* scores, cudaStream_t s) {
   if (n_cand == 0) return cudaSuccess;
-  { const cudaError_t e_ = launch_k(k_dev_reduce, dim3(grid_for(n_cand, 256)), dim3(256), 0, s, part, part_lo, n_parts, ld, n_cand, cand_pos, scores); if (e_ != cudaSuccess) return e_; }
+  { const cudaError_t e_ = launch_k(k_dev_reduce, dim3((n_cand + 31) / 32), dim3(256), 0, s, part, part_lo, n_parts, ld, n_cand, cand_pos, scores); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
@@ -721,32 +735,41 @@ __device__ __forceinline__ int block_excl_scan(int v, int* total, int* sh) {
   return base + x - v;
 }
 
+// Up to this many keys are staged in shared memory (64 KB) and every pass reads them there.
+constexpr int kTopkSmemKeys = 16384;
+
+template <bool SMEM>
 __global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores, int n, int k,
                                                int32_t* __restrict__ out) {
   pdl_wait();
   pdl_trigger();
+  extern __shared__ uint32_t skey[];
   __shared__ int hist[256];
   __shared__ int sh[32];
   __shared__ uint32_t s_prefix;
   __shared__ int s_remaining;
   const int tid = threadIdx.x, bd = blockDim.x;
-  // validity check of every score (finite, non-negative)
+  // validity check of every score (finite, non-negative); the keys are staged on the way
+  bool bad = false;
   for (int i = tid; i < n; i += bd) {
     const float v = scores[i];
-    if (!(v >= 0.0f) || isinf(v)) atomicOr(&g_err_mem, ERRBIT_NONFINITE);
+    if (!(v >= 0.0f) || isinf(v)) bad = true;
+    if (SMEM) skey[i] = score_key(v);
   }
+  if (bad) atomicOr(&g_err_mem, ERRBIT_NONFINITE);
   if (k <= 0) return;
   if (k >= n) {
     for (int i = tid; i < n; i += bd) out[i] = i;
     return;
   }
+  auto key_at = [&](int i) -> uint32_t { return SMEM ? skey[i] : score_key(scores[i]); };
   uint32_t prefix = 0, mask = 0;
   int remaining = k;
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = tid; i < 256; i += bd) hist[i] = 0;
     __syncthreads();
     for (int i = tid; i < n; i += bd) {
-      const uint32_t key = score_key(scores[i]);
+      const uint32_t key = key_at(i);
       if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
     }
     __syncthreads();
@@ -788,6 +811,33 @@ __global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores,
     mask |= 255u << shift;
     __syncthreads();
   }
+  // every key > T, and the first `remaining` keys == T in index order
+  if (SMEM) {
+    // one block scan: thread t owns keys [t E, t E + E); counts of keys > T and == T packed
+    // in one int (n <= kTopkSmemKeys < 2^16)
+    const int E = (n + bd - 1) / bd;
+    const int i0 = min(n, tid * E), i1 = min(n, i0 + E);
+    int gt = 0, eq = 0;
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t key = skey[i];
+      gt += key > prefix;
+      eq += key == prefix;
+    }
+    int tot;
+    const int before = block_excl_scan(gt | (eq << 16), &tot, sh);
+    int eq_seen = before >> 16;
+    int pos = (before & 0xFFFF) + min(eq_seen, remaining);
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t key = skey[i];
+      if (key > prefix) {
+        out[pos++] = i;
+      } else if (key == prefix) {
+        if (eq_seen < remaining) out[pos++] = i;
+        ++eq_seen;
+      }
+    }
+    return;
+  }
   int eq_base = 0, out_base = 0;
   for (int i0 = 0; i0 < n; i0 += bd) {
     const int i = i0 + tid;
@@ -807,7 +857,20 @@ __global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores,
 
 cudaError_t launch_topk(const float* scores, int n, int k, int32_t* out_ord, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  { const cudaError_t e_ = launch_k(k_topk, dim3(1), dim3(1024), 0, s, scores, n, k, out_ord); if (e_ != cudaSuccess) return e_; }
+  if (n <= kTopkSmemKeys) {
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+      const cudaError_t e = cudaFuncSetAttribute(k_topk<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kTopkSmemKeys * 4);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    { const cudaError_t e_ = launch_k(k_topk<true>, dim3(1), dim3(1024), (size_t)n * 4, s, scores, n, k, out_ord); if (e_ != cudaSuccess) return e_; }
+  } else {
+    { const cudaError_t e_ = launch_k(k_topk<false>, dim3(1), dim3(1024), 0, s, scores, n, k, out_ord); if (e_ != cudaSuccess) return e_; }
+  }
   return cudaGetLastError();
 }
 

@@ -887,7 +887,7 @@ int cb_lmhead_argmax(const void* h, const void* final_norm, const void* w_lm, co
   cudaStream_t s = S(stream);
   L_RMSNORM(dims->dtype, CB_F32, hn, h, nullptr, final_norm, 1, dims->d_model, dims->rms_eps, s);
   L_LMGEMV(dims->dtype, lg, hn, w_lm, dims->vocab, dims->d_model, bb, s);
-  L_ARGMAX(bb, nb, token, s);
+  L_ARGMAX(bb, (int)lm_block_count(dims->vocab, dims->dtype), token, s);
   return CB_OK;
 }
 

@@ -120,7 +120,8 @@ cudaError_t launch_rows_to_positions(const int32_t* rows, int k, const int32_t* 
                                      int32_t* pos_out, cudaStream_t s);
 cudaError_t launch_iota(int32_t* out, int n, int32_t start, cudaStream_t s);
 cudaError_t launch_swiglu(int dt, void* out, const void* gu, int64_t M, int F, cudaStream_t s);
-size_t lm_block_best_count(int V);
+size_t lm_block_best_count(int V);          // workspace entries (either type)
+size_t lm_block_count(int V, int dt);       // entries the GEMV of this type writes
 cudaError_t launch_lm_gemv(int dt, float* logits, const float* hn, const void* w, int V, int d,
                            unsigned long long* block_best, cudaStream_t s);
 cudaError_t launch_argmax_keys(const unsigned long long* keys, int n, int32_t* token, cudaStream_t s);

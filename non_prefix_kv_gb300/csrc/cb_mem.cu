@@ -1130,36 +1130,71 @@ __global__ void __launch_bounds__(256) k_lm_gemv(float* __restrict__ logits, con
   const int r0 = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * rows_per_warp;
   const int r1 = min(V, r0 + rows_per_warp);
   unsigned long long best = 0ull;
-  for (int r = r0; r < r1; ++r) {
-    const T* wr = w + (int64_t)r * d;
-    float acc0 = 0.f, acc1 = 0.f;
+  // two rows at a time: eight 16-byte weight loads in flight per lane, and each normalised
+  // hidden value loaded once for both rows; each row's sum is taken in the same order as
+  // one row alone
+  for (int r = r0; r < r1; r += 2) {
+    const bool two = r + 1 < r1;
+    const T* wr0 = w + (int64_t)r * d;
+    const T* wr1 = two ? wr0 + d : wr0;
+    float acc0[2] = {0.f, 0.f}, acc1[2] = {0.f, 0.f};
     int c = lane * 8;
-    for (; c + 768 < d; c += 1024) {     // four 16-byte weight loads in flight per lane
-      float a[4][8];
+    for (; c + 768 < d; c += 1024) {
+      uint4 raw[2][4][sizeof(T) / 2];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) ld8(wr + c + 256 * u, a[u]);
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int q = 0; q < (int)(sizeof(T) / 2); ++q) {
+          raw[0][u][q] = reinterpret_cast<const uint4*>(wr0 + c + 256 * u)[q];
+          raw[1][u][q] = reinterpret_cast<const uint4*>(wr1 + c + 256 * u)[q];
+        }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         float b[8];
         ld8(hn + c + 256 * u, b);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (u & 1) acc1 = fmaf(a[u][i], b[i], acc1);
-          else acc0 = fmaf(a[u][i], b[i], acc0);
+        for (int j = 0; j < 2; ++j) {
+          float a[8];
+          if constexpr (sizeof(T) == 2) {
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw[j][u][0]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = __bfloat1622float2(h2[i]);
+              a[2 * i] = f.x;
+              a[2 * i + 1] = f.y;
+            }
+          } else {
+            const float* f = reinterpret_cast<const float*>(&raw[j][u][0]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a[i] = f[i];
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (u & 1) acc1[j] = fmaf(a[i], b[i], acc1[j]);
+            else acc0[j] = fmaf(a[i], b[i], acc0[j]);
+          }
         }
       }
     }
     for (; c < d; c += 256) {
-      float a[8], b[8];
-      ld8(wr + c, a);
+      float a0[8], a1[8], b[8];
+      ld8(wr0 + c, a0);
+      ld8(wr1 + c, a1);
       ld8(hn + c, b);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc0 = fmaf(a[i], b[i], acc0);
+      for (int i = 0; i < 8; ++i) {
+        acc0[0] = fmaf(a0[i], b[i], acc0[0]);
+        acc0[1] = fmaf(a1[i], b[i], acc0[1]);
+      }
     }
-    float acc = warp_sum(acc0 + acc1);
-    if (lane == 0) logits[r] = acc;
-    const unsigned long long key = argmax_key(acc, r);
-    best = key > best ? key : best;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (j == 1 && !two) break;
+      const float acc = warp_sum(acc0[j] + acc1[j]);
+      if (lane == 0) logits[r + j] = acc;
+      const unsigned long long key = argmax_key(acc, r + j);
+      best = key > best ? key : best;
+    }
   }
   if (lane == 0) red[wid] = best;
   __syncthreads();
@@ -1170,23 +1205,43 @@ __global__ void __launch_bounds__(256) k_lm_gemv(float* __restrict__ logits, con
   }
 }
 
-// rows per warp: the fewest that cover the vocabulary with the warps of 8 resident 256-thread
-// blocks per SM; the grid then holds just enough warps for that
-static int lm_rows_per_warp(int V) {
-  const int64_t warps = (int64_t)sm_count() * 8 * 8;
+// 256-thread blocks of the GEMV resident per SM (register-limited), once per device and type
+static int lm_blocks_per_sm(int dt) {
+  static int cached[64][2] = {{0}};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int t = dt == DT_BF16 ? 1 : 0;
+  if (dev >= 0 && dev < 64 && cached[dev][t]) return cached[dev][t];
+  int n = 0;
+  if (dt == DT_BF16)
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_lm_gemv<bf16>, 256, 0);
+  else
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_lm_gemv<float>, 256, 0);
+  cudaGetLastError();
+  if (n < 1) n = 1;
+  if (dev >= 0 && dev < 64) cached[dev][t] = n;
+  return n;
+}
+// rows per warp: the fewest that cover the vocabulary with the warps that are resident at
+// once; the grid then holds just enough warps for that, so every warp runs from the start
+// and all of them finish together (no partial last round of rows)
+static int lm_rows_per_warp(int V, int dt) {
+  const int64_t warps = (int64_t)sm_count() * lm_blocks_per_sm(dt) * 8;
   return (int)std::max<int64_t>(1, (V + warps - 1) / warps);
 }
-static unsigned lm_grid(int V) {
-  const int64_t warps = (V + lm_rows_per_warp(V) - 1) / lm_rows_per_warp(V);
+static unsigned lm_grid(int V, int dt) {
+  const int rpw = lm_rows_per_warp(V, dt);
+  const int64_t warps = (V + rpw - 1) / rpw;
   return (unsigned)std::max<int64_t>(1, (warps + 7) / 8);
 }
 
-size_t lm_block_best_count(int V) { return lm_grid(V); }
+size_t lm_block_best_count(int V) { return std::max(lm_grid(V, DT_BF16), lm_grid(V, DT_F32)); }
+size_t lm_block_count(int V, int dt) { return lm_grid(V, dt); }
 
 cudaError_t launch_lm_gemv(int dt, float* logits, const float* hn, const void* w, int V, int d,
                            unsigned long long* block_best, cudaStream_t s) {
-  const unsigned grid = lm_grid(V);
-  const int rpw = lm_rows_per_warp(V);
+  const unsigned grid = lm_grid(V, dt);
+  const int rpw = lm_rows_per_warp(V, dt);
   if (dt == DT_BF16)
     { const cudaError_t e_ = launch_k(k_lm_gemv<bf16>, dim3(grid), dim3(256), 0, s, logits, hn, (const bf16*)w, V, d, rpw, block_best); if (e_ != cudaSuccess) return e_; }
   else

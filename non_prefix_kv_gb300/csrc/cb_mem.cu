@@ -26,10 +26,39 @@ static int sm_count() {
   return n;
 }
 
-// grid for a grid-stride loop: enough blocks for the work, at most 8 resident per SM
-static unsigned grid_for(int64_t work_items, int threads) {
+// Blocks of `threads` threads of this kernel resident per SM at once (registers, shared
+// memory), once per kernel, block size and device.
+static int resident_blocks(const void* kernel, int threads) {
+  static std::mutex mu;
+  struct Ent {
+    const void* k;
+    int dev, threads, n;
+  };
+  static Ent cache[64];
+  static int used = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> g(mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].k == kernel && cache[i].dev == dev && cache[i].threads == threads) return cache[i].n;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = 1;
+  }
+  std::lock_guard<std::mutex> g(mu);
+  if (used < 64) cache[used++] = Ent{kernel, dev, threads, n};
+  return n;
+}
+
+// grid for a grid-stride loop: enough blocks for the work, at most as many as are resident
+// at once (a block beyond that would run in a partial second round, after the others)
+template <typename K>
+static unsigned grid_for(K* kernel, int64_t work_items, int threads) {
   int64_t b = (work_items + threads - 1) / threads;
-  int64_t cap = (int64_t)sm_count() * 8;
+  const int64_t cap = (int64_t)sm_count() * resident_blocks(reinterpret_cast<const void*>(kernel), threads);
   if (b > cap) b = cap;
   if (b < 1) b = 1;
   return (unsigned)b;
@@ -117,7 +146,7 @@ cudaError_t launch_rope_shift(int dt, void* kd, void* vd, const void* ks, const 
                               int W, int hd, const float* tab, int max_pos, cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
   const int64_t work = n_rows * (W / 8);
-  const unsigned grid = grid_for(work, 256);
+  const unsigned grid = dt == DT_BF16 ? grid_for(k_rope_shift<bf16>, work, 256) : grid_for(k_rope_shift<float>, work, 256);
   const float2* t2 = reinterpret_cast<const float2*>(tab);
   if (dt == DT_BF16)
     { const cudaError_t e_ = launch_k(k_rope_shift<bf16>, dim3(grid), dim3(256), 0, s, (bf16*)kd, (bf16*)vd, (const bf16*)ks,
@@ -298,7 +327,8 @@ cudaError_t launch_rope_shift_q8(int dt, void* kd, void* vd, const uint8_t* kq, 
                                  const int32_t* delta, int64_t n_rows, int W, int hd, const float* tab,
                                  int max_pos, cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
-  const unsigned grid = grid_for((n_rows + kQ8Rows - 1) / kQ8Rows * (W / 8), 256);
+  const int64_t work = (n_rows + kQ8Rows - 1) / kQ8Rows * (W / 8);
+  const unsigned grid = dt == DT_BF16 ? grid_for(k_rope_shift_q8<bf16>, work, 256) : grid_for(k_rope_shift_q8<float>, work, 256);
   const float2* t2 = reinterpret_cast<const float2*>(tab);
   if (dt == DT_BF16)
     { const cudaError_t e_ = launch_k(k_rope_shift_q8<bf16>, dim3(grid), dim3(256), 0, s, (bf16*)kd, (bf16*)vd, kq, vq, ks, kz, vs, vz, src_row, n_src, qrow, n_q, delta, n_rows, W, hd, t2, max_pos); if (e_ != cudaSuccess) return e_; }
@@ -353,11 +383,11 @@ cudaError_t launch_copy_rows(void* dst, const int32_t* dst_idx, const void* src,
   const bool v16 = (row_bytes % 16 == 0) && ((uintptr_t)dst % 16 == 0) && ((uintptr_t)src % 16 == 0);
   if (v16) {
     const int64_t rv = row_bytes / 16;
-    { const cudaError_t e_ = launch_k(k_copy_rows<uint4>, dim3(grid_for(n * rv, 256)), dim3(256), 0, s, (uint4*)dst, dst_idx, (const uint4*)src,
+    { const cudaError_t e_ = launch_k(k_copy_rows<uint4>, dim3(grid_for(k_copy_rows<uint4>, n * rv, 256)), dim3(256), 0, s, (uint4*)dst, dst_idx, (const uint4*)src,
                                                            src_idx, n, rv, dst_bound, src_bound); if (e_ != cudaSuccess) return e_; }
   } else {
     const int64_t rv = row_bytes / 4;
-    { const cudaError_t e_ = launch_k(k_copy_rows<uint32_t>, dim3(grid_for(n * rv, 256)), dim3(256), 0, s, (uint32_t*)dst, dst_idx,
+    { const cudaError_t e_ = launch_k(k_copy_rows<uint32_t>, dim3(grid_for(k_copy_rows<uint32_t>, n * rv, 256)), dim3(256), 0, s, (uint32_t*)dst, dst_idx,
                                                               (const uint32_t*)src, src_idx, n, rv,
                                                               dst_bound, src_bound); if (e_ != cudaSuccess) return e_; }
   }
@@ -405,7 +435,7 @@ cudaError_t launch_copy_rows_multi(const CopyJobs& J, cudaStream_t s) {
   if (J.n < 1 || J.n > kMaxCopyJobs) return cudaErrorInvalidValue;
   const int64_t total = J.end[J.n - 1];
   if (total == 0) return cudaSuccess;
-  { const cudaError_t e_ = launch_k(k_copy_rows_multi, dim3(grid_for(total, 256)), dim3(256), 0, s, J); if (e_ != cudaSuccess) return e_; }
+  { const cudaError_t e_ = launch_k(k_copy_rows_multi, dim3(grid_for(k_copy_rows_multi, total, 256)), dim3(256), 0, s, J); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
@@ -683,10 +713,11 @@ cudaError_t launch_deviation(int dt, const void* kn, const void* vn, const void*
                              int n_cand, int W, int use_v, float* scores, cudaStream_t s) {
   if (n_cand == 0) return cudaSuccess;
   if (dt == DT_BF16 && W % 1024 == 0) {
-    { const cudaError_t e_ = launch_k(k_deviation_wide, dim3(grid_for((int64_t)n_cand * 32, 256)), dim3(256), 0, s, (const bf16*)kn, (const bf16*)vn, (const bf16*)kr, (const bf16*)vr, new_row, ref_row, n_cand, W, use_v, scores); if (e_ != cudaSuccess) return e_; }
+    { const cudaError_t e_ = launch_k(k_deviation_wide, dim3(grid_for(k_deviation_wide, (int64_t)n_cand * 32, 256)), dim3(256), 0, s, (const bf16*)kn, (const bf16*)vn, (const bf16*)kr, (const bf16*)vr, new_row, ref_row, n_cand, W, use_v, scores); if (e_ != cudaSuccess) return e_; }
     return cudaGetLastError();
   }
-  const unsigned grid = grid_for((int64_t)n_cand * 32, 256);
+  const unsigned grid = dt == DT_BF16 ? grid_for(k_deviation<bf16>, (int64_t)n_cand * 32, 256)
+                                      : grid_for(k_deviation<float>, (int64_t)n_cand * 32, 256);
   if (dt == DT_BF16)
     { const cudaError_t e_ = launch_k(k_deviation<bf16>, dim3(grid), dim3(256), 0, s, (const bf16*)kn, (const bf16*)vn, (const bf16*)kr,
                                            (const bf16*)vr, new_row, ref_row, n_cand, W, use_v,
@@ -1089,7 +1120,7 @@ __global__ void k_swiglu(T* __restrict__ out, const T* __restrict__ gu, int64_t 
 
 cudaError_t launch_swiglu(int dt, void* out, const void* gu, int64_t M, int F, cudaStream_t s) {
   if (M == 0) return cudaSuccess;
-  const unsigned grid = grid_for(M * F, 256);
+  const unsigned grid = dt == DT_BF16 ? grid_for(k_swiglu<bf16>, M * F, 256) : grid_for(k_swiglu<float>, M * F, 256);
   if (dt == DT_BF16)
     { const cudaError_t e_ = launch_k(k_swiglu<bf16>, dim3(grid), dim3(256), 0, s, (bf16*)out, (const bf16*)gu, M, F); if (e_ != cudaSuccess) return e_; }
   else
@@ -1205,22 +1236,10 @@ __global__ void __launch_bounds__(256) k_lm_gemv(float* __restrict__ logits, con
   }
 }
 
-// 256-thread blocks of the GEMV resident per SM (register-limited), once per device and type
+// 256-thread blocks of the GEMV resident per SM (register-limited)
 static int lm_blocks_per_sm(int dt) {
-  static int cached[64][2] = {{0}};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const int t = dt == DT_BF16 ? 1 : 0;
-  if (dev >= 0 && dev < 64 && cached[dev][t]) return cached[dev][t];
-  int n = 0;
-  if (dt == DT_BF16)
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_lm_gemv<bf16>, 256, 0);
-  else
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_lm_gemv<float>, 256, 0);
-  cudaGetLastError();
-  if (n < 1) n = 1;
-  if (dev >= 0 && dev < 64) cached[dev][t] = n;
-  return n;
+  return dt == DT_BF16 ? resident_blocks(reinterpret_cast<const void*>(k_lm_gemv<bf16>), 256)
+                       : resident_blocks(reinterpret_cast<const void*>(k_lm_gemv<float>), 256);
 }
 // rows per warp: the fewest that cover the vocabulary with the warps that are resident at
 // once; the grid then holds just enough warps for that, so every warp runs from the start

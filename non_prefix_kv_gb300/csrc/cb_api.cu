@@ -142,6 +142,9 @@ double gemm_bytes(int dt, const GemmDesc& g) {
   CB_LAUNCH(CB_PROF_TOPK, 0, (n), (k), 0, 0.0, 4.0 * (n) + 4.0 * (k), s, launch_topk(sc, n, k, ord, s))
 #define L_MAP(ord, k, map, out, s) \
   CB_LAUNCH(CB_PROF_INDEX, 0, (k), 0, 0, 0.0, 12.0 * (k), s, launch_map_rows(ord, k, map, out, s))
+#define L_TOPK_SEL(sc, n, k, cr, f0, fp0, nf, so, ko, s)                                          \
+  CB_LAUNCH(CB_PROF_TOPK, 0, (n), (k), 0, 0.0, 4.0 * (n) + 8.0 * ((k) + (nf)), s,                \
+            launch_topk_sel(sc, n, k, cr, f0, fp0, nf, so, ko, s))
 #define L_BUILD_SEL(ord, k, cr, f0, fp0, nf, so, ko, s)                                          \
   CB_LAUNCH(CB_PROF_INDEX, 0, (k) + (nf), 0, 0, 0.0, 16.0 * ((k) + (nf)), s,                     \
             launch_build_sel(ord, k, cr, f0, fp0, nf, so, ko, s))
@@ -783,16 +786,22 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         L_GEMM(dims->dtype, gkv, s);
         L_DEV(dims->dtype, L.knew, L.vnew, k_cache, v_cache, cpos, crows, n_cand, W, use_v, sc, s);
       }
-      if (k_budget > 0) {
-        if (sel_override)
-          L_R2P(sel_override, k_budget, (check && !fmask) ? nullptr : crows, n_cand, L.ord, s);
+      if (k_budget > 0 && !sel_override && !fmask) {
+        // top-k and the selection build (S = candidate rows of the top k ++ forced rows) in
+        // one launch
+        L_TOPK_SEL(sc, n_cand, k_budget, rows_in, f0, m_in - n_forced, n_forced, s_out, L.keep, s);
+      } else {
+        if (k_budget > 0) {
+          if (sel_override)
+            L_R2P(sel_override, k_budget, (check && !fmask) ? nullptr : crows, n_cand, L.ord, s);
+          else
+            L_TOPK(sc, n_cand, k_budget, L.ord, s);
+        }
+        if (fmask)
+          L_MERGE(L.ord, k_budget, L.crows, L.cpos, L.frows, L.fpos, n_forced, s_out, L.keep, s);
         else
-          L_TOPK(sc, n_cand, k_budget, L.ord, s);
+          L_BUILD_SEL(L.ord, k_budget, rows_in, f0, m_in - n_forced, n_forced, s_out, L.keep, s);
       }
-      if (fmask)
-        L_MERGE(L.ord, k_budget, L.crows, L.cpos, L.frows, L.fpos, n_forced, s_out, L.keep, s);
-      else
-        L_BUILD_SEL(L.ord, k_budget, rows_in, f0, m_in - n_forced, n_forced, s_out, L.keep, s);
       // Step 3, KV expansion (the recomputed K/V of S replace the cached rows), and the
       // gathers of S's queries (or normalised rows) and residual rows: one launch
       {

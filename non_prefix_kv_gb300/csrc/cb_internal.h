@@ -111,6 +111,9 @@ cudaError_t launch_deviation(int dt, const void* kn, const void* vn, const void*
                              const void* vr, const int32_t* new_row, const int32_t* ref_row,
                              int n_cand, int W, int use_v, float* scores, cudaStream_t s);
 cudaError_t launch_topk(const float* scores, int n, int k, int32_t* out_ord, cudaStream_t s);
+// top-k fused with the selection build of the default layout (see launch_build_sel)
+cudaError_t launch_topk_sel(const float* scores, int n, int k, const int32_t* cand_row, int32_t forced_row0,
+                            int32_t forced_pos0, int n_forced, int32_t* s_out, int32_t* keep_out, cudaStream_t s);
 cudaError_t launch_map_rows(const int32_t* ord, int k, const int32_t* map, int32_t* out,
                             cudaStream_t s);
 cudaError_t launch_build_sel(const int32_t* ord, int k, const int32_t* cand_row,

@@ -769,11 +769,38 @@ __device__ __forceinline__ int block_excl_scan(int v, int* total, int* sh) {
 // Up to this many keys are staged in shared memory (64 KB) and every pass reads them there.
 constexpr int kTopkSmemKeys = 16384;
 
+// Optional fused selection output (the default row layout): instead of the ordinals, write
+// S = (candidate rows of the top-k ordinals, ascending) ++ (forced rows forced_row0 + f) and
+// each row's position in the layer's input set (keep: the ordinal, or forced_pos0 + f).
+struct SelOut {
+  const int32_t* cand_row;   // null: the ordinal is the row
+  int32_t forced_row0, forced_pos0;
+  int n_forced;
+  int32_t* s_out;            // null: plain ordinals to `out`
+  int32_t* keep;
+};
+
 template <bool SMEM>
 __global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores, int n, int k,
-                                               int32_t* __restrict__ out) {
+                                               int32_t* __restrict__ out, const SelOut so) {
   pdl_wait();
   pdl_trigger();
+  // the ordinal i taken at position pos of the selection
+  auto emit = [&](int pos, int i) {
+    if (so.s_out) {
+      so.s_out[pos] = so.cand_row ? so.cand_row[i] : i;
+      if (so.keep) so.keep[pos] = i;
+    } else {
+      out[pos] = i;
+    }
+  };
+  if (so.s_out) {
+    const int kk = k < n ? k : n;
+    for (int f = threadIdx.x; f < so.n_forced; f += blockDim.x) {
+      so.s_out[kk + f] = so.forced_row0 + f;
+      if (so.keep) so.keep[kk + f] = so.forced_pos0 + f;
+    }
+  }
   extern __shared__ uint32_t skey[];
   __shared__ int hist[256];
   __shared__ int sh[32];
@@ -790,7 +817,7 @@ __global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores,
   if (bad) atomicOr(&g_err_mem, ERRBIT_NONFINITE);
   if (k <= 0) return;
   if (k >= n) {
-    for (int i = tid; i < n; i += bd) out[i] = i;
+    for (int i = tid; i < n; i += bd) emit(i, i);
     return;
   }
   auto key_at = [&](int i) -> uint32_t { return SMEM ? skey[i] : score_key(scores[i]); };
@@ -861,9 +888,9 @@ __global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores,
     for (int i = i0; i < i1; ++i) {
       const uint32_t key = skey[i];
       if (key > prefix) {
-        out[pos++] = i;
+        emit(pos++, i);
       } else if (key == prefix) {
-        if (eq_seen < remaining) out[pos++] = i;
+        if (eq_seen < remaining) emit(pos++, i);
         ++eq_seen;
       }
     }
@@ -880,14 +907,14 @@ __global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores,
     const int take = gt || (eq && (eq_base + eq_rank) < remaining);
     int take_tot;
     const int pos = block_excl_scan(take, &take_tot, sh);
-    if (take) out[out_base + pos] = i;
+    if (take) emit(out_base + pos, i);
     eq_base += eq_tot;
     out_base += take_tot;
   }
 }
 
-cudaError_t launch_topk(const float* scores, int n, int k, int32_t* out_ord, cudaStream_t s) {
-  if (n == 0) return cudaSuccess;
+static cudaError_t topk_launch(const float* scores, int n, int k, int32_t* out_ord, const SelOut& so,
+                               cudaStream_t s) {
   if (n <= kTopkSmemKeys) {
     static bool attr_set[64] = {false};
     int dev = 0;
@@ -898,11 +925,22 @@ cudaError_t launch_topk(const float* scores, int n, int k, int32_t* out_ord, cud
       if (e != cudaSuccess) return e;
       if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    { const cudaError_t e_ = launch_k(k_topk<true>, dim3(1), dim3(1024), (size_t)n * 4, s, scores, n, k, out_ord); if (e_ != cudaSuccess) return e_; }
+    { const cudaError_t e_ = launch_k(k_topk<true>, dim3(1), dim3(1024), (size_t)n * 4, s, scores, n, k, out_ord, so); if (e_ != cudaSuccess) return e_; }
   } else {
-    { const cudaError_t e_ = launch_k(k_topk<false>, dim3(1), dim3(1024), 0, s, scores, n, k, out_ord); if (e_ != cudaSuccess) return e_; }
+    { const cudaError_t e_ = launch_k(k_topk<false>, dim3(1), dim3(1024), 0, s, scores, n, k, out_ord, so); if (e_ != cudaSuccess) return e_; }
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const float* scores, int n, int k, int32_t* out_ord, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  return topk_launch(scores, n, k, out_ord, SelOut{nullptr, 0, 0, 0, nullptr, nullptr}, s);
+}
+
+cudaError_t launch_topk_sel(const float* scores, int n, int k, const int32_t* cand_row, int32_t forced_row0,
+                            int32_t forced_pos0, int n_forced, int32_t* s_out, int32_t* keep_out, cudaStream_t s) {
+  if (n == 0 && n_forced == 0) return cudaSuccess;
+  return topk_launch(scores, n, k, nullptr, SelOut{cand_row, forced_row0, forced_pos0, n_forced, s_out, keep_out}, s);
 }
 
 // out[i] = map[ord[i]] (map null: ord[i])

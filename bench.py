@@ -562,13 +562,19 @@ def our_arm(args):
     top_key, top = max(gemms.items(), key=lambda kv: kv[1][1]) if gemms else ((0, 0, 0, 0), [1, 1.0, 0.0])
     top_ms = top[1] / top[0]
     achieved = top[2] / (top_ms / 1e3) / 1e12
-    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]) if shape.dtype == "bf16" \
-        else peaks.get("bf16_tflops_sustained", 1700.0) / 16.0
+    # the sustained figure (seconds under the power cap) where the timed region ran under the
+    # power cap, else the burst figure (a short timed region at full clocks)
+    capped = "sw_power_cap" in (clocks.get("reasons") or [])
+    pkey = "bf16_tflops_sustained" if capped else "bf16_tflops"
+    peak = peaks.get(pkey, FALLBACK_PEAKS[pkey])
+    if shape.dtype != "bf16":
+        peak /= 16.0
     top_desc = (top_key[0], top_key[1], top_key[2], epi_names.get(top_key[3], top_key[3]))
     roofline = {"bound": "tensor",
                 "kernel": "tcgen05 GEMM M=%d N=%d K=%d epilogue=%s (largest launch of the step; CTA-pair kernel k_gemm_tc_pair at this shape)" % top_desc,
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
+                "peak_source": (f"{peak_src} bf16_tflops_sustained (the timed region ran under the power cap)" if capped
+                                else f"{peak_src} bf16_tflops burst (the timed region ran at full clocks, no power cap)"),
                 "traffic": GEMM_TRAFFIC.get(top_desc), "traffic_unit": "bytes per launch (ncu dram read+write)",
                 "flops_per_launch": top[2], "ms_per_launch": top_ms,
                 "all_gemm_launches_tflops": all_gemm_tflops}
@@ -582,8 +588,8 @@ def our_arm(args):
             floor_s += max(r["bytes"] / (hbm_peak * 1e9), r["flops"] / (peak * 1e12)) / args.profile_steps
     step_roofline = {"floor_ms": floor_s * 1e3, "measured_ms": ms, "frac": floor_s * 1e3 / ms,
                      "model": "sum over the step's launches of max(algorithmic bytes / measured copy GB/s, "
-                              "FLOPs / measured sustained bf16 TFLOP/s); attention FLOPs from the selected rows' "
-                              "positions"}
+                              "FLOPs / the roofline's measured bf16 TFLOP/s); attention FLOPs from the selected "
+                              "rows' positions", "tensor_peak_tflops": peak}
     hbm_kernels = {}
     # (bf16 takes the deviation inside the K/V GEMM; only its small tile-sum pass remains)
     for name in ("rope_shift", "copy_rows", "lmhead_gemv") + (() if shape.dtype == "bf16" else ("deviation",)):

@@ -44,7 +44,7 @@ constexpr uint32_t TMEM_COLS = 512;   // two accumulators of up to 256 columns, 
 // 224).  A narrower tile leaves room for a fifth ring stage.
 template <int BN>
 struct TileCfg {
-  static_assert(BN % 32 == 0 && BN <= 256, "8 epilogue warps take BN/32 16-column chunks each");
+  static_assert(BN % 16 == 0 && BN <= 256, "the epilogue takes 16-column chunks");
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGES = BN == 256 ? 4 : 5;
   static constexpr int SMEM_BYTES = STAGES * (A_BYTES + B_BYTES) + 1024 /*align slack*/ + 256 /*barriers*/;
@@ -108,7 +108,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmDesc& g, int m, int n0, 
     }
     if (m < g.M) p.dev_part[((int64_t)(n0 / BN) * 2 + half) * p.dev_ld + m] = dsum;
   } else if (!swiglu) {
-    for (int c = half * CH; c < (half + 1) * CH; ++c) {
+    // the two warps of a row band split the tile's 16-column chunks (7 + 6 at 208 columns)
+    constexpr int NCH = BN / 16, H0 = (NCH + 1) / 2;
+    for (int c = half ? H0 : 0; c < (half ? NCH : H0); ++c) {
       float v[16];
       tc::tmem_ld16(trow + c * 16, v);
       const int n = n0 + c * 16;
@@ -569,16 +571,17 @@ int tiles_for(const GemmDesc* gs, int n, int out_cols) {
 
 // Tile width for one launch: each SM's share of the work is ceil(tiles / SMs) tiles of BN
 // columns, so pick the BN with the smallest product; a narrower tile must save at least 5%
-// (it moves more operand bytes per FLOP).  SwiGLU (gate and up halves of 16-column chunks per
-// epilogue warp) and the fused deviation (partials laid out per 256 columns) keep 256.
+// (it moves more operand bytes per FLOP).  208 fits one wave of 7 x 20 tiles (832 x 4096)
+// where 224 leaves 19 SMs idle.  SwiGLU (gate and up halves of 16-column chunks per epilogue
+// warp) and the fused deviation (partials laid out per 256 columns) keep 256.
 int pick_tile_n(const GemmDesc* gs, int n, int n_sm) {
   if (gs[0].epi.kind == EPI_SWIGLU) return 256;
   for (int p = 0; p < n; ++p)
     if (gs[p].epi.dev_part != nullptr) return 256;
-  const int cand[3] = {256, 224, 192};
+  const int cand[4] = {256, 224, 208, 192};
   int best = 256;
   int64_t best_cost = 0;
-  for (int c = 0; c < 3; ++c) {
+  for (int c = 0; c < 4; ++c) {
     const int64_t cost = (int64_t)((tiles_for(gs, n, cand[c]) + n_sm - 1) / n_sm) * cand[c];
     if (c == 0 || cost * 20 <= best_cost * 19) {
       if (c == 0 || cost < best_cost) {
@@ -780,6 +783,8 @@ cudaError_t launch_gemm_tc_group(const GemmDesc* gs, int n, cudaStream_t s) {
   switch (tp.bn) {
     case 224:
       return launch_tiles<224>(gs, n, swiglu, n_sm, s);
+    case 208:
+      return launch_tiles<208>(gs, n, swiglu, n_sm, s);
     case 192:
       return launch_tiles<192>(gs, n, swiglu, n_sm, s);
     default:

@@ -217,8 +217,9 @@ struct LayerWs {
   int32_t *ord, *keep, *pos, *rows, *cpos, *crows, *fpos, *frows;
 };
 
-// deviation partials per row of a GEMM over ncols Wqkv columns: one per half column tile
-int dev_parts(int ncols) { return 2 * ((ncols + kGemmTileN - 1) / kGemmTileN); }
+// deviation partials per row of a GEMM over ncols Wqkv columns in tiles of bn columns: one
+// per half tile (the workspace holds enough for the narrowest tile)
+int dev_parts(int ncols, int bn = kGemmTileNMinDev) { return 2 * ((ncols + bn - 1) / bn); }
 int qkv_cols(const cb_dims* d) { return (d->n_heads + 2 * d->n_kv_heads) * d->head_dim; }
 
 // R = rows entering the layer, M = rows selected (M <= R)
@@ -779,9 +780,11 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         gkv.epi.ref_row = rows_in;
         gkv.epi.ref_rows = N;
         gkv.epi.dev_use_v = use_v ? 1 : 0;
+        const int bn = gemm_tc_tile_n(&gkv, 1);
         L_GEMM(dims->dtype, gkv, s);
-        // partials of tiles that hold only Q columns are zero: start at the first K tile
-        L_DEVRED(L.dev_part, q_all ? 2 * (qc / kGemmTileN) : 0, dev_parts(ncols), m_in, n_cand, cpos, W, use_v, sc, s);
+        // partials of tiles that hold only Q columns are zero: start at the first tile that
+        // holds K columns
+        L_DEVRED(L.dev_part, q_all ? 2 * (qc / bn) : 0, dev_parts(ncols, bn), m_in, n_cand, cpos, W, use_v, sc, s);
       } else {
         L_GEMM(dims->dtype, gkv, s);
         L_DEV(dims->dtype, L.knew, L.vnew, k_cache, v_cache, cpos, crows, n_cand, W, use_v, sc, s);

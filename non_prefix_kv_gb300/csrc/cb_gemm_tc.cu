@@ -573,15 +573,17 @@ int tiles_for(const GemmDesc* gs, int n, int out_cols) {
 // columns, so pick the BN with the smallest product; a narrower tile must save at least 5%
 // (it moves more operand bytes per FLOP).  208 fits one wave of 7 x 20 tiles (832 x 4096)
 // where 224 leaves 19 SMs idle.  SwiGLU (gate and up halves of 16-column chunks per epilogue
-// warp) and the fused deviation (partials laid out per 256 columns) keep 256.
+// warp) keeps 256; the fused deviation (one partial per half tile of whole 32-column pairs
+// of chunks) takes 256, 224 or 192.
 int pick_tile_n(const GemmDesc* gs, int n, int n_sm) {
   if (gs[0].epi.kind == EPI_SWIGLU) return 256;
-  for (int p = 0; p < n; ++p)
-    if (gs[p].epi.dev_part != nullptr) return 256;
+  bool dev = false;
+  for (int p = 0; p < n; ++p) dev = dev || gs[p].epi.dev_part != nullptr;
   const int cand[4] = {256, 224, 208, 192};
   int best = 256;
   int64_t best_cost = 0;
   for (int c = 0; c < 4; ++c) {
+    if (dev && cand[c] == 208) continue;
     const int64_t cost = (int64_t)((tiles_for(gs, n, cand[c]) + n_sm - 1) / n_sm) * cand[c];
     if (c == 0 || cost * 20 <= best_cost * 19) {
       if (c == 0 || cost < best_cost) {
@@ -727,8 +729,7 @@ TilePlan plan_tiles(const GemmDesc* gs, int n, int n_sm, int n_pairs) {
   TilePlan tp{false, pick_tile_n(gs, n, n_sm)};
   const int mode = pair_mode();
   if (mode == 0 || n_pairs < 1) return tp;
-  bool fixed = gs[0].epi.kind == EPI_SWIGLU;
-  for (int p = 0; p < n; ++p) fixed = fixed || gs[p].epi.dev_part != nullptr;
+  const bool fixed = gs[0].epi.kind == EPI_SWIGLU;
   const int cand[3] = {256, 224, 192};
   int pbn = 256;
   int64_t pcost = 0, pwaves = 0;
@@ -755,6 +756,12 @@ TilePlan plan_tiles(const GemmDesc* gs, int n, int n_sm, int n_pairs) {
 }
 
 }  // namespace
+
+// The tile width (output columns per tile, SwiGLU: gate + up) launch_gemm_tc_group will use
+// for this launch; the fused deviation's partials are laid out per half tile of this width.
+int gemm_tc_tile_n(const GemmDesc* gs, int n) {
+  return plan_tiles(gs, n, sm_count(), pair_slots()).bn;
+}
 
 // Host preconditions (checked by the caller's validation, re-checked here): K % 8 == 0,
 // lda/ldb % 8 == 0, A and B 16-byte aligned, N % 16 == 0.

@@ -45,8 +45,9 @@ struct EpiParams {
   const float* rope = nullptr;      // cos/sin table [max_pos][hd/2][2]
   int max_pos = 0;
   // EPI_QKV on the tensor-core path: squared deviation of the (bf16-rounded) K/V columns
-  // from the cached rows, one partial per output row and half of a kGemmTileN-column tile
-  float* dev_part = nullptr;        // [2 * ceil(N / kGemmTileN)][dev_ld]
+  // from the cached rows, one partial per output row and half of a BN-column tile (BN the
+  // launch's tile width, gemm_tc_tile_n)
+  float* dev_part = nullptr;        // [2 * ceil(N / BN)][dev_ld]
   int64_t dev_ld = 0;
   const void* k_ref = nullptr;      // rows ref_row[m] (or m) of [ref_rows, kv_cols]
   const void* v_ref = nullptr;
@@ -55,7 +56,8 @@ struct EpiParams {
   int dev_use_v = 1;
 };
 
-constexpr int kGemmTileN = 256;     // output columns per tensor-core GEMM tile
+constexpr int kGemmTileN = 256;     // widest tensor-core GEMM tile (output columns)
+constexpr int kGemmTileNMinDev = 192;   // narrowest tile a fused-deviation launch takes
 
 struct GemmDesc {
   int M = 0, N = 0, K = 0;
@@ -66,6 +68,10 @@ struct GemmDesc {
   int64_t b_up_row = 0;     // EPI_SWIGLU: row of B holding the 'up' partner of row 0
   EpiParams epi;
 };
+
+// ---- cb_gemm_tc.cu --------------------------------------------------------------------
+// tile width (output columns) the tensor-core GEMM launch of these problems will use
+int gemm_tc_tile_n(const GemmDesc* gs, int n);
 
 // ---- cb_mem.cu ------------------------------------------------------------------------
 cudaError_t launch_rope_table(float* tab, int max_pos, int hd, double base, cudaStream_t s);

@@ -123,12 +123,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   int* s_qmax = reinterpret_cast<int*>(kv_empty + NST + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // heads vary fastest in launch order and the latest (longest) query tiles come first, so
-  // every head's heavy tiles start in the first wave and the short ones fill in behind
-  const int qt = gridDim.y - 1 - blockIdx.y;
+  // Query tiles are cut from the end of the (position-sorted) rows: tile y holds rows
+  // [M - 128 (y + 1), M - 128 y), so a partial tile, if any, is the one with the smallest
+  // positions (the cheapest) rather than the last one (which sees every key).  Heads vary
+  // fastest in launch order and the latest (longest) query tiles come first, so every
+  // head's heavy tiles start in the first wave and the short ones fill in behind.
   const int h = blockIdx.x;
   const int g = h / (H / Hkv);
-  const int m0 = qt * BM;
+  const int m0 = M - (int)(blockIdx.y + 1) * BM;   // may be negative for the first rows' tile
 
   if (threadIdx.x == 0) {
     tc::mbar_init(q_full, 1);
@@ -151,7 +153,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int mx = 0;
     for (int i = lane; i < BM; i += 32) {
       const int m = m0 + i;
-      if (m < M) {
+      if (m >= 0 && m < M) {
         int p = q_pos[m];
         if (p < 0 || p >= n_kv) {
           atomicOr(&g_err_attn_tc, ERRBIT_INDEX);
@@ -256,8 +258,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int half = (warp - 2) >> 2;
     const int r = lane_base + lane;
     const int m = m0 + r;
+    const bool row_valid = m >= 0 && m < M;
     int qp = 0;
-    if (m < M) {
+    if (row_valid) {
       qp = q_pos[m];
       qp = qp < 0 ? 0 : (qp >= n_kv ? (int)(n_kv - 1) : qp);
     }
@@ -372,14 +375,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::tc_fence_after();
       const float lt = xsum[r] + xsum[BM + r];
       const float inv = lt > 0.f ? 1.0f / lt : 0.f;
-      bf16* orow = out + (int64_t)m * H * HD + (int64_t)h * HD + half * (HD / 2);
+      bf16* orow = out + (int64_t)(row_valid ? m : 0) * H * HD + (int64_t)h * HD + half * (HD / 2);
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
         float o[16];
         tc::tmem_ld16(tO + c * 16, o);
 #pragma unroll
         for (int i = 0; i < 16; ++i) o[i] *= inv;
-        if (m < M) {
+        if (row_valid) {
           if ((reinterpret_cast<uintptr_t>(orow + c * 16) & 31) == 0) {
             st16_v8(orow + c * 16, o);
           } else {

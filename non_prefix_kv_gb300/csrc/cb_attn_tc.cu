@@ -274,8 +274,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int b = j % NSB;
       ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(&s_full[b], (j / NSB) & 1));
       const uint32_t tS = trow + TM_S0 + b * BN;
+      const int key0 = j * BN + half * 64;
+      // every key of this half lies beyond the positions of all 32 rows of this warp (scattered
+      // selected rows): the scores are neither read nor exponentiated, P is written as zeros
+      const bool none = __all_sync(0xffffffffu, key0 > qp);
       uint32_t sr[64];
-      if (ok) {
+      if (ok && !none) {
         tc::tc_fence_after();
         tc::tmem_ld32_nowait(tS + half * 64, sr);
         tc::tmem_ld32_nowait(tS + half * 64 + 32, sr + 32);
@@ -284,12 +288,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 64; ++i) sr[i] = 0u;
       }
-      const int key0 = j * BN + half * 64;
       const bool full_row = key0 + 63 <= qp;            // no causal mask in these 64 keys
       float pmx[4];
 #pragma unroll
       for (int a = 0; a < 4; ++a) pmx[a] = -INFINITY;
-      if (full_row) {
+      if (none) {
+        // nothing visible: the maximum stays -inf
+      } else if (full_row) {
 #pragma unroll
         for (int i = 0; i < 64; i += 8) {
 #pragma unroll
@@ -341,6 +346,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t pk[16];
+        if (none) {
+#pragma unroll
+          for (int w = 0; w < 16; ++w) pk[w] = 0u;
+          tc::tmem_st16u_nowait(tS + half * 32 + c * 16, pk);
+          continue;
+        }
 #pragma unroll
         for (int w = 0; w < 16; ++w) {
           const int k0 = c * 32 + 2 * w;

@@ -722,9 +722,10 @@ struct TilePlan {
 // co-resident CTAs, or pairs) x BN per SM.  A pair tile does the same per-SM work as a
 // single-SM tile of its width in about 1/1.12 of the time (measured at equal wave counts:
 // 4096 x 8192 x 4096 and 8192^3 ran 13-15% faster as pairs), but pads M to 256 rows: pairs
-// are taken only with at least two waves and at most 2% more padded rows than single tiles
-// (832 rows pad to 1024 as pairs), and there where their cost is lower.  SwiGLU and the
-// fused deviation keep 256 columns either way.
+// are taken only with at least two waves and at most 8% more padded rows than single tiles
+// (832 rows pad to 1024 as pairs, 14% more than 896; 1664 rows to 1792, 7.7% more, where the
+// 1664 x 13824 SwiGLU runs 430 -> 405 us as pairs), and there where their cost is lower.
+// SwiGLU keeps 256 columns either way.
 TilePlan plan_tiles(const GemmDesc* gs, int n, int n_sm, int n_pairs) {
   TilePlan tp{false, pick_tile_n(gs, n, n_sm)};
   const int mode = pair_mode();
@@ -751,7 +752,7 @@ TilePlan plan_tiles(const GemmDesc* gs, int n, int n_sm, int n_pairs) {
   }
   const int out_s = gs[0].epi.kind == EPI_SWIGLU ? tp.bn / 2 : tp.bn;
   const int64_t scost = (int64_t)((tiles_for(gs, n, out_s) + n_sm - 1) / n_sm) * tp.bn;
-  if (pwaves >= 2 && rows_pair * 100 <= rows_single * 102 && pcost * 100 < scost * 112) return TilePlan{true, pbn};
+  if (pwaves >= 2 && rows_pair * 100 <= rows_single * 108 && pcost * 100 < scost * 112) return TilePlan{true, pbn};
   return tp;
 }
 

@@ -510,6 +510,15 @@ def our_arm(args):
             for r in reqs:
                 E.run_blend(r, plan, overlap_assembly=False)
     recs = B.cb_profile_end(100000)
+    # per-layer time: CUDA events around each layer call (eager, one more pass)
+    lev = []
+    with torch.cuda.stream(stream):
+        for r in reqs:
+            E.run_blend(r, plan, overlap_assembly=False, layer_events=lev)
+    stream.synchronize()
+    per_layer = {}
+    for l, a, b in lev:
+        per_layer[l] = per_layer.get(l, 0.0) + a.elapsed_time(b)
     # selected rows of each layer (for the attention FLOPs)
     with torch.cuda.stream(stream):
         for r in reqs:
@@ -521,6 +530,8 @@ def our_arm(args):
         name = {B.CB_LAYER_PRECHECK: "precheck", B.CB_LAYER_CHECK: "check", B.CB_LAYER_STEADY: "steady",
                 B.CB_LAYER_GRADUAL: "gradual"}[mode]
         sel_sums.append((len(S), float(np.sum(S + 1)), name))
+    layers_ms = [{"layer": l, "mode": sel_sums[l][2], "rows": sel_sums[l][0], "ms": per_layer.get(l, 0.0)}
+                 for l in range(len(plan))]
     flops = step_flops(wl, sel_sums) * len(reqs)
     attn_flops_step = sum(4.0 * shape.n_heads * shape.head_dim * ps for _, ps, _ in sel_sums) * len(reqs)
 
@@ -776,7 +787,7 @@ def our_arm(args):
         "gpu_launches": int(launches_per_step * args.steps),
         "launches_per_step": int(launches_per_step),
         "step_tflops": flops / (ms / 1e3) / 1e12,
-        "roofline": roofline, "step_roofline": step_roofline, "hbm_kernels": hbm_kernels, "kernels": kernels, "gemm_launches": gemm_detail,
+        "roofline": roofline, "step_roofline": step_roofline, "layers": layers_ms, "hbm_kernels": hbm_kernels, "kernels": kernels, "gemm_launches": gemm_detail,
         "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "full_prefill": full, "quality_diagnostics": quality,
         "setup_s": setup_s,
     }

@@ -432,7 +432,8 @@ class RequestGraph:
 def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None, keep_history=False,
               assemble: bool = True, stream=None, host_pool: Optional[HostPool] = None,
               file_store: Optional[FileStore] = None, recompute_precheck_kv: bool = False,
-              precheck_load_rows: Optional[int] = None, overlap_assembly: bool = True):
+              precheck_load_rows: Optional[int] = None, overlap_assembly: bool = True,
+              layer_events: Optional[list] = None):
     """One blended prefill: re-position the chunk KV of every layer, run the layer plan,
     then the lm_head argmax.  Returns the number of rows carried out of the last layer.
 
@@ -454,6 +455,9 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
     engine's assembly stream, queued layer by layer between the layers, and each layer waits
     for its own layer's event at its first cached-row access, instead of all of it up front
     on the layers' stream (32-layer 7B-shape step 12.25 -> 12.15 ms; no change at 3 layers).
+
+    layer_events: a list that receives (layer, start, end) CUDA events recorded on the
+    layers' stream around each layer (timing only).
 
     precheck_load_rows: the pre-check layers use the chunk caches for the first X cached
     rows only and compute K/V for the rest (R5 again); only those X rows of their chunk KV
@@ -591,6 +595,9 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
                 loader.join()
                 raise errors[0]
         ov = None if sel_override is None else sel_override.get(l)
+        if layer_events is not None:
+            ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            ev[0].record(torch.cuda.current_stream() if stream is None else stream)
         m_out = B.cb_blend_layer(dims, dm.layers_c[l], mode, req.x[cur], s_in, m_in, req.N, req.n_cached,
                                  req.K[l], req.V[l], eng.cos_sin, eng.max_pos, k, dev_mode, ov,
                                  req.x[1 - cur], req.s[1 - cur],
@@ -600,6 +607,9 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
                                            None if (host_pool is None or l in skip) else host_pool.done[l]),
                                  forced_mask=req.forced_mask, n_forced=req.n_forced, recompute_kv=l in skip,
                                  recompute_from=split if (split is not None and l in pre) else 0)
+        if layer_events is not None:
+            ev[1].record(torch.cuda.current_stream() if stream is None else stream)
+            layer_events.append((l, ev[0], ev[1]))
         cur = 1 - cur
         s_in = req.s[cur]
         m_in = m_out

@@ -29,7 +29,7 @@ def declared_symbols():
     return sorted(set(re.findall(r"\b(cb_[a-z0-9_]+)\s*\(", text)))
 
 
-def test_header_declares_the_north_star_calls():
+def test_header_declares_the_hot_path_calls():
     names = declared_symbols()
     for n in ["cb_rope_shift", "cb_kv_deviation_topk", "cb_gather_rows", "cb_selective_qkv",
               "cb_partial_attention", "cb_scatter_kv", "cb_blend_layer", "cb_full_prefill"]:

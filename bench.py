@@ -185,6 +185,18 @@ def step_flops(wl, sel_sums):
     return total
 
 
+def whole_step_floor_ms(recs, profile_steps, attn_flops_step, hbm_gbs, tflops):
+    """The step's roofline time: every launch at its own bound, the longer of its algorithmic
+    bytes at hbm_gbs and its FLOPs at tflops, summed over the launches of profile_steps steps
+    and divided by profile_steps.  Attention launches are taken together from the step's
+    attention FLOPs (their records carry no per-launch FLOP count of the selected rows)."""
+    floor_s = attn_flops_step / (tflops * 1e12)
+    for r in recs:
+        if r["kind"] != "attention":
+            floor_s += max(r["bytes"] / (hbm_gbs * 1e9), r["flops"] / (tflops * 1e12)) / profile_steps
+    return floor_s * 1e3
+
+
 # ------------------------------------------------------------------------------ CPU oracle sample
 def oracle_sample(wl, frac_rows=4):
     """Times the CPU oracle on a bounded sample of the step: the steady layer (selective
@@ -632,11 +644,8 @@ def our_arm(args):
     # copy bandwidth, or its FLOPs at the sustained tensor rate, whichever is longer), summed
     # over one step and set against the measured graph-replayed step
     hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-    floor_s = attn_flops_step / (peak * 1e12)
-    for r in recs:
-        if r["kind"] != "attention":
-            floor_s += max(r["bytes"] / (hbm_peak * 1e9), r["flops"] / (peak * 1e12)) / args.profile_steps
-    step_roofline = {"floor_ms": floor_s * 1e3, "measured_ms": ms, "frac": floor_s * 1e3 / ms,
+    floor_ms = whole_step_floor_ms(recs, args.profile_steps, attn_flops_step, hbm_peak, peak)
+    step_roofline = {"floor_ms": floor_ms, "measured_ms": ms, "frac": floor_ms / ms,
                      "model": "sum over the step's launches of max(algorithmic bytes / measured copy GB/s, "
                               "FLOPs / the roofline's measured bf16 TFLOP/s); attention FLOPs from the selected "
                               "rows' positions", "tensor_peak_tflops": peak}

@@ -243,11 +243,7 @@ class Request:
     def pool_ranges(self, n_rows: int):
         """Pool rows feeding the request's first n_rows cached slots, as (first row, rows)
         ranges of consecutive pool rows."""
-        src = self.src_host[:n_rows]
-        if len(src) == 0:
-            return []
-        cut = np.nonzero(np.diff(src) != 1)[0] + 1
-        return [(int(a[0]), int(len(a))) for a in np.split(src, cut)]
+        return contiguous_ranges(self.src_host[:n_rows])
 
     def plan(self, ratios: Sequence[Optional[float]], check_layer: int = 1, gradual: bool = False):
         return layer_plan(self.eng.dm.shape, self.N, self.n_cached, ratios, check_layer, gradual,
@@ -263,6 +259,15 @@ class Request:
         self.start_rows = torch.from_numpy(rows).to(self.tokens.device)
         self.start_tokens = torch.from_numpy(self.tokens_host[first:].copy()).to(self.tokens.device)
         return [(B.CB_LAYER_STEADY, 0)] * self.eng.dm.shape.n_layers
+
+
+def contiguous_ranges(rows) -> list:
+    """(first, count) runs of consecutive values in a row list, in list order."""
+    src = np.asarray(rows, np.int64)
+    if len(src) == 0:
+        return []
+    cut = np.nonzero(np.diff(src) != 1)[0] + 1
+    return [(int(a[0]), int(len(a))) for a in np.split(src, cut)]
 
 
 def precheck_split_rows(shape: ModelShape, n_tok: int, n_cached: int, link_gbs: float, gemm_tflops: float,

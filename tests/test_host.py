@@ -210,3 +210,30 @@ def test_precheck_split_balances_load_and_recompute():
     assert E.precheck_split_rows(shape, N, nc, 400.0, 1800.0, 6800.0) > x
     assert E.precheck_split_rows(shape, N, nc, 200.0, 3600.0, 6800.0) < x
     assert E.precheck_split_rows(shape, N, nc, 1e6, 1800.0, 6800.0) == nc
+
+
+def test_contiguous_pool_ranges():
+    """The pool rows a partial pre-check load copies: runs of consecutive pool rows in the
+    request's slot order (chunks may come from anywhere in the pool, in any order)."""
+    from non_prefix_kv_gb300 import engine as E
+    assert E.contiguous_ranges([]) == []
+    assert E.contiguous_ranges([5]) == [(5, 1)]
+    assert E.contiguous_ranges(range(10, 20)) == [(10, 10)]
+    # chunk 2 (rows 1280..1919) then chunk 0 (0..639), a partial third chunk (640..703)
+    rows = list(range(1280, 1920)) + list(range(0, 640)) + list(range(640, 704))
+    assert E.contiguous_ranges(rows) == [(1280, 640), (0, 704)]
+    # a repeated chunk is two runs
+    assert E.contiguous_ranges(list(range(0, 4)) + list(range(0, 4))) == [(0, 4), (0, 4)]
+
+
+def test_whole_step_roofline_floor():
+    """bench.py's step floor: each launch at the longer of bytes / bandwidth and FLOPs / rate,
+    attention from the step's FLOPs, averaged over the profiled steps."""
+    import bench
+    recs = [{"kind": "gemm", "bytes": 1e9, "flops": 2e12},        # 1.0 ms at 2 PFLOP/s (> 0.1 ms of bytes)
+            {"kind": "rmsnorm", "bytes": 5e9, "flops": 1e9},       # 0.5 ms at 10 TB/s
+            {"kind": "attention", "bytes": 1e9, "flops": 9e12},    # replaced by the step's FLOPs
+            {"kind": "gemm", "bytes": 1e9, "flops": 2e12},         # the second profiled step
+            {"kind": "rmsnorm", "bytes": 5e9, "flops": 1e9}]
+    got = bench.whole_step_floor_ms(recs, 2, 1e12, 10000.0, 2000.0)
+    assert abs(got - 2.0) < 1e-9                           # (1.0 + 0.5 + 1.0 + 0.5) / 2 + 0.5

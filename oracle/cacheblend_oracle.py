@@ -206,7 +206,9 @@ def full_prefill(model: dict, tokens: np.ndarray, pos0: int = 0) -> Dict[str, ob
 
 
 def lm_head_argmax(model: dict, h_last: np.ndarray):
-    """First token of the answer: argmax(RMSNorm(h) W_lm^T), lowest index on ties (R8)."""
+    """First token of the answer: argmax(RMSNorm(h) W_lm^T), lowest index on ties (R8).
+    Pinned by: a hand-built case (one-hot lm_head rows, a non-unit final-norm gain,
+    closed-form logits, a tie between equal rows)."""
     shape = model["shape"]
     b = rmsnorm(np.asarray(h_last, F64)[None, :], model["final_norm"], shape.rms_eps)
     logits = linear(b, model["w_lm"])[0]
@@ -263,8 +265,9 @@ def ratio_schedule(r: float, n_layers: int, check_layer: int, gradual: bool,
                    r1_factor: float = 1.5) -> List[Optional[float]]:
     """Per-layer ratio: None for layers before the check layer; r at the check layer and
     after it in fixed mode; in gradual mode r_c = r1 = min(1, r1_factor*r) decaying toward
-    r as r + (r1 - r) 2^-(l-c) ([CB-A] §Gradual filtering; R6).  Parity unpinned beyond
-    its own definition (the pages give no numbers)."""
+    r as r + (r1 - r) 2^-(l-c) ([CB-A] §Gradual filtering; R6).  The pages give no numbers,
+    only the shape.  Pinned by: that shape (r1 >= r and <= 1, never increasing, never
+    below r, tending to r; constant r in fixed mode) and non-increasing budgets."""
     out: List[Optional[float]] = []
     r1 = min(1.0, r1_factor * r)
     for l in range(n_layers):

@@ -154,6 +154,51 @@ def test_budget_golden():
     assert O.budget(3840, 0.15, n_candidates=100) == 100
 
 
+@pytest.mark.parametrize("r", [0.0, 0.05, 0.15, 0.18, 0.5, 0.7, 1.0])
+def test_ratio_schedule_follows_gradual_filtering(r):
+    """CacheBlend explainer §Gradual filtering fixes the shape of the per-layer ratio: nothing
+    before the check layer; the check layer's r1 is at least r (a little above it) and at most
+    1; later layers never increase the ratio and approach r; fixed mode keeps r at every layer
+    from the check layer on.  The nested selections need the budgets to be non-increasing."""
+    L, c = 40, 1
+    fixed = O.ratio_schedule(r, L, c, gradual=False)
+    assert fixed[:c] == [None] * c and all(x == r for x in fixed[c:])
+    grad = O.ratio_schedule(r, L, c, gradual=True)
+    assert grad[:c] == [None] * c
+    rs = np.array(grad[c:], dtype=np.float64)
+    assert r <= rs[0] <= 1.0
+    if 0.0 < r < 1.0:
+        assert rs[0] > r                       # strictly above r at the check layer
+    assert np.all(np.diff(rs) <= 0.0)          # non-increasing
+    assert np.all(rs >= r)                     # never below the target
+    assert rs[-1] - r < 1e-9 * max(r, 1.0)     # tends to r
+    ks = [O.budget(3840, x) for x in rs]
+    assert all(a >= b for a, b in zip(ks, ks[1:]))
+    assert ks[-1] == O.budget(3840, r)
+    # another check layer shifts the schedule without changing its values
+    assert O.ratio_schedule(r, L, 3, gradual=True)[3:] == grad[1:L - 2]
+
+
+def test_lm_head_argmax_hand_built():
+    """First-token step on a hand-built case: one-hot lm_head rows, a non-unit final-norm gain,
+    closed-form logits and a tie (lowest index wins, R8).  h = (3, -4, 0, 0) has
+    mean(h^2) = 25/4, so RMSNorm(h) = h / sqrt(6.25 + eps)."""
+    shape = synth.ModelShape(n_layers=1, d_model=4, n_heads=1, n_kv_heads=1, head_dim=4, d_ff=4, vocab=5)
+    e = np.eye(4)
+    w_lm = np.stack([e[0], e[1], 2.0 * e[2], -e[1], e[0]])   # rows 0 and 4 are the same
+    h = np.array([3.0, -4.0, 0.0, 0.0])
+    rms = math.sqrt(6.25 + shape.rms_eps)
+    for gain, want_tok in (([2.0, 0.5, 1.0, 1.0], 0), ([0.5, 2.0, 1.0, 1.0], 3)):
+        model = {"shape": shape, "final_norm": np.array(gain), "w_lm": w_lm}
+        tok, logits = O.lm_head_argmax(model, h)
+        b0, b1 = 3.0 * gain[0] / rms, -4.0 * gain[1] / rms
+        np.testing.assert_allclose(logits, [b0, b1, 0.0, -b1, b0], rtol=1e-14, atol=1e-15)
+        assert tok == want_tok
+    # every logit equal: the lowest index
+    flat = {"shape": shape, "final_norm": np.ones(4), "w_lm": np.zeros((5, 4))}
+    assert O.lm_head_argmax(flat, h)[0] == 0
+
+
 def test_kv_deviation_closed_form():
     g = synth.rng(8, synth.P_NOISE)
     k = g.standard_normal((6, 2, 4))

@@ -229,10 +229,16 @@ def oracle_sample(wl, frac_rows=4):
 
 
 def cpu_threads():
+    """Threads the oracle's BLAS runs with: the thread-count variable if one is set, else the
+    CPUs this process may run on (its affinity mask, not the machine's logical CPU count)."""
+    try:
+        avail = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        avail = os.cpu_count() or 1
     for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
         if os.environ.get(var):
-            return int(os.environ[var])
-    return os.cpu_count() or 1
+            return min(int(os.environ[var]), avail)
+    return avail
 
 
 def nominal_step_flops(wl):

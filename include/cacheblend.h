@@ -23,6 +23,10 @@
  *    call that returns an error has enqueued nothing.  Kernels that detect bad data at run
  *    time (a non-finite deviation score, an index out of range) set a sticky device error
  *    word that cb_sync() returns; they never trap.
+ *  - Row indices: every call that takes a device array of row indices also takes the row
+ *    count of the buffer they index (n_*_rows).  An index outside [0, that count) is not
+ *    followed: the kernel skips that row (its output row is left unwritten), records the
+ *    error and cb_sync() returns CB_ERR_DEVICE.
  *  - Layout: row-major, token-major.  A K or V cache is [n_rows, n_kv_heads * head_dim]
  *    (heads contiguous inside a row).  Hidden rows are [n, d_model].  Weights are stored
  *    output-major, [out_features, in_features], so a projection is y = x W^T.
@@ -111,6 +115,14 @@ int cb_sync(void* stream, double timeout_s);
  * usable.  No trap, no hang. */
 int cb_selftest_wait(int32_t max_polls, int32_t arrive, void* stream);
 
+/* Releases the library's host-side per-device state: the cached SM counts, occupancy and
+ * CTA-pair figures, the kernels' shared-memory attribute flags, the allocation-free entry
+ * point's cached scratch address, and the calling thread's profiler events.  Every later
+ * call rebuilds what it needs, so the library stays usable.  Call it with no library work
+ * in flight (after cb_sync on every stream that ran library calls), e.g. before the
+ * process resets its device context.  Frees no caller memory. */
+void cb_shutdown(void);
+
 /* Device workspace (bytes) large enough for every call below on rows up to n_tok and a
  * selected set of up to m_max rows, for these dims.  Host-only. */
 int cb_workspace_bytes(const cb_dims* dims, int64_t n_tok, int64_t m_max, size_t* out_host);
@@ -141,16 +153,18 @@ int cb_rope_table(float* cos_sin, int32_t max_pos, int32_t head_dim, double base
 /* Re-positions cached keys: k_dst[i] = R(delta[i]) k_src[src_row[i]], and copies values
  * v_dst[i] = v_src[src_row[i]] ([PC] §RoPE position adjustment, k(p) = R(p-p') k(p');
  * [CB-B] position correction when loading chunk KV).
- *   k_src, v_src : [*, Hkv hd] source rows (e.g. a pool of precomputed chunk caches)
- *   src_row      : [n_rows] int32 source row per destination row, or NULL (row i)
+ *   k_src, v_src : [n_src_rows, Hkv hd] source rows (e.g. a pool of precomputed chunk caches)
+ *   src_row      : [n_rows] int32 source row per destination row, each in [0, n_src_rows),
+ *                  or NULL (row i; then n_src_rows >= n_rows)
  *   delta        : [n_rows] int32 position offset p - p', |delta| < max_pos
  *   k_dst, v_dst : [n_rows, Hkv hd]; v_src/v_dst may both be NULL (keys only).
  * In-place (k_dst == k_src) is allowed only with src_row == NULL.  The sources may be
  * pinned host memory mapped at the same device address (read over the host link, no
  * landing copy); any other host pointer is rejected before launch. */
 int cb_rope_shift(void* k_dst, void* v_dst, const void* k_src, const void* v_src,
-                  const int32_t* src_row, const int32_t* delta, int64_t n_rows,
-                  const cb_dims* dims, const float* cos_sin, int32_t max_pos, void* stream);
+                  const int32_t* src_row, int64_t n_src_rows, const int32_t* delta,
+                  int64_t n_rows, const cb_dims* dims, const float* cos_sin, int32_t max_pos,
+                  void* stream);
 
 /* ---- 8-bit chunk KV ([CG] §Step 1 per-channel quantization; entropy coding is not done) */
 
@@ -184,15 +198,17 @@ int cb_rope_shift_q8(void* k_dst, void* v_dst, const uint8_t* k_codes, const uin
  *             (+ the same over V when dev_mode == CB_DEV_KV), fp32 accumulation;
  *   sel       = the k candidates with the largest scores, ties to the lower candidate
  *               index, written ascending as ref_row values (length k).
- *   k_new/v_new : [*, Hkv hd] freshly computed rows; k_ref/v_ref : [*, Hkv hd] the cache
- *   new_row/ref_row : [n_cand] int32 ascending row maps, or NULL (identity)
+ *   k_new/v_new : [n_new_rows, Hkv hd] freshly computed rows
+ *   k_ref/v_ref : [n_ref_rows, Hkv hd] the cache
+ *   new_row/ref_row : [n_cand] int32 ascending row maps into those, or NULL (identity: then
+ *                     the buffer holds at least n_cand rows)
  *   scores : [n_cand] fp32 (output, may be NULL)
  * 0 <= k <= n_cand.  A non-finite score sets CB_ERR_NONFINITE (cb_sync). */
-int cb_kv_deviation_topk(const void* k_new, const void* v_new, const void* k_ref,
-                         const void* v_ref, const int32_t* new_row, const int32_t* ref_row,
-                         int32_t n_cand, int32_t k, int32_t dev_mode, const cb_dims* dims,
-                         float* scores, int32_t* sel, void* ws, size_t ws_bytes,
-                         void* stream);
+int cb_kv_deviation_topk(const void* k_new, const void* v_new, int64_t n_new_rows,
+                         const void* k_ref, const void* v_ref, int64_t n_ref_rows,
+                         const int32_t* new_row, const int32_t* ref_row, int32_t n_cand,
+                         int32_t k, int32_t dev_mode, const cb_dims* dims, float* scores,
+                         int32_t* sel, void* ws, size_t ws_bytes, void* stream);
 
 /* Allocation-free variant of cb_kv_deviation_topk, for callers that cannot hand the
  * library device memory: for example a plugin running inside a host program that owns and
@@ -204,15 +220,18 @@ int cb_kv_deviation_topk(const void* k_new, const void* v_new, const void* k_ref
  * memory, held by every GPU that loads the library until the process exits.
  *   - n_cand is limited to 65536; larger returns CB_ERR_UNSUPPORTED before any launch.
  *   - The first call on a device looks up the array's device address (once per device,
- *     with that device current); make that first call before any stream capture.
+ *     with that device current, in the context current then: the device's primary context
+ *     for callers of the runtime API) and keeps it until cb_shutdown(); make that first
+ *     call before any stream capture, and call cb_shutdown() after resetting the device.
  *   - Every call shares the one array and it keeps the last call's contents: calls that
  *     may overlap on the GPU (different streams, or different host threads, on the same
  *     device) race with each other.  Serialise them. */
-int cb_kv_deviation_topk_noalloc(const void* k_new, const void* v_new, const void* k_ref,
-                                 const void* v_ref, const int32_t* new_row,
-                                 const int32_t* ref_row, int32_t n_cand, int32_t k,
-                                 int32_t dev_mode, const cb_dims* dims, float* scores,
-                                 int32_t* sel, void* stream);
+int cb_kv_deviation_topk_noalloc(const void* k_new, const void* v_new, int64_t n_new_rows,
+                                 const void* k_ref, const void* v_ref, int64_t n_ref_rows,
+                                 const int32_t* new_row, const int32_t* ref_row,
+                                 int32_t n_cand, int32_t k, int32_t dev_mode,
+                                 const cb_dims* dims, float* scores, int32_t* sel,
+                                 void* stream);
 
 /* Top-k of given fp32 scores (>= 0, finite), ties to the lower index, output ascending
  * as cand[c] (cand NULL = c).  The selection step alone, for bit-exact checks. */
@@ -223,34 +242,39 @@ int cb_topk_from_scores(const float* scores, const int32_t* cand, int32_t n_cand
 
 /* RMSNorm of rows: out[i] = x[rows[i]] / sqrt(mean(x[rows[i]]^2) + eps) * gain (rows NULL:
  * row i), the pre-norm of every layer ([CB-A] model: RMSNorm before attention and FFN).
- *   x : [*, d] of dtype_in;  gain : [d] of dtype_in;  out : [n, d] of dtype_out
+ *   x : [n_x_rows, d] of dtype_in;  rows : [n] in [0, n_x_rows), or NULL (n <= n_x_rows)
+ *   gain : [d] of dtype_in;  out : [n, d] of dtype_out
  *   (bf16 -> bf16, bf16 -> fp32 or fp32 -> fp32);  d a multiple of 8.  Sums in fp32. */
-int cb_rmsnorm(void* out, const void* x, const int32_t* rows, int64_t n, int32_t d, const void* gain,
-               float eps, int32_t dtype_in, int32_t dtype_out, void* stream);
+int cb_rmsnorm(void* out, const void* x, int64_t n_x_rows, const int32_t* rows, int64_t n,
+               int32_t d, const void* gain, float eps, int32_t dtype_in, int32_t dtype_out,
+               void* stream);
 
-/* dst[i] = src[idx[i]] for i < n; rows of row_bytes bytes (a multiple of 4); idx NULL
- * means i ([CB-A] §Selective recomputation, Step 1: restrict the input to S).  dst and src
- * must not overlap (rows are copied in parallel, in no fixed order). */
-int cb_gather_rows(void* dst, const void* src, const int32_t* idx, int64_t n,
-                   int64_t row_bytes, void* stream);
+/* dst[i] = src[idx[i]] for i < n; rows of row_bytes bytes (a multiple of 4); src holds
+ * n_src_rows rows and every idx[i] must lie in [0, n_src_rows) (e.g. token ids into an
+ * embedding table of vocab rows); idx NULL means i ([CB-A] §Selective recomputation,
+ * Step 1: restrict the input to S).  dst and src must not overlap (rows are copied in
+ * parallel, in no fixed order). */
+int cb_gather_rows(void* dst, const void* src, int64_t n_src_rows, const int32_t* idx,
+                   int64_t n, int64_t row_bytes, void* stream);
 
 /* KV expansion ([CB-A] §Selective recomputation, Step 3: K_new = Concat(K_pre[not S],
  * K_recomp[S])):  k_cache[dst_idx[i]] = k_rows[src_idx[i]] and the same for V, i < n.
- * src_idx NULL means i.  Rows are [Hkv hd].  The caches must not overlap the row
- * buffers (rows are copied in parallel, in no fixed order). */
-int cb_scatter_kv(void* k_cache, void* v_cache, const void* k_rows, const void* v_rows,
-                  const int32_t* dst_idx, const int32_t* src_idx, int64_t n,
-                  const cb_dims* dims, void* stream);
+ * Rows are [Hkv hd]; the caches hold n_cache_rows rows, the row buffers n_src_rows rows;
+ * dst_idx[i] < n_cache_rows, src_idx[i] < n_src_rows (src_idx NULL means i).  The caches
+ * must not overlap the row buffers (rows are copied in parallel, in no fixed order). */
+int cb_scatter_kv(void* k_cache, void* v_cache, int64_t n_cache_rows, const void* k_rows,
+                  const void* v_rows, int64_t n_src_rows, const int32_t* dst_idx,
+                  const int32_t* src_idx, int64_t n, const cb_dims* dims, void* stream);
 
 /* ---- selective layer pieces --------------------------------------------------------- */
 
 /* Q/K/V of selected rows ([CB-A] §Selective recomputation, Step 2; [CB-B] §技術の仕組み):
  *   a = RMSNorm(x[rows[i]]) * attn_norm;  q = a Wq^T, k = a Wk^T, v = a Wv^T;
  *   RoPE on q and k at position pos[i].
- *   x : [*, d];  rows : [M] int32 or NULL (i);  pos : [M] int32 (< max_pos)
- *   q : [M, H hd] or NULL;  k, v : [M, Hkv hd] or both NULL. */
-int cb_selective_qkv(const void* x, const int32_t* rows, const int32_t* pos, int32_t M,
-                     const cb_dims* dims, const cb_layer_w* w, const float* cos_sin,
+ *   x : [n_x_rows, d];  rows : [M] int32 in [0, n_x_rows), or NULL (i; M <= n_x_rows)
+ *   pos : [M] int32 (< max_pos);  q : [M, H hd] or NULL;  k, v : [M, Hkv hd] or both NULL. */
+int cb_selective_qkv(const void* x, int64_t n_x_rows, const int32_t* rows, const int32_t* pos,
+                     int32_t M, const cb_dims* dims, const cb_layer_w* w, const float* cos_sin,
                      int32_t max_pos, void* q, void* k, void* v, void* ws, size_t ws_bytes,
                      void* stream);
 
@@ -276,7 +300,8 @@ int cb_o_proj_ffn(const void* attn, const void* x_res, int32_t M, const cb_dims*
  * chunk caches already re-positioned into k_cache/v_cache ([n_tok, Hkv hd], updated in
  * place); rows >= n_cached are the uncached suffix.  Forced rows F = [n_cached, n_tok)
  * plus row n_tok-1 are always recomputed.
- *   x_in [m_in, d] : hidden rows of the incoming set s_in (ascending; NULL = 0..m_in-1)
+ *   x_in [m_in, d] : hidden rows of the incoming set s_in (ascending, each in [0, n_tok);
+ *                    NULL = 0..m_in-1; a row outside is not followed, see Row indices)
  *   mode PRECHECK  : all rows (m_in == n_tok); Q for every row, K/V only for rows
  *                    >= n_cached; output all rows.
  *   mode CHECK     : all rows in; K/V for every row; deviation over the cached,

@@ -62,15 +62,16 @@ _PROTOS = {
     "cb_gradual_ratio": (C.c_double, [C.c_double, _I32, _I32, C.c_double]),
     "cb_load_controller_ratio": (C.c_double, [C.c_double, C.c_double, C.c_double]),
     "cb_rope_table": (C.c_int, [_P, _I32, _I32, C.c_double, _P]),
-    "cb_rope_shift": (C.c_int, [_P, _P, _P, _P, _P, _P, _I64, C.POINTER(cb_dims), _P, _I32, _P]),
-    "cb_kv_deviation_topk": (C.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, C.POINTER(cb_dims),
+    "cb_shutdown": (None, []),
+    "cb_rope_shift": (C.c_int, [_P, _P, _P, _P, _P, _I64, _P, _I64, C.POINTER(cb_dims), _P, _I32, _P]),
+    "cb_kv_deviation_topk": (C.c_int, [_P, _P, _I64, _P, _P, _I64, _P, _P, _I32, _I32, _I32, C.POINTER(cb_dims),
                                        _P, _P, _P, _SZ, _P]),
-    "cb_kv_deviation_topk_noalloc": (C.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, C.POINTER(cb_dims),
-                                               _P, _P, _P]),
+    "cb_kv_deviation_topk_noalloc": (C.c_int, [_P, _P, _I64, _P, _P, _I64, _P, _P, _I32, _I32, _I32,
+                                               C.POINTER(cb_dims), _P, _P, _P]),
     "cb_topk_from_scores": (C.c_int, [_P, _P, _I32, _I32, _P, _P, _SZ, _P]),
-    "cb_gather_rows": (C.c_int, [_P, _P, _P, _I64, _I64, _P]),
-    "cb_scatter_kv": (C.c_int, [_P, _P, _P, _P, _P, _P, _I64, C.POINTER(cb_dims), _P]),
-    "cb_selective_qkv": (C.c_int, [_P, _P, _P, _I32, C.POINTER(cb_dims), C.POINTER(cb_layer_w), _P, _I32,
+    "cb_gather_rows": (C.c_int, [_P, _P, _I64, _P, _I64, _I64, _P]),
+    "cb_scatter_kv": (C.c_int, [_P, _P, _I64, _P, _P, _I64, _P, _P, _I64, C.POINTER(cb_dims), _P]),
+    "cb_selective_qkv": (C.c_int, [_P, _I64, _P, _P, _I32, C.POINTER(cb_dims), C.POINTER(cb_layer_w), _P, _I32,
                                    _P, _P, _P, _P, _SZ, _P]),
     "cb_partial_attention": (C.c_int, [_P, _P, _I32, _P, _P, _I64, C.POINTER(cb_dims), _P, _P, _SZ, _P]),
     "cb_o_proj_ffn": (C.c_int, [_P, _P, _I32, C.POINTER(cb_dims), C.POINTER(cb_layer_w), _P, _P, _SZ, _P]),
@@ -85,7 +86,7 @@ _PROTOS = {
     "cb_file_read": (C.c_int, [C.c_char_p, C.c_uint64, _P, _SZ, _I32]),
     "cb_selftest_wait": (C.c_int, [_I32, _I32, _P]),
     "cb_copy_async": (C.c_int, [_P, _P, _SZ, _P]),
-    "cb_rmsnorm": (C.c_int, [_P, _P, _P, _I64, _I32, _P, C.c_float, _I32, _I32, _P]),
+    "cb_rmsnorm": (C.c_int, [_P, _P, _I64, _P, _I64, _I32, _P, C.c_float, _I32, _I32, _P]),
     "cb_io_error_message": (C.c_char_p, []),
     "cb_rope_shift_q8": (C.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _I32, _P, _I64,
                                    C.POINTER(cb_dims), _P, _I32, _P]),
@@ -164,32 +165,51 @@ def cb_sync(stream=None, timeout_s: float = 60.0) -> None:
     _check("cb_sync", lib().cb_sync(_stream(stream), timeout_s))
 
 
+def cb_shutdown() -> None:
+    lib().cb_shutdown()
+
+
+def _rows(t, n: Optional[int]) -> int:
+    """Row count of a buffer for the index checks: given, or the tensor's first dimension."""
+    if n is not None:
+        return int(n)
+    if t is None or isinstance(t, int):
+        raise ValueError("the row count of a raw pointer must be given")
+    return int(t.shape[0])
+
+
 # ---- device entry points --------------------------------------------------------------------
 def cb_rope_table(cos_sin, max_pos: int, head_dim: int, base: float, stream=None):
     _check("cb_rope_table", lib().cb_rope_table(_ptr(cos_sin), max_pos, head_dim, base, _stream(stream)))
 
 
 def cb_rope_shift(k_dst, v_dst, k_src, v_src, src_row, delta, n_rows: int, dims: cb_dims, cos_sin,
-                  max_pos: int, stream=None):
+                  max_pos: int, stream=None, n_src_rows: Optional[int] = None):
+    """n_src_rows: rows of k_src/v_src (default: k_src's first dimension)."""
     _check("cb_rope_shift", lib().cb_rope_shift(_ptr(k_dst), _ptr(v_dst), _ptr(k_src), _ptr(v_src),
-                                                _ptr(src_row), _ptr(delta), n_rows, C.byref(dims),
-                                                _ptr(cos_sin), max_pos, _stream(stream)))
+                                                _ptr(src_row), _rows(k_src, n_src_rows), _ptr(delta), n_rows,
+                                                C.byref(dims), _ptr(cos_sin), max_pos, _stream(stream)))
 
 
 def cb_kv_deviation_topk(k_new, v_new, k_ref, v_ref, new_row, ref_row, n_cand: int, k: int, dev_mode: int,
-                         dims: cb_dims, scores, sel, ws, stream=None):
+                         dims: cb_dims, scores, sel, ws, stream=None, n_new_rows: Optional[int] = None,
+                         n_ref_rows: Optional[int] = None):
+    """n_new_rows / n_ref_rows: rows of k_new and k_ref (default: their first dimension)."""
     _check("cb_kv_deviation_topk", lib().cb_kv_deviation_topk(
-        _ptr(k_new), _ptr(v_new), _ptr(k_ref), _ptr(v_ref), _ptr(new_row), _ptr(ref_row), n_cand, k,
-        dev_mode, C.byref(dims), _ptr(scores), _ptr(sel), _ptr(ws), _nbytes(ws), _stream(stream)))
+        _ptr(k_new), _ptr(v_new), _rows(k_new, n_new_rows), _ptr(k_ref), _ptr(v_ref), _rows(k_ref, n_ref_rows),
+        _ptr(new_row), _ptr(ref_row), n_cand, k, dev_mode, C.byref(dims), _ptr(scores), _ptr(sel), _ptr(ws),
+        _nbytes(ws), _stream(stream)))
 
 
 def cb_kv_deviation_topk_noalloc(k_new, v_new, k_ref, v_ref, new_row, ref_row, n_cand: int, k: int,
-                                 dev_mode: int, dims: cb_dims, scores, sel, stream=None):
+                                 dev_mode: int, dims: cb_dims, scores, sel, stream=None,
+                                 n_new_rows: Optional[int] = None, n_ref_rows: Optional[int] = None):
     """Same as cb_kv_deviation_topk, with the scratch in the library's fixed device array
     (for callers that cannot allocate; at most 65536 candidates; overlapping calls race)."""
     _check("cb_kv_deviation_topk_noalloc", lib().cb_kv_deviation_topk_noalloc(
-        _ptr(k_new), _ptr(v_new), _ptr(k_ref), _ptr(v_ref), _ptr(new_row), _ptr(ref_row), n_cand, k,
-        dev_mode, C.byref(dims), _ptr(scores), _ptr(sel), _stream(stream)))
+        _ptr(k_new), _ptr(v_new), _rows(k_new, n_new_rows), _ptr(k_ref), _ptr(v_ref), _rows(k_ref, n_ref_rows),
+        _ptr(new_row), _ptr(ref_row), n_cand, k, dev_mode, C.byref(dims), _ptr(scores), _ptr(sel),
+        _stream(stream)))
 
 
 def cb_topk_from_scores(scores, cand, n_cand: int, k: int, sel, ws, stream=None):
@@ -197,22 +217,25 @@ def cb_topk_from_scores(scores, cand, n_cand: int, k: int, sel, ws, stream=None)
                                                             _ptr(ws), _nbytes(ws), _stream(stream)))
 
 
-def cb_gather_rows(dst, src, idx, n: int, row_bytes: int, stream=None):
-    _check("cb_gather_rows", lib().cb_gather_rows(_ptr(dst), _ptr(src), _ptr(idx), n, row_bytes,
-                                                  _stream(stream)))
+def cb_gather_rows(dst, src, idx, n: int, row_bytes: int, stream=None, n_src_rows: Optional[int] = None):
+    """n_src_rows: rows of src that idx may address (default: src's first dimension)."""
+    _check("cb_gather_rows", lib().cb_gather_rows(_ptr(dst), _ptr(src), _rows(src, n_src_rows), _ptr(idx), n,
+                                                  row_bytes, _stream(stream)))
 
 
-def cb_scatter_kv(k_cache, v_cache, k_rows, v_rows, dst_idx, src_idx, n: int, dims: cb_dims, stream=None):
-    _check("cb_scatter_kv", lib().cb_scatter_kv(_ptr(k_cache), _ptr(v_cache), _ptr(k_rows), _ptr(v_rows),
+def cb_scatter_kv(k_cache, v_cache, k_rows, v_rows, dst_idx, src_idx, n: int, dims: cb_dims, stream=None,
+                  n_cache_rows: Optional[int] = None, n_src_rows: Optional[int] = None):
+    _check("cb_scatter_kv", lib().cb_scatter_kv(_ptr(k_cache), _ptr(v_cache), _rows(k_cache, n_cache_rows),
+                                                _ptr(k_rows), _ptr(v_rows), _rows(k_rows, n_src_rows),
                                                 _ptr(dst_idx), _ptr(src_idx), n, C.byref(dims),
                                                 _stream(stream)))
 
 
 def cb_selective_qkv(x, rows, pos, M: int, dims: cb_dims, w: cb_layer_w, cos_sin, max_pos: int, q, k, v,
-                     ws, stream=None):
+                     ws, stream=None, n_x_rows: Optional[int] = None):
     _check("cb_selective_qkv", lib().cb_selective_qkv(
-        _ptr(x), _ptr(rows), _ptr(pos), M, C.byref(dims), C.byref(w), _ptr(cos_sin), max_pos, _ptr(q),
-        _ptr(k), _ptr(v), _ptr(ws), _nbytes(ws), _stream(stream)))
+        _ptr(x), _rows(x, n_x_rows), _ptr(rows), _ptr(pos), M, C.byref(dims), C.byref(w), _ptr(cos_sin), max_pos,
+        _ptr(q), _ptr(k), _ptr(v), _ptr(ws), _nbytes(ws), _stream(stream)))
 
 
 def cb_partial_attention(q, q_pos, M: int, k_cache, v_cache, n_kv: int, dims: cb_dims, out, ws=None,
@@ -276,9 +299,10 @@ def cb_file_read(path: str, offset: int, dst, nbytes: int, n_threads: int = 8):
         raise CBError("cb_file_read", st, lib().cb_io_error_message().decode(errors="replace"))
 
 
-def cb_rmsnorm(out, x, rows, n: int, d: int, gain, eps: float, dtype_in: int, dtype_out: int, stream=None):
-    _check("cb_rmsnorm", lib().cb_rmsnorm(_ptr(out), _ptr(x), _ptr(rows), n, d, _ptr(gain), eps, dtype_in,
-                                          dtype_out, _stream(stream)))
+def cb_rmsnorm(out, x, rows, n: int, d: int, gain, eps: float, dtype_in: int, dtype_out: int, stream=None,
+               n_x_rows: Optional[int] = None):
+    _check("cb_rmsnorm", lib().cb_rmsnorm(_ptr(out), _ptr(x), _rows(x, n_x_rows), _ptr(rows), n, d, _ptr(gain),
+                                          eps, dtype_in, dtype_out, _stream(stream)))
 
 
 def cb_copy_async(dst, src, nbytes: int, stream=None):

@@ -17,7 +17,6 @@
 namespace cb {
 uint32_t take_error_gemm_tc();
 uint32_t take_error_attn_tc();
-cudaError_t launch_gemm_simt_bf16(const GemmDesc& g, cudaStream_t s);
 }  // namespace cb
 
 using namespace cb;
@@ -116,19 +115,21 @@ double gemm_bytes(int dt, const GemmDesc& g) {
   } while (0)
 #define L_IOTA(out, n, start, s) \
   CB_LAUNCH(CB_PROF_INDEX, 0, (n), 0, 0, 0.0, 4.0 * (n), s, launch_iota(out, n, start, s))
-#define L_RMSNORM(dti, dto, out, x, rows, g, n, d, eps, s)                                       \
+#define L_RMSNORM(dti, dto, out, x, rows, g, n, d, eps, s) L_RMSNORM_B(dti, dto, out, x, rows, -1, g, n, d, eps, s)
+#define L_RMSNORM_B(dti, dto, out, x, rows, nsrc, g, n, d, eps, s)                               \
   CB_LAUNCH(CB_PROF_RMSNORM, 0, (n), (d), 0, 3.0 * (n) * (d),                                    \
-            (double)(n) * (d) * (esize(dti) + esize(dto)), s, launch_rmsnorm(dti, dto, out, x, rows, g, n, d, eps, s))
+            (double)(n) * (d) * (esize(dti) + esize(dto)), s,                                    \
+            launch_rmsnorm(dti, dto, out, x, rows, nsrc, g, n, d, eps, s))
 #define L_ATTN(dt, q, qpos, M, kc, vc, nkv, H, Hkv, hd, out, ws, wsb, s)                         \
   CB_LAUNCH(CB_PROF_ATTENTION, 0, (M), (nkv), (H), 0.0, 0.0, s,                                  \
             launch_attention(dt, q, qpos, M, kc, vc, nkv, H, Hkv, hd, out, ws, wsb, s))
 #define L_COPY(dst, di, src, si, n, rb, db, sb, s)                                               \
   CB_LAUNCH(CB_PROF_COPY_ROWS, 0, (n), (rb), 0, 0.0, 2.0 * (n) * (rb), s,                        \
             launch_copy_rows(dst, di, src, si, n, rb, db, sb, s))
-#define L_DEV(dt, kn, vn, kr, vr, nr, rr, nc, W, usev, sc, s)                                    \
+#define L_DEV(dt, kn, vn, kr, vr, nr, rr, nc, nnew, nref, W, usev, sc, s)                       \
   CB_LAUNCH(CB_PROF_DEVIATION, 0, (nc), (W), (usev), 3.0 * (nc) * (W) * ((usev) ? 2 : 1),        \
             (double)(nc) * (W) * esize(dt) * ((usev) ? 4 : 2) + 4.0 * (nc), s,                   \
-            launch_deviation(dt, kn, vn, kr, vr, nr, rr, nc, W, usev, sc, s))
+            launch_deviation(dt, kn, vn, kr, vr, nr, rr, nc, nnew, nref, W, usev, sc, s))
 #define L_DEVRED(part, plo, np, ld, nc, cpos, W, usev, sc, s)                                    \
   CB_LAUNCH(CB_PROF_DEVIATION, 1, (nc), (W), (usev), (double)(nc) * ((np) - (plo)),                 \
             4.0 * (nc) * ((np) - (plo) + 1), s, launch_dev_reduce(part, plo, np, ld, nc, cpos, sc, s))
@@ -150,10 +151,10 @@ double gemm_bytes(int dt, const GemmDesc& g) {
             launch_build_sel(ord, k, cr, f0, fp0, nf, so, ko, s))
 #define L_R2P(rows, k, sin, m, out, s) \
   CB_LAUNCH(CB_PROF_INDEX, 0, (k), 0, 0, 0.0, 8.0 * (k), s, launch_rows_to_positions(rows, k, sin, m, out, s))
-#define L_ROPE_SHIFT(dt, kd, vd, ks, vs, sr, dl, n, W, hd, tab, mp, s)                           \
+#define L_ROPE_SHIFT(dt, kd, vd, ks, vs, sr, nsrc, dl, n, W, hd, tab, mp, s)                     \
   CB_LAUNCH(CB_PROF_ROPE_SHIFT, 0, (n), (W), 0, 3.0 * (n) * (W),                                 \
             (double)(n) * (W) * esize(dt) * ((vd) ? 4 : 2) + 4.0 * (n), s,                       \
-            launch_rope_shift(dt, kd, vd, ks, vs, sr, dl, n, W, hd, tab, mp, s))
+            launch_rope_shift(dt, kd, vd, ks, vs, sr, nsrc, dl, n, W, hd, tab, mp, s))
 #define L_LMGEMV(dt, lg, hn, w, V, d, bb, s)                                                     \
   CB_LAUNCH(CB_PROF_LMHEAD, 0, (V), (d), 0, 2.0 * (V) * (d), (double)(V) * (d) * esize(dt) + 4.0 * (V), s, \
             launch_lm_gemv(dt, lg, hn, w, V, d, bb, s))
@@ -474,19 +475,21 @@ int cb_rope_table(float* cos_sin, int32_t max_pos, int32_t head_dim, double base
 }
 
 int cb_rope_shift(void* k_dst, void* v_dst, const void* k_src, const void* v_src, const int32_t* src_row,
-                  const int32_t* delta, int64_t n_rows, const cb_dims* dims, const float* cos_sin,
-                  int32_t max_pos, void* stream) {
+                  int64_t n_src_rows, const int32_t* delta, int64_t n_rows, const cb_dims* dims,
+                  const float* cos_sin, int32_t max_pos, void* stream) {
   int st = check_dims(dims);
   if (st) return st;
-  if (n_rows < 0) return fail(CB_ERR_SHAPE, "n_rows < 0");
+  if (n_rows < 0 || n_src_rows < 0) return fail(CB_ERR_SHAPE, "n_rows < 0 or n_src_rows < 0");
   if (n_rows == 0) return CB_OK;
+  if (!src_row && n_src_rows < n_rows) return fail(CB_ERR_SHAPE, "n_src_rows < n_rows with src_row NULL");
   if (!k_dst || !k_src || !delta || !cos_sin || max_pos < 1)
     return fail(CB_ERR_INVALID_ARG, "rope_shift pointer is NULL");
   if ((v_dst == nullptr) != (v_src == nullptr)) return fail(CB_ERR_INVALID_ARG, "v_dst/v_src must both be set or NULL");
   if (k_dst == k_src && src_row) return fail(CB_ERR_INVALID_ARG, "in-place shift needs src_row == NULL");
   if ((st = check_readable(k_src, "k_src")) || (st = check_readable(v_src, "v_src"))) return st;
   const int W = dims->n_kv_heads * dims->head_dim;
-  L_ROPE_SHIFT(dims->dtype, k_dst, v_dst, k_src, v_src, src_row, delta, n_rows, W, dims->head_dim, cos_sin, max_pos, S(stream));
+  L_ROPE_SHIFT(dims->dtype, k_dst, v_dst, k_src, v_src, src_row, n_src_rows, delta, n_rows, W, dims->head_dim, cos_sin,
+               max_pos, S(stream));
   return CB_OK;
 }
 
@@ -527,13 +530,24 @@ int cb_rope_shift_q8(void* k_dst, void* v_dst, const uint8_t* k_codes, const uin
   return CB_OK;
 }
 
-int cb_kv_deviation_topk(const void* k_new, const void* v_new, const void* k_ref, const void* v_ref,
-                         const int32_t* new_row, const int32_t* ref_row, int32_t n_cand, int32_t k,
-                         int32_t dev_mode, const cb_dims* dims, float* scores, int32_t* sel, void* ws,
-                         size_t ws_bytes, void* stream) {
+// row counts of the new and cached K/V: with a row map every index is checked on the device;
+// without one the candidates are rows 0..n_cand-1, which must exist
+int check_dev_rows(const int32_t* new_row, const int32_t* ref_row, int32_t n_cand, int64_t n_new_rows,
+                   int64_t n_ref_rows) {
+  if (n_new_rows < 0 || n_ref_rows < 0) return fail(CB_ERR_SHAPE, "negative row count");
+  if ((!new_row && n_new_rows < n_cand) || (!ref_row && n_ref_rows < n_cand))
+    return fail(CB_ERR_SHAPE, "fewer rows than candidates without a row map");
+  return CB_OK;
+}
+
+int cb_kv_deviation_topk(const void* k_new, const void* v_new, int64_t n_new_rows, const void* k_ref,
+                         const void* v_ref, int64_t n_ref_rows, const int32_t* new_row, const int32_t* ref_row,
+                         int32_t n_cand, int32_t k, int32_t dev_mode, const cb_dims* dims, float* scores,
+                         int32_t* sel, void* ws, size_t ws_bytes, void* stream) {
   int st = check_dims(dims);
   if (st) return st;
   if (n_cand < 0 || k < 0 || k > n_cand) return fail(CB_ERR_SHAPE, "need 0 <= k <= n_cand");
+  if ((st = check_dev_rows(new_row, ref_row, n_cand, n_new_rows, n_ref_rows))) return st;
   if (dev_mode != CB_DEV_KV && dev_mode != CB_DEV_K) return fail(CB_ERR_INVALID_ARG, "dev_mode");
   if (n_cand == 0) return CB_OK;
   if (!k_new || !k_ref || (dev_mode == CB_DEV_KV && (!v_new || !v_ref)) || (k > 0 && !sel))
@@ -544,7 +558,8 @@ int cb_kv_deviation_topk(const void* k_new, const void* v_new, const void* k_ref
   float* sc = scores ? scores : static_cast<float*>(c.take((size_t)n_cand * 4));
   int32_t* ord = static_cast<int32_t*>(c.take((size_t)n_cand * 4));
   const int W = dims->n_kv_heads * dims->head_dim;
-  L_DEV(dims->dtype, k_new, v_new, k_ref, v_ref, new_row, ref_row, n_cand, W, dev_mode == CB_DEV_KV, sc, S(stream));
+  L_DEV(dims->dtype, k_new, v_new, k_ref, v_ref, new_row, ref_row, n_cand, n_new_rows, n_ref_rows, W,
+        dev_mode == CB_DEV_KV, sc, S(stream));
   if (k > 0) {
     L_TOPK(sc, n_cand, k, ord, S(stream));
     L_MAP(ord, k, ref_row, sel, S(stream));
@@ -552,12 +567,14 @@ int cb_kv_deviation_topk(const void* k_new, const void* v_new, const void* k_ref
   return CB_OK;
 }
 
-int cb_kv_deviation_topk_noalloc(const void* k_new, const void* v_new, const void* k_ref, const void* v_ref,
-                                 const int32_t* new_row, const int32_t* ref_row, int32_t n_cand, int32_t k,
-                                 int32_t dev_mode, const cb_dims* dims, float* scores, int32_t* sel, void* stream) {
+int cb_kv_deviation_topk_noalloc(const void* k_new, const void* v_new, int64_t n_new_rows, const void* k_ref,
+                                 const void* v_ref, int64_t n_ref_rows, const int32_t* new_row,
+                                 const int32_t* ref_row, int32_t n_cand, int32_t k, int32_t dev_mode,
+                                 const cb_dims* dims, float* scores, int32_t* sel, void* stream) {
   int st = check_dims(dims);
   if (st) return st;
   if (n_cand < 0 || k < 0 || k > n_cand) return fail(CB_ERR_SHAPE, "need 0 <= k <= n_cand");
+  if ((st = check_dev_rows(new_row, ref_row, n_cand, n_new_rows, n_ref_rows))) return st;
   if (n_cand > noalloc_max_candidates())
     return fail(CB_ERR_UNSUPPORTED, "n_cand %d exceeds the fixed scratch of %d candidates", n_cand,
                 noalloc_max_candidates());
@@ -566,8 +583,9 @@ int cb_kv_deviation_topk_noalloc(const void* k_new, const void* v_new, const voi
   if (!k_new || !k_ref || (dev_mode == CB_DEV_KV && (!v_new || !v_ref)) || (k > 0 && !sel))
     return fail(CB_ERR_INVALID_ARG, "deviation pointer is NULL");
   const int W = dims->n_kv_heads * dims->head_dim;
-  CB_CUDA(launch_deviation_topk_noalloc(dims->dtype, k_new, v_new, k_ref, v_ref, new_row, ref_row, n_cand, k, W,
-                                        dev_mode == CB_DEV_KV, scores, sel, S(stream)));
+  CB_CUDA(launch_deviation_topk_noalloc(dims->dtype, k_new, v_new, k_ref, v_ref, new_row, ref_row, n_cand,
+                                        n_new_rows, n_ref_rows, k, W, dev_mode == CB_DEV_KV, scores, sel,
+                                        S(stream)));
   g_launches.fetch_add(k > 0 ? 3 : 1, std::memory_order_relaxed);
   return CB_OK;
 }
@@ -586,53 +604,60 @@ int cb_topk_from_scores(const float* scores, const int32_t* cand, int32_t n_cand
   return CB_OK;
 }
 
-int cb_rmsnorm(void* out, const void* x, const int32_t* rows, int64_t n, int32_t d, const void* gain, float eps,
-               int32_t dtype_in, int32_t dtype_out, void* stream) {
+int cb_rmsnorm(void* out, const void* x, int64_t n_x_rows, const int32_t* rows, int64_t n, int32_t d,
+               const void* gain, float eps, int32_t dtype_in, int32_t dtype_out, void* stream) {
   if ((dtype_in != CB_F32 && dtype_in != CB_BF16) || (dtype_out != CB_F32 && dtype_out != CB_BF16) ||
       (dtype_in == CB_F32 && dtype_out == CB_BF16))
     return fail(CB_ERR_DTYPE, "rmsnorm dtypes %d -> %d", dtype_in, dtype_out);
-  if (n < 0 || d < 8 || d % 8 || !(eps >= 0.0f)) return fail(CB_ERR_SHAPE, "rmsnorm n/d/eps");
+  if (n < 0 || n_x_rows < 0 || d < 8 || d % 8 || !(eps >= 0.0f)) return fail(CB_ERR_SHAPE, "rmsnorm n/d/eps");
   if (n == 0) return CB_OK;
+  if (!rows && n_x_rows < n) return fail(CB_ERR_SHAPE, "n_x_rows < n with rows NULL");
   if (!out || !x || !gain) return fail(CB_ERR_INVALID_ARG, "rmsnorm pointer is NULL");
-  L_RMSNORM(dtype_in, dtype_out, out, x, rows, gain, n, d, eps, S(stream));
+  L_RMSNORM_B(dtype_in, dtype_out, out, x, rows, n_x_rows, gain, n, d, eps, S(stream));
   return CB_OK;
 }
 
-int cb_gather_rows(void* dst, const void* src, const int32_t* idx, int64_t n, int64_t row_bytes, void* stream) {
-  if (n < 0 || row_bytes < 0 || row_bytes % 4) return fail(CB_ERR_SHAPE, "n/row_bytes");
+int cb_gather_rows(void* dst, const void* src, int64_t n_src_rows, const int32_t* idx, int64_t n, int64_t row_bytes,
+                   void* stream) {
+  if (n < 0 || n_src_rows < 0 || row_bytes < 0 || row_bytes % 4) return fail(CB_ERR_SHAPE, "n/n_src_rows/row_bytes");
   if (n == 0) return CB_OK;
+  if (!idx && n_src_rows < n) return fail(CB_ERR_SHAPE, "n_src_rows < n with idx NULL");
   if (!dst || !src) return fail(CB_ERR_INVALID_ARG, "gather pointer is NULL");
-  L_COPY(dst, nullptr, src, idx, n, row_bytes, -1, -1, S(stream));
+  L_COPY(dst, nullptr, src, idx, n, row_bytes, n, n_src_rows, S(stream));
   return CB_OK;
 }
 
-int cb_scatter_kv(void* k_cache, void* v_cache, const void* k_rows, const void* v_rows, const int32_t* dst_idx,
-                  const int32_t* src_idx, int64_t n, const cb_dims* dims, void* stream) {
+int cb_scatter_kv(void* k_cache, void* v_cache, int64_t n_cache_rows, const void* k_rows, const void* v_rows,
+                  int64_t n_src_rows, const int32_t* dst_idx, const int32_t* src_idx, int64_t n,
+                  const cb_dims* dims, void* stream) {
   int st = check_dims(dims);
   if (st) return st;
-  if (n < 0) return fail(CB_ERR_SHAPE, "n < 0");
+  if (n < 0 || n_cache_rows < 0 || n_src_rows < 0) return fail(CB_ERR_SHAPE, "negative size");
   if (n == 0) return CB_OK;
+  if (!src_idx && n_src_rows < n) return fail(CB_ERR_SHAPE, "n_src_rows < n with src_idx NULL");
   if (!k_cache || !k_rows || !dst_idx || ((v_cache == nullptr) != (v_rows == nullptr)))
     return fail(CB_ERR_INVALID_ARG, "scatter pointer is NULL");
   const int64_t rb = (int64_t)dims->n_kv_heads * dims->head_dim * esize(dims->dtype);
-  L_COPY(k_cache, dst_idx, k_rows, src_idx, n, rb, -1, -1, S(stream));
-  if (v_cache) L_COPY(v_cache, dst_idx, v_rows, src_idx, n, rb, -1, -1, S(stream));
+  L_COPY(k_cache, dst_idx, k_rows, src_idx, n, rb, n_cache_rows, n_src_rows, S(stream));
+  if (v_cache) L_COPY(v_cache, dst_idx, v_rows, src_idx, n, rb, n_cache_rows, n_src_rows, S(stream));
   return CB_OK;
 }
 
-int cb_selective_qkv(const void* x, const int32_t* rows, const int32_t* pos, int32_t M, const cb_dims* dims,
-                     const cb_layer_w* w, const float* cos_sin, int32_t max_pos, void* q, void* k, void* v,
-                     void* ws, size_t ws_bytes, void* stream) {
+int cb_selective_qkv(const void* x, int64_t n_x_rows, const int32_t* rows, const int32_t* pos, int32_t M,
+                     const cb_dims* dims, const cb_layer_w* w, const float* cos_sin, int32_t max_pos, void* q,
+                     void* k, void* v, void* ws, size_t ws_bytes, void* stream) {
   int st = check_dims(dims);
   if (st || (st = check_w(w))) return st;
-  if (M < 0) return fail(CB_ERR_SHAPE, "M < 0");
+  if (M < 0 || n_x_rows < 0) return fail(CB_ERR_SHAPE, "M < 0 or n_x_rows < 0");
   if (M == 0) return CB_OK;
+  if (!rows && n_x_rows < M) return fail(CB_ERR_SHAPE, "n_x_rows < M with rows NULL");
   if (!x || !pos || !cos_sin || (!q && !k) || ((k == nullptr) != (v == nullptr)))
     return fail(CB_ERR_INVALID_ARG, "selective_qkv pointer is NULL");
   LayerWs L;
   if ((st = need_ws(dims, M, M, ws, ws_bytes, &L))) return st;
   const int qc = dims->n_heads * dims->head_dim, W = dims->n_kv_heads * dims->head_dim;
-  L_RMSNORM(dims->dtype, dims->dtype, L.a, x, rows, w->attn_norm, M, dims->d_model, dims->rms_eps, S(stream));
+  L_RMSNORM_B(dims->dtype, dims->dtype, L.a, x, rows, n_x_rows, w->attn_norm, M, dims->d_model, dims->rms_eps,
+              S(stream));
   const int col0 = q ? 0 : qc;
   const int ncols = (q ? qc : 0) + (k ? 2 * W : 0);
   L_GEMM(dims->dtype, qkv_desc(dims, w, L.a, M, col0, ncols, q, k, v, pos, nullptr, cos_sin, max_pos), S(stream));
@@ -711,7 +736,9 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
       if (opts && opts->recompute_kv) {
         // every row's Q, K and V in one GEMM; the cached rows are overwritten, not read
         WAIT_CACHED_ROWS();
-        L_GEMM(dims->dtype, qkv_desc(dims, w, L.a, N, 0, qc + 2 * W, L.q, k_cache, v_cache, s_out, s_out, cos_sin, max_pos), s);
+        GemmDesc g = qkv_desc(dims, w, L.a, N, 0, qc + 2 * W, L.q, k_cache, v_cache, s_out, s_out, cos_sin, max_pos);
+        g.epi.kv_bound = N;
+        L_GEMM(dims->dtype, g, s);
         L_ATTN(dims->dtype, L.q, s_out, N, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
         return o_ffn(dims, w, L.attn, x_in, N, x_out, L, s);
       }
@@ -723,11 +750,15 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         // K/V of the forced rows, wherever they are: gather their normalised rows first
         L_SPLIT(nullptr, N, fmask, N, n_forced, L.cpos, L.crows, L.fpos, L.frows, s);
         L_COPY(L.ag, nullptr, L.a, L.frows, n_forced, (int64_t)dims->d_model * B, n_forced, N, s);
-        L_GEMM2(dims->dtype, gq, qkv_desc(dims, w, L.ag, n_forced, qc, 2 * W, nullptr, k_cache, v_cache, L.frows, L.frows, cos_sin, max_pos), s);
+        GemmDesc gkv = qkv_desc(dims, w, L.ag, n_forced, qc, 2 * W, nullptr, k_cache, v_cache, L.frows, L.frows, cos_sin, max_pos);
+        gkv.epi.kv_bound = N;
+        L_GEMM2(dims->dtype, gq, gkv, s);
       } else if (N > kv0) {
         const int nu = N - kv0;
         const void* a_u = static_cast<const char*>(L.a) + (size_t)kv0 * dims->d_model * B;
-        L_GEMM2(dims->dtype, gq, qkv_desc(dims, w, a_u, nu, qc, 2 * W, nullptr, k_cache, v_cache, s_out + kv0, s_out + kv0, cos_sin, max_pos), s);
+        GemmDesc gkv = qkv_desc(dims, w, a_u, nu, qc, 2 * W, nullptr, k_cache, v_cache, s_out + kv0, s_out + kv0, cos_sin, max_pos);
+        gkv.epi.kv_bound = N;
+        L_GEMM2(dims->dtype, gq, gkv, s);
       } else {
         L_GEMM(dims->dtype, gq, s);
       }
@@ -787,7 +818,7 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         L_DEVRED(L.dev_part, q_all ? 2 * (qc / bn) : 0, dev_parts(ncols, bn), m_in, n_cand, cpos, W, use_v, sc, s);
       } else {
         L_GEMM(dims->dtype, gkv, s);
-        L_DEV(dims->dtype, L.knew, L.vnew, k_cache, v_cache, cpos, crows, n_cand, W, use_v, sc, s);
+        L_DEV(dims->dtype, L.knew, L.vnew, k_cache, v_cache, cpos, crows, n_cand, m_in, N, W, use_v, sc, s);
       }
       if (k_budget > 0 && !sel_override && !fmask) {
         // top-k and the selection build (S = candidate rows of the top k ++ forced rows) in
@@ -835,7 +866,10 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         L_IOTA(s_out, m_in, 0, s);
       L_RMSNORM(dims->dtype, dims->dtype, L.a, x_in, nullptr, w->attn_norm, m_in, dims->d_model, dims->rms_eps, s);
       WAIT_CACHED_ROWS();
-      L_GEMM(dims->dtype, qkv_desc(dims, w, L.a, m_in, 0, qc + 2 * W, L.q, k_cache, v_cache, s_out, s_out, cos_sin, max_pos), s);
+      // s_out is the caller's row set: its rows are checked against the cache height
+      GemmDesc g = qkv_desc(dims, w, L.a, m_in, 0, qc + 2 * W, L.q, k_cache, v_cache, s_out, s_out, cos_sin, max_pos);
+      g.epi.kv_bound = N;
+      L_GEMM(dims->dtype, g, s);
       L_ATTN(dims->dtype, L.q, s_out, m_in, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
       return o_ffn(dims, w, L.attn, x_in, m_in, x_out, L, s);
     }
@@ -944,6 +978,20 @@ int cb_stream_wait(void* stream, void* event) {
 }
 
 int64_t cb_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void cb_shutdown(void) {
+  reset_mem_caches();
+  reset_gemm_tc_caches();
+  reset_attn_tc_caches();
+  ProfState& P = g_prof;
+  bool failed = false;
+  for (cudaEvent_t e : P.ev) failed = cudaEventDestroy(e) != cudaSuccess || failed;
+  if (failed) cudaGetLastError();   // clears the errors of the destroys just made
+  P.ev.clear();
+  P.rec.clear();
+  P.on = false;
+  P.cap = 0;
+}
 
 int cb_profile_begin(int32_t max_records) {
   if (max_records < 1) return fail(CB_ERR_INVALID_ARG, "max_records < 1");

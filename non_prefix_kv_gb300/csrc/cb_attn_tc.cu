@@ -18,6 +18,8 @@
 #include <cuda.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "cb_common.cuh"
 #include "cb_internal.h"
 #include "cb_tc.cuh"
@@ -415,21 +417,26 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// which kernel variants have their shared-memory limit set, per device (one bit per head
+// size), guarded for calls from several host threads; emptied by reset_attn_tc_caches()
+std::mutex g_attn_mu;
+uint32_t g_attn_attr[64];
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// looked up once per process (a function-local static: thread-safe initialisation)
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
+  static const EncodeTiledFn fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (e == cudaSuccess && q == cudaDriverEntryPointSuccess) return reinterpret_cast<EncodeTiledFn>(p);
+    if (e != cudaSuccess) cudaGetLastError();   // clears the error of this lookup only
+    return static_cast<EncodeTiledFn>(nullptr);
+  }();
   return fn;
 }
 
@@ -454,13 +461,25 @@ cudaError_t launch_hd(const void* q, const int32_t* q_pos, int M, const void* kc
       !make_map(&tk, kc, n_kv, (int64_t)Hkv * HD, (int64_t)Hkv * HD) ||
       !make_map(&tv, vc, n_kv, (int64_t)Hkv * HD, (int64_t)Hkv * HD))
     return cudaErrorInvalidValue;
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<HD>::SMEM);
+  {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    const bool cached = dev >= 0 && dev < 64;
+    const uint32_t bit = HD == 128 ? 1u : 2u;
+    bool set = false;
+    if (cached) {
+      std::lock_guard<std::mutex> g(g_attn_mu);
+      set = (g_attn_attr[dev] & bit) != 0;
+    }
+    if (!set) {
+      e = cudaFuncSetAttribute(k_attn_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<HD>::SMEM);
+      if (e != cudaSuccess) return e;
+      if (cached) {
+        std::lock_guard<std::mutex> g(g_attn_mu);
+        g_attn_attr[dev] |= bit;
+      }
+    }
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
   dim3 grid(H, (M + BM - 1) / BM);
@@ -472,6 +491,11 @@ cudaError_t launch_hd(const void* q, const int32_t* q_pos, int M, const void* kc
 }  // namespace
 
 bool attention_tc_supported(int hd) { return hd == 64 || hd == 128; }
+
+void reset_attn_tc_caches() {
+  std::lock_guard<std::mutex> g(g_attn_mu);
+  for (int i = 0; i < 64; ++i) g_attn_attr[i] = 0;
+}
 
 cudaError_t launch_attention_tc(const void* q, const int32_t* q_pos, int M, const void* kc, const void* vc,
                                 int64_t n_kv, int H, int Hkv, int hd, void* out, cudaStream_t s) {

@@ -114,12 +114,11 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 
 // Programmatic dependent launch is on unless CB_PDL=0 (read once; a measurement switch).
 inline bool pdl_enabled() {
-  static int on = -1;
-  if (on < 0) {
+  static const bool on = [] {
     const char* v = getenv("CB_PDL");
-    on = (v && v[0] == '0') ? 0 : 1;
-  }
-  return on != 0;
+    return !(v && v[0] == '0');
+  }();
+  return on;
 }
 
 // Host side: launch with the programmatic-stream-serialization attribute.

@@ -86,7 +86,7 @@ __device__ __forceinline__ bool epi_apply(const EpiParams& p, int m, int n, floa
         return true;
       }
       const int64_t kr = p.kv_row ? (int64_t)p.kv_row[m] : (int64_t)m;
-      if (kr < 0) return false;
+      if (kr < 0 || (p.kv_bound >= 0 && kr >= p.kv_bound)) return false;
       if (g < p.q_cols + p.kv_cols)
         st_vec<T, NV>((T*)p.k + kr * p.ldkv + (g - p.q_cols), v);
       else

@@ -131,9 +131,4 @@ cudaError_t launch_gemm_pair(int dt, const GemmDesc& a, const GemmDesc& b, cudaS
   return launch_gemm(dt, b, s);
 }
 
-// bf16 SIMT instance: an independent cross-check of the tensor-core GEMM.
-cudaError_t launch_gemm_simt_bf16(const GemmDesc& g, cudaStream_t s) {
-  return launch_simt<bf16>(g, s);
-}
-
 }  // namespace cb

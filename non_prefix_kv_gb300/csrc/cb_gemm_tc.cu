@@ -13,6 +13,7 @@
 #include <cuda.h>
 
 #include <cstdlib>
+#include <mutex>
 
 #include "cb_common.cuh"
 #include "cb_epilogue.cuh"
@@ -517,16 +518,16 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// looked up once per process (a function-local static: thread-safe initialisation)
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
+  static const EncodeTiledFn fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (e == cudaSuccess && q == cudaDriverEntryPointSuccess) return reinterpret_cast<EncodeTiledFn>(p);
+    if (e != cudaSuccess) cudaGetLastError();   // clears the error of this lookup only
+    return static_cast<EncodeTiledFn>(nullptr);
+  }();
   return fn;
 }
 
@@ -554,14 +555,55 @@ cudaError_t launch_wait_selftest(uint32_t max_polls, int arrive, cudaStream_t s)
 
 namespace {
 
+// Host-side caches of this file, per device: SM count, which kernel variants have their
+// shared-memory limit set (one bit each), co-resident CTA pairs.  One mutex guards them
+// (calls may come from several host threads); a failed query is not cached, and
+// reset_gemm_tc_caches() empties them.
+std::mutex g_tc_mu;
+int g_tc_sms[64];
+uint32_t g_tc_attr[64];
+int g_pair_slots[64];
+bool g_pair_done[64];
+
 int sm_count() {
-  static int sms[64] = {0};
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return 148;
-  if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-  return sms[dev] > 0 ? sms[dev] : 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  {
+    std::lock_guard<std::mutex> g(g_tc_mu);
+    if (g_tc_sms[dev]) return g_tc_sms[dev];
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();   // clears the error of the call just made
+    return 148;
+  }
+  if (n <= 0) return 148;
+  std::lock_guard<std::mutex> g(g_tc_mu);
+  g_tc_sms[dev] = n;
+  return n;
 }
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` once per device (bit `bit` of the
+// device's mask records it).
+cudaError_t ensure_smem_attr(const void* kernel, int bytes, int bit) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < 64;
+  if (cached) {
+    std::lock_guard<std::mutex> g(g_tc_mu);
+    if ((g_tc_attr[dev] >> bit) & 1u) return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  if (cached) {
+    std::lock_guard<std::mutex> g(g_tc_mu);
+    g_tc_attr[dev] |= 1u << bit;
+  }
+  return cudaSuccess;
+}
+constexpr int attr_bit_single(int bn) { return bn == 256 ? 0 : bn == 224 ? 1 : bn == 208 ? 2 : 3; }
+constexpr int attr_bit_pair(int bn) { return 4 + (bn == 256 ? 0 : bn == 224 ? 1 : 2); }
 
 int tiles_for(const GemmDesc* gs, int n, int out_cols) {
   int tiles = 0;
@@ -610,13 +652,9 @@ cudaError_t launch_tiles(const GemmDesc* gs, int n, bool swiglu, int n_sm, cudaS
     tmA[1] = tmA[0];
     tmB[1] = tmB[0];
   }
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  {
+    const cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(k_gemm_tc<BN>), SMEM_BYTES, attr_bit_single(BN));
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int tiles = tiles_for(gs, n, out_cols);
   const int grid = tiles < n_sm ? tiles : n_sm;
@@ -635,8 +673,8 @@ int pair_tiles_for(const GemmDesc* gs, int n, int out_cols) {
 
 template <int BN>
 cudaError_t pair_attr() {
-  return cudaFuncSetAttribute(k_gemm_tc_pair<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              PairCfg<BN>::SMEM_BYTES);
+  return ensure_smem_attr(reinterpret_cast<const void*>(k_gemm_tc_pair<BN>), PairCfg<BN>::SMEM_BYTES,
+                          attr_bit_pair(BN));
 }
 
 cudaLaunchConfig_t pair_config(cudaLaunchAttribute* attr, cudaStream_t s) {
@@ -655,26 +693,31 @@ cudaLaunchConfig_t pair_config(cudaLaunchAttribute* attr, cudaStream_t s) {
 }
 
 // Co-resident CTA pairs on this device (one CTA per SM), once per device; 0 if pair launches
-// are unavailable.  Also sets the pair kernels' shared-memory limits.
+// are unavailable.  Also sets the pair kernels' shared-memory limits.  A failed query gives 0
+// for this call only (it is asked again next time); only its own error is cleared.
 int pair_slots() {
-  static int slots[64];
-  static bool done[64] = {false};
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && done[dev]) return slots[dev];
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  {
+    std::lock_guard<std::mutex> g(g_tc_mu);
+    if (g_pair_done[dev]) return g_pair_slots[dev];
+  }
+  if (pair_attr<256>() != cudaSuccess || pair_attr<224>() != cudaSuccess || pair_attr<192>() != cudaSuccess) {
+    cudaGetLastError();   // clears the error of the call that just failed
+    return 0;
+  }
   int mp = 0;
-  if (pair_attr<256>() == cudaSuccess && pair_attr<224>() == cudaSuccess && pair_attr<192>() == cudaSuccess) {
-    cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = pair_config(attr, 0);
-    cfg.dynamicSmemBytes = PairCfg<256>::SMEM_BYTES;
-    cfg.gridDim = dim3(2 * (sm_count() / 2));
-    if (cudaOccupancyMaxActiveClusters(&mp, k_gemm_tc_pair<256>, &cfg) != cudaSuccess) mp = 0;
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = pair_config(attr, 0);
+  cfg.dynamicSmemBytes = PairCfg<256>::SMEM_BYTES;
+  cfg.gridDim = dim3(2 * (sm_count() / 2));
+  if (cudaOccupancyMaxActiveClusters(&mp, k_gemm_tc_pair<256>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
   }
-  cudaGetLastError();
-  if (dev >= 0 && dev < 64) {
-    slots[dev] = mp;
-    done[dev] = true;
-  }
+  std::lock_guard<std::mutex> g(g_tc_mu);
+  g_pair_slots[dev] = mp;
+  g_pair_done[dev] = true;
   return mp;
 }
 
@@ -705,11 +748,10 @@ cudaError_t launch_pair(const GemmDesc* gs, int n, bool swiglu, int n_pairs, cud
 // CB_GEMM_PAIR=0 forces single-SM tiles, =1 pair tiles wherever a pair launch is possible
 // (for measurement); unset, plan_tiles decides.
 int pair_mode() {
-  static int mode = -2;
-  if (mode == -2) {
+  static const int mode = [] {
     const char* v = getenv("CB_GEMM_PAIR");
-    mode = (v && v[0] == '0') ? 0 : (v && v[0] == '1') ? 1 : -1;
-  }
+    return (v && v[0] == '0') ? 0 : (v && v[0] == '1') ? 1 : -1;
+  }();
   return mode;
 }
 
@@ -757,6 +799,16 @@ TilePlan plan_tiles(const GemmDesc* gs, int n, int n_sm, int n_pairs) {
 }
 
 }  // namespace
+
+void reset_gemm_tc_caches() {
+  std::lock_guard<std::mutex> g(g_tc_mu);
+  for (int i = 0; i < 64; ++i) {
+    g_tc_sms[i] = 0;
+    g_tc_attr[i] = 0;
+    g_pair_slots[i] = 0;
+    g_pair_done[i] = false;
+  }
+}
 
 // The tile width (output columns per tile, SwiGLU: gate + up) launch_gemm_tc_group will use
 // for this launch; the fused deviation's partials are laid out per half tile of this width.

@@ -42,6 +42,7 @@ struct EpiParams {
   int64_t ldkv = 0;
   const int32_t* pos = nullptr;     // [M] RoPE position per row
   const int32_t* kv_row = nullptr;  // [M] destination row of k/v, or null
+  int64_t kv_bound = -1;            // rows of k/v for the check of kv_row (< 0: unchecked)
   const float* rope = nullptr;      // cos/sin table [max_pos][hd/2][2]
   int max_pos = 0;
   // EPI_QKV on the tensor-core path: squared deviation of the (bf16-rounded) K/V columns
@@ -76,8 +77,9 @@ int gemm_tc_tile_n(const GemmDesc* gs, int n);
 // ---- cb_mem.cu ------------------------------------------------------------------------
 cudaError_t launch_rope_table(float* tab, int max_pos, int hd, double base, cudaStream_t s);
 cudaError_t launch_rope_shift(int dt, void* kd, void* vd, const void* ks, const void* vs,
-                              const int32_t* src_row, const int32_t* delta, int64_t n_rows,
-                              int W, int hd, const float* tab, int max_pos, cudaStream_t s);
+                              const int32_t* src_row, int64_t n_src, const int32_t* delta,
+                              int64_t n_rows, int W, int hd, const float* tab, int max_pos,
+                              cudaStream_t s);
 cudaError_t launch_kv_quantize(int dt, const void* x, int64_t n, int W, uint8_t* q, float* scale,
                                float* zero, cudaStream_t s);
 cudaError_t launch_rope_shift_q8(int dt, void* kd, void* vd, const uint8_t* kq, const uint8_t* vq,
@@ -88,9 +90,10 @@ cudaError_t launch_rope_shift_q8(int dt, void* kd, void* vd, const uint8_t* kq, 
 cudaError_t launch_copy_rows(void* dst, const int32_t* dst_idx, const void* src,
                              const int32_t* src_idx, int64_t n, int64_t row_bytes,
                              int64_t dst_bound, int64_t src_bound, cudaStream_t s);
+// rows index x; n_src is x's row count for the index check (< 0: unchecked)
 cudaError_t launch_rmsnorm(int dt_in, int dt_out, void* out, const void* x,
-                           const int32_t* rows, const void* g, int64_t n, int d, float eps,
-                           cudaStream_t s);
+                           const int32_t* rows, int64_t n_src, const void* g, int64_t n, int d,
+                           float eps, cudaStream_t s);
 cudaError_t launch_dev_reduce(const float* part, int part_lo, int n_parts, int64_t ld, int n_cand,
                               const int32_t* cand_pos, float* scores, cudaStream_t s);
 constexpr int kMaxCopyJobs = 4;
@@ -113,9 +116,11 @@ cudaError_t launch_split_rows(const int32_t* rows_in, int m, const uint8_t* mask
 cudaError_t launch_merge_sel(const int32_t* ord, int k, const int32_t* cand_rows, const int32_t* cand_pos,
                              const int32_t* forced_rows, const int32_t* forced_pos, int nf, int32_t* s_out,
                              int32_t* keep_out, cudaStream_t s);
+// n_new / n_ref: row counts of the new and cached K/V for the index checks (< 0: unchecked)
 cudaError_t launch_deviation(int dt, const void* kn, const void* vn, const void* kr,
                              const void* vr, const int32_t* new_row, const int32_t* ref_row,
-                             int n_cand, int W, int use_v, float* scores, cudaStream_t s);
+                             int n_cand, int64_t n_new, int64_t n_ref, int W, int use_v,
+                             float* scores, cudaStream_t s);
 cudaError_t launch_topk(const float* scores, int n, int k, int32_t* out_ord, cudaStream_t s);
 // top-k fused with the selection build of the default layout (see launch_build_sel)
 cudaError_t launch_topk_sel(const float* scores, int n, int k, const int32_t* cand_row, int32_t forced_row0,
@@ -138,8 +143,13 @@ uint32_t take_error_mem();
 int noalloc_max_candidates();
 cudaError_t launch_deviation_topk_noalloc(int dt, const void* kn, const void* vn, const void* kr,
                                           const void* vr, const int32_t* new_row,
-                                          const int32_t* ref_row, int n_cand, int k, int W,
-                                          int use_v, float* scores, int32_t* sel, cudaStream_t s);
+                                          const int32_t* ref_row, int n_cand, int64_t n_new,
+                                          int64_t n_ref, int k, int W, int use_v, float* scores,
+                                          int32_t* sel, cudaStream_t s);
+// empty the host-side per-device caches of each translation unit (cb_shutdown)
+void reset_mem_caches();
+void reset_gemm_tc_caches();
+void reset_attn_tc_caches();
 
 // ---- cb_gemm.cu -----------------------------------------------------------------------
 cudaError_t launch_gemm(int dt, const GemmDesc& g, cudaStream_t s);

@@ -14,42 +14,69 @@ namespace cb {
 
 static __device__ uint32_t g_err_mem;
 
+// Host-side caches of this file, per device: SM count, resident blocks per kernel, the
+// top-k kernel's shared-memory attribute, the allocation-free scratch address.  One mutex
+// guards them (calls may come from several host threads); reset_mem_caches() empties them.
+namespace {
+std::mutex g_mem_mu;
+int g_sms[64];
+struct ResidentEnt {
+  const void* k;
+  int dev, threads, n;
+};
+ResidentEnt g_resident[64];
+int g_resident_used = 0;
+bool g_topk_attr[64];
+void* g_noalloc_addr[64];
+}  // namespace
+
+void reset_mem_caches() {
+  std::lock_guard<std::mutex> g(g_mem_mu);
+  for (int i = 0; i < 64; ++i) {
+    g_sms[i] = 0;
+    g_topk_attr[i] = false;
+    g_noalloc_addr[i] = nullptr;
+  }
+  g_resident_used = 0;
+}
+
 static int sm_count() {
-  static int cached[64] = {0};
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  {
+    std::lock_guard<std::mutex> g(g_mem_mu);
+    if (g_sms[dev]) return g_sms[dev];
+  }
   int n = 0;
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  if (n <= 0) n = 148;
-  if (dev >= 0 && dev < 64) cached[dev] = n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();   // clears the error of the call just made (nothing is cached)
+    return 148;
+  }
+  if (n <= 0) return 148;
+  std::lock_guard<std::mutex> g(g_mem_mu);
+  g_sms[dev] = n;
   return n;
 }
 
 // Blocks of `threads` threads of this kernel resident per SM at once (registers, shared
-// memory), once per kernel, block size and device.
+// memory), once per kernel, block size and device.  A failed query is not cached.
 static int resident_blocks(const void* kernel, int threads) {
-  static std::mutex mu;
-  struct Ent {
-    const void* k;
-    int dev, threads, n;
-  };
-  static Ent cache[64];
-  static int used = 0;
   int dev = 0;
-  cudaGetDevice(&dev);
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
   {
-    std::lock_guard<std::mutex> g(mu);
-    for (int i = 0; i < used; ++i)
-      if (cache[i].k == kernel && cache[i].dev == dev && cache[i].threads == threads) return cache[i].n;
+    std::lock_guard<std::mutex> g(g_mem_mu);
+    for (int i = 0; i < g_resident_used; ++i)
+      if (g_resident[i].k == kernel && g_resident[i].dev == dev && g_resident[i].threads == threads)
+        return g_resident[i].n;
   }
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) {
-    cudaGetLastError();
-    n = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess) {
+    cudaGetLastError();   // clears the error of the call just made
+    return 1;
   }
-  std::lock_guard<std::mutex> g(mu);
-  if (used < 64) cache[used++] = Ent{kernel, dev, threads, n};
+  if (n < 1) n = 1;
+  std::lock_guard<std::mutex> g(g_mem_mu);
+  if (g_resident_used < 64) g_resident[g_resident_used++] = ResidentEnt{kernel, dev, threads, n};
   return n;
 }
 
@@ -97,13 +124,14 @@ cudaError_t launch_rope_table(float* tab, int max_pos, int hd, double base, cuda
 // ------------------------------------------------------------------------ RoPE shift
 // k_dst[r] = R(delta[r]) k_src[src_row[r]]; v_dst[r] = v_src[src_row[r]].
 // One thread per 8 consecutive elements (4 rotation pairs, never crossing a head since
-// hd % 8 == 0).  The negative-offset rotation negates the sine.
+// hd % 8 == 0).  The negative-offset rotation negates the sine.  A source row outside
+// [0, n_src) or an offset outside the table records ERRBIT_INDEX and the row is skipped.
 template <typename T>
 __global__ void __launch_bounds__(256) k_rope_shift(T* __restrict__ kd, T* __restrict__ vd,
                                                     const T* ks, const T* __restrict__ vs,
                                                     const int32_t* __restrict__ src_row,
                                                     const int32_t* __restrict__ delta,
-                                                    int64_t n_rows, int W, int hd,
+                                                    int64_t n_rows, int64_t n_src, int W, int hd,
                                                     const float2* __restrict__ tab, int max_pos) {
   pdl_wait();
   pdl_trigger();
@@ -117,7 +145,7 @@ __global__ void __launch_bounds__(256) k_rope_shift(T* __restrict__ kd, T* __res
     const int64_t sr = src_row ? (int64_t)src_row[r] : r;
     const int dl = delta[r];
     const int ad = dl < 0 ? -dl : dl;
-    if (ad >= max_pos || sr < 0) {
+    if (ad >= max_pos || sr < 0 || sr >= n_src) {
       atomicOr(&g_err_mem, ERRBIT_INDEX);
       continue;
     }
@@ -142,19 +170,20 @@ __global__ void __launch_bounds__(256) k_rope_shift(T* __restrict__ kd, T* __res
 }
 
 cudaError_t launch_rope_shift(int dt, void* kd, void* vd, const void* ks, const void* vs,
-                              const int32_t* src_row, const int32_t* delta, int64_t n_rows,
-                              int W, int hd, const float* tab, int max_pos, cudaStream_t s) {
+                              const int32_t* src_row, int64_t n_src, const int32_t* delta,
+                              int64_t n_rows, int W, int hd, const float* tab, int max_pos,
+                              cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
   const int64_t work = n_rows * (W / 8);
   const unsigned grid = dt == DT_BF16 ? grid_for(k_rope_shift<bf16>, work, 256) : grid_for(k_rope_shift<float>, work, 256);
   const float2* t2 = reinterpret_cast<const float2*>(tab);
   if (dt == DT_BF16)
     { const cudaError_t e_ = launch_k(k_rope_shift<bf16>, dim3(grid), dim3(256), 0, s, (bf16*)kd, (bf16*)vd, (const bf16*)ks,
-                                            (const bf16*)vs, src_row, delta, n_rows, W, hd, t2,
+                                            (const bf16*)vs, src_row, delta, n_rows, n_src, W, hd, t2,
                                             max_pos); if (e_ != cudaSuccess) return e_; }
   else
     { const cudaError_t e_ = launch_k(k_rope_shift<float>, dim3(grid), dim3(256), 0, s, (float*)kd, (float*)vd, (const float*)ks,
-                                             (const float*)vs, src_row, delta, n_rows, W, hd, t2,
+                                             (const float*)vs, src_row, delta, n_rows, n_src, W, hd, t2,
                                              max_pos); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
@@ -440,16 +469,21 @@ cudaError_t launch_copy_rows_multi(const CopyJobs& J, cudaStream_t s) {
 }
 
 // ------------------------------------------------------------------------ RMSNorm
-// out[r] = x[rows[r]] / sqrt(mean(x^2) + eps) * g.  One block per row.
+// out[r] = x[rows[r]] / sqrt(mean(x^2) + eps) * g.  One block per row.  A row index outside
+// [0, n_src) (n_src < 0: unchecked) records ERRBIT_INDEX and the output row is not written.
 template <typename Ti, typename To>
 __global__ void __launch_bounds__(256) k_rmsnorm(To* __restrict__ out, const Ti* __restrict__ x,
-                                                 const int32_t* __restrict__ rows,
+                                                 const int32_t* __restrict__ rows, int64_t n_src,
                                                  const Ti* __restrict__ g, int d, float eps) {
   pdl_wait();
   pdl_trigger();
   __shared__ float red[32];
   const int64_t r = blockIdx.x;
   const int64_t src = rows ? (int64_t)rows[r] : r;
+  if (src < 0 || (n_src >= 0 && src >= n_src)) {   // uniform over the block
+    if (threadIdx.x == 0) atomicOr(&g_err_mem, ERRBIT_INDEX);
+    return;
+  }
   const Ti* xr = x + src * d;
   float ss = 0.f;
   for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
@@ -484,13 +518,17 @@ __global__ void __launch_bounds__(256) k_rmsnorm(To* __restrict__ out, const Ti*
 // VPT 16-byte vectors in registers between the sum and the scaling (the row is read once).
 template <int VPT>
 __global__ void __launch_bounds__(128) k_rmsnorm_reg(bf16* __restrict__ out, const bf16* __restrict__ x,
-                                                     const int32_t* __restrict__ rows,
+                                                     const int32_t* __restrict__ rows, int64_t n_src,
                                                      const bf16* __restrict__ g, int d, float eps) {
   pdl_wait();
   pdl_trigger();
   __shared__ float red[4];
   const int64_t r = blockIdx.x;
   const int64_t src = rows ? (int64_t)rows[r] : r;
+  if (src < 0 || (n_src >= 0 && src >= n_src)) {   // uniform over the block
+    if (threadIdx.x == 0) atomicOr(&g_err_mem, ERRBIT_INDEX);
+    return;
+  }
   const uint4* xr = reinterpret_cast<const uint4*>(x + src * d);
   const int nv = d >> 3;
   uint4 v[VPT];
@@ -536,37 +574,40 @@ __global__ void __launch_bounds__(128) k_rmsnorm_reg(bf16* __restrict__ out, con
 }
 
 cudaError_t launch_rmsnorm(int dt_in, int dt_out, void* out, const void* x, const int32_t* rows,
-                           const void* g, int64_t n, int d, float eps, cudaStream_t s) {
+                           int64_t n_src, const void* g, int64_t n, int d, float eps, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   if (dt_in == DT_BF16 && dt_out == DT_BF16 && d % 8 == 0 && d <= 128 * 8 * 8) {
     if (d <= 128 * 8 * 4)
-      { const cudaError_t e_ = launch_k(k_rmsnorm_reg<4>, dim3((unsigned)n), dim3(128), 0, s, (bf16*)out, (const bf16*)x, rows, (const bf16*)g, d, eps); if (e_ != cudaSuccess) return e_; }
+      { const cudaError_t e_ = launch_k(k_rmsnorm_reg<4>, dim3((unsigned)n), dim3(128), 0, s, (bf16*)out, (const bf16*)x, rows, n_src, (const bf16*)g, d, eps); if (e_ != cudaSuccess) return e_; }
     else
-      { const cudaError_t e_ = launch_k(k_rmsnorm_reg<8>, dim3((unsigned)n), dim3(128), 0, s, (bf16*)out, (const bf16*)x, rows, (const bf16*)g, d, eps); if (e_ != cudaSuccess) return e_; }
+      { const cudaError_t e_ = launch_k(k_rmsnorm_reg<8>, dim3((unsigned)n), dim3(128), 0, s, (bf16*)out, (const bf16*)x, rows, n_src, (const bf16*)g, d, eps); if (e_ != cudaSuccess) return e_; }
     return cudaGetLastError();
   }
   const int threads = d >= 2048 ? 256 : (d >= 512 ? 64 : 32);
   if (dt_in == DT_BF16 && dt_out == DT_BF16)
     { const cudaError_t e_ = launch_k(k_rmsnorm<bf16, bf16>, dim3((unsigned)n), dim3(threads), 0, s, (bf16*)out, (const bf16*)x, rows,
-                                                          (const bf16*)g, d, eps); if (e_ != cudaSuccess) return e_; }
+                                                          n_src, (const bf16*)g, d, eps); if (e_ != cudaSuccess) return e_; }
   else if (dt_in == DT_BF16)
     { const cudaError_t e_ = launch_k(k_rmsnorm<bf16, float>, dim3((unsigned)n), dim3(threads), 0, s, (float*)out, (const bf16*)x, rows,
-                                                           (const bf16*)g, d, eps); if (e_ != cudaSuccess) return e_; }
+                                                           n_src, (const bf16*)g, d, eps); if (e_ != cudaSuccess) return e_; }
   else
     { const cudaError_t e_ = launch_k(k_rmsnorm<float, float>, dim3((unsigned)n), dim3(threads), 0, s, (float*)out, (const float*)x, rows,
-                                                            (const float*)g, d, eps); if (e_ != cudaSuccess) return e_; }
+                                                            n_src, (const float*)g, d, eps); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------------ KV deviation
 // scores[c] = sum (kn[new_row[c]] - kr[ref_row[c]])^2 (+ V).  One warp per candidate;
-// each lane reads 16-byte vectors, partial sums reduced by shuffles (fixed order).
+// each lane reads 16-byte vectors, partial sums reduced by shuffles (fixed order).  A row
+// outside [0, n_new) or [0, n_ref) (bound < 0: unchecked) records ERRBIT_INDEX and the
+// candidate's score is not written.
 template <typename T>
 __global__ void __launch_bounds__(256) k_deviation(const T* __restrict__ kn, const T* __restrict__ vn,
                                                    const T* __restrict__ kr, const T* __restrict__ vr,
                                                    const int32_t* __restrict__ new_row,
                                                    const int32_t* __restrict__ ref_row, int n_cand,
-                                                   int W, int use_v, float* __restrict__ scores) {
+                                                   int64_t n_new, int64_t n_ref, int W, int use_v,
+                                                   float* __restrict__ scores) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
@@ -574,6 +615,10 @@ __global__ void __launch_bounds__(256) k_deviation(const T* __restrict__ kn, con
   for (int c = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; c < n_cand; c += warps_total) {
     const int64_t rn = new_row ? (int64_t)new_row[c] : c;
     const int64_t rr = ref_row ? (int64_t)ref_row[c] : c;
+    if (rn < 0 || rr < 0 || (n_new >= 0 && rn >= n_new) || (n_ref >= 0 && rr >= n_ref)) {   // warp-uniform
+      if (lane == 0) atomicOr(&g_err_mem, ERRBIT_INDEX);
+      continue;
+    }
     float acc = 0.f, accv = 0.f;
     const T* a = kn + rn * W;
     const T* b = kr + rr * W;
@@ -651,8 +696,9 @@ cudaError_t launch_dev_reduce(const float* part, int part_lo, int n_parts, int64
 __global__ void __launch_bounds__(256) k_deviation_wide(const bf16* __restrict__ kn, const bf16* __restrict__ vn,
                                                         const bf16* __restrict__ kr, const bf16* __restrict__ vr,
                                                         const int32_t* __restrict__ new_row,
-                                                        const int32_t* __restrict__ ref_row, int n_cand, int W,
-                                                        int use_v, float* __restrict__ scores) {
+                                                        const int32_t* __restrict__ ref_row, int n_cand,
+                                                        int64_t n_new, int64_t n_ref, int W, int use_v,
+                                                        float* __restrict__ scores) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
@@ -660,6 +706,10 @@ __global__ void __launch_bounds__(256) k_deviation_wide(const bf16* __restrict__
   for (int c = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; c < n_cand; c += warps_total) {
     const int64_t rn = new_row ? (int64_t)new_row[c] : c;
     const int64_t rr = ref_row ? (int64_t)ref_row[c] : c;
+    if (rn < 0 || rr < 0 || (n_new >= 0 && rn >= n_new) || (n_ref >= 0 && rr >= n_ref)) {   // warp-uniform
+      if (lane == 0) atomicOr(&g_err_mem, ERRBIT_INDEX);
+      continue;
+    }
     const uint4* a = reinterpret_cast<const uint4*>(kn + rn * W);
     const uint4* b = reinterpret_cast<const uint4*>(kr + rr * W);
     const uint4* av = reinterpret_cast<const uint4*>(vn + rn * W);
@@ -710,21 +760,22 @@ __global__ void __launch_bounds__(256) k_deviation_wide(const bf16* __restrict__
 
 cudaError_t launch_deviation(int dt, const void* kn, const void* vn, const void* kr,
                              const void* vr, const int32_t* new_row, const int32_t* ref_row,
-                             int n_cand, int W, int use_v, float* scores, cudaStream_t s) {
+                             int n_cand, int64_t n_new, int64_t n_ref, int W, int use_v, float* scores,
+                             cudaStream_t s) {
   if (n_cand == 0) return cudaSuccess;
   if (dt == DT_BF16 && W % 1024 == 0) {
-    { const cudaError_t e_ = launch_k(k_deviation_wide, dim3(grid_for(k_deviation_wide, (int64_t)n_cand * 32, 256)), dim3(256), 0, s, (const bf16*)kn, (const bf16*)vn, (const bf16*)kr, (const bf16*)vr, new_row, ref_row, n_cand, W, use_v, scores); if (e_ != cudaSuccess) return e_; }
+    { const cudaError_t e_ = launch_k(k_deviation_wide, dim3(grid_for(k_deviation_wide, (int64_t)n_cand * 32, 256)), dim3(256), 0, s, (const bf16*)kn, (const bf16*)vn, (const bf16*)kr, (const bf16*)vr, new_row, ref_row, n_cand, n_new, n_ref, W, use_v, scores); if (e_ != cudaSuccess) return e_; }
     return cudaGetLastError();
   }
   const unsigned grid = dt == DT_BF16 ? grid_for(k_deviation<bf16>, (int64_t)n_cand * 32, 256)
                                       : grid_for(k_deviation<float>, (int64_t)n_cand * 32, 256);
   if (dt == DT_BF16)
     { const cudaError_t e_ = launch_k(k_deviation<bf16>, dim3(grid), dim3(256), 0, s, (const bf16*)kn, (const bf16*)vn, (const bf16*)kr,
-                                           (const bf16*)vr, new_row, ref_row, n_cand, W, use_v,
+                                           (const bf16*)vr, new_row, ref_row, n_cand, n_new, n_ref, W, use_v,
                                            scores); if (e_ != cudaSuccess) return e_; }
   else
     { const cudaError_t e_ = launch_k(k_deviation<float>, dim3(grid), dim3(256), 0, s, (const float*)kn, (const float*)vn, (const float*)kr,
-                                            (const float*)vr, new_row, ref_row, n_cand, W, use_v,
+                                            (const float*)vr, new_row, ref_row, n_cand, n_new, n_ref, W, use_v,
                                             scores); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
@@ -916,14 +967,21 @@ __global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores,
 static cudaError_t topk_launch(const float* scores, int n, int k, int32_t* out_ord, const SelOut& so,
                                cudaStream_t s) {
   if (n <= kTopkSmemKeys) {
-    static bool attr_set[64] = {false};
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-      const cudaError_t e = cudaFuncSetAttribute(k_topk<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 kTopkSmemKeys * 4);
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    bool set = false;
+    if (dev >= 0 && dev < 64) {
+      std::lock_guard<std::mutex> g(g_mem_mu);
+      set = g_topk_attr[dev];
+    }
+    if (!set) {
+      e = cudaFuncSetAttribute(k_topk<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopkSmemKeys * 4);
       if (e != cudaSuccess) return e;
-      if (dev >= 0 && dev < 64) attr_set[dev] = true;
+      if (dev >= 0 && dev < 64) {
+        std::lock_guard<std::mutex> g(g_mem_mu);
+        g_topk_attr[dev] = true;
+      }
     }
     { const cudaError_t e_ = launch_k(k_topk<true>, dim3(1), dim3(1024), (size_t)n * 4, s, scores, n, k, out_ord, so); if (e_ != cudaSuccess) return e_; }
   } else {
@@ -1340,22 +1398,21 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[(size_t)kNoAllo
 int noalloc_max_candidates() { return kNoAllocMaxCand; }
 
 // The array's name is only a host-side stand-in in host code; its device address is looked
-// up once per device (with that device current) and reused.
+// up once per device (with that device current, in the context current then: the primary
+// context for callers that use the runtime API) and reused until reset_mem_caches().
 static cudaError_t noalloc_scratch_address(void** out) {
-  static std::mutex mu;
-  static void* addr[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  std::lock_guard<std::mutex> lock(g_mem_mu);
+  if (!g_noalloc_addr[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    addr[dev] = p;
+    g_noalloc_addr[dev] = p;
   }
-  *out = addr[dev];
+  *out = g_noalloc_addr[dev];
   return cudaSuccess;
 }
 
@@ -1364,14 +1421,15 @@ static cudaError_t noalloc_scratch_address(void** out) {
 // nothing in it has to start at zero.  n_cand <= kNoAllocMaxCand is checked by the caller.
 cudaError_t launch_deviation_topk_noalloc(int dt, const void* kn, const void* vn, const void* kr,
                                           const void* vr, const int32_t* new_row,
-                                          const int32_t* ref_row, int n_cand, int k, int W,
-                                          int use_v, float* scores, int32_t* sel, cudaStream_t s) {
+                                          const int32_t* ref_row, int n_cand, int64_t n_new, int64_t n_ref,
+                                          int k, int W, int use_v, float* scores, int32_t* sel,
+                                          cudaStream_t s) {
   void* base = nullptr;
   cudaError_t e = noalloc_scratch_address(&base);
   if (e != cudaSuccess) return e;
   float* sc = scores ? scores : static_cast<float*>(base);
   int32_t* ord = reinterpret_cast<int32_t*>(static_cast<char*>(base) + (size_t)kNoAllocMaxCand * 4);
-  e = launch_deviation(dt, kn, vn, kr, vr, new_row, ref_row, n_cand, W, use_v, sc, s);
+  e = launch_deviation(dt, kn, vn, kr, vr, new_row, ref_row, n_cand, n_new, n_ref, W, use_v, sc, s);
   if (e != cudaSuccess || k <= 0) return e;
   e = launch_topk(sc, n_cand, k, ord, s);
   if (e != cudaSuccess) return e;

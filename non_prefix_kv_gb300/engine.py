@@ -226,7 +226,7 @@ class Request:
         self.delta = torch.tensor(delta, dtype=torch.int32, device=dev)
         self.qrow = torch.tensor(qrow, dtype=torch.int32, device=dev)
         self.n_pool_rows = int(sum(pool.lens))
-        self.tokens_host = np.asarray(tokens, np.int32)
+        self.tokens_host = check_token_ids(tokens, s.vocab)
         self.tokens = torch.from_numpy(self.tokens_host).to(dev)
         self.K = [torch.zeros(self.N, s.kv_width, dtype=dt, device=dev) for _ in range(s.n_layers)]
         self.V = [torch.zeros(self.N, s.kv_width, dtype=dt, device=dev) for _ in range(s.n_layers)]
@@ -259,6 +259,15 @@ class Request:
         self.start_rows = torch.from_numpy(rows).to(self.tokens.device)
         self.start_tokens = torch.from_numpy(self.tokens_host[first:].copy()).to(self.tokens.device)
         return [(B.CB_LAYER_STEADY, 0)] * self.eng.dm.shape.n_layers
+
+
+def check_token_ids(tokens, vocab: int) -> np.ndarray:
+    """Token ids as int32, each in [0, vocab) (the embedding lookup's rows); raises otherwise.
+    The device gather checks them again against the table height."""
+    t = np.asarray(tokens)
+    if t.ndim != 1 or (t.size and (int(t.min()) < 0 or int(t.max()) >= vocab)):
+        raise ValueError(f"token ids must be a 1-D array of values in [0, {vocab})")
+    return t.astype(np.int32)
 
 
 def contiguous_ranges(rows) -> list:
@@ -427,7 +436,10 @@ class RequestGraph:
 
     def run(self, tokens=None) -> int:
         if tokens is not None:
-            self.host_tokens.numpy()[:] = np.asarray(tokens, np.int32)
+            t = check_token_ids(tokens, self.req.eng.dm.shape.vocab)
+            if t.shape != (self.req.N,):
+                raise ValueError(f"a captured request takes exactly {self.req.N} token ids")
+            self.host_tokens.numpy()[:] = t
         with torch.cuda.stream(self.stream):      # a graph replays on the current stream
             self.graph.replay()
         self.stream.synchronize()
@@ -528,6 +540,8 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
 
         def load():
             try:
+                # this thread's calls size and launch work for the engine's device
+                torch.cuda.set_device(hp.side.device)
                 for l in range(s.n_layers):
                     if l in skip:
                         ready[l].set()

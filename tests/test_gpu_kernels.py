@@ -580,3 +580,123 @@ def test_host_sync_limit_returns_timeout_then_completes(B):
     assert e.value.status == 7
     B.cb_sync(s, timeout_s=0.0)
     assert abs(float(y[0, 0]) - n * 1e-4) < 0.05 * n * 1e-4
+
+
+# ------------------------------------------------------------------------------ index checks
+def _expect_device_error(B):
+    with pytest.raises(B.CBError) as e:
+        B.cb_sync(None)
+    assert e.value.status == 9 and "out-of-range index" in str(e.value)
+    B.cb_sync(None)                       # the word was cleared; the context still works
+
+
+def test_rope_shift_out_of_range_source_row_is_skipped_and_reported(B):
+    """A source row at or past the pool's height is not read: that destination row stays as
+    it was, every other row is re-positioned, and cb_sync reports CB_ERR_DEVICE."""
+    torch = torch_mod()
+    shape = synth.ModelShape(1, 256, 2, 2, 128, 256, 64, dtype="bf16")
+    dims = dims_for(B, shape)
+    n_src, n = 300, 64
+    ks = synth.test_tensor((n_src, 256), 41, dtype="bf16")
+    vs = synth.test_tensor((n_src, 256), 42, dtype="bf16")
+    src_row = np.arange(n, dtype=np.int32) * 3
+    src_row[17] = n_src                   # one past the end
+    delta = np.full(n, 640, np.int32)
+    tab = rope_tab(B, 4096, 128, 1e4)
+    kd = torch.full((n, 256), 7.0, dtype=torch.bfloat16, device="cuda")
+    vd = torch.full((n, 256), 7.0, dtype=torch.bfloat16, device="cuda")
+    B.cb_rope_shift(kd, vd, dev(ks, "bf16"), dev(vs, "bf16"), dev_i32(src_row), dev_i32(delta), n, dims, tab, 4096)
+    _expect_device_error(B)
+    ok = np.arange(n) != 17
+    want = O.rope_shift(ks[src_row[ok]].reshape(-1, 2, 128), 640, 1e4).reshape(-1, 256)
+    assert rel(host(kd)[ok], want) < 4e-3
+    np.testing.assert_array_equal(host(vd)[ok], vs[src_row[ok]])
+    assert np.all(host(kd)[17] == 7.0) and np.all(host(vd)[17] == 7.0)
+
+
+def test_embedding_gather_out_of_range_token_is_skipped_and_reported(B):
+    """A token id >= vocab is not looked up (the embedding table is bounded by its height)."""
+    torch = torch_mod()
+    vocab, d, n = 512, 256, 40
+    table = synth.test_tensor((vocab, d), 43, dtype="bf16")
+    ids = synth.rng(44, synth.P_TOKENS).integers(0, vocab, n).astype(np.int32)
+    ids[5], ids[30] = vocab, -1
+    out = torch.full((n, d), 3.0, dtype=torch.bfloat16, device="cuda")
+    B.cb_gather_rows(out, dev(table, "bf16"), dev_i32(ids), n, d * 2)
+    _expect_device_error(B)
+    ok = (ids >= 0) & (ids < vocab)
+    np.testing.assert_array_equal(host(out)[ok], table[ids[ok]])
+    assert np.all(host(out)[~ok] == 3.0)
+
+
+def test_scatter_out_of_range_cache_row_is_skipped_and_reported(B):
+    torch = torch_mod()
+    shape = synth.ModelShape(1, 256, 2, 2, 128, 256, 64, dtype="bf16")
+    dims = dims_for(B, shape)
+    cache = synth.test_tensor((100, 256), 45, dtype="bf16")
+    rows = synth.test_tensor((10, 256), 46, dtype="bf16")
+    dst_idx = np.arange(10, dtype=np.int32) * 9
+    dst_idx[4] = 100                      # past the cache
+    kc, vc = dev(cache, "bf16"), dev(cache, "bf16")
+    B.cb_scatter_kv(kc, vc, dev(rows, "bf16"), dev(rows, "bf16"), dev_i32(dst_idx), None, 10, dims)
+    _expect_device_error(B)
+    want = cache.copy()
+    ok = dst_idx < 100
+    want[dst_idx[ok]] = rows[ok]
+    np.testing.assert_array_equal(host(kc), want)
+    np.testing.assert_array_equal(host(vc), want)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_rmsnorm_and_deviation_out_of_range_rows_are_reported(B, dtype):
+    torch = torch_mod()
+    n_x, d = 50, 512
+    x = synth.test_tensor((n_x, d), 47, dtype=dtype)
+    gain = np.ones(d, np.float32)
+    rows = np.array([3, 7, n_x, 1], np.int32)
+    out = torch.full((4, d), 5.0, dtype=tdt(dtype), device="cuda")
+    code = B.CB_BF16 if dtype == "bf16" else B.CB_F32
+    B.cb_rmsnorm(out, dev(x, dtype), dev_i32(rows), 4, d, dev(gain, dtype), 1e-5, code, code)
+    _expect_device_error(B)
+    assert np.all(host(out)[2] == 5.0)
+    want = O.rmsnorm(x[[3, 7, 1]], gain, 1e-5)
+    assert rel(host(out)[[0, 1, 3]], want) < (1e-6 if dtype == "f32" else 1e-2)
+    # deviation with one cached row past the cache
+    shape = synth.ModelShape(1, 256, 2, 2, 128, 256, 64, dtype=dtype)
+    dims = dims_for(B, shape)
+    kn, vn = (dev(synth.test_tensor((20, 256), s, dtype=dtype), dtype) for s in (48, 49))
+    kr, vr = (dev(synth.test_tensor((30, 256), s, dtype=dtype), dtype) for s in (50, 51))
+    ref_row = np.arange(20, dtype=np.int32)
+    ref_row[11] = 30
+    sc = torch.full((20,), -1.0, device="cuda")
+    sel = torch.empty(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(1 << 16, dtype=torch.uint8, device="cuda")
+    B.cb_kv_deviation_topk(kn, vn, kr, vr, None, dev_i32(ref_row), 20, 0, B.CB_DEV_KV, dims, sc, sel, ws)
+    _expect_device_error(B)
+    s = sc.cpu().numpy()
+    assert s[11] == -1.0 and np.all(s[np.arange(20) != 11] > 0)
+
+
+def test_steady_layer_with_a_row_past_the_cache_writes_nothing_there(B):
+    """STEADY takes the caller's row set as the rows whose K/V it writes: a row at or past
+    n_tok is not written (the error word reports it), the cache outside stays untouched."""
+    torch = torch_mod()
+    from non_prefix_kv_gb300 import engine as E
+    shape = SHAPE_BF16
+    model = synth.make_model(shape, seed=3)
+    dm = E.DeviceModel.from_host(model)
+    eng = E.BlendEngine(dm, 300)
+    N = 256
+    W = shape.kv_width
+    # the caches live inside a larger buffer so that a stray write past row N would show
+    big_k = torch.zeros(N + 64, W, dtype=torch.bfloat16, device="cuda")
+    big_v = torch.zeros_like(big_k)
+    s_in = np.array([10, 50, 100, 255, N + 3], np.int32)
+    x = dev(synth.test_tensor((5, shape.d_model), 52, dtype="bf16"), "bf16")
+    x_out = torch.empty_like(x)
+    s_out = torch.empty(5, dtype=torch.int32, device="cuda")
+    B.cb_blend_layer(dm.dims, dm.layers_c[0], B.CB_LAYER_STEADY, x, dev_i32(s_in), 5, N, N - 32, big_k[:N],
+                     big_v[:N], eng.cos_sin, eng.max_pos, 0, 0, None, x_out, s_out, None, eng.ws)
+    _expect_device_error(B)
+    assert torch.count_nonzero(big_k[N:]) == 0 and torch.count_nonzero(big_v[N:]) == 0
+    assert torch.count_nonzero(big_k[[10, 50, 100, 255]].float().abs().sum(1)) == 4

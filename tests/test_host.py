@@ -107,17 +107,28 @@ FAKE = 0x10000   # never dereferenced: every call below fails validation before 
 def test_entry_points_reject_bad_arguments_before_launch(lib):
     d = _dims()
     w = B.cb_layer_w(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)
-    st = lib.cb_rope_shift(FAKE, None, FAKE, FAKE, None, None, 10, ctypes.byref(d), FAKE, 100, None)
+    st = lib.cb_rope_shift(FAKE, None, FAKE, FAKE, None, 10, None, 10, ctypes.byref(d), FAKE, 100, None)
     assert st == 1        # delta NULL
-    st = lib.cb_rope_shift(FAKE, FAKE, FAKE, None, None, FAKE, 10, ctypes.byref(d), FAKE, 100, None)
+    st = lib.cb_rope_shift(FAKE, FAKE, FAKE, None, None, 10, FAKE, 10, ctypes.byref(d), FAKE, 100, None)
     assert st == 1        # v_dst without v_src
-    st = lib.cb_kv_deviation_topk(FAKE, FAKE, FAKE, FAKE, None, None, 10, 11, 0, ctypes.byref(d), None, FAKE,
-                                  FAKE, 1 << 20, None)
+    st = lib.cb_rope_shift(FAKE, FAKE, FAKE, FAKE, None, 9, FAKE, 10, ctypes.byref(d), FAKE, 100, None)
+    assert st == 2        # no row map and fewer source rows than destination rows
+    st = lib.cb_kv_deviation_topk(FAKE, FAKE, 10, FAKE, FAKE, 10, None, None, 10, 11, 0, ctypes.byref(d), None,
+                                  FAKE, FAKE, 1 << 20, None)
     assert st == 2        # k > n_cand
+    st = lib.cb_kv_deviation_topk(FAKE, FAKE, 10, FAKE, FAKE, 9, None, None, 10, 5, 0, ctypes.byref(d), None,
+                                  FAKE, FAKE, 1 << 20, None)
+    assert st == 2        # no ref_row map and fewer cached rows than candidates
     st = lib.cb_topk_from_scores(FAKE, None, 100, 5, FAKE, FAKE, 16, None)
     assert st == 4        # workspace too small
-    st = lib.cb_gather_rows(FAKE, FAKE, None, 3, 6, None)
+    st = lib.cb_gather_rows(FAKE, FAKE, 3, None, 3, 6, None)
     assert st == 2        # row_bytes not a multiple of 4
+    st = lib.cb_gather_rows(FAKE, FAKE, 2, None, 3, 8, None)
+    assert st == 2        # no index and fewer source rows than rows to copy
+    st = lib.cb_scatter_kv(FAKE, FAKE, -1, FAKE, FAKE, 10, FAKE, None, 3, ctypes.byref(d), None)
+    assert st == 2        # negative cache height
+    st = lib.cb_rmsnorm(FAKE, FAKE, 4, None, 5, 64, FAKE, ctypes.c_float(1e-5), B.CB_BF16, B.CB_BF16, None)
+    assert st == 2        # no row map and fewer input rows than outputs
     m_out = ctypes.c_int32(-1)
     args = lambda mode, m_in, k, ws_bytes=1 << 40: (ctypes.byref(d), ctypes.byref(w), mode, FAKE, None, m_in, 416,
                                                    384, FAKE, FAKE, FAKE, 416, k, 0, None, FAKE + 64, FAKE,
@@ -143,6 +154,18 @@ def test_entry_points_reject_bad_arguments_before_launch(lib):
     assert b"rope table" in lib.cb_last_error_message()
     st = lib.cb_linear(FAKE, FAKE, FAKE, 4, 24, 64, B.CB_BF16, None)
     assert st == 8                    # bf16 N % 16
+
+
+def test_shutdown_releases_state_and_the_library_stays_usable(lib):
+    """cb_shutdown empties the per-device caches; every later call rebuilds what it needs."""
+    d = _dims()
+    before = B.cb_workspace_bytes(d, 416, 416)
+    B.cb_shutdown()
+    B.cb_shutdown()                      # twice in a row is harmless
+    assert B.cb_workspace_bytes(d, 416, 416) == before
+    assert B.cb_hkvd_budget(3840, 0.15, 3840) == 576
+    st = lib.cb_gather_rows(FAKE, FAKE, 3, None, 3, 6, None)
+    assert st == 2 and b"row_bytes" in lib.cb_last_error_message()
 
 
 def test_layer_plan_sizes_match_oracle_selection(lib):
@@ -237,3 +260,11 @@ def test_whole_step_roofline_floor():
             {"kind": "rmsnorm", "bytes": 5e9, "flops": 1e9}]
     got = bench.whole_step_floor_ms(recs, 2, 1e12, 10000.0, 2000.0)
     assert abs(got - 2.0) < 1e-9                           # (1.0 + 0.5 + 1.0 + 0.5) / 2 + 0.5
+
+
+def test_token_ids_are_checked_on_the_host():
+    from non_prefix_kv_gb300 import engine as E
+    np.testing.assert_array_equal(E.check_token_ids([0, 5, 1023], 1024), [0, 5, 1023])
+    for bad in ([0, 1024], [-1, 3], [[1, 2]]):
+        with pytest.raises(ValueError):
+            E.check_token_ids(bad, 1024)

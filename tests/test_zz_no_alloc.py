@@ -65,7 +65,7 @@ def test_noalloc_rejects_more_candidates_than_its_scratch():
     from non_prefix_kv_gb300 import engine as E
     dims = E.make_dims(synth.ModelShape(1, 256, 8, 2, 128, 256, 64, dtype="bf16"))
     fake = 0x10000      # never dereferenced: the size check fails before any launch
-    st = B.lib().cb_kv_deviation_topk_noalloc(fake, fake, fake, fake, None, None, 65537, 10, 0,
+    st = B.lib().cb_kv_deviation_topk_noalloc(fake, fake, 65537, fake, fake, 65537, None, None, 65537, 10, 0,
                                               ctypes.byref(dims), None, fake, None)
     assert st == 8
     assert b"65536" in B.lib().cb_last_error_message()

@@ -67,7 +67,26 @@ def with_text_segments(req_h, vocab, seed=11):
     return segs, toks
 
 
-def run_case(E, wl, r, gradual, tol, check_sets=True, q8=False, segments=False, recompute=False, split=None):
+def loaded_source(E, pool, load, tmp_path):
+    """Layer-ahead loading of the chunk KV: from pinned host memory ("host") or from a file
+    read layer by layer into pinned memory ("file").  The device pool is cleared first (and
+    for the file tier the pinned copy too), so every cached value the blend uses must have
+    travelled through that tier."""
+    hp = E.HostPool(pool)
+    for ts in hp.dev:
+        for t in ts:
+            t.zero_()
+    if load == "host":
+        return {"host_pool": hp}
+    fs = E.FileStore(str(tmp_path / "chunk_store.bin"), hp)
+    for ts in hp.host:
+        for t in ts:
+            t.zero_()
+    return {"file_store": fs}
+
+
+def run_case(E, wl, r, gradual, tol, check_sets=True, q8=False, segments=False, recompute=False, split=None,
+             load=None, tmp_path=None):
     torch = torch_mod()
     shape = wl.shape
     model = synth.make_model(shape, seed=wl.seed)
@@ -94,7 +113,8 @@ def run_case(E, wl, r, gradual, tol, check_sets=True, q8=False, segments=False, 
         pool = q8_pool_from_codes(E, pool, chunk_kv, dm.dims)
     req = E.Request(eng, pool, req_h.order, tokens, segments=segs)
     plan = req.plan(ratios, gradual=gradual)
-    m = E.run_blend(req, plan, keep_history=True, recompute_precheck_kv=recompute, precheck_load_rows=split)
+    src = loaded_source(E, pool, load, tmp_path) if load else {}
+    m = E.run_blend(req, plan, keep_history=True, recompute_precheck_kv=recompute, precheck_load_rows=split, **src)
     from non_prefix_kv_gb300 import binding as B
     B.cb_sync(None)
     forced_teacher = False
@@ -120,7 +140,7 @@ def run_case(E, wl, r, gradual, tol, check_sets=True, q8=False, segments=False, 
                 T = np.setdiff1d(ref["S"][l], ref["forced"]).astype(np.int32)
                 override[l] = torch.from_numpy(T).cuda()
         m = E.run_blend(req, plan, sel_override=override, keep_history=True, recompute_precheck_kv=recompute,
-                        precheck_load_rows=split)
+                        precheck_load_rows=split, **src)
         B.cb_sync(None)
         for l in range(shape.n_layers):
             np.testing.assert_array_equal(req.sel_hist[l].cpu().numpy(), ref["S"][l])
@@ -293,6 +313,28 @@ def test_layer_ahead_loading_matches_resident_pool(E, q8, from_file, recompute, 
     for l in range(wl.shape.n_layers):
         assert torch.equal(ka[l], b.K[l])
     assert torch.equal(xa, b.x_last[:b.m_last]) and ta == int(b.token.item())
+
+
+@pytest.mark.parametrize("load,q8,gradual,extra", [
+    ("host", False, False, {}), ("file", False, True, {}), ("host", True, False, {}), ("file", True, False, {}),
+    ("host", False, False, {"split": 200}), ("file", False, False, {"recompute": True})],
+    ids=["host", "file_gradual", "host_8bit", "file_8bit", "host_split", "file_precheck_recomputed"])
+def test_blend_loaded_layer_by_layer_matches_oracle_f32(E, load, q8, gradual, extra, tmp_path):
+    """The pages' pipeline (CacheBlend explainer §Pipelining and load controller): each layer's
+    chunk KV is loaded one layer ahead, from pinned host memory or from a file, while the
+    previous layer recomputes.  The blend built from the loaded KV (bf16/fp32, or 8-bit codes
+    decoded while re-positioning) matches the oracle's blend over the same store."""
+    wl = synth.WORKLOADS["tiny_f32"]
+    wl = replace(wl, shape=replace(wl.shape, n_layers=3))
+    run_case(E, wl, 0.15, gradual, TOL["f32"], q8=q8, load=load, tmp_path=tmp_path, **extra)
+
+
+@pytest.mark.parametrize("load,extra", [("host", {"split": 160}), ("file", {}), ("host", {"q8": True})],
+                         ids=["host_split", "file", "host_8bit"])
+def test_blend_loaded_layer_by_layer_matches_oracle_bf16(E, load, extra, tmp_path):
+    wl = synth.Workload("bf16_small", BF16_SMALL, chunk_len=96, n_distinct=4, order=(0, 1, 2, 3), n_query=32,
+                        ratio=0.15)
+    run_case(E, wl, 0.15, True, TOL["bf16"], check_sets=False, load=load, tmp_path=tmp_path, **extra)
 
 
 def test_short_request_is_prefilled_in_full(E):

@@ -153,3 +153,118 @@ def test_full_width_layer_of_the_larger_workloads(name):
     assert rel(host(k[0]), ref["K"][0].reshape(n, -1)) < 1e-2
     assert rel(host(v[0]), ref["V"][0].reshape(n, -1)) < 1e-2
     assert rel(host(x_all), ref["x"][1]) < 1e-2
+
+
+@pytest.fixture(scope="module")
+def stepwise(setup):
+    """The three layers of the benchmark's request run one call at a time on the GPU, each
+    on freshly re-positioned chunk KV, with every layer's input and output kept: the
+    pre-check layer over all 4096 rows, the check layer (K/V for every row, deviation, top-k
+    576 + 256 forced rows) and the steady layer over the check layer's rows."""
+    s = setup
+    torch, B, E = s["torch"], s["B"], s["E"]
+    req, dm, eng, wl = s["req"], s["dm"], s["eng"], s["wl"]
+    N, n_c, W, d = wl.n_tokens, wl.n_cached, wl.shape.kv_width, wl.shape.d_model
+
+    def cache(l):
+        k = torch.zeros(N, W, dtype=torch.bfloat16, device="cuda")
+        v = torch.zeros_like(k)
+        B.cb_rope_shift(k[:n_c], v[:n_c], s["pool"].k[l], s["pool"].v[l], req.src_row, req.delta, n_c, dm.dims,
+                        eng.cos_sin, eng.max_pos)
+        return k, v
+
+    x0 = torch.empty(N, d, dtype=torch.bfloat16, device="cuda")
+    B.cb_gather_rows(x0, dm.embed, req.tokens, N, d * 2)
+    x1, x2, x3 = (torch.empty_like(x0) for _ in range(3))
+    s1, s2, s3 = (torch.empty(N, dtype=torch.int32, device="cuda") for _ in range(3))
+    K0, V0 = cache(0)
+    B.cb_blend_layer(dm.dims, dm.layers_c[0], B.CB_LAYER_PRECHECK, x0, None, N, N, n_c, K0, V0, eng.cos_sin,
+                     eng.max_pos, 0, 0, None, x1, s1, None, eng.ws)
+    K1, V1 = cache(1)
+    K1_pre, V1_pre = K1.clone(), V1.clone()
+    scores = torch.empty(N, dtype=torch.float32, device="cuda")
+    k = s["plan"][1][1]
+    m2 = B.cb_blend_layer(dm.dims, dm.layers_c[1], B.CB_LAYER_CHECK, x1, None, N, N, n_c, K1, V1, eng.cos_sin,
+                          eng.max_pos, k, B.CB_DEV_KV, None, x2, s2, scores, eng.ws)
+    K2, V2 = cache(2)
+    K2_pre, V2_pre = K2.clone(), V2.clone()
+    m3 = B.cb_blend_layer(dm.dims, dm.layers_c[2], B.CB_LAYER_STEADY, x2[:m2], s2[:m2], m2, N, n_c, K2, V2,
+                          eng.cos_sin, eng.max_pos, 0, 0, None, x3, s3, None, eng.ws)
+    B.cb_sync(None)
+    S = s2[:m2].cpu().numpy().astype(np.int64)
+    return dict(k=k, S=S, m3=m3, x1=host(x1), x2=host(x2[:m2]), x3=host(x3[:m3]), s3=s3[:m3].cpu().numpy(),
+                scores=scores[:n_c].cpu().numpy().astype(np.float64), K1_pre=host(K1_pre), V1_pre=host(V1_pre),
+                K1=host(K1), V1=host(V1), K2_pre=host(K2_pre), V2_pre=host(V2_pre), K2=host(K2), V2=host(V2))
+
+
+def _oracle_layer_rows(shape, layer, x_rows, rows, K, V, sample):
+    """The oracle's selective recompute of one layer for the given rows (their hidden inputs
+    x_rows, positions = rows): K/V of every row written into K, V (Step 3), then Q,
+    attention over the whole cache and O-proj + FFN for the rows at `sample` (indices into
+    rows).  Returns (K/V rows, the sampled output rows)."""
+    a = O.rmsnorm(x_rows, layer["attn_norm"], shape.rms_eps)
+    p = O.project_qkv(layer, a, rows, shape, want=("k", "v"))
+    K[rows] = p["k"]
+    V[rows] = p["v"]
+    q = O.project_qkv(layer, a[sample], rows[sample], shape, want=("q",))["q"]
+    o = O.attend(q, rows[sample], K, V)
+    return p, O.out_ffn(layer, x_rows[sample], o, shape)
+
+
+def test_check_layer_scores_selection_and_outputs_match_oracle(setup, stepwise):
+    """The check layer at the 7B shape ([CB-A] §Selective recomputation Steps 1-4; §HKVD
+    selection), the oracle fed the GPU's own layer input x1: the deviation scores of all 3840
+    candidates (1e-2 relative), the chosen 576 rows a top-k of the oracle's fp64 scores up to
+    the arithmetic's error, then (teacher-forced with the GPU's set) the recomputed K/V at S,
+    the layer's output rows (a sample, always with the last row) at 1e-2."""
+    s, t = setup, stepwise
+    wl = s["wl"]
+    shape, layer = wl.shape, s["model"]["layers"][1]
+    N, n_c, Hkv, hd = wl.n_tokens, wl.n_cached, shape.n_kv_heads, shape.head_dim
+    rows = np.arange(N)
+    a = O.rmsnorm(t["x1"], layer["attn_norm"], shape.rms_eps)
+    p = O.project_qkv(layer, a, rows, shape, want=("k", "v"))
+    Kc = t["K1_pre"].reshape(N, Hkv, hd)
+    Vc = t["V1_pre"].reshape(N, Hkv, hd)
+    sc = O.kv_deviation(p["k"][:n_c], Kc[:n_c], p["v"][:n_c], Vc[:n_c])
+    assert rel(t["scores"], sc) < 1e-2
+    # the selection: k cached rows + the 256 query rows, ascending
+    k, S = t["k"], t["S"]
+    T = S[S < n_c]
+    assert len(T) == k and np.array_equal(S[k:], np.arange(n_c, N)) and np.all(np.diff(S) > 0)
+    kth = np.sort(sc)[::-1][k - 1]
+    tol = 2e-2 * kth
+    assert sc[T].min() >= kth - tol
+    assert np.delete(sc, T).max() <= kth + tol
+    jacc = len(set(T) & set(O.topk_rows(sc, np.arange(n_c), k))) / len(set(T) | set(O.topk_rows(sc, np.arange(n_c), k)))
+    print(f"check layer: HKVD set Jaccard overlap with the oracle's fp64 top-k {jacc:.3f}")
+    # teacher-forced with the GPU's set: K/V at S, then the sampled output rows
+    K = Kc.copy()
+    V = Vc.copy()
+    sample = np.unique(np.concatenate([np.linspace(0, len(S) - 1, 48).astype(int), [len(S) - 1]]))
+    pk, y = _oracle_layer_rows(shape, layer, t["x1"][S], S, K, V, sample)
+    assert rel(t["K1"][S], pk["k"].reshape(len(S), -1)) < 1e-2
+    assert rel(t["V1"][S], pk["v"].reshape(len(S), -1)) < 1e-2
+    keep = np.setdiff1d(rows, S)
+    np.testing.assert_array_equal(t["K1"][keep], t["K1_pre"][keep])      # rows outside S keep the cache
+    assert rel(t["x2"][sample], y) < 1e-2
+
+
+def test_steady_layer_outputs_and_last_hidden_row_match_oracle(setup, stepwise):
+    """The steady layer at the 7B shape (fixed mode: S_2 = S_1, [CB-A] §Selective
+    recomputation), the oracle fed the GPU's x2 rows: K/V written at S, the sampled output
+    rows and the last hidden row h_last (row N-1, the one the first token comes from) at 1e-2."""
+    s, t = setup, stepwise
+    wl = s["wl"]
+    shape, layer = wl.shape, s["model"]["layers"][2]
+    N, Hkv, hd = wl.n_tokens, shape.n_kv_heads, shape.head_dim
+    S = t["S"]
+    assert t["m3"] == len(S) and np.array_equal(t["s3"], S)
+    K = t["K2_pre"].reshape(N, Hkv, hd).copy()
+    V = t["V2_pre"].reshape(N, Hkv, hd).copy()
+    sample = np.unique(np.concatenate([np.linspace(0, len(S) - 1, 48).astype(int), [len(S) - 1]]))
+    pk, y = _oracle_layer_rows(shape, layer, t["x2"], S, K, V, sample)
+    assert rel(t["K2"][S], pk["k"].reshape(len(S), -1)) < 1e-2
+    assert rel(t["V2"][S], pk["v"].reshape(len(S), -1)) < 1e-2
+    assert rel(t["x3"][sample], y) < 1e-2
+    assert rel(t["x3"][-1], y[-1]) < 1e-2            # h_last

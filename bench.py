@@ -52,6 +52,11 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-quality", action="store_true", help="skip the blend-vs-full-prefill diagnostics")
     p.add_argument("--profile-steps", type=int, default=3)
+    p.add_argument("--cpu-full-step", action="store_true",
+                   help="also time one whole oracle step of the workload (about 140 s on 16 Grace cores at the "
+                        "7B shape)")
+    p.add_argument("--no-deep-stack", action="store_true",
+                   help="skip the 32-layer block (ratio sweep, e2e) that the default N = 1 run adds")
     return p.parse_args(argv)
 
 
@@ -228,6 +233,73 @@ def oracle_sample(wl, frac_rows=4):
     return dt, fl, desc
 
 
+def oracle_full_step(wl_name: str):
+    """Times one whole blended step of the CPU oracle on a workload: assembly (re-rotation of
+    every layer's chunk KV), the pre-check, check and steady (or gradual) layers and the
+    lm_head argmax, fp64 numpy.  The chunk KV is drawn at random with the precomputed
+    caches' shapes (the offline precompute is not part of a step, and the timing does not
+    depend on the values).  Returns (seconds, description)."""
+    import oracle.cacheblend_oracle as O
+    wl = synth.WORKLOADS[wl_name]
+    s = wl.shape
+    model = synth.make_model(s, seed=wl.seed)
+    req = synth.make_requests(wl)[0]
+    L = s.n_layers
+    chunk_kv = []
+    for c in range(len(req.chunk_tokens)):
+        n = len(req.chunk_tokens[c])
+        chunk_kv.append({key: [synth.test_tensor((n, s.n_kv_heads, s.head_dim), 1000 + 7 * c + l, std=0.5)
+                               .astype(np.float64) for l in range(L)] for key in ("K", "V")})
+    ratios = O.ratio_schedule(wl.ratio, L, wl.check_layer, wl.gradual)
+    t0 = time.perf_counter()
+    O.blend(model, chunk_kv, req.order, req.tokens, ratios, check_layer=wl.check_layer, gradual=wl.gradual)
+    dt = time.perf_counter() - t0
+    desc = (f"one whole blended step of {wl.name} ({L} layers, {wl.n_tokens} tokens, r = {wl.ratio}) by the "
+            f"fp64 numpy oracle, measured end to end; chunk KV drawn at random with the precomputed caches' shapes")
+    return dt, desc
+
+
+def oracle_full_step_subprocess(wl_name: str, threads: int, runs: int = 1):
+    """oracle_full_step in a fresh interpreter whose BLAS uses `threads` threads; the median
+    of `runs` steps (seconds)."""
+    env = dict(os.environ)
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = str(threads)
+    code = ("import json, statistics, sys; sys.path.insert(0, %r); import bench; "
+            "t = [bench.oracle_full_step(%r)[0] for _ in range(%d)]; print(json.dumps(statistics.median(t)))"
+            % (ROOT, wl_name, runs))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle timing failed: {r.stderr[-500:]}")
+    return float(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline_leg(wl, full_step: bool):
+    """The oracle on the host cores (rank 0 at N = 1).  value: a bounded sample of the
+    benchmark's workload (a quarter of the steady layer's selected rows at the full shape,
+    about 5-7 s), scaled to one step by the FLOP ratio and labelled as extrapolated.  Beside
+    it: the tiny fp32 workload (configuration 1) timed in full with every core and with one
+    thread, and, with full_step, one whole step of the workload measured once (a minute or
+    more at the 7B shape)."""
+    cores = cpu_threads()
+    dt, fl, sdesc = oracle_sample(wl)
+    t_est = dt * nominal_step_flops(wl) / fl
+    out = {"value": wl.n_tokens * wl.n_requests / t_est, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+           "sample": sdesc, "sample_s": dt, "extrapolated": True, "ms_per_step": t_est * 1e3}
+    if full_step:
+        t_full, desc = oracle_full_step(wl.name)
+        out["full_step_measured"] = {"value": wl.n_tokens * wl.n_requests / t_full, "unit": "tokens/s",
+                                     "ms_per_step": t_full * 1e3, "sample": desc + " (once, no warm-up)"}
+    tiny = synth.WORKLOADS["tiny_f32"]
+    t_tiny = oracle_full_step_subprocess("tiny_f32", cores, runs=3)
+    t_tiny1 = oracle_full_step_subprocess("tiny_f32", 1, runs=3)
+    out["tiny_f32_full"] = {"tokens_per_s": tiny.n_tokens / t_tiny, "ms_per_step": t_tiny * 1e3, "threads": cores,
+                            "runs": 3, "note": "median of 3 whole steps, fresh interpreter"}
+    out["tiny_f32_full_1thread"] = {"tokens_per_s": tiny.n_tokens / t_tiny1, "ms_per_step": t_tiny1 * 1e3,
+                                    "threads": 1, "runs": 3}
+    return out
+
+
 def cpu_threads():
     """Threads the oracle's BLAS runs with: the thread-count variable if one is set, else the
     CPUs this process may run on (its affinity mask, not the machine's logical CPU count)."""
@@ -267,12 +339,16 @@ def reference_arm(args):
         return 0
     wl = synth.WORKLOADS[args.workload]
     full = nominal_step_flops(wl)
-    times = []
+    times, sample_s = [], []
     desc = ""
     for i in range(args.warmup + args.steps):
         dt, fl, desc = oracle_sample(wl)
         if i >= args.warmup:
             times.append(dt * full / fl)
+            sample_s.append(dt)
+    # each step times a bounded sample (a quarter of the steady layer's selected rows at the
+    # full shape) so that the run ends within minutes; the step time is scaled from it by the
+    # algorithmic FLOP ratio, so ms_per_step x steps exceeds the time the arm ran
     t_step = statistics.median(times)
     value = wl.n_tokens * wl.n_requests / t_step
     cores = cpu_threads()
@@ -281,9 +357,15 @@ def reference_arm(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl.name, "n_tokens": wl.n_tokens, "chunks": f"{len(wl.order)}x{wl.chunk_len}",
                        "n_query": wl.n_query, "ratio": wl.ratio, "layers": wl.shape.n_layers},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc,
+                             "extrapolated": True},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-            "ttft_ms": t_step * 1e3}
+            "ttft_ms": t_step * 1e3, "extrapolated": True,
+            "measured_sample_s_per_step": statistics.median(sample_s),
+            "note": "extrapolated: every step times the sample above and scales it to one whole step by the "
+                    "algorithmic FLOP ratio (ms_per_step is that estimate, not a measured time; the time "
+                    "actually spent per step is measured_sample_s_per_step).  A whole step measured once is "
+                    "in the default run's cpu_baseline"}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -478,6 +560,143 @@ def int8_store_e2e(E, B, eng, dm, pool, r0, plan, stream, host_tok, args):
             "first_token": int(out8.item()), "same_first_token": int(out8.item()) == int(r0.token.item()),
             "h_last_rel_diff": float((h8 - h0).norm() / h0.norm()),
             "layer0_cached_k_rel_err": float((k8 - k0).norm() / k0.norm())}
+
+
+def deep_stack_block(args, E, B, torch, local, peaks, link_gbs):
+    """The 32-layer 7B-shaped stack (8 chunks x 480 tokens, two of them repeated, + 256 query
+    tokens, gradual filtering from layer 1), random-init weights drawn on the device.  TTFT at
+    r in {5, 10, 15, 18} % beside the GPU full prefill of the same request, every one replayed
+    from a CUDA graph and timed with CUDA events; at r = 15 % also the whole-step roofline and
+    the end-to-end time through the public API (engine.RequestGraph: token ids in from pinned
+    host memory, every layer's chunk KV loaded one layer ahead from pinned host memory, the
+    first-token id read back)."""
+    wl = synth.WORKLOADS["llama7b_32_4k"]
+    shape = wl.shape
+    L, N = shape.n_layers, wl.n_tokens
+    dm = E.DeviceModel.random_on_device(shape, seed=wl.seed)
+    rh = synth.make_requests(wl)[0]
+    eng = E.BlendEngine(dm, N)
+    pool = eng.precompute_pool(rh.chunk_tokens)
+    req = E.Request(eng, pool, rh.order, rh.tokens)
+    stream = torch.cuda.Stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def plan_for(r):
+        ratios = [None if l < wl.check_layer else
+                  (B.cb_gradual_ratio(r, l, wl.check_layer, 1.5) if wl.gradual else r) for l in range(L)]
+        return E.layer_plan(shape, N, wl.n_cached, ratios, wl.check_layer, wl.gradual)
+
+    def time_graph(fn, steps):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        with torch.cuda.stream(stream):
+            for _ in range(max(args.warmup, 3)):
+                g.replay()
+        stream.synchronize()
+        ev0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(steps):
+                g.replay()
+        ev1.record(stream)
+        stream.synchronize()
+        B.cb_sync(stream, 120.0)
+        return ev0.elapsed_time(ev1) / steps
+
+    h_last = torch.empty(shape.d_model, dtype=torch.bfloat16, device=req.tokens.device)
+    full_tok = torch.empty(1, dtype=torch.int32, device=req.tokens.device)
+
+    def full_step():
+        eng.full_prefill(req.tokens, req.K, req.V, h_last)
+        B.cb_lmhead_argmax(h_last, dm.final_norm, dm.w_lm, dm.dims, None, full_tok, eng.ws)
+
+    sweep = []
+    with ClockSampler(local) as clk:
+        for r in (0.05, 0.10, 0.15, 0.18):
+            plan = plan_for(r)
+            ms = time_graph(lambda: E.run_blend(req, plan), args.steps)
+            sweep.append({"ratio": r, "ttft_ms": ms, "tokens_per_s": N / (ms / 1e3),
+                          "check_layer_k": plan[wl.check_layer][1], "last_layer_k": plan[-1][1]})
+        full_ms = time_graph(full_step, max(3, min(args.steps, 10)))
+    clocks = clk.summary()
+    for e in sweep:
+        e["full_prefill_ttft_ms"] = full_ms
+        e["speedup_vs_full_prefill"] = full_ms / e["ttft_ms"]
+    head = next(e for e in sweep if e["ratio"] == wl.ratio)
+
+    # whole-step roofline at r = 15 % (per-launch events, eager; re-positioning on the layers' stream)
+    plan = plan_for(wl.ratio)
+    B.cb_profile_begin(200000)
+    with torch.cuda.stream(stream):
+        for _ in range(args.profile_steps):
+            E.run_blend(req, plan, overlap_assembly=False)
+    recs = B.cb_profile_end(200000)
+    with torch.cuda.stream(stream):
+        E.run_blend(req, plan, keep_history=True)
+    stream.synchronize()
+    sel_sums = []
+    for l, (mode, _) in enumerate(plan):
+        S = req.sel_hist[l].cpu().numpy().astype(np.float64)
+        name = {B.CB_LAYER_PRECHECK: "precheck", B.CB_LAYER_CHECK: "check", B.CB_LAYER_STEADY: "steady",
+                B.CB_LAYER_GRADUAL: "gradual"}[mode]
+        sel_sums.append((len(S), float(np.sum(S + 1)), name))
+    attn_flops = sum(4.0 * shape.n_heads * shape.head_dim * ps for _, ps, _ in sel_sums)
+    capped = "sw_power_cap" in (clocks.get("reasons") or [])
+    pkey = "bf16_tflops_sustained" if capped else "bf16_tflops"
+    tflops = peaks.get(pkey, FALLBACK_PEAKS[pkey])
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    floor = whole_step_floor_ms(recs, args.profile_steps, attn_flops, hbm, tflops)
+    g_ms = sum(r["ms"] for r in recs if r["kind"] == "gemm")
+    g_fl = sum(r["flops"] for r in recs if r["kind"] == "gemm")
+    gemm_tflops = g_fl / (g_ms / 1e3) / 1e12 if g_ms else 1.0
+    step_flops_ = step_flops(wl, sel_sums)
+    out = {"workload": wl.name, "layers": L, "n_tokens": N, "chunks": f"{len(wl.order)}x{wl.chunk_len}",
+           "n_query": wl.n_query, "gradual": wl.gradual, "ratio": wl.ratio,
+           "ttft_ms": head["ttft_ms"], "tokens_per_s": head["tokens_per_s"],
+           "full_prefill_ttft_ms": full_ms, "speedup_vs_full_prefill": head["speedup_vs_full_prefill"],
+           "ratio_sweep": sweep, "clocks": clocks,
+           "step_tflops": step_flops_ / (head["ttft_ms"] / 1e3) / 1e12,
+           "step_roofline": {"floor_ms": floor, "measured_ms": head["ttft_ms"], "frac": floor / head["ttft_ms"],
+                             "tensor_peak_tflops": tflops, "peak_source": pkey,
+                             "model": "sum over the step's launches of max(algorithmic bytes / measured copy GB/s, "
+                                      "FLOPs / measured bf16 TFLOP/s)"},
+           "rows_per_layer": [m for m, _, _ in sel_sums],
+           "timing": "CUDA-graph replays timed with CUDA events on the launching stream; inputs (13 GB of weights, "
+                     "chunk KV, blended KV) far larger than L2"}
+
+    # end to end through the public API
+    hp = E.HostPool(pool)
+    pre = [l for l, (mode, _) in enumerate(plan) if mode == B.CB_LAYER_PRECHECK]
+    split = E.precheck_split_rows(shape, N, req.n_cached, link_gbs or 200.0, max(gemm_tflops, 1.0), hbm)
+    rg = E.RequestGraph(req, plan, host_pool=hp, stream=stream, precheck_load_rows=split)
+    times, tok = [], None
+    for i in range(args.warmup + args.steps):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        tok = rg.run(req.tokens_host)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    # the same request from the device-resident pool with the same pre-check split: the loaded
+    # run must give the same first token
+    with torch.cuda.stream(stream):
+        E.run_blend(req, plan, precheck_load_rows=split)
+    stream.synchronize()
+    row_b = pool.k[0].shape[1] * pool.k[0].element_size()
+    h2d = hp.nbytes + N * 4 - sum(t.numel() * t.element_size() for l in pre for t in hp.host[l]) + \
+        sum(2 * n * row_b for l in pre for _, n in req.pool_ranges(split))
+    t_e = statistics.median(times)
+    out["e2e"] = {"value": N / t_e, "unit": "tokens/s", "ttft_ms": t_e * 1e3, "h2d_bytes_per_step": int(h2d),
+                  "d2h_bytes_per_step": 4, "precheck_load_rows": split, "first_token": tok,
+                  "same_first_token_as_resident_run": tok == int(req.token.item()),
+                  "api": "engine.RequestGraph(req, plan, host_pool=..., precheck_load_rows=X).run(tokens): token "
+                         "ids in from pinned host memory, every layer's chunk KV loaded one layer ahead from pinned "
+                         "host memory on a side stream, the first-token id read back; host wall clock"}
+    del rg, hp
+    return out
 
 
 def our_arm(args):
@@ -821,13 +1040,17 @@ def our_arm(args):
                                            full_ms / shape.n_layers, e2e["h2d_gbs_serial"])
     B.cb_sync(stream, 120.0)
 
+    # ---------------- the 32-layer stack (N = 1 only): ratio sweep beside the full prefill
+    deep = None
+    if world == 1 and not args.no_deep_stack:
+        deep = deep_stack_block(args, E, B, torch, local, peaks,
+                                e2e.get("h2d_gbs_serial") if e2e else None)
+        torch.cuda.empty_cache()
+
     # ---------------- CPU oracle baseline (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        dt, fl, desc = oracle_sample(wl)
-        t_step = dt * nominal_step_flops(wl) / fl
-        cpu = {"value": wl.n_tokens / t_step, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-               "sample": desc, "sample_s": dt}
+        cpu = cpu_baseline_leg(wl, args.cpu_full_step)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -843,6 +1066,7 @@ def our_arm(args):
         "step_tflops": flops / (ms / 1e3) / 1e12,
         "roofline": roofline, "step_roofline": step_roofline, "layers": layers_ms, "hbm_kernels": hbm_kernels, "kernels": kernels, "gemm_launches": gemm_detail,
         "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "full_prefill": full, "quality_diagnostics": quality,
+        "deep_stack": deep,
         "setup_s": setup_s,
     }
     if rank == 0:

@@ -6,15 +6,15 @@
 //   S_j = Q K_j^T          tcgen05.mma, A = Q (K-major), B = K_j (K-major), into TMEM
 //   P_j = exp2(S_j * log2(e)/sqrt(hd) - m)   softmax warps, row = TMEM lane, key t of a
 //                          row visible iff t <= q_pos[row]
-//   O  += P_j V_j          tcgen05.mma, B = V_j (MN-major), fp32 accumulator in TMEM
-// The running max m is raised lazily: O is rescaled only when a row's max grows by more
-// than 2^8, so most tiles never touch O.  One CTA per (128-query tile, query head), launched
-// heads fastest and longest query tiles first.  S is triple-buffered in TMEM (S_0 | S_1 | S_2
-// | O), so S_{j+1} and S_{j+2} are computed while the softmax works on S_j; P_j is written
-// back over S_j in TMEM (bf16 pairs) and the P.V MMA takes its A operand from there; K and V
-// stream through a TMA ring.  Warp roles: 0 = TMA producer, 1 = TMEM allocator + MMA issuer
-// (the whole warp runs the issue loop, the elected lane issues), 2..9 = softmax and
-// epilogue; warp w reads TMEM lanes 32*(w%4)..+31.
+//   O  += P_j V_j          tcgen05.mma, A = P_j from TMEM, B = V_j (MN-major), fp32 in TMEM
+// Two softmax groups take alternate key tiles, each with its own S buffer, running max, row
+// sum and O accumulator (TMEM: S_0 | S_1 | O_0 | O_1); one thread owns one query row of its
+// group's tiles, so no warp waits for another until the two halves of the key range are
+// merged at the end.  The running max is raised lazily: O is rescaled only when a row's max
+// grows by more than 2^8.  One CTA per (128-query tile, query head); K and V stream through
+// a TMA ring.  Warp roles: 0 = TMA producer, 1 = TMEM allocator + MMA issuer (the whole warp
+// runs the issue loop, the elected lane issues), 2..9 = softmax groups and epilogue; warp w
+// reads TMEM lanes 32*(w%4)..+31.
 #include <cuda.h>
 #include <math.h>
 
@@ -40,26 +40,10 @@ namespace {
 constexpr int BM = 128;              // queries per CTA
 constexpr int BN = 128;              // keys per tile
 constexpr int SLAB = 128 * 128;      // bytes of one [128 rows x 64 bf16] swizzled slab
-constexpr int NSOFT = 8;             // softmax warps: two per TMEM lane quarter
+constexpr int NSOFT = 8;             // softmax warps: two groups of one per TMEM lane quarter
 constexpr int THREADS = 32 * (2 + NSOFT);
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S0 = 0, TM_O1 = 384;  // S_0 | S_1 | S_2 | O
 constexpr float kRescaleLog2 = 8.0f;
-
-template <int HD>
-struct Layout {
-  static constexpr int NSLAB = HD / 64;
-  static constexpr int Q_BYTES = NSLAB * SLAB;
-  static constexpr int KV_BYTES = NSLAB * SLAB;
-  static constexpr int KV_STAGES = HD == 128 ? 5 : 10;      // ring K_0, V_0, K_1, V_1, ...
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = OFF_Q + Q_BYTES;
-  static constexpr int OFF_X = OFF_KV + KV_STAGES * KV_BYTES;  // row max / sum exchange
-  static constexpr int X_BYTES = (2 * 2 + 2) * BM * 4;
-  static constexpr int OFF_BAR = OFF_X + X_BYTES;
-  static constexpr int BYTES = OFF_BAR + 256;
-  static constexpr int SMEM = BYTES + 1024;
-};
 
 // Packed fp32 pairs (sm_100+): one instruction updates two score elements.
 __device__ __forceinline__ uint64_t f2_pack(float a, float b) {
@@ -91,38 +75,58 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, %0;" ::"n"(NSOFT * 32) : "memory"); }
 
-// One 128-query tile per CTA.  TMEM: S_0 | S_1 | S_2 | O; key tile j's scores go to S_{j%3},
-// so S(j+1) is computed while the softmax works on S(j).  The softmax writes P(j) (bf16, two
-// keys per 32-bit column) over the first 64 columns of S_{j%3} and O += P(j) V_j takes its A
-// operand from there; S(j+3) reuses the buffer once that P.V has completed.  Eight softmax
-// warps, two per TMEM lane quarter: `half` 0 owns keys 0..63 of each tile and O columns
-// 0..HD/2-1, half 1 the rest; the two exchange row maxima and sums through shared memory.
+// ---- two softmax groups on alternating key tiles ------------------------------------------
+// TMEM: S_0 | S_1 | O_0 | O_1.  Group g (warps 2 + 4g .. 5 + 4g, one per TMEM lane quarter)
+// owns the key tiles j = g, g + 2, ...: each of its threads reads one query row's 128 scores
+// of S_g, keeps that row's running maximum and sum for the group's tiles, writes P_j (bf16
+// pairs) over S_g and the tensor core adds P_j V_j into O_g.  Neither group waits for the
+// other until the end, where the two partial results are merged per row:
+//   O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / (l_0 2^(m_0 - m) + l_1 2^(m_1 - m)),  m = max(m_0, m_1),
+// the same online-softmax algebra that joins consecutive tiles, applied to two interleaved
+// halves of the key range.  While one group exponentiates, the tensor core works on the
+// other group's tiles; S(j + 2) reuses S_g once P.V(j) has completed.
+template <int HD>
+struct Layout {
+  static constexpr int NSLAB = HD / 64;
+  static constexpr int Q_BYTES = NSLAB * SLAB;
+  static constexpr int KV_BYTES = NSLAB * SLAB;
+  static constexpr int KV_STAGES = HD == 128 ? 5 : 10;      // ring K_0, V_0, K_1, V_1, ...
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = OFF_Q + Q_BYTES;
+  static constexpr int OFF_X = OFF_KV + KV_STAGES * KV_BYTES;  // per group: row max, row sum
+  static constexpr int X_BYTES = 2 * 2 * BM * 4;
+  static constexpr int OFF_BAR = OFF_X + X_BYTES;
+  static constexpr int BYTES = OFF_BAR + 256;
+  static constexpr int SMEM = BYTES + 1024;
+  static_assert((1 + 6 + 2 * KV_STAGES) * 8 + 8 <= 256, "barriers exceed their region");
+};
+constexpr uint32_t TM2_O = 2 * BN;   // O_0 at column 256, O_1 right after it
+
 template <int HD>
 __global__ void __launch_bounds__(THREADS, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-              const __grid_constant__ CUtensorMap tmV, const int32_t* __restrict__ q_pos, int M,
-              int64_t n_kv, int H, int Hkv, bf16* __restrict__ out, float scale_log2) {
+               const __grid_constant__ CUtensorMap tmV, const int32_t* __restrict__ q_pos, int M,
+               int64_t n_kv, int H, int Hkv, bf16* __restrict__ out, float scale_log2) {
   pdl_wait();
   pdl_trigger();
   using L = Layout<HD>;
   constexpr int NST = L::KV_STAGES;
-  constexpr int NSB = 3;   // S buffers: S_0 | S_1 | S_2 | O fill the 512 TMEM columns
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = tc::smem_u32(smem_raw);
   uint8_t* base = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
   uint8_t* sQ = base + L::OFF_Q;
   uint8_t* sKV = base + L::OFF_KV;
-  float* xmax = reinterpret_cast<float*>(base + L::OFF_X);   // [2 parity][2 half][BM]
-  float* xsum = xmax + 4 * BM;                                 // [2 half][BM]
+  float* xm = reinterpret_cast<float*>(base + L::OFF_X);   // [2 groups][BM] row max
+  float* xl = xm + 2 * BM;                                  // [2 groups][BM] row sum
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::OFF_BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* s_full = bars + 1;           // [NSB S buffers]
-  uint64_t* p_full = bars + 1 + NSB;     // [NSB]
-  uint64_t* pv_done = bars + 1 + 2 * NSB;  // [NSB]
-  uint64_t* kv_full = bars + 1 + 3 * NSB;  // [NST]
-  uint64_t* kv_empty = kv_full + NST;      // [NST]
+  uint64_t* s_full = bars + 1;     // [2] per group: S_g holds tile j's scores
+  uint64_t* p_full = bars + 3;     // [2] the group's four warps wrote P_j
+  uint64_t* pv_done = bars + 5;    // [2] P_j V_j into O_g completed
+  uint64_t* kv_full = bars + 7;    // [NST]
+  uint64_t* kv_empty = kv_full + NST;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(kv_empty + NST);
-  int* s_qmax = reinterpret_cast<int*>(kv_empty + NST + 1);
+  int* s_qmax = reinterpret_cast<int*>(kv_empty + NST) + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Query tiles are cut from the end of the (position-sorted) rows: tile y holds rows
@@ -131,14 +135,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   // fastest in launch order and the latest (longest) query tiles come first, so every
   // head's heavy tiles start in the first wave and the short ones fill in behind.
   const int h = blockIdx.x;
-  const int g = h / (H / Hkv);
-  const int m0 = M - (int)(blockIdx.y + 1) * BM;   // may be negative for the first rows' tile
+  const int g_kv = h / (H / Hkv);
+  const int m0 = M - (int)(blockIdx.y + 1) * BM;
 
   if (threadIdx.x == 0) {
     tc::mbar_init(q_full, 1);
-    for (int i = 0; i < NSB; ++i) {
+    for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&s_full[i], 1);
-      tc::mbar_init(&p_full[i], NSOFT);
+      tc::mbar_init(&p_full[i], 4);
       tc::mbar_init(&pv_done[i], 1);
     }
     for (int i = 0; i < NST; ++i) {
@@ -151,7 +155,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc::tma_prefetch_desc(&tmV);
   }
   if (warp == 0) {
-    // furthest key any query of this tile may see
     int mx = 0;
     for (int i = lane; i < BM; i += 32) {
       const int m = m0 + i;
@@ -185,7 +188,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------------ TMA producer
     tc::mbar_expect_tx(q_full, L::Q_BYTES);
     for (int s = 0; s < L::NSLAB; ++s) tc::tma_load_2d(sQ + s * SLAB, &tmQ, q_full, h * HD + 64 * s, m0);
-    // ring entry i: K_{i/2} (i even) or V_{i/2} (i odd)
     for (int i = 0; i < 2 * T; ++i) {
       const int st = i % NST;
       if (!tc::mbar_wait(&kv_empty[st], ((i / NST) & 1) ^ 1)) {
@@ -195,26 +197,22 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::mbar_expect_tx(&kv_full[st], L::KV_BYTES);
       const CUtensorMap* map = (i & 1) ? &tmV : &tmK;
       for (int s = 0; s < L::NSLAB; ++s)
-        tc::tma_load_2d(sKV + st * L::KV_BYTES + s * SLAB, map, &kv_full[st], g * HD + 64 * s, (i >> 1) * BN);
+        tc::tma_load_2d(sKV + st * L::KV_BYTES + s * SLAB, map, &kv_full[st], g_kv * HD + 64 * s, (i >> 1) * BN);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer (warp 1)
-    // S(0), S(1), then per key tile j: P.V(j) once its P is written, then S(j+2) into the
-    // buffer of tile j-1, whose P.V was issued a softmax earlier and has normally completed.
-    // The whole warp runs the loop and waits; the elected lane issues.
+    // S(0), S(1); then per key tile j: P.V(j) once its group wrote P, and S(j + 2) into the
+    // same group's buffer once that P.V has completed.
     constexpr uint32_t idesc_s = tc::idesc_bf16_f32(BM, BN);
     constexpr uint32_t idesc_o = tc::idesc_bf16_f32(BM, HD, true);
-    // descriptor of K/V slot 0 and of Q; the address field (bits 0-13, bytes >> 4) is advanced
-    // by plain addition below
     const uint64_t kv_desc = tc::desc_sw128(tc::smem_u32(sKV));
     const uint64_t v_desc = tc::desc_sw128_mn(tc::smem_u32(sKV), SLAB);
     const uint64_t q_desc = tc::desc_sw128(tc::smem_u32(sQ));
-    // ok stays warp-uniform, so every lane reaches each elect.sync / __syncwarp
     bool ok = __all_sync(0xffffffffu, tc::mbar_wait(q_full, 0));
     auto issue_s = [&](int jj) {
-      const int b = jj % NSB, i = 2 * jj, st = i % NST;
+      const int b = jj & 1, i = 2 * jj, st = i % NST;
       ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(&kv_full[st], (i / NST) & 1) &&
-                                             (jj < NSB || tc::mbar_wait(&pv_done[b], ((jj - NSB) / NSB) & 1)));
+                                             (jj < 2 || tc::mbar_wait(&pv_done[b], ((jj - 2) >> 1) & 1)));
       if (!ok) return;
       tc::tc_fence_after();
       if (tc::elect_one()) {
@@ -222,7 +220,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const uint32_t off = ((k >> 2) * SLAB + (k & 3) * 32) >> 4;
-          tc::mma_bf16(tmem + TM_S0 + b * BN, q_desc + off, kd + off, idesc_s, k > 0);
+          tc::mma_bf16(tmem + b * BN, q_desc + off, kd + off, idesc_s, k > 0);
         }
         tc::mma_commit(&s_full[b]);
         tc::mma_commit(&kv_empty[st]);
@@ -230,18 +228,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
     };
     auto issue_pv = [&](int jj) {
-      const int b = jj % NSB, i = 2 * jj + 1, st = i % NST;
-      ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(&p_full[b], (jj / NSB) & 1) &&
+      const int b = jj & 1, i = 2 * jj + 1, st = i % NST;
+      ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(&p_full[b], (jj >> 1) & 1) &&
                                              tc::mbar_wait(&kv_full[st], (i / NST) & 1));
       if (!ok) return;
       tc::tc_fence_after();
       if (tc::elect_one()) {
         const uint64_t vd = v_desc + (uint64_t)((st * L::KV_BYTES) >> 4);
-        const uint32_t pa = tmem + TM_S0 + b * BN;
+        const uint32_t pa = tmem + b * BN;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          tc::mma_bf16_ts(tmem + TM_O1, pa + k * 8, vd + (uint64_t)((k * 16 * 128) >> 4), idesc_o,
-                          (jj > 0 || k > 0) ? 1u : 0u);
+          tc::mma_bf16_ts(tmem + TM2_O + b * HD, pa + k * 8, vd + (uint64_t)((k * 16 * 128) >> 4), idesc_o,
+                          (jj >= 2 || k > 0) ? 1u : 0u);
         tc::mma_commit(&pv_done[b]);
         tc::mma_commit(&kv_empty[st]);
       }
@@ -255,10 +253,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (!ok && lane == 0) atomicOr(&g_err_attn_tc, ERRBIT_TIMEOUT);
   } else if (warp >= 2) {
-    // ------------------------------------------------------------------ softmax + epilogue
-    const int lane_base = (warp & 3) * 32;
-    const int half = (warp - 2) >> 2;
-    const int r = lane_base + lane;
+    // ------------------------------------------------------------------ softmax groups
+    const int grp = (warp - 2) >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
     const int m = m0 + r;
     const bool row_valid = m >= 0 && m < M;
     int qp = 0;
@@ -266,69 +264,60 @@ __global__ void __launch_bounds__(THREADS, 1)
       qp = q_pos[m];
       qp = qp < 0 ? 0 : (qp >= n_kv ? (int)(n_kv - 1) : qp);
     }
-    const uint32_t trow = tmem + (static_cast<uint32_t>(lane_base) << 16);
-    const uint32_t tO = trow + TM_O1 + half * (HD / 2);
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t tS = trow + grp * BN;
+    const uint32_t tO = trow + TM2_O + grp * HD;
     float m_used = -INFINITY, l = 0.f;
-    // ok is warp-uniform.  A failed (timed-out) wait stops the work of this warp but never
-    // the loop: every softmax warp reaches every named barrier, so none can be left waiting.
-    bool ok = true;
-    for (int j = 0; j < T; ++j) {
-      const int b = j % NSB;
-      ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(&s_full[b], (j / NSB) & 1));
-      const uint32_t tS = trow + TM_S0 + b * BN;
-      const int key0 = j * BN + half * 64;
-      // every key of this half lies beyond the positions of all 32 rows of this warp (scattered
-      // selected rows): the scores are neither read nor exponentiated, P is written as zeros
+    bool ok = true;   // warp-uniform; a failed wait stops the work, never the loop
+    int u = 0;        // this group's tile count
+    for (int j = grp; j < T; j += 2, ++u) {
+      ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(&s_full[grp], u & 1));
+      const int key0 = j * BN;
+      // every key of this tile lies beyond all 32 rows' positions: no load, P = 0
       const bool none = __all_sync(0xffffffffu, key0 > qp);
-      uint32_t sr[64];
-      if (ok && !none) {
-        tc::tc_fence_after();
-        tc::tmem_ld32_nowait(tS + half * 64, sr);
-        tc::tmem_ld32_nowait(tS + half * 64 + 32, sr + 32);
-        tc::tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) sr[i] = 0u;
-      }
-      const bool full_row = key0 + 63 <= qp;            // no causal mask in these 64 keys
+      const bool full_row = key0 + BN - 1 <= qp;
+      // pass 1: the row's maximum over the tile, 64 columns at a time (a whole 128-column row
+      // does not fit in the registers three warps per sub-partition leave)
       float pmx[4];
 #pragma unroll
       for (int a = 0; a < 4; ++a) pmx[a] = -INFINITY;
-      if (none) {
-        // nothing visible: the maximum stays -inf
-      } else if (full_row) {
+      if (ok && !none) {
+        tc::tc_fence_after();
 #pragma unroll
-        for (int i = 0; i < 64; i += 8) {
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t sr[64];
+          tc::tmem_ld32_nowait(tS + hf * 64, sr);
+          tc::tmem_ld32_nowait(tS + hf * 64 + 32, sr + 32);
+          tc::tmem_wait_ld();
+          if (full_row) {
 #pragma unroll
-          for (int a = 0; a < 4; ++a)
-            pmx[a] = fmax3(pmx[a], __uint_as_float(sr[i + 2 * a]), __uint_as_float(sr[i + 2 * a + 1]));
+            for (int i = 0; i < 64; i += 8) {
+#pragma unroll
+              for (int a = 0; a < 4; ++a)
+                pmx[a] = fmax3(pmx[a], __uint_as_float(sr[i + 2 * a]), __uint_as_float(sr[i + 2 * a + 1]));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+              if (key0 + hf * 64 + i <= qp) pmx[i & 3] = fmaxf(pmx[i & 3], __uint_as_float(sr[i]));
+          }
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (key0 + i <= qp) pmx[i & 3] = fmaxf(pmx[i & 3], __uint_as_float(sr[i]));
       }
-      float* xm = xmax + (j & 1) * 2 * BM;
-      xm[half * BM + r] = fmaxf(fmax3(pmx[0], pmx[1], pmx[2]), pmx[3]);
-      // after this barrier both halves have read their scores: P may overwrite them
-      tc::tc_fence_before();
-      softmax_bar();
-      tc::tc_fence_after();
       if (!ok) continue;
-      const float mt = fmaxf(xm[r], xm[BM + r]) * scale_log2;
+      const float mt = fmaxf(fmaxf(pmx[0], pmx[1]), fmaxf(pmx[2], pmx[3])) * scale_log2;
       const float m_new = fmaxf(m_used, mt);
-      if (j == 0) {
-        m_used = m_new;
+      if (u == 0) {
+        m_used = m_new;            // O_g is written, not added to, by this tile's P.V
       } else {
         const bool need = m_new > m_used + kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
-          // O must be stable: the previous tile's P.V has completed
-          ok = __all_sync(0xffffffffu, tc::mbar_wait(&pv_done[(j - 1) % NSB], ((j - 1) / NSB) & 1));
+          // O_g must be stable: the group's previous P.V has completed
+          ok = __all_sync(0xffffffffu, tc::mbar_wait(&pv_done[grp], (u - 1) & 1));
           if (!ok) continue;
           tc::tc_fence_after();
           const float alpha = need ? tc::ex2_approx(m_used - m_new) : 1.0f;
 #pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
+          for (int c = 0; c < HD / 16; ++c) {
             float o[16];
             tc::tmem_ld16(tO + c * 16, o);
 #pragma unroll
@@ -339,37 +328,48 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (need) m_used = m_new;
         }
       }
-      // p = 2^(s * log2(e)/sqrt(hd) - m), scaled and shifted two scores per instruction;
-      // keys 2w, 2w+1 of this half go to P column half * 32 + w
+      // pass 2: P = 2^(s * log2(e)/sqrt(hd) - m), two scores per packed instruction; keys 2w,
+      // 2w+1 go to P column w (bf16 pair).  Keys 0..63 are read again and their P written to
+      // columns 0..31 before keys 64..127 are read; P of those lands in columns 32..63, whose
+      // scores were read in the first half.
       const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-m_used, -m_used);
       uint64_t ls2[4];
 #pragma unroll
       for (int a = 0; a < 4; ++a) ls2[a] = 0ull;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t pk[16];
-        if (none) {
-#pragma unroll
-          for (int w = 0; w < 16; ++w) pk[w] = 0u;
-          tc::tmem_st16u_nowait(tS + half * 32 + c * 16, pk);
-          continue;
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sr[64];
+        if (!none) {
+          tc::tmem_ld32_nowait(tS + hf * 64, sr);
+          tc::tmem_ld32_nowait(tS + hf * 64 + 32, sr + 32);
+          tc::tmem_wait_ld();
         }
 #pragma unroll
-        for (int w = 0; w < 16; ++w) {
-          const int k0 = c * 32 + 2 * w;
-          const float2 z =
-              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k0]), __uint_as_float(sr[k0 + 1])), sc2, nm2));
-          float p0 = tc::ex2_approx(z.x);
-          float p1 = tc::ex2_approx(z.y);
-          if (!full_row) {
-            p0 = (key0 + k0 <= qp) ? p0 : 0.f;
-            p1 = (key0 + k0 + 1 <= qp) ? p1 : 0.f;
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[16];
+          if (none) {
+#pragma unroll
+            for (int w = 0; w < 16; ++w) pk[w] = 0u;
+          } else {
+#pragma unroll
+            for (int w = 0; w < 16; ++w) {
+              const int k0 = c * 32 + 2 * w;
+              const int key = key0 + hf * 64 + k0;
+              const float2 z =
+                  f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k0]), __uint_as_float(sr[k0 + 1])), sc2, nm2));
+              float p0 = tc::ex2_approx(z.x);
+              float p1 = tc::ex2_approx(z.y);
+              if (!full_row) {
+                p0 = (key <= qp) ? p0 : 0.f;
+                p1 = (key + 1 <= qp) ? p1 : 0.f;
+              }
+              ls2[w & 3] = f2_add(ls2[w & 3], f2_pack(p0, p1));
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+              pk[w] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
           }
-          ls2[w & 3] = f2_add(ls2[w & 3], f2_pack(p0, p1));
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-          pk[w] = *reinterpret_cast<const uint32_t*>(&b2);
+          tc::tmem_st16u_nowait(tS + hf * 32 + c * 16, pk);
         }
-        tc::tmem_st16u_nowait(tS + half * 32 + c * 16, pk);
       }
       {
         const float2 a = f2_unpack(f2_add(ls2[0], ls2[1])), c = f2_unpack(f2_add(ls2[2], ls2[3]));
@@ -378,29 +378,44 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::tmem_wait_st();
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&p_full[b]);
+      if (lane == 0) tc::mbar_arrive(&p_full[grp]);
     }
-    const bool done = ok && __all_sync(0xffffffffu, tc::mbar_wait(&pv_done[(T - 1) % NSB], ((T - 1) / NSB) & 1));
-    // row sum = both halves' partial sums (every softmax warp reaches this barrier)
-    xsum[half * BM + r] = l;
-    softmax_bar();
+    // the group's last P.V, then both groups' row statistics meet in shared memory
+    const bool done = ok && (u == 0 || __all_sync(0xffffffffu, tc::mbar_wait(&pv_done[grp], (u - 1) & 1)));
+    xm[grp * BM + r] = m_used;
+    xl[grp * BM + r] = l;
+    tc::tc_fence_before();
+    softmax_bar();   // every softmax warp reaches this barrier exactly once
     if (done) {
       tc::tc_fence_after();
-      const float lt = xsum[r] + xsum[BM + r];
+      const bool has1 = T > 1;       // group 1 saw at least one tile (else O_1 was never written)
+      const float ma = xm[r], mb = has1 ? xm[BM + r] : -INFINITY;
+      const float mm = fmaxf(ma, mb);
+      const float a0 = ma == -INFINITY ? 0.f : tc::ex2_approx(ma - mm);
+      const float a1 = mb == -INFINITY ? 0.f : tc::ex2_approx(mb - mm);
+      const float lt = xl[r] * a0 + (has1 ? xl[BM + r] * a1 : 0.f);
       const float inv = lt > 0.f ? 1.0f / lt : 0.f;
-      bf16* orow = out + (int64_t)(row_valid ? m : 0) * H * HD + (int64_t)h * HD + half * (HD / 2);
+      // group g finalises output columns [g HD/2, (g + 1) HD/2) of its rows
+      bf16* orow = out + (int64_t)(row_valid ? m : 0) * H * HD + (int64_t)h * HD + grp * (HD / 2);
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
-        float o[16];
-        tc::tmem_ld16(tO + c * 16, o);
+        const uint32_t col = TM2_O + grp * (HD / 2) + c * 16;
+        float o0[16], o1[16];
+        tc::tmem_ld16(trow + col, o0);
+        if (has1) {
+          tc::tmem_ld16(trow + col + HD, o1);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) o[i] *= inv;
+          for (int i = 0; i < 16; ++i) o1[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o0[i] = (o0[i] * a0 + o1[i] * a1) * inv;
         if (row_valid) {
           if ((reinterpret_cast<uintptr_t>(orow + c * 16) & 31) == 0) {
-            st16_v8(orow + c * 16, o);
+            st16_v8(orow + c * 16, o0);
           } else {
-            st8(orow + c * 16, o);
-            st8(orow + c * 16 + 8, o + 8);
+            st8(orow + c * 16, o0);
+            st8(orow + c * 16 + 8, o0 + 8);
           }
         }
       }
@@ -461,6 +476,8 @@ cudaError_t launch_hd(const void* q, const int32_t* q_pos, int M, const void* kc
       !make_map(&tk, kc, n_kv, (int64_t)Hkv * HD, (int64_t)Hkv * HD) ||
       !make_map(&tv, vc, n_kv, (int64_t)Hkv * HD, (int64_t)Hkv * HD))
     return cudaErrorInvalidValue;
+  auto kern = k_attn_tc<HD>;
+  const int smem = Layout<HD>::SMEM;
   {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -473,7 +490,7 @@ cudaError_t launch_hd(const void* q, const int32_t* q_pos, int M, const void* kc
       set = (g_attn_attr[dev] & bit) != 0;
     }
     if (!set) {
-      e = cudaFuncSetAttribute(k_attn_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<HD>::SMEM);
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
       if (cached) {
         std::lock_guard<std::mutex> g(g_attn_mu);
@@ -483,7 +500,7 @@ cudaError_t launch_hd(const void* q, const int32_t* q_pos, int M, const void* kc
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
   dim3 grid(H, (M + BM - 1) / BM);
-  { const cudaError_t e_ = launch_k(k_attn_tc<HD>, dim3(grid), dim3(THREADS), Layout<HD>::SMEM, s, tq, tk, tv, q_pos, M, n_kv, H, Hkv,
+  { const cudaError_t e_ = launch_k(kern, dim3(grid), dim3(THREADS), smem, s, tq, tk, tv, q_pos, M, n_kv, H, Hkv,
                                     static_cast<bf16*>(out), scale_log2); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }

@@ -357,6 +357,25 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode,
                    int32_t* m_out_host, float* scores_out, const cb_layer_opts* opts, void* ws,
                    size_t ws_bytes, void* stream);
 
+/* A steady layer (fixed mode, S_l = S_c) of n_req requests at once ([CB-A] §Selective
+ * recomputation Steps 2-4 for each request; the batch of independent requests shares the
+ * weights).  The selected rows of all requests are one set of GEMM rows, so the Q/K/V,
+ * O-projection and FFN GEMMs run once over all of them and read each weight once; attention
+ * runs per request over that request's own cache.  Per row the arithmetic is that of
+ * cb_blend_layer(STEADY).
+ *   row0_host : [n_req + 1] host prefix offsets: request r owns rows [row0[r], row0[r+1])
+ *               (row0[0] = 0, non-decreasing, at most n_tok rows per request, n_req <= 64)
+ *   x_in  : [row0[n_req], d] hidden rows of every request's selection, request by request
+ *   s_in  : [row0[n_req]] each row's position in its request (ascending within a request,
+ *           each in [0, n_tok); a row outside is not followed, see Row indices)
+ *   k_cache, v_cache : [n_req * n_tok, Hkv hd] the requests' caches of this layer back to back
+ *           (request r's row j at r * n_tok + j), updated in place at the selected rows
+ *   x_out : [row0[n_req], d] (must not alias x_in).  n_req * n_tok must fit in int32. */
+int cb_blend_steady_batch(const cb_dims* dims, const cb_layer_w* w, int32_t n_req,
+                          const int32_t* row0_host, const void* x_in, const int32_t* s_in,
+                          int64_t n_tok, void* k_cache, void* v_cache, const float* cos_sin,
+                          int32_t max_pos, void* x_out, void* ws, size_t ws_bytes, void* stream);
+
 /* Standard causal prefill of n tokens at positions pos0..pos0+n-1 through n_layers
  * layers: the quality reference (KV^full, [CB-A] §KV cache definitions; [CB-B] "full KV
  * recompute") and the per-chunk precompute (KV^pre, pos0 = 0).

@@ -78,6 +78,8 @@ _PROTOS = {
     "cb_blend_layer": (C.c_int, [C.POINTER(cb_dims), C.POINTER(cb_layer_w), _I32, _P, _P, _I32, _I64, _I64,
                                  _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, C.POINTER(_I32), _P,
                                  C.POINTER(cb_layer_opts), _P, _SZ, _P]),
+    "cb_blend_steady_batch": (C.c_int, [C.POINTER(cb_dims), C.POINTER(cb_layer_w), _I32, C.POINTER(_I32), _P, _P,
+                                        _I64, _P, _P, _P, _I32, _P, _P, _SZ, _P]),
     "cb_full_prefill": (C.c_int, [C.POINTER(cb_dims), _I32, C.POINTER(cb_layer_w), _P, _P, _I32, _I32,
                                   C.POINTER(_P), C.POINTER(_P), _P, _P, _P, _I32, _P, _SZ, _P]),
     "cb_lmhead_argmax": (C.c_int, [_P, _P, _P, C.POINTER(cb_dims), _P, _P, _P, _SZ, _P]),
@@ -269,6 +271,15 @@ def cb_blend_layer(dims: cb_dims, w: cb_layer_w, mode: int, x_in, s_in, m_in: in
         _ptr(v_cache), _ptr(cos_sin), max_pos, k_budget, dev_mode, _ptr(sel_override), _ptr(x_out),
         _ptr(s_out), C.byref(m_out), _ptr(scores_out), opts, _ptr(ws), _nbytes(ws), _stream(stream)))
     return int(m_out.value)
+
+
+def cb_blend_steady_batch(dims: cb_dims, w: cb_layer_w, row0: Sequence[int], x_in, s_in, n_tok: int, k_cache,
+                          v_cache, cos_sin, max_pos: int, x_out, ws, stream=None):
+    """One steady layer of len(row0) - 1 requests at once (request r: rows [row0[r], row0[r+1]))."""
+    arr = (C.c_int32 * len(row0))(*[int(v) for v in row0])
+    _check("cb_blend_steady_batch", lib().cb_blend_steady_batch(
+        C.byref(dims), C.byref(w), len(row0) - 1, arr, _ptr(x_in), _ptr(s_in), n_tok, _ptr(k_cache), _ptr(v_cache),
+        _ptr(cos_sin), max_pos, _ptr(x_out), _ptr(ws), _nbytes(ws), _stream(stream)))
 
 
 def cb_full_prefill(dims: cb_dims, layers: Sequence[cb_layer_w], embed, tokens, n: int, pos0: int,

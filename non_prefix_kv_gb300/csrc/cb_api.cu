@@ -879,6 +879,51 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
 #undef WAIT_CACHED_ROWS
 }
 
+int cb_blend_steady_batch(const cb_dims* dims, const cb_layer_w* w, int32_t n_req, const int32_t* row0_host,
+                          const void* x_in, const int32_t* s_in, int64_t n_tok, void* k_cache, void* v_cache,
+                          const float* cos_sin, int32_t max_pos, void* x_out, void* ws, size_t ws_bytes,
+                          void* stream) {
+  int st = check_dims(dims);
+  if (st || (st = check_w(w))) return st;
+  if (!row0_host || !x_in || !s_in || !k_cache || !v_cache || !cos_sin || !x_out)
+    return fail(CB_ERR_INVALID_ARG, "blend_steady_batch pointer is NULL");
+  if (x_out == x_in) return fail(CB_ERR_INVALID_ARG, "x_out must not alias x_in");
+  if (n_req < 1 || n_req > kMaxBatch) return fail(CB_ERR_SHAPE, "n_req %d outside [1, %d]", n_req, kMaxBatch);
+  if (n_tok < 1 || n_tok > max_pos) return fail(CB_ERR_SHAPE, "need 1 <= n_tok <= max_pos");
+  if ((int64_t)n_req * n_tok > INT32_MAX) return fail(CB_ERR_SHAPE, "n_req * n_tok exceeds the int32 row range");
+  BatchRows br{};
+  br.n_req = n_req;
+  if (row0_host[0] != 0) return fail(CB_ERR_SHAPE, "row0[0] must be 0");
+  for (int r = 0; r <= n_req; ++r) {
+    if (r > 0 && (row0_host[r] < row0_host[r - 1] || row0_host[r] - row0_host[r - 1] > n_tok))
+      return fail(CB_ERR_SHAPE, "request %d: rows must be non-decreasing, at most n_tok per request", r - 1);
+    br.row0[r] = row0_host[r];
+  }
+  const int M = row0_host[n_req];
+  if (M == 0) return CB_OK;
+  LayerWs L;
+  if ((st = need_ws(dims, M, M, ws, ws_bytes, &L))) return st;
+  cudaStream_t s = S(stream);
+  const int qc = dims->n_heads * dims->head_dim, W = dims->n_kv_heads * dims->head_dim;
+  const size_t B = esize(dims->dtype);
+  L_RMSNORM(dims->dtype, dims->dtype, L.a, x_in, nullptr, w->attn_norm, M, dims->d_model, dims->rms_eps, s);
+  CB_LAUNCH(CB_PROF_INDEX, 3, M, 0, 0, 0.0, 8.0 * M, s, launch_batch_kv_rows(s_in, M, n_tok, br, L.rows, s));
+  // one Q/K/V GEMM over every request's rows: RoPE at each row's position in its request,
+  // K/V written straight into its request's cache rows
+  GemmDesc g = qkv_desc(dims, w, L.a, M, 0, qc + 2 * W, L.q, k_cache, v_cache, s_in, L.rows, cos_sin, max_pos);
+  g.epi.kv_bound = (int64_t)n_req * n_tok;
+  L_GEMM(dims->dtype, g, s);
+  for (int r = 0; r < n_req; ++r) {
+    const int m0 = row0_host[r], mr = row0_host[r + 1] - m0;
+    if (mr == 0) continue;
+    const size_t off = (size_t)r * n_tok * W * B;
+    L_ATTN(dims->dtype, static_cast<const char*>(L.q) + (size_t)m0 * qc * B, s_in + m0, mr,
+           static_cast<const char*>(k_cache) + off, static_cast<const char*>(v_cache) + off, n_tok, dims->n_heads,
+           dims->n_kv_heads, dims->head_dim, static_cast<char*>(L.attn) + (size_t)m0 * qc * B, L.attn_ws, 0, s);
+  }
+  return o_ffn(dims, w, L.attn, x_in, M, x_out, L, s);
+}
+
 int cb_full_prefill(const cb_dims* dims, int32_t n_layers, const cb_layer_w* layers_host, const void* embed,
                     const int32_t* tokens, int32_t n, int32_t pos0, void* const* k_out_host,
                     void* const* v_out_host, void* h_last, void* x_all, const float* cos_sin, int32_t max_pos,

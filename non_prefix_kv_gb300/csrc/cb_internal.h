@@ -133,6 +133,14 @@ cudaError_t launch_build_sel(const int32_t* ord, int k, const int32_t* cand_row,
 cudaError_t launch_rows_to_positions(const int32_t* rows, int k, const int32_t* s_in, int m_in,
                                      int32_t* pos_out, cudaStream_t s);
 cudaError_t launch_iota(int32_t* out, int n, int32_t start, cudaStream_t s);
+// row offsets of the requests of a batched steady layer (request r owns rows [row0[r], row0[r+1]))
+constexpr int kMaxBatch = 64;
+struct BatchRows {
+  int32_t row0[kMaxBatch + 1];
+  int n_req;
+};
+cudaError_t launch_batch_kv_rows(const int32_t* s_in, int m_total, int64_t n_tok, const BatchRows& b,
+                                 int32_t* kv_row, cudaStream_t s);
 cudaError_t launch_swiglu(int dt, void* out, const void* gu, int64_t M, int F, cudaStream_t s);
 size_t lm_block_best_count(int V);          // workspace entries (either type)
 size_t lm_block_count(int V, int dt);       // entries the GEMV of this type writes

@@ -1198,6 +1198,33 @@ cudaError_t launch_iota(int32_t* out, int n, int32_t start, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// kv_row[i] = r * n_tok + s_in[i] for the rows i of request r, [row0[r], row0[r+1]): each
+// selected row's place in the requests' caches laid back to back.  A position outside
+// [0, n_tok) records ERRBIT_INDEX and maps to -1, which the K/V epilogue does not write.
+__global__ void k_batch_kv_rows(const int32_t* __restrict__ s_in, int m_total, int64_t n_tok, const BatchRows b,
+                                int32_t* __restrict__ kv_row) {
+  pdl_wait();
+  pdl_trigger();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= m_total) return;
+  int r = 0;
+  while (r + 1 < b.n_req && i >= b.row0[r + 1]) ++r;
+  const int32_t p = s_in[i];
+  if (p < 0 || p >= n_tok) {
+    atomicOr(&g_err_mem, ERRBIT_INDEX);
+    kv_row[i] = -1;
+    return;
+  }
+  kv_row[i] = (int32_t)(r * n_tok + p);
+}
+
+cudaError_t launch_batch_kv_rows(const int32_t* s_in, int m_total, int64_t n_tok, const BatchRows& b,
+                                 int32_t* kv_row, cudaStream_t s) {
+  if (m_total == 0) return cudaSuccess;
+  { const cudaError_t e_ = launch_k(k_batch_kv_rows, dim3((m_total + 255) / 256), dim3(256), 0, s, s_in, m_total, n_tok, b, kv_row); if (e_ != cudaSuccess) return e_; }
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------------ SwiGLU (SIMT path)
 // out[m][j] = silu(gu[m][j]) * gu[m][F + j]
 template <typename T>

@@ -181,7 +181,9 @@ class Request:
     prompt, separators, query spans, in any order) the uncached rows are given to the
     library as a forced-row mask; `tokens` is then the whole input in segment order."""
 
-    def __init__(self, eng: BlendEngine, pool, order: Sequence[int], tokens: np.ndarray, segments=None):
+    def __init__(self, eng: BlendEngine, pool, order: Sequence[int], tokens: np.ndarray, segments=None, kv=None):
+        """kv: optional (K, V) lists of per-layer [N, Hkv*hd] tensors to use as this
+        request's blended cache (e.g. views into a batch's shared caches)."""
         s = eng.dm.shape
         dev = eng.device
         dt = torch_dtype(s)
@@ -228,8 +230,11 @@ class Request:
         self.n_pool_rows = int(sum(pool.lens))
         self.tokens_host = check_token_ids(tokens, s.vocab)
         self.tokens = torch.from_numpy(self.tokens_host).to(dev)
-        self.K = [torch.zeros(self.N, s.kv_width, dtype=dt, device=dev) for _ in range(s.n_layers)]
-        self.V = [torch.zeros(self.N, s.kv_width, dtype=dt, device=dev) for _ in range(s.n_layers)]
+        if kv is not None:
+            self.K, self.V = list(kv[0]), list(kv[1])
+        else:
+            self.K = [torch.zeros(self.N, s.kv_width, dtype=dt, device=dev) for _ in range(s.n_layers)]
+            self.V = [torch.zeros(self.N, s.kv_width, dtype=dt, device=dev) for _ in range(s.n_layers)]
         self.x = [torch.empty(self.N, s.d_model, dtype=dt, device=dev) for _ in range(2)]
         self.s = [torch.empty(self.N, dtype=torch.int32, device=dev) for _ in range(2)]
         self.scores = torch.empty(self.N, dtype=torch.float32, device=dev)
@@ -450,7 +455,7 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
               assemble: bool = True, stream=None, host_pool: Optional[HostPool] = None,
               file_store: Optional[FileStore] = None, recompute_precheck_kv: bool = False,
               precheck_load_rows: Optional[int] = None, overlap_assembly: bool = True,
-              layer_events: Optional[list] = None):
+              layer_events: Optional[list] = None, upto: Optional[int] = None, x_out_last=None, s_out_last=None):
     """One blended prefill: re-position the chunk KV of every layer, run the layer plan,
     then the lm_head argmax.  Returns the number of rows carried out of the last layer.
 
@@ -479,7 +484,11 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
     precheck_load_rows: the pre-check layers use the chunk caches for the first X cached
     rows only and compute K/V for the rest (R5 again); only those X rows of their chunk KV
     are loaded and re-positioned.  precheck_split_rows() picks the X at which the load
-    ends with the GEMMs that precede the layer's attention."""
+    ends with the GEMMs that precede the layer's attention.
+
+    upto: run layers [0, upto) only and skip the lm_head (every layer's chunk KV is still
+    re-positioned); the last of them writes its rows to x_out_last / s_out_last when given.
+    Returns that layer's row count."""
     eng = req.eng
     dm = eng.dm
     s = dm.shape
@@ -608,6 +617,9 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
     if keep_history:
         req.sel_hist, req.m_hist = [], []
     for l, (mode, k) in enumerate(plan):
+        if upto is not None and l >= upto:
+            break
+        last = upto is not None and l == upto - 1
         if ready is not None:
             ready[l].wait()
             if errors:
@@ -619,7 +631,8 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
             ev[0].record(torch.cuda.current_stream() if stream is None else stream)
         m_out = B.cb_blend_layer(dims, dm.layers_c[l], mode, req.x[cur], s_in, m_in, req.N, req.n_cached,
                                  req.K[l], req.V[l], eng.cos_sin, eng.max_pos, k, dev_mode, ov,
-                                 req.x[1 - cur], req.s[1 - cur],
+                                 x_out_last if (last and x_out_last is not None) else req.x[1 - cur],
+                                 s_out_last if (last and s_out_last is not None) else req.s[1 - cur],
                                  req.scores if mode in (B.CB_LAYER_CHECK, B.CB_LAYER_GRADUAL) else None,
                                  eng.ws, stream,
                                  kv_ready=(asm_ready.get(l) if asm_ready is not None else
@@ -637,13 +650,94 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
         if keep_history:
             req.sel_hist.append(req.s[cur][:m_out].clone())
             req.m_hist.append(m_out)
+    if upto is not None and queue_loads is not None:
+        queue_loads(s.n_layers)          # the layers run later (by a batch) still need their KV
     if loader is not None:
         loader.join()
     if asm_ready is not None:
         # join the assembly stream (each layer already waited for its own re-positioning)
         (torch.cuda.current_stream() if stream is None else stream).wait_stream(eng.asm_stream)
+    if upto is not None:
+        return m_in
     req.m_last = m_in
     req.x_last = req.x[cur]
     h_last = req.x[cur][m_in - 1]
     B.cb_lmhead_argmax(h_last, dm.final_norm, dm.w_lm, dims, None, req.token, eng.ws, stream)
     return m_in
+
+
+class RequestBatch:
+    """Independent requests of the same length over one chunk pool, run together (the
+    batch of the Yi-34B-shaped workload).  Each layer's blended caches of the R requests are
+    one [R * N, Hkv*hd] tensor (request r's rows at [r N, (r + 1) N)).  The layers up to the
+    check layer run per request; from there on (fixed mode: every later layer keeps the
+    check layer's rows) the selected rows of all requests are one set of GEMM rows, so each
+    steady layer reads its weights once for the whole batch (cb_blend_steady_batch)."""
+
+    def __init__(self, eng: BlendEngine, pool, orders: Sequence[Sequence[int]], tokens_list: Sequence[np.ndarray]):
+        s = eng.dm.shape
+        dev = eng.device
+        dt = torch_dtype(s)
+        N = {len(t) for t in tokens_list}
+        if len(N) != 1:
+            raise ValueError("the requests of a batch must have the same length")
+        self.N = N.pop()
+        self.R = len(tokens_list)
+        self.eng = eng
+        self.K = [torch.zeros(self.R * self.N, s.kv_width, dtype=dt, device=dev) for _ in range(s.n_layers)]
+        self.V = [torch.zeros(self.R * self.N, s.kv_width, dtype=dt, device=dev) for _ in range(s.n_layers)]
+        self.reqs = []
+        for r, (order, toks) in enumerate(zip(orders, tokens_list)):
+            sl = slice(r * self.N, (r + 1) * self.N)
+            self.reqs.append(Request(eng, pool, order, toks, kv=([k[sl] for k in self.K], [v[sl] for v in self.V])))
+        self.X = None
+        self.S = None
+        self.ws = None
+
+    def _buffers(self, m_total: int):
+        s = self.eng.dm.shape
+        if self.X is None or self.X[0].shape[0] < m_total:
+            dt = torch_dtype(s)
+            dev = self.eng.device
+            self.X = [torch.empty(m_total, s.d_model, dtype=dt, device=dev) for _ in range(2)]
+            self.S = torch.empty(m_total, dtype=torch.int32, device=dev)
+            self.ws = torch.empty(B.cb_workspace_bytes(self.eng.dm.dims, m_total, m_total), dtype=torch.uint8,
+                                  device=dev)
+
+
+def run_blend_batch(batch: RequestBatch, plan, stream=None) -> List[int]:
+    """One blended prefill of every request of the batch: per request the pre-check and the
+    check layer (HKVD selection), then every steady layer once for all requests' selected
+    rows, then each request's lm_head argmax (into req.token).
+    Returns the rows each request carries out of the last layer."""
+    eng = batch.eng
+    dm = eng.dm
+    s = dm.shape
+    modes = [m for m, _ in plan]
+    if B.CB_LAYER_CHECK not in modes:
+        raise ValueError("a batched blend needs a check layer")
+    c = modes.index(B.CB_LAYER_CHECK)
+    if any(m != B.CB_LAYER_STEADY for m in modes[c + 1:]):
+        raise ValueError("layers after the check layer must be steady (fixed mode) in a batched blend")
+    if any(r.forced_mask is not None for r in batch.reqs):
+        raise ValueError("a batched blend takes the default layout (chunks, then the query)")
+    m_r = [plan[c][1] + r.n_forced for r in batch.reqs]
+    row0 = [0]
+    for m in m_r:
+        row0.append(row0[-1] + m)
+    batch._buffers(row0[-1])
+    for r, req in enumerate(batch.reqs):
+        m = run_blend(req, plan, stream=stream, upto=c + 1, x_out_last=batch.X[0][row0[r]:row0[r + 1]],
+                      s_out_last=batch.S[row0[r]:row0[r + 1]])
+        if m != m_r[r]:
+            raise RuntimeError(f"request {r}: {m} rows out of the check layer, {m_r[r]} expected")
+    cur = 0
+    for l in range(c + 1, s.n_layers):
+        B.cb_blend_steady_batch(dm.dims, dm.layers_c[l], row0, batch.X[cur], batch.S, batch.N, batch.K[l], batch.V[l],
+                                eng.cos_sin, eng.max_pos, batch.X[1 - cur], batch.ws, stream)
+        cur = 1 - cur
+    for r, req in enumerate(batch.reqs):
+        req.m_last = m_r[r]
+        req.x_last = batch.X[cur][row0[r]:row0[r + 1]]
+        B.cb_lmhead_argmax(req.x_last[m_r[r] - 1], dm.final_norm, dm.w_lm, dm.dims, None, req.token, eng.ws, stream)
+    return m_r

@@ -395,3 +395,45 @@ def test_request_graph_replays_match_eager_runs(E):
         for l in range(wl.shape.n_layers):
             assert torch.equal(ks[l], b.K[l])
         assert torch.equal(xs, b.x_last[:b.m_last])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_batched_steady_layers_match_per_request_blends(E, dtype):
+    """Three requests over one chunk pool (chunk orders shuffled per request, as in the Yi
+    workload's batch): the pre-check and check layers per request, then every steady layer
+    once for all requests' selected rows.  Sets, every layer's blended K/V, the last layer's
+    rows and the first token match the requests blended one at a time."""
+    torch = torch_mod()
+    from non_prefix_kv_gb300 import binding as B
+    if dtype == "f32":
+        shape = replace(synth.WORKLOADS["tiny_f32"].shape, n_layers=4)
+        tol = TOL["f32"]
+    else:
+        shape = replace(BF16_SMALL, n_layers=4, n_heads=8, n_kv_heads=2, head_dim=64)
+        tol = 1e-3
+    wl = synth.Workload("batch", shape, chunk_len=96, n_distinct=6, order=(0, 1, 2), n_query=40, ratio=0.15,
+                        n_requests=3)
+    model = synth.make_model(shape, seed=5)
+    reqs_h = synth.make_requests(wl)
+    dm = E.DeviceModel.from_host(model)
+    eng = E.BlendEngine(dm, wl.n_tokens)
+    pool = eng.precompute_pool(reqs_h[0].chunk_tokens)
+    ratios = O.ratio_schedule(wl.ratio, shape.n_layers, 1, False)
+    plan = E.layer_plan(shape, wl.n_tokens, wl.n_cached, ratios)
+    single = []
+    for rh in reqs_h:
+        a = E.Request(eng, pool, rh.order, rh.tokens)
+        E.run_blend(a, plan, keep_history=True)
+        B.cb_sync(None)
+        single.append(a)
+    batch = E.RequestBatch(eng, pool, [rh.order for rh in reqs_h], [rh.tokens for rh in reqs_h])
+    ms = E.run_blend_batch(batch, plan)
+    B.cb_sync(None)
+    for r, (a, b) in enumerate(zip(single, batch.reqs)):
+        assert ms[r] == a.m_last
+        np.testing.assert_array_equal(batch.S[sum(ms[:r]):sum(ms[:r + 1])].cpu().numpy(),
+                                      a.sel_hist[1].cpu().numpy())
+        for l in range(shape.n_layers):
+            assert rel(host(b.K[l]), host(a.K[l])) <= tol and rel(host(b.V[l]), host(a.V[l])) <= tol, (r, l)
+        assert rel(host(b.x_last[:ms[r]]), host(a.x_last[:a.m_last])) <= tol
+        assert int(b.token.item()) == int(a.token.item())

@@ -347,6 +347,21 @@ typedef struct {
    * the two is the load controller's choice at this layer, [CB-A] §Pipelining and load
    * controller).  kv_ready then marks rows [0, r) only. */
   int32_t recompute_from;
+  /* PRECHECK only: input row i is row x_rows[i] (in [0, n_x_rows)) of x_in instead of row i,
+   * e.g. x_in = the embedding table [vocab, d] and x_rows = the token ids, so the layer reads
+   * the embedding rows in place (no gather of the input rows).  NULL = rows 0..n_tok-1. */
+  const int32_t* x_rows;
+  int64_t n_x_rows;
+  /* CHECK/GRADUAL: a second stream (cudaStream_t) and two events (cudaEvent_t) owned by the
+   * caller, all three set or all NULL.  With them the KV expansion of the selected rows (Step
+   * 3) runs on aux_stream while the main stream computes the selected rows' queries; the
+   * main stream waits for it (aux_join) before attention.  The call forks at aux_fork.  A
+   * gradual layer that computes Q for every incoming row in its K/V GEMM has no Q GEMM to
+   * overlap and expands on the main stream.  The caller must not use the three concurrently
+   * elsewhere. */
+  void* aux_stream;
+  void* aux_fork;
+  void* aux_join;
 } cb_layer_opts;
 
 int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode,

@@ -213,7 +213,7 @@ struct Carver {
 };
 
 struct LayerWs {
-  void *a, *q, *knew, *vnew, *attn, *h, *b, *act, *xg, *ag, *qg, *xa, *xb, *attn_ws;
+  void *a, *q, *knew, *vnew, *attn, *h, *b, *act, *ag, *qg, *xa, *xb, *attn_ws;
   float *scores, *hn, *logits, *dev_part;
   int32_t *ord, *keep, *pos, *rows, *cpos, *crows, *fpos, *frows;
 };
@@ -236,7 +236,6 @@ LayerWs carve_layer(Carver& c, const cb_dims* d, int64_t R, int64_t M) {
   w.h = c.take(std::max(R, M) * d->d_model * B);
   w.b = c.take(std::max(R, M) * d->d_model * B);
   w.act = c.take(std::max(R, M) * d->d_ff * B);
-  w.xg = c.take(M * d->d_model * B);
   w.ag = c.take(M * d->d_model * B);
   w.xa = c.take(R * d->d_model * B);
   w.xb = c.take(R * d->d_model * B);
@@ -355,9 +354,11 @@ GemmDesc qkv_desc(const cb_dims* d, const cb_layer_w* w, const void* a, int M, i
   return g;
 }
 
-// h = x_res + attn Wo^T ; x_out = h + (silu(b Wg^T) * b Wu^T) Wd^T, b = RMSNorm(h) g
+// h = x_res[res_row[m]] + attn Wo^T ; x_out = h + (silu(b Wg^T) * b Wu^T) Wd^T, b = RMSNorm(h) g.
+// res_row null: row m of x_res; otherwise rows of x_res (res_rows of them) read in place, so the
+// residual rows of a selection need no gather.
 int o_ffn(const cb_dims* d, const cb_layer_w* w, const void* attn, const void* x_res, int M, void* x_out,
-          const LayerWs& ws, cudaStream_t s) {
+          const LayerWs& ws, cudaStream_t s, const int32_t* res_row = nullptr, int64_t res_rows = -1) {
   if (M == 0) return CB_OK;
   const int qc = d->n_heads * d->head_dim;
   GemmDesc go = make_gemm(M, d->d_model, qc, attn, qc, w->wo, qc);
@@ -366,6 +367,8 @@ int o_ffn(const cb_dims* d, const cb_layer_w* w, const void* attn, const void* x
   go.epi.ldo = d->d_model;
   go.epi.resid = x_res;
   go.epi.ldr = d->d_model;
+  go.epi.resid_row = res_row;
+  go.epi.resid_rows = res_rows;
   L_GEMM(d->dtype, go, s);
   L_RMSNORM(d->dtype, d->dtype, ws.b, ws.h, nullptr, w->ffn_norm, M, d->d_model, d->rms_eps, s);
   GemmDesc gu = make_gemm(M, d->d_ff, d->d_model, ws.b, d->d_model, w->w_gate_up, d->d_model);
@@ -706,6 +709,14 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
   const int N = (int)n_tok;
   const uint8_t* fmask = opts ? opts->forced_mask : nullptr;
   void* kv_ready = opts ? opts->kv_ready : nullptr;
+  const int32_t* x_rows = opts ? opts->x_rows : nullptr;
+  const int64_t n_x_rows = opts ? opts->n_x_rows : 0;
+  if (x_rows && (mode != CB_LAYER_PRECHECK || n_x_rows < 1))
+    return fail(CB_ERR_INVALID_ARG, "x_rows applies to PRECHECK, with n_x_rows >= 1");
+  const bool fork = opts && opts->aux_stream;
+  if (opts && ((opts->aux_stream == nullptr) != (opts->aux_fork == nullptr) ||
+               (opts->aux_stream == nullptr) != (opts->aux_join == nullptr)))
+    return fail(CB_ERR_INVALID_ARG, "aux_stream, aux_fork and aux_join must all be set or all NULL");
   if (fmask && (opts->n_forced < 1 || opts->n_forced > N))
     return fail(CB_ERR_SHAPE, "n_forced %d outside [1, n_tok]", opts ? opts->n_forced : 0);
   if (opts && opts->recompute_from != 0) {
@@ -732,7 +743,10 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
       if ((st = need_ws(dims, N, N, ws, ws_bytes, &L))) return st;
       *m_out_host = N;
       L_IOTA(s_out, N, 0, s);
-      L_RMSNORM(dims->dtype, dims->dtype, L.a, x_in, nullptr, w->attn_norm, N, dims->d_model, dims->rms_eps, s);
+      // input row i is x_in[x_rows[i]] when a row map is given (e.g. the embedding table and the
+      // token ids): the norm and the residual read the table rows in place
+      L_RMSNORM_B(dims->dtype, dims->dtype, L.a, x_in, x_rows, x_rows ? n_x_rows : -1, w->attn_norm, N, dims->d_model,
+                  dims->rms_eps, s);
       if (opts && opts->recompute_kv) {
         // every row's Q, K and V in one GEMM; the cached rows are overwritten, not read
         WAIT_CACHED_ROWS();
@@ -740,7 +754,7 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         g.epi.kv_bound = N;
         L_GEMM(dims->dtype, g, s);
         L_ATTN(dims->dtype, L.q, s_out, N, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
-        return o_ffn(dims, w, L.attn, x_in, N, x_out, L, s);
+        return o_ffn(dims, w, L.attn, x_in, N, x_out, L, s, x_rows, x_rows ? n_x_rows : -1);
       }
       // Q of every row and K/V of the uncached rows (and of the cached rows from
       // recompute_from on): independent, so one shared launch
@@ -764,7 +778,7 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
       }
       WAIT_CACHED_ROWS();
       L_ATTN(dims->dtype, L.q, s_out, N, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
-      return o_ffn(dims, w, L.attn, x_in, N, x_out, L, s);
+      return o_ffn(dims, w, L.attn, x_in, N, x_out, L, s, x_rows, x_rows ? n_x_rows : -1);
     }
     case CB_LAYER_CHECK:
     case CB_LAYER_GRADUAL: {
@@ -837,23 +851,35 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
           L_BUILD_SEL(L.ord, k_budget, rows_in, f0, m_in - n_forced, n_forced, s_out, L.keep, s);
       }
       // Step 3, KV expansion (the recomputed K/V of S replace the cached rows), and the
-      // gathers of S's queries (or normalised rows) and residual rows: one launch
+      // gather of S's queries (or normalised rows): one launch, or with an aux stream the
+      // expansion there, beside the Q GEMM.  S's residual rows are read in place by the
+      // O-projection's epilogue (row map keep).
       {
-        RowCopies rc;
-        rc.add(k_cache, s_out, L.knew, L.keep, M, (int64_t)W * B, N, m_in);
-        rc.add(v_cache, s_out, L.vnew, L.keep, M, (int64_t)W * B, N, m_in);
+        // the expansion overlaps only a Q GEMM; with Q already computed, attention waits for it
+        const bool fork_kv = fork && !q_all;
+        RowCopies rc, kv;
+        RowCopies& kvc = fork_kv ? kv : rc;
+        kvc.add(k_cache, s_out, L.knew, L.keep, M, (int64_t)W * B, N, m_in);
+        kvc.add(v_cache, s_out, L.vnew, L.keep, M, (int64_t)W * B, N, m_in);
         if (q_all)
           rc.add(L.qg, nullptr, L.q, L.keep, M, (int64_t)qc * B, M, m_in);
         else
           rc.add(L.ag, nullptr, L.a, L.keep, M, (int64_t)dims->d_model * B, M, m_in);
-        rc.add(L.xg, nullptr, x_in, L.keep, M, (int64_t)dims->d_model * B, M, m_in);
+        if (fork_kv) {
+          cudaStream_t aux = S(opts->aux_stream);
+          CB_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(opts->aux_fork), s));
+          CB_CUDA(cudaStreamWaitEvent(aux, static_cast<cudaEvent_t>(opts->aux_fork), 0));
+          if ((st = kv.launch(aux))) return st;
+          CB_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(opts->aux_join), aux));
+        }
         if ((st = rc.launch(s))) return st;
       }
       const void* qsel = q_all ? L.qg : L.q;
       if (!q_all)
         L_GEMM(dims->dtype, qkv_desc(dims, w, L.ag, M, 0, qc, L.q, nullptr, nullptr, s_out, nullptr, cos_sin, max_pos), s);
+      if (fork && !q_all) CB_CUDA(cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(opts->aux_join), 0));
       L_ATTN(dims->dtype, qsel, s_out, M, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
-      return o_ffn(dims, w, L.attn, L.xg, M, x_out, L, s);
+      return o_ffn(dims, w, L.attn, x_in, M, x_out, L, s, L.keep, m_in);
     }
     case CB_LAYER_STEADY: {
       if (m_in < 1 || m_in > N) return fail(CB_ERR_SHAPE, "STEADY needs 1 <= m_in <= n_tok");

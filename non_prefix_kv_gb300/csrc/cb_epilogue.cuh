@@ -65,8 +65,10 @@ __device__ __forceinline__ bool epi_apply(const EpiParams& p, int m, int n, floa
       st_vec<T, NV>((T*)p.out + (int64_t)m * p.ldo + n, v);
       return true;
     case EPI_RESID: {
+      const int64_t rr = p.resid_row ? (int64_t)p.resid_row[m] : (int64_t)m;
+      if (rr < 0 || (p.resid_rows >= 0 && rr >= p.resid_rows)) return false;
       float r[NV];
-      ld_vec<T, NV>((const T*)p.resid + (int64_t)m * p.ldr + n, r);
+      ld_vec<T, NV>((const T*)p.resid + rr * p.ldr + n, r);
 #pragma unroll
       for (int i = 0; i < NV; ++i) v[i] += r[i];
       st_vec<T, NV>((T*)p.out + (int64_t)m * p.ldo + n, v);

@@ -30,6 +30,8 @@ struct EpiParams {
   int64_t ldo = 0;
   const void* resid = nullptr;
   int64_t ldr = 0;
+  const int32_t* resid_row = nullptr;  // EPI_RESID: row of resid added to output row m, or null (m)
+  int64_t resid_rows = -1;             // rows of resid for the check of resid_row (< 0: unchecked)
   // EPI_QKV
   int col0 = 0;        // first Wqkv row covered by this launch
   int q_cols = 0;      // H * hd

@@ -150,6 +150,12 @@ class BlendEngine:
         # event per layer (run_blend(..., overlap_assembly=True))
         self.asm_stream = torch.cuda.Stream(device=device)
         self.asm_done = [torch.cuda.Event() for _ in range(dm.shape.n_layers)]
+        # check and gradual layers expand the selected rows' K/V on this stream beside the
+        # selected queries' GEMM (run_blend(..., aux_expansion=True))
+        self.aux_stream = torch.cuda.Stream(device=device)
+        self.aux_events = (torch.cuda.Event(), torch.cuda.Event())
+        for ev in self.aux_events:       # torch creates the CUDA event on its first record
+            ev.record(self.aux_stream)
 
     # ---- precompute (offline: KV^pre) ------------------------------------------------------
     def precompute_pool(self, chunk_tokens: Sequence[np.ndarray]) -> ChunkPool:
@@ -455,7 +461,8 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
               assemble: bool = True, stream=None, host_pool: Optional[HostPool] = None,
               file_store: Optional[FileStore] = None, recompute_precheck_kv: bool = False,
               precheck_load_rows: Optional[int] = None, overlap_assembly: bool = True,
-              layer_events: Optional[list] = None, upto: Optional[int] = None, x_out_last=None, s_out_last=None):
+              layer_events: Optional[list] = None, upto: Optional[int] = None, x_out_last=None, s_out_last=None,
+              aux_expansion: bool = True):
     """One blended prefill: re-position the chunk KV of every layer, run the layer plan,
     then the lm_head argmax.  Returns the number of rows carried out of the last layer.
 
@@ -485,6 +492,9 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
     rows only and compute K/V for the rest (R5 again); only those X rows of their chunk KV
     are loaded and re-positioned.  precheck_split_rows() picks the X at which the load
     ends with the GEMMs that precede the layer's attention.
+
+    aux_expansion (default on): check and gradual layers expand the selected rows' K/V on
+    the engine's aux stream beside the selected queries' GEMM.
 
     upto: run layers [0, upto) only and skip the lm_head (every layer's chunk KV is still
     re-positioned); the last of them writes its rows to x_out_last / s_out_last when given.
@@ -584,7 +594,12 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
                 queued[0] += 1
         queue_loads(1)
 
-    if req.start_rows is None:
+    # a first layer that runs every row reads its input rows in place from the embedding table
+    # (row map = the token ids); otherwise the rows are gathered first
+    embed_in_place = req.start_rows is None and plan[0][0] == B.CB_LAYER_PRECHECK
+    if embed_in_place:
+        m_in, s_in = req.N, None
+    elif req.start_rows is None:
         B.cb_gather_rows(req.x[0], dm.embed, req.tokens, req.N, s.d_model * esz, stream)
         m_in, s_in = req.N, None
     else:
@@ -629,7 +644,9 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
         if layer_events is not None:
             ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             ev[0].record(torch.cuda.current_stream() if stream is None else stream)
-        m_out = B.cb_blend_layer(dims, dm.layers_c[l], mode, req.x[cur], s_in, m_in, req.N, req.n_cached,
+        first = embed_in_place and l == 0
+        m_out = B.cb_blend_layer(dims, dm.layers_c[l], mode, dm.embed if first else req.x[cur], s_in, m_in, req.N,
+                                 req.n_cached,
                                  req.K[l], req.V[l], eng.cos_sin, eng.max_pos, k, dev_mode, ov,
                                  x_out_last if (last and x_out_last is not None) else req.x[1 - cur],
                                  s_out_last if (last and s_out_last is not None) else req.s[1 - cur],
@@ -638,7 +655,10 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
                                  kv_ready=(asm_ready.get(l) if asm_ready is not None else
                                            None if (host_pool is None or l in skip) else host_pool.done[l]),
                                  forced_mask=req.forced_mask, n_forced=req.n_forced, recompute_kv=l in skip,
-                                 recompute_from=split if (split is not None and l in pre) else 0)
+                                 recompute_from=split if (split is not None and l in pre) else 0,
+                                 x_rows=req.tokens if first else None, n_x_rows=s.vocab if first else 0,
+                                 aux=((eng.aux_stream,) + eng.aux_events
+                                      if aux_expansion and mode in (B.CB_LAYER_CHECK, B.CB_LAYER_GRADUAL) else None))
         if layer_events is not None:
             ev[1].record(torch.cuda.current_stream() if stream is None else stream)
             layer_events.append((l, ev[0], ev[1]))

@@ -437,3 +437,52 @@ def test_batched_steady_layers_match_per_request_blends(E, dtype):
             assert rel(host(b.K[l]), host(a.K[l])) <= tol and rel(host(b.V[l]), host(a.V[l])) <= tol, (r, l)
         assert rel(host(b.x_last[:ms[r]]), host(a.x_last[:a.m_last])) <= tol
         assert int(b.token.item()) == int(a.token.item())
+
+
+def test_precheck_reads_embedding_rows_in_place(E):
+    """The pre-check layer given the embedding table and the token ids as its input rows gives
+    the same K/V and output rows, bit for bit, as the layer given the gathered rows; a token
+    id past the vocabulary is reported (CB_ERR_DEVICE), not followed."""
+    torch = torch_mod()
+    from non_prefix_kv_gb300 import binding as B
+    wl = synth.Workload("bf16_small", BF16_SMALL, chunk_len=96, n_distinct=4, order=(0, 1, 2, 3), n_query=32,
+                        ratio=0.15)
+    model = synth.make_model(wl.shape, seed=2)
+    req_h = synth.make_requests(wl)[0]
+    dm = E.DeviceModel.from_host(model)
+    eng = E.BlendEngine(dm, wl.n_tokens)
+    pool = eng.precompute_pool(req_h.chunk_tokens)
+    req = E.Request(eng, pool, req_h.order, req_h.tokens)
+    N, d, W = wl.n_tokens, wl.shape.d_model, wl.shape.kv_width
+    outs = []
+    for in_place in (False, True):
+        K = torch.zeros(N, W, dtype=torch.bfloat16, device="cuda")
+        V = torch.zeros_like(K)
+        B.cb_rope_shift(K[:req.n_cached], V[:req.n_cached], pool.k[0], pool.v[0], req.src_row, req.delta,
+                        req.n_cached, dm.dims, eng.cos_sin, eng.max_pos)
+        x1 = torch.empty(N, d, dtype=torch.bfloat16, device="cuda")
+        s1 = torch.empty(N, dtype=torch.int32, device="cuda")
+        if in_place:
+            B.cb_blend_layer(dm.dims, dm.layers_c[0], B.CB_LAYER_PRECHECK, dm.embed, None, N, N, req.n_cached, K, V,
+                             eng.cos_sin, eng.max_pos, 0, 0, None, x1, s1, None, eng.ws, x_rows=req.tokens,
+                             n_x_rows=wl.shape.vocab)
+        else:
+            x0 = torch.empty(N, d, dtype=torch.bfloat16, device="cuda")
+            B.cb_gather_rows(x0, dm.embed, req.tokens, N, d * 2)
+            B.cb_blend_layer(dm.dims, dm.layers_c[0], B.CB_LAYER_PRECHECK, x0, None, N, N, req.n_cached, K, V,
+                             eng.cos_sin, eng.max_pos, 0, 0, None, x1, s1, None, eng.ws)
+        B.cb_sync(None)
+        outs.append((K, V, x1))
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
+    bad = req.tokens.clone()
+    bad[7] = wl.shape.vocab
+    x1 = torch.empty(N, d, dtype=torch.bfloat16, device="cuda")
+    s1 = torch.empty(N, dtype=torch.int32, device="cuda")
+    B.cb_blend_layer(dm.dims, dm.layers_c[0], B.CB_LAYER_PRECHECK, dm.embed, None, N, N, req.n_cached,
+                     outs[1][0].clone(), outs[1][1].clone(), eng.cos_sin, eng.max_pos, 0, 0, None, x1, s1, None,
+                     eng.ws, x_rows=bad, n_x_rows=wl.shape.vocab)
+    with pytest.raises(B.CBError) as e:
+        B.cb_sync(None)
+    assert e.value.status == 9
+    B.cb_sync(None)

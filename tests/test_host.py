@@ -147,6 +147,10 @@ def test_entry_points_reject_bad_arguments_before_launch(lib):
     assert with_opts(B.CB_LAYER_PRECHECK, 416, 0, 385) == 2
     assert with_opts(B.CB_LAYER_PRECHECK, 416, 0, -1) == 2
     assert with_opts(B.CB_LAYER_PRECHECK, 416, 0, 128, rkv=1) == 1
+    o = B.cb_layer_opts(None, 0, None, 0, 0, None, 0, FAKE, None, None)
+    a = list(args(B.CB_LAYER_CHECK, 416, 5))
+    a[19] = ctypes.byref(o)
+    assert lib.cb_blend_layer(*a) == 1   # aux stream without its two events
     assert m_out.value == -1          # nothing reported for a rejected call
     st = lib.cb_blend_layer(ctypes.byref(d), ctypes.byref(w), 0, FAKE, None, 416, 416, 384, FAKE, FAKE, FAKE,
                             100, 0, 0, None, FAKE + 64, FAKE, ctypes.byref(m_out), None, None, FAKE, 1 << 40, None)

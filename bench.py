@@ -650,6 +650,10 @@ def deep_stack_block(args, E, B, torch, local, peaks, link_gbs):
     tflops = peaks.get(pkey, FALLBACK_PEAKS[pkey])
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     floor = whole_step_floor_ms(recs, args.profile_steps, attn_flops, hbm, tflops)
+    floor_clk = None
+    if clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
+        tf_clk = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * clocks["sm_mhz"] / clocks["sm_max_mhz"]
+        floor_clk = whole_step_floor_ms(recs, args.profile_steps, attn_flops, hbm, tf_clk)
     g_ms = sum(r["ms"] for r in recs if r["kind"] == "gemm")
     g_fl = sum(r["flops"] for r in recs if r["kind"] == "gemm")
     gemm_tflops = g_fl / (g_ms / 1e3) / 1e12 if g_ms else 1.0
@@ -663,7 +667,10 @@ def deep_stack_block(args, E, B, torch, local, peaks, link_gbs):
            "step_roofline": {"floor_ms": floor, "measured_ms": head["ttft_ms"], "frac": floor / head["ttft_ms"],
                              "tensor_peak_tflops": tflops, "peak_source": pkey,
                              "model": "sum over the step's launches of max(algorithmic bytes / measured copy GB/s, "
-                                      "FLOPs / measured bf16 TFLOP/s)"},
+                                      "FLOPs / measured bf16 TFLOP/s)",
+                             "frac_at_run_clock": None if floor_clk is None else floor_clk / head["ttft_ms"],
+                             "run_clock_note": "the same floor with the burst bf16 rate scaled to the median SM clock "
+                                               "under load"},
            "rows_per_layer": [m for m, _, _ in sel_sums],
            "timing": "CUDA-graph replays timed with CUDA events on the launching stream; inputs (13 GB of weights, "
                      "chunk KV, blended KV) far larger than L2"}
@@ -894,6 +901,15 @@ def our_arm(args):
                 "traffic": GEMM_TRAFFIC.get(top_desc), "traffic_unit": "bytes per launch (ncu dram read+write)",
                 "flops_per_launch": top[2], "ms_per_launch": top_ms,
                 "all_gemm_launches_tflops": all_gemm_tflops}
+    # the burst figure scaled to the SM clock this run held (median under load): a fraction
+    # that does not mix the clocks of the peak's measurement and of this run
+    burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) / (16.0 if shape.dtype != "bf16" else 1.0)
+    if clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
+        pk_clk = burst * clocks["sm_mhz"] / clocks["sm_max_mhz"]
+        roofline["peak_at_run_clock"] = pk_clk
+        roofline["frac_at_run_clock"] = achieved / pk_clk
+        roofline["run_clock_note"] = ("burst bf16 TFLOP/s x median SM MHz under load / max SM MHz (the burst figure "
+                                      "is taken at full clocks)")
     # whole-step roofline: every launch at its own bound (its algorithmic bytes at the measured
     # copy bandwidth, or its FLOPs at the sustained tensor rate, whichever is longer), summed
     # over one step and set against the measured graph-replayed step

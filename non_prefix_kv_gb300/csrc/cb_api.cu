@@ -298,8 +298,8 @@ struct RowCopies {
       J.rv[m] = o.rb / 16;
       J.dbound[m] = o.db;
       J.sbound[m] = o.sb;
-      acc += o.n * (o.rb / 16);
-      J.end[m] = acc;
+      acc += o.n;
+      J.row_end[m] = acc;
       bytes += 2 * o.n * o.rb;
       rows += o.n;
       ++m;

@@ -107,7 +107,7 @@ struct CopyJobs {          // row copies of 16-byte words: dst[di[r]] = src[si[r
   int64_t rv[kMaxCopyJobs];       // 16-byte words per row
   int64_t dbound[kMaxCopyJobs];   // row bounds for the index checks (< 0: unchecked)
   int64_t sbound[kMaxCopyJobs];
-  int64_t end[kMaxCopyJobs];      // inclusive prefix sums of rows * rv
+  int64_t row_end[kMaxCopyJobs];  // inclusive prefix sums of the jobs' row counts
   int n;
 };
 cudaError_t launch_copy_rows_multi(const CopyJobs& J, cudaStream_t s);

@@ -424,47 +424,51 @@ cudaError_t launch_copy_rows(void* dst, const int32_t* dst_idx, const void* src,
 }
 
 // Up to kMaxCopyJobs independent row copies in one launch (the KV expansion and the row
-// gathers that follow a selection share their indices and their moment): job j owns the
-// linear work range [end[j-1], end[j]) of 16-byte words.
+// gathers that follow a selection share their indices and their moment).  One warp per row:
+// the job, the indices and their checks are looked up once per row, and each lane issues
+// all its 16-byte loads of the row (up to kCopyVec per pass) before it stores any.  Row r
+// of all jobs together belongs to job j when row_end[j-1] <= r < row_end[j].
+constexpr int kCopyVec = 16;
 __global__ void __launch_bounds__(256) k_copy_rows_multi(const CopyJobs J) {
   pdl_wait();
   pdl_trigger();
-  constexpr int U = 4;                   // words per thread per pass, loaded before stored
-  const int64_t total = J.end[J.n - 1];
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t0 < total; t0 += U * stride) {
-    uint4 val[U];
-    uint4* dst[U];
-#pragma unroll
-    for (int k = 0; k < U; ++k) {
-      dst[k] = nullptr;
-      const int64_t t = t0 + k * stride;
-      if (t >= total) continue;
-      int j = 0;
-      while (t >= J.end[j]) ++j;
-      const int64_t u = t - (j ? J.end[j - 1] : 0);
-      const int64_t rv = J.rv[j];
-      const int64_t r = u / rv, c = u - r * rv;
-      const int64_t d = J.di[j] ? (int64_t)J.di[j][r] : r;
-      const int64_t sr = J.si[j] ? (int64_t)J.si[j][r] : r;
-      if (d < 0 || sr < 0 || (J.dbound[j] >= 0 && d >= J.dbound[j]) || (J.sbound[j] >= 0 && sr >= J.sbound[j])) {
-        atomicOr(&g_err_mem, ERRBIT_INDEX);
-        continue;
-      }
-      val[k] = static_cast<const uint4*>(J.src[j])[sr * rv + c];
-      dst[k] = static_cast<uint4*>(J.dst[j]) + d * rv + c;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t total = J.row_end[J.n - 1];
+  for (int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < total; row += nwarps) {
+    int j = 0;
+    while (row >= J.row_end[j]) ++j;
+    const int64_t r = row - (j ? J.row_end[j - 1] : 0);
+    const int64_t d = J.di[j] ? (int64_t)J.di[j][r] : r;
+    const int64_t sr = J.si[j] ? (int64_t)J.si[j][r] : r;
+    if (d < 0 || sr < 0 || (J.dbound[j] >= 0 && d >= J.dbound[j]) || (J.sbound[j] >= 0 && sr >= J.sbound[j])) {
+      if (lane == 0) atomicOr(&g_err_mem, ERRBIT_INDEX);   // warp-uniform: the whole row is skipped
+      continue;
     }
+    const int64_t rv = J.rv[j];
+    const uint4* src = static_cast<const uint4*>(J.src[j]) + sr * rv;
+    uint4* dst = static_cast<uint4*>(J.dst[j]) + d * rv;
+    for (int64_t c0 = 0; c0 < rv; c0 += 32 * kCopyVec) {
+      uint4 v[kCopyVec];
 #pragma unroll
-    for (int k = 0; k < U; ++k)
-      if (dst[k]) *dst[k] = val[k];
+      for (int k = 0; k < kCopyVec; ++k) {
+        const int64_t c = c0 + k * 32 + lane;
+        if (c < rv) v[k] = src[c];
+      }
+#pragma unroll
+      for (int k = 0; k < kCopyVec; ++k) {
+        const int64_t c = c0 + k * 32 + lane;
+        if (c < rv) dst[c] = v[k];
+      }
+    }
   }
 }
 
 cudaError_t launch_copy_rows_multi(const CopyJobs& J, cudaStream_t s) {
   if (J.n < 1 || J.n > kMaxCopyJobs) return cudaErrorInvalidValue;
-  const int64_t total = J.end[J.n - 1];
-  if (total == 0) return cudaSuccess;
-  { const cudaError_t e_ = launch_k(k_copy_rows_multi, dim3(grid_for(k_copy_rows_multi, total, 256)), dim3(256), 0, s, J); if (e_ != cudaSuccess) return e_; }
+  const int64_t rows = J.row_end[J.n - 1];
+  if (rows == 0) return cudaSuccess;
+  { const cudaError_t e_ = launch_k(k_copy_rows_multi, dim3(grid_for(k_copy_rows_multi, rows * 32, 256)), dim3(256), 0, s, J); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 

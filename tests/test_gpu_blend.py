@@ -486,3 +486,59 @@ def test_precheck_reads_embedding_rows_in_place(E):
         B.cb_sync(None)
     assert e.value.status == 9
     B.cb_sync(None)
+
+
+def test_shutdown_then_fresh_calls_and_concurrent_host_threads(E):
+    """cb_shutdown between two blends leaves the library usable: the second blend (which
+    rebuilds every per-device cache) gives bit-identical results.  Two host threads then blend
+    two requests at once on their own streams and engines (the per-device caches are shared
+    and guarded): each result equals its request's blend run alone."""
+    import threading
+    torch = torch_mod()
+    from non_prefix_kv_gb300 import binding as B
+    wl = synth.Workload("bf16_small", BF16_SMALL, chunk_len=96, n_distinct=4, order=(0, 1, 2, 3), n_query=32,
+                        ratio=0.15, n_requests=2)
+    model = synth.make_model(wl.shape, seed=4)
+    reqs_h = synth.make_requests(wl)
+    dm = E.DeviceModel.from_host(model)
+    plan = E.layer_plan(wl.shape, wl.n_tokens, wl.n_cached, [None, 0.15, 0.15])
+    engines = [E.BlendEngine(dm, wl.n_tokens) for _ in range(2)]
+    pool = engines[0].precompute_pool(reqs_h[0].chunk_tokens)
+    alone = []
+    for i, rh in enumerate(reqs_h):
+        a = E.Request(engines[i], pool, rh.order, rh.tokens)
+        E.run_blend(a, plan)
+        B.cb_sync(None)
+        alone.append(([k.clone() for k in a.K], a.x_last[:a.m_last].clone(), int(a.token.item())))
+    B.cb_shutdown()
+    again = E.Request(engines[0], pool, reqs_h[0].order, reqs_h[0].tokens)
+    E.run_blend(again, plan)
+    B.cb_sync(None)
+    assert all(torch.equal(x, y) for x, y in zip(alone[0][0], again.K))
+    assert torch.equal(alone[0][1], again.x_last[:again.m_last])
+    B.cb_shutdown()
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    reqs = [E.Request(engines[i], pool, rh.order, rh.tokens) for i, rh in enumerate(reqs_h)]
+    errors = []
+
+    def work(i):
+        try:
+            torch.cuda.set_device(0)
+            with torch.cuda.stream(streams[i]):
+                for _ in range(3):
+                    E.run_blend(reqs[i], plan, stream=streams[i])
+            streams[i].synchronize()
+        except BaseException as e:   # reported by the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    B.cb_sync(None)
+    for i in range(2):
+        assert all(torch.equal(x, y) for x, y in zip(alone[i][0], reqs[i].K))
+        assert torch.equal(alone[i][1], reqs[i].x_last[:reqs[i].m_last])
+        assert alone[i][2] == int(reqs[i].token.item())

@@ -83,7 +83,11 @@ typedef struct {
     int32_t dtype;        /* CB_F32 or CB_BF16                                       */
 } cb_dims;
 
-/* One decoder layer's weights (device, dims->dtype).  Pre-norm Llama layer, no biases. */
+/* One decoder layer's weights (device, dims->dtype).  Pre-norm Llama layer, no biases.
+ * attn_norm / ffn_norm may be NULL: unit gains (a caller with other gains may fold them
+ * into the columns of wqkv / w_gate_up and pass NULL).  With a NULL ffn_norm the bf16 path
+ * folds the FFN norm into the GEMMs: the O-projection's epilogue leaves each row's partial
+ * sums of squares and the gate/up GEMM scales its rows by 1/rms in its epilogue. */
 typedef struct {
     const void* attn_norm;   /* [d]                                                 */
     const void* wqkv;        /* [(H + 2 Hkv) hd, d]: rows of Wq, then Wk, then Wv    */

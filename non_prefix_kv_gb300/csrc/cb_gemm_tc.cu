@@ -57,6 +57,14 @@ template <int BN>
 __device__ __forceinline__ void epilogue_tile(const GemmDesc& g, int m, int n0, int half, uint32_t trow,
                                               int swiglu) {
   constexpr int CH = BN / 32;              // 16-column chunks per warp
+  // fused RMSNorm: the row's scale from the partial sums of squares its producer left
+  float rs = 1.f;
+  const bool scaled = g.epi.rs_in != nullptr;
+  if (scaled && m < g.M) {
+    float sum = 0.f;
+    for (int p = 0; p < g.epi.rs_parts; ++p) sum += g.epi.rs_in[(int64_t)p * g.epi.rs_ld + m];
+    rs = rsqrtf(sum * g.epi.rs_inv_d + g.epi.rs_eps);
+  }
   if (!swiglu && g.epi.dev_part != nullptr) {
     // K/V columns with the deviation against the cached row: the cached values of the
     // chunk DEV_AHEAD further on are loaded while this chunk is processed
@@ -94,6 +102,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmDesc& g, int m, int n0, 
     for (int c = 0; c < CH; ++c) {
       float v[16];
       tc::tmem_ld16(trow + (half * CH + c) * 16, v);
+      if (scaled) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) v[q] *= rs;
+      }
       const int n = n0 + (half * CH + c) * 16;
       if (m < g.M && n < g.N) {
         if (!epi_apply<bf16, 16>(p, m, n, v)) atomicOr(&g_err_tc, ERRBIT_INDEX);
@@ -111,19 +123,51 @@ __device__ __forceinline__ void epilogue_tile(const GemmDesc& g, int m, int n0, 
   } else if (!swiglu) {
     // the two warps of a row band split the tile's 16-column chunks (7 + 6 at 208 columns)
     constexpr int NCH = BN / 16, H0 = (NCH + 1) / 2;
+    const EpiParams& p = g.epi;
+    float ssq = 0.f;
     for (int c = half ? H0 : 0; c < (half ? NCH : H0); ++c) {
       float v[16];
       tc::tmem_ld16(trow + c * 16, v);
+      if (scaled) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) v[q] *= rs;
+      }
       const int n = n0 + c * 16;
       if (m < g.M && n < g.N) {
-        if (!epi_apply<bf16, 16>(g.epi, m, n, v)) atomicOr(&g_err_tc, ERRBIT_INDEX);
+        if (p.ssq_out != nullptr && p.kind == EPI_RESID) {
+          // residual add, then the squares of the values as stored (bf16) for the next norm
+          const int64_t rr = p.resid_row ? (int64_t)p.resid_row[m] : (int64_t)m;
+          if (rr < 0 || (p.resid_rows >= 0 && rr >= p.resid_rows)) {
+            atomicOr(&g_err_tc, ERRBIT_INDEX);
+          } else {
+            float r[16];
+            ld_vec<bf16, 16>(static_cast<const bf16*>(p.resid) + rr * p.ldr + n, r);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              v[q] += r[q];
+              const float b = __bfloat162float(__float2bfloat16_rn(v[q]));
+              ssq = fmaf(b, b, ssq);
+            }
+            st_vec<bf16, 16>(static_cast<bf16*>(p.out) + (int64_t)m * p.ldo + n, v);
+          }
+        } else if (!epi_apply<bf16, 16>(p, m, n, v)) {
+          atomicOr(&g_err_tc, ERRBIT_INDEX);
+        }
       }
     }
+    if (p.ssq_out != nullptr && m < g.M) p.ssq_out[((int64_t)(n0 / BN) * 2 + half) * p.ssq_ld + m] = ssq;
   } else {
     for (int c = half * (CH / 2); c < (half + 1) * (CH / 2); ++c) {
       float gt[16], up[16];
       tc::tmem_ld16(trow + c * 16, gt);
       tc::tmem_ld16(trow + BN / 2 + c * 16, up);
+      if (scaled) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          gt[q] *= rs;
+          up[q] *= rs;
+        }
+      }
       const int j = n0 + c * 16;
       if (m < g.M && j < g.N) {
 #pragma unroll

@@ -57,6 +57,18 @@ struct EpiParams {
   const int32_t* ref_row = nullptr;
   int64_t ref_rows = 0;
   int dev_use_v = 1;
+  // A fused RMSNorm (tensor-core path, unit gains).  Producer (EPI_RESID): each warp writes
+  // the sum of squares of its stored (bf16) output values of row m over its half of the tile
+  // to ssq_out[(tile * 2 + half) * ssq_ld + m].  Consumer: its A operand holds the rows
+  // before the norm; row m's accumulator is multiplied by
+  // 1 / sqrt(sum_{p < rs_parts} rs_in[p * rs_ld + m] * rs_inv_d + rs_eps) first.
+  float* ssq_out = nullptr;
+  int64_t ssq_ld = 0;
+  const float* rs_in = nullptr;
+  int rs_parts = 0;
+  int64_t rs_ld = 0;
+  float rs_inv_d = 0.f;
+  float rs_eps = 0.f;
 };
 
 constexpr int kGemmTileN = 256;     // widest tensor-core GEMM tile (output columns)

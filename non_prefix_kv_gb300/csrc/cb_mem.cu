@@ -511,7 +511,12 @@ __global__ void __launch_bounds__(256) k_rmsnorm(To* __restrict__ out, const Ti*
   for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
     float v[8], gg[8], y[8];
     ld8(xr + c, v);
-    ld8(g + c, gg);
+    if (g) {
+      ld8(g + c, gg);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) gg[i] = 1.f;
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) y[i] = v[i] * inv * gg[i];
     st8(orow + c, y);
@@ -562,7 +567,7 @@ __global__ void __launch_bounds__(128) k_rmsnorm_reg(bf16* __restrict__ out, con
   for (int i = 0; i < VPT; ++i) {
     const int c = threadIdx.x + 128 * i;
     if (c < nv) {
-      const uint4 gw = gv[c];
+      const uint4 gw = gv ? gv[c] : make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);   // bf16 ones
       const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
       const __nv_bfloat162* hg = reinterpret_cast<const __nv_bfloat162*>(&gw);
       uint4 o;

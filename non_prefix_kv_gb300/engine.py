@@ -28,14 +28,19 @@ def make_dims(shape: ModelShape) -> B.cb_dims:
 class DeviceModel:
     """Weights on the device in the shape's storage dtype."""
 
-    def __init__(self, shape: ModelShape, layers: List[dict], embed, final_norm, w_lm):
+    def __init__(self, shape: ModelShape, layers: List[dict], embed, final_norm, w_lm, unit_gains=None):
+        """unit_gains: per layer (attn_norm, ffn_norm) flags, True where that norm's gains are
+        all one; the library is then given NULL for it (unit gains), which lets the bf16 path
+        fold the norm into the neighbouring GEMMs."""
         self.shape = shape
         self.dims = make_dims(shape)
         self.layers = layers
         self.embed, self.final_norm, self.w_lm = embed, final_norm, w_lm
-        self.layers_c = [B.cb_layer_w(*(l[k].data_ptr() for k in
-                                        ("attn_norm", "wqkv", "wo", "ffn_norm", "w_gate_up", "w_down")))
-                         for l in layers]
+        unit_gains = unit_gains or [(False, False)] * len(layers)
+        self.layers_c = [B.cb_layer_w(0 if ug[0] else l["attn_norm"].data_ptr(), l["wqkv"].data_ptr(),
+                                      l["wo"].data_ptr(), 0 if ug[1] else l["ffn_norm"].data_ptr(),
+                                      l["w_gate_up"].data_ptr(), l["w_down"].data_ptr())
+                         for l, ug in zip(layers, unit_gains)]
 
     @classmethod
     def from_host(cls, model: dict, device="cuda") -> "DeviceModel":
@@ -52,7 +57,9 @@ class DeviceModel:
             if id(l) not in cache:
                 cache[id(l)] = {k: up(v) for k, v in l.items()}
             layers.append(cache[id(l)])
-        return cls(shape, layers, up(model["embed"]), up(model["final_norm"]), up(model["w_lm"]))
+        unit = [(bool(np.all(np.asarray(l["attn_norm"]) == 1)), bool(np.all(np.asarray(l["ffn_norm"]) == 1)))
+                for l in model["layers"]]
+        return cls(shape, layers, up(model["embed"]), up(model["final_norm"]), up(model["w_lm"]), unit)
 
     @classmethod
     def random_on_device(cls, shape: ModelShape, seed: int = 0, device="cuda") -> "DeviceModel":
@@ -81,7 +88,9 @@ class DeviceModel:
         layers = [distinct[0 if shape.shared_layers else i] for i in range(shape.n_layers)]
         embed = normal(shape.vocab, d, std=shape.emb_std)
         w_lm = normal(shape.vocab, d, std=shape.w_std)
-        return cls(shape, layers, embed, torch.ones(d, device=device, dtype=dt), w_lm)
+        # the norm gains are ones by construction
+        return cls(shape, layers, embed, torch.ones(d, device=device, dtype=dt), w_lm,
+                   [(True, True)] * shape.n_layers)
 
 
 @dataclass

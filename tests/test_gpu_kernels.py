@@ -402,11 +402,19 @@ def test_partial_attention_at_scale(B, H, Hkv, hd, M, N):
 @pytest.mark.parametrize("shape,M", [(SHAPE_F32, 1), (SHAPE_F32, 130), (SHAPE_BF16, 1), (SHAPE_BF16, 130),
                                      (SHAPE_BF16_MID, 640)], ids=["f32-1", "f32-130", "bf16-1", "bf16-130",
                                                                   "bf16_mid-640"])
-def test_o_proj_ffn(B, shape, M):
+@pytest.mark.parametrize("unit_gains", [False, True], ids=["gains", "unit_gains"])
+def test_o_proj_ffn(B, shape, M, unit_gains):
+    """O-projection + residual, SwiGLU FFN + residual.  With unit FFN-norm gains passed as
+    NULL, the bf16 path folds the norm into the GEMMs (the O-projection leaves the rows' sums
+    of squares, the gate/up GEMM scales its rows by 1/rms); fp32 normalises with unit gains."""
     torch = torch_mod()
     dims = dims_for(B, shape)
     layer = _layer(shape, seed=3)
+    if unit_gains:
+        layer = dict(layer, ffn_norm=np.ones(shape.d_model, np.float32))
     t, w = _layer_dev(B, shape, layer)
+    if unit_gains:
+        w.ffn_norm = None
     attn = synth.test_tensor((M, shape.q_width), 80, dtype=shape.dtype)
     xr = synth.test_tensor((M, shape.d_model), 81, dtype=shape.dtype)
     out = torch.empty(M, shape.d_model, dtype=tdt(shape.dtype), device="cuda")

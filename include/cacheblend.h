@@ -366,6 +366,18 @@ typedef struct {
   void* aux_stream;
   void* aux_fork;
   void* aux_join;
+  /* Row statistics passed from layer to layer, so that the bf16 path with unit attention-norm
+   * gains (attn_norm NULL) needs no separate norm pass.
+   *   x_out_ssq : caller memory of n_tok * 2 * ceil(d / 192) floats, or NULL.  The call writes
+   *     there each x_out row's partial sums of squares (a layout private to the library) and
+   *     their count to *x_out_ssq_parts_host (0 when it wrote none: fp32).
+   *   x_in_ssq / x_in_ssq_parts : the same from the call that produced x_in (x_in_ssq_parts 0
+   *     or NULL x_in_ssq: none).  CHECK, GRADUAL and STEADY then read x_in un-normalised and
+   *     scale each row by 1/rms in their Q/K/V GEMMs' epilogues. */
+  float* x_out_ssq;
+  int32_t* x_out_ssq_parts_host;
+  const float* x_in_ssq;
+  int32_t x_in_ssq_parts;
 } cb_layer_opts;
 
 int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode,

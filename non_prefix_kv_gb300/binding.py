@@ -29,7 +29,8 @@ class cb_layer_opts(C.Structure):
     _fields_ = [("forced_mask", C.c_void_p), ("n_forced", C.c_int32), ("kv_ready", C.c_void_p),
                 ("recompute_kv", C.c_int32), ("recompute_from", C.c_int32), ("x_rows", C.c_void_p),
                 ("n_x_rows", C.c_int64), ("aux_stream", C.c_void_p), ("aux_fork", C.c_void_p),
-                ("aux_join", C.c_void_p)]
+                ("aux_join", C.c_void_p), ("x_out_ssq", C.c_void_p), ("x_out_ssq_parts_host", C.POINTER(C.c_int32)),
+                ("x_in_ssq", C.c_void_p), ("x_in_ssq_parts", C.c_int32)]
 
 
 class cb_dims(C.Structure):
@@ -258,7 +259,8 @@ def cb_blend_layer(dims: cb_dims, w: cb_layer_w, mode: int, x_in, s_in, m_in: in
                    k_cache, v_cache, cos_sin, max_pos: int, k_budget: int, dev_mode: int, sel_override,
                    x_out, s_out, scores_out, ws, stream=None, kv_ready=None, forced_mask=None,
                    n_forced: int = 0, recompute_kv: bool = False, recompute_from: int = 0, x_rows=None,
-                   n_x_rows: int = 0, aux=None) -> int:
+                   n_x_rows: int = 0, aux=None, x_out_ssq=None, ssq_parts_out: Optional[list] = None, x_in_ssq=None,
+                   x_in_ssq_parts: int = 0) -> int:
     """kv_ready: a torch.cuda.Event (or raw cudaEvent_t) the layer waits for just before it
     first touches the cached rows, or None.  forced_mask/n_forced: uncached rows anywhere
     (a uint8 device tensor over the tokens, marking the last row too), or None.
@@ -266,20 +268,28 @@ def cb_blend_layer(dims: cb_dims, w: cb_layer_w, mode: int, x_in, s_in, m_in: in
     x_rows / n_x_rows: PRECHECK only, input row i is x_in[x_rows[i]] (e.g. x_in = the embedding
     table, x_rows = the token ids).
     aux: (stream, fork event, join event) for the CHECK/GRADUAL KV expansion beside the Q GEMM,
-    or None."""
+    or None.
+    x_out_ssq: a float32 device buffer that receives the output rows' partial sums of squares;
+    their count is stored in ssq_parts_out[0].  x_in_ssq / x_in_ssq_parts: the same from the
+    call that produced x_in (lets the bf16 path with unit attention-norm gains skip the norm)."""
     m_out = _I32(0)
     opts = None
+    parts = _I32(0)
     if (kv_ready is not None or forced_mask is not None or recompute_kv or recompute_from or x_rows is not None
-            or aux is not None):
+            or aux is not None or x_out_ssq is not None or x_in_ssq is not None):
         ev = kv_ready if (kv_ready is None or isinstance(kv_ready, int)) else kv_ready.cuda_event
         ax = (None, None, None) if aux is None else (_stream(aux[0]), _event(aux[1]), _event(aux[2]))
         opts = C.byref(cb_layer_opts(_ptr(forced_mask), n_forced if forced_mask is not None else 0, ev,
                                      1 if recompute_kv else 0, int(recompute_from), _ptr(x_rows),
-                                     int(n_x_rows) if x_rows is not None else 0, *ax))
+                                     int(n_x_rows) if x_rows is not None else 0, *ax, _ptr(x_out_ssq),
+                                     C.pointer(parts) if x_out_ssq is not None else None, _ptr(x_in_ssq),
+                                     int(x_in_ssq_parts) if x_in_ssq is not None else 0))
     _check("cb_blend_layer", lib().cb_blend_layer(
         C.byref(dims), C.byref(w), mode, _ptr(x_in), _ptr(s_in), m_in, n_tok, n_cached, _ptr(k_cache),
         _ptr(v_cache), _ptr(cos_sin), max_pos, k_budget, dev_mode, _ptr(sel_override), _ptr(x_out),
         _ptr(s_out), C.byref(m_out), _ptr(scores_out), opts, _ptr(ws), _nbytes(ws), _stream(stream)))
+    if ssq_parts_out is not None:
+        ssq_parts_out[:] = [int(parts.value)]
     return int(m_out.value)
 
 

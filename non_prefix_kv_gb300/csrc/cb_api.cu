@@ -359,8 +359,11 @@ GemmDesc qkv_desc(const cb_dims* d, const cb_layer_w* w, const void* a, int M, i
 // h = x_res[res_row[m]] + attn Wo^T ; x_out = h + (silu(b Wg^T) * b Wu^T) Wd^T, b = RMSNorm(h) g.
 // res_row null: row m of x_res; otherwise rows of x_res (res_rows of them) read in place, so the
 // residual rows of a selection need no gather.
+// x_ssq / x_ssq_parts_host (optional): the bf16 path writes each x_out row's partial sums
+// of squares there (for the next layer's norm) and their count on the host.
 int o_ffn(const cb_dims* d, const cb_layer_w* w, const void* attn, const void* x_res, int M, void* x_out,
-          const LayerWs& ws, cudaStream_t s, const int32_t* res_row = nullptr, int64_t res_rows = -1) {
+          const LayerWs& ws, cudaStream_t s, const int32_t* res_row = nullptr, int64_t res_rows = -1,
+          float* x_ssq = nullptr, int32_t* x_ssq_parts_host = nullptr) {
   if (M == 0) return CB_OK;
   const int qc = d->n_heads * d->head_dim;
   // with unit FFN-norm gains (ffn_norm NULL) the bf16 path folds the norm into the GEMMs:
@@ -400,6 +403,12 @@ int o_ffn(const cb_dims* d, const cb_layer_w* w, const void* attn, const void* x
   gd.epi.ldo = d->d_model;
   gd.epi.resid = ws.h;
   gd.epi.ldr = d->d_model;
+  const bool stats = d->dtype == CB_BF16 && x_ssq != nullptr;
+  if (stats) {
+    gd.epi.ssq_out = x_ssq;
+    gd.epi.ssq_ld = M;
+  }
+  if (x_ssq_parts_host) *x_ssq_parts_host = stats ? dev_parts(d->d_model, gemm_tc_tile_n(&gd, 1)) : 0;
   L_GEMM(d->dtype, gd, s);
   return CB_OK;
 }
@@ -731,6 +740,16 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
   if (x_rows && (mode != CB_LAYER_PRECHECK || n_x_rows < 1))
     return fail(CB_ERR_INVALID_ARG, "x_rows applies to PRECHECK, with n_x_rows >= 1");
   const bool fork = opts && opts->aux_stream;
+  float* ssq_out = opts ? opts->x_out_ssq : nullptr;
+  int32_t* ssq_out_parts = opts ? opts->x_out_ssq_parts_host : nullptr;
+  if (ssq_out && !ssq_out_parts) return fail(CB_ERR_INVALID_ARG, "x_out_ssq needs x_out_ssq_parts_host");
+  const float* ssq_in = opts ? opts->x_in_ssq : nullptr;
+  const int ssq_in_parts = opts ? opts->x_in_ssq_parts : 0;
+  if (ssq_in && (ssq_in_parts < 0 || ssq_in_parts > dev_parts(dims->d_model)))
+    return fail(CB_ERR_SHAPE, "x_in_ssq_parts %d outside [0, %d]", ssq_in_parts, dev_parts(dims->d_model));
+  // the attention norm folded into the Q/K/V GEMMs: bf16, unit gains, the input's statistics
+  const bool fuse_in = ssq_in && ssq_in_parts > 0 && dims->dtype == CB_BF16 && w->attn_norm == nullptr &&
+                       mode != CB_LAYER_PRECHECK;
   if (opts && ((opts->aux_stream == nullptr) != (opts->aux_fork == nullptr) ||
                (opts->aux_stream == nullptr) != (opts->aux_join == nullptr)))
     return fail(CB_ERR_INVALID_ARG, "aux_stream, aux_fork and aux_join must all be set or all NULL");
@@ -771,7 +790,7 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         g.epi.kv_bound = N;
         L_GEMM(dims->dtype, g, s);
         L_ATTN(dims->dtype, L.q, s_out, N, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
-        return o_ffn(dims, w, L.attn, x_in, N, x_out, L, s, x_rows, x_rows ? n_x_rows : -1);
+        return o_ffn(dims, w, L.attn, x_in, N, x_out, L, s, x_rows, x_rows ? n_x_rows : -1, ssq_out, ssq_out_parts);
       }
       // Q of every row and K/V of the uncached rows (and of the cached rows from
       // recompute_from on): independent, so one shared launch
@@ -795,7 +814,7 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
       }
       WAIT_CACHED_ROWS();
       L_ATTN(dims->dtype, L.q, s_out, N, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
-      return o_ffn(dims, w, L.attn, x_in, N, x_out, L, s, x_rows, x_rows ? n_x_rows : -1);
+      return o_ffn(dims, w, L.attn, x_in, N, x_out, L, s, x_rows, x_rows ? n_x_rows : -1, ssq_out, ssq_out_parts);
     }
     case CB_LAYER_CHECK:
     case CB_LAYER_GRADUAL: {
@@ -824,15 +843,27 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         cpos = L.cpos;
         crows = L.crows;
       }
-      L_RMSNORM(dims->dtype, dims->dtype, L.a, x_in, nullptr, w->attn_norm, m_in, dims->d_model, dims->rms_eps, s);
+      if (!fuse_in)
+        L_RMSNORM(dims->dtype, dims->dtype, L.a, x_in, nullptr, w->attn_norm, m_in, dims->d_model, dims->rms_eps, s);
+      const void* a_in = fuse_in ? x_in : L.a;   // the GEMMs' rows: normalised, or scaled in the epilogue
+      auto fold_norm = [&](GemmDesc& g, const int32_t* row_map) {
+        if (!fuse_in) return;
+        g.epi.rs_in = ssq_in;
+        g.epi.rs_row = row_map;
+        g.epi.rs_parts = ssq_in_parts;
+        g.epi.rs_ld = m_in;
+        g.epi.rs_inv_d = 1.0f / (float)dims->d_model;
+        g.epi.rs_eps = dims->rms_eps;
+      };
       WAIT_CACHED_ROWS();
       // A gradual layer whose incoming set is at most 25% larger than its selection computes
       // Q for every incoming row in the same GEMM (one wider launch) and gathers the
       // selected queries afterwards; otherwise Q is computed for the selected rows only.
       const bool q_all = !check && (int64_t)m_in * 4 <= (int64_t)M * 5;
       const int col0 = q_all ? 0 : qc, ncols = q_all ? qc + 2 * W : 2 * W;
-      GemmDesc gkv = qkv_desc(dims, w, L.a, m_in, col0, ncols, q_all ? L.q : nullptr, L.knew, L.vnew, rows_in, nullptr,
+      GemmDesc gkv = qkv_desc(dims, w, a_in, m_in, col0, ncols, q_all ? L.q : nullptr, L.knew, L.vnew, rows_in, nullptr,
                               cos_sin, max_pos);
+      fold_norm(gkv, nullptr);
       if (dims->dtype == CB_BF16) {
         // the deviation is taken in the K/V GEMM's epilogue; a small pass sums the tiles
         gkv.epi.dev_part = L.dev_part;
@@ -881,7 +912,7 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         if (q_all)
           rc.add(L.qg, nullptr, L.q, L.keep, M, (int64_t)qc * B, M, m_in);
         else
-          rc.add(L.ag, nullptr, L.a, L.keep, M, (int64_t)dims->d_model * B, M, m_in);
+          rc.add(L.ag, nullptr, a_in, L.keep, M, (int64_t)dims->d_model * B, M, m_in);
         if (fork_kv) {
           cudaStream_t aux = S(opts->aux_stream);
           CB_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(opts->aux_fork), s));
@@ -892,11 +923,14 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         if ((st = rc.launch(s))) return st;
       }
       const void* qsel = q_all ? L.qg : L.q;
-      if (!q_all)
-        L_GEMM(dims->dtype, qkv_desc(dims, w, L.ag, M, 0, qc, L.q, nullptr, nullptr, s_out, nullptr, cos_sin, max_pos), s);
+      if (!q_all) {
+        GemmDesc gq = qkv_desc(dims, w, L.ag, M, 0, qc, L.q, nullptr, nullptr, s_out, nullptr, cos_sin, max_pos);
+        fold_norm(gq, L.keep);   // row m of the selection is row keep[m] of the input
+        L_GEMM(dims->dtype, gq, s);
+      }
       if (fork && !q_all) CB_CUDA(cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(opts->aux_join), 0));
       L_ATTN(dims->dtype, qsel, s_out, M, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
-      return o_ffn(dims, w, L.attn, x_in, M, x_out, L, s, L.keep, m_in);
+      return o_ffn(dims, w, L.attn, x_in, M, x_out, L, s, L.keep, m_in, ssq_out, ssq_out_parts);
     }
     case CB_LAYER_STEADY: {
       if (m_in < 1 || m_in > N) return fail(CB_ERR_SHAPE, "STEADY needs 1 <= m_in <= n_tok");
@@ -907,14 +941,23 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
         CB_CUDA(cudaMemcpyAsync(s_out, s_in, (size_t)m_in * 4, cudaMemcpyDeviceToDevice, s));
       else
         L_IOTA(s_out, m_in, 0, s);
-      L_RMSNORM(dims->dtype, dims->dtype, L.a, x_in, nullptr, w->attn_norm, m_in, dims->d_model, dims->rms_eps, s);
+      if (!fuse_in)
+        L_RMSNORM(dims->dtype, dims->dtype, L.a, x_in, nullptr, w->attn_norm, m_in, dims->d_model, dims->rms_eps, s);
       WAIT_CACHED_ROWS();
       // s_out is the caller's row set: its rows are checked against the cache height
-      GemmDesc g = qkv_desc(dims, w, L.a, m_in, 0, qc + 2 * W, L.q, k_cache, v_cache, s_out, s_out, cos_sin, max_pos);
+      GemmDesc g = qkv_desc(dims, w, fuse_in ? x_in : L.a, m_in, 0, qc + 2 * W, L.q, k_cache, v_cache, s_out, s_out,
+                            cos_sin, max_pos);
       g.epi.kv_bound = N;
+      if (fuse_in) {
+        g.epi.rs_in = ssq_in;
+        g.epi.rs_parts = ssq_in_parts;
+        g.epi.rs_ld = m_in;
+        g.epi.rs_inv_d = 1.0f / (float)dims->d_model;
+        g.epi.rs_eps = dims->rms_eps;
+      }
       L_GEMM(dims->dtype, g, s);
       L_ATTN(dims->dtype, L.q, s_out, m_in, k_cache, v_cache, N, dims->n_heads, dims->n_kv_heads, dims->head_dim, L.attn, L.attn_ws, 0, s);
-      return o_ffn(dims, w, L.attn, x_in, m_in, x_out, L, s);
+      return o_ffn(dims, w, L.attn, x_in, m_in, x_out, L, s, nullptr, -1, ssq_out, ssq_out_parts);
     }
     default:
       return fail(CB_ERR_INVALID_ARG, "mode %d", mode);

@@ -51,20 +51,36 @@ struct TileCfg {
   static constexpr int SMEM_BYTES = STAGES * (A_BYTES + B_BYTES) + 1024 /*align slack*/ + 256 /*barriers*/;
 };
 
+// Fused RMSNorm: row m's scale 1/rms from the partial sums of squares its producer left
+// (1 without them).  Read before the epilogue waits for its accumulator, so the loads are
+// hidden under the tile's main loop; eight are in flight at a time, summed in a fixed order.
+__device__ __forceinline__ float row_scale(const GemmDesc& g, int m) {
+  const EpiParams& p = g.epi;
+  if (p.rs_in == nullptr || m >= g.M) return 1.f;
+  const int64_t sm = p.rs_row ? (int64_t)p.rs_row[m] : (int64_t)m;
+  if (sm < 0 || sm >= p.rs_ld) {
+    atomicOr(&g_err_tc, ERRBIT_INDEX);
+    return 1.f;
+  }
+  float sum = 0.f;
+  for (int p0 = 0; p0 < p.rs_parts; p0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = p0 + i < p.rs_parts ? p.rs_in[(int64_t)(p0 + i) * p.rs_ld + sm] : 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sum += v[i];
+  }
+  return rsqrtf(sum * p.rs_inv_d + p.rs_eps);
+}
+
 // Epilogue of one output tile for one epilogue warp: this lane's accumulator row m (TMEM row
-// band at trow), the warp's half of the tile's columns [n0, n0 + BN).
+// band at trow), the warp's half of the tile's columns [n0, n0 + BN); rs scales the row
+// (fused RMSNorm, see row_scale).
 template <int BN>
 __device__ __forceinline__ void epilogue_tile(const GemmDesc& g, int m, int n0, int half, uint32_t trow,
-                                              int swiglu) {
+                                              int swiglu, float rs) {
   constexpr int CH = BN / 32;              // 16-column chunks per warp
-  // fused RMSNorm: the row's scale from the partial sums of squares its producer left
-  float rs = 1.f;
   const bool scaled = g.epi.rs_in != nullptr;
-  if (scaled && m < g.M) {
-    float sum = 0.f;
-    for (int p = 0; p < g.epi.rs_parts; ++p) sum += g.epi.rs_in[(int64_t)p * g.epi.rs_ld + m];
-    rs = rsqrtf(sum * g.epi.rs_inv_d + g.epi.rs_eps);
-  }
   if (!swiglu && g.epi.dev_part != nullptr) {
     // K/V columns with the deviation against the cached row: the cached values of the
     // chunk DEV_AHEAD further on are loaded while this chunk is processed
@@ -330,6 +346,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       locate(t, pr, m0, n0);
       const GemmDesc& g = pr ? g1 : g0;
       const int m = m0 + lane_base + lane;
+      const float rs = row_scale(g, m);
       // every lane waits, then the warp re-converges before the .sync.aligned TMEM loads
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&acc_full[b], (i >> 1) & 1))) {
         if (lane == 0) atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
@@ -337,7 +354,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc::tc_fence_after();
       const uint32_t trow = tmem + b * 256 + (static_cast<uint32_t>(lane_base) << 16);
-      epilogue_tile<BN>(g, m, n0, half, trow, swiglu);
+      epilogue_tile<BN>(g, m, n0, half, trow, swiglu, rs);
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&acc_empty[b]);
@@ -518,13 +535,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       locate(t, pr, m0, n0);
       const GemmDesc& g = pr ? g1 : g0;
       const int m = m0 + (int)rank * BM + lane_base + lane;
+      const float rs = row_scale(g, m);
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&acc_full[b], (i >> 1) & 1))) {
         if (lane == 0) atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
         break;
       }
       tc::tc_fence_after();
       const uint32_t trow = tmem + b * 256 + (static_cast<uint32_t>(lane_base) << 16);
-      epilogue_tile<BN>(g, m, n0, half, trow, swiglu);
+      epilogue_tile<BN>(g, m, n0, half, trow, swiglu, rs);
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_cluster(b ? release1 : release0);

@@ -65,6 +65,7 @@ struct EpiParams {
   float* ssq_out = nullptr;
   int64_t ssq_ld = 0;
   const float* rs_in = nullptr;
+  const int32_t* rs_row = nullptr;  // row of rs_in's statistics for output row m, or null (m)
   int rs_parts = 0;
   int64_t rs_ld = 0;
   float rs_inv_d = 0.f;

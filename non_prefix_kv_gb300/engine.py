@@ -251,6 +251,10 @@ class Request:
             self.K = [torch.zeros(self.N, s.kv_width, dtype=dt, device=dev) for _ in range(s.n_layers)]
             self.V = [torch.zeros(self.N, s.kv_width, dtype=dt, device=dev) for _ in range(s.n_layers)]
         self.x = [torch.empty(self.N, s.d_model, dtype=dt, device=dev) for _ in range(2)]
+        # each hidden-row buffer's partial sums of squares (left by the layer that wrote it, so
+        # the next layer's norm folds into its GEMMs); at most 2 * ceil(d / 192) per row
+        self.ssq = [torch.empty(2 * -(-s.d_model // 192) * self.N, dtype=torch.float32, device=dev)
+                    for _ in range(2)]
         self.s = [torch.empty(self.N, dtype=torch.int32, device=dev) for _ in range(2)]
         self.scores = torch.empty(self.N, dtype=torch.float32, device=dev)
         self.token = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -471,7 +475,7 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
               file_store: Optional[FileStore] = None, recompute_precheck_kv: bool = False,
               precheck_load_rows: Optional[int] = None, overlap_assembly: bool = True,
               layer_events: Optional[list] = None, upto: Optional[int] = None, x_out_last=None, s_out_last=None,
-              aux_expansion: bool = True):
+              aux_expansion: bool = True, fold_norms: bool = True):
     """One blended prefill: re-position the chunk KV of every layer, run the layer plan,
     then the lm_head argmax.  Returns the number of rows carried out of the last layer.
 
@@ -504,6 +508,10 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
 
     aux_expansion (default on): check and gradual layers expand the selected rows' K/V on
     the engine's aux stream beside the selected queries' GEMM.
+
+    fold_norms (default on): each layer hands its output rows' sums of squares to the next,
+    so that with unit attention-norm gains (bf16) the next layer folds its norm into its
+    Q/K/V GEMMs instead of running a norm pass.
 
     upto: run layers [0, upto) only and skip the lm_head (every layer's chunk KV is still
     re-positioned); the last of them writes its rows to x_out_last / s_out_last when given.
@@ -638,6 +646,7 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
                 if l not in skip:
                     assemble_layer(l, stream)
     cur = 0
+    ssq_parts = 0                       # statistics of req.x[cur] (none for the first layer)
     if keep_history:
         req.sel_hist, req.m_hist = [], []
     for l, (mode, k) in enumerate(plan):
@@ -654,6 +663,7 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
             ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             ev[0].record(torch.cuda.current_stream() if stream is None else stream)
         first = embed_in_place and l == 0
+        parts_out = [0]
         m_out = B.cb_blend_layer(dims, dm.layers_c[l], mode, dm.embed if first else req.x[cur], s_in, m_in, req.N,
                                  req.n_cached,
                                  req.K[l], req.V[l], eng.cos_sin, eng.max_pos, k, dev_mode, ov,
@@ -667,13 +677,18 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
                                  recompute_from=split if (split is not None and l in pre) else 0,
                                  x_rows=req.tokens if first else None, n_x_rows=s.vocab if first else 0,
                                  aux=((eng.aux_stream,) + eng.aux_events
-                                      if aux_expansion and mode in (B.CB_LAYER_CHECK, B.CB_LAYER_GRADUAL) else None))
+                                      if aux_expansion and mode in (B.CB_LAYER_CHECK, B.CB_LAYER_GRADUAL) else None),
+                                 x_out_ssq=None if (last or not fold_norms) else req.ssq[1 - cur],
+                                 ssq_parts_out=parts_out,
+                                 x_in_ssq=req.ssq[cur] if (ssq_parts and not first) else None,
+                                 x_in_ssq_parts=ssq_parts)
         if layer_events is not None:
             ev[1].record(torch.cuda.current_stream() if stream is None else stream)
             layer_events.append((l, ev[0], ev[1]))
         cur = 1 - cur
         s_in = req.s[cur]
         m_in = m_out
+        ssq_parts = parts_out[0]
         if queue_loads is not None:
             queue_loads(l + 2)
         if keep_history:
@@ -757,7 +772,7 @@ def run_blend_batch(batch: RequestBatch, plan, stream=None) -> List[int]:
     batch._buffers(row0[-1])
     for r, req in enumerate(batch.reqs):
         m = run_blend(req, plan, stream=stream, upto=c + 1, x_out_last=batch.X[0][row0[r]:row0[r + 1]],
-                      s_out_last=batch.S[row0[r]:row0[r + 1]])
+                      s_out_last=batch.S[row0[r]:row0[r + 1]], fold_norms=False)
         if m != m_r[r]:
             raise RuntimeError(f"request {r}: {m} rows out of the check layer, {m_r[r]} expected")
     cur = 0

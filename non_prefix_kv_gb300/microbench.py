@@ -48,6 +48,9 @@ def run(argv=None):
     p.add_argument("--n", type=int, default=8192)
     p.add_argument("--k", type=int, default=4096)
     p.add_argument("--epi", choices=["store", "swiglu"], default="store")
+    p.add_argument("--unit-gains", action="store_true",
+                   help="swiglu: NULL norm gains, as the bf16 step runs it (the FFN norm folded into the "
+                        "gate/up GEMM, the O-projection leaving its rows' sums of squares)")
     p.add_argument("--host-src", action="store_true", help="rope_shift: sources in pinned host memory")
     p.add_argument("--heads", type=int, default=32)
     p.add_argument("--kv-heads", type=int, default=32)
@@ -81,15 +84,15 @@ def run(argv=None):
                   "ffn_norm": torch.ones(a.k, device="cuda", dtype=bf),
                   "w_gate_up": (torch.randn(2 * a.n, a.k, device="cuda", generator=g) * 0.02).to(bf),
                   "w_down": (torch.randn(a.k, a.n, device="cuda", generator=g) * 0.02).to(bf)}
-            cw = B.cb_layer_w(*(lw[k].data_ptr() for k in ("attn_norm", "wqkv", "wo", "ffn_norm", "w_gate_up",
-                                                            "w_down")))
+            cw = B.cb_layer_w(*(0 if a.unit_gains and k.endswith("_norm") else lw[k].data_ptr()
+                                for k in ("attn_norm", "wqkv", "wo", "ffn_norm", "w_gate_up", "w_down")))
             attn = torch.randn(a.m, 128, device="cuda", generator=g).to(bf)
             x = torch.randn(a.m, a.k, device="cuda", generator=g).to(bf)
             y = torch.empty_like(x)
             ws = torch.empty(B.cb_workspace_bytes(dims, a.m, a.m), dtype=torch.uint8, device="cuda")
             ms = _time(lambda: B.cb_o_proj_ffn(attn, x, a.m, dims, cw, y, ws), a.iters, a.warmup)
             fl = 2.0 * a.m * a.k * (128 + 3 * a.n)
-        out.update(ms=ms, tflops=fl / (ms / 1e3) / 1e12, m=a.m, n=a.n, k=a.k, epi=a.epi)
+        out.update(ms=ms, tflops=fl / (ms / 1e3) / 1e12, m=a.m, n=a.n, k=a.k, epi=a.epi, unit_gains=a.unit_gains)
     elif a.what == "attention":
         shape = ModelShape(1, 256, a.heads, a.kv_heads, a.hd, 256, 64, dtype="bf16")
         dims = E.make_dims(shape)

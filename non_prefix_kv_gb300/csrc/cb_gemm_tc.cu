@@ -73,18 +73,35 @@ __device__ __forceinline__ float row_scale(const GemmDesc& g, int m) {
   return rsqrtf(sum * p.rs_inv_d + p.rs_eps);
 }
 
+// Side inputs of the plain epilogue, per 16-column chunk: the residual row's 16 values (two
+// 16-byte words) or the RoPE cos/sin of the row's position for the chunk's 8 pairs (four
+// words).  They are loaded a few chunks ahead of their use, the first ones before the
+// accumulator is ready, so the loads' latency overlaps the tile's main loop instead of
+// following each TMEM read.
+template <int WORDS, int AHEAD>
+struct SideRing {
+  uint4 w[AHEAD][WORDS];
+  __device__ __forceinline__ void load(int slot, const uint4* src) {
+    if (src) {
+#pragma unroll
+      for (int i = 0; i < WORDS; ++i) w[slot][i] = __ldg(src + i);
+    }
+  }
+};
+
 // Epilogue of one output tile for one epilogue warp: this lane's accumulator row m (TMEM row
 // band at trow), the warp's half of the tile's columns [n0, n0 + BN); rs scales the row
-// (fused RMSNorm, see row_scale).
-template <int BN>
-__device__ __forceinline__ void epilogue_tile(const GemmDesc& g, int m, int n0, int half, uint32_t trow,
-                                              int swiglu, float rs) {
+// (fused RMSNorm, see row_scale).  The loads that do not depend on the accumulator are
+// issued first; wait_acc() then waits for it (false: the wait gave up, nothing is written).
+template <int BN, typename WaitFn>
+__device__ __forceinline__ bool epilogue_tile(const GemmDesc& g, int m, int n0, int half, uint32_t trow,
+                                              int swiglu, float rs, WaitFn wait_acc) {
   constexpr int CH = BN / 32;              // 16-column chunks per warp
   const bool scaled = g.epi.rs_in != nullptr;
-  if (!swiglu && g.epi.dev_part != nullptr) {
+  const EpiParams& p = g.epi;
+  if (!swiglu && p.dev_part != nullptr) {
     // K/V columns with the deviation against the cached row: the cached values of the
     // chunk DEV_AHEAD further on are loaded while this chunk is processed
-    const EpiParams& p = g.epi;
     int64_t rr = -1;
     if (m < g.M) {
       rr = p.ref_row ? (int64_t)p.ref_row[m] : (int64_t)m;
@@ -104,15 +121,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmDesc& g, int m, int n0, 
                                             (gc - p.q_cols - (is_v ? p.kv_cols : 0)));
     };
     constexpr int DEV_AHEAD = 4;
-    uint4 ring[DEV_AHEAD][2];
+    SideRing<2, DEV_AHEAD> ring;
 #pragma unroll
-    for (int c = 0; c < DEV_AHEAD; ++c) {
-      const uint4* q = ref_ptr(c);
-      if (q) {
-        ring[c][0] = __ldg(q);
-        ring[c][1] = __ldg(q + 1);
-      }
-    }
+    for (int c = 0; c < DEV_AHEAD; ++c) ring.load(c, ref_ptr(c));
+    if (!wait_acc()) return false;
     float dsum = 0.f;
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
@@ -126,53 +138,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmDesc& g, int m, int n0, 
       if (m < g.M && n < g.N) {
         if (!epi_apply<bf16, 16>(p, m, n, v)) atomicOr(&g_err_tc, ERRBIT_INDEX);
       }
-      if (ref_ptr(c)) dsum += sq_dev16(v, ring[c % DEV_AHEAD]);
-      if (c + DEV_AHEAD < CH) {
-        const uint4* q = ref_ptr(c + DEV_AHEAD);
-        if (q) {
-          ring[c % DEV_AHEAD][0] = __ldg(q);
-          ring[c % DEV_AHEAD][1] = __ldg(q + 1);
-        }
-      }
+      if (ref_ptr(c)) dsum += sq_dev16(v, ring.w[c % DEV_AHEAD]);
+      if (c + DEV_AHEAD < CH) ring.load(c % DEV_AHEAD, ref_ptr(c + DEV_AHEAD));
     }
     if (m < g.M) p.dev_part[((int64_t)(n0 / BN) * 2 + half) * p.dev_ld + m] = dsum;
-  } else if (!swiglu) {
-    // the two warps of a row band split the tile's 16-column chunks (7 + 6 at 208 columns)
-    constexpr int NCH = BN / 16, H0 = (NCH + 1) / 2;
-    const EpiParams& p = g.epi;
-    float ssq = 0.f;
-    for (int c = half ? H0 : 0; c < (half ? NCH : H0); ++c) {
-      float v[16];
-      tc::tmem_ld16(trow + c * 16, v);
-      if (scaled) {
-#pragma unroll
-        for (int q = 0; q < 16; ++q) v[q] *= rs;
-      }
-      const int n = n0 + c * 16;
-      if (m < g.M && n < g.N) {
-        if (p.ssq_out != nullptr && p.kind == EPI_RESID) {
-          // residual add, then the squares of the values as stored (bf16) for the next norm
-          const int64_t rr = p.resid_row ? (int64_t)p.resid_row[m] : (int64_t)m;
-          if (rr < 0 || (p.resid_rows >= 0 && rr >= p.resid_rows)) {
-            atomicOr(&g_err_tc, ERRBIT_INDEX);
-          } else {
-            float r[16];
-            ld_vec<bf16, 16>(static_cast<const bf16*>(p.resid) + rr * p.ldr + n, r);
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              v[q] += r[q];
-              const float b = __bfloat162float(__float2bfloat16_rn(v[q]));
-              ssq = fmaf(b, b, ssq);
-            }
-            st_vec<bf16, 16>(static_cast<bf16*>(p.out) + (int64_t)m * p.ldo + n, v);
-          }
-        } else if (!epi_apply<bf16, 16>(p, m, n, v)) {
-          atomicOr(&g_err_tc, ERRBIT_INDEX);
-        }
-      }
-    }
-    if (p.ssq_out != nullptr && m < g.M) p.ssq_out[((int64_t)(n0 / BN) * 2 + half) * p.ssq_ld + m] = ssq;
-  } else {
+    return true;
+  }
+  if (swiglu) {
+    if (!wait_acc()) return false;
     for (int c = half * (CH / 2); c < (half + 1) * (CH / 2); ++c) {
       float gt[16], up[16];
       tc::tmem_ld16(trow + c * 16, gt);
@@ -188,10 +161,159 @@ __device__ __forceinline__ void epilogue_tile(const GemmDesc& g, int m, int n0, 
       if (m < g.M && j < g.N) {
 #pragma unroll
         for (int q = 0; q < 16; ++q) gt[q] = silu_f(gt[q]) * up[q];
-        st_vec<bf16, 16>(static_cast<bf16*>(g.epi.out) + (int64_t)m * g.epi.ldo + j, gt);
+        st_vec<bf16, 16>(static_cast<bf16*>(p.out) + (int64_t)m * p.ldo + j, gt);
       }
     }
+    return true;
   }
+  // the two warps of a row band split the tile's 16-column chunks (7 + 6 at 208 columns)
+  constexpr int NCH = BN / 16, H0 = (NCH + 1) / 2;
+  const int c_lo = half ? H0 : 0, c_hi = half ? NCH : H0;
+  if (p.kind == EPI_RESID) {
+    // residual add (and, for the next layer's norm, the squares of the values as stored)
+    const int64_t rr = m < g.M ? (p.resid_row ? (int64_t)p.resid_row[m] : (int64_t)m) : -1;
+    const bool row_ok = m < g.M && rr >= 0 && (p.resid_rows < 0 || rr < p.resid_rows);
+    if (m < g.M && !row_ok) atomicOr(&g_err_tc, ERRBIT_INDEX);
+    const bf16* rrow = row_ok ? static_cast<const bf16*>(p.resid) + rr * p.ldr : nullptr;
+    const bool vec = rrow != nullptr && ((reinterpret_cast<uintptr_t>(rrow + n0) & 15) == 0);
+    SideRing<2, 2> ring;
+    auto src = [&](int c) -> const uint4* {
+      const int n = n0 + c * 16;
+      return (vec && c < c_hi && n < g.N) ? reinterpret_cast<const uint4*>(rrow + n) : nullptr;
+    };
+    ring.load(0, src(c_lo));
+    ring.load(1, src(c_lo + 1));
+    if (!wait_acc()) return false;
+    float ssq = 0.f;
+    // chunks in pairs, so ring slot = chunk parity at compile time with two chunk bodies of code;
+    // chunk c + 2's side input is requested while chunk c is processed
+    for (int c2 = c_lo; c2 < c_hi; c2 += 2) {
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        const int c = c2 + a;
+        if (c >= c_hi) break;
+        float v[16];
+        tc::tmem_ld16(trow + c * 16, v);
+        if (scaled) {
+#pragma unroll
+          for (int q = 0; q < 16; ++q) v[q] *= rs;
+        }
+        const int n = n0 + c * 16;
+        if (row_ok && n < g.N) {
+          float r[16];
+          if (vec) {
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(ring.w[a]);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float2 f = __bfloat1622float2(h2[q]);
+              r[2 * q] = f.x;
+              r[2 * q + 1] = f.y;
+            }
+          } else {
+            ld_vec<bf16, 16>(rrow + n, r);
+          }
+#pragma unroll
+          for (int q = 0; q < 16; ++q) v[q] += r[q];
+          if (p.ssq_out != nullptr) {
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const float b = __bfloat162float(__float2bfloat16_rn(v[q]));
+              ssq = fmaf(b, b, ssq);
+            }
+          }
+          st_vec<bf16, 16>(static_cast<bf16*>(p.out) + (int64_t)m * p.ldo + n, v);
+        }
+        ring.load(a, src(c + 2));
+      }
+    }
+    if (p.ssq_out != nullptr && m < g.M) p.ssq_out[((int64_t)(n0 / BN) * 2 + half) * p.ssq_ld + m] = ssq;
+    return true;
+  }
+  if (p.kind == EPI_QKV) {
+    // RoPE on Q and K columns at the row's position, then Q / K / V stores (K and V into the
+    // rows kv_row names, when given)
+    const int hhalf = p.hd >> 1;
+    const int n_lo = n0 + c_lo * 16, n_hi = min(n0 + c_hi * 16, g.N);   // this warp's columns
+    const bool rot = n_lo < n_hi && p.col0 + n_lo < p.q_cols + p.kv_cols;   // some chunk is rotated
+    const bool has_kv = n_lo < n_hi && p.col0 + n_hi > p.q_cols;              // some chunk is K or V
+    bool pos_ok = m < g.M, kv_ok = m < g.M;
+    int pos = 0;
+    int64_t kr = 0;
+    if (m < g.M && rot) {
+      pos = p.pos[m];
+      pos_ok = pos >= 0 && pos < p.max_pos;
+    }
+    if (m < g.M && has_kv) {
+      kr = p.kv_row ? (int64_t)p.kv_row[m] : (int64_t)m;
+      kv_ok = kr >= 0 && (p.kv_bound < 0 || kr < p.kv_bound);
+    }
+    if (m < g.M && (!pos_ok || !kv_ok)) atomicOr(&g_err_tc, ERRBIT_INDEX);
+    const float2* cs_row =
+        pos_ok && rot ? reinterpret_cast<const float2*>(p.rope) + (int64_t)pos * hhalf : nullptr;
+    const bool vec = cs_row != nullptr && ((reinterpret_cast<uintptr_t>(cs_row) & 15) == 0) && (hhalf % 2) == 0;
+    SideRing<4, 2> ring;
+    auto src = [&](int c) -> const uint4* {
+      const int n = n0 + c * 16, gc = p.col0 + n;
+      if (!vec || c >= c_hi || n >= g.N || gc >= p.q_cols + p.kv_cols) return nullptr;
+      const int seg = gc < p.q_cols ? gc : gc - p.q_cols;
+      return reinterpret_cast<const uint4*>(cs_row + ((seg % p.hd) >> 1));
+    };
+    ring.load(0, src(c_lo));
+    ring.load(1, src(c_lo + 1));
+    if (!wait_acc()) return false;
+    for (int c2 = c_lo; c2 < c_hi; c2 += 2) {   // in pairs: ring slot = chunk parity, as above
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        const int c = c2 + a;
+        if (c >= c_hi) break;
+        float v[16];
+        tc::tmem_ld16(trow + c * 16, v);
+        if (scaled) {
+#pragma unroll
+          for (int q = 0; q < 16; ++q) v[q] *= rs;
+        }
+        const int n = n0 + c * 16;
+        const int gc = p.col0 + n;
+        const bool rotated = gc < p.q_cols + p.kv_cols;
+        if (m < g.M && n < g.N && (!rotated || pos_ok) && (gc < p.q_cols || kv_ok)) {
+          if (rotated) {
+            const int seg = gc < p.q_cols ? gc : gc - p.q_cols;
+            const float2* cs = vec ? reinterpret_cast<const float2*>(ring.w[a]) : cs_row + ((seg % p.hd) >> 1);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float2 t = cs[q];
+              const float x0 = v[2 * q], x1 = v[2 * q + 1];
+              v[2 * q] = x0 * t.x - x1 * t.y;
+              v[2 * q + 1] = x0 * t.y + x1 * t.x;
+            }
+          }
+          if (gc < p.q_cols)
+            st_vec<bf16, 16>(static_cast<bf16*>(p.q) + (int64_t)m * p.ldq + gc, v);
+          else if (gc < p.q_cols + p.kv_cols)
+            st_vec<bf16, 16>(static_cast<bf16*>(p.k) + kr * p.ldkv + (gc - p.q_cols), v);
+          else
+            st_vec<bf16, 16>(static_cast<bf16*>(p.v) + kr * p.ldkv + (gc - p.q_cols - p.kv_cols), v);
+        }
+        ring.load(a, src(c + 2));
+      }
+    }
+    return true;
+  }
+  // plain store
+  if (!wait_acc()) return false;
+  for (int c = c_lo; c < c_hi; ++c) {
+    float v[16];
+    tc::tmem_ld16(trow + c * 16, v);
+    if (scaled) {
+#pragma unroll
+      for (int q = 0; q < 16; ++q) v[q] *= rs;
+    }
+    const int n = n0 + c * 16;
+    if (m < g.M && n < g.N) {
+      if (!epi_apply<bf16, 16>(p, m, n, v)) atomicOr(&g_err_tc, ERRBIT_INDEX);
+    }
+  }
+  return true;
 }
 
 template <int BN>
@@ -347,14 +469,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       const GemmDesc& g = pr ? g1 : g0;
       const int m = m0 + lane_base + lane;
       const float rs = row_scale(g, m);
+      const uint32_t trow = tmem + b * 256 + (static_cast<uint32_t>(lane_base) << 16);
       // every lane waits, then the warp re-converges before the .sync.aligned TMEM loads
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&acc_full[b], (i >> 1) & 1))) {
+      const bool done = epilogue_tile<BN>(g, m, n0, half, trow, swiglu, rs, [&] {
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(&acc_full[b], (i >> 1) & 1))) return false;
+        tc::tc_fence_after();
+        return true;
+      });
+      if (!done) {
         if (lane == 0) atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
         break;
       }
-      tc::tc_fence_after();
-      const uint32_t trow = tmem + b * 256 + (static_cast<uint32_t>(lane_base) << 16);
-      epilogue_tile<BN>(g, m, n0, half, trow, swiglu, rs);
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&acc_empty[b]);
@@ -536,13 +661,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       const GemmDesc& g = pr ? g1 : g0;
       const int m = m0 + (int)rank * BM + lane_base + lane;
       const float rs = row_scale(g, m);
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&acc_full[b], (i >> 1) & 1))) {
+      const uint32_t trow = tmem + b * 256 + (static_cast<uint32_t>(lane_base) << 16);
+      const bool done = epilogue_tile<BN>(g, m, n0, half, trow, swiglu, rs, [&] {
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(&acc_full[b], (i >> 1) & 1))) return false;
+        tc::tc_fence_after();
+        return true;
+      });
+      if (!done) {
         if (lane == 0) atomicOr(&g_err_tc, ERRBIT_TIMEOUT);
         break;
       }
-      tc::tc_fence_after();
-      const uint32_t trow = tmem + b * 256 + (static_cast<uint32_t>(lane_base) << 16);
-      epilogue_tile<BN>(g, m, n0, half, trow, swiglu, rs);
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_cluster(b ? release1 : release0);

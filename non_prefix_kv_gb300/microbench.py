@@ -42,7 +42,8 @@ def _time(fn, iters: int, warmup: int):
 
 def run(argv=None):
     p = argparse.ArgumentParser()
-    p.add_argument("what", choices=["gemm", "attention", "rope_shift", "rope_shift_q8", "deviation", "check_layer",
+    p.add_argument("what", choices=["gemm", "o_proj_ffn", "attention", "rope_shift", "rope_shift_q8", "deviation",
+                                    "check_layer",
                                     "rmsnorm", "gather", "lmhead"])
     p.add_argument("--m", type=int, default=4096)
     p.add_argument("--n", type=int, default=8192)
@@ -93,6 +94,39 @@ def run(argv=None):
             ms = _time(lambda: B.cb_o_proj_ffn(attn, x, a.m, dims, cw, y, ws), a.iters, a.warmup)
             fl = 2.0 * a.m * a.k * (128 + 3 * a.n)
         out.update(ms=ms, tflops=fl / (ms / 1e3) / 1e12, m=a.m, n=a.n, k=a.k, epi=a.epi, unit_gains=a.unit_gains)
+    elif a.what == "o_proj_ffn":
+        # the O-projection + residual and the SwiGLU FFN of --m rows, d = --k, --heads heads of 128,
+        # F = --n, unit norm gains (the FFN norm folded into the gate/up GEMM, as in the bf16 step);
+        # per-launch times from the library's launch profile
+        shape = ModelShape(1, a.k, a.heads, a.heads, 128, a.n, 64, dtype="bf16")
+        dims = E.make_dims(shape)
+        qc = a.heads * 128
+
+        def rnd(*sz, std=0.02):
+            return (torch.randn(*sz, device="cuda", generator=g) * std).to(bf)
+        lw = {"wqkv": rnd(3 * qc, a.k), "wo": rnd(a.k, qc), "w_gate_up": rnd(2 * a.n, a.k), "w_down": rnd(a.k, a.n)}
+        cw = B.cb_layer_w(0, lw["wqkv"].data_ptr(), lw["wo"].data_ptr(), 0, lw["w_gate_up"].data_ptr(),
+                          lw["w_down"].data_ptr())
+        attn = rnd(a.m, qc, std=1.0)
+        x = rnd(a.m, a.k, std=1.0)
+        y = torch.empty_like(x)
+        ws = torch.empty(B.cb_workspace_bytes(dims, a.m, a.m), dtype=torch.uint8, device="cuda")
+        call = lambda: B.cb_o_proj_ffn(attn, x, a.m, dims, cw, y, ws)   # noqa: E731
+        ms = _time(call, a.iters, a.warmup)
+        B.cb_profile_begin(64 * a.iters)
+        for _ in range(a.iters):
+            call()
+        torch.cuda.synchronize()
+        recs = B.cb_profile_end(64 * a.iters)
+        per = {}
+        for r in recs:
+            key = "%dx%dx%d" % (r["m"], r["n"], r["k"])
+            t = per.setdefault(key, [0, 0.0, r["flops"]])
+            t[0] += 1
+            t[1] += r["ms"]
+        launches = {k: {"us": 1e3 * v[1] / v[0], "tflops": v[2] / (v[1] / v[0] / 1e3) / 1e12} for k, v in per.items()}
+        fl = 2.0 * a.m * a.k * (qc + 3 * a.n)
+        out.update(ms=ms, tflops=fl / (ms / 1e3) / 1e12, m=a.m, d=a.k, heads=a.heads, f=a.n, launches=launches)
     elif a.what == "attention":
         shape = ModelShape(1, 256, a.heads, a.kv_heads, a.hd, 256, 64, dtype="bf16")
         dims = E.make_dims(shape)

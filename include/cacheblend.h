@@ -16,6 +16,11 @@
  *    the call path.  Scratch comes from a caller-provided device workspace whose size
  *    cb_workspace_bytes() returns.  Pointers named *_host are host memory; all others
  *    are device memory.  The library never frees caller memory.
+ *  - Alignment: device buffers start on a 16-byte boundary (cudaMalloc and the PyTorch
+ *    allocator return 256-byte aligned blocks); the kernels move rows in 16- and 32-byte
+ *    vectors.  A misaligned buffer is refused with CB_ERR_INVALID_ARG before any launch.
+ *    Exceptions: cb_gather_rows and cb_scatter_kv need 4 bytes, 8-bit codes 8 bytes, and
+ *    arrays of row indices, positions or scores 4 bytes.
  *  - Streams: every call takes a cudaStream_t (passed as void*, NULL = legacy default
  *    stream), enqueues its kernels on it and returns without synchronising, unless the
  *    description says otherwise.

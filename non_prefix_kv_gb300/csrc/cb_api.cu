@@ -9,6 +9,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <initializer_list>
 #include <vector>
 
 #include "../../include/cacheblend.h"
@@ -193,10 +194,22 @@ int check_readable(const void* p, const char* what) {
   return fail(CB_ERR_INVALID_ARG, "%s: host memory not mapped at the same device address", what);
 }
 
+// Device buffers that kernels read or write in 16-byte vectors (activation rows, KV caches,
+// weights, tables, workspaces) must start on a 16-byte boundary; every row width the library
+// accepts keeps later rows on one.  A misaligned base is refused here, before any launch,
+// rather than faulting on the GPU.  NULL entries (optional buffers) pass.
+int check_al16(std::initializer_list<const void*> ps, const char* what) {
+  for (const void* p : ps)
+    if (reinterpret_cast<uintptr_t>(p) & 15) return fail(CB_ERR_INVALID_ARG, "%s: buffer not 16-byte aligned", what);
+  return CB_OK;
+}
+
 // the norm gains may be NULL (unit gains); the matrices may not
 int check_w(const cb_layer_w* w) {
   if (!w || !w->wqkv || !w->wo || !w->w_gate_up || !w->w_down)
     return fail(CB_ERR_INVALID_ARG, "layer weight pointer is NULL");
+  if (int st = check_al16({w->attn_norm, w->wqkv, w->wo, w->ffn_norm, w->w_gate_up, w->w_down}, "layer weights"))
+    return st;
   return CB_OK;
 }
 
@@ -515,6 +528,7 @@ int cb_rope_shift(void* k_dst, void* v_dst, const void* k_src, const void* v_src
     return fail(CB_ERR_INVALID_ARG, "rope_shift pointer is NULL");
   if ((v_dst == nullptr) != (v_src == nullptr)) return fail(CB_ERR_INVALID_ARG, "v_dst/v_src must both be set or NULL");
   if (k_dst == k_src && src_row) return fail(CB_ERR_INVALID_ARG, "in-place shift needs src_row == NULL");
+  if ((st = check_al16({k_dst, v_dst, k_src, v_src, cos_sin}, "rope_shift"))) return st;
   if ((st = check_readable(k_src, "k_src")) || (st = check_readable(v_src, "v_src"))) return st;
   const int W = dims->n_kv_heads * dims->head_dim;
   L_ROPE_SHIFT(dims->dtype, k_dst, v_dst, k_src, v_src, src_row, n_src_rows, delta, n_rows, W, dims->head_dim, cos_sin,
@@ -528,6 +542,8 @@ int cb_kv_quantize(const void* x, int64_t n_rows, int32_t W, int32_t dtype, uint
   if (n_rows < 0 || W < 1) return fail(CB_ERR_SHAPE, "need n_rows >= 0, W >= 1");
   if (n_rows == 0) return CB_OK;
   if (!x || !codes || !scale || !zero) return fail(CB_ERR_INVALID_ARG, "kv_quantize pointer is NULL");
+  if (int st = check_al16({x, scale, zero}, "kv_quantize")) return st;
+  if (reinterpret_cast<uintptr_t>(codes) & 7) return fail(CB_ERR_INVALID_ARG, "kv_quantize: codes not 8-byte aligned");
   CB_LAUNCH(CB_PROF_QUANT, 0, n_rows, W, 0, 0.0, (double)n_rows * W * (2.0 * esize(dtype) + 1.0) + 8.0 * W,
             S(stream), launch_kv_quantize(dtype, x, n_rows, W, codes, scale, zero, S(stream)));
   return CB_OK;
@@ -549,6 +565,7 @@ int cb_rope_shift_q8(void* k_dst, void* v_dst, const uint8_t* k_codes, const uin
   const uintptr_t a = (uintptr_t)k_codes | (uintptr_t)v_codes;
   const uintptr_t b = (uintptr_t)k_scale | (uintptr_t)k_zero | (uintptr_t)v_scale | (uintptr_t)v_zero;
   if ((a & 7) || (b & 15)) return fail(CB_ERR_INVALID_ARG, "codes need 8-byte, scale/zero 16-byte alignment");
+  if ((st = check_al16({k_dst, v_dst, cos_sin}, "rope_shift_q8"))) return st;
   if ((st = check_readable(k_codes, "k_codes")) || (st = check_readable(v_codes, "v_codes"))) return st;
   const int W = dims->n_kv_heads * dims->head_dim;
   const double bytes = (double)n_rows * W * ((v_dst ? 2.0 : 1.0) * (1.0 + esize(dims->dtype))) + 4.0 * n_rows;
@@ -581,6 +598,7 @@ int cb_kv_deviation_topk(const void* k_new, const void* v_new, int64_t n_new_row
   if (n_cand == 0) return CB_OK;
   if (!k_new || !k_ref || (dev_mode == CB_DEV_KV && (!v_new || !v_ref)) || (k > 0 && !sel))
     return fail(CB_ERR_INVALID_ARG, "deviation pointer is NULL");
+  if ((st = check_al16({k_new, v_new, k_ref, v_ref, ws}, "kv_deviation_topk"))) return st;
   const size_t need = 256 + (size_t)n_cand * 8 + 512;
   if (!ws || ws_bytes < need) return fail(CB_ERR_WORKSPACE, "workspace %zu < %zu", ws_bytes, need);
   Carver c(ws);
@@ -611,6 +629,7 @@ int cb_kv_deviation_topk_noalloc(const void* k_new, const void* v_new, int64_t n
   if (n_cand == 0) return CB_OK;
   if (!k_new || !k_ref || (dev_mode == CB_DEV_KV && (!v_new || !v_ref)) || (k > 0 && !sel))
     return fail(CB_ERR_INVALID_ARG, "deviation pointer is NULL");
+  if ((st = check_al16({k_new, v_new, k_ref, v_ref}, "kv_deviation_topk_noalloc"))) return st;
   const int W = dims->n_kv_heads * dims->head_dim;
   CB_CUDA(launch_deviation_topk_noalloc(dims->dtype, k_new, v_new, k_ref, v_ref, new_row, ref_row, n_cand,
                                         n_new_rows, n_ref_rows, k, W, dev_mode == CB_DEV_KV, scores, sel,
@@ -624,6 +643,7 @@ int cb_topk_from_scores(const float* scores, const int32_t* cand, int32_t n_cand
   if (n_cand < 0 || k < 0 || k > n_cand) return fail(CB_ERR_SHAPE, "need 0 <= k <= n_cand");
   if (n_cand == 0) return CB_OK;
   if (!scores || (k > 0 && !sel)) return fail(CB_ERR_INVALID_ARG, "topk pointer is NULL");
+  if (int st = check_al16({scores, ws}, "topk_from_scores")) return st;
   const size_t need = 256 + (size_t)n_cand * 4;
   if (!ws || ws_bytes < need) return fail(CB_ERR_WORKSPACE, "workspace %zu < %zu", ws_bytes, need);
   Carver c(ws);
@@ -642,6 +662,7 @@ int cb_rmsnorm(void* out, const void* x, int64_t n_x_rows, const int32_t* rows, 
   if (n == 0) return CB_OK;
   if (!rows && n_x_rows < n) return fail(CB_ERR_SHAPE, "n_x_rows < n with rows NULL");
   if (!out || !x || !gain) return fail(CB_ERR_INVALID_ARG, "rmsnorm pointer is NULL");
+  if (int st = check_al16({out, x, gain}, "rmsnorm")) return st;
   L_RMSNORM_B(dtype_in, dtype_out, out, x, rows, n_x_rows, gain, n, d, eps, S(stream));
   return CB_OK;
 }
@@ -652,6 +673,9 @@ int cb_gather_rows(void* dst, const void* src, int64_t n_src_rows, const int32_t
   if (n == 0) return CB_OK;
   if (!idx && n_src_rows < n) return fail(CB_ERR_SHAPE, "n_src_rows < n with idx NULL");
   if (!dst || !src) return fail(CB_ERR_INVALID_ARG, "gather pointer is NULL");
+  // rows are copied in 16-byte words where both bases allow it, else in 4-byte words
+  if ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 3)
+    return fail(CB_ERR_INVALID_ARG, "gather: buffer not 4-byte aligned");
   L_COPY(dst, nullptr, src, idx, n, row_bytes, n, n_src_rows, S(stream));
   return CB_OK;
 }
@@ -666,6 +690,9 @@ int cb_scatter_kv(void* k_cache, void* v_cache, int64_t n_cache_rows, const void
   if (!src_idx && n_src_rows < n) return fail(CB_ERR_SHAPE, "n_src_rows < n with src_idx NULL");
   if (!k_cache || !k_rows || !dst_idx || ((v_cache == nullptr) != (v_rows == nullptr)))
     return fail(CB_ERR_INVALID_ARG, "scatter pointer is NULL");
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
+       reinterpret_cast<uintptr_t>(k_rows) | reinterpret_cast<uintptr_t>(v_rows)) & 3)
+    return fail(CB_ERR_INVALID_ARG, "scatter_kv: buffer not 4-byte aligned");
   const int64_t rb = (int64_t)dims->n_kv_heads * dims->head_dim * esize(dims->dtype);
   L_COPY(k_cache, dst_idx, k_rows, src_idx, n, rb, n_cache_rows, n_src_rows, S(stream));
   if (v_cache) L_COPY(v_cache, dst_idx, v_rows, src_idx, n, rb, n_cache_rows, n_src_rows, S(stream));
@@ -682,6 +709,7 @@ int cb_selective_qkv(const void* x, int64_t n_x_rows, const int32_t* rows, const
   if (!rows && n_x_rows < M) return fail(CB_ERR_SHAPE, "n_x_rows < M with rows NULL");
   if (!x || !pos || !cos_sin || (!q && !k) || ((k == nullptr) != (v == nullptr)))
     return fail(CB_ERR_INVALID_ARG, "selective_qkv pointer is NULL");
+  if ((st = check_al16({x, q, k, v, cos_sin, ws}, "selective_qkv"))) return st;
   LayerWs L;
   if ((st = need_ws(dims, M, M, ws, ws_bytes, &L))) return st;
   const int qc = dims->n_heads * dims->head_dim, W = dims->n_kv_heads * dims->head_dim;
@@ -700,6 +728,7 @@ int cb_partial_attention(const void* q, const int32_t* q_pos, int32_t M, const v
   if (M < 0 || n_kv < 1) return fail(CB_ERR_SHAPE, "M/n_kv");
   if (M == 0) return CB_OK;
   if (!q || !q_pos || !k_cache || !v_cache || !out) return fail(CB_ERR_INVALID_ARG, "attention pointer is NULL");
+  if ((st = check_al16({q, k_cache, v_cache, out, ws}, "partial_attention"))) return st;
   const size_t need = attention_ws_bytes(dims->dtype, M, dims->n_heads, dims->head_dim);
   if (need && (!ws || ws_bytes < need)) return fail(CB_ERR_WORKSPACE, "workspace %zu < %zu", ws_bytes, need);
   L_ATTN(dims->dtype, q, q_pos, M, k_cache, v_cache, n_kv, dims->n_heads, dims->n_kv_heads, dims->head_dim, out, ws, ws_bytes, S(stream));
@@ -713,6 +742,7 @@ int cb_o_proj_ffn(const void* attn, const void* x_res, int32_t M, const cb_dims*
   if (M < 0) return fail(CB_ERR_SHAPE, "M < 0");
   if (M == 0) return CB_OK;
   if (!attn || !x_res || !x_out) return fail(CB_ERR_INVALID_ARG, "o_proj_ffn pointer is NULL");
+  if ((st = check_al16({attn, x_res, x_out, ws}, "o_proj_ffn"))) return st;
   LayerWs L;
   if ((st = need_ws(dims, M, M, ws, ws_bytes, &L))) return st;
   return o_ffn(dims, w, attn, x_res, M, x_out, L, S(stream));
@@ -728,6 +758,7 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
   if (!x_in || !k_cache || !v_cache || !cos_sin || !x_out || !s_out || !m_out_host)
     return fail(CB_ERR_INVALID_ARG, "blend_layer pointer is NULL");
   if (x_out == x_in) return fail(CB_ERR_INVALID_ARG, "x_out must not alias x_in");
+  if ((st = check_al16({x_in, k_cache, v_cache, cos_sin, x_out, ws}, "blend_layer"))) return st;
   if (n_tok < 1 || n_tok > INT32_MAX || n_cached < 0 || n_cached > n_tok)
     return fail(CB_ERR_SHAPE, "need 0 <= n_cached <= n_tok, n_tok >= 1");
   if (n_tok > max_pos) return fail(CB_ERR_SHAPE, "rope table (%d) shorter than n_tok (%lld)", max_pos, (long long)n_tok);
@@ -974,6 +1005,7 @@ int cb_blend_steady_batch(const cb_dims* dims, const cb_layer_w* w, int32_t n_re
   if (!row0_host || !x_in || !s_in || !k_cache || !v_cache || !cos_sin || !x_out)
     return fail(CB_ERR_INVALID_ARG, "blend_steady_batch pointer is NULL");
   if (x_out == x_in) return fail(CB_ERR_INVALID_ARG, "x_out must not alias x_in");
+  if ((st = check_al16({x_in, k_cache, v_cache, cos_sin, x_out, ws}, "blend_steady_batch"))) return st;
   if (n_req < 1 || n_req > kMaxBatch) return fail(CB_ERR_SHAPE, "n_req %d outside [1, %d]", n_req, kMaxBatch);
   if (n_tok < 1 || n_tok > max_pos) return fail(CB_ERR_SHAPE, "need 1 <= n_tok <= max_pos");
   if ((int64_t)n_req * n_tok > INT32_MAX) return fail(CB_ERR_SHAPE, "n_req * n_tok exceeds the int32 row range");
@@ -1021,7 +1053,9 @@ int cb_full_prefill(const cb_dims* dims, int32_t n_layers, const cb_layer_w* lay
   for (int l = 0; l < n_layers; ++l) {
     if ((st = check_w(&layers_host[l]))) return st;
     if (!k_out_host[l] || !v_out_host[l]) return fail(CB_ERR_INVALID_ARG, "k_out/v_out[%d] is NULL", l);
+    if ((st = check_al16({k_out_host[l], v_out_host[l]}, "full_prefill k_out/v_out"))) return st;
   }
+  if ((st = check_al16({embed, h_last, x_all, cos_sin, ws}, "full_prefill"))) return st;
   if (n < 1 || pos0 < 0) return fail(CB_ERR_SHAPE, "n >= 1, pos0 >= 0");
   if ((int64_t)pos0 + n > max_pos) return fail(CB_ERR_SHAPE, "rope table shorter than pos0 + n");
   LayerWs L;
@@ -1054,6 +1088,7 @@ int cb_lmhead_argmax(const void* h, const void* final_norm, const void* w_lm, co
   int st = check_dims(dims);
   if (st) return st;
   if (!h || !final_norm || !w_lm || !token) return fail(CB_ERR_INVALID_ARG, "lmhead pointer is NULL");
+  if ((st = check_al16({h, final_norm, w_lm, logits, ws}, "lmhead_argmax"))) return st;
   const int nb = (int)lm_block_best_count(dims->vocab);
   const size_t need = 256 + (size_t)dims->d_model * 4 + 256 + (size_t)dims->vocab * 4 + 256 + (size_t)nb * 8 + 256;
   if (!ws || ws_bytes < need) return fail(CB_ERR_WORKSPACE, "workspace %zu < %zu", ws_bytes, need);
@@ -1074,6 +1109,7 @@ int cb_linear(const void* x, const void* w, void* y, int32_t M, int32_t N, int32
   if (M < 0 || N < 1 || K < 1) return fail(CB_ERR_SHAPE, "M/N/K");
   if (M == 0) return CB_OK;
   if (!x || !w || !y) return fail(CB_ERR_INVALID_ARG, "linear pointer is NULL");
+  if (int st = check_al16({x, w, y}, "linear")) return st;
   if (dtype == CB_BF16 && (N % 16 || K % 8)) return fail(CB_ERR_UNSUPPORTED, "bf16 needs N %% 16 == 0, K %% 8 == 0");
   if (dtype == CB_F32 && N % 4) return fail(CB_ERR_UNSUPPORTED, "fp32 needs N %% 4 == 0");
   GemmDesc g = make_gemm(M, N, K, x, K, w, K);

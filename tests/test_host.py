@@ -160,6 +160,35 @@ def test_entry_points_reject_bad_arguments_before_launch(lib):
     assert st == 8                    # bf16 N % 16
 
 
+def test_misaligned_buffers_are_refused_before_launch(lib):
+    """Device buffers the kernels move in 16-byte vectors must start on a 16-byte boundary:
+    a misaligned one is refused on the host (CB_ERR_INVALID_ARG, nothing launched) instead of
+    faulting on the GPU.  The row copies need only 4 bytes."""
+    d = _dims()
+    odd = FAKE + 8          # 8-byte aligned, not 16
+    st = lib.cb_rmsnorm(FAKE, odd, 4, None, 4, 64, FAKE, ctypes.c_float(1e-5), B.CB_BF16, B.CB_BF16, None)
+    assert st == 1 and b"16-byte" in lib.cb_last_error_message()
+    st = lib.cb_rope_shift(odd, None, FAKE, None, None, 10, FAKE, 10, ctypes.byref(d), FAKE, 100, None)
+    assert st == 1
+    st = lib.cb_linear(FAKE, odd, FAKE, 4, 32, 64, B.CB_BF16, None)
+    assert st == 1
+    w = B.cb_layer_w(None, FAKE, odd, None, FAKE, FAKE)
+    st = lib.cb_o_proj_ffn(FAKE, FAKE, 4, ctypes.byref(d), ctypes.byref(w), FAKE + 64, FAKE, 1 << 30, None)
+    assert st == 1 and b"layer weights" in lib.cb_last_error_message()
+    w = B.cb_layer_w(None, FAKE, FAKE, None, FAKE, FAKE)
+    st = lib.cb_o_proj_ffn(FAKE, odd, 4, ctypes.byref(d), ctypes.byref(w), FAKE + 64, FAKE, 1 << 30, None)
+    assert st == 1 and b"o_proj_ffn" in lib.cb_last_error_message()
+    st = lib.cb_partial_attention(odd, FAKE, 4, FAKE, FAKE, 16, ctypes.byref(d), FAKE, None, 0, None)
+    assert st == 1
+    st = lib.cb_gather_rows(FAKE, FAKE + 2, 3, None, 3, 8, None)
+    assert st == 1 and b"4-byte" in lib.cb_last_error_message()
+    m_out = ctypes.c_int32(-1)
+    st = lib.cb_blend_layer(ctypes.byref(d), ctypes.byref(w), B.CB_LAYER_PRECHECK, odd, None, 416, 416, 384, FAKE,
+                            FAKE, FAKE, 416, 0, 0, None, FAKE + 64, FAKE, ctypes.byref(m_out), None, None, FAKE,
+                            1 << 40, None)
+    assert st == 1 and m_out.value == -1
+
+
 def test_shutdown_releases_state_and_the_library_stays_usable(lib):
     """cb_shutdown empties the per-device caches; every later call rebuilds what it needs."""
     d = _dims()

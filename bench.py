@@ -1040,7 +1040,7 @@ def our_arm(args):
                                             peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         # the same request captured once as a CUDA graph and replayed (engine.RequestGraph)
         rg = E.RequestGraph(r0, plan, host_pool=hp, stream=stream, precheck_load_rows=split_rows)
-        # every variant runs once per round, in turn, so that all of them see the same clocks
+        # every variant runs once per pass of the loop, in turn, so that all of them see the same clocks
         # (under the power cap a long run drifts); the eager split runs last of the eager ones
         modes = ("serial", "overlap", "full_load", "split", "graph")
         times = {m: [] for m in modes}

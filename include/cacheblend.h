@@ -110,6 +110,11 @@ const char* cb_status_string(int status);
 /* Detail of the last error raised on the calling thread (static, thread-local). */
 const char* cb_last_error_message(void);
 
+/* The last failing CUDA runtime call on the calling thread (the one behind the latest
+ * CB_ERR_CUDA): error name, text and the call; "" if there has been none.  Static,
+ * thread-local. */
+const char* cb_last_cuda_error(void);
+
 /* Waits for `stream` (polling, up to timeout_s seconds; <= 0 means no limit), then reads
  * and clears the sticky device error word.  Returns CB_OK, CB_ERR_TIMEOUT (nothing was
  * cancelled; the work is still queued), CB_ERR_NONFINITE, CB_ERR_DEVICE or CB_ERR_CUDA.

@@ -59,6 +59,7 @@ _SZ = C.c_size_t
 _PROTOS = {
     "cb_status_string": (C.c_char_p, [C.c_int]),
     "cb_last_error_message": (C.c_char_p, []),
+    "cb_last_cuda_error": (C.c_char_p, []),
     "cb_sync": (C.c_int, [_P, C.c_double]),
     "cb_workspace_bytes": (C.c_int, [C.POINTER(cb_dims), _I64, _I64, C.POINTER(_SZ)]),
     "cb_hkvd_budget": (_I64, [_I64, C.c_double, _I64]),
@@ -145,6 +146,11 @@ def _check(fn: str, st: int):
 
 def _nbytes(t) -> int:
     return 0 if t is None else t.numel() * t.element_size()
+
+
+def cb_last_cuda_error() -> str:
+    """The last failing CUDA runtime call on this thread ("" if none)."""
+    return lib().cb_last_cuda_error().decode(errors="replace")
 
 
 # ---- host helpers -------------------------------------------------------------------------

@@ -25,6 +25,12 @@ using namespace cb;
 namespace {
 
 thread_local char g_msg[512] = "";
+thread_local char g_cuda_msg[256] = "";   // the last failing CUDA call on this thread
+
+// records a failing CUDA call for cb_last_cuda_error
+void note_cuda(cudaError_t e, const char* what) {
+  snprintf(g_cuda_msg, sizeof(g_cuda_msg), "%s (%s): %s", cudaGetErrorName(e), cudaGetErrorString(e), what);
+}
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -37,8 +43,10 @@ int fail(int code, const char* fmt, ...) {
 #define CB_CUDA(expr)                                                                    \
   do {                                                                                   \
     cudaError_t e__ = (expr);                                                            \
-    if (e__ != cudaSuccess)                                                              \
+    if (e__ != cudaSuccess) {                                                            \
+      note_cuda(e__, #expr);                                                             \
       return fail(CB_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e__));         \
+    }                                                                                    \
   } while (0)
 
 inline cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
@@ -455,12 +463,17 @@ const char* cb_status_string(int status) {
 
 const char* cb_last_error_message(void) { return g_msg; }
 
+const char* cb_last_cuda_error(void) { return g_cuda_msg; }
+
 int cb_sync(void* stream, double timeout_s) {
   const double t0 = now_s();
   for (;;) {
     cudaError_t e = cudaStreamQuery(S(stream));
     if (e == cudaSuccess) break;
-    if (e != cudaErrorNotReady) return fail(CB_ERR_CUDA, "stream error: %s", cudaGetErrorString(e));
+    if (e != cudaErrorNotReady) {
+      note_cuda(e, "cudaStreamQuery");
+      return fail(CB_ERR_CUDA, "stream error: %s", cudaGetErrorString(e));
+    }
     if (timeout_s > 0 && now_s() - t0 > timeout_s)
       return fail(CB_ERR_TIMEOUT, "stream not idle after %.3f s", timeout_s);
     timespec ts{0, 50000};

@@ -160,6 +160,19 @@ def test_entry_points_reject_bad_arguments_before_launch(lib):
     assert st == 8                    # bf16 N % 16
 
 
+def test_cuda_failures_are_reported_with_the_failing_call(lib):
+    """A failing CUDA runtime call comes back as CB_ERR_CUDA, and cb_last_cuda_error names
+    the error and the call.  Without a GPU, cb_sync's stream query is such a call."""
+    import torch
+    st = lib.cb_sync(None, ctypes.c_double(1.0))
+    if torch.cuda.is_available():
+        assert st == 0
+    else:
+        assert st == 6
+        msg = B.cb_last_cuda_error()
+        assert "cudaStreamQuery" in msg and "cuda" in msg.lower()
+
+
 def test_misaligned_buffers_are_refused_before_launch(lib):
     """Device buffers the kernels move in 16-byte vectors must start on a 16-byte boundary:
     a misaligned one is refused on the host (CB_ERR_INVALID_ARG, nothing launched) instead of

@@ -508,11 +508,13 @@ def file_store_e2e(E, B, wl, r0, plan, stream, host_tok, hp, args, t_prefill_lay
                                 "r_min": wl.ratio, "r_star": r_star, "controlled": ctl}}
 
 
-def int8_store_e2e(E, B, eng, dm, pool, r0, plan, stream, host_tok, args):
+def int8_store_e2e(E, B, eng, dm, pool, r0, plan, stream, host_tok, args, split_rule=None):
     """The same request with the chunk store kept as 8-bit per-channel codes (CacheGen's
     per-channel quantization): half the bytes cross the host link and the decode is fused
-    into the re-positioning pass.  Reported beside the bf16 store: end-to-end TTFT, the
-    device-resident step, and how far the result moves (first token, last hidden row)."""
+    into the re-positioning pass.  Reported beside the bf16 store: end-to-end TTFT (eager with
+    every row loaded; and, like the bf16 headline, the captured request with the pre-check
+    layer's split, split_rule(store_esz) giving X), the device-resident step, and how far the
+    result moves (first token, last hidden row)."""
     import torch
     pool8 = E.ChunkPoolQ8.from_pool(pool, dm.dims)
     r8 = E.Request(eng, pool8, r0.order, r0.tokens_host)
@@ -534,6 +536,20 @@ def int8_store_e2e(E, B, eng, dm, pool, r0, plan, stream, host_tok, args):
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     ttft = statistics.median(times)
+    graph_split = None
+    if split_rule is not None:
+        split8 = split_rule(1)
+        rg8 = E.RequestGraph(r8, plan, host_pool=hp8, stream=stream, precheck_load_rows=split8)
+        gt, gtok = [], None
+        for i in range(args.warmup + args.steps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            gtok = rg8.run(r8.tokens_host)
+            if i >= args.warmup:
+                gt.append(time.perf_counter() - t0)
+        del rg8
+        graph_split = {"ttft_ms": statistics.median(gt) * 1e3, "precheck_load_rows": split8, "first_token": gtok,
+                       "api": "engine.RequestGraph(req, plan, host_pool=<8-bit store>, precheck_load_rows=X).run"}
     # device-resident 8-bit store, graph replay
     g8 = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g8, stream=stream):
@@ -554,7 +570,7 @@ def int8_store_e2e(E, B, eng, dm, pool, r0, plan, stream, host_tok, args):
     h0 = r0.x_last[m0 - 1].float()
     k8 = r8.K[0][:r8.n_cached].float()
     k0 = r0.K[0][:r0.n_cached].float()
-    return {"ttft_ms": ttft * 1e3, "tokens_per_s": r0.N / ttft,
+    return {"ttft_ms": ttft * 1e3, "tokens_per_s": r0.N / ttft, "graph_split": graph_split,
             "h2d_bytes_per_step": int(hp8.nbytes + host_tok.numel() * 4),
             "step_ms_device_resident": ev0.elapsed_time(ev1) / 10,
             "first_token": int(out8.item()), "same_first_token": int(out8.item()) == int(r0.token.item()),
@@ -1080,7 +1096,11 @@ def our_arm(args):
                "eager_ttft_ms_without_overlap": res["serial"] * 1e3,
                "h2d_gbs_serial": h2d / max(res["serial"] - ms / 1e3 / len(reqs), 1e-6) / 1e9}
         if shape.dtype == "bf16":
-            e2e["int8_store"] = int8_store_e2e(E, B, eng, dm, pool, r0, plan, stream, host_tok, args)
+            e2e["int8_store"] = int8_store_e2e(
+                E, B, eng, dm, pool, r0, plan, stream, host_tok, args,
+                split_rule=lambda store_esz: E.precheck_split_rows(
+                    shape, r0.N, r0.n_cached, link_gbs, max(all_gemm_tflops, 1.0),
+                    peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]), store_esz=store_esz))
         e2e["file_store"] = file_store_e2e(E, B, wl, r0, plan, stream, host_tok, hp, args,
                                            full_ms / shape.n_layers, e2e["h2d_gbs_serial"])
     B.cb_sync(stream, 120.0)

@@ -304,20 +304,23 @@ def contiguous_ranges(rows) -> list:
 
 
 def precheck_split_rows(shape: ModelShape, n_tok: int, n_cached: int, link_gbs: float, gemm_tflops: float,
-                        hbm_gbs: float) -> int:
+                        hbm_gbs: float, store_esz: Optional[int] = None) -> int:
     """How many cached rows of the pre-check layer to load (the rest have their K/V
     recomputed): the load controller's balance ([CB-A] §Pipelining and load controller)
     applied at that layer, where recomputing is exact up to rounding (R5).  Loading X rows
     over the host link and re-positioning them should take as long as the work queued ahead
     of the layer's attention: RMSNorm and Q for every row, K/V for the other N - X rows.
-    Both sides are linear in X; the result is where they meet, rounded down to 64 rows."""
+    Both sides are linear in X; the result is where they meet, rounded down to 64 rows.
+    store_esz: bytes per stored K/V element on the host (default: the compute dtype's; 1 for
+    an 8-bit store, whose decode is part of the re-positioning pass)."""
     s = shape
     esz = 2 if s.dtype == "bf16" else 4
+    sesz = esz if store_esz is None else store_esz
     N, d, qc, W = n_tok, s.d_model, s.q_width, s.kv_width
     R, L, H = gemm_tflops * 1e12, link_gbs * 1e9, hbm_gbs * 1e9
     t_q = 2.0 * N * d * qc / R + 2.0 * N * d * esz / H
     c = 2.0 * d * 2 * W / R
-    l = 2.0 * W * esz / L + 4.0 * W * esz / H
+    l = 2.0 * W * sesz / L + 2.0 * W * (sesz + esz) / H
     x = int((t_q + N * c) / (c + l)) // 64 * 64
     return max(1, min(n_cached, x))
 
@@ -369,13 +372,15 @@ class HostPool:
 
     def copy_layer(self, l: int, ranges=None):
         """Queue layer l's copy on the side stream: the whole layer, or only the given
-        (first pool row, rows) ranges of its K and V (bf16/fp32 pools)."""
-        if ranges is not None and not isinstance(self.pool, ChunkPool):
-            raise ValueError("partial layer loads need a bf16/fp32 chunk pool")
-        for h, d in zip(self.host[l], self.dev[l]):
-            if ranges is None:
+        (first pool row, rows) ranges of its K and V rows (bf16/fp32 values, or 8-bit codes;
+        an 8-bit pool's per-chunk scale/zero tables are copied whole)."""
+        n_rows = self.dev[l][0].shape[0]
+        for i, (h, d) in enumerate(zip(self.host[l], self.dev[l])):
+            row_indexed = i < 2   # K and V rows (values or codes); the rest are per-chunk tables
+            if ranges is None or not row_indexed:
                 B.cb_prefetch_layer(d, h, h.numel() * h.element_size(), self.side, self.done[l])
             else:
+                assert h.shape[0] == n_rows
                 rb = h.shape[1] * h.element_size()
                 for r0, n in ranges:
                     B.cb_prefetch_layer(d[r0:r0 + n], h[r0:r0 + n], n * rb, self.side, self.done[l])

@@ -266,9 +266,11 @@ def test_blend_bf16_gqa(E):
 
 @pytest.mark.parametrize("q8,from_file,recompute", [(False, False, False), (True, False, False), (False, True, False),
                                                      (True, True, False), (False, False, True), (False, True, True),
-                                                     (False, False, 160), (False, True, 200)],
+                                                     (False, False, 160), (False, True, 200), (True, False, 160),
+                                                     (True, True, 200)],
                          ids=["bf16_pool", "8bit_pool", "bf16_file", "8bit_file", "bf16_pool_recompute",
-                              "bf16_file_recompute", "bf16_pool_split", "bf16_file_split"])
+                              "bf16_file_recompute", "bf16_pool_split", "bf16_file_split", "8bit_pool_split",
+                              "8bit_file_split"])
 def test_layer_ahead_loading_matches_resident_pool(E, q8, from_file, recompute, tmp_path):
     """Loading every layer's chunk KV (bf16, or 8-bit codes with their tables) from pinned
     host memory on a side stream, one event per layer, or from a file read layer by layer

@@ -279,6 +279,14 @@ def test_precheck_split_balances_load_and_recompute():
     assert E.precheck_split_rows(shape, N, nc, 400.0, 1800.0, 6800.0) > x
     assert E.precheck_split_rows(shape, N, nc, 200.0, 3600.0, 6800.0) < x
     assert E.precheck_split_rows(shape, N, nc, 1e6, 1800.0, 6800.0) == nc
+    # an 8-bit store moves one byte per element over the link and its decode reads the codes
+    # and writes bf16: a row costs less to load, so more rows are loaded
+    x8 = E.precheck_split_rows(shape, N, nc, 200.0, 1800.0, 6800.0, store_esz=1)
+    R, L, H = 1800.0e12, 200.0e9, 6800.0e9
+    comp8 = lambda x: 2.0 * N * d * qc / R + 2.0 * N * d * 2 / H + (N - x) * 2.0 * d * 2 * W / R  # noqa: E731
+    load8 = lambda x: x * (2.0 * W * 1 / L + 2.0 * W * (1 + 2) / H)  # noqa: E731
+    assert x8 > x and x8 % 64 == 0
+    assert load8(x8) <= comp8(x8) and (x8 == nc or load8(x8 + 64) > comp8(x8 + 64))
 
 
 def test_contiguous_pool_ranges():

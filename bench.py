@@ -347,25 +347,27 @@ def reference_arm(args):
             times.append(dt * full / fl)
             sample_s.append(dt)
     # each step times a bounded sample (a quarter of the steady layer's selected rows at the
-    # full shape) so that the run ends within minutes; the step time is scaled from it by the
-    # algorithmic FLOP ratio, so ms_per_step x steps exceeds the time the arm ran
+    # full shape) so that the run ends within minutes: ms_per_step is that measured step, and
+    # the workload's throughput (value) is the sample's scaled to one whole step by the
+    # algorithmic FLOP ratio, stated as extrapolated beside it
     t_step = statistics.median(times)
+    t_sample = statistics.median(sample_s)
     value = wl.n_tokens * wl.n_requests / t_step
     cores = cpu_threads()
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_sample * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl.name, "n_tokens": wl.n_tokens, "chunks": f"{len(wl.order)}x{wl.chunk_len}",
                        "n_query": wl.n_query, "ratio": wl.ratio, "layers": wl.shape.n_layers},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc,
                              "extrapolated": True},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-            "ttft_ms": t_step * 1e3, "extrapolated": True,
-            "measured_sample_s_per_step": statistics.median(sample_s),
-            "note": "extrapolated: every step times the sample above and scales it to one whole step by the "
-                    "algorithmic FLOP ratio (ms_per_step is that estimate, not a measured time; the time "
-                    "actually spent per step is measured_sample_s_per_step).  A whole step measured once is "
-                    "in the default run's cpu_baseline"}
+            "extrapolated": True,
+            "ms_per_full_step_extrapolated": t_step * 1e3, "ttft_ms_extrapolated": t_step * 1e3,
+            "note": "each step runs and times the bounded sample above (ms_per_step, measured); value is the "
+                    "workload's throughput extrapolated from it to one whole step by the algorithmic FLOP "
+                    "ratio (ms_per_full_step_extrapolated, not a measured time).  One whole step is measured "
+                    "once by bench.py --cpu-full-step (cpu_baseline.full_step_measured)"}
     print(json.dumps(line), flush=True)
     return 0
 

@@ -1050,10 +1050,18 @@ def our_arm(args):
             out = fn()
             return time.perf_counter() - t0, out
 
-        # host-link rate from a few serial runs (their copies alone), GEMM rate from the step
-        n_cal = max(args.warmup, 2)
-        cal = [timed(lambda: e2e_step("serial"))[0] for _ in range(n_cal + 3)][n_cal:]
-        link_gbs = hp.nbytes / max(statistics.median(cal) - ms / 1e3 / len(reqs), 1e-6) / 1e9
+        # host-link rate measured directly (one layer's chunk KV copied from pinned memory on
+        # the loading stream, CUDA events), GEMM rate from the step
+        lay_bytes = sum(t.numel() * t.element_size() for t in hp.host[0])
+        lt = []
+        for _ in range(6):
+            a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_ev.record(hp.side)
+            hp.copy_layer(0)
+            b_ev.record(hp.side)
+            hp.side.synchronize()
+            lt.append(a_ev.elapsed_time(b_ev) / 1e3)
+        link_gbs = lay_bytes / statistics.median(lt[1:]) / 1e9
         split_rows = E.precheck_split_rows(shape, r0.N, r0.n_cached, link_gbs, max(all_gemm_tflops, 1.0),
                                             peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         # the same request captured once as a CUDA graph and replayed (engine.RequestGraph)
@@ -1096,7 +1104,8 @@ def our_arm(args):
                "eager_ttft_ms_precheck_kv_recomputed": res["overlap"] * 1e3,
                "h2d_bytes_precheck_kv_recomputed": int(h2d_skip),
                "eager_ttft_ms_without_overlap": res["serial"] * 1e3,
-               "h2d_gbs_serial": h2d / max(res["serial"] - ms / 1e3 / len(reqs), 1e-6) / 1e9}
+               "h2d_gbs_serial": h2d / max(res["serial"] - ms / 1e3 / len(reqs), 1e-6) / 1e9,
+               "h2d_gbs_link": link_gbs}
         if shape.dtype == "bf16":
             e2e["int8_store"] = int8_store_e2e(
                 E, B, eng, dm, pool, r0, plan, stream, host_tok, args,
@@ -1111,7 +1120,7 @@ def our_arm(args):
     deep = None
     if world == 1 and not args.no_deep_stack:
         deep = deep_stack_block(args, E, B, torch, local, peaks,
-                                e2e.get("h2d_gbs_serial") if e2e else None)
+                                e2e.get("h2d_gbs_link") if e2e else None)
         torch.cuda.empty_cache()
 
     # ---------------- CPU oracle baseline (rank 0, N = 1 only)

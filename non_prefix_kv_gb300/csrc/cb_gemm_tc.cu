@@ -1,13 +1,18 @@
 // bf16 GEMM on the 5th-generation tensor cores: TMA-fed shared-memory pipeline, tcgen05.mma
-// into a TMEM accumulator, fused epilogues (RoPE + KV scatter, residual add, SwiGLU).
+// into a TMEM accumulator, fused epilogues (RoPE + KV scatter, residual add, SwiGLU, the
+// check layer's KV deviation, and the RMSNorm row scale / row sums of squares of the folded
+// norms).
 //
 //   acc[m][n] = sum_k A[m][k] * B[n][k]      A: activations [M, K], B: weight rows [N, K]
 //
-// Persistent: one CTA per SM walks 128 x 256 output tiles (SwiGLU: 128 gate + 128 up
-// columns -> 128 outputs), K consumed in 64-element (128-byte) slabs through a 4-stage
-// ring; two TMEM accumulators let the epilogue of one tile overlap the next tile's MMAs.
+// Persistent: one CTA per SM walks 128 x BN output tiles (BN 256, 224, 208 or 192 chosen per
+// launch; SwiGLU: BN/2 gate + BN/2 up columns -> BN/2 outputs), K consumed in 64-element
+// (128-byte) slabs through a 4- or 5-stage ring; two TMEM accumulators let the epilogue of one
+// tile overlap the next tile's MMAs.  The CTA-pair variant below computes 256 x BN tiles on two
+// SMs with tcgen05.mma.cta_group::2.
 // Warp roles:
-//   warp 0 lane 0 : TMA producer     warp 1 : TMEM allocator, lane 0 issues the MMAs
+//   warp 0 lane 0 : TMA producer     warp 1 : TMEM allocator; the whole warp runs the MMA
+//                                             issue loop, its elected lane issues
 //   warps 2..9    : epilogue; warp w reads the 32 TMEM lanes (rows) of quadrant w % 4 and
 //                   one half of the accumulator columns, so two warps share each row band.
 #include <cuda.h>

@@ -322,3 +322,27 @@ def test_token_ids_are_checked_on_the_host():
     for bad in ([0, 1024], [-1, 3], [[1, 2]]):
         with pytest.raises(ValueError):
             E.check_token_ids(bad, 1024)
+
+
+def test_reference_arm_prints_the_contract_line():
+    """bench.py --impl reference runs the oracle on the host cores and prints one JSON line
+    with the contract's keys: ms_per_step is the measured step (the bounded sample), and the
+    workload's throughput extrapolated from it is labelled as such."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["higher_is_better"] is True
+    assert line["extrapolated"] is True and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    # the measured step is the sample; the whole step's time is an estimate several times longer
+    assert 0 < line["ms_per_step"] < line["ms_per_full_step_extrapolated"]
+    assert abs(line["value"] - 4096 / (line["ms_per_full_step_extrapolated"] / 1e3)) < 1e-6 * line["value"]

@@ -478,7 +478,11 @@ typedef struct {
     int64_t m, n, k;   /* launch sizes (GEMM: M, N, K; attention: queries, keys, heads) */
     double  flops;     /* algorithmic floating-point operations (0 if not known on host) */
     double  bytes;     /* algorithmic HBM bytes (compulsory reads + writes)             */
-    float   ms;        /* device time between events recorded around the launch        */
+    float   ms;        /* device time between events recorded around the launch (-1 in
+                        * span mode)                                                    */
+    float   span_ms;   /* span mode: from the first CTA past its wait on the preceding
+                        * launch to the last CTA's end, from the GPU's global timer; -1
+                        * for kernels that do not record spans, and in event mode         */
 } cb_prof_record;
 
 /* Number of kernels this library has launched in the process (host-side count). */
@@ -488,8 +492,17 @@ int64_t cb_kernel_launch_count(void);
  * thread, up to max_records launches.  Not for use while a stream is being captured. */
 int cb_profile_begin(int32_t max_records);
 
-/* Stops recording, waits for the recorded events, writes up to max_records records
- * (host memory) and their count. */
+/* Starts span profiling for the calling thread, up to max_records launches (at most 8192):
+ * no events are recorded between launches, so programmatic dependent launch overlaps them as
+ * in an unprofiled run.  Instead each tensor-core GEMM and attention kernel records in its
+ * launch's slot of a library-owned device buffer the global-timer time at which its first CTA
+ * passed the wait on the preceding launch and the time at which its last CTA finished.  The
+ * result is that launch's execution window inside the launch chain.  Synchronises the device.
+ * Not for use while a stream is being captured. */
+int cb_profile_begin_spans(int32_t max_records);
+
+/* Stops recording (either mode), waits for the recorded events (event mode) or for the
+ * device (span mode), writes up to max_records records (host memory) and their count. */
 int cb_profile_end(cb_prof_record* out_host, int32_t max_records, int32_t* n_out_host);
 
 /* Plain projection y = x W^T on the same GEMM kernels the layer calls use (tcgen05/TMEM

@@ -46,7 +46,7 @@ class cb_layer_w(C.Structure):
 
 class cb_prof_record(C.Structure):
     _fields_ = [("kind", C.c_int32), ("aux", C.c_int32), ("m", C.c_int64), ("n", C.c_int64), ("k", C.c_int64),
-                ("flops", C.c_double), ("bytes", C.c_double), ("ms", C.c_float)]
+                ("flops", C.c_double), ("bytes", C.c_double), ("ms", C.c_float), ("span_ms", C.c_float)]
 
 
 PROF_KINDS = {0: "rope_shift", 1: "copy_rows", 2: "rmsnorm", 3: "gemm", 4: "attention", 5: "deviation",
@@ -100,6 +100,7 @@ _PROTOS = {
     "cb_stream_wait": (C.c_int, [_P, _P]),
     "cb_kernel_launch_count": (_I64, []),
     "cb_profile_begin": (C.c_int, [_I32]),
+    "cb_profile_begin_spans": (C.c_int, [_I32]),
     "cb_profile_end": (C.c_int, [C.POINTER(cb_prof_record), _I32, C.POINTER(_I32)]),
 }
 
@@ -371,13 +372,17 @@ def cb_profile_begin(max_records: int = 4096):
     _check("cb_profile_begin", lib().cb_profile_begin(max_records))
 
 
+def cb_profile_begin_spans(max_records: int = 4096):
+    _check("cb_profile_begin_spans", lib().cb_profile_begin_spans(max_records))
+
+
 def cb_profile_end(max_records: int = 4096):
-    """Returns a list of dicts {kind, aux, m, n, k, flops, bytes, ms}, one per launch."""
+    """Returns a list of dicts {kind, aux, m, n, k, flops, bytes, ms, span_ms}, one per launch."""
     arr = (cb_prof_record * max_records)()
     n = _I32(0)
     _check("cb_profile_end", lib().cb_profile_end(arr, max_records, C.byref(n)))
     return [{"kind": PROF_KINDS.get(r.kind, str(r.kind)), "aux": r.aux, "m": r.m, "n": r.n, "k": r.k,
-             "flops": r.flops, "bytes": r.bytes, "ms": r.ms} for r in arr[:n.value]]
+             "flops": r.flops, "bytes": r.bytes, "ms": r.ms, "span_ms": r.span_ms} for r in arr[:n.value]]
 
 
 def _event(ev) -> int:

@@ -56,11 +56,18 @@ std::atomic<long long> g_launches{0};
 
 struct ProfState {
   bool on = false;
+  bool spans = false;                 // span mode: kernel-side timestamps instead of events
   int cap = 0;
   std::vector<cudaEvent_t> ev;        // 2 per record, created once and reused
   std::vector<cb_prof_record> rec;
+  unsigned long long* span_base = nullptr;
 };
 thread_local ProfState g_prof;
+
+// span slots: two words per record (earliest start, latest end; %globaltimer ns)
+constexpr int kSpanMax = 8192;
+__device__ unsigned long long g_span_buf[2 * kSpanMax];
+thread_local unsigned long long* g_cur_span = nullptr;
 
 struct ProfScope {
   int idx = -1;
@@ -81,10 +88,17 @@ struct ProfScope {
     r.flops = flops;
     r.bytes = bytes;
     P.rec.push_back(r);
-    cudaEventRecord(P.ev[2 * idx], s);
+    if (P.spans)
+      g_cur_span = P.span_base + 2 * idx;
+    else
+      cudaEventRecord(P.ev[2 * idx], s);
   }
   ~ProfScope() {
-    if (idx >= 0) cudaEventRecord(g_prof.ev[2 * idx + 1], s);
+    if (idx < 0) return;
+    if (g_prof.spans)
+      g_cur_span = nullptr;
+    else
+      cudaEventRecord(g_prof.ev[2 * idx + 1], s);
   }
 };
 
@@ -441,6 +455,10 @@ double now_s() {
 }
 
 }  // namespace
+
+namespace cb {
+unsigned long long* prof_span_slot() { return g_cur_span; }
+}  // namespace cb
 
 extern "C" {
 
@@ -1170,7 +1188,9 @@ void cb_shutdown(void) {
   P.ev.clear();
   P.rec.clear();
   P.on = false;
+  P.spans = false;
   P.cap = 0;
+  g_cur_span = nullptr;
 }
 
 int cb_profile_begin(int32_t max_records) {
@@ -1188,16 +1208,51 @@ int cb_profile_begin(int32_t max_records) {
   return CB_OK;
 }
 
+int cb_profile_begin_spans(int32_t max_records) {
+  if (max_records < 1 || max_records > kSpanMax) return fail(CB_ERR_INVALID_ARG, "max_records outside 1..%d", kSpanMax);
+  ProfState& P = g_prof;
+  void* addr = nullptr;
+  CB_CUDA(cudaGetSymbolAddress(&addr, g_span_buf));
+  std::vector<unsigned long long> init(2 * (size_t)max_records, 0ull);
+  for (int i = 0; i < max_records; ++i) init[2 * i] = ~0ull;
+  CB_CUDA(cudaDeviceSynchronize());
+  CB_CUDA(cudaMemcpy(addr, init.data(), init.size() * sizeof(unsigned long long), cudaMemcpyHostToDevice));
+  P.span_base = static_cast<unsigned long long*>(addr);
+  P.rec.clear();
+  P.rec.reserve(max_records);
+  P.cap = max_records;
+  P.spans = true;
+  P.on = true;
+  return CB_OK;
+}
+
 int cb_profile_end(cb_prof_record* out_host, int32_t max_records, int32_t* n_out_host) {
   ProfState& P = g_prof;
   P.on = false;
+  const bool spans = P.spans;
+  P.spans = false;
+  g_cur_span = nullptr;
   if (!n_out_host) return fail(CB_ERR_INVALID_ARG, "n_out_host is NULL");
   const int n = std::min<int>((int)P.rec.size(), std::max(0, max_records));
-  for (int i = 0; i < (int)P.rec.size(); ++i) {
-    CB_CUDA(cudaEventSynchronize(P.ev[2 * i + 1]));
-    float ms = 0.f;
-    CB_CUDA(cudaEventElapsedTime(&ms, P.ev[2 * i], P.ev[2 * i + 1]));
-    P.rec[i].ms = ms;
+  if (spans) {
+    std::vector<unsigned long long> t(2 * P.rec.size() + 2, 0ull);
+    CB_CUDA(cudaDeviceSynchronize());
+    if (!P.rec.empty())
+      CB_CUDA(cudaMemcpy(t.data(), P.span_base, 2 * P.rec.size() * sizeof(unsigned long long),
+                         cudaMemcpyDeviceToHost));
+    for (int i = 0; i < (int)P.rec.size(); ++i) {
+      const unsigned long long a = t[2 * i], b = t[2 * i + 1];
+      P.rec[i].ms = -1.f;
+      P.rec[i].span_ms = (a != ~0ull && b >= a) ? (float)((double)(b - a) * 1e-6) : -1.f;
+    }
+  } else {
+    for (int i = 0; i < (int)P.rec.size(); ++i) {
+      CB_CUDA(cudaEventSynchronize(P.ev[2 * i + 1]));
+      float ms = 0.f;
+      CB_CUDA(cudaEventElapsedTime(&ms, P.ev[2 * i], P.ev[2 * i + 1]));
+      P.rec[i].ms = ms;
+      P.rec[i].span_ms = -1.f;
+    }
   }
   if (out_host && n > 0) memcpy(out_host, P.rec.data(), sizeof(cb_prof_record) * n);
   *n_out_host = n;

@@ -106,9 +106,11 @@ template <int HD>
 __global__ void __launch_bounds__(THREADS, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const int32_t* __restrict__ q_pos, int M,
-               int64_t n_kv, int H, int Hkv, bf16* __restrict__ out, float scale_log2) {
+               int64_t n_kv, int H, int Hkv, bf16* __restrict__ out, float scale_log2,
+               unsigned long long* span) {
   pdl_wait();
   pdl_trigger();
+  span_begin(span);
   using L = Layout<HD>;
   constexpr int NST = L::KV_STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -425,6 +427,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   tc::tc_fence_before();
   __syncthreads();
+  span_end(span);
   if (warp == 1) {
     __syncwarp();
     tc::tc_fence_after();
@@ -501,7 +504,8 @@ cudaError_t launch_hd(const void* q, const int32_t* q_pos, int M, const void* kc
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
   dim3 grid(H, (M + BM - 1) / BM);
   { const cudaError_t e_ = launch_k(kern, dim3(grid), dim3(THREADS), smem, s, tq, tk, tv, q_pos, M, n_kv, H, Hkv,
-                                    static_cast<bf16*>(out), scale_log2); if (e_ != cudaSuccess) return e_; }
+                                    static_cast<bf16*>(out), scale_log2, prof_span_slot());
+    if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 

@@ -112,6 +112,21 @@ __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z));
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Execution span of a launch, for measurement: a kernel given a slot (two words: earliest
+// start, latest end, in %globaltimer nanoseconds) records the moment its CTA passed
+// pdl_wait() and the moment the CTA finished.  NULL slot: nothing is recorded.
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void span_begin(unsigned long long* slot) {
+  if (slot && threadIdx.x == 0) atomicMin(slot, globaltimer_ns());
+}
+__device__ __forceinline__ void span_end(unsigned long long* slot) {
+  if (slot && threadIdx.x == 0) atomicMax(slot + 1, globaltimer_ns());
+}
+
 // Programmatic dependent launch is on unless CB_PDL=0 (read once; a measurement switch).
 inline bool pdl_enabled() {
   static const bool on = [] {

@@ -325,7 +325,7 @@ template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
               const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
-              const GemmDesc g0, const GemmDesc g1, int n_prob, int swiglu) {
+              const GemmDesc g0, const GemmDesc g1, int n_prob, int swiglu, unsigned long long* span) {
   constexpr int STAGES = TileCfg<BN>::STAGES;
   constexpr int B_BYTES = TileCfg<BN>::B_BYTES;
   extern __shared__ uint8_t smem_raw[];
@@ -387,6 +387,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // the prologue above overlaps the previous kernel's tail; inputs are read only from here
   pdl_wait();
   pdl_trigger();
+  span_begin(span);
 
   // Tiles are visited M-fastest: the CTAs in flight share a few weight tiles and the whole
   // (small) activation matrix, so both stay in L2 and each is read from HBM about once.
@@ -492,6 +493,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   tc::tc_fence_before();
   __syncthreads();
+  span_end(span);
   if (warp == 1) {
     __syncwarp();
     tc::tc_fence_after();
@@ -520,7 +522,7 @@ template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_tc_pair(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
-                   const GemmDesc g0, const GemmDesc g1, int n_prob, int swiglu) {
+                   const GemmDesc g0, const GemmDesc g1, int n_prob, int swiglu, unsigned long long* span) {
   constexpr int STAGES = PairCfg<BN>::STAGES;
   constexpr int B_BYTES = PairCfg<BN>::B_BYTES;
   extern __shared__ uint8_t smem_raw[];
@@ -582,6 +584,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   pdl_wait();
   pdl_trigger();
+  span_begin(span);
 
   bool ok = true;
   if (warp == 0 && lane == 0) {
@@ -685,6 +688,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc::tc_fence_before();
   // neither CTA frees its TMEM (or exits) before the pair's last MMA and epilogue are done
   tc::cluster_sync();
+  span_end(span);
   if (warp == 1) {
     tc::tc_fence_after();
     tc::tmem_dealloc_pair(tmem, TMEM_COLS);
@@ -854,7 +858,7 @@ cudaError_t launch_tiles(const GemmDesc* gs, int n, bool swiglu, int n_sm, cudaS
   const int tiles = tiles_for(gs, n, out_cols);
   const int grid = tiles < n_sm ? tiles : n_sm;
   const cudaError_t e = launch_k(k_gemm_tc<BN>, dim3(grid), dim3(THREADS), SMEM_BYTES, s, tmA[0], tmB[0], tmA[1],
-                                 tmB[1], gs[0], n > 1 ? gs[1] : gs[0], n, swiglu ? 1 : 0);
+                                 tmB[1], gs[0], n > 1 ? gs[1] : gs[0], n, swiglu ? 1 : 0, prof_span_slot());
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -935,7 +939,7 @@ cudaError_t launch_pair(const GemmDesc* gs, int n, bool swiglu, int n_pairs, cud
   const int tiles = pair_tiles_for(gs, n, swiglu ? BN / 2 : BN);
   cfg.gridDim = dim3(2 * (tiles < n_pairs ? tiles : n_pairs));
   const cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc_pair<BN>, tmA[0], tmB[0], tmA[1], tmB[1], gs[0],
-                                           n > 1 ? gs[1] : gs[0], n, swiglu ? 1 : 0);
+                                           n > 1 ? gs[1] : gs[0], n, swiglu ? 1 : 0, prof_span_slot());
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

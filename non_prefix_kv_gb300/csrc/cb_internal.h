@@ -175,6 +175,8 @@ void reset_gemm_tc_caches();
 void reset_attn_tc_caches();
 
 // ---- cb_gemm.cu -----------------------------------------------------------------------
+// The span slot of the launch being made by this thread (span profiling on), else NULL.
+unsigned long long* prof_span_slot();
 cudaError_t launch_gemm(int dt, const GemmDesc& g, cudaStream_t s);
 cudaError_t launch_gemm_pair(int dt, const GemmDesc& a, const GemmDesc& b, cudaStream_t s);
 uint32_t take_error_gemm();

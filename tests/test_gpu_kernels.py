@@ -708,3 +708,47 @@ def test_steady_layer_with_a_row_past_the_cache_writes_nothing_there(B):
     _expect_device_error(B)
     assert torch.count_nonzero(big_k[N:]) == 0 and torch.count_nonzero(big_v[N:]) == 0
     assert torch.count_nonzero(big_k[[10, 50, 100, 255]].float().abs().sum(1)) == 4
+
+
+# ------------------------------------------------------------------------------ span profiling
+def test_span_profiling_records_execution_windows(B):
+    """Span mode: every tensor-core GEMM launch records its execution window from the GPU's
+    global timer; a kernel without span support reports -1 and no launch gets events.  Launches
+    on one stream run one after another (each waits for its predecessor), so their windows add
+    up to no more than the event-timed duration of the whole chain."""
+    torch = torch_mod()
+    M, N, K, d = 832, 4096, 4096, 2048
+    x = dev(synth.test_tensor((M, K), 90, dtype="bf16"), "bf16")
+    w = dev(synth.test_tensor((N, K), 91, std=0.02, dtype="bf16"), "bf16")
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    xn = dev(synth.test_tensor((64, d), 92, dtype="bf16"), "bf16")
+    g = dev(synth.round_bf16(synth.test_tensor((d,), 93, std=0.1, dtype="bf16") + 1.0), "bf16")
+    out = torch.empty((64, d), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+
+    def chain():
+        for _ in range(4):
+            B.cb_linear(x, w, y, M, N, K, B.CB_BF16, s)
+        B.cb_rmsnorm(out, xn, None, 64, d, g, 1e-5, B.CB_BF16, B.CB_BF16, s)
+
+    chain()
+    s.synchronize()
+    B.cb_profile_begin_spans(16)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    chain()
+    e1.record(s)
+    recs = B.cb_profile_end(16)
+    total_ms = e0.elapsed_time(e1)
+    gemm = [r for r in recs if r["kind"] == "gemm"]
+    norm = [r for r in recs if r["kind"] == "rmsnorm"]
+    assert len(gemm) == 4 and len(norm) == 1
+    assert all(r["span_ms"] > 0 for r in gemm), gemm
+    assert norm[0]["span_ms"] == -1
+    assert all(r["ms"] == -1 for r in recs)
+    assert sum(r["span_ms"] for r in gemm) <= total_ms * 1.01 + 0.002, (gemm, total_ms)
+    # event mode again afterwards: events, no spans
+    B.cb_profile_begin(16)
+    chain()
+    ev = B.cb_profile_end(16)
+    assert len(ev) == 5 and all(r["ms"] > 0 and r["span_ms"] == -1 for r in ev)

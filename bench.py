@@ -38,7 +38,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of this shape, from
 # an ncu capture of the CTA-pair tcgen05 GEMM (k_gemm_tc_pair); to be cleared when that
 # kernel changes.
-GEMM_TRAFFIC = {(4096, 11008, 4096, "swiglu"): 248.700160e6 + 79.730432e6}
+GEMM_TRAFFIC = {(4096, 11008, 4096, "swiglu"): 249.959424e6 + 80.663296e6}
 
 
 def parse_args(argv=None):
@@ -843,12 +843,13 @@ def our_arm(args):
     # the same launches without events between them: each tensor-core kernel records its own
     # execution window (global timer, first CTA past its wait on the preceding launch to the
     # last CTA's end), so programmatic dependent launch overlaps the launches as in the step
+    # (the re-positioning again on the layers' stream, as in the event pass)
     n_span = min(8192, 64 * args.profile_steps * len(reqs))
     B.cb_profile_begin_spans(n_span)
     with torch.cuda.stream(stream):
         for _ in range(args.profile_steps):
             for r in reqs:
-                E.run_blend(r, plan)
+                E.run_blend(r, plan, overlap_assembly=False)
     span_recs = B.cb_profile_end(n_span)
     # per-layer time: CUDA events around each layer call (eager, one more pass)
     lev = []
@@ -920,6 +921,22 @@ def our_arm(args):
             ent["span_us"] = 1e3 * sp[1] / sp[0]
             ent["span_tflops"] = sp[2] / (sp[1] / sp[0] / 1e3) / 1e12
         gemm_detail.append(ent)
+    # attention per layer: a step's attention launches come in layer order, one per layer
+    attn_ev = [r["ms"] for r in recs if r["kind"] == "attention"]
+    attn_sp = [r["span_ms"] for r in span_recs if r["kind"] == "attention"]
+    attention_layers = []
+    if len(attn_ev) == len(plan) * len(reqs) * args.profile_steps:
+        nl = len(plan)
+        for l in range(nl):
+            ev_l = attn_ev[l::nl]
+            sp_l = [v for v in attn_sp[l::nl] if v > 0] if len(attn_sp) == len(attn_ev) else []
+            fl = 4.0 * shape.n_heads * shape.head_dim * sel_sums[l][1]
+            ent = {"layer": l, "mode": sel_sums[l][2], "rows": sel_sums[l][0], "keys": wl.n_tokens,
+                   "us": 1e3 * statistics.mean(ev_l), "tflops": fl / (statistics.mean(ev_l) / 1e3) / 1e12}
+            if sp_l:
+                ent["span_us"] = 1e3 * statistics.mean(sp_l)
+                ent["span_tflops"] = fl / (statistics.mean(sp_l) / 1e3) / 1e12
+            attention_layers.append(ent)
     sp = spans.get(("attention",))
     if sp and "attention" in kernels:
         kernels["attention"]["span_ms_per_step"] = sp[1] / args.profile_steps
@@ -1175,7 +1192,7 @@ def our_arm(args):
         "gpu_launches": int(launches_per_step * args.steps),
         "launches_per_step": int(launches_per_step),
         "step_tflops": flops / (ms / 1e3) / 1e12,
-        "roofline": roofline, "step_roofline": step_roofline, "layers": layers_ms, "hbm_kernels": hbm_kernels, "kernels": kernels, "gemm_launches": gemm_detail, "span_note": span_note,
+        "roofline": roofline, "step_roofline": step_roofline, "layers": layers_ms, "hbm_kernels": hbm_kernels, "kernels": kernels, "gemm_launches": gemm_detail, "attention_launches": attention_layers, "span_note": span_note,
         "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "full_prefill": full, "quality_diagnostics": quality,
         "deep_stack": deep,
         "setup_s": setup_s,

@@ -908,9 +908,10 @@ def our_arm(args):
     for r in span_recs:
         if r["span_ms"] > 0:
             key = (r["kind"],) + ((r["m"], r["n"], r["k"], r["aux"]) if r["kind"] == "gemm" else ())
-            e = spans.setdefault(key, [0, 0.0, r["flops"]])
+            e = spans.setdefault(key, [0, 0.0, r["flops"], 0.0])
             e[0] += 1
             e[1] += r["span_ms"]
+            e[3] += r["bytes"]
     epi_names = {0: "store", 1: "resid", 2: "qkv", 3: "swiglu", 102: "qkv+qkv (two problems, one launch)"}
     gemm_detail = []
     for k, v in sorted(gemms.items(), key=lambda kv: -kv[1][1]):
@@ -941,8 +942,9 @@ def our_arm(args):
     if sp and "attention" in kernels:
         kernels["attention"]["span_ms_per_step"] = sp[1] / args.profile_steps
         kernels["attention"]["span_tflops"] = attn_flops_step * args.profile_steps / (sp[1] / 1e3) / 1e12
-    span_note = ("span_us / span_tflops / span_ms_per_step: a second eager pass without events between the "
-                 "launches; each tensor-core GEMM and attention kernel records, from the GPU's global timer, "
+    span_note = ("span_us / span_tflops / span_ms_per_step / span_gbs: a second eager pass without events between "
+                 "the launches; each tensor-core GEMM and attention kernel, and the re-positioning, row-copy and "
+                 "lm_head kernels, record, from the GPU's global timer, "
                  "the moment its first CTA passed the wait on the preceding launch and the moment its last CTA "
                  "ended. us / tflops / ms_per_step: CUDA events around each launch, which stop programmatic "
                  "dependent launch between the bracketed launches")
@@ -992,6 +994,23 @@ def our_arm(args):
         if name in kinds and kinds[name]["bytes"]:
             gbs = kinds[name]["bytes"] / (kinds[name]["ms"] / 1e3) / 1e9
             hbm_kernels[name] = {"gbs": gbs, "frac": gbs / peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])}
+            sp = spans.get((name,))
+            if sp and sp[1] > 0 and sp[3] > 0:
+                sgbs = sp[3] / (sp[1] / 1e3) / 1e9
+                hbm_kernels[name]["span_gbs"] = sgbs
+                hbm_kernels[name]["span_frac"] = sgbs / peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    if "copy_rows" in hbm_kernels:
+        # one step's row copies, launch by launch (both passes launch them in the same order)
+        ev_c = [r for r in recs if r["kind"] == "copy_rows"]
+        sp_c = [r for r in span_recs if r["kind"] == "copy_rows"]
+        per = len(ev_c) // max(1, args.profile_steps)
+        if per and len(sp_c) == len(ev_c):
+            hbm_kernels["copy_rows"]["launches"] = [
+                {"rows": ev_c[i]["m"], "bytes": ev_c[i]["bytes"], "us": 1e3 * ev_c[i]["ms"],
+                 "span_us": 1e3 * sp_c[i]["span_ms"] if sp_c[i]["span_ms"] > 0 else None} for i in range(per)]
+        hbm_kernels["copy_rows"]["note"] = (
+            "the check layer's KV expansion runs on the layer's second stream beside the selected queries' GEMM, "
+            "whose CTAs hold the SMs: its window includes the wait for them, so its span is no per-kernel rate")
 
     # ---------------- the quality reference: full prefill of the same request on the GPU
     # (every token through every layer, then the same lm_head), replayed from a CUDA graph

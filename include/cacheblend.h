@@ -494,7 +494,8 @@ int cb_profile_begin(int32_t max_records);
 
 /* Starts span profiling for the calling thread, up to max_records launches (at most 8192):
  * no events are recorded between launches, so programmatic dependent launch overlaps them as
- * in an unprofiled run.  Instead each tensor-core GEMM and attention kernel records in its
+ * in an unprofiled run.  Instead each tensor-core GEMM and attention kernel, and the
+ * re-positioning (bf16/fp32), multi-row copy and lm_head GEMV kernels, record in their
  * launch's slot of a library-owned device buffer the global-timer time at which its first CTA
  * passed the wait on the preceding launch and the time at which its last CTA finished.  The
  * result is that launch's execution window inside the launch chain.  Synchronises the device.

@@ -133,9 +133,11 @@ __global__ void __launch_bounds__(256) k_rope_shift(T* __restrict__ kd, T* __res
                                                     const int32_t* __restrict__ src_row,
                                                     const int32_t* __restrict__ delta,
                                                     int64_t n_rows, int64_t n_src, int W, int hd,
-                                                    const float2* __restrict__ tab, int max_pos) {
+                                                    const float2* __restrict__ tab, int max_pos,
+                                                    unsigned long long* span) {
   pdl_wait();
   pdl_trigger();
+  span_begin(span);
   const int per_row = W >> 3;
   const int half = hd >> 1;
   const int64_t total = n_rows * per_row;
@@ -168,6 +170,10 @@ __global__ void __launch_bounds__(256) k_rope_shift(T* __restrict__ kd, T* __res
       st8(vd + r * W + c0, v);
     }
   }
+  if (span) {   // uniform; every thread of the block reaches this point
+    __syncthreads();
+    span_end(span);
+  }
 }
 
 cudaError_t launch_rope_shift(int dt, void* kd, void* vd, const void* ks, const void* vs,
@@ -181,11 +187,11 @@ cudaError_t launch_rope_shift(int dt, void* kd, void* vd, const void* ks, const 
   if (dt == DT_BF16)
     { const cudaError_t e_ = launch_k(k_rope_shift<bf16>, dim3(grid), dim3(256), 0, s, (bf16*)kd, (bf16*)vd, (const bf16*)ks,
                                             (const bf16*)vs, src_row, delta, n_rows, n_src, W, hd, t2,
-                                            max_pos); if (e_ != cudaSuccess) return e_; }
+                                            max_pos, prof_span_slot()); if (e_ != cudaSuccess) return e_; }
   else
     { const cudaError_t e_ = launch_k(k_rope_shift<float>, dim3(grid), dim3(256), 0, s, (float*)kd, (float*)vd, (const float*)ks,
                                              (const float*)vs, src_row, delta, n_rows, n_src, W, hd, t2,
-                                             max_pos); if (e_ != cudaSuccess) return e_; }
+                                             max_pos, prof_span_slot()); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
@@ -430,9 +436,10 @@ cudaError_t launch_copy_rows(void* dst, const int32_t* dst_idx, const void* src,
 // all its 16-byte loads of the row (up to kCopyVec per pass) before it stores any.  Row r
 // of all jobs together belongs to job j when row_end[j-1] <= r < row_end[j].
 constexpr int kCopyVec = 16;
-__global__ void __launch_bounds__(256) k_copy_rows_multi(const CopyJobs J) {
+__global__ void __launch_bounds__(256) k_copy_rows_multi(const CopyJobs J, unsigned long long* span) {
   pdl_wait();
   pdl_trigger();
+  span_begin(span);
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int64_t total = J.row_end[J.n - 1];
@@ -463,13 +470,17 @@ __global__ void __launch_bounds__(256) k_copy_rows_multi(const CopyJobs J) {
       }
     }
   }
+  if (span) {   // uniform; every thread of the block reaches this point
+    __syncthreads();
+    span_end(span);
+  }
 }
 
 cudaError_t launch_copy_rows_multi(const CopyJobs& J, cudaStream_t s) {
   if (J.n < 1 || J.n > kMaxCopyJobs) return cudaErrorInvalidValue;
   const int64_t rows = J.row_end[J.n - 1];
   if (rows == 0) return cudaSuccess;
-  { const cudaError_t e_ = launch_k(k_copy_rows_multi, dim3(grid_for(k_copy_rows_multi, rows * 32, 256)), dim3(256), 0, s, J); if (e_ != cudaSuccess) return e_; }
+  { const cudaError_t e_ = launch_k(k_copy_rows_multi, dim3(grid_for(k_copy_rows_multi, rows * 32, 256)), dim3(256), 0, s, J, prof_span_slot()); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
@@ -1284,9 +1295,11 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
 template <typename T>
 __global__ void __launch_bounds__(256) k_lm_gemv(float* __restrict__ logits, const float* __restrict__ hn,
                                                  const T* __restrict__ w, int V, int d, int rows_per_warp,
-                                                 unsigned long long* __restrict__ block_best) {
+                                                 unsigned long long* __restrict__ block_best,
+                                                 unsigned long long* span) {
   pdl_wait();
   pdl_trigger();
+  span_begin(span);
   __shared__ unsigned long long red[8];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   // each warp owns rows_per_warp consecutive rows; the grid is sized so that every warp is
@@ -1367,6 +1380,10 @@ __global__ void __launch_bounds__(256) k_lm_gemv(float* __restrict__ logits, con
     b = warp_max_u64(b);
     if (lane == 0) block_best[blockIdx.x] = b;
   }
+  if (span) {   // uniform; every thread of the block reaches this point
+    __syncthreads();
+    span_end(span);
+  }
 }
 
 // 256-thread blocks of the GEMV resident per SM (register-limited)
@@ -1395,9 +1412,9 @@ cudaError_t launch_lm_gemv(int dt, float* logits, const float* hn, const void* w
   const unsigned grid = lm_grid(V, dt);
   const int rpw = lm_rows_per_warp(V, dt);
   if (dt == DT_BF16)
-    { const cudaError_t e_ = launch_k(k_lm_gemv<bf16>, dim3(grid), dim3(256), 0, s, logits, hn, (const bf16*)w, V, d, rpw, block_best); if (e_ != cudaSuccess) return e_; }
+    { const cudaError_t e_ = launch_k(k_lm_gemv<bf16>, dim3(grid), dim3(256), 0, s, logits, hn, (const bf16*)w, V, d, rpw, block_best, prof_span_slot()); if (e_ != cudaSuccess) return e_; }
   else
-    { const cudaError_t e_ = launch_k(k_lm_gemv<float>, dim3(grid), dim3(256), 0, s, logits, hn, (const float*)w, V, d, rpw, block_best); if (e_ != cudaSuccess) return e_; }
+    { const cudaError_t e_ = launch_k(k_lm_gemv<float>, dim3(grid), dim3(256), 0, s, logits, hn, (const float*)w, V, d, rpw, block_best, prof_span_slot()); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 

@@ -499,7 +499,9 @@ int cb_profile_begin(int32_t max_records);
  * launch's slot of a library-owned device buffer the global-timer time at which its first CTA
  * passed the wait on the preceding launch and the time at which its last CTA finished.  The
  * result is that launch's execution window inside the launch chain.  Synchronises the device.
- * Not for use while a stream is being captured. */
+ * The buffer is the current device's and serves one host thread at a time: while another
+ * thread is in span mode the call fails with CB_ERR_INVALID_ARG.  Not for use while a stream
+ * is being captured. */
 int cb_profile_begin_spans(int32_t max_records);
 
 /* Stops recording (either mode), waits for the recorded events (event mode) or for the

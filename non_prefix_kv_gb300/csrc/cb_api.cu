@@ -68,6 +68,7 @@ thread_local ProfState g_prof;
 constexpr int kSpanMax = 8192;
 __device__ unsigned long long g_span_buf[2 * kSpanMax];
 thread_local unsigned long long* g_cur_span = nullptr;
+std::atomic<bool> g_span_taken{false};   // the slot buffer serves one host thread at a time
 
 struct ProfScope {
   int idx = -1;
@@ -1188,6 +1189,7 @@ void cb_shutdown(void) {
   P.ev.clear();
   P.rec.clear();
   P.on = false;
+  if (P.spans) g_span_taken.store(false);
   P.spans = false;
   P.cap = 0;
   g_cur_span = nullptr;
@@ -1196,6 +1198,11 @@ void cb_shutdown(void) {
 int cb_profile_begin(int32_t max_records) {
   if (max_records < 1) return fail(CB_ERR_INVALID_ARG, "max_records < 1");
   ProfState& P = g_prof;
+  if (P.spans) {   // leaving span mode: the slot buffer is free for other threads
+    P.spans = false;
+    g_cur_span = nullptr;
+    g_span_taken.store(false);
+  }
   while ((int)P.ev.size() < 2 * max_records) {
     cudaEvent_t e;
     CB_CUDA(cudaEventCreate(&e));
@@ -1211,12 +1218,23 @@ int cb_profile_begin(int32_t max_records) {
 int cb_profile_begin_spans(int32_t max_records) {
   if (max_records < 1 || max_records > kSpanMax) return fail(CB_ERR_INVALID_ARG, "max_records outside 1..%d", kSpanMax);
   ProfState& P = g_prof;
+  if (!P.spans) {
+    bool expected = false;
+    if (!g_span_taken.compare_exchange_strong(expected, true))
+      return fail(CB_ERR_INVALID_ARG, "span profiling is active on another thread");
+  }
+  P.spans = false;   // re-armed below once the buffer is reset
   void* addr = nullptr;
-  CB_CUDA(cudaGetSymbolAddress(&addr, g_span_buf));
+  const cudaError_t ea = cudaGetSymbolAddress(&addr, g_span_buf);
+  if (ea != cudaSuccess) g_span_taken.store(false);
+  CB_CUDA(ea);
   std::vector<unsigned long long> init(2 * (size_t)max_records, 0ull);
   for (int i = 0; i < max_records; ++i) init[2 * i] = ~0ull;
-  CB_CUDA(cudaDeviceSynchronize());
-  CB_CUDA(cudaMemcpy(addr, init.data(), init.size() * sizeof(unsigned long long), cudaMemcpyHostToDevice));
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess)
+    e = cudaMemcpy(addr, init.data(), init.size() * sizeof(unsigned long long), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) g_span_taken.store(false);
+  CB_CUDA(e);
   P.span_base = static_cast<unsigned long long*>(addr);
   P.rec.clear();
   P.rec.reserve(max_records);
@@ -1232,6 +1250,7 @@ int cb_profile_end(cb_prof_record* out_host, int32_t max_records, int32_t* n_out
   const bool spans = P.spans;
   P.spans = false;
   g_cur_span = nullptr;
+  if (spans) g_span_taken.store(false);
   if (!n_out_host) return fail(CB_ERR_INVALID_ARG, "n_out_host is NULL");
   const int n = std::min<int>((int)P.rec.size(), std::max(0, max_records));
   if (spans) {

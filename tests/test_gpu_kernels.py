@@ -752,3 +752,29 @@ def test_span_profiling_records_execution_windows(B):
     chain()
     ev = B.cb_profile_end(16)
     assert len(ev) == 5 and all(r["ms"] > 0 and r["span_ms"] == -1 for r in ev)
+
+
+def test_span_profiling_serves_one_thread_at_a_time(B):
+    """The span slot buffer is the device's: while one host thread is in span mode another
+    thread's request is refused, and it succeeds once the first thread has ended."""
+    import threading
+    out = {}
+
+    def other(tag):
+        try:
+            B.cb_profile_begin_spans(4)
+            out[tag] = "ok"
+            B.cb_profile_end(4)
+        except RuntimeError as e:
+            out[tag] = str(e)
+
+    B.cb_profile_begin_spans(4)
+    t = threading.Thread(target=other, args=("while_held",))
+    t.start()
+    t.join()
+    B.cb_profile_end(4)
+    t = threading.Thread(target=other, args=("after_end",))
+    t.start()
+    t.join()
+    assert out["while_held"] != "ok" and "another thread" in out["while_held"], out
+    assert out["after_end"] == "ok", out

@@ -56,6 +56,8 @@ def run(argv=None):
     p.add_argument("--heads", type=int, default=32)
     p.add_argument("--kv-heads", type=int, default=32)
     p.add_argument("--hd", type=int, default=128)
+    p.add_argument("--pos-const", type=int, default=None,
+                   help="attention: every query at this position (each query tile visits the same key tiles)")
     p.add_argument("--rows", type=int, default=3840)
     p.add_argument("--width", type=int, default=4096)
     p.add_argument("--cand", type=int, default=3840)
@@ -135,8 +137,11 @@ def run(argv=None):
         V = torch.randn(n, a.kv_heads * a.hd, device="cuda", generator=g).to(bf)
         q = torch.randn(a.m, a.heads * a.hd, device="cuda", generator=g).to(bf)
         rng = np.random.default_rng(0)
-        pos = np.sort(rng.choice(n, a.m, replace=False)) if a.m < n else np.arange(n)[:a.m]
-        pos[-1] = n - 1
+        if a.pos_const is not None:
+            pos = np.full(a.m, min(max(a.pos_const, 0), n - 1), dtype=np.int64)
+        else:
+            pos = np.sort(rng.choice(n, a.m, replace=False)) if a.m < n else np.arange(n)[:a.m]
+            pos[-1] = n - 1
         q_pos = torch.from_numpy(pos.astype(np.int32)).cuda()
         o = torch.empty_like(q)
         ms = _time(lambda: B.cb_partial_attention(q, q_pos, a.m, K, V, n, dims, o), a.iters, a.warmup)

@@ -844,7 +844,7 @@ def our_arm(args):
     # execution window (global timer, first CTA past its wait on the preceding launch to the
     # last CTA's end), so programmatic dependent launch overlaps the launches as in the step
     # (the re-positioning again on the layers' stream, as in the event pass)
-    n_span = min(8192, 64 * args.profile_steps * len(reqs))
+    n_span = min(8192, len(recs) + 16)   # the event pass made the same launches
     B.cb_profile_begin_spans(n_span)
     with torch.cuda.stream(stream):
         for _ in range(args.profile_steps):

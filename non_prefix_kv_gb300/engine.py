@@ -653,7 +653,7 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
     cur = 0
     ssq_parts = 0                       # statistics of req.x[cur] (none for the first layer)
     if keep_history:
-        req.sel_hist, req.m_hist = [], []
+        req.sel_hist, req.m_hist, req.score_hist = [], [], []
     for l, (mode, k) in enumerate(plan):
         if upto is not None and l >= upto:
             break
@@ -699,6 +699,7 @@ def run_blend(req: Request, plan, dev_mode: int = B.CB_DEV_KV, sel_override=None
         if keep_history:
             req.sel_hist.append(req.s[cur][:m_out].clone())
             req.m_hist.append(m_out)
+            req.score_hist.append(req.scores.clone() if mode in (B.CB_LAYER_CHECK, B.CB_LAYER_GRADUAL) else None)
     if upto is not None and queue_loads is not None:
         queue_loads(s.n_layers)          # the layers run later (by a batch) still need their KV
     if loader is not None:

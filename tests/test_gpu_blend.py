@@ -37,6 +37,35 @@ def _near_tie(ref, l, got_set, tol):
     return all(abs(sc[idx[r]] - kth) <= tol * kth for r in diff if r in idx)
 
 
+def _score_gap(ref, l, got_scores):
+    """Largest |GPU score - oracle score| over layer l's candidates, and the oracle's largest
+    score (the GPU's scores come back in the same candidate order)."""
+    sc = np.asarray(ref["scores"][l], dtype=np.float64)
+    g = got_scores[:len(sc)].astype(np.float64)
+    return float(np.max(np.abs(g - sc))) if len(sc) else 0.0, float(np.max(sc)) if len(sc) else 0.0
+
+
+def _within_score_gap(ref, l, got_set, delta):
+    """True when every row that the GPU set and the oracle's set do not share has an oracle
+    score within 2 delta of the oracle's k-th largest score: with the scores perturbed by at
+    most delta, an exact top-k can swap only such rows."""
+    sc, cand = ref["scores"][l], ref["cand"][l]
+    k = len(ref["S"][l]) - len(ref["forced"])
+    if k == 0 or k == len(cand):
+        return False
+    kth = np.sort(sc)[::-1][k - 1]
+    diff = set(ref["S"][l].tolist()) ^ set(got_set.tolist())
+    idx = {int(c): i for i, c in enumerate(cand)}
+    return all(abs(sc[idx[r]] - kth) <= 2.0 * delta * (1 + 1e-6) for r in diff if r in idx)
+
+
+# bf16 deviation scores against the oracle's, relative to the layer's largest score.  A score
+# is a sum of squared differences K_new - K_cached (and V); the differences carry the bf16
+# rounding of the rows they come from, about 2^-8 relative, so a large score moves by about
+# 2 x 2^-8 of itself.  Measured on GB300: at most 3.2e-3.
+BF16_SCORE_TOL = 1e-2
+
+
 def q8_pool_from_codes(E, pool, chunk_kv, dims):
     """An 8-bit device pool holding the oracle's codes of the oracle's chunk KV, so the GPU
     decodes exactly the values the oracle blends with (the quantizer itself is checked bit
@@ -118,20 +147,25 @@ def run_case(E, wl, r, gradual, tol, check_sets=True, q8=False, segments=False, 
     from non_prefix_kv_gb300 import binding as B
     B.cb_sync(None)
     forced_teacher = False
+    diverged = False   # a set differed at an earlier layer: later layers see other inputs
     for l in range(shape.n_layers):
         got = req.sel_hist[l].cpu().numpy()
         assert len(got) == len(ref["S"][l]), (l, len(got), len(ref["S"][l]))
         assert np.all(np.diff(got) > 0) and set(ref["forced"].tolist()) <= set(got.tolist())
+        if not check_sets and not diverged and ref["scores"][l] is not None:
+            # bf16: the layer's scores against the oracle's, and the set against the scores
+            delta, smax = _score_gap(ref, l, host(req.score_hist[l]))
+            print(f"layer {l}: bf16 deviation scores, max gap {delta / max(smax, 1e-30):.2e} of the largest")
+            assert delta <= BF16_SCORE_TOL * smax, (l, delta, smax)
+            if not np.array_equal(got, ref["S"][l]):
+                assert _within_score_gap(ref, l, got, delta), f"layer {l}: set differs beyond the score gap"
         if not np.array_equal(got, ref["S"][l]):
             a, b = set(got.tolist()), set(ref["S"][l].tolist())
             jacc = len(a & b) / len(a | b)
             print(f"layer {l}: HKVD set Jaccard overlap with the oracle {jacc:.3f}")
             if check_sets:
                 assert _near_tie(ref, l, got, 1e-4), f"layer {l} set differs"
-            else:
-                # bf16: scores of near-zero true deviation are dominated by rounding, so the
-                # GPU set is compared only loosely and the floats are checked teacher-forced
-                assert jacc > 0.3, f"layer {l}: overlap {jacc:.3f}"
+            diverged = True
             forced_teacher = True
     if forced_teacher or not check_sets:
         override = {}
@@ -144,6 +178,12 @@ def run_case(E, wl, r, gradual, tol, check_sets=True, q8=False, segments=False, 
         B.cb_sync(None)
         for l in range(shape.n_layers):
             np.testing.assert_array_equal(req.sel_hist[l].cpu().numpy(), ref["S"][l])
+            if not check_sets and ref["scores"][l] is not None:
+                # teacher-forced: every check and gradual layer sees the oracle's sets
+                delta, smax = _score_gap(ref, l, host(req.score_hist[l]))
+                print(f"layer {l} (teacher-forced): bf16 deviation scores, max gap "
+                      f"{delta / max(smax, 1e-30):.2e} of the largest")
+                assert delta <= BF16_SCORE_TOL * smax, (l, delta, smax)
     assert m == len(ref["S"][-1])
     for l in range(shape.n_layers):
         assert rel(host(req.K[l]), ref["K"][l].reshape(req.N, -1)) < tol, l

@@ -14,7 +14,8 @@
 // grows by more than 2^8.  One CTA per (128-query tile, query head); K and V stream through
 // a TMA ring.  Warp roles: 0 = TMA producer, 1 = TMEM allocator + MMA issuer (the whole warp
 // runs the issue loop, the elected lane issues), 2..9 = softmax groups and epilogue; warp w
-// reads TMEM lanes 32*(w%4)..+31.
+// reads TMEM lanes 32*(w%4)..+31.  A second kernel (k_attn_tc2) takes two query tiles per
+// CTA, one per softmax group, for dense launches with many query tiles.
 #include <cuda.h>
 #include <math.h>
 
@@ -435,6 +436,352 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// ---- two query tiles per CTA --------------------------------------------------------------
+// For launches with many query tiles per head.  Group g owns query tile y_g = 2 p + g of the
+// CTA's pair p (tile 2 p is the later, longer one) and walks every key tile up to its own
+// bound; both groups' S use the same K_j from shared memory and both P.V the same V_j.  Each
+// group's row statistics and O_g then cover its whole key range, so the epilogue needs no
+// merge.  TMEM is laid out as in the kernel above (S_0 | S_1 | O_0 | O_1).  Per key tile and
+// query tile the work is the same as there; the CTAs, and with them the ramp at the start and
+// the drain at the end of every CTA's chain of hand-offs, are half as many, and every K/V
+// tile is loaded once for two query tiles.
+template <int HD>
+struct Layout2 {
+  static constexpr int NSLAB = HD / 64;
+  static constexpr int Q_BYTES = NSLAB * SLAB;                // one query tile
+  static constexpr int KV_BYTES = NSLAB * SLAB;
+  static constexpr int KV_STAGES = HD == 128 ? 5 : 10;
+  static constexpr int OFF_Q = 0;                             // [2 query tiles]
+  static constexpr int OFF_KV = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_BAR = OFF_KV + KV_STAGES * KV_BYTES;
+  static constexpr int BYTES = OFF_BAR + 256;
+  static constexpr int SMEM = BYTES + 1024;
+  static_assert((1 + 6 + 2 * KV_STAGES) * 8 + 16 <= 256, "barriers exceed their region");
+  static_assert(SMEM <= 227 * 1024, "shared memory exceeds the per-block limit");
+};
+
+template <int HD>
+__global__ void __launch_bounds__(THREADS, 1)
+    k_attn_tc2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const int32_t* __restrict__ q_pos, int M,
+               int64_t n_kv, int H, int Hkv, bf16* __restrict__ out, float scale_log2,
+               unsigned long long* span) {
+  pdl_wait();
+  pdl_trigger();
+  span_begin(span);
+  using L = Layout2<HD>;
+  constexpr int NST = L::KV_STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = tc::smem_u32(smem_raw);
+  uint8_t* base = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
+  uint8_t* sQ = base + L::OFF_Q;
+  uint8_t* sKV = base + L::OFF_KV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::OFF_BAR);
+  uint64_t* q_full = bars + 0;
+  uint64_t* s_full = bars + 1;     // [2] per group: S_g holds key tile j's scores
+  uint64_t* p_full = bars + 3;     // [2] the group's four warps wrote P_j
+  uint64_t* pv_done = bars + 5;    // [2] P_j V_j into O_g completed
+  uint64_t* kv_full = bars + 7;    // [NST]
+  uint64_t* kv_empty = kv_full + NST;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(kv_empty + NST);
+  int* s_tmax = reinterpret_cast<int*>(kv_empty + NST) + 1;   // [2] key tiles per group
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x;
+  const int g_kv = h / (H / Hkv);
+  const int n_qt = (M + BM - 1) / BM;
+  // query tile y holds rows [M - 128 (y + 1), M - 128 y): tile 0 is the latest (longest)
+  const int y0 = 2 * (int)blockIdx.y, y1 = y0 + 1;
+  const bool has1 = y1 < n_qt;
+  const int m00 = M - (y0 + 1) * BM, m01 = M - (y1 + 1) * BM;
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&s_full[i], 1);
+      tc::mbar_init(&p_full[i], 4);
+      tc::mbar_init(&pv_done[i], 1);
+    }
+    for (int i = 0; i < NST; ++i) {
+      tc::mbar_init(&kv_full[i], 1);
+      tc::mbar_init(&kv_empty[i], 1);
+    }
+    tc::fence_mbar_init();
+    tc::tma_prefetch_desc(&tmQ);
+    tc::tma_prefetch_desc(&tmK);
+    tc::tma_prefetch_desc(&tmV);
+  }
+  if (warp == 0) {
+    // key tiles each query tile visits: up to its largest position
+    for (int g = 0; g < 2; ++g) {
+      const int m0 = g ? m01 : m00;
+      int mx = -1;
+      if (g == 0 || has1) {
+        for (int i = lane; i < BM; i += 32) {
+          const int m = m0 + i;
+          if (m >= 0 && m < M) {
+            int p = q_pos[m];
+            if (p < 0 || p >= n_kv) {
+              atomicOr(&g_err_attn_tc, ERRBIT_INDEX);
+              p = p < 0 ? 0 : (int)(n_kv - 1);
+            }
+            mx = p > mx ? p : mx;
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const int y = __shfl_xor_sync(0xffffffffu, mx, o);
+        mx = y > mx ? y : mx;
+      }
+      if (lane == 0) s_tmax[g] = mx < 0 ? 0 : mx / BN + 1;
+    }
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int T0 = s_tmax[0], T1 = s_tmax[1];   // T1 = 0: no second query tile
+  const int Tm = T0 > T1 ? T0 : T1;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    tc::mbar_expect_tx(q_full, (T1 > 0 ? 2 : 1) * L::Q_BYTES);
+    for (int s = 0; s < L::NSLAB; ++s) tc::tma_load_2d(sQ + s * SLAB, &tmQ, q_full, h * HD + 64 * s, m00);
+    if (T1 > 0)
+      for (int s = 0; s < L::NSLAB; ++s)
+        tc::tma_load_2d(sQ + L::Q_BYTES + s * SLAB, &tmQ, q_full, h * HD + 64 * s, m01);
+    for (int i = 0; i < 2 * Tm; ++i) {
+      const int st = i % NST;
+      if (!tc::mbar_wait(&kv_empty[st], ((i / NST) & 1) ^ 1)) {
+        atomicOr(&g_err_attn_tc, ERRBIT_TIMEOUT);
+        break;
+      }
+      tc::mbar_expect_tx(&kv_full[st], L::KV_BYTES);
+      const CUtensorMap* map = (i & 1) ? &tmV : &tmK;
+      for (int s = 0; s < L::NSLAB; ++s)
+        tc::tma_load_2d(sKV + st * L::KV_BYTES + s * SLAB, map, &kv_full[st], g_kv * HD + 64 * s, (i >> 1) * BN);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer (warp 1)
+    // S_0(0), S_1(0); then per key tile j: P_0.V(j), S_0(j + 1), P_1.V(j), S_1(j + 1), each
+    // group's S(j + 1) once its P.V(j) has completed.  A K or V stage is released by the last
+    // MMA that reads it (group 1's while group 1 still has key tiles, else group 0's).
+    constexpr uint32_t idesc_s = tc::idesc_bf16_f32(BM, BN);
+    constexpr uint32_t idesc_o = tc::idesc_bf16_f32(BM, HD, true);
+    const uint64_t kv_desc = tc::desc_sw128(tc::smem_u32(sKV));
+    const uint64_t v_desc = tc::desc_sw128_mn(tc::smem_u32(sKV), SLAB);
+    const uint64_t q_desc = tc::desc_sw128(tc::smem_u32(sQ));
+    bool ok = __all_sync(0xffffffffu, tc::mbar_wait(q_full, 0));
+    auto issue_s = [&](int g, int j) {
+      const int i = 2 * j, st = i % NST;
+      ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(&kv_full[st], (i / NST) & 1) &&
+                                             (j == 0 || tc::mbar_wait(&pv_done[g], (j - 1) & 1)));
+      if (!ok) return;
+      tc::tc_fence_after();
+      if (tc::elect_one()) {
+        const uint64_t kd = kv_desc + (uint64_t)((st * L::KV_BYTES) >> 4);
+        const uint64_t qd = q_desc + (uint64_t)((g * L::Q_BYTES) >> 4);
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint32_t off = ((k >> 2) * SLAB + (k & 3) * 32) >> 4;
+          tc::mma_bf16(tmem + g * BN, qd + off, kd + off, idesc_s, k > 0);
+        }
+        tc::mma_commit(&s_full[g]);
+        if (g == 1 || j >= T1) tc::mma_commit(&kv_empty[st]);
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int g, int j) {
+      const int i = 2 * j + 1, st = i % NST;
+      ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(&p_full[g], j & 1) &&
+                                             tc::mbar_wait(&kv_full[st], (i / NST) & 1));
+      if (!ok) return;
+      tc::tc_fence_after();
+      if (tc::elect_one()) {
+        const uint64_t vd = v_desc + (uint64_t)((st * L::KV_BYTES) >> 4);
+        const uint32_t pa = tmem + g * BN;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k)
+          tc::mma_bf16_ts(tmem + TM2_O + g * HD, pa + k * 8, vd + (uint64_t)((k * 16 * 128) >> 4), idesc_o,
+                          (j > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit(&pv_done[g]);
+        if (g == 1 || j >= T1) tc::mma_commit(&kv_empty[st]);
+      }
+      __syncwarp();
+    };
+    issue_s(0, 0);
+    if (T1 > 0) issue_s(1, 0);
+    for (int j = 0; ok && j < Tm; ++j) {
+      if (j < T0) {
+        issue_pv(0, j);
+        if (j + 1 < T0) issue_s(0, j + 1);
+      }
+      if (j < T1) {
+        issue_pv(1, j);
+        if (j + 1 < T1) issue_s(1, j + 1);
+      }
+    }
+    if (!ok && lane == 0) atomicOr(&g_err_attn_tc, ERRBIT_TIMEOUT);
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------------ softmax groups
+    const int grp = (warp - 2) >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int m = (grp ? m01 : m00) + r;
+    const int T = grp ? T1 : T0;
+    const bool row_valid = (grp == 0 || has1) && m >= 0 && m < M;
+    int qp = 0;
+    if (row_valid) {
+      qp = q_pos[m];
+      qp = qp < 0 ? 0 : (qp >= n_kv ? (int)(n_kv - 1) : qp);
+    }
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t tS = trow + grp * BN;
+    const uint32_t tO = trow + TM2_O + grp * HD;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;   // warp-uniform; a failed wait stops the work, never the loop
+    for (int j = 0; j < T; ++j) {
+      ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(&s_full[grp], j & 1));
+      const int key0 = j * BN;
+      const bool none = __all_sync(0xffffffffu, key0 > qp);
+      const bool full_row = key0 + BN - 1 <= qp;
+      float pmx[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) pmx[a] = -INFINITY;
+      if (ok && !none) {
+        tc::tc_fence_after();
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t sr[64];
+          tc::tmem_ld32_nowait(tS + hf * 64, sr);
+          tc::tmem_ld32_nowait(tS + hf * 64 + 32, sr + 32);
+          tc::tmem_wait_ld();
+          if (full_row) {
+#pragma unroll
+            for (int i = 0; i < 64; i += 8) {
+#pragma unroll
+              for (int a = 0; a < 4; ++a)
+                pmx[a] = fmax3(pmx[a], __uint_as_float(sr[i + 2 * a]), __uint_as_float(sr[i + 2 * a + 1]));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+              if (key0 + hf * 64 + i <= qp) pmx[i & 3] = fmaxf(pmx[i & 3], __uint_as_float(sr[i]));
+          }
+        }
+      }
+      if (!ok) continue;
+      const float mt = fmaxf(fmaxf(pmx[0], pmx[1]), fmaxf(pmx[2], pmx[3])) * scale_log2;
+      const float m_new = fmaxf(m_used, mt);
+      if (j == 0) {
+        m_used = m_new;            // O_g is written, not added to, by this tile's P.V
+      } else {
+        const bool need = m_new > m_used + kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          ok = __all_sync(0xffffffffu, tc::mbar_wait(&pv_done[grp], (j - 1) & 1));
+          if (!ok) continue;
+          tc::tc_fence_after();
+          const float alpha = need ? tc::ex2_approx(m_used - m_new) : 1.0f;
+#pragma unroll 1
+          for (int c = 0; c < HD / 16; ++c) {
+            float o[16];
+            tc::tmem_ld16(tO + c * 16, o);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] *= alpha;
+            tc::tmem_st16(tO + c * 16, o);
+          }
+          l *= alpha;
+          if (need) m_used = m_new;
+        }
+      }
+      const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-m_used, -m_used);
+      uint64_t ls2[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) ls2[a] = 0ull;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sr[64];
+        if (!none) {
+          tc::tmem_ld32_nowait(tS + hf * 64, sr);
+          tc::tmem_ld32_nowait(tS + hf * 64 + 32, sr + 32);
+          tc::tmem_wait_ld();
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[16];
+          if (none) {
+#pragma unroll
+            for (int w = 0; w < 16; ++w) pk[w] = 0u;
+          } else {
+#pragma unroll
+            for (int w = 0; w < 16; ++w) {
+              const int k0 = c * 32 + 2 * w;
+              const int key = key0 + hf * 64 + k0;
+              const float2 z =
+                  f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k0]), __uint_as_float(sr[k0 + 1])), sc2, nm2));
+              float p0 = tc::ex2_approx(z.x);
+              float p1 = tc::ex2_approx(z.y);
+              if (!full_row) {
+                p0 = (key <= qp) ? p0 : 0.f;
+                p1 = (key + 1 <= qp) ? p1 : 0.f;
+              }
+              ls2[w & 3] = f2_add(ls2[w & 3], f2_pack(p0, p1));
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+              pk[w] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+          }
+          tc::tmem_st16u_nowait(tS + hf * 32 + c * 16, pk);
+        }
+      }
+      {
+        const float2 a = f2_unpack(f2_add(ls2[0], ls2[1])), c = f2_unpack(f2_add(ls2[2], ls2[3]));
+        l += (a.x + a.y) + (c.x + c.y);
+      }
+      tc::tmem_wait_st();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&p_full[grp]);
+    }
+    // the group's last P.V; then O_g / l is this tile's output (no second half to merge)
+    const bool done = ok && (T == 0 || __all_sync(0xffffffffu, tc::mbar_wait(&pv_done[grp], (T - 1) & 1)));
+    if (done && T > 0) {
+      tc::tc_fence_after();
+      const float inv = l > 0.f ? 1.0f / l : 0.f;
+      bf16* orow = out + (int64_t)(row_valid ? m : 0) * H * HD + (int64_t)h * HD;
+#pragma unroll 1
+      for (int c = 0; c < HD / 16; ++c) {
+        float o[16];
+        tc::tmem_ld16(tO + c * 16, o);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] *= inv;
+        if (row_valid) {
+          if ((reinterpret_cast<uintptr_t>(orow + c * 16) & 31) == 0) {
+            st16_v8(orow + c * 16, o);
+          } else {
+            st8(orow + c * 16, o);
+            st8(orow + c * 16 + 8, o + 8);
+          }
+        }
+      }
+    } else if (!done && lane == 0) {
+      atomicOr(&g_err_attn_tc, ERRBIT_TIMEOUT);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  span_end(span);
+  if (warp == 1) {
+    __syncwarp();
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
 // which kernel variants have their shared-memory limit set, per device (one bit per head
 // size), guarded for calls from several host threads; emptied by reset_attn_tc_caches()
 std::mutex g_attn_mu;
@@ -471,6 +818,22 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// CB_ATTN_PAIR=0 keeps one query tile per CTA, =1 takes two wherever possible (for
+// measurement and tests).  Unset, two are taken when a head has at least kPairMinTiles query
+// tiles and the queries cover at least half the keys: there the two tiles of a CTA visit
+// nearly the same key tiles (dense causal: one apart).  A sparse selection spreads a pair's
+// bounds apart, one group idles while the other finishes, and with fewer, longer CTAs the
+// packing onto the SMs is coarser (measured: 3328 of 16384 rows 662 -> 692 us; dense 4096
+// 149 -> 137 us, 8192 495 -> 467 us).
+constexpr int kPairMinTiles = 8;
+int attn_pair_mode() {
+  static const int mode = [] {
+    const char* v = getenv("CB_ATTN_PAIR");
+    return v && v[0] == '0' ? 0 : (v && v[0] == '1' ? 1 : -1);
+  }();
+  return mode;
+}
+
 template <int HD>
 cudaError_t launch_hd(const void* q, const int32_t* q_pos, int M, const void* kc, const void* vc, int64_t n_kv,
                       int H, int Hkv, void* out, cudaStream_t s) {
@@ -479,14 +842,17 @@ cudaError_t launch_hd(const void* q, const int32_t* q_pos, int M, const void* kc
       !make_map(&tk, kc, n_kv, (int64_t)Hkv * HD, (int64_t)Hkv * HD) ||
       !make_map(&tv, vc, n_kv, (int64_t)Hkv * HD, (int64_t)Hkv * HD))
     return cudaErrorInvalidValue;
-  auto kern = k_attn_tc<HD>;
-  const int smem = Layout<HD>::SMEM;
+  const int n_qt = (M + BM - 1) / BM;
+  const int mode = attn_pair_mode();
+  const bool pair = mode == 1 ? n_qt >= 2 : (mode == 0 ? false : n_qt >= kPairMinTiles && 2 * (int64_t)M >= n_kv);
+  auto kern = pair ? k_attn_tc2<HD> : k_attn_tc<HD>;
+  const int smem = pair ? Layout2<HD>::SMEM : Layout<HD>::SMEM;
   {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const bool cached = dev >= 0 && dev < 64;
-    const uint32_t bit = HD == 128 ? 1u : 2u;
+    const uint32_t bit = (HD == 128 ? 1u : 2u) << (pair ? 2 : 0);
     bool set = false;
     if (cached) {
       std::lock_guard<std::mutex> g(g_attn_mu);
@@ -502,7 +868,7 @@ cudaError_t launch_hd(const void* q, const int32_t* q_pos, int M, const void* kc
     }
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
-  dim3 grid(H, (M + BM - 1) / BM);
+  dim3 grid(H, pair ? (n_qt + 1) / 2 : n_qt);
   { const cudaError_t e_ = launch_k(kern, dim3(grid), dim3(THREADS), smem, s, tq, tk, tv, q_pos, M, n_kv, H, Hkv,
                                     static_cast<bf16*>(out), scale_log2, prof_span_slot());
     if (e_ != cudaSuccess) return e_; }

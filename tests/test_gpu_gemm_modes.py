@@ -29,3 +29,19 @@ def test_gemm_parity_with_each_kernel_forced(mode):
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
     assert " passed" in r.stdout
+
+
+@pytest.mark.parametrize("mode", ["0", "1"], ids=["one_query_tile", "two_query_tiles"])
+def test_attention_parity_with_each_kernel_forced(mode):
+    """The tensor-core attention has two kernels: one query tile per CTA (two softmax groups
+    on alternate key tiles) and two query tiles per CTA (one group per query tile over every
+    key tile), chosen by the query tiles per head.  The attention and blend parity tests run
+    once more with each kernel forced for every launch (CB_ATTN_PAIR)."""
+    torch_mod()
+    ensure_lib()
+    env = dict(os.environ, CB_ATTN_PAIR=mode)
+    r = subprocess.run([sys.executable, "-m", "pytest", "tests/test_gpu_kernels.py", "tests/test_gpu_blend.py", "-m",
+                        "gpu", "-x", "-q", "-p", "no:cacheprovider", "-k", "attention or attn or blend"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+    assert " passed" in r.stdout

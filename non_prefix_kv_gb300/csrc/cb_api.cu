@@ -321,7 +321,7 @@ struct RowCopies {
            int64_t sb) {
     list[n++] = One{d, di, src, si, rows, rb, db, sb};
   }
-  int launch(cudaStream_t s) {
+  int launch(cudaStream_t s, bool beside = false) {
     bool vec = true;
     int64_t acc = 0, bytes = 0, rows = 0;
     int m = 0;
@@ -351,7 +351,7 @@ struct RowCopies {
       }
       return CB_OK;
     }
-    CB_LAUNCH(CB_PROF_COPY_ROWS, m, rows, 0, 0, 0.0, (double)bytes, s, launch_copy_rows_multi(J, s));
+    CB_LAUNCH(CB_PROF_COPY_ROWS, m, rows, 0, 0, 0.0, (double)bytes, s, launch_copy_rows_multi(J, s, beside));
     return CB_OK;
   }
 };
@@ -980,7 +980,7 @@ int cb_blend_layer(const cb_dims* dims, const cb_layer_w* w, int32_t mode, const
           cudaStream_t aux = S(opts->aux_stream);
           CB_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(opts->aux_fork), s));
           CB_CUDA(cudaStreamWaitEvent(aux, static_cast<cudaEvent_t>(opts->aux_fork), 0));
-          if ((st = kv.launch(aux))) return st;
+          if ((st = kv.launch(aux, /*beside=*/true))) return st;   // runs beside the Q GEMM
           CB_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(opts->aux_join), aux));
         }
         if ((st = rc.launch(s))) return st;

@@ -123,7 +123,8 @@ struct CopyJobs {          // row copies of 16-byte words: dst[di[r]] = src[si[r
   int64_t row_end[kMaxCopyJobs];  // inclusive prefix sums of the jobs' row counts
   int n;
 };
-cudaError_t launch_copy_rows_multi(const CopyJobs& J, cudaStream_t s);
+// beside = true: small low-register blocks for a copy that runs beside a GEMM on another stream
+cudaError_t launch_copy_rows_multi(const CopyJobs& J, cudaStream_t s, bool beside = false);
 cudaError_t launch_wait_selftest(uint32_t max_polls, int arrive, cudaStream_t s);
 cudaError_t launch_split_rows(const int32_t* rows_in, int m, const uint8_t* mask, int64_t mask_len,
                               int n_forced, int32_t* cand_pos, int32_t* cand_rows, int32_t* forced_pos,

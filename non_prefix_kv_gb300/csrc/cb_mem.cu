@@ -436,10 +436,8 @@ cudaError_t launch_copy_rows(void* dst, const int32_t* dst_idx, const void* src,
 // all its 16-byte loads of the row (up to kCopyVec per pass) before it stores any.  Row r
 // of all jobs together belongs to job j when row_end[j-1] <= r < row_end[j].
 constexpr int kCopyVec = 16;
-__global__ void __launch_bounds__(256) k_copy_rows_multi(const CopyJobs J, unsigned long long* span) {
-  pdl_wait();
-  pdl_trigger();
-  span_begin(span);
+template <int VEC>
+__device__ __forceinline__ void copy_rows_body(const CopyJobs& J) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int64_t total = J.row_end[J.n - 1];
@@ -456,31 +454,61 @@ __global__ void __launch_bounds__(256) k_copy_rows_multi(const CopyJobs J, unsig
     const int64_t rv = J.rv[j];
     const uint4* src = static_cast<const uint4*>(J.src[j]) + sr * rv;
     uint4* dst = static_cast<uint4*>(J.dst[j]) + d * rv;
-    for (int64_t c0 = 0; c0 < rv; c0 += 32 * kCopyVec) {
-      uint4 v[kCopyVec];
+    for (int64_t c0 = 0; c0 < rv; c0 += 32 * VEC) {
+      uint4 v[VEC];
 #pragma unroll
-      for (int k = 0; k < kCopyVec; ++k) {
+      for (int k = 0; k < VEC; ++k) {
         const int64_t c = c0 + k * 32 + lane;
         if (c < rv) v[k] = src[c];
       }
 #pragma unroll
-      for (int k = 0; k < kCopyVec; ++k) {
+      for (int k = 0; k < VEC; ++k) {
         const int64_t c = c0 + k * 32 + lane;
         if (c < rv) dst[c] = v[k];
       }
     }
   }
+}
+
+__global__ void __launch_bounds__(256) k_copy_rows_multi(const CopyJobs J, unsigned long long* span) {
+  pdl_wait();
+  pdl_trigger();
+  span_begin(span);
+  copy_rows_body<kCopyVec>(J);
   if (span) {   // uniform; every thread of the block reaches this point
     __syncthreads();
     span_end(span);
   }
 }
 
-cudaError_t launch_copy_rows_multi(const CopyJobs& J, cudaStream_t s) {
+// The same copies in small blocks with few registers (four loads in flight per lane), for a
+// launch that runs beside a tensor-core GEMM on another stream: a block fits in the registers
+// and shared memory a GEMM CTA leaves free on its SM, so the copy proceeds on every SM instead
+// of waiting for the GEMM's SMs to empty.
+__global__ void __launch_bounds__(128) k_copy_rows_beside(const CopyJobs J, unsigned long long* span) {
+  pdl_wait();
+  pdl_trigger();
+  span_begin(span);
+  copy_rows_body<4>(J);
+  if (span) {   // uniform; every thread of the block reaches this point
+    __syncthreads();
+    span_end(span);
+  }
+}
+
+cudaError_t launch_copy_rows_multi(const CopyJobs& J, cudaStream_t s, bool beside) {
   if (J.n < 1 || J.n > kMaxCopyJobs) return cudaErrorInvalidValue;
   const int64_t rows = J.row_end[J.n - 1];
   if (rows == 0) return cudaSuccess;
-  { const cudaError_t e_ = launch_k(k_copy_rows_multi, dim3(grid_for(k_copy_rows_multi, rows * 32, 256)), dim3(256), 0, s, J, prof_span_slot()); if (e_ != cudaSuccess) return e_; }
+  if (beside) {
+    const cudaError_t e_ = launch_k(k_copy_rows_beside, dim3(grid_for(k_copy_rows_beside, rows * 32, 128)), dim3(128),
+                                    0, s, J, prof_span_slot());
+    if (e_ != cudaSuccess) return e_;
+  } else {
+    const cudaError_t e_ = launch_k(k_copy_rows_multi, dim3(grid_for(k_copy_rows_multi, rows * 32, 256)), dim3(256),
+                                    0, s, J, prof_span_slot());
+    if (e_ != cudaSuccess) return e_;
+  }
   return cudaGetLastError();
 }
 

@@ -1,7 +1,7 @@
 // Bandwidth- and latency-bound kernels of the blend path: RoPE table and re-rotation (also
 // from 8-bit per-channel codes, and the 8-bit quantization itself), row gathers/scatters and
-// the batched row copies after a selection, RMSNorm, KV deviation, exact top-k, selection
-// bookkeeping, lm_head GEMV + argmax.
+// the batched row copies after a selection (also in small blocks that run beside a GEMM),
+// RMSNorm, KV deviation, exact top-k, selection bookkeeping, lm_head GEMV + argmax.
 //
 // Sources: CacheBlend explainer (0h-n0.github.io/posts/paper-2312-03052) — §KV deviation,
 // §HKVD selection, §Selective recomputation Steps 1 and 3, §RoPE; Prompt Cache explainer

@@ -74,6 +74,124 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// One key tile of a softmax group, shared by both attention kernels; a thread owns one query
+// row of the group's S and O in TMEM.  Pass 1 takes the row's maximum over the tile, the
+// running max is raised lazily (O_g rescaled only when it grows by more than 2^8), pass 2
+// writes P over S and adds it to the row sum, then the group's P_j is signalled.  u is the
+// tile's index among the group's tiles (the barriers' phases; u = 0 starts O_g).  Returns
+// false when a wait gave up.
+template <int HD>
+__device__ __forceinline__ bool softmax_tile(uint64_t* s_full_g, uint64_t* p_full_g, uint64_t* pv_done_g, uint32_t u,
+                                             int key0, int qp, uint32_t tS, uint32_t tO, float scale_log2,
+                                             float& m_used, float& l, int lane) {
+  if (!__all_sync(0xffffffffu, tc::mbar_wait(s_full_g, u & 1))) return false;
+  // every key of this tile lies beyond all 32 rows' positions: no load, P = 0
+  const bool none = __all_sync(0xffffffffu, key0 > qp);
+  const bool full_row = key0 + BN - 1 <= qp;
+  // pass 1: the row's maximum over the tile, 64 columns at a time (a whole 128-column row
+  // does not fit in the registers three warps per sub-partition leave)
+  float pmx[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) pmx[a] = -INFINITY;
+  if (!none) {
+    tc::tc_fence_after();
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t sr[64];
+      tc::tmem_ld32_nowait(tS + hf * 64, sr);
+      tc::tmem_ld32_nowait(tS + hf * 64 + 32, sr + 32);
+      tc::tmem_wait_ld();
+      if (full_row) {
+#pragma unroll
+        for (int i = 0; i < 64; i += 8) {
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+            pmx[a] = fmax3(pmx[a], __uint_as_float(sr[i + 2 * a]), __uint_as_float(sr[i + 2 * a + 1]));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (key0 + hf * 64 + i <= qp) pmx[i & 3] = fmaxf(pmx[i & 3], __uint_as_float(sr[i]));
+      }
+    }
+  }
+  const float mt = fmaxf(fmaxf(pmx[0], pmx[1]), fmaxf(pmx[2], pmx[3])) * scale_log2;
+  const float m_new = fmaxf(m_used, mt);
+  if (u == 0) {
+    m_used = m_new;            // O_g is written, not added to, by this tile's P.V
+  } else {
+    const bool need = m_new > m_used + kRescaleLog2;
+    if (__any_sync(0xffffffffu, need)) {
+      // O_g must be stable: the group's previous P.V has completed
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(pv_done_g, (u - 1) & 1))) return false;
+      tc::tc_fence_after();
+      const float alpha = need ? tc::ex2_approx(m_used - m_new) : 1.0f;
+#pragma unroll 1
+      for (int c = 0; c < HD / 16; ++c) {
+        float o[16];
+        tc::tmem_ld16(tO + c * 16, o);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] *= alpha;
+        tc::tmem_st16(tO + c * 16, o);
+      }
+      l *= alpha;
+      if (need) m_used = m_new;
+    }
+  }
+  // pass 2: P = 2^(s * log2(e)/sqrt(hd) - m), two scores per packed instruction; keys 2w,
+  // 2w+1 go to P column w (bf16 pair).  Keys 0..63 are read again and their P written to
+  // columns 0..31 before keys 64..127 are read; P of those lands in columns 32..63, whose
+  // scores were read in the first half.
+  const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-m_used, -m_used);
+  uint64_t ls2[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) ls2[a] = 0ull;
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    uint32_t sr[64];
+    if (!none) {
+      tc::tmem_ld32_nowait(tS + hf * 64, sr);
+      tc::tmem_ld32_nowait(tS + hf * 64 + 32, sr + 32);
+      tc::tmem_wait_ld();
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      uint32_t pk[16];
+      if (none) {
+#pragma unroll
+        for (int w = 0; w < 16; ++w) pk[w] = 0u;
+      } else {
+#pragma unroll
+        for (int w = 0; w < 16; ++w) {
+          const int k0 = c * 32 + 2 * w;
+          const int key = key0 + hf * 64 + k0;
+          const float2 z =
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k0]), __uint_as_float(sr[k0 + 1])), sc2, nm2));
+          float p0 = tc::ex2_approx(z.x);
+          float p1 = tc::ex2_approx(z.y);
+          if (!full_row) {
+            p0 = (key <= qp) ? p0 : 0.f;
+            p1 = (key + 1 <= qp) ? p1 : 0.f;
+          }
+          ls2[w & 3] = f2_add(ls2[w & 3], f2_pack(p0, p1));
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+          pk[w] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+      }
+      tc::tmem_st16u_nowait(tS + hf * 32 + c * 16, pk);
+    }
+  }
+  {
+    const float2 a = f2_unpack(f2_add(ls2[0], ls2[1])), c = f2_unpack(f2_add(ls2[2], ls2[3]));
+    l += (a.x + a.y) + (c.x + c.y);
+  }
+  tc::tmem_wait_st();
+  tc::tc_fence_before();
+  __syncwarp();
+  if (lane == 0) tc::mbar_arrive(p_full_g);
+  return true;
+}
+
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, %0;" ::"n"(NSOFT * 32) : "memory"); }
 
 // ---- two softmax groups on alternating key tiles ------------------------------------------
@@ -273,116 +391,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;   // warp-uniform; a failed wait stops the work, never the loop
     int u = 0;        // this group's tile count
-    for (int j = grp; j < T; j += 2, ++u) {
-      ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(&s_full[grp], u & 1));
-      const int key0 = j * BN;
-      // every key of this tile lies beyond all 32 rows' positions: no load, P = 0
-      const bool none = __all_sync(0xffffffffu, key0 > qp);
-      const bool full_row = key0 + BN - 1 <= qp;
-      // pass 1: the row's maximum over the tile, 64 columns at a time (a whole 128-column row
-      // does not fit in the registers three warps per sub-partition leave)
-      float pmx[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) pmx[a] = -INFINITY;
-      if (ok && !none) {
-        tc::tc_fence_after();
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t sr[64];
-          tc::tmem_ld32_nowait(tS + hf * 64, sr);
-          tc::tmem_ld32_nowait(tS + hf * 64 + 32, sr + 32);
-          tc::tmem_wait_ld();
-          if (full_row) {
-#pragma unroll
-            for (int i = 0; i < 64; i += 8) {
-#pragma unroll
-              for (int a = 0; a < 4; ++a)
-                pmx[a] = fmax3(pmx[a], __uint_as_float(sr[i + 2 * a]), __uint_as_float(sr[i + 2 * a + 1]));
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 64; ++i)
-              if (key0 + hf * 64 + i <= qp) pmx[i & 3] = fmaxf(pmx[i & 3], __uint_as_float(sr[i]));
-          }
-        }
-      }
-      if (!ok) continue;
-      const float mt = fmaxf(fmaxf(pmx[0], pmx[1]), fmaxf(pmx[2], pmx[3])) * scale_log2;
-      const float m_new = fmaxf(m_used, mt);
-      if (u == 0) {
-        m_used = m_new;            // O_g is written, not added to, by this tile's P.V
-      } else {
-        const bool need = m_new > m_used + kRescaleLog2;
-        if (__any_sync(0xffffffffu, need)) {
-          // O_g must be stable: the group's previous P.V has completed
-          ok = __all_sync(0xffffffffu, tc::mbar_wait(&pv_done[grp], (u - 1) & 1));
-          if (!ok) continue;
-          tc::tc_fence_after();
-          const float alpha = need ? tc::ex2_approx(m_used - m_new) : 1.0f;
-#pragma unroll 1
-          for (int c = 0; c < HD / 16; ++c) {
-            float o[16];
-            tc::tmem_ld16(tO + c * 16, o);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] *= alpha;
-            tc::tmem_st16(tO + c * 16, o);
-          }
-          l *= alpha;
-          if (need) m_used = m_new;
-        }
-      }
-      // pass 2: P = 2^(s * log2(e)/sqrt(hd) - m), two scores per packed instruction; keys 2w,
-      // 2w+1 go to P column w (bf16 pair).  Keys 0..63 are read again and their P written to
-      // columns 0..31 before keys 64..127 are read; P of those lands in columns 32..63, whose
-      // scores were read in the first half.
-      const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-m_used, -m_used);
-      uint64_t ls2[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) ls2[a] = 0ull;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t sr[64];
-        if (!none) {
-          tc::tmem_ld32_nowait(tS + hf * 64, sr);
-          tc::tmem_ld32_nowait(tS + hf * 64 + 32, sr + 32);
-          tc::tmem_wait_ld();
-        }
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t pk[16];
-          if (none) {
-#pragma unroll
-            for (int w = 0; w < 16; ++w) pk[w] = 0u;
-          } else {
-#pragma unroll
-            for (int w = 0; w < 16; ++w) {
-              const int k0 = c * 32 + 2 * w;
-              const int key = key0 + hf * 64 + k0;
-              const float2 z =
-                  f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k0]), __uint_as_float(sr[k0 + 1])), sc2, nm2));
-              float p0 = tc::ex2_approx(z.x);
-              float p1 = tc::ex2_approx(z.y);
-              if (!full_row) {
-                p0 = (key <= qp) ? p0 : 0.f;
-                p1 = (key + 1 <= qp) ? p1 : 0.f;
-              }
-              ls2[w & 3] = f2_add(ls2[w & 3], f2_pack(p0, p1));
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-              pk[w] = *reinterpret_cast<const uint32_t*>(&b2);
-            }
-          }
-          tc::tmem_st16u_nowait(tS + hf * 32 + c * 16, pk);
-        }
-      }
-      {
-        const float2 a = f2_unpack(f2_add(ls2[0], ls2[1])), c = f2_unpack(f2_add(ls2[2], ls2[3]));
-        l += (a.x + a.y) + (c.x + c.y);
-      }
-      tc::tmem_wait_st();
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&p_full[grp]);
-    }
+    for (int j = grp; j < T; j += 2, ++u)
+      if (ok) ok = softmax_tile<HD>(&s_full[grp], &p_full[grp], &pv_done[grp], (uint32_t)u, j * BN, qp, tS, tO,
+                                    scale_log2, m_used, l, lane);
     // the group's last P.V, then both groups' row statistics meet in shared memory
     const bool done = ok && (u == 0 || __all_sync(0xffffffffu, tc::mbar_wait(&pv_done[grp], (u - 1) & 1)));
     xm[grp * BM + r] = m_used;
@@ -645,108 +656,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tO = trow + TM2_O + grp * HD;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;   // warp-uniform; a failed wait stops the work, never the loop
-    for (int j = 0; j < T; ++j) {
-      ok = ok && __all_sync(0xffffffffu, tc::mbar_wait(&s_full[grp], j & 1));
-      const int key0 = j * BN;
-      const bool none = __all_sync(0xffffffffu, key0 > qp);
-      const bool full_row = key0 + BN - 1 <= qp;
-      float pmx[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) pmx[a] = -INFINITY;
-      if (ok && !none) {
-        tc::tc_fence_after();
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t sr[64];
-          tc::tmem_ld32_nowait(tS + hf * 64, sr);
-          tc::tmem_ld32_nowait(tS + hf * 64 + 32, sr + 32);
-          tc::tmem_wait_ld();
-          if (full_row) {
-#pragma unroll
-            for (int i = 0; i < 64; i += 8) {
-#pragma unroll
-              for (int a = 0; a < 4; ++a)
-                pmx[a] = fmax3(pmx[a], __uint_as_float(sr[i + 2 * a]), __uint_as_float(sr[i + 2 * a + 1]));
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 64; ++i)
-              if (key0 + hf * 64 + i <= qp) pmx[i & 3] = fmaxf(pmx[i & 3], __uint_as_float(sr[i]));
-          }
-        }
-      }
-      if (!ok) continue;
-      const float mt = fmaxf(fmaxf(pmx[0], pmx[1]), fmaxf(pmx[2], pmx[3])) * scale_log2;
-      const float m_new = fmaxf(m_used, mt);
-      if (j == 0) {
-        m_used = m_new;            // O_g is written, not added to, by this tile's P.V
-      } else {
-        const bool need = m_new > m_used + kRescaleLog2;
-        if (__any_sync(0xffffffffu, need)) {
-          ok = __all_sync(0xffffffffu, tc::mbar_wait(&pv_done[grp], (j - 1) & 1));
-          if (!ok) continue;
-          tc::tc_fence_after();
-          const float alpha = need ? tc::ex2_approx(m_used - m_new) : 1.0f;
-#pragma unroll 1
-          for (int c = 0; c < HD / 16; ++c) {
-            float o[16];
-            tc::tmem_ld16(tO + c * 16, o);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] *= alpha;
-            tc::tmem_st16(tO + c * 16, o);
-          }
-          l *= alpha;
-          if (need) m_used = m_new;
-        }
-      }
-      const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-m_used, -m_used);
-      uint64_t ls2[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) ls2[a] = 0ull;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t sr[64];
-        if (!none) {
-          tc::tmem_ld32_nowait(tS + hf * 64, sr);
-          tc::tmem_ld32_nowait(tS + hf * 64 + 32, sr + 32);
-          tc::tmem_wait_ld();
-        }
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t pk[16];
-          if (none) {
-#pragma unroll
-            for (int w = 0; w < 16; ++w) pk[w] = 0u;
-          } else {
-#pragma unroll
-            for (int w = 0; w < 16; ++w) {
-              const int k0 = c * 32 + 2 * w;
-              const int key = key0 + hf * 64 + k0;
-              const float2 z =
-                  f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k0]), __uint_as_float(sr[k0 + 1])), sc2, nm2));
-              float p0 = tc::ex2_approx(z.x);
-              float p1 = tc::ex2_approx(z.y);
-              if (!full_row) {
-                p0 = (key <= qp) ? p0 : 0.f;
-                p1 = (key + 1 <= qp) ? p1 : 0.f;
-              }
-              ls2[w & 3] = f2_add(ls2[w & 3], f2_pack(p0, p1));
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-              pk[w] = *reinterpret_cast<const uint32_t*>(&b2);
-            }
-          }
-          tc::tmem_st16u_nowait(tS + hf * 32 + c * 16, pk);
-        }
-      }
-      {
-        const float2 a = f2_unpack(f2_add(ls2[0], ls2[1])), c = f2_unpack(f2_add(ls2[2], ls2[3]));
-        l += (a.x + a.y) + (c.x + c.y);
-      }
-      tc::tmem_wait_st();
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&p_full[grp]);
-    }
+    for (int j = 0; j < T; ++j)
+      if (ok) ok = softmax_tile<HD>(&s_full[grp], &p_full[grp], &pv_done[grp], (uint32_t)j, j * BN, qp, tS, tO,
+                                    scale_log2, m_used, l, lane);
     // the group's last P.V; then O_g / l is this tile's output (no second half to merge)
     const bool done = ok && (T == 0 || __all_sync(0xffffffffu, tc::mbar_wait(&pv_done[grp], (T - 1) & 1)));
     if (done && T > 0) {
